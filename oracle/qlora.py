@@ -1,0 +1,98 @@
+"""Frozen-base QLoRA linear, forward and backward, in float64: plain CPU oracle.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+The pages never typeset the formula; it follows from [ADAPT] section "One model
+contract" (an NF4 base is frozen and needs an adapter), section "Packed NF4 and the
+portable QLoRA profile" ("compute FP32 input gradients through the frozen base; no
+base weight gradients are produced"), section "LoRA FA includes gradient
+preconditioning" (s = alpha / rank) and section "Adapter API" (rank 1..256; rsLoRA
+a separate method, whose primary paper fixes s = alpha / sqrt(rank)):
+
+    T  = x A^T                       [M, r]   (kept for the backward pass)
+    y  = x W^T + s T B^T             [M, N]
+    G  = dY B                        [M, r]
+    dX = dY W + s G A                [M, K]
+    dA = s G^T x                     [r, K]
+    dB = s dY^T T                    [N, r]
+
+with W = deq(W_nf4) [N, K], A [r, K], B [N, r], no bias, no dropout.  [GATE] section
+"The TFLOPS back-check" counts no dL/dW for the frozen base.
+
+Precision: every product and sum here is float64 (numpy matmul is the library
+step).  The operands are the exact values the device path multiplies: for the
+bfloat16 profile x, dY, A, B and the decoded W are first rounded to bfloat16
+(the decoded W as float32 nf4*a' then rounded once); for the float32 profile they
+stay float32.  Results are compared with a relative Frobenius tolerance because
+the accumulation order is not unique.
+"""
+
+import math
+
+import numpy as np
+
+from .nf4 import round_bf16
+
+RANK_MIN, RANK_MAX = 1, 256
+
+
+def lora_scale(alpha: float, rank: int, mode: str = "lora") -> float:
+    """s = alpha / rank (LoRA) or alpha / sqrt(rank) (rsLoRA); rank must be 1..256."""
+    if not (RANK_MIN <= rank <= RANK_MAX):
+        raise ValueError("rank out of range 1..256")
+    if mode == "lora":
+        return float(alpha) / rank
+    if mode == "rslora":
+        return float(alpha) / math.sqrt(rank)
+    raise ValueError("unknown scale mode")
+
+
+def _operands(compute: str, *arrays):
+    """Operands as float64 after the rounding the device applies ('f64' keeps them unrounded)."""
+    out = []
+    for a in arrays:
+        if compute == "f64":
+            out.append(np.asarray(a, dtype=np.float64))
+            continue
+        a32 = np.asarray(a, dtype=np.float32)
+        if compute == "bf16":
+            a32 = round_bf16(a32)
+        elif compute != "f32":
+            raise ValueError("compute must be 'bf16', 'f32' or 'f64'")
+        out.append(a32.astype(np.float64))
+    return out
+
+
+def forward(x, W, A, B, s: float, compute: str = "bf16"):
+    """Return (y, T) in float64.  W is the decoded weight [N, K] (float32 values)."""
+    x64, W64, A64, B64 = _operands(compute, x, W, A, B)
+    T = x64 @ A64.T
+    y = x64 @ W64.T + s * (T @ B64.T)
+    return y, T
+
+
+def backward(dy, x, W, A, B, s: float, compute: str = "bf16"):
+    """Return (dX, dA, dB, G) in float64 for the loss gradient dy = dL/dy."""
+    dy64, x64, W64, A64, B64 = _operands(compute, dy, x, W, A, B)
+    T = x64 @ A64.T
+    G = dy64 @ B64
+    dX = dy64 @ W64 + s * (G @ A64)
+    dA = s * (G.T @ x64)
+    dB = s * (dy64.T @ T)
+    return dX, dA, dB, G
+
+
+def rel_frobenius(got, want) -> float:
+    """||got - want||_F / ||want||_F (0 when both are zero)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    den = np.linalg.norm(want)
+    num = np.linalg.norm(got - want)
+    if den == 0.0:
+        return 0.0 if num == 0.0 else math.inf
+    return float(num / den)
+
+
+def linear_flops(M: int, N: int, K: int, r: int) -> int:
+    """Algorithmic flops of one forward + backward: 4MNK base (y and dX) + 6Mr(N+K) adapter."""
+    return 4 * M * N * K + 6 * M * r * (N + K)
