@@ -1,0 +1,250 @@
+"""Thin Python binding of libqlora_nf4.so (ctypes): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module only
+allocates outputs and workspaces with PyTorch, passes device pointers and the
+current CUDA stream through the C ABI declared in ``include/qlora_nf4.h``, and turns
+a non-OK status into :class:`Nf4Error`.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+NF4_OK, NF4_ERR_ARG, NF4_ERR_SHAPE, NF4_ERR_ALIGN, NF4_ERR_DTYPE = 0, 1, 2, 3, 4
+NF4_ERR_NONFINITE, NF4_ERR_CORRUPT, NF4_ERR_CUDA, NF4_ERR_TIMEOUT, NF4_ERR_WORKSPACE = 5, 6, 7, 8, 9
+NF4_F32, NF4_BF16 = 0, 1
+SCALE_LORA, SCALE_RSLORA = 0, 1
+
+ENTRY_POINTS = (
+    "nf4_abi_version", "nf4_status_str", "nf4_num_blocks", "nf4_num_nested", "nf4_packed_bytes",
+    "nf4_code_tables", "nf4_quantize_workspace_bytes", "nf4_quantize", "nf4_dequantize",
+    "qlora_fwd_workspace_bytes", "qlora_bwd_workspace_bytes", "qlora_linear_fwd",
+    "qlora_linear_bwd", "qlora_last_device_status", "nf4_kernel_launch_count",
+)
+
+
+class Nf4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_status_str(status)} (status {status})")
+
+
+class _Nf4Tensor(ctypes.Structure):
+    _fields_ = [("numel", ctypes.c_int64), ("double_quant", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("packed", ctypes.c_void_p),
+                ("absmax", ctypes.c_void_p), ("nested_absmax", ctypes.c_void_p),
+                ("offset", ctypes.c_void_p)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library (build it first with ``bit_nf4_quantized_gb300.build``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libqlora_nf4.so is not built ({path}); run bit_nf4_quantized_gb300.build")
+    lib = ctypes.CDLL(path)
+    i64, i32, sz, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+    tp = ctypes.POINTER(_Nf4Tensor)
+    sig = {
+        "nf4_abi_version": (i32, []),
+        "nf4_status_str": (ctypes.c_char_p, [i32]),
+        "nf4_num_blocks": (i64, [i64]),
+        "nf4_num_nested": (i64, [i64]),
+        "nf4_packed_bytes": (sz, [i64, i32]),
+        "nf4_code_tables": (None, [vp, vp]),
+        "nf4_quantize_workspace_bytes": (sz, [i64, i32]),
+        "nf4_quantize": (i32, [vp, i32, i64, tp, vp, sz, vp]),
+        "nf4_dequantize": (i32, [tp, vp, i32, vp]),
+        "qlora_fwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
+        "qlora_bwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
+        "qlora_linear_fwd": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, tp, vp, vp, vp, vp, vp, sz, vp]),
+        "qlora_linear_bwd": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, vp, vp, tp, vp, vp,
+                                   vp, vp, vp, vp, sz, vp]),
+        "qlora_last_device_status": (i32, [vp, i32]),
+        "nf4_kernel_launch_count": (i64, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _status_str(s: int) -> str:
+    try:
+        return load().nf4_status_str(s).decode()
+    except Exception:  # the library itself may be what failed to load
+        return "unknown"
+
+
+def _check(status: int, where: str):
+    if status != NF4_OK:
+        raise Nf4Error(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return NF4_F32
+    if dt == torch.bfloat16:
+        return NF4_BF16
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class Nf4Tensor:
+    """A quantized tensor held in device memory (torch buffers) plus its logical shape."""
+    shape: tuple
+    double_quant: bool
+    packed: torch.Tensor
+    absmax: torch.Tensor
+    nested_absmax: torch.Tensor = None
+    offset: torch.Tensor = None
+
+    @property
+    def numel(self) -> int:
+        n = 1
+        for d in self.shape:
+            n *= d
+        return n
+
+    def c_struct(self) -> _Nf4Tensor:
+        return _Nf4Tensor(self.numel, int(self.double_quant), 0, self.packed.data_ptr(),
+                          self.absmax.data_ptr(),
+                          None if self.nested_absmax is None else self.nested_absmax.data_ptr(),
+                          None if self.offset is None else self.offset.data_ptr())
+
+    def nbytes(self) -> int:
+        n = self.packed.numel() + self.absmax.numel() * self.absmax.element_size()
+        if self.nested_absmax is not None:
+            n += 4 * self.nested_absmax.numel()
+        return n
+
+    @staticmethod
+    def empty(shape, double_quant=True, device="cuda"):
+        lib = load()
+        n = 1
+        for d in shape:
+            n *= d
+        nb, nnb = lib.nf4_num_blocks(n), lib.nf4_num_nested(n)
+        packed = torch.empty((n + 1) // 2, dtype=torch.uint8, device=device)
+        if double_quant:
+            return Nf4Tensor(tuple(shape), True, packed,
+                             torch.empty(nb, dtype=torch.uint8, device=device),
+                             torch.empty(nnb, dtype=torch.float32, device=device),
+                             torch.zeros(4, dtype=torch.float32, device=device))  # 16-byte slot, [0] used
+        return Nf4Tensor(tuple(shape), False, packed, torch.empty(nb, dtype=torch.float32, device=device))
+
+
+def code_tables():
+    """(nf4[16], dyn8[256]) float32 tables exported by the library."""
+    lib = load()
+    nf4 = (ctypes.c_float * 16)()
+    dyn8 = (ctypes.c_float * 256)()
+    lib.nf4_code_tables(nf4, dyn8)
+    return list(nf4), list(dyn8)
+
+
+def nf4_quantize(x: torch.Tensor, double_quant: bool = True, out: Nf4Tensor = None,
+                 workspace: torch.Tensor = None, stream=None) -> Nf4Tensor:
+    lib = load()
+    x = x.contiguous()
+    if out is None:
+        out = Nf4Tensor.empty(tuple(x.shape), double_quant, x.device)
+    need = lib.nf4_quantize_workspace_bytes(x.numel(), int(double_quant))
+    ws = workspace if workspace is not None else _workspace(need, x.device)
+    cs = out.c_struct()
+    _check(lib.nf4_quantize(_ptr(x), _dtype_code(x.dtype), x.numel(), ctypes.byref(cs), _ptr(ws),
+                            ws.numel(), _stream(stream)), "nf4_quantize")
+    return out
+
+
+def nf4_dequantize(q: Nf4Tensor, dtype=torch.float32, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    lib = load()
+    y = out if out is not None else torch.empty(q.shape, dtype=dtype, device=q.packed.device)
+    cs = q.c_struct()
+    _check(lib.nf4_dequantize(ctypes.byref(cs), _ptr(y), _dtype_code(y.dtype), _stream(stream)),
+           "nf4_dequantize")
+    return y
+
+
+def qlora_linear_fwd(x: torch.Tensor, W: Nf4Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                     mode: int = SCALE_LORA, y: torch.Tensor = None, T: torch.Tensor = None,
+                     workspace: torch.Tensor = None, stream=None):
+    """y = x W^T + s (x A^T) B^T; returns (y, T).  x is [M, K] in the compute dtype."""
+    lib = load()
+    M, K = x.shape
+    N = W.shape[0]
+    r = A.shape[0]
+    cd = _dtype_code(x.dtype)
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else _workspace(
+        lib.qlora_fwd_workspace_bytes(M, N, K, r, cd), x.device)
+    cs = W.c_struct()
+    _check(lib.qlora_linear_fwd(M, N, K, r, ctypes.c_float(alpha), mode, cd, _ptr(x), ctypes.byref(cs),
+                                _ptr(A), _ptr(B), _ptr(y), _ptr(T), _ptr(ws), ws.numel(), _stream(stream)),
+           "qlora_linear_fwd")
+    return y, T
+
+
+def qlora_linear_bwd(dy: torch.Tensor, x: torch.Tensor, T: torch.Tensor, W: Nf4Tensor, A: torch.Tensor,
+                     B: torch.Tensor, alpha: float, mode: int = SCALE_LORA, dx: torch.Tensor = None,
+                     dA: torch.Tensor = None, dB: torch.Tensor = None, workspace: torch.Tensor = None,
+                     stream=None):
+    """Returns (dX, dA, dB) for the frozen-base QLoRA linear."""
+    lib = load()
+    M, K = x.shape
+    N = W.shape[0]
+    r = A.shape[0]
+    cd = _dtype_code(x.dtype)
+    if dx is None:
+        dx = torch.empty((M, K), dtype=x.dtype, device=x.device)
+    if dA is None:
+        dA = torch.empty((r, K), dtype=torch.float32, device=x.device)
+    if dB is None:
+        dB = torch.empty((N, r), dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else _workspace(
+        lib.qlora_bwd_workspace_bytes(M, N, K, r, cd), x.device)
+    cs = W.c_struct()
+    _check(lib.qlora_linear_bwd(M, N, K, r, ctypes.c_float(alpha), mode, cd, _ptr(dy), _ptr(x), _ptr(T),
+                                ctypes.byref(cs), _ptr(A), _ptr(B), _ptr(dx), _ptr(dA), _ptr(dB),
+                                _ptr(ws), ws.numel(), _stream(stream)), "qlora_linear_bwd")
+    return dx, dA, dB
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    return int(load().qlora_last_device_status(_stream(stream), int(clear)))
+
+
+def launch_count() -> int:
+    return int(load().nf4_kernel_launch_count())

@@ -1,0 +1,341 @@
+// The C ABI of libqlora_nf4.so: argument validation, constant tables, the
+// per-device status word, workspace layout and dispatch to the kernels.
+//
+// Contract ("Native model adaptation and NF4"): the NF4 base is frozen and needs an
+// adapter ("One model contract"); storage is NF4 with or without double
+// quantization ("Packed NF4 and the portable QLoRA profile"); rank is 1..256 and
+// s = alpha / rank, rsLoRA a separate scale ("Adapter API", "LoRA FA includes
+// gradient preconditioning"); no CPU fallback and no automatic precision change,
+// unsupported values fail explicitly ("Explicit accelerated training profiles").
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "linear_tc.cuh"
+
+namespace qnf4 {
+
+// ---- constant tables ---------------------------------------------------------------
+namespace {
+
+// The 16 NF4 values as published with QLoRA (Dettmers et al. 2023, appendix
+// "NormalFloat 4-bit data type"), ascending.
+constexpr float kNf4Values[16] = {
+    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
+    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
+    0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
+    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
+
+// Signed dynamic tree quantization (Dettmers et al. 2022, "8-bit Optimizers via
+// Block-wise Quantization"): after the sign, E zero bits give the decade 10^-E, a
+// 1 bit ends them and F = 6 - E bits pick one of 2^F equal bins of [0.1, 1]; the
+// value is the bin midpoint.  The two all-zero patterns stand for 0 and +1.
+// Magnitude of bin f in decade E: (2^(F+1) + 9(2f+1)) / (20 * 2^F * 10^E), an exact
+// quotient of small integers, divided once in double and rounded once to float.
+void build_dyn8(float out[256]) {
+  float pos[127];
+  int n = 0;
+  for (int e = 6; e >= 0; --e) {           // ascending magnitude: smallest decade first
+    const int f_bits = 6 - e;
+    const int bins = 1 << f_bits;
+    double pow10 = 1.0;
+    for (int i = 0; i < e; ++i) pow10 *= 10.0;
+    for (int f = 0; f < bins; ++f) {
+      const double num = static_cast<double>((2 << f_bits) + 9 * (2 * f + 1));
+      const double den = 20.0 * static_cast<double>(bins) * pow10;
+      pos[n++] = static_cast<float>(num / den);
+    }
+  }
+  for (int i = 0; i < 127; ++i) out[i] = -pos[126 - i];
+  out[127] = 0.0f;
+  for (int i = 0; i < 127; ++i) out[128 + i] = pos[i];
+  out[255] = 1.0f;
+}
+
+// thr[j] = smallest float strictly above the exact midpoint of codes j and j+1, so
+// that #{j : v >= thr[j]} is the nearest code with ties going to the lower index.
+void build_thresholds(const float* codes, int n, float* thr) {
+  for (int j = 0; j + 1 < n; ++j) {
+    const double mid = (static_cast<double>(codes[j]) + static_cast<double>(codes[j + 1])) * 0.5;
+    const float f = static_cast<float>(mid);
+    thr[j] = (static_cast<double>(f) > mid) ? f : std::nextafter(f, INFINITY);
+  }
+  for (int j = n - 1; j < 16 && n == 16; ++j) thr[j] = INFINITY;
+  if (n == 256) thr[255] = INFINITY;
+}
+
+struct Tables {
+  DecodeTables dec;
+  EncodeTables enc;
+  Tables() {
+    std::memcpy(dec.nf4, kNf4Values, sizeof(kNf4Values));
+    build_dyn8(dec.dyn8);
+    build_thresholds(dec.nf4, 16, enc.nf4_thr);
+    build_thresholds(dec.dyn8, 256, enc.dyn8_thr);
+  }
+};
+
+const Tables& tables() {
+  static const Tables t;
+  return t;
+}
+
+std::atomic<int64_t> g_launches{0};
+
+// One status word per device (the module's copy on each device).
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_addr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+nf4_status device_status_ptr(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NF4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (g_status_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return NF4_ERR_CUDA;
+    g_status_addr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_addr[dev];
+  return NF4_OK;
+}
+
+}  // namespace
+
+const DecodeTables& decode_tables() { return tables().dec; }
+const EncodeTables& encode_tables() { return tables().enc; }
+void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace qnf4
+
+using namespace qnf4;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t a256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+nf4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NF4_OK : NF4_ERR_CUDA; }
+
+// Checks an nf4_tensor descriptor against an expected element count.
+nf4_status check_tensor(const nf4_tensor* t, int64_t numel) {
+  if (t == nullptr) return NF4_ERR_ARG;
+  if (t->numel != numel || t->numel <= 0) return NF4_ERR_CORRUPT;
+  if ((t->double_quant != 0 && t->double_quant != 1) || t->reserved != 0) return NF4_ERR_CORRUPT;
+  if (t->packed == nullptr || t->absmax == nullptr) return NF4_ERR_ARG;
+  if (t->double_quant) {
+    if (t->nested_absmax == nullptr || t->offset == nullptr) return NF4_ERR_CORRUPT;
+  } else if (t->nested_absmax != nullptr || t->offset != nullptr) {
+    return NF4_ERR_CORRUPT;
+  }
+  if (!aligned16(t->packed) || !aligned16(t->absmax)) return NF4_ERR_ALIGN;
+  if (t->double_quant && (!aligned16(t->nested_absmax) || !aligned16(t->offset))) return NF4_ERR_ALIGN;
+  return NF4_OK;
+}
+
+Nf4View view_of(const nf4_tensor* t) {
+  Nf4View v;
+  v.packed = t->packed;
+  v.absmax = t->absmax;
+  v.nested = t->nested_absmax;
+  v.offset = t->offset;
+  v.numel = t->numel;
+  v.dq = t->double_quant;
+  return v;
+}
+
+nf4_status check_linear(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                        qlora_scale_mode mode, nf4_dtype compute, float* s_out) {
+  if (M < 0 || N <= 0 || K <= 0) return NF4_ERR_ARG;
+  if (N > (int64_t(1) << 40) / K) return NF4_ERR_SHAPE;
+  if (rank < 1 || rank > 256 || rank > N || rank > K) return NF4_ERR_ARG;
+  if (!std::isfinite(alpha)) return NF4_ERR_ARG;
+  if (mode != QLORA_SCALE_LORA && mode != QLORA_SCALE_RSLORA) return NF4_ERR_ARG;
+  if (compute != NF4_F32 && compute != NF4_BF16) return NF4_ERR_DTYPE;
+  if (compute == NF4_BF16 && (K % 64 != 0 || N % 8 != 0)) return NF4_ERR_SHAPE;
+  *s_out = (mode == QLORA_SCALE_LORA)
+               ? alpha / static_cast<float>(rank)
+               : static_cast<float>(static_cast<double>(alpha) / std::sqrt(static_cast<double>(rank)));
+  return NF4_OK;
+}
+
+// Workspace layouts.  bwd: G fp32 [M, r], then whatever the selected path needs.
+size_t fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
+  if (cd == NF4_BF16) return tc_fwd_ws_bytes(M, N, K, r);
+  return 0;
+}
+size_t bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
+  size_t b = a256(sizeof(float) * static_cast<size_t>(M) * r);
+  if (cd == NF4_BF16) b += tc_bwd_ws_bytes(M, N, K, r);
+  return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t nf4_abi_version(void) { return QLORA_NF4_ABI_VERSION; }
+
+const char* nf4_status_str(nf4_status s) {
+  switch (s) {
+    case NF4_OK: return "ok";
+    case NF4_ERR_ARG: return "invalid argument";
+    case NF4_ERR_SHAPE: return "unsupported shape";
+    case NF4_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case NF4_ERR_DTYPE: return "unsupported dtype";
+    case NF4_ERR_NONFINITE: return "non-finite input";
+    case NF4_ERR_CORRUPT: return "inconsistent NF4 descriptor";
+    case NF4_ERR_CUDA: return "CUDA runtime error";
+    case NF4_ERR_TIMEOUT: return "device-side wait timed out";
+    case NF4_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+int64_t nf4_num_blocks(int64_t numel) { return numel <= 0 ? 0 : (numel + kBlock - 1) / kBlock; }
+int64_t nf4_num_nested(int64_t numel) {
+  return numel <= 0 ? 0 : (nf4_num_blocks(numel) + kNested - 1) / kNested;
+}
+
+size_t nf4_packed_bytes(int64_t numel, int32_t double_quant) {
+  if (numel <= 0) return 0;
+  const size_t packed = static_cast<size_t>((numel + 1) / 2);
+  const size_t nb = static_cast<size_t>(nf4_num_blocks(numel));
+  if (!double_quant) return packed + 4 * nb;
+  return packed + nb + 4 * static_cast<size_t>(nf4_num_nested(numel));
+}
+
+void nf4_code_tables(float* nf4_out16, float* dyn8_out256) {
+  const DecodeTables& t = decode_tables();
+  if (nf4_out16) std::memcpy(nf4_out16, t.nf4, sizeof(t.nf4));
+  if (dyn8_out256) std::memcpy(dyn8_out256, t.dyn8, sizeof(t.dyn8));
+}
+
+size_t nf4_quantize_workspace_bytes(int64_t numel, int32_t double_quant) {
+  return numel <= 0 ? 0 : quantize_ws_bytes(numel, double_quant ? 1 : 0);
+}
+
+nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel, const nf4_tensor* out,
+                        void* ws, size_t ws_bytes, void* stream) {
+  if (x == nullptr || numel <= 0) return NF4_ERR_ARG;
+  if (x_dtype != NF4_F32 && x_dtype != NF4_BF16) return NF4_ERR_DTYPE;
+  nf4_status st = check_tensor(out, numel);
+  if (st != NF4_OK) return st;
+  if (!aligned16(x)) return NF4_ERR_ALIGN;
+  const size_t need = quantize_ws_bytes(numel, out->double_quant);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
+  int* status = nullptr;
+  if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+  return from_cuda(launch_quantize(x, x_dtype, numel, *out, ws, status,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream) {
+  if (w == nullptr || y == nullptr) return NF4_ERR_ARG;
+  if (out_dtype != NF4_F32 && out_dtype != NF4_BF16) return NF4_ERR_DTYPE;
+  nf4_status st = check_tensor(w, w->numel);
+  if (st != NF4_OK) return st;
+  if (!aligned16(y)) return NF4_ERR_ALIGN;
+  return from_cuda(launch_dequantize(view_of(w), y, out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
+  if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256) return 0;
+  return fwd_ws(M, N, K, rank, compute);
+}
+
+size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
+  if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256) return 0;
+  return bwd_ws(M, N, K, rank, compute);
+}
+
+nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                            qlora_scale_mode mode, nf4_dtype compute,
+                            const void* x, const nf4_tensor* W, const float* A, const float* B,
+                            void* y, float* T_out, void* ws, size_t ws_bytes, void* stream) {
+  float s = 0.0f;
+  nf4_status st = check_linear(M, N, K, rank, alpha, mode, compute, &s);
+  if (st != NF4_OK) return st;
+  if ((st = check_tensor(W, N * K)) != NF4_OK) return st;
+  if (A == nullptr || B == nullptr) return NF4_ERR_ARG;
+  if (M > 0 && (x == nullptr || y == nullptr || T_out == nullptr)) return NF4_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || (M > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(T_out))))
+    return NF4_ERR_ALIGN;
+  const size_t need = fwd_ws(M, N, K, rank, compute);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
+  if (M == 0) return NF4_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  LinearArgs a{M, N, K, rank, s, view_of(W)};
+  if (compute == NF4_BF16) {
+    int* status = nullptr;
+    if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+    return from_cuda(tc_forward(a, x, A, B, y, T_out, ws, status, cs));
+  }
+  cudaError_t e = launch_lora_down(a, compute, x, A, T_out, cs);
+  if (e == cudaSuccess) e = launch_fwd_simt(a, compute, x, T_out, B, y, cs);
+  return from_cuda(e);
+}
+
+nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                            qlora_scale_mode mode, nf4_dtype compute,
+                            const void* dy, const void* x, const float* T,
+                            const nf4_tensor* W, const float* A, const float* B,
+                            void* dx, float* dA, float* dB,
+                            void* ws, size_t ws_bytes, void* stream) {
+  float s = 0.0f;
+  nf4_status st = check_linear(M, N, K, rank, alpha, mode, compute, &s);
+  if (st != NF4_OK) return st;
+  if ((st = check_tensor(W, N * K)) != NF4_OK) return st;
+  if (A == nullptr || B == nullptr || dA == nullptr || dB == nullptr) return NF4_ERR_ARG;
+  if (M > 0 && (dy == nullptr || x == nullptr || T == nullptr || dx == nullptr)) return NF4_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(dA) || !aligned16(dB)) return NF4_ERR_ALIGN;
+  if (M > 0 && (!aligned16(dy) || !aligned16(x) || !aligned16(T) || !aligned16(dx))) return NF4_ERR_ALIGN;
+  const size_t need = bwd_ws(M, N, K, rank, compute);
+  if (ws == nullptr || ws_bytes < need) return NF4_ERR_WORKSPACE;
+  if (!aligned16(ws)) return NF4_ERR_ALIGN;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (M == 0) {   // no tokens: the adapter gradients are zero
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * static_cast<size_t>(rank) * K, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, sizeof(float) * static_cast<size_t>(N) * rank, cs);
+    return from_cuda(e);
+  }
+  LinearArgs a{M, N, K, rank, s, view_of(W)};
+  float* G = static_cast<float*>(ws);
+  if (compute == NF4_BF16) {
+    int* status = nullptr;
+    if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+    void* tc_ws = static_cast<char*>(ws) + a256(sizeof(float) * static_cast<size_t>(M) * rank);
+    return from_cuda(tc_backward(a, dy, x, T, A, B, dx, dA, dB, G, tc_ws, status, cs));
+  }
+  cudaError_t e = launch_lora_g(a, compute, dy, B, G, cs);
+  if (e == cudaSuccess) e = launch_dx_simt(a, compute, dy, G, A, dx, cs);
+  if (e == cudaSuccess) e = launch_lora_dA(a, compute, G, x, dA, cs);
+  if (e == cudaSuccess) e = launch_lora_dB(a, compute, dy, T, dB, cs);
+  return from_cuda(e);
+}
+
+nf4_status qlora_last_device_status(void* stream, int32_t clear) {
+  int* p = nullptr;
+  nf4_status st = device_status_ptr(&p);
+  if (st != NF4_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return NF4_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NF4_ERR_CUDA;
+  if (clear && v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return NF4_ERR_CUDA;
+  }
+  return static_cast<nf4_status>(v);
+}
+
+int64_t nf4_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

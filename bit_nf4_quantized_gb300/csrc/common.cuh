@@ -1,0 +1,109 @@
+// Internal declarations shared by the translation units of libqlora_nf4.so.
+//
+// The code tables reach the kernels as by-value kernel parameters (copied to
+// shared memory at kernel start), so no __constant__ or __device__ state has to
+// be shared between translation units.  The one piece of device state, the
+// per-device status word, lives in abi.cu; kernels get its address as `status`.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "qlora_nf4.h"
+
+namespace qnf4 {
+
+constexpr int kBlock = 64;            // NF4 absmax block
+constexpr int kNested = 256;          // absmax values per nested block
+constexpr int kGroupElems = kBlock * kNested;
+constexpr int kNf4ZeroCode = 7;       // nf4[7] == 0.0
+constexpr int kDyn8ZeroCode = 127;    // dyn8[127] == 0.0
+
+// Decode tables: the 16 NF4 values and the 256 dynamic8 values, ascending.
+struct DecodeTables {
+  float nf4[16];
+  float dyn8[256];
+};
+
+// Encode tables: thr[j] is the smallest float whose nearest code (ties to the
+// lower index) is j + 1, so code(v) = #{ j : v >= thr[j] }.
+struct EncodeTables {
+  float nf4_thr[16];   // 15 used
+  float dyn8_thr[256]; // 255 used
+};
+
+const DecodeTables& decode_tables();
+const EncodeTables& encode_tables();
+
+// Launch accounting (for the launch count reported by the ABI).
+void note_launch(int n = 1);
+
+// Per-call view of an nf4_tensor for device code.
+struct Nf4View {
+  const uint8_t* packed;
+  const void* absmax;      // uint8 codes (dq) or float
+  const float* nested;
+  const float* offset;     // device scalar (dq)
+  int64_t numel;
+  int dq;
+};
+
+// ---- quant.cu -----------------------------------------------------------------
+cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf4_tensor& out,
+                            void* ws, int* status, cudaStream_t st);
+size_t quantize_ws_bytes(int64_t numel, int dq);
+cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st);
+
+// ---- linear_simt.cu (fp32 profile; adapter reductions for both profiles) -------
+struct LinearArgs {
+  int64_t M, N, K;
+  int r;
+  float s;
+  Nf4View W;
+};
+cudaError_t launch_lora_down(const LinearArgs& a, nf4_dtype cd, const void* x, const float* A,
+                             float* T, cudaStream_t st);
+cudaError_t launch_fwd_simt(const LinearArgs& a, nf4_dtype cd, const void* x, const float* T,
+                            const float* B, void* y, cudaStream_t st);
+cudaError_t launch_lora_g(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* B,
+                          float* G, cudaStream_t st);
+cudaError_t launch_dx_simt(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* G,
+                           const float* A, void* dx, cudaStream_t st);
+cudaError_t launch_lora_dA(const LinearArgs& a, nf4_dtype cd, const float* G, const void* x,
+                           float* dA, cudaStream_t st);
+cudaError_t launch_lora_dB(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* T,
+                           float* dB, cudaStream_t st);
+
+// ---- device helpers -----------------------------------------------------------
+__device__ __forceinline__ float load_as_float(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_as_float(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_from_float(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_from_float(__nv_bfloat16* p, int64_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+// Round a float to the nearest bf16 value and return it as a float.
+__device__ __forceinline__ float round_bf16(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// a' of block b: dyn8[code] * nested + offset as two separately rounded operations
+// (the decode the pages' kernels use: "decode-separate-rn"), or the fp32 absmax.
+__device__ __forceinline__ float block_scale(const Nf4View& w, int64_t b, const float* dyn8_smem,
+                                             float offset) {
+  if (w.dq) {
+    const uint8_t code = static_cast<const uint8_t*>(w.absmax)[b];
+    return __fadd_rn(__fmul_rn(dyn8_smem[code], w.nested[b >> 8]), offset);
+  }
+  return static_cast<const float*>(w.absmax)[b];
+}
+
+// 4-bit code of flat element i (high nibble holds the even element).
+__device__ __forceinline__ int nf4_code_at(const uint8_t* packed, int64_t i) {
+  const uint8_t byte = packed[i >> 1];
+  return (i & 1) ? (byte & 0x0F) : (byte >> 4);
+}
+
+}  // namespace qnf4

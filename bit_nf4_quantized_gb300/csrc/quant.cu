@@ -1,0 +1,303 @@
+// NF4 blockwise quantization with nested dynamic8 absmax, and dequantization.
+//
+// Format and decode: "Native model adaptation and NF4", section "Packed NF4 and the
+// portable QLoRA profile" (64-element absmax blocks, the 16-value NF4 codebook, two
+// codes per byte, block maxima centred by their global FP32 mean and quantized with
+// dynamic8 in blocks of 256) and section "Fused GPU NF4 decodes inside the matrix
+// kernel".  Deterministic, byte-identical requantization: "NF4 Layer Streaming --
+// Gate results", section "P3 is solved".
+//
+// Lane mapping (all kernels here): a warp walks "quad rows" of 128 elements; lane l
+// owns elements 4l..4l+3 of the row, so a half warp covers one 64-element block and
+// every global access of a warp instruction is contiguous.
+//
+// quantize = three launches:
+//   1. nf4_encode_blocks: absmax, 4-bit codes, packing; per 256-block group the
+//      float64 pairwise-tree sum of the absmax values (double quant only).
+//   2. nf4_absmax_mean: one CTA finishes the tree over the group sums -> offset.
+//   3. nf4_encode_nested: centre, nested absmax per group, dynamic8 codes.
+#include "common.cuh"
+
+namespace qnf4 {
+namespace {
+
+constexpr int kQuantThreads = 256;                 // 8 warps
+constexpr int kQuadRowsPerWarp = 16;               // 8 warps x 16 x 128 = one 16384 group
+
+__device__ __forceinline__ int nf4_encode(float v, const float* thr) {
+  int c = (v >= thr[7]) ? 8 : 0;
+  c += (v >= thr[c + 3]) ? 4 : 0;
+  c += (v >= thr[c + 1]) ? 2 : 0;
+  c += (v >= thr[c]) ? 1 : 0;
+  return c;
+}
+
+__device__ __forceinline__ int dyn8_encode(float v, const float* thr) {
+  int c = 0;
+#pragma unroll
+  for (int step = 128; step >= 1; step >>= 1) c += (v >= thr[c + step - 1]) ? step : 0;
+  return c;
+}
+
+__device__ __forceinline__ void load_quad(const float* x, int64_t e0, int64_t n, float v[4]) {
+  if (e0 + 3 < n) {
+    const float4 t = __ldcs(reinterpret_cast<const float4*>(x + e0));
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (e0 + i < n) ? x[e0 + i] : 0.0f;
+  }
+}
+
+__device__ __forceinline__ void load_quad(const __nv_bfloat16* x, int64_t e0, int64_t n, float v[4]) {
+  if (e0 + 3 < n) {
+    const uint2 t = __ldcs(reinterpret_cast<const uint2*>(x + e0));
+    v[0] = __uint_as_float(t.x << 16);
+    v[1] = __uint_as_float(t.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(t.y << 16);
+    v[3] = __uint_as_float(t.y & 0xFFFF0000u);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (e0 + i < n) ? __bfloat162float(x[e0 + i]) : 0.0f;
+  }
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kQuantThreads)
+nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict__ packed,
+                  float* __restrict__ absmax, double* __restrict__ group_sum, EncodeTables tabs,
+                  int* status) {
+  __shared__ float thr[16];
+  __shared__ double gsum[kNested];
+  if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t group_base = static_cast<int64_t>(blockIdx.x) * kGroupElems;
+  bool nonfinite = false;
+
+#pragma unroll 4
+  for (int u = 0; u < kQuadRowsPerWarp; ++u) {
+    const int64_t e0 = group_base + warp * (kQuadRowsPerWarp * 128) + u * 128 + 4 * lane;
+    float v[4];
+    load_quad(x, e0, numel, v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) nonfinite |= !isfinite(v[i]);
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+
+    int code[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int c = kNf4ZeroCode;
+      if (m > 0.0f) c = nf4_encode(__fdiv_rn(v[i], m), thr);
+      code[i] = (e0 + i < numel) ? c : 0;   // pad nibble of an odd tail is 0
+    }
+    const uint32_t b0 = static_cast<uint32_t>((code[0] << 4) | code[1]);
+    const uint32_t b1 = static_cast<uint32_t>((code[2] << 4) | code[3]);
+    const int64_t byte0 = e0 >> 1;
+    if (e0 + 3 < numel) {
+      *reinterpret_cast<uint16_t*>(packed + byte0) = static_cast<uint16_t>(b0 | (b1 << 8));
+    } else if (e0 < numel) {
+      packed[byte0] = static_cast<uint8_t>(b0);
+      if (e0 + 2 < numel) packed[byte0 + 1] = static_cast<uint8_t>(b1);
+    }
+    const int block_in_group = warp * 32 + 2 * u + (lane >> 4);
+    if ((lane & 15) == 0) {
+      if (e0 < numel) absmax[e0 >> 6] = m;
+      gsum[block_in_group] = (e0 < numel) ? static_cast<double>(m) : 0.0;
+    }
+  }
+  if (nonfinite) atomicCAS(status, 0, static_cast<int>(NF4_ERR_NONFINITE));
+  if (group_sum == nullptr) return;
+  __syncthreads();
+  // float64 pairwise tree: s[i] += s[i + h] for h = 128, 64, ..., 1
+  for (int h = kNested / 2; h >= 1; h >>= 1) {
+    if (threadIdx.x < h) gsum[threadIdx.x] += gsum[threadIdx.x + h];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) group_sum[blockIdx.x] = gsum[0];
+}
+
+// One CTA: the same pairwise tree over the group sums padded with zeros to p2
+// entries (in place in the workspace), then offset = float(sum / nb).
+__global__ void __launch_bounds__(1024)
+nf4_absmax_mean(double* __restrict__ gs, int64_t ng, int64_t p2, int64_t nb, float* __restrict__ offset) {
+  int64_t valid = ng;
+  for (int64_t h = p2 / 2; h >= 1; h /= 2) {
+    for (int64_t i = threadIdx.x; i < h; i += blockDim.x) {
+      const double a = (i < valid) ? gs[i] : 0.0;
+      const double b = (i + h < valid) ? gs[i + h] : 0.0;
+      gs[i] = a + b;
+    }
+    valid = h;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *offset = __double2float_rn(__ddiv_rn(gs[0], static_cast<double>(nb)));
+}
+
+__global__ void __launch_bounds__(kNested)
+nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __restrict__ offset_p,
+                  uint8_t* __restrict__ codes, float* __restrict__ nested, EncodeTables tabs) {
+  __shared__ float thr[256];
+  __shared__ float red[kNested / 32];
+  thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
+  const float offset = *offset_p;
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * kNested + threadIdx.x;
+  const float c = (b < nb) ? __fsub_rn(absmax[b], offset) : 0.0f;
+  float m = fabsf(c);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int w = 1; w < kNested / 32; ++w) m = fmaxf(m, red[w]);
+  if (b < nb) {
+    const int code = (m > 0.0f) ? dyn8_encode(__fdiv_rn(c, m), thr) : kDyn8ZeroCode;
+    codes[b] = static_cast<uint8_t>(code);
+  }
+  if (threadIdx.x == 0) nested[blockIdx.x] = m;
+}
+
+// ---- dequantize -----------------------------------------------------------------
+
+constexpr int kDeqThreads = 256;
+constexpr int kDeqQuadRows = 8;    // per warp: 8 x 128 elements
+
+__device__ __forceinline__ void store_quad(float* y, int64_t e0, int64_t n, const float w[4]) {
+  if (e0 + 3 < n) {
+    __stcs(reinterpret_cast<float4*>(y + e0), make_float4(w[0], w[1], w[2], w[3]));
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (e0 + i < n) y[e0 + i] = w[i];
+  }
+}
+
+__device__ __forceinline__ void store_quad(__nv_bfloat16* y, int64_t e0, int64_t n, const float w[4]) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(w[0], w[1]);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(w[2], w[3]);
+  if (e0 + 3 < n) {
+    uint2 t;
+    t.x = *reinterpret_cast<const uint32_t*>(&lo);
+    t.y = *reinterpret_cast<const uint32_t*>(&hi);
+    __stcs(reinterpret_cast<uint2*>(y + e0), t);
+  } else {
+    for (int i = 0; i < 4; ++i)
+      if (e0 + i < n) y[e0 + i] = __float2bfloat16_rn(w[i]);
+  }
+}
+
+template <typename Tout, bool kDQ>
+__global__ void __launch_bounds__(kDeqThreads)
+nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
+  __shared__ float lut[16][32];        // NF4 values replicated per lane: conflict-free lookups
+  __shared__ float dyn8[256];
+  for (int i = threadIdx.x; i < 16 * 32; i += kDeqThreads) lut[i >> 5][i & 31] = tabs.nf4[i >> 5];
+  dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = w.numel;
+  const float offset = kDQ ? *w.offset : 0.0f;
+  const int64_t warp_base =
+      (static_cast<int64_t>(blockIdx.x) * (kDeqThreads / 32) + warp) * (kDeqQuadRows * 128);
+#pragma unroll 4
+  for (int u = 0; u < kDeqQuadRows; ++u) {
+    const int64_t e0 = warp_base + u * 128 + 4 * lane;
+    if (e0 >= n) break;
+    const int64_t byte0 = e0 >> 1;
+    uint32_t bytes;
+    if (e0 + 3 < n) {
+      bytes = __ldcs(reinterpret_cast<const uint16_t*>(w.packed + byte0));
+    } else {
+      bytes = w.packed[byte0];
+      if (e0 + 2 < n) bytes |= static_cast<uint32_t>(w.packed[byte0 + 1]) << 8;
+    }
+    const int64_t blk = e0 >> 6;
+    float a;
+    if (kDQ) {
+      const uint8_t c = static_cast<const uint8_t*>(w.absmax)[blk];
+      a = __fadd_rn(__fmul_rn(dyn8[c], w.nested[blk >> 8]), offset);
+    } else {
+      a = static_cast<const float*>(w.absmax)[blk];
+    }
+    float v[4];
+    v[0] = __fmul_rn(lut[(bytes >> 4) & 15][lane], a);
+    v[1] = __fmul_rn(lut[bytes & 15][lane], a);
+    v[2] = __fmul_rn(lut[(bytes >> 12) & 15][lane], a);
+    v[3] = __fmul_rn(lut[(bytes >> 8) & 15][lane], a);
+    store_quad(y, e0, n, v);
+  }
+}
+
+int64_t pow2_at_least(int64_t v) {
+  int64_t p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t quantize_ws_bytes(int64_t numel, int dq) {
+  if (!dq) return 0;
+  const int64_t nb = (numel + kBlock - 1) / kBlock;
+  const int64_t ng = (nb + kNested - 1) / kNested;
+  return align256(sizeof(float) * nb) + align256(sizeof(double) * pow2_at_least(ng));
+}
+
+cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf4_tensor& out,
+                            void* ws, int* status, cudaStream_t st) {
+  const int64_t nb = (numel + kBlock - 1) / kBlock;
+  const int64_t ng = (nb + kNested - 1) / kNested;
+  const EncodeTables& et = encode_tables();
+  float* absmax_f = out.double_quant ? static_cast<float*>(ws) : static_cast<float*>(out.absmax);
+  double* gsum = out.double_quant
+                     ? reinterpret_cast<double*>(static_cast<char*>(ws) + align256(sizeof(float) * nb))
+                     : nullptr;
+  if (ng > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ng));
+  if (xd == NF4_F32)
+    nf4_encode_blocks<float><<<grid, kQuantThreads, 0, st>>>(static_cast<const float*>(x), numel,
+                                                             out.packed, absmax_f, gsum, et, status);
+  else
+    nf4_encode_blocks<__nv_bfloat16><<<grid, kQuantThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), numel, out.packed, absmax_f, gsum, et, status);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !out.double_quant) return e;
+  nf4_absmax_mean<<<1, 1024, 0, st>>>(gsum, ng, pow2_at_least(ng), nb, out.offset);
+  note_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  nf4_encode_nested<<<grid, kNested, 0, st>>>(absmax_f, nb, out.offset,
+                                              static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st) {
+  const int64_t per_cta = static_cast<int64_t>(kDeqThreads / 32) * kDeqQuadRows * 128;
+  const int64_t ctas = (w.numel + per_cta - 1) / per_cta;
+  if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ctas));
+  const DecodeTables& dt = decode_tables();
+  if (od == NF4_F32) {
+    if (w.dq) nf4_decode<float, true><<<grid, kDeqThreads, 0, st>>>(w, static_cast<float*>(y), dt);
+    else nf4_decode<float, false><<<grid, kDeqThreads, 0, st>>>(w, static_cast<float*>(y), dt);
+  } else {
+    auto* yb = static_cast<__nv_bfloat16*>(y);
+    if (w.dq) nf4_decode<__nv_bfloat16, true><<<grid, kDeqThreads, 0, st>>>(w, yb, dt);
+    else nf4_decode<__nv_bfloat16, false><<<grid, kDeqThreads, 0, st>>>(w, yb, dt);
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace qnf4

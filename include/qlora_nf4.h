@@ -1,0 +1,168 @@
+/*
+ * qlora_nf4.h -- C ABI of the NF4 double-quantized frozen-base QLoRA linear for
+ * one NVIDIA GB300 (sm_103a).  Library: libqlora_nf4.so (built in-tree).
+ *
+ * Sources, cited by page title and section:
+ *   [ADAPT] "Native model adaptation and NF4" (anerlang.org/docs/gen-adaptation)
+ *   [GATE]  "NF4 Layer Streaming -- Gate results" (Soup, gate-v0.72.2-nf4.md)
+ *   [QUAL]  V100 accelerated qualification record (native_training_accelerated_20261031.json)
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device addresses on the current device; the
+ *     caller owns every buffer.  The library keeps no pointer after a call returns
+ *     and allocates no device memory: scratch comes from the caller's workspace.
+ *   - Device buffers must be 16-byte aligned (NF4_ERR_ALIGN otherwise).
+ *   - "stream" is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *     asynchronously; argument, shape and alignment errors are reported
+ *     synchronously by the return value and enqueue nothing.
+ *   - Conditions only the device can see (a non-finite input found while
+ *     quantizing, a bounded wait that gave up) set a per-device status word that
+ *     qlora_last_device_status() reads.
+ *   - There is no CPU fallback and no silent precision change ([ADAPT] "Explicit
+ *     accelerated training profiles": "There is no automatic precision change or
+ *     CPU fallback"; unsupported values "fail explicitly").
+ *
+ * NF4 format ([ADAPT] "Packed NF4 and the portable QLoRA profile"; sizes from
+ * [GATE] "P3 is solved" and [QUAL] component_benchmarks.packed_gpu_bytes):
+ *   A tensor of numel elements (row-major [N, K] for a weight, flattened) is cut
+ *   into nb = ceil(numel/64) blocks.  Element i has a 4-bit code; two codes per
+ *   byte, element 2j in the high nibble, 2j+1 in the low nibble (pad nibble 0).
+ *   Without double quantization each block has an fp32 absmax.  With it, each
+ *   block has a uint8 dynamic8 code of (absmax - offset), nnb = ceil(nb/256) fp32
+ *   nested absmax values and one fp32 offset (the mean of all block absmax values).
+ *   Decode: a' = dyn8[code] * nested + offset (two roundings, no FMA), then
+ *   w = nf4[q] * a'.
+ */
+#ifndef QLORA_NF4_H
+#define QLORA_NF4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QLORA_NF4_ABI_VERSION 1
+
+typedef enum {
+  NF4_OK = 0,
+  NF4_ERR_ARG = 1,        /* null pointer, numel <= 0, bad enum, rank out of 1..256 */
+  NF4_ERR_SHAPE = 2,      /* shape the selected path does not support */
+  NF4_ERR_ALIGN = 3,      /* a device pointer is not 16-byte aligned */
+  NF4_ERR_DTYPE = 4,      /* dtype not allowed for this call */
+  NF4_ERR_NONFINITE = 5,  /* NaN or Inf in an input to nf4_quantize (device status) */
+  NF4_ERR_CORRUPT = 6,    /* descriptor inconsistent with its numel / double_quant */
+  NF4_ERR_CUDA = 7,       /* a CUDA runtime call failed (launch, no device, ...) */
+  NF4_ERR_TIMEOUT = 8,    /* a device-side bounded wait gave up (device status) */
+  NF4_ERR_WORKSPACE = 9   /* workspace null or smaller than the size query returns */
+} nf4_status;
+
+typedef enum { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
+
+typedef enum {
+  QLORA_SCALE_LORA = 0,   /* s = alpha / rank        ([ADAPT] "LoRA FA includes ...") */
+  QLORA_SCALE_RSLORA = 1  /* s = alpha / sqrt(rank)  ([ADAPT] "Adapter API": rs_lora) */
+} qlora_scale_mode;
+
+/* One quantized tensor.  All pointers are device pointers owned by the caller. */
+typedef struct {
+  int64_t numel;          /* number of logical elements (> 0) */
+  int32_t double_quant;   /* 1: nested dynamic8 absmax; 0: fp32 absmax */
+  int32_t reserved;       /* must be 0 */
+  uint8_t* packed;        /* [ceil(numel/2)] two 4-bit codes per byte */
+  void* absmax;           /* double_quant: uint8[nb] codes; else float[nb] */
+  float* nested_absmax;   /* double_quant: float[nnb]; else NULL */
+  float* offset;          /* double_quant: float[1]; else NULL */
+} nf4_tensor;
+
+/* ABI version (QLORA_NF4_ABI_VERSION). */
+int32_t nf4_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* nf4_status_str(nf4_status s);
+
+/* nb = ceil(numel/64) and nnb = ceil(nb/256); 0 when numel <= 0. */
+int64_t nf4_num_blocks(int64_t numel);
+int64_t nf4_num_nested(int64_t numel);
+
+/* Device bytes of one quantized tensor without the offset scalar:
+ *   double_quant: ceil(n/2) + nb + 4*nnb   ([QUAL] packed_gpu_bytes; [GATE] "P3 is solved")
+ *   otherwise:    ceil(n/2) + 4*nb
+ * Returns 0 when numel <= 0. */
+size_t nf4_packed_bytes(int64_t numel, int32_t double_quant);
+
+/* Copy the library's constant code tables to host memory: 16 NF4 values and 256
+ * dynamic8 values, both ascending ([GATE] "P3 is solved": one shared constant copy
+ * of each).  Either pointer may be NULL. */
+void nf4_code_tables(float* nf4_out16, float* dyn8_out256);
+
+/* Workspace (device bytes) nf4_quantize needs for numel elements. */
+size_t nf4_quantize_workspace_bytes(int64_t numel, int32_t double_quant);
+
+/* Quantize x (device, x_dtype NF4_F32 or NF4_BF16, numel elements, contiguous)
+ * into *out, whose numel and double_quant select the format and whose pointers
+ * receive the result ([ADAPT] "Packed NF4 ...": absmax blocks of 64, nearest of the
+ * 16 NF4 codes; with double quantization the block maxima are centred by their
+ * global FP32 mean and quantized with dynamic8 in blocks of 256).  Deterministic:
+ * the same input gives the same bytes on every call ([GATE] "P3 is solved").
+ * ws: device workspace of at least nf4_quantize_workspace_bytes() bytes.
+ * A NaN/Inf input sets NF4_ERR_NONFINITE in the device status word; the output
+ * bytes are then unspecified. */
+nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel,
+                        const nf4_tensor* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Decode *w into y (device, out_dtype NF4_F32 or NF4_BF16, w->numel elements).
+ * fp32 output is exact nf4[q]*a'; bf16 output is that value rounded to nearest
+ * even ([ADAPT] "Fused GPU NF4 decodes inside the matrix kernel"). */
+nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream);
+
+/* Workspace (device bytes) needed by qlora_linear_fwd / qlora_linear_bwd. */
+size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
+size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
+
+/* Forward of the frozen-base QLoRA linear ([ADAPT] "One model contract": the NF4
+ * base is frozen and needs an adapter; "Packed NF4 ...": linear operations decode
+ * the weight; [ADAPT] "LoRA FA ...": s = alpha / rank):
+ *     T = x A^T          (T_out, fp32 [M, rank], kept for the backward pass)
+ *     y = x W^T + s T B^T
+ * Shapes: x [M, K] row-major, W an nf4_tensor of numel N*K holding [N, K]
+ * row-major, A fp32 [rank, K], B fp32 [N, rank], y [M, N].
+ * compute = NF4_F32: x and y fp32, fp32 arithmetic, no TF32, any M, N, K >= 1.
+ * compute = NF4_BF16: x and y bf16, bf16 tensor-core operands (the decoded weight
+ *   rounded once to bf16, A and B rounded to bf16, s*T rounded to bf16) with fp32
+ *   accumulation; needs K % 64 == 0 and N % 8 == 0 (NF4_ERR_SHAPE otherwise).
+ * rank 1..256 ([ADAPT] "Adapter API") and rank <= min(N, K); alpha finite.
+ * ws: device workspace of qlora_fwd_workspace_bytes() bytes. */
+nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                            qlora_scale_mode mode, nf4_dtype compute,
+                            const void* x, const nf4_tensor* W, const float* A, const float* B,
+                            void* y, float* T_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward ([ADAPT] "Packed NF4 ...": input gradients through the frozen base, no
+ * base-weight gradient; [GATE] "The TFLOPS back-check": no dL/dW):
+ *     G  = dY B                    (internal, fp32 [M, rank])
+ *     dX = dY W + s G A            [M, K], dtype of compute
+ *     dA = s G^T x                 fp32 [rank, K]  (overwritten, not accumulated)
+ *     dB = s dY^T T                fp32 [N, rank]  (overwritten, not accumulated)
+ * dy [M, N] and x [M, K] in the compute dtype; T is the forward's T_out.
+ * Shape rules as for the forward.  Reductions are deterministic (no atomics). */
+nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                            qlora_scale_mode mode, nf4_dtype compute,
+                            const void* dy, const void* x, const float* T,
+                            const nf4_tensor* W, const float* A, const float* B,
+                            void* dx, float* dA, float* dB,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronize `stream`, then return the current device's status word (NF4_OK if no
+ * device-side condition was recorded); clear != 0 resets it to NF4_OK. */
+nf4_status qlora_last_device_status(void* stream, int32_t clear);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t nf4_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_NF4_H */

@@ -82,6 +82,14 @@ def backward(dy, x, W, A, B, s: float, compute: str = "bf16"):
     return dX, dA, dB, G
 
 
+def adapter_backward(dy, x, A, B, s: float, compute: str = "bf16"):
+    """(dA, dB, G) alone -- the same formulas as ``backward`` without the M x N x K dX product."""
+    dy64, x64, A64, B64 = _operands(compute, dy, x, A, B)
+    T = x64 @ A64.T
+    G = dy64 @ B64
+    return s * (G.T @ x64), s * (dy64.T @ T), G
+
+
 def rel_frobenius(got, want) -> float:
     """||got - want||_F / ||want||_F (0 when both are zero)."""
     got = np.asarray(got, dtype=np.float64)

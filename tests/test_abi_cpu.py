@@ -1,0 +1,125 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, its size queries and tables agree with the oracle, and invalid
+arguments are refused before any device work (no compute call is made here)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from bit_nf4_quantized_gb300 import binding, build
+from oracle import codebooks as cb
+from oracle import nf4 as onf4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("defined",):
+                names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding.ENTRY_POINTS) <= set(names)
+    assert lib.nf4_abi_version() == 1
+
+
+def test_size_queries_match_oracle(lib):
+    for n in (1, 2, 63, 64, 65, 16383, 16384, 16385, 576 * 576, 4096 * 14336, 2 ** 30, 2 ** 31 + 5):
+        assert lib.nf4_num_blocks(n) == onf4.num_blocks(n)
+        assert lib.nf4_num_nested(n) == onf4.num_nested(n)
+        assert lib.nf4_packed_bytes(n, 1) == onf4.packed_bytes(n, True)
+        assert lib.nf4_packed_bytes(n, 0) == onf4.packed_bytes(n, False)
+    assert lib.nf4_packed_bytes(0, 1) == 0
+
+
+def test_tables_equal_oracle_bit_for_bit():
+    nf4, dyn8 = binding.code_tables()
+    assert np.array_equal(np.array(nf4, np.float32).view(np.uint32), cb.nf4_codebook().view(np.uint32))
+    assert np.array_equal(np.array(dyn8, np.float32).view(np.uint32),
+                          cb.dynamic8_codebook().view(np.uint32))
+
+
+def _fake_tensor(numel, dq=1, base=0x10000000):
+    t = binding._Nf4Tensor()
+    t.numel, t.double_quant, t.reserved = numel, dq, 0
+    t.packed, t.absmax = base, base + 0x100000
+    t.nested_absmax = base + 0x200000 if dq else None
+    t.offset = base + 0x300000 if dq else None
+    return t
+
+
+def test_validation_refuses_bad_arguments(lib):
+    x = ctypes.c_void_p(0x20000000)
+    ws = ctypes.c_void_p(0x30000000)
+    t = _fake_tensor(1000)
+    q = lambda *a: lib.nf4_quantize(*a)  # noqa: E731
+    assert q(None, 0, 1000, ctypes.byref(t), ws, 1 << 20, None) == binding.NF4_ERR_ARG
+    assert q(x, 0, 0, ctypes.byref(t), ws, 1 << 20, None) == binding.NF4_ERR_ARG
+    assert q(x, 7, 1000, ctypes.byref(t), ws, 1 << 20, None) == binding.NF4_ERR_DTYPE
+    assert q(x, 0, 999, ctypes.byref(t), ws, 1 << 20, None) == binding.NF4_ERR_CORRUPT
+    assert q(ctypes.c_void_p(0x20000004), 0, 1000, ctypes.byref(t), ws, 1 << 20, None) == binding.NF4_ERR_ALIGN
+    assert q(x, 0, 1000, ctypes.byref(t), ws, 8, None) == binding.NF4_ERR_WORKSPACE
+    bad = _fake_tensor(1000)
+    bad.nested_absmax = None
+    assert q(x, 0, 1000, ctypes.byref(bad), ws, 1 << 20, None) == binding.NF4_ERR_CORRUPT
+    nodq = _fake_tensor(1000, dq=0)
+    nodq.offset = 0x40000000
+    assert q(x, 0, 1000, ctypes.byref(nodq), ws, 1 << 20, None) == binding.NF4_ERR_CORRUPT
+
+    assert lib.nf4_dequantize(None, x, 0, None) == binding.NF4_ERR_ARG
+    assert lib.nf4_dequantize(ctypes.byref(t), x, 3, None) == binding.NF4_ERR_DTYPE
+
+    w = _fake_tensor(64 * 128)
+    p = ctypes.c_void_p(0x50000000)
+    f = lambda M, N, K, r, alpha=16.0, mode=0, cd=1, wt=w, wsz=1 << 30: lib.qlora_linear_fwd(  # noqa: E731
+        M, N, K, r, ctypes.c_float(alpha), mode, cd, p, ctypes.byref(wt), p, p, p, p, ws, wsz, None)
+    assert f(4, 64, 128, 0) == binding.NF4_ERR_ARG            # rank below 1
+    assert f(4, 64, 128, 257) == binding.NF4_ERR_ARG          # rank above 256
+    assert f(4, 64, 128, 65) == binding.NF4_ERR_ARG           # rank above min(N, K)
+    assert f(4, 64, 128, 8, alpha=float("nan")) == binding.NF4_ERR_ARG
+    assert f(4, 64, 128, 8, mode=5) == binding.NF4_ERR_ARG
+    assert f(4, 64, 128, 8, cd=9) == binding.NF4_ERR_DTYPE
+    w2 = _fake_tensor(100 * 96)
+    assert f(4, 100, 96, 8, wt=w2) == binding.NF4_ERR_SHAPE  # bf16 needs K % 64 == 0
+    w3 = _fake_tensor(100 * 128)
+    assert f(4, 100, 128, 8, wt=w3) == binding.NF4_ERR_SHAPE  # bf16 needs N % 8 == 0
+    assert f(4, 64, 64, 8) == binding.NF4_ERR_CORRUPT        # numel != N*K
+    if lib.qlora_fwd_workspace_bytes(4, 64, 128, 8, 1) > 0:
+        assert f(4, 64, 128, 8, wsz=1) == binding.NF4_ERR_WORKSPACE
+    b = lambda wsz: lib.qlora_linear_bwd(  # noqa: E731
+        4, 64, 128, 8, ctypes.c_float(16.0), 0, 1, p, p, p, ctypes.byref(w), p, p, p, p, p, ws, wsz, None)
+    assert b(0) == binding.NF4_ERR_WORKSPACE
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert lib.nf4_status_str(s).decode()
+    assert lib.nf4_status_str(99).decode() == "unknown status"
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB", None)
+    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        binding.load()

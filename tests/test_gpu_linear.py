@@ -1,0 +1,145 @@
+"""GPU parity of qlora_linear_fwd / qlora_linear_bwd against the float64 oracle.
+
+Tolerances (relative Frobenius): 1e-5 for the fp32 profile, 2e-2 for the bf16
+profile.  Every case uses B != 0 so the adapter path carries weight.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bit_nf4_quantized_gb300 import binding
+from bit_nf4_quantized_gb300 import workloads as wl
+from oracle import nf4 as onf4
+from oracle import qlora
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def _quantized_weight(N, K, seed, dist="normal"):
+    if dist == "t":
+        w = wl.student_t((N, K), 5, 0.02, 3, seed)
+    else:
+        w = wl.normal((N, K), 0.02, 2, seed)
+    ref = onf4.quantize(w, double_quant=True)
+    q = binding.Nf4Tensor.empty((N, K), True, DEV)
+    q.packed.copy_(torch.from_numpy(ref["packed"]))
+    q.absmax.copy_(torch.from_numpy(ref["absmax"]))
+    q.nested_absmax.copy_(torch.from_numpy(ref["nested"]))
+    q.offset[0] = float(ref["offset"])
+    return q, onf4.dequantize(ref, "f32").reshape(N, K)
+
+
+def _run_case(M, N, K, r, alpha, compute, mode=binding.SCALE_LORA, seed=0, dist="normal", rows=None):
+    tdt = torch.float32 if compute == "f32" else torch.bfloat16
+    q, w_deq = _quantized_weight(N, K, seed, dist)
+    x = wl.normal((M, K), 1.0, 1, seed + 1)
+    dy = wl.normal((M, N), 1.0, 1, seed + 2)
+    A, B = wl.adapters(N, K, r, 1, seed + 3)
+    xd = torch.from_numpy(x).to(DEV).to(tdt)
+    dyd = torch.from_numpy(dy).to(DEV).to(tdt)
+    Ad, Bd = torch.from_numpy(A).to(DEV), torch.from_numpy(B).to(DEV)
+    y, T = binding.qlora_linear_fwd(xd, q, Ad, Bd, alpha, mode)
+    dx, dA, dB = binding.qlora_linear_bwd(dyd, xd, T, q, Ad, Bd, alpha, mode)
+    torch.cuda.synchronize()
+    s = qlora.lora_scale(alpha, r, "lora" if mode == binding.SCALE_LORA else "rslora")
+    xh, dyh = xd.float().cpu().numpy(), dyd.float().cpu().numpy()
+    sel = slice(None) if rows is None else rows
+    y_ref, T_ref = qlora.forward(xh[sel], w_deq, A, B, s, compute)
+    dX_ref, _, _, _ = qlora.backward(dyh[sel], xh[sel], w_deq, A, B, s, compute)
+    dA_ref, dB_ref, _ = qlora.adapter_backward(dyh, xh, A, B, s, compute)
+    tol = TOL[compute]
+    got = dict(y=y.float().cpu().numpy()[sel], T=T.cpu().numpy()[sel], dX=dx.float().cpu().numpy()[sel],
+               dA=dA.cpu().numpy(), dB=dB.cpu().numpy())
+    want = dict(y=y_ref, T=T_ref, dX=dX_ref, dA=dA_ref, dB=dB_ref)
+    errs = {k: qlora.rel_frobenius(got[k], want[k]) for k in got}
+    for k, e in errs.items():
+        assert e <= tol, (k, e, errs)
+    assert np.any(got["dA"] != 0)
+    return errs
+
+
+def test_fp32_profile_576(lib):
+    c = wl.W1
+    _run_case(c["M"], c["N"], c["K"], c["r"], c["alpha"], "f32")
+
+
+@pytest.mark.parametrize("M,N,K,r", [(1, 8, 64, 1), (3, 40, 100, 2), (77, 130, 200, 5), (200, 96, 64, 16)])
+def test_fp32_profile_ragged(lib, M, N, K, r):
+    _run_case(M, N, K, r, 8.0, "f32", seed=M)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 17, 33])
+def test_bf16_small_m(lib, M):
+    _run_case(M, 520, 1024, 8, 16.0, "bf16", seed=M)
+
+
+@pytest.mark.parametrize("M,N,K,r", [(64, 8, 64, 1), (130, 200, 192, 5), (300, 264, 576, 16),
+                                     (511, 1032, 640, 64), (129, 136, 128, 128)])
+def test_bf16_tiles_and_tails(lib, M, N, K, r):
+    _run_case(M, N, K, r, 16.0, "bf16", seed=N)
+
+
+def test_bf16_rslora_scale(lib):
+    _run_case(40, 256, 512, 8, 16.0, "bf16", mode=binding.SCALE_RSLORA)
+
+
+def test_bf16_rank_256(lib):
+    _run_case(96, 512, 256, 256, 16.0, "bf16")
+
+
+def test_smollm2_qv_shapes(lib):
+    c = wl.W2
+    for name, N, K in c["shapes"]:
+        if name in c["targets"]:
+            _run_case(c["M"], N, K, c["r"], c["alpha"], "bf16", seed=N)
+
+
+@pytest.mark.parametrize("name", ["k_proj", "gate_proj", "down_proj"])
+def test_llama8b_layer_sampled_rows(lib, name):
+    c = wl.W3
+    N, K = {n: (a, b) for n, a, b in c["shapes"]}[name]
+    rows = np.sort(np.random.default_rng(5).choice(c["M"], 64, replace=False))
+    _run_case(c["M"], N, K, c["r"], c["alpha"], "bf16", seed=K, dist="t", rows=rows)
+
+
+def test_empty_batch(lib):
+    q, _ = _quantized_weight(64, 128, 1)
+    A = torch.randn(4, 128, device=DEV)
+    B = torch.randn(64, 4, device=DEV)
+    x = torch.empty(0, 128, device=DEV, dtype=torch.bfloat16)
+    y, T = binding.qlora_linear_fwd(x, q, A, B, 8.0)
+    assert y.shape == (0, 64)
+    dy = torch.empty(0, 64, device=DEV, dtype=torch.bfloat16)
+    dx, dA, dB = binding.qlora_linear_bwd(dy, x, T, q, A, B, 8.0,
+                                          dA=torch.full((4, 128), 7.0, device=DEV),
+                                          dB=torch.full((64, 4), 7.0, device=DEV))
+    assert torch.all(dA == 0) and torch.all(dB == 0)
+
+
+def test_shape_errors_are_explicit(lib):
+    q, _ = _quantized_weight(64, 96, 1)
+    x = torch.randn(4, 96, device=DEV, dtype=torch.bfloat16)
+    with pytest.raises(binding.Nf4Error) as e:
+        binding.qlora_linear_fwd(x, q, torch.randn(4, 96, device=DEV), torch.randn(64, 4, device=DEV), 8.0)
+    assert e.value.status == binding.NF4_ERR_SHAPE
+
+
+def test_linear_is_deterministic(lib):
+    q, _ = _quantized_weight(520, 1024, 3)
+    x = torch.randn(300, 1024, device=DEV, dtype=torch.bfloat16)
+    dy = torch.randn(300, 520, device=DEV, dtype=torch.bfloat16)
+    A = torch.randn(16, 1024, device=DEV) / 16
+    B = torch.randn(520, 16, device=DEV) / 100
+    outs = []
+    for _ in range(2):
+        y, T = binding.qlora_linear_fwd(x, q, A, B, 16.0)
+        dx, dA, dB = binding.qlora_linear_bwd(dy, x, T, q, A, B, 16.0)
+        outs.append([t.clone() for t in (y, T, dx, dA, dB)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)

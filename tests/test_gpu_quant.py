@@ -1,0 +1,163 @@
+"""GPU parity of nf4_quantize / nf4_dequantize against the oracle (bit-exact).
+
+Inputs come from the seeded generators in bit_nf4_quantized_gb300.workloads; the
+same bytes go to the CUDA path (through the C ABI) and to the oracle.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from bit_nf4_quantized_gb300 import binding
+from bit_nf4_quantized_gb300 import workloads as wl
+from oracle import codebooks as cb
+from oracle import nf4 as onf4
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _to_device(x32: np.ndarray, dtype):
+    t = torch.from_numpy(x32).to(DEV)
+    return t.to(dtype)
+
+
+def _host_values(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy()
+
+
+def _assert_same_quant(q_gpu, q_ref):
+    assert np.array_equal(q_gpu.packed.cpu().numpy(), q_ref["packed"])
+    if q_ref["double_quant"]:
+        assert np.array_equal(q_gpu.absmax.cpu().numpy(), q_ref["absmax"])
+        assert np.array_equal(q_gpu.nested_absmax.cpu().numpy().view(np.uint32),
+                              q_ref["nested"].view(np.uint32))
+        assert q_gpu.offset[0].cpu().numpy().view(np.uint32) == np.float32(q_ref["offset"]).view(np.uint32)
+    else:
+        assert np.array_equal(q_gpu.absmax.cpu().numpy().view(np.uint32), q_ref["absmax"].view(np.uint32))
+
+
+SIZES = [1, 2, 3, 63, 64, 65, 127, 129, 1000, 16383, 16384, 16385, 64 * 256 * 3 + 17, 2 ** 20 + 7 * 16384]
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dq", [True, False])
+def test_quantize_bit_exact(lib, n, dtype, dq):
+    x = wl.normal(n, 0.02, 5, n % 1000)
+    if n > 200:
+        x = wl.with_outliers(x, 0.001, 50.0, 5, 500)
+    xd = _to_device(x, dtype)
+    q = binding.nf4_quantize(xd, double_quant=dq)
+    ref = onf4.quantize(_host_values(xd), double_quant=dq)
+    _assert_same_quant(q, ref)
+    assert binding.device_status() == binding.NF4_OK
+
+
+def test_quantize_special_blocks(lib):
+    nf4 = cb.nf4_codebook()
+    x = np.zeros(64 * 300 + 5, np.float32)
+    # block 0: exact code multiples and exact ties at absmax 1
+    x[0] = 1.0
+    x[1:17] = nf4
+    mids = [(nf4[j] + nf4[j + 1]) / np.float32(2) for j in range(15)]
+    x[17:32] = np.array(mids, np.float32)
+    # block 1 stays all zero; block 2 has -0.0 and one tiny subnormal
+    x[128:192] = -0.0
+    x[150] = 1e-44
+    # block 3: the maximum is negative
+    x[192:256] = np.linspace(-3, 1, 64, dtype=np.float32)
+    for dq in (True, False):
+        xd = torch.from_numpy(x).to(DEV)
+        q = binding.nf4_quantize(xd, double_quant=dq)
+        _assert_same_quant(q, onf4.quantize(x, double_quant=dq))
+
+
+def test_quantize_is_deterministic(lib):
+    x = _to_device(wl.normal(64 * 256 * 40 + 3, 0.02, 5, 900), torch.float32)
+    a = binding.nf4_quantize(x)
+    b = binding.nf4_quantize(x)
+    for f in ("packed", "absmax", "nested_absmax"):
+        assert torch.equal(getattr(a, f), getattr(b, f))
+    assert torch.equal(a.offset[:1], b.offset[:1])
+
+
+def test_nonfinite_sets_device_status(lib):
+    binding.device_status(clear=True)
+    for bad in (float("nan"), float("inf")):
+        x = torch.zeros(5000, device=DEV)
+        x[1234] = bad
+        binding.nf4_quantize(x)
+        assert binding.device_status(clear=True) == binding.NF4_ERR_NONFINITE
+    binding.nf4_quantize(torch.ones(5000, device=DEV))
+    assert binding.device_status(clear=True) == binding.NF4_OK
+
+
+def _upload(ref, shape):
+    """The oracle's quantized tensor copied to the device (so dequant is tested on its own)."""
+    q = binding.Nf4Tensor.empty(shape, ref["double_quant"], DEV)
+    q.packed.copy_(torch.from_numpy(ref["packed"]))
+    q.absmax.copy_(torch.from_numpy(ref["absmax"]))
+    if ref["double_quant"]:
+        q.nested_absmax.copy_(torch.from_numpy(ref["nested"]))
+        q.offset[0] = float(ref["offset"])
+    return q
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 65, 1000, 16385, 64 * 256 * 5 + 33, 2 ** 20 + 7 * 16384])
+@pytest.mark.parametrize("dq", [True, False])
+def test_dequantize_bit_exact(lib, n, dq):
+    x = wl.student_t(n, 5, 0.02, 5, 7)
+    ref = onf4.quantize(x, double_quant=dq)
+    q = _upload(ref, (n,))
+    for dtype, odt in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+        y = binding.nf4_dequantize(q, dtype)
+        want = onf4.dequantize(ref, odt)
+        got = y.float().cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def _sampled_groups_check(x_host: np.ndarray, q, groups):
+    """Check selected 16384-element groups of a large quantization against the oracle's steps."""
+    a = onf4.block_absmax(x_host)
+    offset = onf4.absmax_offset(a)
+    assert q.offset[0].cpu().numpy().view(np.uint32) == np.float32(offset).view(np.uint32)
+    packed = q.packed.cpu().numpy()
+    codes = q.absmax.cpu().numpy()
+    nested = q.nested_absmax.cpu().numpy()
+    dyn8 = cb.dynamic8_codebook()
+    nb = a.size
+    for g in groups:
+        e0, e1 = g * 16384, min((g + 1) * 16384, x_host.size)
+        part = onf4.quantize(x_host[e0:e1], double_quant=False)
+        assert np.array_equal(packed[e0 // 2:(e1 + 1) // 2], part["packed"])
+        b0, b1 = g * 256, min((g + 1) * 256, nb)
+        c = (a[b0:b1] - offset).astype(np.float32)
+        na = np.float32(np.max(np.abs(c)))
+        assert nested[g] == na
+        want = onf4.nearest_code(c / na, dyn8) if na > 0 else np.full(c.size, 127, np.uint8)
+        assert np.array_equal(codes[b0:b1], want)
+
+
+@pytest.mark.parametrize("log2n", [24, 28])
+def test_quantize_large_sampled(lib, log2n):
+    n = 2 ** log2n
+    x = wl.device_normal((n,), 0.02, wl.seed_for(5, log2n), DEV, torch.float32)
+    q = binding.nf4_quantize(x)
+    x_host = x.cpu().numpy()
+    ng = n // 16384
+    groups = sorted(set([0, 1, ng // 2, ng - 1] + list(np.random.default_rng(log2n).integers(0, ng, 6))))
+    _sampled_groups_check(x_host, q, groups)
+    # dequantized values of the sampled groups, bf16 output
+    y = binding.nf4_dequantize(q, torch.bfloat16)
+    ys = y.float().cpu().numpy()
+    ref_full = dict(numel=n, double_quant=True, packed=q.packed.cpu().numpy(), absmax=q.absmax.cpu().numpy(),
+                    nested=q.nested_absmax.cpu().numpy(), offset=q.offset[0].cpu().numpy())
+    for g in groups[:4]:
+        sub = dict(ref_full)
+        e0, e1 = g * 16384, (g + 1) * 16384
+        sub.update(numel=e1 - e0, packed=ref_full["packed"][e0 // 2:e1 // 2],
+                   absmax=ref_full["absmax"][g * 256:(g + 1) * 256], nested=ref_full["nested"][g:g + 1])
+        want = onf4.dequantize(sub, "bf16")
+        assert np.array_equal(ys[e0:e1].view(np.uint32), want.view(np.uint32))

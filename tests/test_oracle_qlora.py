@@ -75,6 +75,13 @@ def test_backward_is_the_gradient_of_forward():
         assert abs(fd - float(np.sum(grad * d))) <= 1e-6 * max(1.0, abs(fd))
 
 
+def test_adapter_backward_matches_backward():
+    x, W, A, B, dy = _tiny(12)
+    dX, dA, dB, G = qlora.backward(dy, x, W, A, B, 1.3, compute="f64")
+    dA2, dB2, G2 = qlora.adapter_backward(dy, x, A, B, 1.3, compute="f64")
+    assert np.array_equal(dA, dA2) and np.array_equal(dB, dB2) and np.array_equal(G, G2)
+
+
 def test_closed_forms():
     x, W, A, B, dy = _tiny(6)
     s = 2.0
