@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the NF4 double-quant QLoRA hot path on one Llama-3-8B-shaped layer.
+
+One step = the whole hot path over the layer's 7 projections (q, k, v, o, gate,
+up, down; 4096 tokens, rank 16, alpha 16, bf16 compute): for each projection
+  nf4_quantize (bf16 master -> NF4 + double quant), nf4_dequantize (-> bf16),
+  qlora_linear_fwd (T, y) and qlora_linear_bwd (G, dX, dA, dB),
+all through the C ABI of libqlora_nf4.so.  value = fwd+bwd TFLOP/s over the whole
+step (4MNK + 6Mr(N+K) per projection, no dW), so the quantize and dequantize time
+counts against it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torchrun; each rank runs the same workload on its own GPU
+(independent replicas, weak scaling, no data-path collective); a gloo barrier and
+a max over ranks bracket the timed region.
+
+--impl reference times the CPU oracle (oracle/) on the host cores on a bounded
+sample of the same workload; rank 0 alone runs it.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_NAME = "Llama-3-8B-shaped layer: q/o 4096x4096, k/v 1024x4096, gate/up 14336x4096, " \
+                "down 4096x14336; NF4 double quant; QLoRA fwd+bwd on all 7, M=4096 (2x2048), r=16, alpha=16"
+METRIC = "QLoRA NF4 linear fwd+bwd TFLOP/s and dequant weight GB/s vs roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---- distributed bookkeeping (host-side only) -------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- clock sampling ---------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [r for t, r in self.rows if t0 <= t <= t1 and len(r) >= 9]
+        if not rows:
+            rows = [r for _, r in self.rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- the workload -------------------------------------------------------------------
+
+def linear_flops(M, N, K, r):
+    """Algorithmic flops of one forward + backward: 4MNK (y and dX) + 6Mr(N+K) (T, s T B^T, G,
+    s G A, dA, dB); the frozen base has no dW."""
+    return 4 * M * N * K + 6 * M * r * (N + K)
+
+
+def layer_flops(shapes, M, r):
+    return sum(linear_flops(M, N, K, r) for _, N, K in shapes)
+
+
+class Layer:
+    """Device buffers for one step over the 7 projections (allocated once)."""
+
+    def __init__(self, dev, seed_base=0):
+        import torch
+        from bit_nf4_quantized_gb300 import binding
+        from bit_nf4_quantized_gb300 import workloads as wl
+        c = wl.W3
+        self.M, self.r, self.alpha = c["M"], c["r"], c["alpha"]
+        self.shapes = c["shapes"]
+        self.dev = dev
+        self.proj = []
+        lib = binding.load()
+        max_w = max(N * K for _, N, K in self.shapes)
+        self.deq = torch.empty(max_w, dtype=torch.bfloat16, device=dev)
+        ws_q = max(lib.nf4_quantize_workspace_bytes(N * K, 1) for _, N, K in self.shapes)
+        ws_f = max(lib.qlora_fwd_workspace_bytes(self.M, N, K, self.r, 1) for _, N, K in self.shapes)
+        ws_b = max(lib.qlora_bwd_workspace_bytes(self.M, N, K, self.r, 1) for _, N, K in self.shapes)
+        self.ws_q = torch.empty(max(ws_q, 16), dtype=torch.uint8, device=dev)
+        self.ws_f = torch.empty(max(ws_f, 16), dtype=torch.uint8, device=dev)
+        self.ws_b = torch.empty(max(ws_b, 16), dtype=torch.uint8, device=dev)
+        for i, (name, N, K) in enumerate(self.shapes):
+            seed = wl.seed_for(3, 100 * i) + seed_base
+            p = dict(name=name, N=N, K=K)
+            p["w"] = wl.device_student_t((N, K), c["t_df"], c["w_scale"], seed, dev, torch.bfloat16)
+            p["x"] = wl.device_normal((self.M, K), 1.0, seed + 1, dev, torch.bfloat16)
+            p["dy"] = wl.device_normal((self.M, N), 1.0, seed + 2, dev, torch.bfloat16)
+            p["A"] = wl.device_normal((self.r, K), 1.0 / self.r, seed + 3, dev, torch.float32)
+            p["B"] = wl.device_normal((N, self.r), 0.01, seed + 4, dev, torch.float32)
+            p["q"] = binding.Nf4Tensor.empty((N, K), True, dev)
+            p["y"] = torch.empty((self.M, N), dtype=torch.bfloat16, device=dev)
+            p["T"] = torch.empty((self.M, self.r), dtype=torch.float32, device=dev)
+            p["dx"] = torch.empty((self.M, K), dtype=torch.bfloat16, device=dev)
+            p["dA"] = torch.empty((self.r, K), dtype=torch.float32, device=dev)
+            p["dB"] = torch.empty((N, self.r), dtype=torch.float32, device=dev)
+            self.proj.append(p)
+
+    def step(self):
+        from bit_nf4_quantized_gb300 import binding as b
+        for p in self.proj:
+            b.nf4_quantize(p["w"], True, out=p["q"], workspace=self.ws_q)
+            b.nf4_dequantize(p["q"], out=self.deq[:p["N"] * p["K"]].view(p["N"], p["K"]))
+            b.qlora_linear_fwd(p["x"], p["q"], p["A"], p["B"], self.alpha, y=p["y"], T=p["T"],
+                               workspace=self.ws_f)
+            b.qlora_linear_bwd(p["dy"], p["x"], p["T"], p["q"], p["A"], p["B"], self.alpha, dx=p["dx"],
+                               dA=p["dA"], dB=p["dB"], workspace=self.ws_b)
+
+    def input_tensors(self):
+        return [p[k] for p in self.proj for k in ("w", "x", "dy")]
+
+    def result_tensors(self):
+        return [p[k] for p in self.proj for k in ("dA", "dB")]
+
+
+def time_steps(fn, steps, stream):
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+# ---- CPU oracle sample (cpu_baseline and the reference arm) --------------------------
+
+def oracle_sample():
+    """One bounded sample of the same step on the CPU oracle: the k_proj weight rows
+    0..255 (256 x 4096 slice) quantized, dequantized, and QLoRA fwd+bwd for 512 tokens."""
+    import numpy as np
+    from bit_nf4_quantized_gb300 import workloads as wl
+    from oracle import nf4 as onf4
+    from oracle import qlora
+    c = wl.W3
+    N, K, M, r = 256, 4096, 512, c["r"]
+    w = wl.student_t((N, K), c["t_df"], c["w_scale"], 3, 777)
+    x = wl.normal((M, K), 1.0, 3, 778)
+    dy = wl.normal((M, N), 1.0, 3, 779)
+    A, B = wl.adapters(N, K, r, 3, 780)
+    s = qlora.lora_scale(c["alpha"], r)
+
+    def run():
+        q = onf4.quantize(w, double_quant=True)
+        wd = onf4.dequantize(q, "f32").reshape(N, K)
+        _ = onf4.dequantize(q, "bf16")
+        qlora.forward(x, wd, A, B, s, "bf16")
+        qlora.backward(dy, x, wd, A, B, s, "bf16")
+    return run, linear_flops(M, N, K, r), "k_proj rows 0..255 (256x4096 slice): quantize, dequantize " \
+        "(f32 and bf16), fwd+bwd at M=512, r=16; float64 numpy oracle"
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s=12.0):
+    run, flops, sample = oracle_sample()
+    run()  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s:
+        run()
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{sample}; {n} repetitions, {dt:.2f} s each"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    run, flops, sample = oracle_sample()
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    total = time.perf_counter() - t0
+    v = flops * args.steps / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD_NAME, "reference_sample": sample},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- main ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    # the oracle sample runs before the first CUDA call in this process
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    import torch
+    from bit_nf4_quantized_gb300 import binding
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    layer = Layer(dev)
+    pk, pk_src = peaks()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    for _ in range(max(args.warmup, 3)):
+        layer.step()
+    torch.cuda.synchronize(dev)
+    if binding.device_status() != binding.NF4_OK:
+        raise RuntimeError("device status word set during warm-up")
+
+    binding.timing_enable(True)
+    for k in range(5):
+        binding.timing_read(k, reset=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = binding.launch_count()
+    t0 = time.time()
+    ms = time_steps(layer.step, args.steps, stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier(world)
+    launches = binding.launch_count() - launches0
+    binding.timing_enable(False)
+    sampler.stop()
+    kinds = {name: binding.timing_read(k, reset=True) for k, name in
+             enumerate(("quantize", "dequantize", "fwd_gemm", "dx_gemm", "adapter"))}
+    ms_max = max_over_ranks(ms, world)
+
+    M, r = layer.M, layer.r
+    flops = layer_flops(layer.shapes, M, r)
+    value = world * flops * args.steps / (ms_max / 1e3) / 1e12
+    # dominant kernel: the base contraction kind with the larger share of time
+    fwd_f = sum(2 * M * N * K + 2 * M * N * r for _, N, K in layer.shapes)
+    dx_f = sum(2 * M * N * K + 2 * M * K * r for _, N, K in layer.shapes)
+    dom = "fwd_gemm" if kinds["fwd_gemm"][0] >= kinds["dx_gemm"][0] else "dx_gemm"
+    dom_ms, dom_n = kinds[dom]
+    dom_flops = (fwd_f if dom == "fwd_gemm" else dx_f) * args.steps
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0
+    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    nel = sum(N * K for _, N, K in layer.shapes)
+    deq_bytes = nel * 2 + sum(binding.load().nf4_packed_bytes(N * K, 1) for _, N, K in layer.shapes)
+    deq_ms, deq_n = kinds["dequantize"]
+    deq_gbs = deq_bytes * args.steps / (deq_ms / 1e3) / 1e9 if deq_ms > 0 else 0.0
+    q_ms, _ = kinds["quantize"]
+    q_bytes = nel * 2 + sum(binding.load().nf4_packed_bytes(N * K, 1) + 4 for _, N, K in layer.shapes)
+    q_gbs = q_bytes * args.steps / (q_ms / 1e3) / 1e9 if q_ms > 0 else 0.0
+    hbm = float(pk["hbm_gbs"])
+    clocks = sampler.summary(t0, t1)
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in layer.input_tensors()]
+        dev_in = layer.input_tensors()
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in layer.result_tensors()]
+        dev_out = layer.result_tensors()
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            layer.step()
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e_steps = max(3, args.steps // 3)
+        e_ms = max_over_ranks(time_steps(e2e_step, e_steps, stream), world)
+        barrier(world)
+        e2e = {"value": world * flops * e_steps / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "tokens": M, "rank": r, "alpha": layer.alpha,
+                       "targets": [n for n, _, _ in layer.shapes], "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: each step touches ~1.5 GB of distinct buffers",
+                       "step": "per projection: nf4_quantize, nf4_dequantize (bf16), qlora_linear_fwd, "
+                               "qlora_linear_bwd"},
+            "gpu_launches": launches,
+            "phases_ms_per_step": {k: v[0] / args.steps for k, v in kinds.items()},
+            "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": None,
+                         "peak_source": f"{pk_src} bf16_tflops_sustained", "launches": dom_n},
+            "dequant": {"GB/s": deq_gbs, "frac": deq_gbs / hbm, "peak_gbs": hbm,
+                        "bytes_per_step": deq_bytes, "launches": deq_n},
+            "quantize": {"GB/s": q_gbs, "frac": q_gbs / hbm, "bytes_per_step": q_bytes},
+            "clocks": clocks,
+            "e2e": e2e,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
                                    vp, vp, vp, vp, sz, vp]),
         "qlora_last_device_status": (i32, [vp, i32]),
         "nf4_kernel_launch_count": (i64, []),
+        "nf4_timing_enable": (None, [i32]),
+        "nf4_timing_read": (i32, [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -248,3 +250,16 @@ def device_status(clear: bool = True, stream=None) -> int:
 
 def launch_count() -> int:
     return int(load().nf4_kernel_launch_count())
+
+
+def timing_enable(on: bool = True):
+    """Turn the library's per-kernel event timing on or off."""
+    load().nf4_timing_enable(int(on))
+
+
+def timing_read(kind: int, reset: bool = True):
+    """(total milliseconds, launches) of one timed kernel kind since the last reset."""
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(load().nf4_timing_read(kind, ctypes.byref(ms), ctypes.byref(n), int(reset)), "nf4_timing_read")
+    return ms.value, n.value

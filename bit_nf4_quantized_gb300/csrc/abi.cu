@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "linear_tc.cuh"
@@ -105,6 +106,61 @@ nf4_status device_status_ptr(int** out) {
 }
 
 }  // namespace
+
+// ---- optional kernel timing ------------------------------------------------------
+namespace {
+
+struct TimingState {
+  std::mutex mu;
+  std::atomic<bool> enabled{false};
+  std::vector<cudaEvent_t> pool;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[NF4_TIME_KINDS];
+  double total_ms[NF4_TIME_KINDS] = {};
+  int64_t count[NF4_TIME_KINDS] = {};
+};
+
+TimingState& timing() {
+  static TimingState t;
+  return t;
+}
+
+cudaEvent_t take_event(TimingState& t) {
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (!t.pool.empty()) {
+    cudaEvent_t e = t.pool.back();
+    t.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+KernelTimer::KernelTimer(int kind, cudaStream_t st) : kind_(kind), st_(st) {
+  TimingState& t = timing();
+  if (!t.enabled.load(std::memory_order_relaxed)) return;
+  start_ = take_event(t);
+  if (start_ != nullptr && cudaEventRecord(start_, st_) != cudaSuccess) {
+    std::lock_guard<std::mutex> lock(t.mu);
+    t.pool.push_back(start_);
+    start_ = nullptr;
+  }
+}
+
+KernelTimer::~KernelTimer() {
+  if (start_ == nullptr) return;
+  TimingState& t = timing();
+  cudaEvent_t stop = take_event(t);
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (stop == nullptr || cudaEventRecord(stop, st_) != cudaSuccess) {
+    t.pool.push_back(start_);
+    if (stop != nullptr) t.pool.push_back(stop);
+    return;
+  }
+  t.pending[kind_].emplace_back(start_, stop);
+}
 
 const DecodeTables& decode_tables() { return tables().dec; }
 const EncodeTables& encode_tables() { return tables().enc; }
@@ -232,6 +288,7 @@ nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel, const n
   if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
   int* status = nullptr;
   if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+  KernelTimer timer(NF4_TIME_QUANTIZE, static_cast<cudaStream_t>(stream));
   return from_cuda(launch_quantize(x, x_dtype, numel, *out, ws, status,
                                    static_cast<cudaStream_t>(stream)));
 }
@@ -242,6 +299,7 @@ nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, voi
   nf4_status st = check_tensor(w, w->numel);
   if (st != NF4_OK) return st;
   if (!aligned16(y)) return NF4_ERR_ALIGN;
+  KernelTimer timer(NF4_TIME_DEQUANTIZE, static_cast<cudaStream_t>(stream));
   return from_cuda(launch_dequantize(view_of(w), y, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
@@ -337,5 +395,34 @@ nf4_status qlora_last_device_status(void* stream, int32_t clear) {
 }
 
 int64_t nf4_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void nf4_timing_enable(int32_t on) { timing().enabled.store(on != 0); }
+
+nf4_status nf4_timing_read(int32_t kind, double* total_ms, int64_t* launches, int32_t reset) {
+  if (kind < 0 || kind >= NF4_TIME_KINDS) return NF4_ERR_ARG;
+  TimingState& t = timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  nf4_status st = NF4_OK;
+  for (auto& pr : t.pending[kind]) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(pr.second) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, pr.first, pr.second) != cudaSuccess) {
+      st = NF4_ERR_CUDA;
+    } else {
+      t.total_ms[kind] += ms;
+      t.count[kind] += 1;
+    }
+    t.pool.push_back(pr.first);
+    t.pool.push_back(pr.second);
+  }
+  t.pending[kind].clear();
+  if (total_ms) *total_ms = t.total_ms[kind];
+  if (launches) *launches = t.count[kind];
+  if (reset) {
+    t.total_ms[kind] = 0.0;
+    t.count[kind] = 0;
+  }
+  return st;
+}
 
 }  // extern "C"

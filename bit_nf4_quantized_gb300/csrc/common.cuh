@@ -39,6 +39,21 @@ const EncodeTables& encode_tables();
 // Launch accounting (for the launch count reported by the ABI).
 void note_launch(int n = 1);
 
+// Optional event timing of selected kernels (nf4_timing_enable): records a CUDA
+// event pair on the launching stream around the scope when timing is on.
+class KernelTimer {
+ public:
+  KernelTimer(int kind, cudaStream_t st);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  int kind_;
+  cudaStream_t st_;
+  cudaEvent_t start_ = nullptr;
+};
+
 // Per-call view of an nf4_tensor for device code.
 struct Nf4View {
   const uint8_t* packed;

@@ -242,6 +242,7 @@ unsigned blocks_for(int64_t n, int per) { return static_cast<unsigned>((n + per 
 
 cudaError_t launch_lora_down(const LinearArgs& a, nf4_dtype cd, const void* x, const float* A,
                              float* T, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
   const unsigned g = blocks_for(a.M, 8);
   if (cd == NF4_F32)
     lora_down_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), A, T, a.M, a.K, a.r);
@@ -254,6 +255,7 @@ cudaError_t launch_lora_down(const LinearArgs& a, nf4_dtype cd, const void* x, c
 
 cudaError_t launch_lora_g(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* B,
                           float* G, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
   const unsigned g = blocks_for(a.M, 8);
   if (cd == NF4_F32)
     lora_g_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(dy), B, G, a.M, a.N, a.r);
@@ -266,6 +268,7 @@ cudaError_t launch_lora_g(const LinearArgs& a, nf4_dtype cd, const void* dy, con
 
 cudaError_t launch_lora_dA(const LinearArgs& a, nf4_dtype cd, const float* G, const void* x,
                            float* dA, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
   const unsigned g = blocks_for(static_cast<int64_t>(a.r) * a.K, 256);
   if (cd == NF4_F32)
     lora_dA_kernel<float><<<g, 256, 0, st>>>(G, static_cast<const float*>(x), dA, a.M, a.K, a.r, a.s);
@@ -278,6 +281,7 @@ cudaError_t launch_lora_dA(const LinearArgs& a, nf4_dtype cd, const float* G, co
 
 cudaError_t launch_lora_dB(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* T,
                            float* dB, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
   const unsigned g = blocks_for(static_cast<int64_t>(a.r) * a.N, 256);
   if (cd == NF4_F32)
     lora_dB_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(dy), T, dB, a.M, a.N, a.r, a.s);
@@ -290,6 +294,7 @@ cudaError_t launch_lora_dB(const LinearArgs& a, nf4_dtype cd, const void* dy, co
 
 cudaError_t launch_fwd_simt(const LinearArgs& a, nf4_dtype cd, const void* x, const float* T,
                             const float* B, void* y, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_FWD_GEMM, st);
   const dim3 grid(blocks_for(a.N, kTile), blocks_for(a.M, kTile));
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   const DecodeTables& dt = decode_tables();
@@ -306,6 +311,7 @@ cudaError_t launch_fwd_simt(const LinearArgs& a, nf4_dtype cd, const void* x, co
 
 cudaError_t launch_dx_simt(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* G,
                            const float* A, void* dx, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_DX_GEMM, st);
   const dim3 grid(blocks_for(a.K, kTile), blocks_for(a.M, kTile));
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   const DecodeTables& dt = decode_tables();

@@ -161,6 +161,24 @@ nf4_status qlora_last_device_status(void* stream, int32_t clear);
 /* Number of kernels this library has launched in this process (all devices). */
 int64_t nf4_kernel_launch_count(void);
 
+/* Optional timing of the library's kernels, for benchmarks.  While enabled, each
+ * timed kernel (or kernel sequence, for nf4_quantize) is bracketed by a pair of
+ * CUDA events recorded on the stream it is launched on.  nf4_timing_read()
+ * waits for the recorded pairs of one kind, returns the summed milliseconds and
+ * the number of launches, and with reset != 0 clears that kind.  No device memory
+ * is allocated; events are created once and reused. */
+typedef enum {
+  NF4_TIME_QUANTIZE = 0,    /* the three quantize kernels of one nf4_quantize call */
+  NF4_TIME_DEQUANTIZE = 1,  /* the decode kernel */
+  NF4_TIME_FWD_GEMM = 2,    /* base contraction of the forward (y) */
+  NF4_TIME_DX_GEMM = 3,     /* base contraction of the input gradient (dX) */
+  NF4_TIME_ADAPTER = 4,     /* adapter-side kernels (T, G, dA, dB, operand staging) */
+  NF4_TIME_KINDS = 5
+} nf4_timed_kernel;
+
+void nf4_timing_enable(int32_t on);
+nf4_status nf4_timing_read(int32_t kind, double* total_ms, int64_t* launches, int32_t reset);
+
 #ifdef __cplusplus
 }
 #endif
