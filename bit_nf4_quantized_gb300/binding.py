@@ -17,6 +17,8 @@ from . import build as _build
 
 NF4_OK, NF4_ERR_ARG, NF4_ERR_SHAPE, NF4_ERR_ALIGN, NF4_ERR_DTYPE = 0, 1, 2, 3, 4
 NF4_ERR_NONFINITE, NF4_ERR_CORRUPT, NF4_ERR_CUDA, NF4_ERR_TIMEOUT, NF4_ERR_WORKSPACE = 5, 6, 7, 8, 9
+NF4_ERR_TOO_LARGE = 10
+NOALLOC_MAX_NUMEL = 1 << 26
 NF4_F32, NF4_BF16 = 0, 1
 SCALE_LORA, SCALE_RSLORA = 0, 1
 
@@ -69,6 +71,7 @@ def load() -> ctypes.CDLL:
         "nf4_quantize_workspace_bytes": (sz, [i64, i32]),
         "nf4_quantize": (i32, [vp, i32, i64, tp, vp, sz, vp]),
         "nf4_dequantize": (i32, [tp, vp, i32, vp]),
+        "nf4_quantize_noalloc": (i32, [vp, i32, i64, tp, vp]),
         "qlora_fwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "qlora_bwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "qlora_linear_fwd": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, tp, vp, vp, vp, vp, vp, sz, vp]),
@@ -185,6 +188,21 @@ def nf4_quantize(x: torch.Tensor, double_quant: bool = True, out: Nf4Tensor = No
     cs = out.c_struct()
     _check(lib.nf4_quantize(_ptr(x), _dtype_code(x.dtype), x.numel(), ctypes.byref(cs), _ptr(ws),
                             ws.numel(), _stream(stream)), "nf4_quantize")
+    return out
+
+
+def nf4_quantize_noalloc(x: torch.Tensor, out: Nf4Tensor, stream=None) -> Nf4Tensor:
+    """nf4_quantize with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot allocate device memory; ``out`` must be allocated by the
+    caller.  Calls share one scratch array per device, so they must not overlap on
+    the GPU.  numel above NOALLOC_MAX_NUMEL raises Nf4Error(NF4_ERR_TOO_LARGE).
+    """
+    lib = load()
+    x = x.contiguous()
+    cs = out.c_struct()
+    _check(lib.nf4_quantize_noalloc(_ptr(x), _dtype_code(x.dtype), x.numel(), ctypes.byref(cs),
+                                    _stream(stream)), "nf4_quantize_noalloc")
     return out
 
 

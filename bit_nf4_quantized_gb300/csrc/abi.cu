@@ -249,6 +249,7 @@ const char* nf4_status_str(nf4_status s) {
     case NF4_ERR_CUDA: return "CUDA runtime error";
     case NF4_ERR_TIMEOUT: return "device-side wait timed out";
     case NF4_ERR_WORKSPACE: return "workspace missing or too small";
+    case NF4_ERR_TOO_LARGE: return "numel above the fixed scratch limit of nf4_quantize_noalloc";
   }
   return "unknown status";
 }

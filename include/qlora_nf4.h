@@ -55,7 +55,8 @@ typedef enum {
   NF4_ERR_CORRUPT = 6,    /* descriptor inconsistent with its numel / double_quant */
   NF4_ERR_CUDA = 7,       /* a CUDA runtime call failed (launch, no device, ...) */
   NF4_ERR_TIMEOUT = 8,    /* a device-side bounded wait gave up (device status) */
-  NF4_ERR_WORKSPACE = 9   /* workspace null or smaller than the size query returns */
+  NF4_ERR_WORKSPACE = 9,  /* workspace null or smaller than the size query returns */
+  NF4_ERR_TOO_LARGE = 10  /* numel above NF4_QUANTIZE_NOALLOC_MAX_NUMEL (nf4_quantize_noalloc) */
 } nf4_status;
 
 typedef enum { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
@@ -111,6 +112,24 @@ size_t nf4_quantize_workspace_bytes(int64_t numel, int32_t double_quant);
  * bytes are then unspecified. */
 nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel,
                         const nf4_tensor* out, void* ws, size_t ws_bytes, void* stream);
+
+/* nf4_quantize without a workspace, for callers that cannot allocate device
+ * memory: code running inside a host engine or framework that owns all device
+ * memory and hands it only input and output buffers, or a latency-critical loop
+ * where cudaMalloc/cudaFree (and the device synchronization cudaFree implies) are
+ * not allowed.  The pages have no counterpart to this entry point; it computes
+ * exactly what nf4_quantize computes, with the same kernels.
+ * Its scratch is a fixed array of NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES in the
+ * library's own device memory, held by every GPU that loads the library until the
+ * process exits.  numel above NF4_QUANTIZE_NOALLOC_MAX_NUMEL returns
+ * NF4_ERR_TOO_LARGE before any device work.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  All calls share the array: calls that
+ * overlap on the GPU race on it, so serialize them.  No call allocates memory. */
+#define NF4_QUANTIZE_NOALLOC_MAX_NUMEL (67108864LL)        /* 2^26 elements */
+#define NF4_QUANTIZE_NOALLOC_SCRATCH_BYTES (4227072u)      /* 4 MiB + 32 KiB */
+nf4_status nf4_quantize_noalloc(const void* x, nf4_dtype x_dtype, int64_t numel,
+                                const nf4_tensor* out, void* stream);
 
 /* Decode *w into y (device, out_dtype NF4_F32 or NF4_BF16, w->numel elements).
  * fp32 output is exact nf4[q]*a'; bf16 output is that value rounded to nearest
