@@ -21,14 +21,6 @@ namespace qnf4 {
 // ---- constant tables ---------------------------------------------------------------
 namespace {
 
-// The 16 NF4 values as published with QLoRA (Dettmers et al. 2023, appendix
-// "NormalFloat 4-bit data type"), ascending.
-constexpr float kNf4Values[16] = {
-    -1.0f, -0.6961928009986877f, -0.5250730514526367f, -0.39491748809814453f,
-    -0.28444138169288635f, -0.18477343022823334f, -0.09105003625154495f, 0.0f,
-    0.07958029955625534f, 0.16093020141124725f, 0.24611230194568634f, 0.33791524171829224f,
-    0.44070982933044434f, 0.5626170039176941f, 0.7229568362236023f, 1.0f};
-
 // Signed dynamic tree quantization (Dettmers et al. 2022, "8-bit Optimizers via
 // Block-wise Quantization"): after the sign, E zero bits give the decade 10^-E, a
 // 1 bit ends them and F = 6 - E bits pick one of 2^F equal bins of [0.1, 1]; the
@@ -71,7 +63,7 @@ struct Tables {
   DecodeTables dec;
   EncodeTables enc;
   Tables() {
-    std::memcpy(dec.nf4, kNf4Values, sizeof(kNf4Values));
+    for (int i = 0; i < 16; ++i) dec.nf4[i] = nf4_value(i);
     build_dyn8(dec.dyn8);
     build_thresholds(dec.nf4, 16, enc.nf4_thr);
     build_thresholds(dec.dyn8, 256, enc.dyn8_thr);

@@ -20,6 +20,30 @@ constexpr int kGroupElems = kBlock * kNested;
 constexpr int kNf4ZeroCode = 7;       // nf4[7] == 0.0
 constexpr int kDyn8ZeroCode = 127;    // dyn8[127] == 0.0
 
+// The 16 NF4 values as published with QLoRA (Dettmers et al. 2023, appendix
+// "NormalFloat 4-bit data type"), ascending.  A switch so that device code with a
+// compile-time index folds it to an immediate.
+__host__ __device__ constexpr float nf4_value(int i) {
+  switch (i) {
+    case 0: return -1.0f;
+    case 1: return -0.6961928009986877f;
+    case 2: return -0.5250730514526367f;
+    case 3: return -0.39491748809814453f;
+    case 4: return -0.28444138169288635f;
+    case 5: return -0.18477343022823334f;
+    case 6: return -0.09105003625154495f;
+    case 7: return 0.0f;
+    case 8: return 0.07958029955625534f;
+    case 9: return 0.16093020141124725f;
+    case 10: return 0.24611230194568634f;
+    case 11: return 0.33791524171829224f;
+    case 12: return 0.44070982933044434f;
+    case 13: return 0.5626170039176941f;
+    case 14: return 0.7229568362236023f;
+    default: return 1.0f;
+  }
+}
+
 // Decode tables: the 16 NF4 values and the 256 dynamic8 values, ascending.
 struct DecodeTables {
   float nf4[16];
