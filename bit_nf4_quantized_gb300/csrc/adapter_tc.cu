@@ -1,0 +1,361 @@
+// Adapter-side contractions of the bf16 QLoRA linear on tcgen05:
+//   T = x A^T,  G = dY B,  dB = s dY^T T,  dA = s G^T x
+// ("Native model adaptation and NF4", "Mixed precision keeps stable state in FP32":
+// adapter contractions accumulate in FP32; "Packed NF4 ...": no base-weight gradient).
+//
+// Each is a skinny product Out[rows, r] = X[rows, red] . Q[red, r] with a large bf16
+// activation X (x or dY, read once, HBM-bound) and a small bf16 Q (the rank-r side).
+// Kernel adapter_tc: one 128-row tile of Out per CTA and one slice of the reduction;
+// X arrives by TMA as the MMA's A operand (K-major when the reduction runs along the
+// activation's rows, MN-major when it runs down its columns), Q as the B operand
+// (K-major, N = r rounded up to 16); the fp32 accumulator lives in TMEM.  Slices
+// write partial sums that a second kernel adds in a fixed order (deterministic,
+// no atomics) and scales.
+#include "linear_tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace qnf4 {
+namespace {
+
+using namespace tc;
+
+constexpr int kRowsT = 128;          // MMA M
+constexpr int kBKa = 64;             // reduction per stage
+constexpr int kAThreads = 192;       // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
+constexpr int kATileBytes = kRowsT * kBKa * 2;
+constexpr int kTargetCtas = 320;     // fixed, so workspace sizes do not depend on the device
+constexpr int kMaxSplit = 64;
+
+struct SkinnyParams {
+  int64_t rows;     // rows of Out
+  int tiles;        // ceil(rows / 128)
+  int total_steps;  // ceil(red / 64)
+  int sps;          // steps per slice
+  int a_mn_major;
+  int n_mma;        // r rounded up to 16
+  int r;
+  int stages;
+  uint32_t b_bytes; // n_mma * 128
+  uint32_t stage_bytes;
+  float* partial;   // [nsplit][rows][r]
+  int* status;
+};
+
+__global__ void __launch_bounds__(kAThreads, 1)
+adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q, const SkinnyParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + p.stages * p.stage_bytes);
+  // bars: full[stages], empty[stages], accfull
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * p.stages + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * p.stages + 1) + 1;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(p.n_mma)) tmem_cols <<= 1;
+
+  const int tile = blockIdx.x % p.tiles;
+  const int slice = blockIdx.x / p.tiles;
+  const int k_begin = slice * p.sps;
+  const int k_end = min(p.total_steps, k_begin + p.sps);
+  const int nsteps = k_end - k_begin;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(bar(s), 1);
+      mbar_init(bar(p.stages + s), 1);
+    }
+    mbar_init(bar(2 * p.stages), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int last = -1;
+      for (int i = 0; i < nsteps && ok; ++i) {
+        const int s = i % p.stages;
+        const uint32_t ph = (i / p.stages) & 1u;
+        if (!mbar_wait(bar(p.stages + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        const uint32_t a_dst = base + s * p.stage_bytes;
+        const uint32_t b_dst = a_dst + kATileBytes;
+        const int k0 = (k_begin + i) * kBKa;
+        mbar_expect_tx(bar(s), kATileBytes + p.b_bytes);
+        if (p.a_mn_major) {
+          // activation [red rows, rows cols]: two 64-column boxes of 64 reduction rows
+          tma_load_2d(a_dst, &tm_x, bar(s), tile * kRowsT, k0);
+          tma_load_2d(a_dst + kATileBytes / 2, &tm_x, bar(s), tile * kRowsT + 64, k0);
+        } else {
+          tma_load_2d(a_dst, &tm_x, bar(s), k0, tile * kRowsT);
+        }
+        tma_load_2d(b_dst, &tm_q, bar(s), k0, 0);
+        last = i;
+      }
+      if (!ok) {
+        for (int i = (last - p.stages + 1 > 0 ? last - p.stages + 1 : 0); i <= last; ++i)
+          mbar_drain(bar(i % p.stages), (i / p.stages) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRowsT, p.n_mma, p.a_mn_major ? 1u : 0u);
+      bool ok = true;
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % p.stages;
+        const uint32_t ph = (i / p.stages) & 1u;
+        if (!mbar_wait(bar(s), ph, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_s = base + s * p.stage_bytes;
+        const uint32_t b_s = a_s + kATileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBKa / 16; ++kk) {
+          const uint64_t adesc = p.a_mn_major ? smem_desc(a_s + kk * 2048, 8192, 1024)
+                                              : smem_desc(a_s + kk * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(b_s + kk * 32, 16, 1024);
+          umma_bf16(tmem_base, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(p.stages + s));
+      }
+      if (ok && nsteps > 0) umma_commit(bar(2 * p.stages));
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int64_t row = static_cast<int64_t>(tile) * kRowsT + quarter * 32 + lane;
+    const bool have = nsteps > 0 && __all_sync(0xffffffffu, mbar_wait(bar(2 * p.stages), 0, abort_flag, p.status));
+    if (have) {
+      tc_fence_after();
+      float* dst = p.partial + (static_cast<int64_t>(slice) * p.rows + row) * p.r;
+      for (int c0 = 0; c0 < p.n_mma; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem_base + c0 + (static_cast<uint32_t>(quarter * 32) << 16), v);
+        tmem_ld_wait();
+        if (row < p.rows) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < p.r) dst[c0 + j] = __uint_as_float(v[j]);
+        }
+      }
+    } else if (nsteps == 0 && row < p.rows) {
+      float* dst = p.partial + (static_cast<int64_t>(slice) * p.rows + row) * p.r;
+      for (int j = 0; j < p.r; ++j) dst[j] = 0.0f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(tmem_cols)
+                 : "memory");
+  }
+}
+
+// out = scale * sum over slices (fixed order).  Optional outputs:
+//   f32 [rows][r] (or transposed [r][rows] when f32_t), bf16(scale_b * v) [rows][rp]
+//   zero-padded, bf16(v) transposed [nq][ldt] (entries past rows / r left as staged zeros).
+__global__ void finish_partials(const float* __restrict__ partial, int nsplit, int64_t rows, int r, float scale,
+                                float* __restrict__ f32, int f32_t, __nv_bfloat16* __restrict__ b_rows, int rp,
+                                float scale_b, __nv_bfloat16* __restrict__ b_t, int64_t ldt) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t w = static_cast<int64_t>(rows) * (b_rows ? rp : r);
+  if (i >= w) return;
+  const int width = b_rows ? rp : r;
+  const int64_t row = i / width;
+  const int j = static_cast<int>(i % width);
+  float v = 0.0f;
+  if (j < r) {
+    for (int sp = 0; sp < nsplit; ++sp) v += partial[(static_cast<int64_t>(sp) * rows + row) * r + j];
+    if (f32) {
+      if (f32_t) f32[static_cast<int64_t>(j) * rows + row] = scale * v;
+      else f32[row * r + j] = scale * v;
+    }
+    if (b_t) b_t[static_cast<int64_t>(j) * ldt + row] = __float2bfloat16_rn(v);
+  }
+  if (b_rows) b_rows[row * rp + j] = __float2bfloat16_rn(j < r ? scale_b * v : 0.0f);
+}
+
+// dst[j][c] = bf16(src[c][j]) for j < r, c < cols; zero for j in [r, nq) or c in [cols, ldd).
+__global__ void stage_t_bf16(const float* __restrict__ src, int64_t cols, int r, int nq, int64_t ldd,
+                             __nv_bfloat16* __restrict__ dst) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(nq) * ldd) return;
+  const int j = static_cast<int>(i / ldd);
+  const int64_t c = i % ldd;
+  dst[i] = __float2bfloat16_rn((j < r && c < cols) ? src[c * r + j] : 0.0f);
+}
+
+// dst[j][c] = bf16(src[j][c]) for j < r; zero rows j in [r, nq).
+__global__ void stage_rows_direct_bf16(const float* __restrict__ src, int64_t cols, int r, int nq,
+                                       __nv_bfloat16* __restrict__ dst) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(nq) * cols) return;
+  const int j = static_cast<int>(i / cols);
+  dst[i] = __float2bfloat16_rn(j < r ? src[i] : 0.0f);
+}
+
+int nq_of(int r) { return (r + 15) / 16 * 16; }
+int rp_of(int r) { return (r + 63) / 64 * 64; }
+int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
+size_t al(size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); }
+unsigned blocks(int64_t n) { return static_cast<unsigned>((n + 255) / 256); }
+
+struct Plan {
+  int tiles, total_steps, sps, nsplit;
+};
+
+Plan plan(int64_t rows, int64_t red) {
+  Plan pl;
+  pl.tiles = static_cast<int>((rows + kRowsT - 1) / kRowsT);
+  pl.total_steps = static_cast<int>((red + kBKa - 1) / kBKa);
+  int ns = (kTargetCtas + pl.tiles - 1) / pl.tiles;
+  if (ns > kMaxSplit) ns = kMaxSplit;
+  if (ns > pl.total_steps) ns = pl.total_steps;
+  if (ns < 1) ns = 1;
+  pl.sps = (pl.total_steps + ns - 1) / ns;
+  pl.nsplit = (pl.total_steps + pl.sps - 1) / pl.sps;
+  return pl;
+}
+
+size_t partial_bytes(int64_t rows, int64_t red, int r) {
+  const Plan pl = plan(rows, red);
+  return al(sizeof(float) * static_cast<size_t>(pl.nsplit) * rows * r);
+}
+
+// One skinny pass: partial sums of X . Q into `partial`; returns the slice count.
+cudaError_t run_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
+                     int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
+                     cudaStream_t st) {
+  const Plan pl = plan(rows, red);
+  const int nq = nq_of(r);
+  CUtensorMap tx, tq;
+  bool ok = mn_major ? make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, x_inner, x_outer, 2 * x_inner, 64, 64,
+                                CU_TENSOR_MAP_SWIZZLE_128B)
+                     : make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, x_inner, x_outer, 2 * x_inner, 64, kRowsT,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, q_cols, nq, 2 * q_cols, 64, nq,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  SkinnyParams p{};
+  p.rows = rows;
+  p.tiles = pl.tiles;
+  p.total_steps = pl.total_steps;
+  p.sps = pl.sps;
+  p.a_mn_major = mn_major ? 1 : 0;
+  p.n_mma = nq;
+  p.r = r;
+  p.b_bytes = static_cast<uint32_t>(nq * 128);
+  p.stage_bytes = static_cast<uint32_t>(al(kATileBytes + p.b_bytes));
+  p.stages = nq <= 32 ? 6 : 4;
+  p.partial = partial;
+  p.status = status;
+  const int smem = 1024 + p.stages * static_cast<int>(p.stage_bytes) + 256;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(adapter_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 4 * 49152 + 256);
+  });
+  if (attr != cudaSuccess) return attr;
+  adapter_tc<<<pl.tiles * pl.nsplit, kAThreads, smem, st>>>(tx, tq, p);
+  note_launch();
+  *nsplit = pl.nsplit;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t adapter_fwd_ws_bytes(int64_t M, int64_t, int64_t K, int r) {
+  return al(2 * static_cast<size_t>(nq_of(r)) * K) + partial_bytes(M, K, r);
+}
+
+size_t adapter_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
+  const size_t nq = nq_of(r);
+  size_t part = partial_bytes(M, N, r);
+  const size_t p2 = partial_bytes(N, M, r), p3 = partial_bytes(K, M, r);
+  if (p2 > part) part = p2;
+  if (p3 > part) part = p3;
+  return al(2 * nq * N) + 2 * al(2 * nq * pad8(M)) + part;
+}
+
+cudaError_t adapter_forward(const LinearArgs& a, const void* x, const float* A, float* T, __nv_bfloat16* sTp,
+                            void* ws, int* status, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
+  const int nq = nq_of(a.r);
+  auto* Aq = static_cast<__nv_bfloat16*>(ws);
+  auto* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + al(2 * static_cast<size_t>(nq) * a.K));
+  stage_rows_direct_bf16<<<blocks(static_cast<int64_t>(nq) * a.K), 256, 0, st>>>(A, a.K, a.r, nq, Aq);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int ns = 0;
+  if ((e = run_pass(x, a.K, a.M, false, Aq, a.K, a.r, a.M, a.K, partial, status, &ns, st)) != cudaSuccess) return e;
+  const int rp = rp_of(a.r);
+  finish_partials<<<blocks(a.M * rp), 256, 0, st>>>(partial, ns, a.M, a.r, 1.0f, T, 0, sTp, rp, a.s, nullptr, 0);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t adapter_backward_pre(const LinearArgs& a, const void* dy, const float* T, const float* B, float* G,
+                                 __nv_bfloat16* sGp, float* dB, void* ws, int* status, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
+  const int nq = nq_of(a.r);
+  const int64_t Mp = pad8(a.M);
+  char* w = static_cast<char*>(ws);
+  auto* Bt = reinterpret_cast<__nv_bfloat16*>(w);
+  auto* Tt = reinterpret_cast<__nv_bfloat16*>(w + al(2 * static_cast<size_t>(nq) * a.N));
+  auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + al(2 * static_cast<size_t>(nq) * a.N) + al(2 * nq * Mp));
+  auto* partial = reinterpret_cast<float*>(w + al(2 * static_cast<size_t>(nq) * a.N) + 2 * al(2 * nq * Mp));
+  stage_t_bf16<<<blocks(nq * a.N), 256, 0, st>>>(B, a.N, a.r, nq, a.N, Bt);
+  note_launch();
+  stage_t_bf16<<<blocks(nq * Mp), 256, 0, st>>>(T, a.M, a.r, nq, Mp, Tt);
+  note_launch();
+  // Gt's padding (rows r..nq, columns M..Mp) must read as zero; finish_partials fills the rest
+  stage_t_bf16<<<blocks(nq * Mp), 256, 0, st>>>(T, 0, 0, nq, Mp, Gt);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int ns = 0;
+  const int rp = rp_of(a.r);
+  // G = dY B: rows M, reduction over N along dY's rows (K-major)
+  if ((e = run_pass(dy, a.N, a.M, false, Bt, a.N, a.r, a.M, a.N, partial, status, &ns, st)) != cudaSuccess) return e;
+  finish_partials<<<blocks(a.M * rp), 256, 0, st>>>(partial, ns, a.M, a.r, 1.0f, G, 0, sGp, rp, a.s, Gt, Mp);
+  note_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // dB = s dY^T T: rows N, reduction over M down dY's columns (MN-major)
+  if ((e = run_pass(dy, a.N, a.M, true, Tt, Mp, a.r, a.N, a.M, partial, status, &ns, st)) != cudaSuccess) return e;
+  finish_partials<<<blocks(a.N * a.r), 256, 0, st>>>(partial, ns, a.N, a.r, a.s, dB, 0, nullptr, 0, 0.0f, nullptr, 0);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t adapter_backward_post(const LinearArgs& a, const void* x, float* dA, void* ws, int* status,
+                                  cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
+  const int nq = nq_of(a.r);
+  const int64_t Mp = pad8(a.M);
+  char* w = static_cast<char*>(ws);
+  auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + al(2 * static_cast<size_t>(nq) * a.N) + al(2 * nq * Mp));
+  auto* partial = reinterpret_cast<float*>(w + al(2 * static_cast<size_t>(nq) * a.N) + 2 * al(2 * nq * Mp));
+  int ns = 0;
+  // dA = s G^T x: rows K, reduction over M down x's columns (MN-major)
+  cudaError_t e = run_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, partial, status, &ns, st);
+  if (e != cudaSuccess) return e;
+  finish_partials<<<blocks(a.K * a.r), 256, 0, st>>>(partial, ns, a.K, a.r, a.s, dA, 1, nullptr, 0, 0.0f, nullptr, 0);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace qnf4

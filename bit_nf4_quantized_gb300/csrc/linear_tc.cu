@@ -22,15 +22,13 @@
 // main loop of the next.  Every mbarrier wait is bounded in time; a wait that
 // gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
 // freeing its TMEM.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "linear_tc.cuh"
+#include "tc_ptx.cuh"
 
 namespace qnf4 {
 namespace {
+
+using namespace tc;
 
 constexpr int kTileF = 128;                 // MMA M
 constexpr int kTileT = 256;                 // MMA N
@@ -43,131 +41,8 @@ constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024 /*dyn8*/ + 256 /*barriers, flags*/;
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s
 
 static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
-
-// ---- PTX wrappers ------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of `parity` to complete.  Gives up (returns false) when another
-// thread of the CTA has given up, or after kWaitLimitNs, recording the timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_test(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicCAS(status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
-        return false;
-      }
-    }
-  }
-}
-
-// Wait used only while winding down after a timeout: time-bounded, ignores the flag.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_test(bar, parity)) {
-    if (global_ns() - t0 > 500000000ull) return;
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
-      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-// Shared-memory matrix descriptor (tcgen05 format): start, leading and stride byte
-// offsets in 16-byte units, descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= 2ull << 61;
-  return d;
-}
-
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) | (static_cast<uint32_t>(kTileT >> 3) << 17) |
-         (static_cast<uint32_t>(kTileF >> 4) << 24);
-}
 
 // ---- NF4 decode -------------------------------------------------------------------------
 
@@ -336,8 +211,8 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc_main = make_idesc(p.mode == 1 ? 1u : 0u);
-      const uint32_t idesc_slab = make_idesc(0u);
+      const uint32_t idesc_main = idesc_bf16(kTileF, kTileT, p.mode == 1 ? 1u : 0u);
+      const uint32_t idesc_slab = idesc_bf16(kTileF, kTileT, 0u);
       uint32_t it = 0;
       uint32_t lt = 0;
       bool ok = true;
@@ -494,33 +369,6 @@ __global__ void stage_transposed_bf16(const float* __restrict__ A, int64_t K, in
 int padded_rank(int r) { return (r + kBK - 1) / kBK * kBK; }
 size_t a1024(size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// 2-D row-major tensor [outer, inner] with row pitch `pitch` bytes; box [box_outer, box_inner].
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
-              uint64_t pitch, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {pitch};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -575,14 +423,14 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
 
 }  // namespace
 
-size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t, int r) {
+size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   const size_t rp = padded_rank(r);
-  return a1024(2 * rp * M) + a1024(2 * rp * N);
+  return a1024(2 * rp * M) + a1024(2 * rp * N) + a1024(adapter_fwd_ws_bytes(M, N, K, r));
 }
 
-size_t tc_bwd_ws_bytes(int64_t M, int64_t, int64_t K, int r) {
+size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   const size_t rp = padded_rank(r);
-  return a1024(2 * rp * M) + a1024(2 * rp * K);
+  return a1024(2 * rp * M) + a1024(2 * rp * K) + a1024(adapter_bwd_ws_bytes(M, N, K, r));
 }
 
 cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y, float* T,
@@ -590,11 +438,12 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   const int rp = padded_rank(a.r);
   auto* sTp = static_cast<__nv_bfloat16*>(ws);
   auto* Bp = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M));
-  cudaError_t e = launch_lora_down(a, NF4_BF16, x, A, T, st);
+  void* aws = static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M) +
+              a1024(2 * static_cast<size_t>(rp) * a.N);
+  cudaError_t e = adapter_forward(a, x, A, T, sTp, aws, status, st);
   if (e != cudaSuccess) return e;
   {
     KernelTimer timer(NF4_TIME_ADAPTER, st);
-    if ((e = stage_rows(T, a.M, a.r, a.s, sTp, st)) != cudaSuccess) return e;
     if ((e = stage_rows(B, a.N, a.r, 1.0f, Bp, st)) != cudaSuccess) return e;
   }
   CUtensorMap tok, packed, slab_f, slab_t;
@@ -616,11 +465,12 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   const int rp = padded_rank(a.r);
   auto* sGp = static_cast<__nv_bfloat16*>(ws);
   auto* ApT = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M));
-  cudaError_t e = launch_lora_g(a, NF4_BF16, dy, B, G, st);
+  void* aws = static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M) +
+              a1024(2 * static_cast<size_t>(rp) * a.K);
+  cudaError_t e = adapter_backward_pre(a, dy, T, B, G, sGp, dB, aws, status, st);
   if (e != cudaSuccess) return e;
   {
     KernelTimer timer(NF4_TIME_ADAPTER, st);
-    if ((e = stage_rows(G, a.M, a.r, a.s, sGp, st)) != cudaSuccess) return e;
     const int64_t n = a.K * rp;
     stage_transposed_bf16<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(A, a.K, a.r, rp, ApT);
     note_launch();
@@ -638,9 +488,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   if (!ok) return cudaErrorInvalidValue;
   e = launch_gemm(base_params(a, 1, dx, status), tok, packed, slab_f, slab_t, st);
   if (e != cudaSuccess) return e;
-  e = launch_lora_dA(a, NF4_BF16, G, x, dA, st);
-  if (e == cudaSuccess) e = launch_lora_dB(a, NF4_BF16, dy, T, dB, st);
-  return e;
+  return adapter_backward_post(a, x, dA, aws, status, st);
 }
 
 }  // namespace qnf4
