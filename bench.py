@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--only", default=None,
+                   help="restrict the step to one projection (for profiling; not a bench line)")
     return p.parse_args()
 
 
@@ -151,13 +153,15 @@ def layer_flops(shapes, M, r):
 class Layer:
     """Device buffers for one step over the 7 projections (allocated once)."""
 
-    def __init__(self, dev, seed_base=0):
+    def __init__(self, dev, seed_base=0, only=None):
         import torch
         from bit_nf4_quantized_gb300 import binding
         from bit_nf4_quantized_gb300 import workloads as wl
         c = wl.W3
         self.M, self.r, self.alpha = c["M"], c["r"], c["alpha"]
-        self.shapes = c["shapes"]
+        self.shapes = [t for t in c["shapes"] if only is None or t[0] == only]
+        if not self.shapes:
+            raise ValueError(f"no projection named {only}")
         self.dev = dev
         self.proj = []
         lib = binding.load()
@@ -307,7 +311,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    layer = Layer(dev)
+    layer = Layer(dev, only=args.only)
     pk, pk_src = peaks()
     torch.cuda.synchronize(dev)
 

@@ -10,14 +10,18 @@
 // with f = 128 output features per tile (the MMA's M), t = 256 tokens (the MMA's N):
 //   forward: f = rows of W (output features), c = k, Tok = x,  slab (B, s*T)
 //   dX:      f = columns of W (input features), c = n, Tok = dY, slab (A^T, s*G)
-// Warp roles (320 threads):
+// Warp roles (480 threads):
 //   warp 0      TMA producer: token tile (128B-swizzled) + packed NF4 tile per stage,
 //               or the two adapter slab tiles for the last (rank / 64) stages;
 //   warp 1      TMEM allocation; lane 0 issues tcgen05.mma and tcgen05.commit;
-//   warps 2..5  decoders: 128 threads, one 64-element NF4 block (one 128-byte row of
-//               the A tile) each per stage, written bf16 into the swizzled layout
-//               the MMA reads (K-major for the forward, MN-major for dX);
-//   warps 6..9  epilogue: tcgen05.ld of the accumulator, bf16 stores.
+//   warps 2..9  decoders in two groups of four that take alternate stages; a thread
+//               turns one 64-element NF4 block (one 128-byte row of the A tile) into
+//               bf16 in the swizzled layout the MMA reads (K-major for the forward,
+//               MN-major for dX), through a per-block scaled lookup table;
+//   warps 10..13 epilogue: tcgen05.ld of the accumulator, bf16 stores.
+// The per-block scales a' = dyn8[code] * nested + offset are computed once per call
+// by block_scales_kernel and reach each stage by TMA next to the packed codes, so
+// the decoders never wait on global memory.
 // Two accumulators of 256 columns let the epilogue of one tile overlap the
 // main loop of the next.  Every mbarrier wait is bounded in time; a wait that
 // gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
@@ -38,11 +42,13 @@ constexpr int kABytes = kTileF * kBK * 2;   // 16384
 constexpr int kBBytes = kTileT * kBK * 2;   // 32768
 constexpr int kPBytes = 4096;               // packed NF4 bytes per stage
 constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;                // 14 warps, roles below
 constexpr int kTmemCols = 512;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024 /*dyn8*/ + 256 /*barriers, flags*/;
+constexpr int kScaleSlot = 1024;              // fwd: 128 fp32 scales; dX: 64 rows x 4 fp32
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStages * kScaleSlot + 256;
 
 static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
+static_assert(kStages % 2 == 0, "the two decoder groups alternate stages");
 
 // ---- NF4 decode -------------------------------------------------------------------------
 
@@ -62,20 +68,20 @@ __device__ __forceinline__ void build_lut(float a, uint32_t (&L)[4], uint32_t (&
   }
 }
 
-// Eight weights of one packed word (element 2i in the high nibble of byte i) to four
-// bf16x2 registers in element order.
+// Eight weights of one packed word to four bf16x2 registers in element order.  The
+// word's nibbles, low first, are elements 1 0 3 2 5 4 7 6 (element 2i is the high
+// nibble of byte i); the final byte interleave puts them back in order.
 __device__ __forceinline__ void decode8(uint32_t w, const uint32_t (&L)[4], const uint32_t (&H)[4],
                                         uint32_t* out) {
-  const uint32_t ws = ((w >> 4) & 0x0F0F0F0Fu) | ((w << 4) & 0xF0F0F0F0u);  // nibble i = element i
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint32_t q = ws >> (16 * h);
+    const uint32_t q = h == 0 ? w : (w >> 16);
     const uint32_t s7 = q & 0x7777u;                      // index within a half table
     const uint32_t sb = 0x3210u | ((q >> 1) & 0x4444u);   // pick the half by bit 3
     const uint32_t lo = prmt(prmt(L[0], L[1], s7), prmt(L[2], L[3], s7), sb);
     const uint32_t hi = prmt(prmt(H[0], H[1], s7), prmt(H[2], H[3], s7), sb);
-    out[2 * h] = prmt(lo, hi, 0x5140u);
-    out[2 * h + 1] = prmt(lo, hi, 0x7362u);
+    out[2 * h] = prmt(lo, hi, 0x4051u);
+    out[2 * h + 1] = prmt(lo, hi, 0x6273u);
   }
 }
 
@@ -95,46 +101,59 @@ struct GemmParams {
   int* status;
 };
 
-// Block scale inputs of one decode step, loaded one step ahead of use.
-struct BlockMeta {
-  float nested_or_absmax;
-  uint32_t code;
-  bool valid;
-};
-
-__device__ __forceinline__ BlockMeta fetch_meta(const GemmParams& p, int64_t tile, int step, int row) {
-  BlockMeta m{0.0f, 0u, false};
-  const int64_t f0 = (tile / p.tiles_t) * kTileF;
-  int64_t n, kcol;
-  if (p.mode == 0) {
-    n = f0 + row;
-    kcol = static_cast<int64_t>(step) * kBK;
+// Block scales a' = dyn8[code] * nested + offset (two roundings) or the fp32 absmax, one
+// per 64-element block, laid out so each stage's 128 scales are one TMA box:
+//   forward (mode 0): out[kb * N + n]        (a row of 128 consecutive n per stage)
+//   dX (mode 1):      out[n * ldk + kb]      (ldk = K/64 rounded up to 4; 64 rows x 4 per stage)
+// Entries past the matrix are never read as data: the TMA box zero-fills them.
+__global__ void block_scales_kernel(Nf4View w, int64_t N, int64_t K, int mode, int64_t ldk,
+                                    float* __restrict__ out, DecodeTables tabs) {
+  __shared__ float dyn8[256];
+  dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
+  __syncthreads();
+  const int64_t kbn = K / kBlock;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = mode == 0 ? kbn * N : N * ldk;
+  if (i >= total) return;
+  int64_t n, kb;
+  if (mode == 0) {
+    kb = i / N;
+    n = i % N;
   } else {
-    n = static_cast<int64_t>(step) * kBK + (row & 63);
-    kcol = f0 + 64 * (row >> 6);
+    n = i / ldk;
+    kb = i % ldk;
+    if (kb >= kbn) {
+      out[i] = 0.0f;
+      return;
+    }
   }
-  if (n >= p.N || kcol >= p.K) return m;
-  const int64_t blk = n * (p.K / kBlock) + kcol / kBlock;
-  m.valid = true;
-  if (p.dq) {
-    m.code = static_cast<const uint8_t*>(p.absmax)[blk];
-    m.nested_or_absmax = p.nested[blk >> 8];
+  const int64_t blk = n * kbn + kb;
+  float a;
+  if (w.dq) {
+    const uint32_t code = static_cast<const uint8_t*>(w.absmax)[blk];
+    a = __fadd_rn(__fmul_rn(dyn8[code], w.nested[blk >> 8]), *w.offset);
   } else {
-    m.nested_or_absmax = static_cast<const float*>(p.absmax)[blk];
+    a = static_cast<const float*>(w.absmax)[blk];
   }
-  return m;
+  out[i] = a;
 }
 
+// Warp roles:
+//   0       TMA producer (lane 0)
+//   1       TMEM allocation; MMA issue (lane 0)
+//   2..9    decoders: warps 2..5 take the even stages, 6..9 the odd ones; thread =
+//           one 128-byte row of the A tile (one 64-element NF4 block)
+//   10..13  epilogue
 __global__ void __launch_bounds__(kThreads, 1)
 nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_packed,
             const __grid_constant__ CUtensorMap tm_slab_f, const __grid_constant__ CUtensorMap tm_slab_t,
-            const GemmParams p, const DecodeTables tabs) {
+            const __grid_constant__ CUtensorMap tm_scale, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  float* dyn8 = reinterpret_cast<float*>(base_ptr + kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + 1024);
+  const float* scales = reinterpret_cast<const float*>(base_ptr + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + kStages * kScaleSlot);
   // bars: full[4] aready[4] empty[4] accfull[2] accempty[2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16) + 1;
@@ -142,14 +161,14 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   auto stage_a = [&](int s) { return base + s * kStageBytes; };
   auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
   auto stage_p = [&](int s) { return base + s * kStageBytes + kABytes + kBBytes; };
+  auto stage_s = [&](int s) { return base + kStages * kStageBytes + s * kScaleSlot; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 256) dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(s), 1);                 // full: producer arrive + TMA bytes
-      mbar_init(bar(4 + s), 4);             // aready: one arrive per decoder warp
+      mbar_init(bar(4 + s), 4);             // aready: the four warps of one decoder group
       mbar_init(bar(8 + s), 1);             // empty: tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -172,36 +191,43 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
 
   const int64_t total_tiles = static_cast<int64_t>(p.tiles_t) * p.tiles_f;
   const int steps = p.red_steps + p.slab_steps;
+  const int64_t my_tiles =
+      blockIdx.x < total_tiles ? (total_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int64_t total_it = my_tiles * steps;    // every role walks the same step sequence
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      uint32_t it = 0;
       int last_phase[kStages];
       bool issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = false, last_phase[s] = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int64_t it = 0; it < total_it; ++it) {
+        const int64_t tile = blockIdx.x + (it / steps) * gridDim.x;
+        const int step = static_cast<int>(it % steps);
         const int t0 = static_cast<int>((tile % p.tiles_t) * kTileT);
         const int f0 = static_cast<int>((tile / p.tiles_t) * kTileF);
-        for (int step = 0; step < steps; ++step, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait(bar(8 + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          if (step < p.red_steps) {
-            mbar_expect_tx(bar(s), kBBytes + kPBytes);
-            tma_load_2d(stage_b(s), &tm_tok, bar(s), step * kBK, t0);
-            if (p.mode == 0) tma_load_2d(stage_p(s), &tm_packed, bar(s), step * (kBK / 2), f0);
-            else tma_load_2d(stage_p(s), &tm_packed, bar(s), f0 / 2, step * kBK);
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+        if (!mbar_wait(bar(8 + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (step < p.red_steps) {
+          mbar_expect_tx(bar(s), kBBytes + kPBytes + (p.mode == 0 ? kTileF * 4 : 64 * 16));
+          tma_load_2d(stage_b(s), &tm_tok, bar(s), step * kBK, t0);
+          if (p.mode == 0) {
+            tma_load_2d(stage_p(s), &tm_packed, bar(s), step * (kBK / 2), f0);
+            tma_load_2d(stage_s(s), &tm_scale, bar(s), f0, step);
           } else {
-            const int j = (step - p.red_steps) * kBK;
-            mbar_expect_tx(bar(s), kBBytes + kABytes);
-            tma_load_2d(stage_b(s), &tm_slab_t, bar(s), j, t0);
-            tma_load_2d(stage_a(s), &tm_slab_f, bar(s), j, f0);
+            tma_load_2d(stage_p(s), &tm_packed, bar(s), f0 / 2, step * kBK);
+            tma_load_2d(stage_s(s), &tm_scale, bar(s), (f0 / kBlock) & ~3, step * kBK);
           }
-          issued[s] = true;
-          last_phase[s] = ph;
+        } else {
+          const int j = (step - p.red_steps) * kBK;
+          mbar_expect_tx(bar(s), kBBytes + kABytes);
+          tma_load_2d(stage_b(s), &tm_slab_t, bar(s), j, t0);
+          tma_load_2d(stage_a(s), &tm_slab_f, bar(s), j, f0);
         }
+        issued[s] = true;
+        last_phase[s] = ph;
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
         for (int s = 0; s < kStages; ++s)
@@ -213,104 +239,85 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
     if (lane == 0) {
       const uint32_t idesc_main = idesc_bf16(kTileF, kTileT, p.mode == 1 ? 1u : 0u);
       const uint32_t idesc_slab = idesc_bf16(kTileF, kTileT, 0u);
-      uint32_t it = 0;
-      uint32_t lt = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++lt) {
-        const uint32_t b = lt & 1u;
-        const uint32_t aph = (lt >> 1) & 1u;
-        if (!mbar_wait(bar(14 + b), aph ^ 1u, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * kTileT;
-        for (int step = 0; step < steps; ++step, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!mbar_wait(bar(s), ph, abort_flag, p.status) || !mbar_wait(bar(4 + s), ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+      for (int64_t it = 0; it < total_it && ok; ++it) {
+        const int64_t lt = it / steps;
+        const int step = static_cast<int>(it % steps);
+        const uint32_t b = static_cast<uint32_t>(lt) & 1u;
+        if (step == 0) {
+          if (!mbar_wait(bar(14 + b), (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) break;
           tc_fence_after();
-          const bool slab = step >= p.red_steps;
-          const bool mn_major = (p.mode == 1) && !slab;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // K-major: 32 bytes per 16-element k step inside the 128-byte row.
-            // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
-            // 64-feature halves of the tile are 8192 bytes apart.
-            const uint64_t adesc = mn_major ? smem_desc(stage_a(s) + kk * 2048, 8192, 1024)
-                                            : smem_desc(stage_a(s) + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc(stage_b(s) + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, slab ? idesc_slab : idesc_main, (step > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(bar(8 + s));
         }
-        if (!ok) break;
-        umma_commit(bar(12 + b));
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+        if (!mbar_wait(bar(s), ph, abort_flag, p.status) || !mbar_wait(bar(4 + s), ph, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool slab = step >= p.red_steps;
+        const bool mn_major = (p.mode == 1) && !slab;
+        const uint32_t d_tmem = tmem_base + b * kTileT;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // K-major: 32 bytes per 16-element k step inside the 128-byte row.
+          // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
+          // 64-feature halves of the tile are 8192 bytes apart.
+          const uint64_t adesc = mn_major ? smem_desc(stage_a(s) + kk * 2048, 8192, 1024)
+                                          : smem_desc(stage_a(s) + kk * 32, 16, 1024);
+          const uint64_t bdesc = smem_desc(stage_b(s) + kk * 32, 16, 1024);
+          umma_bf16(d_tmem, adesc, bdesc, slab ? idesc_slab : idesc_main, (step > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(8 + s));
+        if (step == steps - 1) umma_commit(bar(12 + b));
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ---------------- NF4 decoders ----------------
-    const int row = threadIdx.x - 64;           // row of the A tile, 0..127
-    uint32_t it = 0;
-    bool ok = true;
-    int64_t tile = blockIdx.x;
-    BlockMeta cur = (tile < total_tiles) ? fetch_meta(p, tile, 0, row) : BlockMeta{0.0f, 0u, false};
-    const float offset = p.dq ? *p.offset : 0.0f;
-    for (; tile < total_tiles && ok; tile += gridDim.x) {
-      for (int step = 0; step < steps; ++step, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
-        if (step < p.red_steps) {
-          BlockMeta nxt{0.0f, 0u, false};
-          if (step + 1 < p.red_steps) nxt = fetch_meta(p, tile, step + 1, row);
-          else if (tile + gridDim.x < total_tiles) nxt = fetch_meta(p, tile + gridDim.x, 0, row);
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(s), ph, abort_flag, p.status))) { ok = false; break; }
-          const uint32_t arow = stage_a(s) + row * 128;
-          const uint32_t sw = static_cast<uint32_t>(row & 7);
-          if (cur.valid) {
-            const float a = p.dq ? __fadd_rn(__fmul_rn(dyn8[cur.code], cur.nested_or_absmax), offset)
-                                 : cur.nested_or_absmax;
-            uint32_t L[4], H[4];
-            build_lut(a, L, H);
-            const uint32_t poff = (p.mode == 0) ? row * 32 : (row & 63) * 64 + (row >> 6) * 32;
-            const uint8_t* src = base_ptr + (stage_p(s) - base) + poff;
-            const uint4 w0 = *reinterpret_cast<const uint4*>(src);
-            const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16);
-            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const int group = (warp - 2) >> 2;
+    const int row = ((warp - 2) & 3) * 32 + lane;  // row of the A tile, 0..127
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    const uint32_t poff = (p.mode == 0) ? row * 32 : (row & 63) * 64 + (row >> 6) * 32;
+    for (int64_t it = group; it < total_it; it += 2) {
+      const int step = static_cast<int>(it % steps);
+      const int s = static_cast<int>(it % kStages);
+      const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(s), ph, abort_flag, p.status))) break;
+      if (step < p.red_steps) {
+        uint32_t L[4], H[4];
+        // forward: scale of row `row`; dX: row (row & 63) of a 64 x 4 box whose first
+        // column is the 128-feature tile's first block rounded down to a multiple of 4
+        const int64_t f0 = (blockIdx.x + (it / steps) * gridDim.x) / p.tiles_t * kTileF;
+        const float a = (p.mode == 0) ? scales[s * (kScaleSlot / 4) + row]
+                                      : scales[s * (kScaleSlot / 4) + (row & 63) * 4 +
+                                               static_cast<int>((f0 / kBlock) & 3) + (row >> 6)];
+        build_lut(a, L, H);
+        const uint8_t* src = base_ptr + (stage_p(s) - base) + poff;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16);
+        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t arow = stage_a(s) + row * 128;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              uint32_t o[4];
-              decode8(words[i], L, H, o);
-              const uint32_t dst = arow + ((static_cast<uint32_t>(i) ^ sw) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                           "r"(o[3])
-                           : "memory");
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t dst = arow + (static_cast<uint32_t>(i) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
-            }
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(4 + s));
-          cur = nxt;
-        } else {
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(s), ph, abort_flag, p.status))) { ok = false; break; }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(4 + s));
+        for (int i = 0; i < 8; ++i) {
+          uint32_t o[4];
+          decode8(words[i], L, H, o);
+          const uint32_t dst = arow + ((static_cast<uint32_t>(i) ^ sw) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                       "r"(o[3])
+                       : "memory");
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(4 + s));
     }
   } else {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    uint32_t lt = 0;
-    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++lt) {
-      const uint32_t b = lt & 1u;
-      const uint32_t aph = (lt >> 1) & 1u;
+    for (int64_t lt = 0; lt < my_tiles; ++lt) {
+      const int64_t tile = blockIdx.x + lt * gridDim.x;
+      const uint32_t b = static_cast<uint32_t>(lt) & 1u;
+      const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(12 + b), aph, abort_flag, p.status))) break;
       tc_fence_after();
       const int64_t t0 = (tile % p.tiles_t) * kTileT;
@@ -377,7 +384,8 @@ int sm_count() {
 }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUtensorMap& packed,
-                        const CUtensorMap& slab_f, const CUtensorMap& slab_t, cudaStream_t st) {
+                        const CUtensorMap& slab_f, const CUtensorMap& slab_t, const CUtensorMap& scale,
+                        cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -387,7 +395,7 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUten
   const int64_t tiles = static_cast<int64_t>(p.tiles_t) * p.tiles_f;
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
-  nf4_tc_gemm<<<grid, kThreads, kSmemBytes, st>>>(tok, packed, slab_f, slab_t, p, decode_tables());
+  nf4_tc_gemm<<<grid, kThreads, kSmemBytes, st>>>(tok, packed, slab_f, slab_t, scale, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -398,6 +406,31 @@ cudaError_t stage_rows(const float* src, int64_t rows, int r, float scale, __nv_
   stage_rows_bf16<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(src, rows, r, rp, scale, dst);
   note_launch();
   return cudaGetLastError();
+}
+
+int64_t scale_ld(int64_t K) { return (K / kBlock + 3) / 4 * 4; }
+
+size_t scales_bytes(int64_t N, int64_t K, int mode) {
+  return a1024(sizeof(float) * static_cast<size_t>(N) * (mode == 0 ? K / kBlock : scale_ld(K)));
+}
+
+// Block scales of W for one GEMM call, and the tensor map each stage's box comes from.
+cudaError_t prepare_scales(const LinearArgs& a, int mode, float* out, CUtensorMap* map, cudaStream_t st) {
+  const int64_t kbn = a.K / kBlock, ldk = scale_ld(a.K);
+  const int64_t n = mode == 0 ? kbn * a.N : a.N * ldk;
+  {
+    KernelTimer timer(NF4_TIME_ADAPTER, st);
+    block_scales_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(a.W, a.N, a.K, mode, ldk, out,
+                                                                                decode_tables());
+    note_launch();
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const bool ok = mode == 0 ? make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, a.N, kbn, 4 * a.N, kTileF, 1,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE)
+                            : make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, ldk, a.N, 4 * ldk, 4, 64,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  return ok ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
@@ -425,12 +458,12 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
 
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   const size_t rp = padded_rank(r);
-  return a1024(2 * rp * M) + a1024(2 * rp * N) + a1024(adapter_fwd_ws_bytes(M, N, K, r));
+  return a1024(2 * rp * M) + a1024(2 * rp * N) + a1024(adapter_fwd_ws_bytes(M, N, K, r)) + scales_bytes(N, K, 0);
 }
 
 size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
   const size_t rp = padded_rank(r);
-  return a1024(2 * rp * M) + a1024(2 * rp * K) + a1024(adapter_bwd_ws_bytes(M, N, K, r));
+  return a1024(2 * rp * M) + a1024(2 * rp * K) + a1024(adapter_bwd_ws_bytes(M, N, K, r)) + scales_bytes(N, K, 1);
 }
 
 cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y, float* T,
@@ -440,8 +473,11 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   auto* Bp = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M));
   void* aws = static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M) +
               a1024(2 * static_cast<size_t>(rp) * a.N);
+  auto* sc = reinterpret_cast<float*>(static_cast<char*>(aws) + a1024(adapter_fwd_ws_bytes(a.M, a.N, a.K, a.r)));
   cudaError_t e = adapter_forward(a, x, A, T, sTp, aws, status, st);
   if (e != cudaSuccess) return e;
+  CUtensorMap scale;
+  if ((e = prepare_scales(a, 0, sc, &scale, st)) != cudaSuccess) return e;
   {
     KernelTimer timer(NF4_TIME_ADAPTER, st);
     if ((e = stage_rows(B, a.N, a.r, 1.0f, Bp, st)) != cudaSuccess) return e;
@@ -456,7 +492,7 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kBK, kTileT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  return launch_gemm(base_params(a, 0, y, status), tok, packed, slab_f, slab_t, st);
+  return launch_gemm(base_params(a, 0, y, status), tok, packed, slab_f, slab_t, scale, st);
 }
 
 cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, const float* T, const float* A,
@@ -467,8 +503,11 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   auto* ApT = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M));
   void* aws = static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M) +
               a1024(2 * static_cast<size_t>(rp) * a.K);
+  auto* sc = reinterpret_cast<float*>(static_cast<char*>(aws) + a1024(adapter_bwd_ws_bytes(a.M, a.N, a.K, a.r)));
   cudaError_t e = adapter_backward_pre(a, dy, T, B, G, sGp, dB, aws, status, st);
   if (e != cudaSuccess) return e;
+  CUtensorMap scale;
+  if ((e = prepare_scales(a, 1, sc, &scale, st)) != cudaSuccess) return e;
   {
     KernelTimer timer(NF4_TIME_ADAPTER, st);
     const int64_t n = a.K * rp;
@@ -486,7 +525,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kBK, kTileT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  e = launch_gemm(base_params(a, 1, dx, status), tok, packed, slab_f, slab_t, st);
+  e = launch_gemm(base_params(a, 1, dx, status), tok, packed, slab_f, slab_t, scale, st);
   if (e != cudaSuccess) return e;
   return adapter_backward_post(a, x, dA, aws, status, st);
 }
