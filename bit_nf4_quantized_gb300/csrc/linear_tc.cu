@@ -46,6 +46,7 @@ constexpr int kThreads = 448;                // 14 warps, roles below
 constexpr int kTmemCols = 512;
 constexpr int kScaleSlot = 1024;              // fwd: 128 fp32 scales; dX: 64 rows x 4 fp32
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStages * kScaleSlot + 256;
+static_assert(20 * 8 + 8 <= 256, "barrier block");
 
 static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
 static_assert(kStages % 2 == 0, "the two decoder groups alternate stages");
@@ -93,6 +94,7 @@ struct GemmParams {
   int red_steps;       // ceil(contraction / 64)
   int slab_steps;      // padded rank / 64
   int tiles_t, tiles_f;
+  int f_fast;          // tile order: 1 = feature tiles vary fastest (dX), 0 = token tiles (forward)
   const void* absmax;  // uint8 codes (dq) or float
   const float* nested;
   const float* offset;
@@ -154,20 +156,24 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   uint8_t* base_ptr = smem_raw + (base - raw);
   const float* scales = reinterpret_cast<const float*>(base_ptr + kStages * kStageBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + kStages * kScaleSlot);
-  // bars: full[4] aready[4] empty[4] accfull[2] accempty[2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 16);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16) + 1;
+  // bars: full_b[4] aready[4] empty[4] accfull[2] accempty[2] full_p[4]
+  //   full_b: token tile (or both slab tiles) landed; full_p: packed codes + scales landed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20) + 1;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   auto stage_a = [&](int s) { return base + s * kStageBytes; };
   auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
   auto stage_p = [&](int s) { return base + s * kStageBytes + kABytes + kBBytes; };
   auto stage_s = [&](int s) { return base + kStages * kStageBytes + s * kScaleSlot; };
+  auto tile_t = [&](int64_t tile) { return p.f_fast ? tile / p.tiles_f : tile % p.tiles_t; };
+  auto tile_f = [&](int64_t tile) { return p.f_fast ? tile % p.tiles_f : tile / p.tiles_t; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(s), 1);                 // full: producer arrive + TMA bytes
+      mbar_init(bar(s), 1);                 // full_b: producer arrive + TMA bytes
+      mbar_init(bar(16 + s), 1);            // full_p: producer arrive (+ TMA bytes on decode steps)
       mbar_init(bar(4 + s), 4);             // aready: the four warps of one decoder group
       mbar_init(bar(8 + s), 1);             // empty: tcgen05.commit
     }
@@ -205,23 +211,26 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       for (int64_t it = 0; it < total_it; ++it) {
         const int64_t tile = blockIdx.x + (it / steps) * gridDim.x;
         const int step = static_cast<int>(it % steps);
-        const int t0 = static_cast<int>((tile % p.tiles_t) * kTileT);
-        const int f0 = static_cast<int>((tile / p.tiles_t) * kTileF);
+        const int t0 = static_cast<int>(tile_t(tile) * kTileT);
+        const int f0 = static_cast<int>(tile_f(tile) * kTileF);
         const int s = static_cast<int>(it % kStages);
         const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
         if (!mbar_wait(bar(8 + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
         if (step < p.red_steps) {
-          mbar_expect_tx(bar(s), kBBytes + kPBytes + (p.mode == 0 ? kTileF * 4 : 64 * 16));
-          tma_load_2d(stage_b(s), &tm_tok, bar(s), step * kBK, t0);
+          // codes and scales first: the decoders start on them while the token tile streams
+          mbar_expect_tx(bar(16 + s), kPBytes + (p.mode == 0 ? kTileF * 4 : 64 * 16));
           if (p.mode == 0) {
-            tma_load_2d(stage_p(s), &tm_packed, bar(s), step * (kBK / 2), f0);
-            tma_load_2d(stage_s(s), &tm_scale, bar(s), f0, step);
+            tma_load_2d(stage_p(s), &tm_packed, bar(16 + s), step * (kBK / 2), f0);
+            tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), f0, step);
           } else {
-            tma_load_2d(stage_p(s), &tm_packed, bar(s), f0 / 2, step * kBK);
-            tma_load_2d(stage_s(s), &tm_scale, bar(s), (f0 / kBlock) & ~3, step * kBK);
+            tma_load_2d(stage_p(s), &tm_packed, bar(16 + s), f0 / 2, step * kBK);
+            tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), (f0 / kBlock) & ~3, step * kBK);
           }
+          mbar_expect_tx(bar(s), kBBytes);
+          tma_load_2d(stage_b(s), &tm_tok, bar(s), step * kBK, t0);
         } else {
           const int j = (step - p.red_steps) * kBK;
+          mbar_arrive(bar(16 + s));
           mbar_expect_tx(bar(s), kBBytes + kABytes);
           tma_load_2d(stage_b(s), &tm_slab_t, bar(s), j, t0);
           tma_load_2d(stage_a(s), &tm_slab_f, bar(s), j, f0);
@@ -231,7 +240,10 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
         for (int s = 0; s < kStages; ++s)
-          if (issued[s]) mbar_drain(bar(s), last_phase[s]);
+          if (issued[s]) {
+            mbar_drain(bar(s), last_phase[s]);
+            mbar_drain(bar(16 + s), last_phase[s]);
+          }
       }
     }
   } else if (warp == 1) {
@@ -282,12 +294,12 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       const int step = static_cast<int>(it % steps);
       const int s = static_cast<int>(it % kStages);
       const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(s), ph, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(16 + s), ph, abort_flag, p.status))) break;
       if (step < p.red_steps) {
         uint32_t L[4], H[4];
         // forward: scale of row `row`; dX: row (row & 63) of a 64 x 4 box whose first
         // column is the 128-feature tile's first block rounded down to a multiple of 4
-        const int64_t f0 = (blockIdx.x + (it / steps) * gridDim.x) / p.tiles_t * kTileF;
+        const int64_t f0 = tile_f(blockIdx.x + (it / steps) * gridDim.x) * kTileF;
         const float a = (p.mode == 0) ? scales[s * (kScaleSlot / 4) + row]
                                       : scales[s * (kScaleSlot / 4) + (row & 63) * 4 +
                                                static_cast<int>((f0 / kBlock) & 3) + (row >> 6)];
@@ -320,8 +332,8 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(12 + b), aph, abort_flag, p.status))) break;
       tc_fence_after();
-      const int64_t t0 = (tile % p.tiles_t) * kTileT;
-      const int64_t f = (tile / p.tiles_t) * kTileF + quarter * 32 + lane;
+      const int64_t t0 = tile_t(tile) * kTileT;
+      const int64_t f = tile_f(tile) * kTileF + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + b * kTileT + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < kTileT; c0 += 16) {
@@ -445,6 +457,7 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   p.slab_steps = padded_rank(a.r) / kBK;
   p.tiles_t = static_cast<int>((a.M + kTileT - 1) / kTileT);
   p.tiles_f = static_cast<int>((p.F + kTileF - 1) / kTileF);
+  p.f_fast = mode == 1 ? 1 : 0;
   p.absmax = a.W.absmax;
   p.nested = a.W.nested;
   p.offset = a.W.offset;
