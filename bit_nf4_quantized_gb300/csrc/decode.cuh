@@ -1,0 +1,50 @@
+// Register-table decode of packed NF4 codes to bf16, shared by the dequantize kernel
+// and the tensor-core GEMM.  For a block with scale a', entry q of the table is
+// bf16(nf4[q] * a') -- the fp32 product rounded once -- so the decoded values are
+// exactly what nf4_dequantize writes for bf16 output.
+#pragma once
+
+#include "common.cuh"
+
+namespace qnf4 {
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Scaled lookup table of one block: entry i = bf16(nf4[i] * a'), split into low bytes
+// (L, 4 registers of 4 entries) and high bytes (H), so prmt can index it by nibble.
+__device__ __forceinline__ void build_lut(float a, uint32_t (&L)[4], uint32_t (&H)[4]) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(__fmul_rn(nf4_value(4 * t + 0), a),
+                                                    __fmul_rn(nf4_value(4 * t + 1), a));
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(__fmul_rn(nf4_value(4 * t + 2), a),
+                                                    __fmul_rn(nf4_value(4 * t + 3), a));
+    const uint32_t u0 = *reinterpret_cast<const uint32_t*>(&p0);
+    const uint32_t u1 = *reinterpret_cast<const uint32_t*>(&p1);
+    L[t] = prmt(u0, u1, 0x6420u);
+    H[t] = prmt(u0, u1, 0x7531u);
+  }
+}
+
+// Eight weights of one packed word to four bf16x2 registers in element order.  The
+// word's nibbles, low first, are elements 1 0 3 2 5 4 7 6 (element 2i is the high
+// nibble of byte i); the final byte interleave puts them back in order.
+__device__ __forceinline__ void decode8(uint32_t w, const uint32_t (&L)[4], const uint32_t (&H)[4],
+                                        uint32_t* out) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t q = h == 0 ? w : (w >> 16);
+    const uint32_t s7 = q & 0x7777u;                      // index within a half table
+    const uint32_t sb = 0x3210u | ((q >> 1) & 0x4444u);   // pick the half by bit 3
+    const uint32_t lo = prmt(prmt(L[0], L[1], s7), prmt(L[2], L[3], s7), sb);
+    const uint32_t hi = prmt(prmt(H[0], H[1], s7), prmt(H[2], H[3], s7), sb);
+    out[2 * h] = prmt(lo, hi, 0x4051u);
+    out[2 * h + 1] = prmt(lo, hi, 0x6273u);
+  }
+}
+
+}  // namespace qnf4

@@ -27,6 +27,7 @@
 // gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
 // freeing its TMEM.
 #include "linear_tc.cuh"
+#include "decode.cuh"
 #include "tc_ptx.cuh"
 
 namespace qnf4 {
@@ -50,41 +51,6 @@ static_assert(20 * 8 + 8 <= 256, "barrier block");
 
 static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
 static_assert(kStages % 2 == 0, "the two decoder groups alternate stages");
-
-// ---- NF4 decode -------------------------------------------------------------------------
-
-// Scaled lookup table of one block: entry i = bf16(nf4[i] * a'), split into low bytes
-// (L, 4 registers of 4 entries) and high bytes (H), so prmt can index it by nibble.
-__device__ __forceinline__ void build_lut(float a, uint32_t (&L)[4], uint32_t (&H)[4]) {
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const __nv_bfloat162 p0 = __floats2bfloat162_rn(__fmul_rn(nf4_value(4 * t + 0), a),
-                                                    __fmul_rn(nf4_value(4 * t + 1), a));
-    const __nv_bfloat162 p1 = __floats2bfloat162_rn(__fmul_rn(nf4_value(4 * t + 2), a),
-                                                    __fmul_rn(nf4_value(4 * t + 3), a));
-    const uint32_t u0 = *reinterpret_cast<const uint32_t*>(&p0);
-    const uint32_t u1 = *reinterpret_cast<const uint32_t*>(&p1);
-    L[t] = prmt(u0, u1, 0x6420u);
-    H[t] = prmt(u0, u1, 0x7531u);
-  }
-}
-
-// Eight weights of one packed word to four bf16x2 registers in element order.  The
-// word's nibbles, low first, are elements 1 0 3 2 5 4 7 6 (element 2i is the high
-// nibble of byte i); the final byte interleave puts them back in order.
-__device__ __forceinline__ void decode8(uint32_t w, const uint32_t (&L)[4], const uint32_t (&H)[4],
-                                        uint32_t* out) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t q = h == 0 ? w : (w >> 16);
-    const uint32_t s7 = q & 0x7777u;                      // index within a half table
-    const uint32_t sb = 0x3210u | ((q >> 1) & 0x4444u);   // pick the half by bit 3
-    const uint32_t lo = prmt(prmt(L[0], L[1], s7), prmt(L[2], L[3], s7), sb);
-    const uint32_t hi = prmt(prmt(H[0], H[1], s7), prmt(H[2], H[3], s7), sb);
-    out[2 * h] = prmt(lo, hi, 0x4051u);
-    out[2 * h + 1] = prmt(lo, hi, 0x6273u);
-  }
-}
 
 struct GemmParams {
   int64_t M;           // tokens

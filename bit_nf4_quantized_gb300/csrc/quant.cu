@@ -17,6 +17,7 @@
 //   2. nf4_absmax_mean: one CTA finishes the tree over the group sums -> offset.
 //   3. nf4_encode_nested: centre, nested absmax per group, dynamic8 codes.
 #include "common.cuh"
+#include "decode.cuh"
 
 namespace qnf4 {
 namespace {
@@ -165,73 +166,121 @@ nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __r
 }
 
 // ---- dequantize -----------------------------------------------------------------
+//
+// A warp decodes 1024-element chunks: lane l takes elements 32l .. 32l+31 (one 16-byte
+// load of packed codes, one block scale).  bf16 output goes through the register
+// lookup table of decode.cuh (bf16(nf4[q] * a'), exact); fp32 output multiplies the
+// code value by a' per element.  The lane's 64 or 128 output bytes are staged in a
+// swizzled shared buffer so each global store instruction writes 512 contiguous bytes.
 
 constexpr int kDeqThreads = 256;
-constexpr int kDeqQuadRows = 8;    // per warp: 8 x 128 elements
+constexpr int kDeqChunks = 2;                       // chunks per warp, loads issued together
+constexpr int kDeqPerCta = (kDeqThreads / 32) * kDeqChunks * 1024;
 
-__device__ __forceinline__ void store_quad(float* y, int64_t e0, int64_t n, const float w[4]) {
-  if (e0 + 3 < n) {
-    __stcs(reinterpret_cast<float4*>(y + e0), make_float4(w[0], w[1], w[2], w[3]));
-  } else {
-    for (int i = 0; i < 4; ++i)
-      if (e0 + i < n) y[e0 + i] = w[i];
-  }
-}
-
-__device__ __forceinline__ void store_quad(__nv_bfloat16* y, int64_t e0, int64_t n, const float w[4]) {
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(w[0], w[1]);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(w[2], w[3]);
-  if (e0 + 3 < n) {
-    uint2 t;
-    t.x = *reinterpret_cast<const uint32_t*>(&lo);
-    t.y = *reinterpret_cast<const uint32_t*>(&hi);
-    __stcs(reinterpret_cast<uint2*>(y + e0), t);
-  } else {
-    for (int i = 0; i < 4; ++i)
-      if (e0 + i < n) y[e0 + i] = __float2bfloat16_rn(w[i]);
-  }
+// 16-byte slot g of a warp's staging buffer, rows of 8 slots XOR-swizzled by row.
+__device__ __forceinline__ uint32_t stage_slot(uint32_t g) {
+  const uint32_t row = g >> 3, col = g & 7;
+  return ((row << 3) | (col ^ (row & 7))) << 4;
 }
 
 template <typename Tout, bool kDQ>
 __global__ void __launch_bounds__(kDeqThreads)
 nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
-  __shared__ float lut[16][32];        // NF4 values replicated per lane: conflict-free lookups
+  constexpr int kOutBytes = 32 * sizeof(Tout);      // per lane per chunk: 64 (bf16) or 128 (fp32)
   __shared__ float dyn8[256];
-  for (int i = threadIdx.x; i < 16 * 32; i += kDeqThreads) lut[i >> 5][i & 31] = tabs.nf4[i >> 5];
+  __shared__ float lut[16][32];                     // code values replicated per lane (fp32 path)
+  __shared__ __align__(16) uint8_t stage[kDeqThreads / 32][32 * kOutBytes];
   dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
+  for (int i = threadIdx.x; i < 16 * 32; i += kDeqThreads) lut[i >> 5][i & 31] = tabs.nf4[i >> 5];
   __syncthreads();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n = w.numel;
   const float offset = kDQ ? *w.offset : 0.0f;
-  const int64_t warp_base =
-      (static_cast<int64_t>(blockIdx.x) * (kDeqThreads / 32) + warp) * (kDeqQuadRows * 128);
-#pragma unroll 4
-  for (int u = 0; u < kDeqQuadRows; ++u) {
-    const int64_t e0 = warp_base + u * 128 + 4 * lane;
-    if (e0 >= n) break;
-    const int64_t byte0 = e0 >> 1;
-    uint32_t bytes;
-    if (e0 + 3 < n) {
-      bytes = __ldcs(reinterpret_cast<const uint16_t*>(w.packed + byte0));
-    } else {
-      bytes = w.packed[byte0];
-      if (e0 + 2 < n) bytes |= static_cast<uint32_t>(w.packed[byte0 + 1]) << 8;
+  uint8_t* buf = stage[warp];
+  const uint32_t buf_s = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
+  const int64_t chunk0 = (static_cast<int64_t>(blockIdx.x) * (kDeqThreads / 32) + warp) * kDeqChunks;
+
+  uint4 pk[kDeqChunks];
+  float sc[kDeqChunks];
+#pragma unroll
+  for (int u = 0; u < kDeqChunks; ++u) {           // all loads of the warp's chunks first
+    const int64_t e0 = (chunk0 + u) * 1024 + 32 * lane;
+    sc[u] = 0.0f;
+    pk[u] = make_uint4(0, 0, 0, 0);
+    if (e0 + 31 < n) pk[u] = __ldcs(reinterpret_cast<const uint4*>(w.packed + (e0 >> 1)));
+    if (e0 < n) {
+      const int64_t blk = e0 >> 6;
+      if (kDQ) {
+        const uint8_t c = static_cast<const uint8_t*>(w.absmax)[blk];
+        sc[u] = __fadd_rn(__fmul_rn(dyn8[c], w.nested[blk >> 8]), offset);
+      } else {
+        sc[u] = static_cast<const float*>(w.absmax)[blk];
+      }
     }
-    const int64_t blk = e0 >> 6;
-    float a;
-    if (kDQ) {
-      const uint8_t c = static_cast<const uint8_t*>(w.absmax)[blk];
-      a = __fadd_rn(__fmul_rn(dyn8[c], w.nested[blk >> 8]), offset);
+  }
+#pragma unroll
+  for (int u = 0; u < kDeqChunks; ++u) {
+    const int64_t c0 = (chunk0 + u) * 1024;
+    if (c0 >= n) break;
+    const float a = sc[u];
+    if (c0 + 1024 <= n) {
+      const uint32_t words[4] = {pk[u].x, pk[u].y, pk[u].z, pk[u].w};
+      if (sizeof(Tout) == 2) {
+        uint32_t L[4], H[4];
+        build_lut(a, L, H);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t o[4];
+          decode8(words[i], L, H, o);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf_s + stage_slot(4 * lane + i)),
+                       "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                       : "memory");
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t wd = words[i];
+          // nibbles low first: elements 1 0 3 2 5 4 7 6 of this word
+          float v[8];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            v[2 * b] = __fmul_rn(lut[(wd >> (8 * b + 4)) & 15][lane], a);
+            v[2 * b + 1] = __fmul_rn(lut[(wd >> (8 * b)) & 15][lane], a);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf_s + stage_slot(8 * lane + 2 * i + h)),
+                         "r"(__float_as_uint(v[4 * h])), "r"(__float_as_uint(v[4 * h + 1])),
+                         "r"(__float_as_uint(v[4 * h + 2])), "r"(__float_as_uint(v[4 * h + 3]))
+                         : "memory");
+        }
+      }
+      __syncwarp();
+      uint4* out = reinterpret_cast<uint4*>(y + c0);
+#pragma unroll
+      for (int j = 0; j < kOutBytes / 16; ++j) {
+        const uint32_t g = 32 * j + lane;
+        uint4 v;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(buf_s + stage_slot(g)));
+        __stcs(out + g, v);
+      }
+      __syncwarp();
     } else {
-      a = static_cast<const float*>(w.absmax)[blk];
+      // ragged last chunk: element by element
+      const int64_t e0 = c0 + 32 * lane;
+      for (int i = 0; i < 32; ++i) {
+        const int64_t e = e0 + i;
+        if (e >= n) break;
+        const uint8_t byte = w.packed[e >> 1];
+        const int q = (e & 1) ? (byte & 15) : (byte >> 4);
+        const float v = __fmul_rn(tabs.nf4[q], a);
+        if (sizeof(Tout) == 2) reinterpret_cast<__nv_bfloat16*>(y)[e] = __float2bfloat16_rn(v);
+        else reinterpret_cast<float*>(y)[e] = v;
+      }
     }
-    float v[4];
-    v[0] = __fmul_rn(lut[(bytes >> 4) & 15][lane], a);
-    v[1] = __fmul_rn(lut[bytes & 15][lane], a);
-    v[2] = __fmul_rn(lut[(bytes >> 12) & 15][lane], a);
-    v[3] = __fmul_rn(lut[(bytes >> 8) & 15][lane], a);
-    store_quad(y, e0, n, v);
   }
 }
 
@@ -283,8 +332,7 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
 }
 
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st) {
-  const int64_t per_cta = static_cast<int64_t>(kDeqThreads / 32) * kDeqQuadRows * 128;
-  const int64_t ctas = (w.numel + per_cta - 1) / per_cta;
+  const int64_t ctas = (w.numel + kDeqPerCta - 1) / kDeqPerCta;
   if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ctas));
   const DecodeTables& dt = decode_tables();
