@@ -59,6 +59,29 @@ void build_thresholds(const float* codes, int n, float* thr) {
   if (n == 256) thr[255] = INFINITY;
 }
 
+// Bucket table for the quantizer's NF4 search: 64 buckets of width 1/32 over [-1, 1).
+void build_buckets(const float* thr, EncodeTables* e) {
+  e->bucket_ok = 1;
+  for (int k = 0; k < 64; ++k) {
+    const double lo = -1.0 + k / 32.0, hi = lo + 1.0 / 32.0;
+    int base = 0, inner = 0;
+    float t_in = 4.0f;
+    for (int j = 0; j < 15; ++j) {
+      const double t = thr[j];
+      if (t <= lo) ++base;
+      else if (t < hi) { ++inner; t_in = thr[j]; }
+      if (std::fabs(t - lo) < 1.0 / (1 << 18) || std::fabs(t - hi) < 1.0 / (1 << 18)) e->bucket_ok = 0;
+    }
+    if (inner > 1) e->bucket_ok = 0;
+    e->nf4_bcode[k] = base;
+    // band of +-2^-19 (relative) around the threshold: wider than the error of
+    // x * RN(1/a) against RN(x / a) (a few ulp)
+    const double t = t_in, w = std::fabs(t) / (1 << 19);
+    e->nf4_blo[k] = t_in == 4.0f ? 4.0f : static_cast<float>(t - w);
+    e->nf4_bhi[k] = t_in == 4.0f ? 4.0f : static_cast<float>(t + w);
+  }
+}
+
 struct Tables {
   DecodeTables dec;
   EncodeTables enc;
@@ -67,6 +90,7 @@ struct Tables {
     build_dyn8(dec.dyn8);
     build_thresholds(dec.nf4, 16, enc.nf4_thr);
     build_thresholds(dec.dyn8, 256, enc.dyn8_thr);
+    build_buckets(enc.nf4_thr, &enc);
   }
 };
 

@@ -55,6 +55,15 @@ struct DecodeTables {
 struct EncodeTables {
   float nf4_thr[16];   // 15 used
   float dyn8_thr[256]; // 255 used
+  // Bucketed NF4 search over v in [-1, 1): bucket k covers [-1 + k/32, -1 + (k+1)/32);
+  // for a value q within a few ulp of v, code(v) = bcode[k] + (q >= bhi[k]) unless
+  // blo[k] <= q < bhi[k] (the band around the bucket's one threshold; blo = bhi = 4
+  // when none falls inside).  Valid only when bucket_ok (at most one threshold per
+  // bucket, none near an edge).
+  float nf4_blo[64];
+  float nf4_bhi[64];
+  int32_t nf4_bcode[64];
+  int32_t bucket_ok;
 };
 
 const DecodeTables& decode_tables();

@@ -40,77 +40,161 @@ __device__ __forceinline__ int dyn8_encode(float v, const float* thr) {
   return c;
 }
 
-__device__ __forceinline__ void load_quad(const float* x, int64_t e0, int64_t n, float v[4]) {
-  if (e0 + 3 < n) {
-    const float4 t = __ldcs(reinterpret_cast<const float4*>(x + e0));
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-  } else {
+// Loads of the encode kernel: a warp reads 1024 consecutive elements with coalesced
+// 16-byte loads (zero past numel) and parks them in a swizzled shared buffer, from which
+// lane l takes its own 32 elements (half a 64-element block).
+template <typename Tin>
+__device__ __forceinline__ void stage_chunk(const Tin* __restrict__ x, int64_t numel, int64_t c0, int lane,
+                                            uint32_t buf_s) {
+  constexpr int kVec = 16 / sizeof(Tin);                 // elements per 16-byte load
+  constexpr int kRounds = 1024 / (32 * kVec);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (e0 + i < n) ? x[e0 + i] : 0.0f;
+  for (int j = 0; j < kRounds; ++j) {
+    const uint32_t g = 32 * j + lane;                    // 16-byte slot within the chunk
+    const int64_t e = c0 + static_cast<int64_t>(g) * kVec;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (e + kVec <= numel) {
+      v = __ldcs(reinterpret_cast<const uint4*>(x + e));
+    } else if (e < numel) {
+      Tin tmp[kVec];
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) tmp[i] = (e + i < numel) ? x[e + i] : Tin(0.0f);
+      v = *reinterpret_cast<const uint4*>(tmp);
+    }
+    const uint32_t row = g >> 3, col = g & 7;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf_s + (((row << 3) | (col ^ (row & 7))) << 4)),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
   }
 }
 
-__device__ __forceinline__ void load_quad(const __nv_bfloat16* x, int64_t e0, int64_t n, float v[4]) {
-  if (e0 + 3 < n) {
-    const uint2 t = __ldcs(reinterpret_cast<const uint2*>(x + e0));
-    v[0] = __uint_as_float(t.x << 16);
-    v[1] = __uint_as_float(t.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(t.y << 16);
-    v[3] = __uint_as_float(t.y & 0xFFFF0000u);
-  } else {
+// Lane's 32 elements as fp32 from the staging buffer.
+template <typename Tin>
+__device__ __forceinline__ void lane_values(uint32_t buf_s, int lane, float (&v)[32]) {
+  constexpr int kVec = 16 / sizeof(Tin);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (e0 + i < n) ? __bfloat162float(x[e0 + i]) : 0.0f;
+  for (int i = 0; i < 32 / kVec; ++i) {
+    const uint32_t g = static_cast<uint32_t>(lane) * (32 / kVec) + i;
+    const uint32_t row = g >> 3, col = g & 7;
+    uint4 u;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                 : "r"(buf_s + (((row << 3) | (col ^ (row & 7))) << 4)));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if (sizeof(Tin) == 4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[4 * i + k] = __uint_as_float(w[k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+        v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    }
   }
 }
 
+// Block pass: absmax, 4-bit codes and packing for one nested group (256 blocks) per CTA;
+// with double quantization also the float64 pairwise-tree sum of the group's absmax.
+// Codes: q = x * RN(1/a) picks a bucket of the 64-bucket table; when q lies within
+// 1e-6 (relative) of the bucket's threshold, or 1/a overflows, the code is taken from
+// the exact quotient RN(x / a) instead, so the result is always that of the IEEE
+// division.
 template <typename Tin>
 __global__ void __launch_bounds__(kQuantThreads)
 nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict__ packed,
                   float* __restrict__ absmax, double* __restrict__ group_sum, EncodeTables tabs,
                   int* status) {
   __shared__ float thr[16];
+  __shared__ float2 band[64];   // (lo, hi)
+  __shared__ int32_t bcode[64];
   __shared__ double gsum[kNested];
+  // 4 KB of staging per warp: one fp32 chunk at a time, or both bf16 chunks at once
+  __shared__ __align__(16) uint8_t stage[kQuantThreads / 32][4096];
+  constexpr int kChunkBytes = 1024 * static_cast<int>(sizeof(Tin));
+  constexpr bool kBoth = 2 * kChunkBytes <= 4096;
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
+  if (threadIdx.x < 64) {
+    band[threadIdx.x] = make_float2(tabs.nf4_blo[threadIdx.x], tabs.nf4_bhi[threadIdx.x]);
+    bcode[threadIdx.x] = tabs.nf4_bcode[threadIdx.x];
+  }
   __syncthreads();
-
+  const bool fast_ok = tabs.bucket_ok != 0;   // bucket table usable
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t group_base = static_cast<int64_t>(blockIdx.x) * kGroupElems;
+  const uint32_t buf0 = static_cast<uint32_t>(__cvta_generic_to_shared(stage[warp]));
+  // warp w handles elements [w*2048, (w+1)*2048) of the group: two 1024-element chunks
+  const int64_t wbase = group_base + warp * 2048;
+  stage_chunk(x, numel, wbase, lane, buf0);
+  if (kBoth) stage_chunk(x, numel, wbase + 1024, lane, buf0 + kChunkBytes);
+  __syncwarp();
   bool nonfinite = false;
-
-#pragma unroll 4
-  for (int u = 0; u < kQuadRowsPerWarp; ++u) {
-    const int64_t e0 = group_base + warp * (kQuadRowsPerWarp * 128) + u * 128 + 4 * lane;
-    float v[4];
-    load_quad(x, e0, numel, v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) nonfinite |= !isfinite(v[i]);
-    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-
-    int code[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      int c = kNf4ZeroCode;
-      if (m > 0.0f) c = nf4_encode(__fdiv_rn(v[i], m), thr);
-      code[i] = (e0 + i < numel) ? c : 0;   // pad nibble of an odd tail is 0
+#pragma unroll 1
+  for (int u = 0; u < 2; ++u) {
+    const int64_t e0 = wbase + u * 1024 + 32 * lane;    // lane's first element
+    if (!kBoth && u == 1) {
+      __syncwarp();
+      stage_chunk(x, numel, wbase + 1024, lane, buf0);
+      __syncwarp();
     }
-    const uint32_t b0 = static_cast<uint32_t>((code[0] << 4) | code[1]);
-    const uint32_t b1 = static_cast<uint32_t>((code[2] << 4) | code[3]);
-    const int64_t byte0 = e0 >> 1;
-    if (e0 + 3 < numel) {
-      *reinterpret_cast<uint16_t*>(packed + byte0) = static_cast<uint16_t>(b0 | (b1 << 8));
+    float v[32];
+    lane_values<Tin>(kBoth ? buf0 + u * kChunkBytes : buf0, lane, v);
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mb = max(mb, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));  // the lane pair holds one block
+    nonfinite |= mb >= 0x7F800000u;
+    const float a = __uint_as_float(mb);
+    const float r = __frcp_rn(a);
+    uint32_t words[4];
+    if (a == 0.0f) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) words[w] = 0x77777777u;     // every code is that of 0.0
+    } else {
+      bool exact = !(fast_ok && isfinite(r));
+      if (!exact) {
+        bool unsure = false;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) words[w] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float q = v[i] * r;
+          const float qc = fminf(fmaxf(q, -1.0f), 0.999f);
+          const uint32_t k = (__float_as_uint(qc + 3.0f) >> 17) & 63u;
+          const float2 b = band[k];
+          unsure |= (q >= b.x) & (q < b.y);
+          const uint32_t c = static_cast<uint32_t>(bcode[k]) + (q >= b.y ? 1u : 0u);
+          words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
+        }
+        exact = unsure;
+      }
+      if (exact) {  // rare: redo the lane with the IEEE quotient
+#pragma unroll
+        for (int w = 0; w < 4; ++w) words[w] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t c = static_cast<uint32_t>(nf4_encode(__fdiv_rn(v[i], a), thr));
+          words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
+        }
+      }
+    }
+    if (e0 + 31 >= numel) {  // ragged tail: codes past numel are 0 (the pad nibble of an odd tail)
+      const int64_t vc = numel - e0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i >= vc) words[i >> 3] &= ~(0xFu << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4)));
+    }
+    if (e0 + 31 < numel) {
+      *reinterpret_cast<uint4*>(packed + (e0 >> 1)) = make_uint4(words[0], words[1], words[2], words[3]);
     } else if (e0 < numel) {
-      packed[byte0] = static_cast<uint8_t>(b0);
-      if (e0 + 2 < numel) packed[byte0 + 1] = static_cast<uint8_t>(b1);
+      const int64_t nbytes = (numel - e0 + 1) / 2;
+      for (int64_t b = 0; b < nbytes; ++b) packed[(e0 >> 1) + b] = static_cast<uint8_t>(words[b >> 2] >> (8 * (b & 3)));
     }
-    const int block_in_group = warp * 32 + 2 * u + (lane >> 4);
-    if ((lane & 15) == 0) {
-      if (e0 < numel) absmax[e0 >> 6] = m;
-      gsum[block_in_group] = (e0 < numel) ? static_cast<double>(m) : 0.0;
+    const int block_in_group = warp * 32 + u * 16 + (lane >> 1);
+    if ((lane & 1) == 0) {
+      if (e0 < numel) absmax[e0 >> 6] = a;
+      gsum[block_in_group] = (e0 < numel) ? static_cast<double>(a) : 0.0;
     }
   }
   if (nonfinite) atomicCAS(status, 0, static_cast<int>(NF4_ERR_NONFINITE));
