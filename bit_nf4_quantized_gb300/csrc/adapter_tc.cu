@@ -166,7 +166,7 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 
 // out = scale * sum over slices (fixed order).  Optional outputs:
 //   f32 [rows][r] (or transposed [r][rows] when f32_t), bf16(scale_b * v) [rows][rp]
-//   zero-padded, bf16(v) transposed [nq][ldt] (entries past rows / r left as staged zeros).
+//   zero-padded, bf16(v) transposed [nq][ldt] (entries past rows / r must already be zero).
 __global__ void finish_partials(const float* __restrict__ partial, int nsplit, int64_t rows, int r, float scale,
                                 float* __restrict__ f32, int f32_t, __nv_bfloat16* __restrict__ b_rows, int rp,
                                 float scale_b, __nv_bfloat16* __restrict__ b_t, int64_t ldt) {
@@ -188,28 +188,8 @@ __global__ void finish_partials(const float* __restrict__ partial, int nsplit, i
   if (b_rows) b_rows[row * rp + j] = __float2bfloat16_rn(j < r ? scale_b * v : 0.0f);
 }
 
-// dst[j][c] = bf16(src[c][j]) for j < r, c < cols; zero for j in [r, nq) or c in [cols, ldd).
-__global__ void stage_t_bf16(const float* __restrict__ src, int64_t cols, int r, int nq, int64_t ldd,
-                             __nv_bfloat16* __restrict__ dst) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<int64_t>(nq) * ldd) return;
-  const int j = static_cast<int>(i / ldd);
-  const int64_t c = i % ldd;
-  dst[i] = __float2bfloat16_rn((j < r && c < cols) ? src[c * r + j] : 0.0f);
-}
-
-// dst[j][c] = bf16(src[j][c]) for j < r; zero rows j in [r, nq).
-__global__ void stage_rows_direct_bf16(const float* __restrict__ src, int64_t cols, int r, int nq,
-                                       __nv_bfloat16* __restrict__ dst) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<int64_t>(nq) * cols) return;
-  const int j = static_cast<int>(i / cols);
-  dst[i] = __float2bfloat16_rn(j < r ? src[i] : 0.0f);
-}
-
 int nq_of(int r) { return (r + 15) / 16 * 16; }
 int rp_of(int r) { return (r + 63) / 64 * 64; }
-int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
 size_t al(size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); }
 unsigned blocks(int64_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
@@ -217,17 +197,31 @@ struct Plan {
   int tiles, total_steps, sps, nsplit;
 };
 
-Plan plan(int64_t rows, int64_t red) {
+// Slices per row tile: as many as keep tiles * slices within `target` resident CTAs
+// (two per SM fit); workspace is sized with the largest target any device uses.
+Plan plan(int64_t rows, int64_t red, int target = kTargetCtas) {
   Plan pl;
   pl.tiles = static_cast<int>((rows + kRowsT - 1) / kRowsT);
   pl.total_steps = static_cast<int>((red + kBKa - 1) / kBKa);
-  int ns = (kTargetCtas + pl.tiles - 1) / pl.tiles;
+  int ns = target / pl.tiles;
   if (ns > kMaxSplit) ns = kMaxSplit;
   if (ns > pl.total_steps) ns = pl.total_steps;
   if (ns < 1) ns = 1;
   pl.sps = (pl.total_steps + ns - 1) / ns;
   pl.nsplit = (pl.total_steps + pl.sps - 1) / pl.sps;
   return pl;
+}
+
+int resident_ctas() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    n = sms > 0 ? 2 * sms : 2;
+    if (n > kTargetCtas) n = kTargetCtas;
+  }
+  return n;
 }
 
 size_t partial_bytes(int64_t rows, int64_t red, int r) {
@@ -239,7 +233,7 @@ size_t partial_bytes(int64_t rows, int64_t red, int r) {
 cudaError_t run_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
                      int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
                      cudaStream_t st) {
-  const Plan pl = plan(rows, red);
+  const Plan pl = plan(rows, red, resident_ctas());
   const int nq = nq_of(r);
   CUtensorMap tx, tq;
   bool ok = mn_major ? make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, x_inner, x_outer, 2 * x_inner, 64, 64,
@@ -277,83 +271,23 @@ cudaError_t run_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_ma
 
 }  // namespace
 
-size_t adapter_fwd_ws_bytes(int64_t M, int64_t, int64_t K, int r) {
-  return al(2 * static_cast<size_t>(nq_of(r)) * K) + partial_bytes(M, K, r);
-}
+int adapter_nq(int r) { return nq_of(r); }
 
-size_t adapter_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
-  const size_t nq = nq_of(r);
-  size_t part = partial_bytes(M, N, r);
-  const size_t p2 = partial_bytes(N, M, r), p3 = partial_bytes(K, M, r);
-  if (p2 > part) part = p2;
-  if (p3 > part) part = p3;
-  return al(2 * nq * N) + 2 * al(2 * nq * pad8(M)) + part;
-}
+size_t adapter_partial_bytes(int64_t rows, int64_t red, int r) { return partial_bytes(rows, red, r); }
 
-cudaError_t adapter_forward(const LinearArgs& a, const void* x, const float* A, float* T, __nv_bfloat16* sTp,
-                            void* ws, int* status, cudaStream_t st) {
+cudaError_t adapter_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
+                         int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
+                         cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const int nq = nq_of(a.r);
-  auto* Aq = static_cast<__nv_bfloat16*>(ws);
-  auto* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + al(2 * static_cast<size_t>(nq) * a.K));
-  stage_rows_direct_bf16<<<blocks(static_cast<int64_t>(nq) * a.K), 256, 0, st>>>(A, a.K, a.r, nq, Aq);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  int ns = 0;
-  if ((e = run_pass(x, a.K, a.M, false, Aq, a.K, a.r, a.M, a.K, partial, status, &ns, st)) != cudaSuccess) return e;
-  const int rp = rp_of(a.r);
-  finish_partials<<<blocks(a.M * rp), 256, 0, st>>>(partial, ns, a.M, a.r, 1.0f, T, 0, sTp, rp, a.s, nullptr, 0);
-  note_launch();
-  return cudaGetLastError();
+  return run_pass(X, x_inner, x_outer, mn_major, Q, q_cols, r, rows, red, partial, status, nsplit, st);
 }
 
-cudaError_t adapter_backward_pre(const LinearArgs& a, const void* dy, const float* T, const float* B, float* G,
-                                 __nv_bfloat16* sGp, float* dB, void* ws, int* status, cudaStream_t st) {
+cudaError_t adapter_finish(const float* partial, int nsplit, int64_t rows, int r, float scale, float* f32, int f32_t,
+                           __nv_bfloat16* b_rows, int rp, float scale_b, __nv_bfloat16* b_t, int64_t ldt,
+                           cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const int nq = nq_of(a.r);
-  const int64_t Mp = pad8(a.M);
-  char* w = static_cast<char*>(ws);
-  auto* Bt = reinterpret_cast<__nv_bfloat16*>(w);
-  auto* Tt = reinterpret_cast<__nv_bfloat16*>(w + al(2 * static_cast<size_t>(nq) * a.N));
-  auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + al(2 * static_cast<size_t>(nq) * a.N) + al(2 * nq * Mp));
-  auto* partial = reinterpret_cast<float*>(w + al(2 * static_cast<size_t>(nq) * a.N) + 2 * al(2 * nq * Mp));
-  stage_t_bf16<<<blocks(nq * a.N), 256, 0, st>>>(B, a.N, a.r, nq, a.N, Bt);
-  note_launch();
-  stage_t_bf16<<<blocks(nq * Mp), 256, 0, st>>>(T, a.M, a.r, nq, Mp, Tt);
-  note_launch();
-  // Gt's padding (rows r..nq, columns M..Mp) must read as zero; finish_partials fills the rest
-  stage_t_bf16<<<blocks(nq * Mp), 256, 0, st>>>(T, 0, 0, nq, Mp, Gt);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  int ns = 0;
-  const int rp = rp_of(a.r);
-  // G = dY B: rows M, reduction over N along dY's rows (K-major)
-  if ((e = run_pass(dy, a.N, a.M, false, Bt, a.N, a.r, a.M, a.N, partial, status, &ns, st)) != cudaSuccess) return e;
-  finish_partials<<<blocks(a.M * rp), 256, 0, st>>>(partial, ns, a.M, a.r, 1.0f, G, 0, sGp, rp, a.s, Gt, Mp);
-  note_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // dB = s dY^T T: rows N, reduction over M down dY's columns (MN-major)
-  if ((e = run_pass(dy, a.N, a.M, true, Tt, Mp, a.r, a.N, a.M, partial, status, &ns, st)) != cudaSuccess) return e;
-  finish_partials<<<blocks(a.N * a.r), 256, 0, st>>>(partial, ns, a.N, a.r, a.s, dB, 0, nullptr, 0, 0.0f, nullptr, 0);
-  note_launch();
-  return cudaGetLastError();
-}
-
-cudaError_t adapter_backward_post(const LinearArgs& a, const void* x, float* dA, void* ws, int* status,
-                                  cudaStream_t st) {
-  KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const int nq = nq_of(a.r);
-  const int64_t Mp = pad8(a.M);
-  char* w = static_cast<char*>(ws);
-  auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + al(2 * static_cast<size_t>(nq) * a.N) + al(2 * nq * Mp));
-  auto* partial = reinterpret_cast<float*>(w + al(2 * static_cast<size_t>(nq) * a.N) + 2 * al(2 * nq * Mp));
-  int ns = 0;
-  // dA = s G^T x: rows K, reduction over M down x's columns (MN-major)
-  cudaError_t e = run_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, partial, status, &ns, st);
-  if (e != cudaSuccess) return e;
-  finish_partials<<<blocks(a.K * a.r), 256, 0, st>>>(partial, ns, a.K, a.r, a.s, dA, 1, nullptr, 0, 0.0f, nullptr, 0);
+  finish_partials<<<blocks(rows * (b_rows ? rp : r)), 256, 0, st>>>(partial, nsplit, rows, r, scale, f32, f32_t,
+                                                                      b_rows, rp, scale_b, b_t, ldt);
   note_launch();
   return cudaGetLastError();
 }

@@ -20,14 +20,17 @@
 //               MN-major for dX), through a per-block scaled lookup table;
 //   warps 10..13 epilogue: tcgen05.ld of the accumulator, bf16 stores.
 // The per-block scales a' = dyn8[code] * nested + offset are computed once per call
-// by block_scales_kernel and reach each stage by TMA next to the packed codes, so
-// the decoders never wait on global memory.
+// (prep.cu) into an fp32 [N][K/64 rounded up to 4] array and reach each stage by TMA
+// next to the packed codes, so the decoders never wait on global memory.
 // Two accumulators of 256 columns let the epilogue of one tile overlap the
 // main loop of the next.  Every mbarrier wait is bounded in time; a wait that
 // gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
 // freeing its TMEM.
+#include <algorithm>
+
 #include "linear_tc.cuh"
 #include "decode.cuh"
+#include "prep.cuh"
 #include "tc_ptx.cuh"
 
 namespace qnf4 {
@@ -45,7 +48,7 @@ constexpr int kPBytes = 4096;               // packed NF4 bytes per stage
 constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
 constexpr int kThreads = 448;                // 14 warps, roles below
 constexpr int kTmemCols = 512;
-constexpr int kScaleSlot = 1024;              // fwd: 128 fp32 scales; dX: 64 rows x 4 fp32
+constexpr int kScaleSlot = 2048;              // fwd: 128 rows x 4 fp32; dX: 64 rows x 4 fp32
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStages * kScaleSlot + 256;
 static_assert(20 * 8 + 8 <= 256, "barrier block");
 
@@ -68,43 +71,6 @@ struct GemmParams {
   __nv_bfloat16* out;  // [M, F]
   int* status;
 };
-
-// Block scales a' = dyn8[code] * nested + offset (two roundings) or the fp32 absmax, one
-// per 64-element block, laid out so each stage's 128 scales are one TMA box:
-//   forward (mode 0): out[kb * N + n]        (a row of 128 consecutive n per stage)
-//   dX (mode 1):      out[n * ldk + kb]      (ldk = K/64 rounded up to 4; 64 rows x 4 per stage)
-// Entries past the matrix are never read as data: the TMA box zero-fills them.
-__global__ void block_scales_kernel(Nf4View w, int64_t N, int64_t K, int mode, int64_t ldk,
-                                    float* __restrict__ out, DecodeTables tabs) {
-  __shared__ float dyn8[256];
-  dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
-  __syncthreads();
-  const int64_t kbn = K / kBlock;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t total = mode == 0 ? kbn * N : N * ldk;
-  if (i >= total) return;
-  int64_t n, kb;
-  if (mode == 0) {
-    kb = i / N;
-    n = i % N;
-  } else {
-    n = i / ldk;
-    kb = i % ldk;
-    if (kb >= kbn) {
-      out[i] = 0.0f;
-      return;
-    }
-  }
-  const int64_t blk = n * kbn + kb;
-  float a;
-  if (w.dq) {
-    const uint32_t code = static_cast<const uint8_t*>(w.absmax)[blk];
-    a = __fadd_rn(__fmul_rn(dyn8[code], w.nested[blk >> 8]), *w.offset);
-  } else {
-    a = static_cast<const float*>(w.absmax)[blk];
-  }
-  out[i] = a;
-}
 
 // Warp roles:
 //   0       TMA producer (lane 0)
@@ -184,10 +150,10 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
         if (!mbar_wait(bar(8 + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
         if (step < p.red_steps) {
           // codes and scales first: the decoders start on them while the token tile streams
-          mbar_expect_tx(bar(16 + s), kPBytes + (p.mode == 0 ? kTileF * 4 : 64 * 16));
+          mbar_expect_tx(bar(16 + s), kPBytes + (p.mode == 0 ? kTileF * 16 : 64 * 16));
           if (p.mode == 0) {
             tma_load_2d(stage_p(s), &tm_packed, bar(16 + s), step * (kBK / 2), f0);
-            tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), f0, step);
+            tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), step & ~3, f0);
           } else {
             tma_load_2d(stage_p(s), &tm_packed, bar(16 + s), f0 / 2, step * kBK);
             tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), (f0 / kBlock) & ~3, step * kBK);
@@ -266,7 +232,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
         // forward: scale of row `row`; dX: row (row & 63) of a 64 x 4 box whose first
         // column is the 128-feature tile's first block rounded down to a multiple of 4
         const int64_t f0 = tile_f(blockIdx.x + (it / steps) * gridDim.x) * kTileF;
-        const float a = (p.mode == 0) ? scales[s * (kScaleSlot / 4) + row]
+        const float a = (p.mode == 0) ? scales[s * (kScaleSlot / 4) + row * 4 + (step & 3)]
                                       : scales[s * (kScaleSlot / 4) + (row & 63) * 4 +
                                                static_cast<int>((f0 / kBlock) & 3) + (row >> 6)];
         build_lut(a, L, H);
@@ -329,26 +295,6 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   }
 }
 
-// ---- adapter staging: bf16 operands of the LoRA slab, zero-padded to rp columns ------------
-
-__global__ void stage_rows_bf16(const float* __restrict__ src, int64_t rows, int r, int rp, float scale,
-                                __nv_bfloat16* __restrict__ dst) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows * rp) return;
-  const int64_t row = i / rp;
-  const int j = static_cast<int>(i % rp);
-  dst[i] = __float2bfloat16_rn(j < r ? scale * src[row * r + j] : 0.0f);
-}
-
-__global__ void stage_transposed_bf16(const float* __restrict__ A, int64_t K, int r, int rp,
-                                      __nv_bfloat16* __restrict__ dst) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= K * rp) return;
-  const int64_t k = i / rp;
-  const int j = static_cast<int>(i % rp);
-  dst[i] = __float2bfloat16_rn(j < r ? A[static_cast<int64_t>(j) * K + k] : 0.0f);
-}
-
 // ---- host side --------------------------------------------------------------------------
 
 int padded_rank(int r) { return (r + kBK - 1) / kBK * kBK; }
@@ -378,38 +324,56 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUten
   return cudaGetLastError();
 }
 
-cudaError_t stage_rows(const float* src, int64_t rows, int r, float scale, __nv_bfloat16* dst, cudaStream_t st) {
-  const int rp = padded_rank(r);
-  const int64_t n = rows * rp;
-  stage_rows_bf16<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(src, rows, r, rp, scale, dst);
-  note_launch();
-  return cudaGetLastError();
-}
-
 int64_t scale_ld(int64_t K) { return (K / kBlock + 3) / 4 * 4; }
+int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
 
-size_t scales_bytes(int64_t N, int64_t K, int mode) {
-  return a1024(sizeof(float) * static_cast<size_t>(N) * (mode == 0 ? K / kBlock : scale_ld(K)));
+// Block-scale job for the prep launch and the tensor map each GEMM stage reads it by.
+PrepJob scales_job(const LinearArgs& a, float* out) {
+  PrepJob j{};
+  j.kind = kBlockScales;
+  j.width = scale_ld(a.K);
+  j.fdst = out;
+  j.count = a.N * j.width;
+  return j;
 }
 
-// Block scales of W for one GEMM call, and the tensor map each stage's box comes from.
-cudaError_t prepare_scales(const LinearArgs& a, int mode, float* out, CUtensorMap* map, cudaStream_t st) {
-  const int64_t kbn = a.K / kBlock, ldk = scale_ld(a.K);
-  const int64_t n = mode == 0 ? kbn * a.N : a.N * ldk;
-  {
-    KernelTimer timer(NF4_TIME_ADAPTER, st);
-    block_scales_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(a.W, a.N, a.K, mode, ldk, out,
-                                                                                decode_tables());
-    note_launch();
+bool scales_map(const LinearArgs& a, int mode, const float* sc, CUtensorMap* map) {
+  const int64_t ldk = scale_ld(a.K);
+  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sc, ldk, a.N, 4 * ldk, 4, mode == 0 ? kTileF : 64,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Workspace layouts (every part 1024-byte aligned).
+struct FwdWs {
+  size_t sTp, Bp, Aq, part, scale, total;
+  FwdWs(int64_t M, int64_t N, int64_t K, int r) {
+    const size_t rp = padded_rank(r), nq = adapter_nq(r);
+    sTp = 0;
+    Bp = sTp + a1024(2 * rp * M);
+    Aq = Bp + a1024(2 * rp * N);
+    part = Aq + a1024(2 * nq * K);
+    scale = part + a1024(adapter_partial_bytes(M, K, r));
+    total = scale + a1024(4 * static_cast<size_t>(N) * scale_ld(K));
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const bool ok = mode == 0 ? make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, a.N, kbn, 4 * a.N, kTileF, 1,
-                                       CU_TENSOR_MAP_SWIZZLE_NONE)
-                            : make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, ldk, a.N, 4 * ldk, 4, 64,
-                                       CU_TENSOR_MAP_SWIZZLE_NONE);
-  return ok ? cudaSuccess : cudaErrorInvalidValue;
-}
+};
+
+struct BwdWs {
+  size_t sGp, ApT, Bt, Tt, Gt, part, scale, total;
+  BwdWs(int64_t M, int64_t N, int64_t K, int r) {
+    const size_t rp = padded_rank(r), nq = adapter_nq(r), Mp = pad8(M);
+    size_t pb = adapter_partial_bytes(M, N, r);
+    pb = std::max(pb, adapter_partial_bytes(N, M, r));
+    pb = std::max(pb, adapter_partial_bytes(K, M, r));
+    sGp = 0;
+    ApT = sGp + a1024(2 * rp * M);
+    Bt = ApT + a1024(2 * rp * K);
+    Tt = Bt + a1024(2 * nq * N);
+    Gt = Tt + a1024(2 * nq * Mp);
+    part = Gt + a1024(2 * nq * Mp);
+    scale = part + a1024(pb);
+    total = scale + a1024(4 * static_cast<size_t>(N) * scale_ld(K));
+  }
+};
 
 GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   GemmParams p{};
@@ -435,33 +399,49 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
 
 }  // namespace
 
-size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
-  const size_t rp = padded_rank(r);
-  return a1024(2 * rp * M) + a1024(2 * rp * N) + a1024(adapter_fwd_ws_bytes(M, N, K, r)) + scales_bytes(N, K, 0);
-}
+size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return FwdWs(M, N, K, r).total; }
 
-size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) {
-  const size_t rp = padded_rank(r);
-  return a1024(2 * rp * M) + a1024(2 * rp * K) + a1024(adapter_bwd_ws_bytes(M, N, K, r)) + scales_bytes(N, K, 1);
-}
+size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return BwdWs(M, N, K, r).total; }
 
+// Forward: prep (A and B in bf16, block scales) -> T = x A^T (skinny tcgen05) ->
+// T and bf16(s T) -> NF4 GEMM with the (s T) B^T slab.
 cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y, float* T,
                        void* ws, int* status, cudaStream_t st) {
-  const int rp = padded_rank(a.r);
-  auto* sTp = static_cast<__nv_bfloat16*>(ws);
-  auto* Bp = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M));
-  void* aws = static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M) +
-              a1024(2 * static_cast<size_t>(rp) * a.N);
-  auto* sc = reinterpret_cast<float*>(static_cast<char*>(aws) + a1024(adapter_fwd_ws_bytes(a.M, a.N, a.K, a.r)));
-  cudaError_t e = adapter_forward(a, x, A, T, sTp, aws, status, st);
-  if (e != cudaSuccess) return e;
-  CUtensorMap scale;
-  if ((e = prepare_scales(a, 0, sc, &scale, st)) != cudaSuccess) return e;
+  const FwdWs L(a.M, a.N, a.K, a.r);
+  char* w = static_cast<char*>(ws);
+  auto* sTp = reinterpret_cast<__nv_bfloat16*>(w + L.sTp);
+  auto* Bp = reinterpret_cast<__nv_bfloat16*>(w + L.Bp);
+  auto* Aq = reinterpret_cast<__nv_bfloat16*>(w + L.Aq);
+  auto* part = reinterpret_cast<float*>(w + L.part);
+  auto* sc = reinterpret_cast<float*>(w + L.scale);
+  const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
+  PrepBuilder prep(a.W, a.K);
   {
-    KernelTimer timer(NF4_TIME_ADAPTER, st);
-    if ((e = stage_rows(B, a.N, a.r, 1.0f, Bp, st)) != cudaSuccess) return e;
+    PrepJob j{};
+    j.kind = kStageRowsDirect;   // A as the skinny pass's Q: [nq][K]
+    j.r = a.r;
+    j.src = A;
+    j.dst = Aq;
+    j.cols = a.K;
+    j.count = static_cast<int64_t>(nq) * a.K;
+    prep.add(j);
+    PrepJob b{};
+    b.kind = kStageRows;         // B as the slab's A operand: [N][rp]
+    b.r = a.r;
+    b.width = rp;
+    b.scale = 1.0f;
+    b.src = B;
+    b.dst = Bp;
+    b.count = a.N * rp;
+    prep.add(b);
+    prep.add(scales_job(a, sc));
   }
-  CUtensorMap tok, packed, slab_f, slab_t;
+  cudaError_t e = prep.launch(st);
+  if (e != cudaSuccess) return e;
+  int ns = 0;
+  if ((e = adapter_pass(x, a.K, a.M, false, Aq, a.K, a.r, a.M, a.K, part, status, &ns, st)) != cudaSuccess) return e;
+  if ((e = adapter_finish(part, ns, a.M, a.r, 1.0f, T, 0, sTp, rp, a.s, nullptr, 0, st)) != cudaSuccess) return e;
+  CUtensorMap tok, packed, slab_f, slab_t, scale;
   bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kBK, kTileT,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kBK / 2, kTileF,
@@ -470,31 +450,71 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
                       CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kBK, kTileT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && scales_map(a, 0, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   return launch_gemm(base_params(a, 0, y, status), tok, packed, slab_f, slab_t, scale, st);
 }
 
+// Backward: prep (B^T, T^T, zeroed G^T, A^T in bf16, block scales) -> G = dY B ->
+// G, bf16(s G), bf16(G)^T -> dB = s dY^T T -> NF4 GEMM for dX with the (s G) A slab ->
+// dA = s G^T x.
 cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, const float* T, const float* A,
                         const float* B, void* dx, float* dA, float* dB, float* G, void* ws, int* status,
                         cudaStream_t st) {
-  const int rp = padded_rank(a.r);
-  auto* sGp = static_cast<__nv_bfloat16*>(ws);
-  auto* ApT = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M));
-  void* aws = static_cast<char*>(ws) + a1024(2 * static_cast<size_t>(rp) * a.M) +
-              a1024(2 * static_cast<size_t>(rp) * a.K);
-  auto* sc = reinterpret_cast<float*>(static_cast<char*>(aws) + a1024(adapter_bwd_ws_bytes(a.M, a.N, a.K, a.r)));
-  cudaError_t e = adapter_backward_pre(a, dy, T, B, G, sGp, dB, aws, status, st);
-  if (e != cudaSuccess) return e;
-  CUtensorMap scale;
-  if ((e = prepare_scales(a, 1, sc, &scale, st)) != cudaSuccess) return e;
+  const BwdWs L(a.M, a.N, a.K, a.r);
+  char* w = static_cast<char*>(ws);
+  auto* sGp = reinterpret_cast<__nv_bfloat16*>(w + L.sGp);
+  auto* ApT = reinterpret_cast<__nv_bfloat16*>(w + L.ApT);
+  auto* Bt = reinterpret_cast<__nv_bfloat16*>(w + L.Bt);
+  auto* Tt = reinterpret_cast<__nv_bfloat16*>(w + L.Tt);
+  auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + L.Gt);
+  auto* part = reinterpret_cast<float*>(w + L.part);
+  auto* sc = reinterpret_cast<float*>(w + L.scale);
+  const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
+  const int64_t Mp = pad8(a.M);
+  PrepBuilder prep(a.W, a.K);
   {
-    KernelTimer timer(NF4_TIME_ADAPTER, st);
-    const int64_t n = a.K * rp;
-    stage_transposed_bf16<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(A, a.K, a.r, rp, ApT);
-    note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    PrepJob j{};
+    j.kind = kStageTransposed;   // B^T: [nq][N]
+    j.r = a.r;
+    j.width = a.N;
+    j.src = B;
+    j.dst = Bt;
+    j.cols = a.N;
+    j.count = static_cast<int64_t>(nq) * a.N;
+    prep.add(j);
+    PrepJob t = j;               // T^T: [nq][Mp]
+    t.width = Mp;
+    t.src = T;
+    t.dst = Tt;
+    t.cols = a.M;
+    t.count = static_cast<int64_t>(nq) * Mp;
+    prep.add(t);
+    PrepJob g = t;               // G^T starts zero; the G finish fills rows < r, columns < M
+    g.r = 0;
+    g.dst = Gt;
+    prep.add(g);
+    PrepJob c{};
+    c.kind = kStageColumns;      // A^T: [K][rp]
+    c.r = a.r;
+    c.width = rp;
+    c.src = A;
+    c.dst = ApT;
+    c.cols = a.K;
+    c.count = a.K * rp;
+    prep.add(c);
+    prep.add(scales_job(a, sc));
   }
-  CUtensorMap tok, packed, slab_f, slab_t;
+  cudaError_t e = prep.launch(st);
+  if (e != cudaSuccess) return e;
+  int ns = 0;
+  // G = dY B: rows M, reduction over N along dY's rows; also bf16(s G) and bf16(G)^T
+  if ((e = adapter_pass(dy, a.N, a.M, false, Bt, a.N, a.r, a.M, a.N, part, status, &ns, st)) != cudaSuccess) return e;
+  if ((e = adapter_finish(part, ns, a.M, a.r, 1.0f, G, 0, sGp, rp, a.s, Gt, Mp, st)) != cudaSuccess) return e;
+  // dB = s dY^T T: rows N, reduction over M down dY's columns
+  if ((e = adapter_pass(dy, a.N, a.M, true, Tt, Mp, a.r, a.N, a.M, part, status, &ns, st)) != cudaSuccess) return e;
+  if ((e = adapter_finish(part, ns, a.N, a.r, a.s, dB, 0, nullptr, 0, 0.0f, nullptr, 0, st)) != cudaSuccess) return e;
+  CUtensorMap tok, packed, slab_f, slab_t, scale;
   bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kBK, kTileT,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kBK, kBK,
@@ -503,10 +523,13 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
                       CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kBK, kTileT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && scales_map(a, 1, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
-  e = launch_gemm(base_params(a, 1, dx, status), tok, packed, slab_f, slab_t, scale, st);
-  if (e != cudaSuccess) return e;
-  return adapter_backward_post(a, x, dA, aws, status, st);
+  if ((e = launch_gemm(base_params(a, 1, dx, status), tok, packed, slab_f, slab_t, scale, st)) != cudaSuccess)
+    return e;
+  // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
+  if ((e = adapter_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, part, status, &ns, st)) != cudaSuccess) return e;
+  return adapter_finish(part, ns, a.K, a.r, a.s, dA, 1, nullptr, 0, 0.0f, nullptr, 0, st);
 }
 
 }  // namespace qnf4

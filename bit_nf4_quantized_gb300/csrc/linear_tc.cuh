@@ -15,17 +15,20 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G,
                         void* ws, int* status, cudaStream_t st);
 
-// adapter_tc.cu: the rank-r contractions on tcgen05 (workspace sizes and sequences).
-size_t adapter_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
-size_t adapter_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
-// T = x A^T (fp32) and sTp = bf16(s T) zero-padded to a multiple of 64 columns.
-cudaError_t adapter_forward(const LinearArgs& a, const void* x, const float* A, float* T, __nv_bfloat16* sTp,
-                            void* ws, int* status, cudaStream_t st);
-// G = dY B (fp32), sGp = bf16(s G) padded, dB = s dY^T T; keeps bf16(G)^T in ws for the dA pass.
-cudaError_t adapter_backward_pre(const LinearArgs& a, const void* dy, const float* T, const float* B, float* G,
-                                 __nv_bfloat16* sGp, float* dB, void* ws, int* status, cudaStream_t st);
-// dA = s G^T x, using the bf16(G)^T that adapter_backward_pre left in ws.
-cudaError_t adapter_backward_post(const LinearArgs& a, const void* x, float* dA, void* ws, int* status,
-                                  cudaStream_t st);
+// adapter_tc.cu: skinny tcgen05 products Out[rows, r] = X[rows, red] . Q[red, r] for the
+// rank-r contractions.  X is bf16 row-major with `x_inner` columns (the reduction runs
+// along its rows when mn_major == false, down its columns otherwise); Q is bf16
+// [nq][q_cols] (nq = r rounded up to 16).  Reduction slices write partial sums that
+// adapter_finish adds in a fixed order.
+int adapter_nq(int r);
+size_t adapter_partial_bytes(int64_t rows, int64_t red, int r);
+cudaError_t adapter_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
+                         int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
+                         cudaStream_t st);
+// Sum of the slices times `scale` into f32 ([rows][r], or [r][rows] when f32_t), and
+// optionally bf16(scale_b * sum) into b_rows [rows][rp] and bf16(sum) into b_t [nq][ldt].
+cudaError_t adapter_finish(const float* partial, int nsplit, int64_t rows, int r, float scale, float* f32, int f32_t,
+                           __nv_bfloat16* b_rows, int rp, float scale_b, __nv_bfloat16* b_t, int64_t ldt,
+                           cudaStream_t st);
 
 }  // namespace qnf4

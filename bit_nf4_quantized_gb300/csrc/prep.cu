@@ -1,0 +1,97 @@
+// Per-call operand staging for the bf16 QLoRA linear, in one launch: the bf16 copies of
+// the adapter factors in the layouts the tensor-core kernels read, and the fp32 block
+// scales a' of the weight ("Native model adaptation and NF4", "Fused GPU NF4 decodes
+// inside the matrix kernel": a' = dyn8[code] * nested + offset, two roundings).
+#include "prep.cuh"
+
+namespace qnf4 {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+__device__ __forceinline__ void split_index(uint64_t idx, uint64_t width, uint64_t* hi, uint64_t* lo) {
+  if (idx < (1ull << 32) && width < (1ull << 32)) {
+    const uint32_t q = static_cast<uint32_t>(idx) / static_cast<uint32_t>(width);
+    *hi = q;
+    *lo = static_cast<uint32_t>(idx) - q * static_cast<uint32_t>(width);
+  } else {
+    *hi = idx / width;
+    *lo = idx % width;
+  }
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
+  __shared__ float dyn8[256];
+  dyn8[threadIdx.x] = p.dyn8[threadIdx.x];
+  __syncthreads();
+  int j = 0;
+  while (j + 1 < p.n && blockIdx.x >= p.job[j + 1].first_block) ++j;
+  const PrepJob& jb = p.job[j];
+  const uint64_t idx = static_cast<uint64_t>(blockIdx.x - jb.first_block) * kPrepThreads + threadIdx.x;
+  if (idx >= static_cast<uint64_t>(jb.count)) return;
+  uint64_t a, b;
+  switch (jb.kind) {
+    case kStageRows: {         // dst[row][c] = bf16(scale * src[row][c]) for c < r, 0 up to width
+      split_index(idx, jb.width, &a, &b);
+      jb.dst[idx] = __float2bfloat16_rn(b < static_cast<uint64_t>(jb.r) ? jb.scale * jb.src[a * jb.r + b] : 0.0f);
+      break;
+    }
+    case kStageRowsDirect: {   // dst[j][c] = bf16(src[j][c]) for j < r, 0 for j in [r, width rows)
+      split_index(idx, jb.cols, &a, &b);
+      jb.dst[idx] = __float2bfloat16_rn(a < static_cast<uint64_t>(jb.r) ? jb.src[idx] : 0.0f);
+      break;
+    }
+    case kStageTransposed: {   // dst[j][c] = bf16(src[c][j]) for j < r, c < cols; row length width
+      split_index(idx, jb.width, &a, &b);
+      const bool in = a < static_cast<uint64_t>(jb.r) && b < static_cast<uint64_t>(jb.cols);
+      jb.dst[idx] = __float2bfloat16_rn(in ? jb.src[b * jb.r + a] : 0.0f);
+      break;
+    }
+    case kStageColumns: {      // dst[c][j] = bf16(src[j][c]) for j < r; rows of width entries
+      split_index(idx, jb.width, &a, &b);
+      jb.dst[idx] = __float2bfloat16_rn(b < static_cast<uint64_t>(jb.r) ? jb.src[b * jb.cols + a] : 0.0f);
+      break;
+    }
+    case kBlockScales: {       // fdst[n][kb] = a' of block (n, kb); 0 for kb in [K/64, width)
+      split_index(idx, jb.width, &a, &b);
+      float v = 0.0f;
+      if (b < static_cast<uint64_t>(p.kbn)) {
+        const uint64_t blk = a * static_cast<uint64_t>(p.kbn) + b;
+        if (p.w.dq) {
+          const uint32_t code = static_cast<const uint8_t*>(p.w.absmax)[blk];
+          v = __fadd_rn(__fmul_rn(dyn8[code], p.w.nested[blk >> 8]), *p.w.offset);
+        } else {
+          v = static_cast<const float*>(p.w.absmax)[blk];
+        }
+      }
+      jb.fdst[idx] = v;
+      break;
+    }
+    case kZeroWords:
+      jb.fdst[idx] = 0.0f;
+      break;
+    default:
+      break;
+  }
+}
+
+}  // namespace
+
+void PrepBuilder::add(const PrepJob& job) {
+  PrepJob j = job;
+  j.first_block = blocks_;
+  blocks_ += static_cast<int>((j.count + kPrepThreads - 1) / kPrepThreads);
+  jobs_.job[jobs_.n++] = j;
+}
+
+cudaError_t PrepBuilder::launch(cudaStream_t st) {
+  if (jobs_.n == 0) return cudaSuccess;
+  const DecodeTables& t = decode_tables();
+  for (int i = 0; i < 256; ++i) jobs_.dyn8[i] = t.dyn8[i];
+  KernelTimer timer(NF4_TIME_ADAPTER, st);
+  prep_kernel<<<blocks_, kPrepThreads, 0, st>>>(jobs_);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace qnf4

@@ -1,0 +1,55 @@
+// One-launch staging of the per-call operands of the bf16 QLoRA linear (prep.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace qnf4 {
+
+enum PrepKind {
+  kStageRows = 0,         // dst[row][c] = bf16(scale * src[row][c]), c < r; zero up to `width`
+  kStageRowsDirect = 1,   // dst[j][c] = bf16(src[j][c]) for j < r; zero rows up to `width` rows
+  kStageTransposed = 2,   // dst[j][c] = bf16(src[c][j]), j < r, c < cols; rows of `width`
+  kStageColumns = 3,      // dst[c][j] = bf16(src[j][c]) (src rows of `cols`), j < r; rows of `width`
+  kBlockScales = 4,       // fdst[n][kb] = a'(n, kb), kb < K/64; rows of `width` (multiple of 4)
+  kZeroWords = 5          // fdst[i] = 0 (as 32-bit words)
+};
+
+struct PrepJob {
+  int kind;
+  int r;
+  int64_t width;
+  float scale;
+  const float* src;
+  __nv_bfloat16* dst;
+  float* fdst;
+  int64_t cols;
+  int64_t count;          // elements written
+  int first_block;        // set by PrepBuilder
+};
+
+constexpr int kMaxPrepJobs = 6;
+
+struct PrepJobs {
+  PrepJob job[kMaxPrepJobs];
+  int n;
+  Nf4View w;
+  int64_t kbn;            // K / 64
+  float dyn8[256];
+};
+
+class PrepBuilder {
+ public:
+  explicit PrepBuilder(const Nf4View& w, int64_t K) {
+    jobs_.n = 0;
+    jobs_.w = w;
+    jobs_.kbn = K / kBlock;
+  }
+  void add(const PrepJob& job);
+  cudaError_t launch(cudaStream_t st);
+
+ private:
+  PrepJobs jobs_{};
+  int blocks_ = 0;
+};
+
+}  // namespace qnf4
