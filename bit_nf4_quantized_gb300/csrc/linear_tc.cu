@@ -5,23 +5,36 @@
 // kernel"): y = x W^T + s T B^T and dX = dY W + s G A, with W decoded from NF4 on
 // the device and never written to global memory.
 //
-// Kernel nf4_tc_gemm (one CTA per SM, persistent over output tiles):
+// Kernel nf4_tc_gemm: clusters of two CTAs on neighbouring SMs, persistent over tiles of
+// 256 output features x 256 tokens.  The pair runs 2-SM tcgen05.mma operations
+// (M = 256, N = 256, K = 16):
 //   D[f, t] (TMEM, fp32) = sum_c Wdec[f, c] * Tok[t, c]  +  sum_j Slab_A[f, j] * Slab_B[t, j]
-// with f = 128 output features per tile (the MMA's M), t = 256 tokens (the MMA's N):
 //   forward: f = rows of W (output features), c = k, Tok = x,  slab (B, s*T)
 //   dX:      f = columns of W (input features), c = n, Tok = dY, slab (A^T, s*G)
-// Warp roles (480 threads):
-//   warp 0      TMA producer: token tile (128B-swizzled) + packed NF4 tile per stage,
-//               or the two adapter slab tiles for the last (rank / 64) stages;
-//   warp 1      TMEM allocation; lane 0 issues tcgen05.mma and tcgen05.commit;
-//   warps 2..9  decoders in two groups of four that take alternate stages; a thread
-//               turns one 64-element NF4 block (one 128-byte row of the A tile) into
-//               bf16 in the swizzled layout the MMA reads (K-major for the forward,
-//               MN-major for dX), through a per-block scaled lookup table;
-//   warps 10..13 epilogue: tcgen05.ld of the accumulator, bf16 stores.
+// Each CTA decodes its own 128 feature rows of the A operand and loads one 128-token half
+// of the token tile; the even CTA issues the MMAs, which read both CTAs' shared memory and
+// write each CTA's 128 accumulator rows into its own TMEM.  So every SM receives half the
+// token bytes that a one-SM 128 x 256 tile would need for the same work.
+// The contraction advances in steps of 128 (two 64-deep sub-blocks, one NF4 block each),
+// then in 64-deep adapter slab steps.  Two rings of shared-memory buffers: one (kStages)
+// of what TMA brings per step (this CTA's token half, packed codes, block scales) and one
+// (kAStages) of bf16 A tiles (decoded weights, or the adapter factor for slab steps).
+// Warp roles (448 threads, in each CTA):
+//   warp 0      TMA producer: its half of the token tile (128B-swizzled) + packed NF4 tile
+//               and block scales per step, or its half of the s*T / s*G slab tile;
+//   warp 1      TMEM allocation (pair-wide); in the even CTA, lane 0 issues the MMAs; in
+//               the odd CTA, lane 0 forwards "A slot ready" to the even CTA once per step,
+//               so that the decoders only ever arrive on local barriers;
+//   warps 2..9  decoders: a thread turns one 64-element NF4 block (one 128-byte row of an
+//               A sub-block) into bf16 in the swizzled layout the MMA reads (K-major for the
+//               forward, MN-major for dX), through a per-block scaled lookup table; on slab
+//               steps they copy the bf16 adapter factor rows in from global memory;
+//   warps 10..13 epilogue: tcgen05.ld of this CTA's accumulator rows, bf16 stores.
+// Barriers that gate the MMA (stage full, A slot ready, accumulator drained) live in the
+// even CTA; the MMA completion is multicast to both CTAs.
 // The per-block scales a' = dyn8[code] * nested + offset are computed once per call
 // (prep.cu) into an fp32 [N][K/64 rounded up to 4] array and reach each stage by TMA
-// next to the packed codes, so the decoders never wait on global memory.
+// next to the packed codes, so the decoders never wait on global memory for them.
 // Two accumulators of 256 columns let the epilogue of one tile overlap the
 // main loop of the next.  Every mbarrier wait is bounded in time; a wait that
 // gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
@@ -38,209 +51,275 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTileF = 128;                 // MMA M
+constexpr int kTileF = 128;                 // feature rows per CTA (the pair MMA's M is 256)
 constexpr int kTileT = 256;                 // MMA N
-constexpr int kBK = 64;                     // contraction per stage (128 bytes of bf16)
-constexpr int kStages = 4;
-constexpr int kABytes = kTileF * kBK * 2;   // 16384
-constexpr int kBBytes = kTileT * kBK * 2;   // 32768
-constexpr int kPBytes = 4096;               // packed NF4 bytes per stage
-constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
-constexpr int kThreads = 448;                // 14 warps, roles below
+constexpr int kSub = 64;                    // one sub-block: 64 deep, 128 bytes of bf16 per row
+constexpr int kSubs = 2;                    // sub-blocks per decode step
+constexpr int kStepK = kSub * kSubs;        // contraction per decode step
+constexpr int kHalfT = kTileT / 2;          // token rows each CTA of a pair loads
+constexpr int kCluster = 2;
+constexpr int kSubBytes = 128 * kSub * 2;   // 16384: a 128-row sub-block of A or of the token half
+constexpr int kPBytes = 128 * kStepK / 2;   // 8192: packed codes per step
+constexpr int kScaleBytes = 128 * 4 * 4;    // 2048: a 128 x 4 box of fp32 block scales
+constexpr int kStageBytes = kSubs * kSubBytes + kPBytes + kScaleBytes;
+constexpr int kABytes = kSubs * kSubBytes;
+constexpr int kStages = 3;                  // TMA ring
+constexpr int kAStages = 3;                 // A ring
+constexpr int kThreads = 448;               // 14 warps, roles below
 constexpr int kTmemCols = 512;
-constexpr int kScaleSlot = 2048;              // fwd: 128 rows x 4 fp32; dX: 64 rows x 4 fp32
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStages * kScaleSlot + 256;
-static_assert(20 * 8 + 8 <= 256, "barrier block");
-
-static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
-static_assert(kStages % 2 == 0, "the two decoder groups alternate stages");
+constexpr int kDecoderWarps = 8;
+// barriers: full_b[kStages] full_p[kStages] empty[kStages] aready[kAStages] aempty[kAStages]
+// dready[kAStages] accfull[2] accempty[2], then the abort flag and the TMEM address
+constexpr int kBarFullB = 0, kBarFullP = kStages, kBarEmpty = 2 * kStages, kBarAReady = 3 * kStages,
+              kBarAEmpty = 3 * kStages + kAStages, kBarDReady = 3 * kStages + 2 * kAStages,
+              kBarAccFull = 3 * kStages + 3 * kAStages, kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAStages * kABytes + kNumBars * 8 + 16;
+static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "buffers must stay 1024-byte aligned");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
   int64_t M;           // tokens
   int64_t F;           // output features (N forward, K for dX)
   int64_t N, K;        // W is [N, K]
   int mode;            // 0 forward, 1 dX
-  int red_steps;       // ceil(contraction / 64)
+  int red_steps;       // ceil(contraction / 128)
   int slab_steps;      // padded rank / 64
   int tiles_t, tiles_f;
-  int f_fast;          // tile order: 1 = feature tiles vary fastest (dX), 0 = token tiles (forward)
-  const void* absmax;  // uint8 codes (dq) or float
-  const float* nested;
-  const float* offset;
-  int dq;
+  int pairs_f;         // ceil(tiles_f / 2): feature-tile pairs; an odd count leaves the last pair's
+                       // second tile past F (loads read zeros, the epilogue stores nothing)
+  int f_fast;          // pair order: 1 = feature pairs vary fastest (dX), 0 = token tiles (forward)
+  const __nv_bfloat16* slab_f;   // adapter factor on the feature side, bf16 [F][slab_ld]
+  int slab_ld;         // padded rank
   __nv_bfloat16* out;  // [M, F]
   int* status;
 };
 
-// Warp roles:
-//   0       TMA producer (lane 0)
-//   1       TMEM allocation; MMA issue (lane 0)
-//   2..9    decoders: warps 2..5 take the even stages, 6..9 the odd ones; thread =
-//           one 128-byte row of the A tile (one 64-element NF4 block)
-//   10..13  epilogue
+// Position in the step sequence that every role walks, advanced without divisions:
+// the step within the tile, the TMA ring slot and phase, and the A ring slot and phase.
+struct Cursor {
+  int step = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  int a = 0;
+  uint32_t pa = 0;
+  int64_t lt = 0;
+  __device__ __forceinline__ void advance(int steps) {
+    if (++a == kAStages) a = 0, pa ^= 1u;
+    if (++s == kStages) s = 0, ph ^= 1u;
+    if (++step == steps) step = 0, ++lt;
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
 nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_packed,
-            const __grid_constant__ CUtensorMap tm_slab_f, const __grid_constant__ CUtensorMap tm_slab_t,
-            const __grid_constant__ CUtensorMap tm_scale, const GemmParams p) {
+            const __grid_constant__ CUtensorMap tm_slab_t, const __grid_constant__ CUtensorMap tm_scale,
+            const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const float* scales = reinterpret_cast<const float*>(base_ptr + kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + kStages * kScaleSlot);
-  // bars: full_b[4] aready[4] empty[4] accfull[2] accempty[2] full_p[4]
-  //   full_b: token tile (or both slab tiles) landed; full_p: packed codes + scales landed
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20) + 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + kAStages * kABytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars) + 1;
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  auto stage_a = [&](int s) { return base + s * kStageBytes; };
-  auto stage_b = [&](int s) { return base + s * kStageBytes + kABytes; };
-  auto stage_p = [&](int s) { return base + s * kStageBytes + kABytes + kBBytes; };
-  auto stage_s = [&](int s) { return base + kStages * kStageBytes + s * kScaleSlot; };
-  auto tile_t = [&](int64_t tile) { return p.f_fast ? tile / p.tiles_f : tile % p.tiles_t; };
-  auto tile_f = [&](int64_t tile) { return p.f_fast ? tile % p.tiles_f : tile / p.tiles_t; };
+  auto stage_b = [&](int s) { return base + s * kStageBytes; };
+  auto stage_p = [&](int s) { return base + s * kStageBytes + kSubs * kSubBytes; };
+  auto stage_s = [&](int s) { return base + s * kStageBytes + kSubs * kSubBytes + kPBytes; };
+  auto slot_a = [&](int a) { return base + kStages * kStageBytes + a * kABytes; };
+  const uint32_t rank = cluster_ctarank();
+  auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
+  const int64_t cluster_id = blockIdx.x / kCluster;
+  const int64_t n_clusters = gridDim.x / kCluster;
+  auto tile_t = [&](int64_t pair) { return p.f_fast ? pair / p.pairs_f : pair % p.tiles_t; };
+  auto tile_f = [&](int64_t pair) { return 2 * (p.f_fast ? pair % p.pairs_f : pair / p.tiles_t) + rank; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(s), 1);                 // full_b: producer arrive + TMA bytes
-      mbar_init(bar(16 + s), 1);            // full_p: producer arrive (+ TMA bytes on decode steps)
-      mbar_init(bar(4 + s), 4);             // aready: the four warps of one decoder group
-      mbar_init(bar(8 + s), 1);             // empty: tcgen05.commit
+      mbar_init(bar(kBarFullB + s), 1);     // even CTA: its producer's arrive + both CTAs' token bytes
+      mbar_init(bar(kBarFullP + s), 1);     // producer arrive (+ TMA bytes on decode steps)
+      mbar_init(bar(kBarEmpty + s), 1);     // the pair MMAs' commit
+    }
+    for (int a = 0; a < kAStages; ++a) {
+      mbar_init(bar(kBarAReady + a), kDecoderWarps + 1);   // even CTA: its decoder warps + the odd
+                                                           // CTA's forwarder
+      mbar_init(bar(kBarAEmpty + a), 1);                   // the pair MMAs' commit
+      mbar_init(bar(kBarDReady + a), kDecoderWarps);       // odd CTA: its decoder warps
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(12 + b), 1);            // accfull: tcgen05.commit
-      mbar_init(bar(14 + b), 4);            // accempty: one arrive per epilogue warp
+      mbar_init(bar(kBarAccFull + b), 1);                  // the pair MMAs' commit
+      mbar_init(bar(kBarAccEmpty + b), 4 * kCluster);      // the epilogue warps of both CTAs
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+  if (warp == 1) {   // one warp of each CTA of the pair allocates collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
-  __syncthreads();
+  cluster_sync();   // the peer's barriers are initialised before anything signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int64_t total_tiles = static_cast<int64_t>(p.tiles_t) * p.tiles_f;
+  const int64_t total_pairs = static_cast<int64_t>(p.tiles_t) * p.pairs_f;
   const int steps = p.red_steps + p.slab_steps;
   const int64_t my_tiles =
-      blockIdx.x < total_tiles ? (total_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+      cluster_id < total_pairs ? (total_pairs - cluster_id + n_clusters - 1) / n_clusters : 0;
   const int64_t total_it = my_tiles * steps;    // every role walks the same step sequence
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int last_phase[kStages];
-      bool issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = false, last_phase[s] = 0;
       bool ok = true;
-      for (int64_t it = 0; it < total_it; ++it) {
-        const int64_t tile = blockIdx.x + (it / steps) * gridDim.x;
-        const int step = static_cast<int>(it % steps);
-        const int t0 = static_cast<int>(tile_t(tile) * kTileT);
-        const int f0 = static_cast<int>(tile_f(tile) * kTileF);
-        const int s = static_cast<int>(it % kStages);
-        const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-        if (!mbar_wait(bar(8 + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        if (step < p.red_steps) {
-          // codes and scales first: the decoders start on them while the token tile streams
-          mbar_expect_tx(bar(16 + s), kPBytes + (p.mode == 0 ? kTileF * 16 : 64 * 16));
-          if (p.mode == 0) {
-            tma_load_2d(stage_p(s), &tm_packed, bar(16 + s), step * (kBK / 2), f0);
-            tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), step & ~3, f0);
-          } else {
-            tma_load_2d(stage_p(s), &tm_packed, bar(16 + s), f0 / 2, step * kBK);
-            tma_load_2d(stage_s(s), &tm_scale, bar(16 + s), (f0 / kBlock) & ~3, step * kBK);
-          }
-          mbar_expect_tx(bar(s), kBBytes);
-          tma_load_2d(stage_b(s), &tm_tok, bar(s), step * kBK, t0);
-        } else {
-          const int j = (step - p.red_steps) * kBK;
-          mbar_arrive(bar(16 + s));
-          mbar_expect_tx(bar(s), kBBytes + kABytes);
-          tma_load_2d(stage_b(s), &tm_slab_t, bar(s), j, t0);
-          tma_load_2d(stage_a(s), &tm_slab_f, bar(s), j, f0);
+      Cursor c;
+      int th = 0, f0 = 0;
+      int64_t it = 0;
+      for (; it < total_it; ++it, c.advance(steps)) {
+        if (c.step == 0) {
+          const int64_t tile = cluster_id + c.lt * n_clusters;
+          th = static_cast<int>(tile_t(tile) * kTileT) + static_cast<int>(rank) * kHalfT;
+          f0 = static_cast<int>(tile_f(tile) * kTileF);
         }
-        issued[s] = true;
-        last_phase[s] = ph;
-      }
-      if (!ok) {  // let copies already in flight land before the CTA exits
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s]) {
-            mbar_drain(bar(s), last_phase[s]);
-            mbar_drain(bar(16 + s), last_phase[s]);
+        const int s = c.s;
+        if (!mbar_wait(bar(kBarEmpty + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (c.step < p.red_steps) {
+          const int k0 = c.step * kStepK;
+          // codes and scales first: the decoders start on them while the token tile streams
+          mbar_expect_tx(bar(kBarFullP + s), kPBytes + kScaleBytes);
+          if (p.mode == 0) {
+            tma_load_2d(stage_p(s), &tm_packed, bar(kBarFullP + s), k0 / 2, f0);
+            tma_load_2d(stage_s(s), &tm_scale, bar(kBarFullP + s), (k0 / kBlock) & ~3, f0);
+          } else {
+            tma_load_2d(stage_p(s), &tm_packed, bar(kBarFullP + s), f0 / 2, k0);
+            tma_load_2d(stage_s(s), &tm_scale, bar(kBarFullP + s), (f0 / kBlock) & ~3, k0);
           }
+          if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubs * kSubBytes);
+#pragma unroll
+          for (int u = 0; u < kSubs; ++u)
+            tma_load_2d_pair(stage_b(s) + u * kSubBytes, &tm_tok, lead_bar(kBarFullB + s), k0 + u * kSub, th);
+        } else {
+          mbar_arrive(bar(kBarFullP + s));
+          if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubBytes);
+          tma_load_2d_pair(stage_b(s), &tm_slab_t, lead_bar(kBarFullB + s), (c.step - p.red_steps) * kSub, th);
+        }
+      }
+      if (ok) {
+        // the pair MMAs' commits arrive on this CTA's barriers: wait for the last round
+        // of each so that none lands after the CTA has exited
+        bool w = true;
+        for (int k = 0; k < kStages && w; ++k) {
+          w = mbar_wait(bar(kBarEmpty + c.s), c.ph ^ 1u, abort_flag, p.status);
+          if (++c.s == kStages) c.s = 0, c.ph ^= 1u;
+        }
+        for (int k = 0; k < kAStages && w; ++k) {
+          w = mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status);
+          if (++c.a == kAStages) c.a = 0, c.pa ^= 1u;
+        }
+      } else {  // let copies already in flight land before the CTA exits
+        int ds = c.s;
+        uint32_t dph = c.ph;
+        for (int64_t k = 0; k < kStages && k < it; ++k) {
+          if (ds == 0) ds = kStages - 1, dph ^= 1u;
+          else --ds;
+          if (rank == 0) mbar_drain(bar(kBarFullB + ds), dph);
+          mbar_drain(bar(kBarFullP + ds), dph);
+        }
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc_main = idesc_bf16(kTileF, kTileT, p.mode == 1 ? 1u : 0u);
-      const uint32_t idesc_slab = idesc_bf16(kTileF, kTileT, 0u);
-      bool ok = true;
-      for (int64_t it = 0; it < total_it && ok; ++it) {
-        const int64_t lt = it / steps;
-        const int step = static_cast<int>(it % steps);
-        const uint32_t b = static_cast<uint32_t>(lt) & 1u;
-        if (step == 0) {
-          if (!mbar_wait(bar(14 + b), (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) break;
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA) ----------------
+      const uint32_t idesc_main = idesc_bf16(kCluster * kTileF, kTileT, p.mode == 1 ? 1u : 0u);
+      const uint32_t idesc_slab = idesc_bf16(kCluster * kTileF, kTileT, 0u);
+      Cursor c;
+      for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
+        const uint32_t b = static_cast<uint32_t>(c.lt) & 1u;
+        if (c.step == 0) {
+          if (!mbar_wait(bar(kBarAccEmpty + b), (static_cast<uint32_t>(c.lt >> 1) & 1u) ^ 1u, abort_flag, p.status))
+            break;
           tc_fence_after();
         }
-        const int s = static_cast<int>(it % kStages);
-        const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-        if (!mbar_wait(bar(s), ph, abort_flag, p.status) || !mbar_wait(bar(4 + s), ph, abort_flag, p.status)) {
-          ok = false;
+        if (!mbar_wait(bar(kBarFullB + c.s), c.ph, abort_flag, p.status) ||
+            !mbar_wait(bar(kBarAReady + c.a), c.pa, abort_flag, p.status))
           break;
-        }
         tc_fence_after();
-        const bool slab = step >= p.red_steps;
-        const bool mn_major = (p.mode == 1) && !slab;
         const uint32_t d_tmem = tmem_base + b * kTileT;
+        if (c.step < p.red_steps) {
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // K-major: 32 bytes per 16-element k step inside the 128-byte row.
-          // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
-          // 64-feature halves of the tile are 8192 bytes apart.
-          const uint64_t adesc = mn_major ? smem_desc(stage_a(s) + kk * 2048, 8192, 1024)
-                                          : smem_desc(stage_a(s) + kk * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc(stage_b(s) + kk * 32, 16, 1024);
-          umma_bf16(d_tmem, adesc, bdesc, slab ? idesc_slab : idesc_main, (step > 0 || kk > 0) ? 1u : 0u);
+          for (int u = 0; u < kSubs; ++u)
+#pragma unroll
+            for (int kk = 0; kk < kSub / 16; ++kk) {
+              // K-major: 32 bytes per 16-element k step inside the 128-byte row.
+              // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
+              // 64-feature halves of the sub-block are 8192 bytes apart.
+              const uint32_t sa = slot_a(c.a) + u * kSubBytes;
+              const uint64_t adesc = p.mode == 1 ? smem_desc(sa + kk * 2048, 8192, 1024)
+                                                 : smem_desc(sa + kk * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc(stage_b(c.s) + u * kSubBytes + kk * 32, 16, 1024);
+              umma_bf16_pair(d_tmem, adesc, bdesc, idesc_main, (c.step > 0 || u > 0 || kk > 0) ? 1u : 0u);
+            }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kSub / 16; ++kk)
+            umma_bf16_pair(d_tmem, smem_desc(slot_a(c.a) + kk * 32, 16, 1024),
+                           smem_desc(stage_b(c.s) + kk * 32, 16, 1024), idesc_slab, 1u);
         }
-        umma_commit(bar(8 + s));
-        if (step == steps - 1) umma_commit(bar(12 + b));
+        umma_commit_pair_mc(bar(kBarEmpty + c.s), 0x3);    // frees TMA stage s in both CTAs
+        umma_commit_pair_mc(bar(kBarAEmpty + c.a), 0x3);   // and A slot a
+        if (c.step == steps - 1) umma_commit_pair_mc(bar(kBarAccFull + b), 0x3);
+      }
+    } else if (lane == 0) {
+      // ---------------- forwarder (odd CTA) ----------------
+      // one cluster-scope arrive per A slot filled; the decoder warps' own arrives stay local
+      Cursor c;
+      for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
+        if (!mbar_wait(bar(kBarDReady + c.a), c.pa, abort_flag, p.status)) break;
+        mbar_arrive_cluster(lead_bar(kBarAReady + c.a));
       }
     }
   } else if (warp < 10) {
     // ---------------- NF4 decoders ----------------
-    const int group = (warp - 2) >> 2;
-    const int row = ((warp - 2) & 3) * 32 + lane;  // row of the A tile, 0..127
+    const int d = (warp - 2) * 32 + lane;
+    const int row = d & 127;                        // row of an A sub-block (one NF4 block)
+    const int u = d >> 7;                           // which sub-block of the step
     const uint32_t sw = static_cast<uint32_t>(row & 7);
-    const uint32_t poff = (p.mode == 0) ? row * 32 : (row & 63) * 64 + (row >> 6) * 32;
-    for (int64_t it = group; it < total_it; it += 2) {
-      const int step = static_cast<int>(it % steps);
-      const int s = static_cast<int>(it % kStages);
-      const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(16 + s), ph, abort_flag, p.status))) break;
-      if (step < p.red_steps) {
+    // packed bytes of this thread's block within the stage's code tile, and its scale row
+    const uint32_t poff = (p.mode == 0) ? row * (kStepK / 2) + u * 32 : (u * 64 + (row & 63)) * 64 + (row >> 6) * 32;
+    const int srow = (p.mode == 0) ? row * 4 : (u * 64 + (row & 63)) * 4 + (row >> 6);
+    const uint32_t ready = bar((rank == 0 ? kBarAReady : kBarDReady));
+    int scol = 0;
+    int64_t fr = 0;                                 // feature of this thread's slab row
+    uint4 sl[4];                                    // its half of the row, fetched at the tile start
+    Cursor c;
+    for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
+      if (c.step == 0) {
+        const int64_t f0 = tile_f(cluster_id + c.lt * n_clusters) * kTileF;
+        // dX: the tile's first block modulo 4 in a box that starts at it rounded down to 4
+        if (p.mode == 1) scol = static_cast<int>((f0 / kBlock) & 3);
+        // slab step 0: this thread copies 32 of the 64 values of feature row f0 + row
+        fr = f0 + row;
+        const bool fr_ok = fr < p.F;
+        const uint4* src = reinterpret_cast<const uint4*>(p.slab_f + (fr_ok ? fr : 0) * p.slab_ld) + u * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sl[q] = fr_ok ? src[q] : make_uint4(0, 0, 0, 0);
+      }
+      // every stage's full_p phase is waited, in order, so that none is ever two phases behind
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.s), c.ph, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status))) break;
+      if (c.step < p.red_steps) {
+        const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.s) - base));
+        const int col = (p.mode == 0) ? ((c.step * kSubs + u) & 3) : scol;
         uint32_t L[4], H[4];
-        // forward: scale of row `row`; dX: row (row & 63) of a 64 x 4 box whose first
-        // column is the 128-feature tile's first block rounded down to a multiple of 4
-        const int64_t f0 = tile_f(blockIdx.x + (it / steps) * gridDim.x) * kTileF;
-        const float a = (p.mode == 0) ? scales[s * (kScaleSlot / 4) + row * 4 + (step & 3)]
-                                      : scales[s * (kScaleSlot / 4) + (row & 63) * 4 +
-                                               static_cast<int>((f0 / kBlock) & 3) + (row >> 6)];
-        build_lut(a, L, H);
-        const uint8_t* src = base_ptr + (stage_p(s) - base) + poff;
+        build_lut(sc[srow + col], L, H);
+        const uint8_t* src = base_ptr + (stage_p(c.s) - base) + poff;
         const uint4 w0 = *reinterpret_cast<const uint4*>(src);
         const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint32_t arow = stage_a(s) + row * 128;
+        const uint32_t arow = slot_a(c.a) + u * kSubBytes + row * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint32_t o[4];
@@ -250,19 +329,37 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
                        "r"(o[3])
                        : "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      } else {
+        // adapter slab: the 128 x 64 bf16 tile of the feature-side factor, K-major,
+        // 32 values (four 16-byte chunks) per thread
+        const int j = c.step - p.red_steps;
+        if (j > 0) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.slab_f + (fr < p.F ? fr : 0) * p.slab_ld + j * kSub) + u * 4;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) sl[q] = fr < p.F ? src[q] : make_uint4(0, 0, 0, 0);
+        }
+        const uint32_t arow = slot_a(c.a) + row * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t dst = arow + (((static_cast<uint32_t>(u * 4 + q)) ^ sw) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sl[q].x), "r"(sl[q].y),
+                       "r"(sl[q].z), "r"(sl[q].w)
+                       : "memory");
+        }
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(4 + s));
+      if (lane == 0) mbar_arrive(ready + c.a * 8);
     }
   } else {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
     for (int64_t lt = 0; lt < my_tiles; ++lt) {
-      const int64_t tile = blockIdx.x + lt * gridDim.x;
+      const int64_t tile = cluster_id + lt * n_clusters;
       const uint32_t b = static_cast<uint32_t>(lt) & 1u;
       const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(12 + b), aph, abort_flag, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), aph, abort_flag, p.status))) break;
       tc_fence_after();
       const int64_t t0 = tile_t(tile) * kTileT;
       const int64_t f = tile_f(tile) * kTileF + quarter * 32 + lane;
@@ -282,22 +379,22 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(14 + b));
+      if (lane == 0) mbar_arrive_cluster(lead_bar(kBarAccEmpty + b));
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // neither CTA exits while the other may still signal its barriers
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                  : "memory");
   }
 }
 
 // ---- host side --------------------------------------------------------------------------
 
-int padded_rank(int r) { return (r + kBK - 1) / kBK * kBK; }
+int padded_rank(int r) { return (r + kSub - 1) / kSub * kSub; }
 size_t a1024(size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); }
 
 int sm_count() {
@@ -308,20 +405,36 @@ int sm_count() {
 }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUtensorMap& packed,
-                        const CUtensorMap& slab_f, const CUtensorMap& slab_t, const CUtensorMap& scale,
-                        cudaStream_t st) {
+                        const CUtensorMap& slab_t, const CUtensorMap& scale, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(nf4_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr_err != cudaSuccess) return;
+    cfg.gridDim = dim3(static_cast<unsigned>(sm_count() / kCluster * kCluster));
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, nf4_tc_gemm, &cfg);
+    if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int64_t tiles = static_cast<int64_t>(p.tiles_t) * p.tiles_f;
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  const int64_t pairs = static_cast<int64_t>(p.tiles_t) * p.pairs_f;
+  const int64_t clusters = pairs < max_clusters ? pairs : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster));
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
-  nf4_tc_gemm<<<grid, kThreads, kSmemBytes, st>>>(tok, packed, slab_f, slab_t, scale, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, nf4_tc_gemm, tok, packed, slab_t, scale, p);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int64_t scale_ld(int64_t K) { return (K / kBlock + 3) / 4 * 4; }
@@ -339,7 +452,8 @@ PrepJob scales_job(const LinearArgs& a, float* out) {
 
 bool scales_map(const LinearArgs& a, int mode, const float* sc, CUtensorMap* map) {
   const int64_t ldk = scale_ld(a.K);
-  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sc, ldk, a.N, 4 * ldk, 4, mode == 0 ? kTileF : 64,
+  // forward: 128 weight rows x 4 blocks; dX: 128 weight rows (one step of n) x 4 blocks
+  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sc, ldk, a.N, 4 * ldk, 4, mode == 0 ? kTileF : kStepK,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -383,15 +497,13 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   p.F = mode == 0 ? a.N : a.K;
   p.mode = mode;
   const int64_t red = mode == 0 ? a.K : a.N;
-  p.red_steps = static_cast<int>((red + kBK - 1) / kBK);
-  p.slab_steps = padded_rank(a.r) / kBK;
+  p.red_steps = static_cast<int>((red + kStepK - 1) / kStepK);
+  p.slab_steps = padded_rank(a.r) / kSub;
   p.tiles_t = static_cast<int>((a.M + kTileT - 1) / kTileT);
   p.tiles_f = static_cast<int>((p.F + kTileF - 1) / kTileF);
+  p.pairs_f = (p.tiles_f + 1) / 2;
   p.f_fast = mode == 1 ? 1 : 0;
-  p.absmax = a.W.absmax;
-  p.nested = a.W.nested;
-  p.offset = a.W.offset;
-  p.dq = a.W.dq;
+  p.slab_ld = padded_rank(a.r);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = status;
   return p;
@@ -441,18 +553,18 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   int ns = 0;
   if ((e = adapter_pass(x, a.K, a.M, false, Aq, a.K, a.r, a.M, a.K, part, status, &ns, st)) != cudaSuccess) return e;
   if ((e = adapter_finish(part, ns, a.M, a.r, 1.0f, T, 0, sTp, rp, a.s, nullptr, 0, st)) != cudaSuccess) return e;
-  CUtensorMap tok, packed, slab_f, slab_t, scale;
-  bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kBK, kTileT,
+  CUtensorMap tok, packed, slab_t, scale;
+  bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kSub, kHalfT,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kBK / 2, kTileF,
+  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kStepK / 2, kTileF,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok = ok && make_map(&slab_f, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, rp, a.N, 2 * rp, kBK, kTileF,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kBK, kTileT,
+  ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kSub, kHalfT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && scales_map(a, 0, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
-  return launch_gemm(base_params(a, 0, y, status), tok, packed, slab_f, slab_t, scale, st);
+  GemmParams gp = base_params(a, 0, y, status);
+  gp.slab_f = Bp;
+  return launch_gemm(gp, tok, packed, slab_t, scale, st);
 }
 
 // Backward: prep (B^T, T^T, zeroed G^T, A^T in bf16, block scales) -> G = dY B ->
@@ -514,19 +626,18 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   // dB = s dY^T T: rows N, reduction over M down dY's columns
   if ((e = adapter_pass(dy, a.N, a.M, true, Tt, Mp, a.r, a.N, a.M, part, status, &ns, st)) != cudaSuccess) return e;
   if ((e = adapter_finish(part, ns, a.N, a.r, a.s, dB, 0, nullptr, 0, 0.0f, nullptr, 0, st)) != cudaSuccess) return e;
-  CUtensorMap tok, packed, slab_f, slab_t, scale;
-  bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kBK, kTileT,
+  CUtensorMap tok, packed, slab_t, scale;
+  bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kBK, kBK,
+  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kTileF / 2, kStepK,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
-  ok = ok && make_map(&slab_f, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ApT, rp, a.K, 2 * rp, kBK, kTileF,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kBK, kTileT,
+  ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kSub, kHalfT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && scales_map(a, 1, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
-  if ((e = launch_gemm(base_params(a, 1, dx, status), tok, packed, slab_f, slab_t, scale, st)) != cudaSuccess)
-    return e;
+  GemmParams gp = base_params(a, 1, dx, status);
+  gp.slab_f = ApT;
+  if ((e = launch_gemm(gp, tok, packed, slab_t, scale, st)) != cudaSuccess) return e;
   // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
   if ((e = adapter_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, part, status, &ns, st)) != cudaSuccess) return e;
   return adapter_finish(part, ns, a.K, a.r, a.s, dA, 1, nullptr, 0, 0.0f, nullptr, 0, st);
