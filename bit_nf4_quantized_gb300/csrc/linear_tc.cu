@@ -16,20 +16,20 @@
 // write each CTA's 128 accumulator rows into its own TMEM.  So every SM receives half the
 // token bytes that a one-SM 128 x 256 tile would need for the same work.
 // The contraction advances in steps of 128 (two 64-deep sub-blocks, one NF4 block each),
-// then in 64-deep adapter slab steps.  Two rings of shared-memory buffers: one (kStages)
-// of what TMA brings per step (this CTA's token half, packed codes, block scales) and one
-// (kAStages) of bf16 A tiles (decoded weights, or the adapter factor for slab steps).
-// Warp roles (448 threads, in each CTA):
-//   warp 0      TMA producer: its half of the token tile (128B-swizzled) + packed NF4 tile
-//               and block scales per step, or its half of the s*T / s*G slab tile;
-//   warp 1      TMEM allocation (pair-wide); in the even CTA, lane 0 issues the MMAs; in
-//               the odd CTA, lane 0 forwards "A slot ready" to the even CTA once per step,
-//               so that the decoders only ever arrive on local barriers;
+// then in 64-deep adapter slab steps.  Three rings of shared-memory buffers, one slot per
+// step each: this CTA's token half (freed when the pair MMAs have read it), packed codes
+// and block scales (freed as soon as the decoders have read them, so they are refetched
+// well ahead), and bf16 A tiles (decoded weights, or the adapter factor on slab steps).
+// Warp roles (480 threads, in each CTA):
+//   warp 0      TMA producer for the token ring: its half of the token tile (128B-swizzled)
+//               per step, or its half of the s*T / s*G slab tile;
+//   warp 1      TMEM allocation (pair-wide); in the even CTA, lane 0 issues the MMAs;
 //   warps 2..9  decoders: a thread turns one 64-element NF4 block (one 128-byte row of an
 //               A sub-block) into bf16 in the swizzled layout the MMA reads (K-major for the
 //               forward, MN-major for dX), through a per-block scaled lookup table; on slab
 //               steps they copy the bf16 adapter factor rows in from global memory;
-//   warps 10..13 epilogue: tcgen05.ld of this CTA's accumulator rows, bf16 stores.
+//   warps 10..13 epilogue: tcgen05.ld of this CTA's accumulator rows, bf16 stores;
+//   warp 14     TMA producer for the code ring: packed NF4 tile and block scales per step.
 // Barriers that gate the MMA (stage full, A slot ready, accumulator drained) live in the
 // even CTA; the MMA completion is multicast to both CTAs.
 // The per-block scales a' = dyn8[code] * nested + offset are computed once per call
@@ -61,20 +61,24 @@ constexpr int kCluster = 2;
 constexpr int kSubBytes = 128 * kSub * 2;   // 16384: a 128-row sub-block of A or of the token half
 constexpr int kPBytes = 128 * kStepK / 2;   // 8192: packed codes per step
 constexpr int kScaleBytes = 128 * 4 * 4;    // 2048: a 128 x 4 box of fp32 block scales
-constexpr int kStageBytes = kSubs * kSubBytes + kPBytes + kScaleBytes;
+constexpr int kBStageBytes = kSubs * kSubBytes;
+constexpr int kPStageBytes = kPBytes + kScaleBytes;
 constexpr int kABytes = kSubs * kSubBytes;
-constexpr int kStages = 3;                  // TMA ring
+constexpr int kStages = 3;                  // token ring
+constexpr int kPStages = 3;                 // code ring
 constexpr int kAStages = 3;                 // A ring
-constexpr int kThreads = 448;               // 14 warps, roles below
+constexpr int kThreads = 480;               // 15 warps, roles below
 constexpr int kTmemCols = 512;
 constexpr int kDecoderWarps = 8;
-// barriers: full_b[kStages] full_p[kStages] empty[kStages] aready[kAStages] aempty[kAStages]
-// dready[kAStages] accfull[2] accempty[2], then the abort flag and the TMEM address
-constexpr int kBarFullB = 0, kBarFullP = kStages, kBarEmpty = 2 * kStages, kBarAReady = 3 * kStages,
-              kBarAEmpty = 3 * kStages + kAStages, kBarDReady = 3 * kStages + 2 * kAStages,
-              kBarAccFull = 3 * kStages + 3 * kAStages, kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kAStages * kABytes + kNumBars * 8 + 16;
-static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0, "buffers must stay 1024-byte aligned");
+// barriers: full_b/empty_b[kStages] full_p/empty_p[kPStages] aready/aempty[kAStages]
+// accfull[2] accempty[2], then the abort flag and the TMEM address
+constexpr int kBarFullB = 0, kBarEmptyB = kStages, kBarFullP = 2 * kStages, kBarEmptyP = 2 * kStages + kPStages,
+              kBarAReady = 2 * kStages + 2 * kPStages, kBarAEmpty = kBarAReady + kAStages,
+              kBarAccFull = kBarAEmpty + kAStages, kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
+constexpr int kSmemBytes =
+    1024 + kStages * kBStageBytes + kAStages * kABytes + kPStages * kPStageBytes + kNumBars * 8 + 16;
+static_assert(kBStageBytes % 1024 == 0 && kABytes % 1024 == 0 && kPStageBytes % 1024 == 0,
+              "buffers must stay 1024-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
@@ -95,17 +99,20 @@ struct GemmParams {
 };
 
 // Position in the step sequence that every role walks, advanced without divisions:
-// the step within the tile, the TMA ring slot and phase, and the A ring slot and phase.
+// the step within the tile and the slot and phase of each ring.
 struct Cursor {
   int step = 0;
   int s = 0;
   uint32_t ph = 0;
+  int q = 0;
+  uint32_t pq = 0;
   int a = 0;
   uint32_t pa = 0;
   int64_t lt = 0;
   __device__ __forceinline__ void advance(int steps) {
-    if (++a == kAStages) a = 0, pa ^= 1u;
     if (++s == kStages) s = 0, ph ^= 1u;
+    if (++q == kPStages) q = 0, pq ^= 1u;
+    if (++a == kAStages) a = 0, pa ^= 1u;
     if (++step == steps) step = 0, ++lt;
   }
 };
@@ -118,14 +125,15 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + kAStages * kABytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kBStageBytes + kAStages * kABytes +
+                                               kPStages * kPStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars) + 1;
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  auto stage_b = [&](int s) { return base + s * kStageBytes; };
-  auto stage_p = [&](int s) { return base + s * kStageBytes + kSubs * kSubBytes; };
-  auto stage_s = [&](int s) { return base + s * kStageBytes + kSubs * kSubBytes + kPBytes; };
-  auto slot_a = [&](int a) { return base + kStages * kStageBytes + a * kABytes; };
+  auto stage_b = [&](int s) { return base + s * kBStageBytes; };
+  auto slot_a = [&](int a) { return base + kStages * kBStageBytes + a * kABytes; };
+  auto stage_p = [&](int q) { return base + kStages * kBStageBytes + kAStages * kABytes + q * kPStageBytes; };
+  auto stage_s = [&](int q) { return stage_p(q) + kPBytes; };
   const uint32_t rank = cluster_ctarank();
   auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
   const int64_t cluster_id = blockIdx.x / kCluster;
@@ -138,14 +146,15 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarFullB + s), 1);     // even CTA: its producer's arrive + both CTAs' token bytes
-      mbar_init(bar(kBarFullP + s), 1);     // producer arrive (+ TMA bytes on decode steps)
-      mbar_init(bar(kBarEmpty + s), 1);     // the pair MMAs' commit
+      mbar_init(bar(kBarEmptyB + s), 1);    // the pair MMAs' commit
+    }
+    for (int q = 0; q < kPStages; ++q) {
+      mbar_init(bar(kBarFullP + q), 1);                // producer arrive (+ TMA bytes on decode steps)
+      mbar_init(bar(kBarEmptyP + q), kDecoderWarps);   // this CTA's decoder warps
     }
     for (int a = 0; a < kAStages; ++a) {
-      mbar_init(bar(kBarAReady + a), kDecoderWarps + 1);   // even CTA: its decoder warps + the odd
-                                                           // CTA's forwarder
-      mbar_init(bar(kBarAEmpty + a), 1);                   // the pair MMAs' commit
-      mbar_init(bar(kBarDReady + a), kDecoderWarps);       // odd CTA: its decoder warps
+      mbar_init(bar(kBarAReady + a), kCluster * kDecoderWarps);   // even CTA: both CTAs' decoder warps
+      mbar_init(bar(kBarAEmpty + a), 1);                          // the pair MMAs' commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarAccFull + b), 1);                  // the pair MMAs' commit
@@ -172,37 +181,24 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   const int64_t total_it = my_tiles * steps;    // every role walks the same step sequence
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: token ring ----------------
     if (lane == 0) {
       bool ok = true;
       Cursor c;
-      int th = 0, f0 = 0;
+      int th = 0;
       int64_t it = 0;
       for (; it < total_it; ++it, c.advance(steps)) {
-        if (c.step == 0) {
-          const int64_t tile = cluster_id + c.lt * n_clusters;
-          th = static_cast<int>(tile_t(tile) * kTileT) + static_cast<int>(rank) * kHalfT;
-          f0 = static_cast<int>(tile_f(tile) * kTileF);
-        }
+        if (c.step == 0)
+          th = static_cast<int>(tile_t(cluster_id + c.lt * n_clusters) * kTileT) + static_cast<int>(rank) * kHalfT;
         const int s = c.s;
-        if (!mbar_wait(bar(kBarEmpty + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(bar(kBarEmptyB + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
         if (c.step < p.red_steps) {
           const int k0 = c.step * kStepK;
-          // codes and scales first: the decoders start on them while the token tile streams
-          mbar_expect_tx(bar(kBarFullP + s), kPBytes + kScaleBytes);
-          if (p.mode == 0) {
-            tma_load_2d(stage_p(s), &tm_packed, bar(kBarFullP + s), k0 / 2, f0);
-            tma_load_2d(stage_s(s), &tm_scale, bar(kBarFullP + s), (k0 / kBlock) & ~3, f0);
-          } else {
-            tma_load_2d(stage_p(s), &tm_packed, bar(kBarFullP + s), f0 / 2, k0);
-            tma_load_2d(stage_s(s), &tm_scale, bar(kBarFullP + s), (f0 / kBlock) & ~3, k0);
-          }
           if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubs * kSubBytes);
 #pragma unroll
           for (int u = 0; u < kSubs; ++u)
             tma_load_2d_pair(stage_b(s) + u * kSubBytes, &tm_tok, lead_bar(kBarFullB + s), k0 + u * kSub, th);
         } else {
-          mbar_arrive(bar(kBarFullP + s));
           if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubBytes);
           tma_load_2d_pair(stage_b(s), &tm_slab_t, lead_bar(kBarFullB + s), (c.step - p.red_steps) * kSub, th);
         }
@@ -212,21 +208,55 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
         // of each so that none lands after the CTA has exited
         bool w = true;
         for (int k = 0; k < kStages && w; ++k) {
-          w = mbar_wait(bar(kBarEmpty + c.s), c.ph ^ 1u, abort_flag, p.status);
+          w = mbar_wait(bar(kBarEmptyB + c.s), c.ph ^ 1u, abort_flag, p.status);
           if (++c.s == kStages) c.s = 0, c.ph ^= 1u;
         }
         for (int k = 0; k < kAStages && w; ++k) {
           w = mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status);
           if (++c.a == kAStages) c.a = 0, c.pa ^= 1u;
         }
-      } else {  // let copies already in flight land before the CTA exits
+      } else if (rank == 0) {  // let copies already in flight land before the CTA exits
         int ds = c.s;
         uint32_t dph = c.ph;
         for (int64_t k = 0; k < kStages && k < it; ++k) {
           if (ds == 0) ds = kStages - 1, dph ^= 1u;
           else --ds;
-          if (rank == 0) mbar_drain(bar(kBarFullB + ds), dph);
-          mbar_drain(bar(kBarFullP + ds), dph);
+          mbar_drain(bar(kBarFullB + ds), dph);
+        }
+      }
+    }
+  } else if (warp == 14) {
+    // ---------------- TMA producer: code ring ----------------
+    if (lane == 0) {
+      bool ok = true;
+      Cursor c;
+      int f0 = 0;
+      int64_t it = 0;
+      for (; it < total_it; ++it, c.advance(steps)) {
+        if (c.step == 0) f0 = static_cast<int>(tile_f(cluster_id + c.lt * n_clusters) * kTileF);
+        const int q = c.q;
+        if (!mbar_wait(bar(kBarEmptyP + q), c.pq ^ 1u, abort_flag, p.status)) { ok = false; break; }
+        if (c.step < p.red_steps) {
+          const int k0 = c.step * kStepK;
+          mbar_expect_tx(bar(kBarFullP + q), kPBytes + kScaleBytes);
+          if (p.mode == 0) {
+            tma_load_2d(stage_p(q), &tm_packed, bar(kBarFullP + q), k0 / 2, f0);
+            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), (k0 / kBlock) & ~3, f0);
+          } else {
+            tma_load_2d(stage_p(q), &tm_packed, bar(kBarFullP + q), f0 / 2, k0);
+            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), (f0 / kBlock) & ~3, k0);
+          }
+        } else {
+          mbar_arrive(bar(kBarFullP + q));   // slab steps read no codes; keep the ring in step
+        }
+      }
+      if (!ok) {  // let copies already in flight land before the CTA exits
+        int dq = c.q;
+        uint32_t dpq = c.pq;
+        for (int64_t k = 0; k < kPStages && k < it; ++k) {
+          if (dq == 0) dq = kPStages - 1, dpq ^= 1u;
+          else --dq;
+          mbar_drain(bar(kBarFullP + dq), dpq);
         }
       }
     }
@@ -268,17 +298,9 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
             umma_bf16_pair(d_tmem, smem_desc(slot_a(c.a) + kk * 32, 16, 1024),
                            smem_desc(stage_b(c.s) + kk * 32, 16, 1024), idesc_slab, 1u);
         }
-        umma_commit_pair_mc(bar(kBarEmpty + c.s), 0x3);    // frees TMA stage s in both CTAs
+        umma_commit_pair_mc(bar(kBarEmptyB + c.s), 0x3);   // frees token stage s in both CTAs
         umma_commit_pair_mc(bar(kBarAEmpty + c.a), 0x3);   // and A slot a
         if (c.step == steps - 1) umma_commit_pair_mc(bar(kBarAccFull + b), 0x3);
-      }
-    } else if (lane == 0) {
-      // ---------------- forwarder (odd CTA) ----------------
-      // one cluster-scope arrive per A slot filled; the decoder warps' own arrives stay local
-      Cursor c;
-      for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
-        if (!mbar_wait(bar(kBarDReady + c.a), c.pa, abort_flag, p.status)) break;
-        mbar_arrive_cluster(lead_bar(kBarAReady + c.a));
       }
     }
   } else if (warp < 10) {
@@ -290,7 +312,6 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
     // packed bytes of this thread's block within the stage's code tile, and its scale row
     const uint32_t poff = (p.mode == 0) ? row * (kStepK / 2) + u * 32 : (u * 64 + (row & 63)) * 64 + (row >> 6) * 32;
     const int srow = (p.mode == 0) ? row * 4 : (u * 64 + (row & 63)) * 4 + (row >> 6);
-    const uint32_t ready = bar((rank == 0 ? kBarAReady : kBarDReady));
     int scol = 0;
     int64_t fr = 0;                                 // feature of this thread's slab row
     uint4 sl[4];                                    // its half of the row, fetched at the tile start
@@ -307,15 +328,15 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
 #pragma unroll
         for (int q = 0; q < 4; ++q) sl[q] = fr_ok ? src[q] : make_uint4(0, 0, 0, 0);
       }
-      // every stage's full_p phase is waited, in order, so that none is ever two phases behind
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.s), c.ph, abort_flag, p.status))) break;
+      // every slot's full_p phase is waited, in order, so that none is ever two phases behind
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.q), c.pq, abort_flag, p.status))) break;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status))) break;
       if (c.step < p.red_steps) {
-        const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.s) - base));
+        const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.q) - base));
         const int col = (p.mode == 0) ? ((c.step * kSubs + u) & 3) : scol;
         uint32_t L[4], H[4];
         build_lut(sc[srow + col], L, H);
-        const uint8_t* src = base_ptr + (stage_p(c.s) - base) + poff;
+        const uint8_t* src = base_ptr + (stage_p(c.q) - base) + poff;
         const uint4 w0 = *reinterpret_cast<const uint4*>(src);
         const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -348,9 +369,15 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
                        : "memory");
         }
       }
+      // the rows are read by this SM's tensor core (a pair MMA takes each CTA's A rows
+      // from that CTA's shared memory): make them visible to the async proxy, then
+      // tell the even CTA, and hand the code slot back to the producer
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(ready + c.a * 8);
+      if (lane == 0) {
+        mbar_arrive(bar(kBarEmptyP + c.q));
+        mbar_arrive_remote(lead_bar(kBarAReady + c.a));
+      }
     }
   } else {
     // ---------------- epilogue ----------------
@@ -379,7 +406,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lead_bar(kBarAccEmpty + b));
+      if (lane == 0) mbar_arrive_remote(lead_bar(kBarAccEmpty + b));
     }
   }
 

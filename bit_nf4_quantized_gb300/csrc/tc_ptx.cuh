@@ -67,37 +67,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// As mbar_wait, with acquire at cluster scope: for barriers that the peer CTA arrives on
-// after writing shared memory that this thread's next tcgen05 operations read.
-__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  int* status) {
-  if (mbar_test_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_test_cluster(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicCAS(status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
-        return false;
-      }
-    }
-  }
-}
-
 // Wait used only while winding down after a timeout: time-bounded, ignores the flag.
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_ns();
@@ -132,9 +101,9 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's),
-// releasing this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// with the default release semantics of mbarrier.arrive.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Paired-CTA form: the box lands in this CTA's shared memory and completes its bytes on
