@@ -33,8 +33,10 @@
 // Barriers that gate the MMA (stage full, A slot ready, accumulator drained) live in the
 // even CTA; the MMA completion is multicast to both CTAs.
 // The per-block scales a' = dyn8[code] * nested + offset are computed once per call
-// (prep.cu) into an fp32 [N][K/64 rounded up to 4] array and reach each stage by TMA
-// next to the packed codes, so the decoders never wait on global memory for them.
+// (prep.cu) into an fp32 [K/64][N rounded up to 4] array and reach each step by TMA next
+// to the packed codes, so the decoders never wait on global memory for them.  Codes and
+// scales are laid out in shared memory so that a warp's 32 rows read consecutive words
+// (codes as four 16-byte-wide column boxes), free of bank conflicts.
 // Two accumulators of 256 columns let the epilogue of one tile overlap the
 // main loop of the next.  Every mbarrier wait is bounded in time; a wait that
 // gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
@@ -59,8 +61,9 @@ constexpr int kStepK = kSub * kSubs;        // contraction per decode step
 constexpr int kHalfT = kTileT / 2;          // token rows each CTA of a pair loads
 constexpr int kCluster = 2;
 constexpr int kSubBytes = 128 * kSub * 2;   // 16384: a 128-row sub-block of A or of the token half
-constexpr int kPBytes = 128 * kStepK / 2;   // 8192: packed codes per step
-constexpr int kScaleBytes = 128 * 4 * 4;    // 2048: a 128 x 4 box of fp32 block scales
+constexpr int kPBytes = 128 * kStepK / 2;   // 8192: packed codes per step, as [4][128 rows][16 B]
+constexpr int kPBox = 16;                   // bytes per row of one code box
+constexpr int kScaleBytes = kSubs * 128 * 4;   // 1024: [2 blocks][128 rows] fp32 block scales
 constexpr int kBStageBytes = kSubs * kSubBytes;
 constexpr int kPStageBytes = kPBytes + kScaleBytes;
 constexpr int kABytes = kSubs * kSubBytes;
@@ -239,13 +242,17 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
         if (c.step < p.red_steps) {
           const int k0 = c.step * kStepK;
           mbar_expect_tx(bar(kBarFullP + q), kPBytes + kScaleBytes);
-          if (p.mode == 0) {
-            tma_load_2d(stage_p(q), &tm_packed, bar(kBarFullP + q), k0 / 2, f0);
-            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), (k0 / kBlock) & ~3, f0);
-          } else {
-            tma_load_2d(stage_p(q), &tm_packed, bar(kBarFullP + q), f0 / 2, k0);
-            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), (f0 / kBlock) & ~3, k0);
-          }
+          // forward: rows are weight rows f, bytes run along k; dX: rows are weight rows n
+          // (the contraction), bytes run along the features f
+          const int px = p.mode == 0 ? k0 / 2 : f0 / 2, py = p.mode == 0 ? f0 : k0;
+#pragma unroll
+          for (int cb = 0; cb < kPBytes / (128 * kPBox); ++cb)
+            tma_load_2d(stage_p(q) + cb * 128 * kPBox, &tm_packed, bar(kBarFullP + q), px + cb * kPBox, py);
+          // scales [kb][n]: forward blocks (f0.., 2 steps of k), dX blocks (k0.., the tile's 2 of f)
+          if (p.mode == 0)
+            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), f0, k0 / kBlock);
+          else
+            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), k0, f0 / kBlock);
         } else {
           mbar_arrive(bar(kBarFullP + q));   // slab steps read no codes; keep the ring in step
         }
@@ -309,18 +316,20 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
     const int row = d & 127;                        // row of an A sub-block (one NF4 block)
     const int u = d >> 7;                           // which sub-block of the step
     const uint32_t sw = static_cast<uint32_t>(row & 7);
-    // packed bytes of this thread's block within the stage's code tile, and its scale row
-    const uint32_t poff = (p.mode == 0) ? row * (kStepK / 2) + u * 32 : (u * 64 + (row & 63)) * 64 + (row >> 6) * 32;
-    const int srow = (p.mode == 0) ? row * 4 : (u * 64 + (row & 63)) * 4 + (row >> 6);
-    int scol = 0;
+    // the 32 code bytes of this thread's block are two 16-byte columns of the [4][128][16]
+    // code tile, and its scale one entry of the [2][128] scale tile
+    //   forward: row = weight row f, block u of the step;  dX: weight row n = u*64 + (row & 63),
+    //   feature half row >> 6
+    const int prow = (p.mode == 0) ? row : u * 64 + (row & 63);
+    const int pcol = (p.mode == 0) ? u : row >> 6;
+    const uint32_t poff = static_cast<uint32_t>(2 * pcol * 128 * kPBox + prow * kPBox);
+    const int sidx = pcol * 128 + prow;
     int64_t fr = 0;                                 // feature of this thread's slab row
     uint4 sl[4];                                    // its half of the row, fetched at the tile start
     Cursor c;
     for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
       if (c.step == 0) {
         const int64_t f0 = tile_f(cluster_id + c.lt * n_clusters) * kTileF;
-        // dX: the tile's first block modulo 4 in a box that starts at it rounded down to 4
-        if (p.mode == 1) scol = static_cast<int>((f0 / kBlock) & 3);
         // slab step 0: this thread copies 32 of the 64 values of feature row f0 + row
         fr = f0 + row;
         const bool fr_ok = fr < p.F;
@@ -333,12 +342,11 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status))) break;
       if (c.step < p.red_steps) {
         const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.q) - base));
-        const int col = (p.mode == 0) ? ((c.step * kSubs + u) & 3) : scol;
         uint32_t L[4], H[4];
-        build_lut(sc[srow + col], L, H);
+        build_lut(sc[sidx], L, H);
         const uint8_t* src = base_ptr + (stage_p(c.q) - base) + poff;
         const uint4 w0 = *reinterpret_cast<const uint4*>(src);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 128 * kPBox);
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         const uint32_t arow = slot_a(c.a) + u * kSubBytes + row * 128;
 #pragma unroll
@@ -464,23 +472,24 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUten
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-int64_t scale_ld(int64_t K) { return (K / kBlock + 3) / 4 * 4; }
+int64_t scale_ld(int64_t N) { return (N + 3) / 4 * 4; }
 int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
 
 // Block-scale job for the prep launch and the tensor map each GEMM stage reads it by.
 PrepJob scales_job(const LinearArgs& a, float* out) {
   PrepJob j{};
   j.kind = kBlockScales;
-  j.width = scale_ld(a.K);
+  j.width = scale_ld(a.N);
+  j.cols = a.N;
   j.fdst = out;
-  j.count = a.N * j.width;
+  j.count = (a.K / kBlock) * j.width;
   return j;
 }
 
-bool scales_map(const LinearArgs& a, int mode, const float* sc, CUtensorMap* map) {
-  const int64_t ldk = scale_ld(a.K);
-  // forward: 128 weight rows x 4 blocks; dX: 128 weight rows (one step of n) x 4 blocks
-  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sc, ldk, a.N, 4 * ldk, 4, mode == 0 ? kTileF : kStepK,
+// Scales [K/64][N padded to 4]: a box of 128 consecutive n by 2 blocks.
+bool scales_map(const LinearArgs& a, const float* sc, CUtensorMap* map) {
+  const int64_t ldn = scale_ld(a.N);
+  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sc, ldn, a.K / kBlock, 4 * ldn, 128, kSubs,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -494,7 +503,7 @@ struct FwdWs {
     Aq = Bp + a1024(2 * rp * N);
     part = Aq + a1024(2 * nq * K);
     scale = part + a1024(adapter_partial_bytes(M, K, r));
-    total = scale + a1024(4 * static_cast<size_t>(N) * scale_ld(K));
+    total = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
   }
 };
 
@@ -512,7 +521,7 @@ struct BwdWs {
     Gt = Tt + a1024(2 * nq * Mp);
     part = Gt + a1024(2 * nq * Mp);
     scale = part + a1024(pb);
-    total = scale + a1024(4 * static_cast<size_t>(N) * scale_ld(K));
+    total = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
   }
 };
 
@@ -583,11 +592,11 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   CUtensorMap tok, packed, slab_t, scale;
   bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kSub, kHalfT,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kStepK / 2, kTileF,
+  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kPBox, kTileF,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kSub, kHalfT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && scales_map(a, 0, sc, &scale);
+  ok = ok && scales_map(a, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 0, y, status);
   gp.slab_f = Bp;
@@ -656,11 +665,11 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   CUtensorMap tok, packed, slab_t, scale;
   bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kTileF / 2, kStepK,
+  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kPBox, kStepK,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kSub, kHalfT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && scales_map(a, 1, sc, &scale);
+  ok = ok && scales_map(a, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 1, dx, status);
   gp.slab_f = ApT;

@@ -52,11 +52,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
       jb.dst[idx] = __float2bfloat16_rn(b < static_cast<uint64_t>(jb.r) ? jb.src[b * jb.cols + a] : 0.0f);
       break;
     }
-    case kBlockScales: {       // fdst[n][kb] = a' of block (n, kb); 0 for kb in [K/64, width)
+    case kBlockScales: {       // fdst[kb][n] = a' of block (n, kb); 0 for n in [N, width)
       split_index(idx, jb.width, &a, &b);
       float v = 0.0f;
-      if (b < static_cast<uint64_t>(p.kbn)) {
-        const uint64_t blk = a * static_cast<uint64_t>(p.kbn) + b;
+      if (b < static_cast<uint64_t>(jb.cols)) {
+        const uint64_t blk = b * static_cast<uint64_t>(p.kbn) + a;
         if (p.w.dq) {
           const uint32_t code = static_cast<const uint8_t*>(p.w.absmax)[blk];
           v = __fadd_rn(__fmul_rn(dyn8[code], p.w.nested[blk >> 8]), *p.w.offset);

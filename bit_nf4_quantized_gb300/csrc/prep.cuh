@@ -10,7 +10,7 @@ enum PrepKind {
   kStageRowsDirect = 1,   // dst[j][c] = bf16(src[j][c]) for j < r; zero rows up to `width` rows
   kStageTransposed = 2,   // dst[j][c] = bf16(src[c][j]), j < r, c < cols; rows of `width`
   kStageColumns = 3,      // dst[c][j] = bf16(src[j][c]) (src rows of `cols`), j < r; rows of `width`
-  kBlockScales = 4,       // fdst[n][kb] = a'(n, kb), kb < K/64; rows of `width` (multiple of 4)
+  kBlockScales = 4,       // fdst[kb][n] = a'(n, kb), n < cols (= N); rows of `width` (multiple of 4)
   kZeroWords = 5          // fdst[i] = 0 (as 32-bit words)
 };
 
