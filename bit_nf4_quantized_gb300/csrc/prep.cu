@@ -20,13 +20,42 @@ __device__ __forceinline__ void split_index(uint64_t idx, uint64_t width, uint64
   }
 }
 
+constexpr int kScaleTile = 32;   // block-scale transpose tile: 32 blocks x 32 weight rows
+
+// a' of block `blk` (two roundings, as the dequantize kernel computes it)
+__device__ __forceinline__ float block_scale(const PrepJobs& p, const float* dyn8, uint64_t blk) {
+  if (!p.w.dq) return static_cast<const float*>(p.w.absmax)[blk];
+  const uint32_t code = static_cast<const uint8_t*>(p.w.absmax)[blk];
+  return __fadd_rn(__fmul_rn(dyn8[code], p.w.nested[blk >> 8]), *p.w.offset);
+}
+
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
   __shared__ float dyn8[256];
+  __shared__ float tile[kScaleTile][kScaleTile + 1];
   dyn8[threadIdx.x] = p.dyn8[threadIdx.x];
   __syncthreads();
   int j = 0;
   while (j + 1 < p.n && blockIdx.x >= p.job[j + 1].first_block) ++j;
   const PrepJob& jb = p.job[j];
+  if (jb.kind == kBlockScales) {
+    // fdst[kb][n] = a'(n, kb) for n < N, 0 for n in [N, width): one 32 x 32 tile per CTA,
+    // read along kb (the codes' order) and written along n, both coalesced
+    const int64_t tiles_n = (jb.width + kScaleTile - 1) / kScaleTile;
+    const int64_t t = blockIdx.x - jb.first_block;
+    const int64_t n0 = (t % tiles_n) * kScaleTile, kb0 = (t / tiles_n) * kScaleTile;
+    for (int e = threadIdx.x; e < kScaleTile * kScaleTile; e += kPrepThreads) {
+      const int nl = e / kScaleTile, kl = e % kScaleTile;
+      const int64_t n = n0 + nl, kb = kb0 + kl;
+      tile[kl][nl] = (n < jb.cols && kb < p.kbn) ? block_scale(p, dyn8, static_cast<uint64_t>(n * p.kbn + kb)) : 0.0f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kScaleTile * kScaleTile; e += kPrepThreads) {
+      const int kl = e / kScaleTile, nl = e % kScaleTile;
+      const int64_t n = n0 + nl, kb = kb0 + kl;
+      if (n < jb.width && kb < p.kbn) jb.fdst[kb * jb.width + n] = tile[kl][nl];
+    }
+    return;
+  }
   const uint64_t idx = static_cast<uint64_t>(blockIdx.x - jb.first_block) * kPrepThreads + threadIdx.x;
   if (idx >= static_cast<uint64_t>(jb.count)) return;
   uint64_t a, b;
@@ -52,21 +81,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
       jb.dst[idx] = __float2bfloat16_rn(b < static_cast<uint64_t>(jb.r) ? jb.src[b * jb.cols + a] : 0.0f);
       break;
     }
-    case kBlockScales: {       // fdst[kb][n] = a' of block (n, kb); 0 for n in [N, width)
-      split_index(idx, jb.width, &a, &b);
-      float v = 0.0f;
-      if (b < static_cast<uint64_t>(jb.cols)) {
-        const uint64_t blk = b * static_cast<uint64_t>(p.kbn) + a;
-        if (p.w.dq) {
-          const uint32_t code = static_cast<const uint8_t*>(p.w.absmax)[blk];
-          v = __fadd_rn(__fmul_rn(dyn8[code], p.w.nested[blk >> 8]), *p.w.offset);
-        } else {
-          v = static_cast<const float*>(p.w.absmax)[blk];
-        }
-      }
-      jb.fdst[idx] = v;
-      break;
-    }
     case kZeroWords:
       jb.fdst[idx] = 0.0f;
       break;
@@ -80,7 +94,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
 void PrepBuilder::add(const PrepJob& job) {
   PrepJob j = job;
   j.first_block = blocks_;
-  blocks_ += static_cast<int>((j.count + kPrepThreads - 1) / kPrepThreads);
+  if (j.kind == kBlockScales)   // one CTA per 32 x 32 tile
+    blocks_ += static_cast<int>(((j.width + kScaleTile - 1) / kScaleTile) *
+                                ((jobs_.kbn + kScaleTile - 1) / kScaleTile));
+  else
+    blocks_ += static_cast<int>((j.count + kPrepThreads - 1) / kPrepThreads);
   jobs_.job[jobs_.n++] = j;
 }
 
