@@ -99,24 +99,61 @@ struct GemmParams {
   int slab_ld;         // padded rank
   __nv_bfloat16* out;  // [M, F]
   int* status;
+  // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
+  // round of clusters) in `split` parts along the contraction, `chunk` decode steps each;
+  // the last part runs the slab steps and adds the other parts' partial sums, which
+  // they leave in part_ws ([slot][part < split-1][rank][256 tokens][128 rows] fp32) with
+  // one flag per (slot, part, rank, epilogue warp) in part_flags (zero at launch)
+  int64_t full_units, total_units;
+  int split, chunk;
+  float* part_ws;
+  int* part_flags;
 };
 
-// Position in the step sequence that every role walks, advanced without divisions:
-// the step within the tile and the slot and phase of each ring.
-struct Cursor {
-  int step = 0;
+struct Unit {
+  int64_t tile;      // tile pair index
+  int red0, nred;    // decode steps [red0, red0 + nred)
+  int nslab;         // slab steps (last part only)
+  int part;          // 0 .. split-1 (0 for a whole tile)
+  int nparts;        // 1 for a whole tile
+  int64_t slot;      // index of a split tile among the split tiles
+};
+
+__device__ __forceinline__ Unit unit_of(const GemmParams& p, int64_t u) {
+  Unit x;
+  if (u < p.full_units) {
+    x.tile = u;
+    x.red0 = 0;
+    x.nred = p.red_steps;
+    x.nslab = p.slab_steps;
+    x.part = 0;
+    x.nparts = 1;
+    x.slot = 0;
+  } else {
+    const int64_t v = u - p.full_units;
+    x.slot = v / p.split;
+    x.part = static_cast<int>(v - x.slot * p.split);
+    x.tile = p.full_units + x.slot;
+    x.red0 = x.part * p.chunk;
+    x.nred = min(p.chunk, p.red_steps - x.red0);
+    x.nslab = x.part == p.split - 1 ? p.slab_steps : 0;
+    x.nparts = p.split;
+  }
+  return x;
+}
+
+// Slots and phases of the three rings, advanced once per step by every role.
+struct Ring {
   int s = 0;
   uint32_t ph = 0;
   int q = 0;
   uint32_t pq = 0;
   int a = 0;
   uint32_t pa = 0;
-  int64_t lt = 0;
-  __device__ __forceinline__ void advance(int steps) {
+  __device__ __forceinline__ void advance() {
     if (++s == kStages) s = 0, ph ^= 1u;
     if (++q == kPStages) q = 0, pq ^= 1u;
     if (++a == kAStages) a = 0, pa ^= 1u;
-    if (++step == steps) step = 0, ++lt;
   }
 };
 
@@ -177,33 +214,32 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int64_t total_pairs = static_cast<int64_t>(p.tiles_t) * p.pairs_f;
-  const int steps = p.red_steps + p.slab_steps;
-  const int64_t my_tiles =
-      cluster_id < total_pairs ? (total_pairs - cluster_id + n_clusters - 1) / n_clusters : 0;
-  const int64_t total_it = my_tiles * steps;    // every role walks the same step sequence
+  // every role walks the same units (cluster_id, + n_clusters, ...) and steps
+  auto unit_at = [&](int64_t lt) { return cluster_id + lt * n_clusters; };
 
   if (warp == 0) {
     // ---------------- TMA producer: token ring ----------------
     if (lane == 0) {
       bool ok = true;
-      Cursor c;
-      int th = 0;
-      int64_t it = 0;
-      for (; it < total_it; ++it, c.advance(steps)) {
-        if (c.step == 0)
-          th = static_cast<int>(tile_t(cluster_id + c.lt * n_clusters) * kTileT) + static_cast<int>(rank) * kHalfT;
-        const int s = c.s;
-        if (!mbar_wait(bar(kBarEmptyB + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        if (c.step < p.red_steps) {
-          const int k0 = c.step * kStepK;
-          if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubs * kSubBytes);
+      Ring c;
+      int64_t issued = 0;
+      for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
+        const Unit un = unit_of(p, unit_at(lt));
+        const int th = static_cast<int>(tile_t(un.tile) * kTileT) + static_cast<int>(rank) * kHalfT;
+        for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
+          const int s = c.s;
+          if (!mbar_wait(bar(kBarEmptyB + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (st < un.nred) {
+            const int k0 = (un.red0 + st) * kStepK;
+            if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubs * kSubBytes);
 #pragma unroll
-          for (int u = 0; u < kSubs; ++u)
-            tma_load_2d_pair(stage_b(s) + u * kSubBytes, &tm_tok, lead_bar(kBarFullB + s), k0 + u * kSub, th);
-        } else {
-          if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubBytes);
-          tma_load_2d_pair(stage_b(s), &tm_slab_t, lead_bar(kBarFullB + s), (c.step - p.red_steps) * kSub, th);
+            for (int u = 0; u < kSubs; ++u)
+              tma_load_2d_pair(stage_b(s) + u * kSubBytes, &tm_tok, lead_bar(kBarFullB + s), k0 + u * kSub, th);
+          } else {
+            if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubBytes);
+            tma_load_2d_pair(stage_b(s), &tm_slab_t, lead_bar(kBarFullB + s), (st - un.nred) * kSub, th);
+          }
+          ++issued;
         }
       }
       if (ok) {
@@ -221,7 +257,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       } else if (rank == 0) {  // let copies already in flight land before the CTA exits
         int ds = c.s;
         uint32_t dph = c.ph;
-        for (int64_t k = 0; k < kStages && k < it; ++k) {
+        for (int64_t k = 0; k < kStages && k < issued; ++k) {
           if (ds == 0) ds = kStages - 1, dph ^= 1u;
           else --ds;
           mbar_drain(bar(kBarFullB + ds), dph);
@@ -232,35 +268,38 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
     // ---------------- TMA producer: code ring ----------------
     if (lane == 0) {
       bool ok = true;
-      Cursor c;
-      int f0 = 0;
-      int64_t it = 0;
-      for (; it < total_it; ++it, c.advance(steps)) {
-        if (c.step == 0) f0 = static_cast<int>(tile_f(cluster_id + c.lt * n_clusters) * kTileF);
-        const int q = c.q;
-        if (!mbar_wait(bar(kBarEmptyP + q), c.pq ^ 1u, abort_flag, p.status)) { ok = false; break; }
-        if (c.step < p.red_steps) {
-          const int k0 = c.step * kStepK;
-          mbar_expect_tx(bar(kBarFullP + q), kPBytes + kScaleBytes);
-          // forward: rows are weight rows f, bytes run along k; dX: rows are weight rows n
-          // (the contraction), bytes run along the features f
-          const int px = p.mode == 0 ? k0 / 2 : f0 / 2, py = p.mode == 0 ? f0 : k0;
+      Ring c;
+      int64_t issued = 0;
+      for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
+        const Unit un = unit_of(p, unit_at(lt));
+        const int f0 = static_cast<int>(tile_f(un.tile) * kTileF);
+        for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
+          const int q = c.q;
+          if (!mbar_wait(bar(kBarEmptyP + q), c.pq ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (st < un.nred) {
+            const int k0 = (un.red0 + st) * kStepK;
+            mbar_expect_tx(bar(kBarFullP + q), kPBytes + kScaleBytes);
+            // forward: rows are weight rows f, bytes run along k; dX: rows are weight rows n
+            // (the contraction), bytes run along the features f
+            const int px = p.mode == 0 ? k0 / 2 : f0 / 2, py = p.mode == 0 ? f0 : k0;
 #pragma unroll
-          for (int cb = 0; cb < kPBytes / (128 * kPBox); ++cb)
-            tma_load_2d(stage_p(q) + cb * 128 * kPBox, &tm_packed, bar(kBarFullP + q), px + cb * kPBox, py);
-          // scales [kb][n]: forward blocks (f0.., 2 steps of k), dX blocks (k0.., the tile's 2 of f)
-          if (p.mode == 0)
-            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), f0, k0 / kBlock);
-          else
-            tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), k0, f0 / kBlock);
-        } else {
-          mbar_arrive(bar(kBarFullP + q));   // slab steps read no codes; keep the ring in step
+            for (int cb = 0; cb < kPBytes / (128 * kPBox); ++cb)
+              tma_load_2d(stage_p(q) + cb * 128 * kPBox, &tm_packed, bar(kBarFullP + q), px + cb * kPBox, py);
+            // scales [kb][n]: forward blocks (f0.., 2 steps of k), dX blocks (k0.., the tile's 2 of f)
+            if (p.mode == 0)
+              tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), f0, k0 / kBlock);
+            else
+              tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), k0, f0 / kBlock);
+          } else {
+            mbar_arrive(bar(kBarFullP + q));   // slab steps read no codes; keep the ring in step
+          }
+          ++issued;
         }
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
         int dq = c.q;
         uint32_t dpq = c.pq;
-        for (int64_t k = 0; k < kPStages && k < it; ++k) {
+        for (int64_t k = 0; k < kPStages && k < issued; ++k) {
           if (dq == 0) dq = kPStages - 1, dpq ^= 1u;
           else --dq;
           mbar_drain(bar(kBarFullP + dq), dpq);
@@ -272,42 +311,49 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       // ---------------- MMA issuer (even CTA) ----------------
       const uint32_t idesc_main = idesc_bf16(kCluster * kTileF, kTileT, p.mode == 1 ? 1u : 0u);
       const uint32_t idesc_slab = idesc_bf16(kCluster * kTileF, kTileT, 0u);
-      Cursor c;
-      for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
-        const uint32_t b = static_cast<uint32_t>(c.lt) & 1u;
-        if (c.step == 0) {
-          if (!mbar_wait(bar(kBarAccEmpty + b), (static_cast<uint32_t>(c.lt >> 1) & 1u) ^ 1u, abort_flag, p.status))
-            break;
-          tc_fence_after();
-        }
-        if (!mbar_wait(bar(kBarFullB + c.s), c.ph, abort_flag, p.status) ||
-            !mbar_wait(bar(kBarAReady + c.a), c.pa, abort_flag, p.status))
+      bool ok = true;
+      Ring c;
+      for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
+        const Unit un = unit_of(p, unit_at(lt));
+        const int nsteps = un.nred + un.nslab;
+        const uint32_t b = static_cast<uint32_t>(lt) & 1u;
+        if (!mbar_wait(bar(kBarAccEmpty + b), (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
+          ok = false;
           break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kTileT;
-        if (c.step < p.red_steps) {
+        for (int st = 0; st < nsteps; ++st, c.advance()) {
+          if (!mbar_wait(bar(kBarFullB + c.s), c.ph, abort_flag, p.status) ||
+              !mbar_wait(bar(kBarAReady + c.a), c.pa, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (st < un.nred) {
 #pragma unroll
-          for (int u = 0; u < kSubs; ++u)
+            for (int u = 0; u < kSubs; ++u)
 #pragma unroll
-            for (int kk = 0; kk < kSub / 16; ++kk) {
-              // K-major: 32 bytes per 16-element k step inside the 128-byte row.
-              // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
-              // 64-feature halves of the sub-block are 8192 bytes apart.
-              const uint32_t sa = slot_a(c.a) + u * kSubBytes;
-              const uint64_t adesc = p.mode == 1 ? smem_desc(sa + kk * 2048, 8192, 1024)
-                                                 : smem_desc(sa + kk * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc(stage_b(c.s) + u * kSubBytes + kk * 32, 16, 1024);
-              umma_bf16_pair(d_tmem, adesc, bdesc, idesc_main, (c.step > 0 || u > 0 || kk > 0) ? 1u : 0u);
-            }
-        } else {
+              for (int kk = 0; kk < kSub / 16; ++kk) {
+                // K-major: 32 bytes per 16-element k step inside the 128-byte row.
+                // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
+                // 64-feature halves of the sub-block are 8192 bytes apart.
+                const uint32_t sa = slot_a(c.a) + u * kSubBytes;
+                const uint64_t adesc = p.mode == 1 ? smem_desc(sa + kk * 2048, 8192, 1024)
+                                                   : smem_desc(sa + kk * 32, 16, 1024);
+                const uint64_t bdesc = smem_desc(stage_b(c.s) + u * kSubBytes + kk * 32, 16, 1024);
+                umma_bf16_pair(d_tmem, adesc, bdesc, idesc_main, (st > 0 || u > 0 || kk > 0) ? 1u : 0u);
+              }
+          } else {
 #pragma unroll
-          for (int kk = 0; kk < kSub / 16; ++kk)
-            umma_bf16_pair(d_tmem, smem_desc(slot_a(c.a) + kk * 32, 16, 1024),
-                           smem_desc(stage_b(c.s) + kk * 32, 16, 1024), idesc_slab, 1u);
+            for (int kk = 0; kk < kSub / 16; ++kk)
+              umma_bf16_pair(d_tmem, smem_desc(slot_a(c.a) + kk * 32, 16, 1024),
+                             smem_desc(stage_b(c.s) + kk * 32, 16, 1024), idesc_slab, (st > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit_pair_mc(bar(kBarEmptyB + c.s), 0x3);   // frees token stage s in both CTAs
+          umma_commit_pair_mc(bar(kBarAEmpty + c.a), 0x3);   // and A slot a
+          if (st == nsteps - 1) umma_commit_pair_mc(bar(kBarAccFull + b), 0x3);
         }
-        umma_commit_pair_mc(bar(kBarEmptyB + c.s), 0x3);   // frees token stage s in both CTAs
-        umma_commit_pair_mc(bar(kBarAEmpty + c.a), 0x3);   // and A slot a
-        if (c.step == steps - 1) umma_commit_pair_mc(bar(kBarAccFull + b), 0x3);
       }
     }
   } else if (warp < 10) {
@@ -324,86 +370,134 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
     const int pcol = (p.mode == 0) ? u : row >> 6;
     const uint32_t poff = static_cast<uint32_t>(2 * pcol * 128 * kPBox + prow * kPBox);
     const int sidx = pcol * 128 + prow;
-    int64_t fr = 0;                                 // feature of this thread's slab row
-    uint4 sl[4];                                    // its half of the row, fetched at the tile start
-    Cursor c;
-    for (int64_t it = 0; it < total_it; ++it, c.advance(steps)) {
-      if (c.step == 0) {
-        const int64_t f0 = tile_f(cluster_id + c.lt * n_clusters) * kTileF;
-        // slab step 0: this thread copies 32 of the 64 values of feature row f0 + row
-        fr = f0 + row;
-        const bool fr_ok = fr < p.F;
+    bool ok = true;
+    Ring c;
+    for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
+      const Unit un = unit_of(p, unit_at(lt));
+      // slab steps: this thread copies 32 of the 64 values of feature row f0 + row,
+      // the first slab step's fetched before the unit's decode steps
+      const int64_t fr = tile_f(un.tile) * kTileF + row;
+      const bool fr_ok = fr < p.F;
+      uint4 sl[4];
+      if (un.nslab > 0) {
         const uint4* src = reinterpret_cast<const uint4*>(p.slab_f + (fr_ok ? fr : 0) * p.slab_ld) + u * 4;
 #pragma unroll
         for (int q = 0; q < 4; ++q) sl[q] = fr_ok ? src[q] : make_uint4(0, 0, 0, 0);
       }
-      // every slot's full_p phase is waited, in order, so that none is ever two phases behind
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.q), c.pq, abort_flag, p.status))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status))) break;
-      if (c.step < p.red_steps) {
-        const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.q) - base));
-        uint32_t L[4], H[4];
-        build_lut(sc[sidx], L, H);
-        const uint8_t* src = base_ptr + (stage_p(c.q) - base) + poff;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(src);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 128 * kPBox);
-        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const uint32_t arow = slot_a(c.a) + u * kSubBytes + row * 128;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t o[4];
-          decode8(words[i], L, H, o);
-          const uint32_t dst = arow + ((static_cast<uint32_t>(i) ^ sw) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                       "r"(o[3])
-                       : "memory");
+      for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
+        // every slot's phases are waited, in order, so that none is ever two phases behind
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.q), c.pq, abort_flag, p.status)) ||
+            !__all_sync(0xffffffffu, mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status))) {
+          ok = false;
+          break;
         }
-      } else {
-        // adapter slab: the 128 x 64 bf16 tile of the feature-side factor, K-major,
-        // 32 values (four 16-byte chunks) per thread
-        const int j = c.step - p.red_steps;
-        if (j > 0) {
-          const uint4* src =
-              reinterpret_cast<const uint4*>(p.slab_f + (fr < p.F ? fr : 0) * p.slab_ld + j * kSub) + u * 4;
+        if (st < un.nred) {
+          const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.q) - base));
+          uint32_t L[4], H[4];
+          build_lut(sc[sidx], L, H);
+          const uint8_t* src = base_ptr + (stage_p(c.q) - base) + poff;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(src + 128 * kPBox);
+          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const uint32_t arow = slot_a(c.a) + u * kSubBytes + row * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) sl[q] = fr < p.F ? src[q] : make_uint4(0, 0, 0, 0);
-        }
-        const uint32_t arow = slot_a(c.a) + row * 128;
+          for (int i = 0; i < 8; ++i) {
+            uint32_t o[4];
+            decode8(words[i], L, H, o);
+            const uint32_t dst = arow + ((static_cast<uint32_t>(i) ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                         "r"(o[3])
+                         : "memory");
+          }
+        } else {
+          // adapter slab: the 128 x 64 bf16 tile of the feature-side factor, K-major,
+          // 32 values (four 16-byte chunks) per thread
+          const int j = st - un.nred;
+          if (j > 0) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(p.slab_f + (fr_ok ? fr : 0) * p.slab_ld + j * kSub) + u * 4;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t dst = arow + (((static_cast<uint32_t>(u * 4 + q)) ^ sw) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sl[q].x), "r"(sl[q].y),
-                       "r"(sl[q].z), "r"(sl[q].w)
-                       : "memory");
+            for (int q = 0; q < 4; ++q) sl[q] = fr_ok ? src[q] : make_uint4(0, 0, 0, 0);
+          }
+          const uint32_t arow = slot_a(c.a) + row * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t dst = arow + (((static_cast<uint32_t>(u * 4 + q)) ^ sw) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sl[q].x), "r"(sl[q].y),
+                         "r"(sl[q].z), "r"(sl[q].w)
+                         : "memory");
+          }
         }
-      }
-      // the rows are read by this SM's tensor core (a pair MMA takes each CTA's A rows
-      // from that CTA's shared memory): make them visible to the async proxy, then
-      // tell the even CTA, and hand the code slot back to the producer
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(kBarEmptyP + c.q));
-        mbar_arrive_remote(lead_bar(kBarAReady + c.a));
+        // the rows are read by this SM's tensor core (a pair MMA takes each CTA's A rows
+        // from that CTA's shared memory): make them visible to the async proxy, then
+        // tell the even CTA, and hand the code slot back to the producer
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kBarEmptyP + c.q));
+          mbar_arrive_remote(lead_bar(kBarAReady + c.a));
+        }
       }
     }
   } else {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    for (int64_t lt = 0; lt < my_tiles; ++lt) {
-      const int64_t tile = cluster_id + lt * n_clusters;
+    const int lrow = quarter * 32 + lane;       // this thread's row of the CTA's 128
+    for (int64_t lt = 0; unit_at(lt) < p.total_units; ++lt) {
+      const Unit un = unit_of(p, unit_at(lt));
       const uint32_t b = static_cast<uint32_t>(lt) & 1u;
       const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), aph, abort_flag, p.status))) break;
       tc_fence_after();
-      const int64_t t0 = tile_t(tile) * kTileT;
-      const int64_t f = tile_f(tile) * kTileF + quarter * 32 + lane;
+      const int64_t t0 = tile_t(un.tile) * kTileT;
+      const int64_t f = tile_f(un.tile) * kTileF + lrow;
       const uint32_t taddr = tmem_base + b * kTileT + (static_cast<uint32_t>(quarter * 32) << 16);
+      // partial sums of a split tile: [slot][part][rank][256][128] fp32, coalesced along rows
+      auto part_buf = [&](int part) {
+        return p.part_ws + ((un.slot * (p.split - 1) + part) * kCluster + rank) * (static_cast<int64_t>(kTileT) * 128);
+      };
+      auto part_flag = [&](int part) {
+        return p.part_flags + ((un.slot * (p.split - 1) + part) * kCluster + rank) * 4 + quarter;
+      };
+      bool have_parts = true;
+      if (un.nparts > 1 && un.part == un.nparts - 1) {
+        // wait (bounded) for the other parts of this tile, rows of this warp only
+        for (int q = 0; q < un.nparts - 1 && have_parts; ++q) {
+          const int* flag = part_flag(q);
+          const uint64_t w0 = global_ns();
+          int v = 0;
+          for (uint32_t i = 0;; ++i) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+            if (v != 0) break;
+            if ((i & 31u) == 31u && (*abort_flag || global_ns() - w0 > kWaitLimitNs)) {
+              if (!*abort_flag) {
+                *abort_flag = 1;
+                atomicCAS(p.status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
+              }
+              break;
+            }
+          }
+          have_parts = __all_sync(0xffffffffu, v != 0);
+        }
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < kTileT; c0 += 16) {
         uint32_t v[16];
         tmem_ld16(taddr + c0, v);
         tmem_ld_wait();
+        if (un.part < un.nparts - 1) {
+          float* dst = part_buf(un.part) + static_cast<int64_t>(c0) * 128 + lrow;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(v[j]);
+          continue;
+        }
+        if (un.nparts > 1 && have_parts) {
+          for (int q = 0; q < un.nparts - 1; ++q) {   // parts in order: deterministic sums
+            const float* src = part_buf(q) + static_cast<int64_t>(c0) * 128 + lrow;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(src + j * 128));
+          }
+        }
         if (f < p.F) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -411,6 +505,11 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
             if (m < p.M) p.out[m * p.F + f] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
         }
+      }
+      if (un.part < un.nparts - 1) {   // publish this warp's rows of the partial sums
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(part_flag(un.part)), "r"(1) : "memory");
       }
       tc_fence_before();
       __syncwarp();
@@ -437,6 +536,33 @@ int sm_count() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
+}
+
+constexpr int kMaxPartTiles = 80;   // partial-sum tiles (of a cluster pair) a split may use
+constexpr int kMaxSplit = 4;
+constexpr size_t kPartTileBytes = static_cast<size_t>(kCluster) * kTileT * 128 * sizeof(float);
+constexpr size_t kPartFlagBytes = static_cast<size_t>(kMaxPartTiles) * kCluster * 4 * sizeof(int);
+
+// Work units: whole tiles for every full round of clusters; the tiles of a last, partial
+// round are split along the contraction into as many parts as idle clusters allow.
+void split_tail(GemmParams* p, int64_t pairs, int64_t clusters) {
+  const int64_t rounds = pairs / clusters, tail = pairs - rounds * clusters;
+  p->full_units = pairs;
+  p->total_units = pairs;
+  p->split = 1;
+  p->chunk = p->red_steps;
+  if (rounds == 0 || tail == 0) return;
+  int split = static_cast<int>(std::min<int64_t>(clusters / tail, kMaxSplit));
+  split = std::min(split, p->red_steps);
+  while (split > 1 && tail * (split - 1) > kMaxPartTiles) --split;
+  if (split < 2) return;
+  const int chunk = (p->red_steps + split - 1) / split;
+  split = (p->red_steps + chunk - 1) / chunk;   // every part keeps at least one decode step
+  if (split < 2) return;
+  p->full_units = rounds * clusters;
+  p->total_units = p->full_units + tail * split;
+  p->split = split;
+  p->chunk = chunk;
 }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUtensorMap& packed,
@@ -466,8 +592,10 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUten
   const int64_t pairs = static_cast<int64_t>(p.tiles_t) * p.pairs_f;
   const int64_t clusters = pairs < max_clusters ? pairs : max_clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster));
+  GemmParams q = p;
+  split_tail(&q, pairs, clusters);
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, nf4_tc_gemm, tok, packed, slab_t, scale, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, nf4_tc_gemm, tok, packed, slab_t, scale, q);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -486,6 +614,14 @@ PrepJob scales_job(const LinearArgs& a, float* out) {
   return j;
 }
 
+PrepJob zero_flags_job(void* flags) {
+  PrepJob j{};
+  j.kind = kZeroWords;
+  j.fdst = static_cast<float*>(flags);
+  j.count = static_cast<int64_t>(kPartFlagBytes / sizeof(int));
+  return j;
+}
+
 // Scales [K/64][N padded to 4]: a box of 128 consecutive n by 2 blocks.
 bool scales_map(const LinearArgs& a, const float* sc, CUtensorMap* map) {
   const int64_t ldn = scale_ld(a.N);
@@ -494,26 +630,30 @@ bool scales_map(const LinearArgs& a, const float* sc, CUtensorMap* map) {
 }
 
 // Workspace layouts (every part 1024-byte aligned).
+// `part` holds the skinny passes' partial sums and, while the NF4 GEMM runs (never at the
+// same time), its split tiles' partial sums; `flags` the GEMM's per-part flags.
 struct FwdWs {
-  size_t sTp, Bp, Aq, part, scale, total;
+  size_t sTp, Bp, Aq, part, scale, flags, total;
   FwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r);
     sTp = 0;
     Bp = sTp + a1024(2 * rp * M);
     Aq = Bp + a1024(2 * rp * N);
     part = Aq + a1024(2 * nq * K);
-    scale = part + a1024(adapter_partial_bytes(M, K, r));
-    total = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
+    scale = part + a1024(std::max(adapter_partial_bytes(M, K, r), kMaxPartTiles * kPartTileBytes));
+    flags = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
+    total = flags + a1024(kPartFlagBytes);
   }
 };
 
 struct BwdWs {
-  size_t sGp, ApT, Bt, Tt, Gt, part, scale, total;
+  size_t sGp, ApT, Bt, Tt, Gt, part, scale, flags, total;
   BwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r), Mp = pad8(M);
     size_t pb = adapter_partial_bytes(M, N, r);
     pb = std::max(pb, adapter_partial_bytes(N, M, r));
     pb = std::max(pb, adapter_partial_bytes(K, M, r));
+    pb = std::max(pb, kMaxPartTiles * kPartTileBytes);
     sGp = 0;
     ApT = sGp + a1024(2 * rp * M);
     Bt = ApT + a1024(2 * rp * K);
@@ -521,7 +661,8 @@ struct BwdWs {
     Gt = Tt + a1024(2 * nq * Mp);
     part = Gt + a1024(2 * nq * Mp);
     scale = part + a1024(pb);
-    total = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
+    flags = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
+    total = flags + a1024(kPartFlagBytes);
   }
 };
 
@@ -583,6 +724,7 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
     b.count = a.N * rp;
     prep.add(b);
     prep.add(scales_job(a, sc));
+    prep.add(zero_flags_job(w + L.flags));
   }
   cudaError_t e = prep.launch(st);
   if (e != cudaSuccess) return e;
@@ -600,6 +742,8 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 0, y, status);
   gp.slab_f = Bp;
+  gp.part_ws = part;
+  gp.part_flags = reinterpret_cast<int*>(w + L.flags);
   return launch_gemm(gp, tok, packed, slab_t, scale, st);
 }
 
@@ -652,6 +796,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
     c.count = a.K * rp;
     prep.add(c);
     prep.add(scales_job(a, sc));
+    prep.add(zero_flags_job(w + L.flags));
   }
   cudaError_t e = prep.launch(st);
   if (e != cudaSuccess) return e;
@@ -673,6 +818,8 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 1, dx, status);
   gp.slab_f = ApT;
+  gp.part_ws = part;
+  gp.part_flags = reinterpret_cast<int*>(w + L.flags);
   if ((e = launch_gemm(gp, tok, packed, slab_t, scale, st)) != cudaSuccess) return e;
   // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
   if ((e = adapter_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, part, status, &ns, st)) != cudaSuccess) return e;

@@ -92,6 +92,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
 }  // namespace
 
 void PrepBuilder::add(const PrepJob& job) {
+  if (jobs_.n == kMaxPrepJobs) {
+    overflow_ = true;
+    return;
+  }
   PrepJob j = job;
   j.first_block = blocks_;
   if (j.kind == kBlockScales)   // one CTA per 32 x 32 tile
@@ -103,6 +107,7 @@ void PrepBuilder::add(const PrepJob& job) {
 }
 
 cudaError_t PrepBuilder::launch(cudaStream_t st) {
+  if (overflow_) return cudaErrorInvalidValue;
   if (jobs_.n == 0) return cudaSuccess;
   const DecodeTables& t = decode_tables();
   for (int i = 0; i < 256; ++i) jobs_.dyn8[i] = t.dyn8[i];

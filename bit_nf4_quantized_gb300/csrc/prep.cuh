@@ -27,7 +27,7 @@ struct PrepJob {
   int first_block;        // set by PrepBuilder
 };
 
-constexpr int kMaxPrepJobs = 6;
+constexpr int kMaxPrepJobs = 8;
 
 struct PrepJobs {
   PrepJob job[kMaxPrepJobs];
@@ -44,12 +44,13 @@ class PrepBuilder {
     jobs_.w = w;
     jobs_.kbn = K / kBlock;
   }
-  void add(const PrepJob& job);
+  void add(const PrepJob& job);   // at most kMaxPrepJobs; further jobs make launch() fail
   cudaError_t launch(cudaStream_t st);
 
  private:
   PrepJobs jobs_{};
   int blocks_ = 0;
+  bool overflow_ = false;
 };
 
 }  // namespace qnf4

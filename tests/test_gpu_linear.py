@@ -108,6 +108,17 @@ def test_llama8b_layer_sampled_rows(lib, name):
     _run_case(c["M"], N, K, c["r"], c["alpha"], "bf16", seed=K, dist="t", rows=rows)
 
 
+@pytest.mark.parametrize("N,K", [(1344, 1344), (1344, 320)])
+def test_bf16_partial_last_round(lib, N, K):
+    """4096 tokens with 1344 features make 96 tile pairs: more than one round of clusters,
+    with a partial last round whose tiles the GEMM splits along the contraction (the
+    parts' partial sums are added in a fixed order).  K = 320 leaves a half-filled last
+    128-deep step; rows near the tile edges are always checked."""
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([rng.choice(4096, 96, replace=False), [0, 255, 256, 3583, 3584, 4095]]))
+    _run_case(4096, N, K, 16, 16.0, "bf16", seed=N + K, rows=rows)
+
+
 def test_empty_batch(lib):
     q, _ = _quantized_weight(64, 128, 1)
     A = torch.randn(4, 128, device=DEV)
