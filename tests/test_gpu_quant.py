@@ -55,6 +55,37 @@ def test_quantize_bit_exact(lib, n, dtype, dq):
     assert binding.device_status() == binding.NF4_OK
 
 
+def test_quantize_near_every_threshold(lib):
+    """Values whose quotient x/a lands within a few ulps of each midpoint between
+    neighbouring NF4 values, under block maxima that are not powers of two (so that
+    x * RN(1/a) and RN(x/a) can round differently): codes must be those of the IEEE
+    quotient, as the oracle's exact nearest-value search takes them."""
+    nf4 = cb.nf4_codebook().astype(np.float64)
+    mids = (nf4[:-1] + nf4[1:]) / 2
+    rng = np.random.default_rng(11)
+    blocks = []
+    for _ in range(256):
+        a = np.float32(rng.uniform(0.5, 2.0) * 2.0 ** int(rng.integers(-20, 20)))
+        probes = []
+        for m in mids:
+            v0 = np.float32(m * np.float64(a))
+            for k in range(-3, 4):
+                v = v0
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, np.float32(np.inf if k > 0 else -np.inf))
+                probes.append(min(max(v, -a), a))
+        probes = rng.permutation(np.array(probes, np.float32))
+        for c0 in range(0, len(probes), 63):   # every block: its maximum a, then 63 probes
+            chunk = probes[c0:c0 + 63]
+            blocks.append(np.concatenate([[a], chunk, np.zeros(63 - len(chunk), np.float32)]))
+    x = np.concatenate(blocks).astype(np.float32)
+    xd = _to_device(x, torch.float32)
+    q = binding.nf4_quantize(xd, double_quant=False)
+    ref = onf4.quantize(_host_values(xd), double_quant=False)
+    _assert_same_quant(q, ref)
+    assert binding.device_status() == binding.NF4_OK
+
+
 def test_quantize_special_blocks(lib):
     nf4 = cb.nf4_codebook()
     x = np.zeros(64 * 300 + 5, np.float32)
