@@ -96,7 +96,7 @@ struct GemmParams {
                        // second tile past F (loads read zeros, the epilogue stores nothing)
   int f_fast;          // pair order: 1 = feature pairs vary fastest (dX), 0 = token tiles (forward)
   const __nv_bfloat16* slab_f;   // adapter factor on the feature side, bf16 [F][slab_ld]
-  int slab_ld;         // padded rank
+  int slab_ld;         // rank rounded up to 16 (zero past the rank)
   __nv_bfloat16* out;  // [M, F]
   int* status;
   // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
@@ -374,16 +374,22 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
     Ring c;
     for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
       const Unit un = unit_of(p, unit_at(lt));
-      // slab steps: this thread copies 32 of the 64 values of feature row f0 + row,
-      // the first slab step's fetched before the unit's decode steps
+      // slab steps: this thread supplies 32 of the 64 ranks of feature row f0 + row from the
+      // bf16 staging (16-rank chunks, zero past slab_ld); the first slab step's are fetched
+      // before the unit's decode steps and only used at the slab step
       const int64_t fr = tile_f(un.tile) * kTileF + row;
       const bool fr_ok = fr < p.F;
       uint4 sl[4];
-      if (un.nslab > 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.slab_f + (fr_ok ? fr : 0) * p.slab_ld) + u * 4;
+      auto load_slab = [&](int j) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) sl[q] = fr_ok ? src[q] : make_uint4(0, 0, 0, 0);
-      }
+        for (int q = 0; q < 4; ++q) {
+          const int c0 = j * kSub + u * 32 + q * 8;   // first rank of this 16-byte chunk
+          sl[q] = (fr_ok && c0 < p.slab_ld)
+                      ? *reinterpret_cast<const uint4*>(p.slab_f + fr * p.slab_ld + c0)
+                      : make_uint4(0, 0, 0, 0);
+        }
+      };
+      if (un.nslab > 0) load_slab(0);
       for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
         // every slot's phases are waited, in order, so that none is ever two phases behind
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.q), c.pq, abort_flag, p.status)) ||
@@ -413,12 +419,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
           // adapter slab: the 128 x 64 bf16 tile of the feature-side factor, K-major,
           // 32 values (four 16-byte chunks) per thread
           const int j = st - un.nred;
-          if (j > 0) {
-            const uint4* src =
-                reinterpret_cast<const uint4*>(p.slab_f + (fr_ok ? fr : 0) * p.slab_ld + j * kSub) + u * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) sl[q] = fr_ok ? src[q] : make_uint4(0, 0, 0, 0);
-          }
+          if (j > 0) load_slab(j);
           const uint32_t arow = slot_a(c.a) + row * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -633,12 +634,12 @@ bool scales_map(const LinearArgs& a, const float* sc, CUtensorMap* map) {
 // `part` holds the skinny passes' partial sums and, while the NF4 GEMM runs (never at the
 // same time), its split tiles' partial sums; `flags` the GEMM's per-part flags.
 struct FwdWs {
-  size_t sTp, Bp, Aq, part, scale, flags, total;
+  size_t sTp, Bq, Aq, part, scale, flags, total;
   FwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r);
     sTp = 0;
-    Bp = sTp + a1024(2 * rp * M);
-    Aq = Bp + a1024(2 * rp * N);
+    Bq = sTp + a1024(2 * rp * M);
+    Aq = Bq + a1024(2 * nq * N);
     part = Aq + a1024(2 * nq * K);
     scale = part + a1024(std::max(adapter_partial_bytes(M, K, r), kMaxPartTiles * kPartTileBytes));
     flags = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
@@ -647,7 +648,7 @@ struct FwdWs {
 };
 
 struct BwdWs {
-  size_t sGp, ApT, Bt, Tt, Gt, part, scale, flags, total;
+  size_t sGp, AqT, Bt, Tt, Gt, part, scale, flags, total;
   BwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r), Mp = pad8(M);
     size_t pb = adapter_partial_bytes(M, N, r);
@@ -655,8 +656,8 @@ struct BwdWs {
     pb = std::max(pb, adapter_partial_bytes(K, M, r));
     pb = std::max(pb, kMaxPartTiles * kPartTileBytes);
     sGp = 0;
-    ApT = sGp + a1024(2 * rp * M);
-    Bt = ApT + a1024(2 * rp * K);
+    AqT = sGp + a1024(2 * rp * M);
+    Bt = AqT + a1024(2 * nq * K);
     Tt = Bt + a1024(2 * nq * N);
     Gt = Tt + a1024(2 * nq * Mp);
     part = Gt + a1024(2 * nq * Mp);
@@ -680,7 +681,7 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   p.tiles_f = static_cast<int>((p.F + kTileF - 1) / kTileF);
   p.pairs_f = (p.tiles_f + 1) / 2;
   p.f_fast = mode == 1 ? 1 : 0;
-  p.slab_ld = padded_rank(a.r);
+  p.slab_ld = adapter_nq(a.r);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = status;
   return p;
@@ -699,7 +700,6 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   const FwdWs L(a.M, a.N, a.K, a.r);
   char* w = static_cast<char*>(ws);
   auto* sTp = reinterpret_cast<__nv_bfloat16*>(w + L.sTp);
-  auto* Bp = reinterpret_cast<__nv_bfloat16*>(w + L.Bp);
   auto* Aq = reinterpret_cast<__nv_bfloat16*>(w + L.Aq);
   auto* part = reinterpret_cast<float*>(w + L.part);
   auto* sc = reinterpret_cast<float*>(w + L.scale);
@@ -715,13 +715,13 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
     j.count = static_cast<int64_t>(nq) * a.K;
     prep.add(j);
     PrepJob b{};
-    b.kind = kStageRows;         // B as the slab's A operand: [N][rp]
+    b.kind = kStageRows;         // B as the slab's feature side: [N][nq] bf16
     b.r = a.r;
-    b.width = rp;
+    b.width = nq;
     b.scale = 1.0f;
     b.src = B;
-    b.dst = Bp;
-    b.count = a.N * rp;
+    b.dst = reinterpret_cast<__nv_bfloat16*>(w + L.Bq);
+    b.count = a.N * nq;
     prep.add(b);
     prep.add(scales_job(a, sc));
     prep.add(zero_flags_job(w + L.flags));
@@ -741,7 +741,7 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   ok = ok && scales_map(a, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 0, y, status);
-  gp.slab_f = Bp;
+  gp.slab_f = reinterpret_cast<const __nv_bfloat16*>(w + L.Bq);
   gp.part_ws = part;
   gp.part_flags = reinterpret_cast<int*>(w + L.flags);
   return launch_gemm(gp, tok, packed, slab_t, scale, st);
@@ -756,7 +756,6 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   const BwdWs L(a.M, a.N, a.K, a.r);
   char* w = static_cast<char*>(ws);
   auto* sGp = reinterpret_cast<__nv_bfloat16*>(w + L.sGp);
-  auto* ApT = reinterpret_cast<__nv_bfloat16*>(w + L.ApT);
   auto* Bt = reinterpret_cast<__nv_bfloat16*>(w + L.Bt);
   auto* Tt = reinterpret_cast<__nv_bfloat16*>(w + L.Tt);
   auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + L.Gt);
@@ -787,13 +786,13 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
     g.dst = Gt;
     prep.add(g);
     PrepJob c{};
-    c.kind = kStageColumns;      // A^T: [K][rp]
+    c.kind = kStageColumns;      // A^T as the slab's feature side: [K][nq] bf16
     c.r = a.r;
-    c.width = rp;
+    c.width = nq;
     c.src = A;
-    c.dst = ApT;
+    c.dst = reinterpret_cast<__nv_bfloat16*>(w + L.AqT);
     c.cols = a.K;
-    c.count = a.K * rp;
+    c.count = a.K * nq;
     prep.add(c);
     prep.add(scales_job(a, sc));
     prep.add(zero_flags_job(w + L.flags));
@@ -817,7 +816,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   ok = ok && scales_map(a, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 1, dx, status);
-  gp.slab_f = ApT;
+  gp.slab_f = reinterpret_cast<const __nv_bfloat16*>(w + L.AqT);
   gp.part_ws = part;
   gp.part_flags = reinterpret_cast<int*>(w + L.flags);
   if ((e = launch_gemm(gp, tok, packed, slab_t, scale, st)) != cudaSuccess) return e;
