@@ -346,7 +346,7 @@ def main():
     # per-phase breakdown (the dominant kernel's roofline): the same steps again with the
     # library's per-launch CUDA events on, outside the timed region above
     binding.timing_enable(True)
-    for k in range(5):
+    for k in range(6):
         binding.timing_read(k, reset=True)
     for _ in range(args.steps):
         layer.step()
@@ -354,7 +354,7 @@ def main():
     binding.timing_enable(False)
     sampler.stop()
     kinds = {name: binding.timing_read(k, reset=True) for k, name in
-             enumerate(("quantize", "dequantize", "fwd_gemm", "dx_gemm", "adapter"))}
+             enumerate(("quantize", "dequantize", "fwd_gemm", "dx_gemm", "adapter", "weight_decode"))}
     ms_max = max_over_ranks(ms, world)
 
     M, r = layer.M, layer.r

@@ -3,48 +3,38 @@
 // Math ("Native model adaptation and NF4", sections "One model contract", "Packed
 // NF4 and the portable QLoRA profile", "Fused GPU NF4 decodes inside the matrix
 // kernel"): y = x W^T + s T B^T and dX = dY W + s G A, with W decoded from NF4 on
-// the device and never written to global memory.
+// the device.
 //
-// Kernel nf4_tc_gemm: clusters of two CTAs on neighbouring SMs, persistent over tiles of
+// W is decoded once per call into a bf16 copy in the workspace by the dequantize kernel
+// (bit-exact bf16(nf4[q] * a'), as nf4_dequantize writes it) and the contraction runs as
+// a bf16 GEMM fed entirely by TMA.  Decoding inside the matrix kernel would repeat the
+// decode once per 256-token tile (16 times per call at 4096 tokens) on the CUDA cores,
+// which cannot keep pace with the tensor cores; one decode pass costs 2.5 bytes per weight
+// of HBM traffic instead.
+//
+// Kernel bf16_tc_gemm: clusters of two CTAs on neighbouring SMs, persistent over tiles of
 // 256 output features x 256 tokens.  The pair runs 2-SM tcgen05.mma operations
 // (M = 256, N = 256, K = 16):
-//   D[f, t] (TMEM, fp32) = sum_c Wdec[f, c] * Tok[t, c]  +  sum_j Slab_A[f, j] * Slab_B[t, j]
+//   D[f, t] (TMEM, fp32) = sum_c Wb[f, c] * Tok[t, c]  +  sum_j SlabA[f, j] * SlabB[t, j]
 //   forward: f = rows of W (output features), c = k, Tok = x,  slab (B, s*T)
 //   dX:      f = columns of W (input features), c = n, Tok = dY, slab (A^T, s*G)
-// Each CTA decodes its own 128 feature rows of the A operand and loads one 128-token half
-// of the token tile; the even CTA issues the MMAs, which read both CTAs' shared memory and
-// write each CTA's 128 accumulator rows into its own TMEM.  So every SM receives half the
-// token bytes that a one-SM 128 x 256 tile would need for the same work.
-// The contraction advances in steps of 128 (two 64-deep sub-blocks, one NF4 block each),
-// then in 64-deep adapter slab steps.  Three rings of shared-memory buffers, one slot per
-// step each: this CTA's token half (freed when the pair MMAs have read it), packed codes
-// and block scales (freed as soon as the decoders have read them, so they are refetched
-// well ahead), and bf16 A tiles (decoded weights, or the adapter factor on slab steps).
-// Warp roles (480 threads, in each CTA):
-//   warp 0      TMA producer for the token ring: its half of the token tile (128B-swizzled)
-//               per step, or its half of the s*T / s*G slab tile;
+// Each CTA loads its own 128 feature rows of A and one 128-token half of the token tile;
+// the even CTA issues the MMAs, which read both CTAs' shared memory and write each CTA's
+// 128 accumulator rows into its own TMEM.  The contraction advances 128 deep per step
+// (two 64-deep, 128-byte-swizzled sub-blocks), then in 64-deep adapter slab steps.
+// Warp roles (192 threads, in each CTA):
+//   warp 0      TMA producer: A rows (K-major for the forward, MN-major for dX), the token
+//               half, or the slab tiles, all completing on the even CTA's barrier;
 //   warp 1      TMEM allocation (pair-wide); in the even CTA, lane 0 issues the MMAs;
-//   warps 2..9  decoders: a thread turns one 64-element NF4 block (one 128-byte row of an
-//               A sub-block) into bf16 in the swizzled layout the MMA reads (K-major for the
-//               forward, MN-major for dX), through a per-block scaled lookup table; on slab
-//               steps they copy the bf16 adapter factor rows in from global memory;
-//   warps 10..13 epilogue: tcgen05.ld of this CTA's accumulator rows, bf16 stores;
-//   warp 14     TMA producer for the code ring: packed NF4 tile and block scales per step.
-// Barriers that gate the MMA (stage full, A slot ready, accumulator drained) live in the
-// even CTA; the MMA completion is multicast to both CTAs.
-// The per-block scales a' = dyn8[code] * nested + offset are computed once per call
-// (prep.cu) into an fp32 [K/64][N rounded up to 4] array and reach each step by TMA next
-// to the packed codes, so the decoders never wait on global memory for them.  Codes and
-// scales are laid out in shared memory so that a warp's 32 rows read consecutive words
-// (codes as four 16-byte-wide column boxes), free of bank conflicts.
-// Two accumulators of 256 columns let the epilogue of one tile overlap the
-// main loop of the next.  Every mbarrier wait is bounded in time; a wait that
-// gives up sets NF4_ERR_TIMEOUT in the status word and the CTA winds down,
-// freeing its TMEM.
+//   warps 2..5  epilogue: tcgen05.ld of this CTA's accumulator rows, bf16 stores.
+// Two accumulators of 256 columns let the epilogue of one tile overlap the main loop of
+// the next.  Tiles left for a last, partial round of clusters are split along the
+// contraction; the parts' fp32 partial sums are added in a fixed order.  Every mbarrier
+// wait and the partial-sum flag wait is bounded in time; a wait that gives up sets
+// NF4_ERR_TIMEOUT in the status word and the CTA winds down, freeing its TMEM.
 #include <algorithm>
 
 #include "linear_tc.cuh"
-#include "decode.cuh"
 #include "prep.cuh"
 #include "tc_ptx.cuh"
 
@@ -56,32 +46,23 @@ using namespace tc;
 constexpr int kTileF = 128;                 // feature rows per CTA (the pair MMA's M is 256)
 constexpr int kTileT = 256;                 // MMA N
 constexpr int kSub = 64;                    // one sub-block: 64 deep, 128 bytes of bf16 per row
-constexpr int kSubs = 2;                    // sub-blocks per decode step
-constexpr int kStepK = kSub * kSubs;        // contraction per decode step
+constexpr int kSubs = 2;                    // sub-blocks per step
+constexpr int kStepK = kSub * kSubs;        // contraction per step
 constexpr int kHalfT = kTileT / 2;          // token rows each CTA of a pair loads
 constexpr int kCluster = 2;
 constexpr int kSubBytes = 128 * kSub * 2;   // 16384: a 128-row sub-block of A or of the token half
-constexpr int kPBytes = 128 * kStepK / 2;   // 8192: packed codes per step, as [4][128 rows][16 B]
-constexpr int kPBox = 16;                   // bytes per row of one code box
-constexpr int kScaleBytes = kSubs * 128 * 4;   // 1024: [2 blocks][128 rows] fp32 block scales
-constexpr int kBStageBytes = kSubs * kSubBytes;
-constexpr int kPStageBytes = kPBytes + kScaleBytes;
-constexpr int kABytes = kSubs * kSubBytes;
-constexpr int kStages = 3;                  // token ring
-constexpr int kPStages = 3;                 // code ring
-constexpr int kAStages = 3;                 // A ring
-constexpr int kThreads = 480;               // 15 warps, roles below
+constexpr int kHalfSub = kSubBytes / 2;     // 8192: one 64-feature half of an MN-major sub-block
+constexpr int kStageBytes = 2 * kSubs * kSubBytes;   // A then B: 64 KB
+constexpr int kStages = 3;
+constexpr int kThreads = 192;               // 6 warps, roles above
+constexpr int kWarpEpi = 2;                 // first of the 4 epilogue warps
 constexpr int kTmemCols = 512;
-constexpr int kDecoderWarps = 8;
-// barriers: full_b/empty_b[kStages] full_p/empty_p[kPStages] aready/aempty[kAStages]
-// accfull[2] accempty[2], then the abort flag and the TMEM address
-constexpr int kBarFullB = 0, kBarEmptyB = kStages, kBarFullP = 2 * kStages, kBarEmptyP = 2 * kStages + kPStages,
-              kBarAReady = 2 * kStages + 2 * kPStages, kBarAEmpty = kBarAReady + kAStages,
-              kBarAccFull = kBarAEmpty + kAStages, kBarAccEmpty = kBarAccFull + 2, kNumBars = kBarAccEmpty + 2;
-constexpr int kSmemBytes =
-    1024 + kStages * kBStageBytes + kAStages * kABytes + kPStages * kPStageBytes + kNumBars * 8 + 16;
-static_assert(kBStageBytes % 1024 == 0 && kABytes % 1024 == 0 && kPStageBytes % 1024 == 0,
-              "buffers must stay 1024-byte aligned");
+// barriers: full[kStages] empty[kStages] accfull[2] accempty[2], then the abort flag and
+// the TMEM address
+constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages, kBarAccEmpty = kBarAccFull + 2,
+              kNumBars = kBarAccEmpty + 2;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
+static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct GemmParams {
@@ -95,12 +76,10 @@ struct GemmParams {
   int pairs_f;         // ceil(tiles_f / 2): feature-tile pairs; an odd count leaves the last pair's
                        // second tile past F (loads read zeros, the epilogue stores nothing)
   int f_fast;          // pair order: 1 = feature pairs vary fastest (dX), 0 = token tiles (forward)
-  const __nv_bfloat16* slab_f;   // adapter factor on the feature side, bf16 [F][slab_ld]
-  int slab_ld;         // rank rounded up to 16 (zero past the rank)
   __nv_bfloat16* out;  // [M, F]
   int* status;
   // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
-  // round of clusters) in `split` parts along the contraction, `chunk` decode steps each;
+  // round of clusters) in `split` parts along the contraction, `chunk` steps each;
   // the last part runs the slab steps and adds the other parts' partial sums, which
   // they leave in part_ws ([slot][part < split-1][rank][256 tokens][128 rows] fp32) with
   // one flag per (slot, part, rank, epilogue warp) in part_flags (zero at launch)
@@ -112,7 +91,7 @@ struct GemmParams {
 
 struct Unit {
   int64_t tile;      // tile pair index
-  int red0, nred;    // decode steps [red0, red0 + nred)
+  int red0, nred;    // contraction steps [red0, red0 + nred)
   int nslab;         // slab steps (last part only)
   int part;          // 0 .. split-1 (0 for a whole tile)
   int nparts;        // 1 for a whole tile
@@ -142,38 +121,29 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int64_t u) {
   return x;
 }
 
-// Slots and phases of the three rings, advanced once per step by every role.
+// Slot and phase of the stage ring, advanced once per step by every role.
 struct Ring {
   int s = 0;
   uint32_t ph = 0;
-  int q = 0;
-  uint32_t pq = 0;
-  int a = 0;
-  uint32_t pa = 0;
   __device__ __forceinline__ void advance() {
     if (++s == kStages) s = 0, ph ^= 1u;
-    if (++q == kPStages) q = 0, pq ^= 1u;
-    if (++a == kAStages) a = 0, pa ^= 1u;
   }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_packed,
-            const __grid_constant__ CUtensorMap tm_slab_t, const __grid_constant__ CUtensorMap tm_scale,
-            const GemmParams p) {
+bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_tok,
+             const __grid_constant__ CUtensorMap tm_slab_f, const __grid_constant__ CUtensorMap tm_slab_t,
+             const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kBStageBytes + kAStages * kABytes +
-                                               kPStages * kPStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars) + 1;
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  auto stage_b = [&](int s) { return base + s * kBStageBytes; };
-  auto slot_a = [&](int a) { return base + kStages * kBStageBytes + a * kABytes; };
-  auto stage_p = [&](int q) { return base + kStages * kBStageBytes + kAStages * kABytes + q * kPStageBytes; };
-  auto stage_s = [&](int q) { return stage_p(q) + kPBytes; };
+  auto stage_a = [&](int s) { return base + s * kStageBytes; };
+  auto stage_b = [&](int s) { return base + s * kStageBytes + kSubs * kSubBytes; };
   const uint32_t rank = cluster_ctarank();
   auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
   const int64_t cluster_id = blockIdx.x / kCluster;
@@ -185,16 +155,8 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarFullB + s), 1);     // even CTA: its producer's arrive + both CTAs' token bytes
-      mbar_init(bar(kBarEmptyB + s), 1);    // the pair MMAs' commit
-    }
-    for (int q = 0; q < kPStages; ++q) {
-      mbar_init(bar(kBarFullP + q), 1);                // producer arrive (+ TMA bytes on decode steps)
-      mbar_init(bar(kBarEmptyP + q), kDecoderWarps);   // this CTA's decoder warps
-    }
-    for (int a = 0; a < kAStages; ++a) {
-      mbar_init(bar(kBarAReady + a), kCluster * kDecoderWarps);   // even CTA: both CTAs' decoder warps
-      mbar_init(bar(kBarAEmpty + a), 1);                          // the pair MMAs' commit
+      mbar_init(bar(kBarFull + s), 1);      // even CTA: its producer's arrive + both CTAs' TMA bytes
+      mbar_init(bar(kBarEmpty + s), 1);     // the pair MMAs' commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarAccFull + b), 1);                  // the pair MMAs' commit
@@ -218,7 +180,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
   auto unit_at = [&](int64_t lt) { return cluster_id + lt * n_clusters; };
 
   if (warp == 0) {
-    // ---------------- TMA producer: token ring ----------------
+    // ---------------- TMA producer ----------------
     if (lane == 0) {
       bool ok = true;
       Ring c;
@@ -226,33 +188,42 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
       for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
         const Unit un = unit_of(p, unit_at(lt));
         const int th = static_cast<int>(tile_t(un.tile) * kTileT) + static_cast<int>(rank) * kHalfT;
+        const int f0 = static_cast<int>(tile_f(un.tile) * kTileF);
         for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
           const int s = c.s;
-          if (!mbar_wait(bar(kBarEmptyB + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(bar(kBarEmpty + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t full = lead_bar(kBarFull + s);
           if (st < un.nred) {
             const int k0 = (un.red0 + st) * kStepK;
-            if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubs * kSubBytes);
+            if (rank == 0) mbar_expect_tx(bar(kBarFull + s), kCluster * 2 * kSubs * kSubBytes);
 #pragma unroll
-            for (int u = 0; u < kSubs; ++u)
-              tma_load_2d_pair(stage_b(s) + u * kSubBytes, &tm_tok, lead_bar(kBarFullB + s), k0 + u * kSub, th);
+            for (int u = 0; u < kSubs; ++u) {
+              const uint32_t a = stage_a(s) + u * kSubBytes;
+              if (p.mode == 0) {
+                // forward: 128 rows of W (features f0..) x 64 of k, K-major
+                tma_load_2d_pair(a, &tm_w, full, k0 + u * kSub, f0);
+              } else {
+                // dX: rows n of W are the contraction; two 64-feature halves, MN-major
+                tma_load_2d_pair(a, &tm_w, full, f0, k0 + u * kSub);
+                tma_load_2d_pair(a + kHalfSub, &tm_w, full, f0 + 64, k0 + u * kSub);
+              }
+              tma_load_2d_pair(stage_b(s) + u * kSubBytes, &tm_tok, full, k0 + u * kSub, th);
+            }
           } else {
-            if (rank == 0) mbar_expect_tx(bar(kBarFullB + s), kCluster * kSubBytes);
-            tma_load_2d_pair(stage_b(s), &tm_slab_t, lead_bar(kBarFullB + s), (st - un.nred) * kSub, th);
+            const int j = (st - un.nred) * kSub;
+            if (rank == 0) mbar_expect_tx(bar(kBarFull + s), kCluster * 2 * kSubBytes);
+            tma_load_2d_pair(stage_a(s), &tm_slab_f, full, j, f0);
+            tma_load_2d_pair(stage_b(s), &tm_slab_t, full, j, th);
           }
           ++issued;
         }
       }
       if (ok) {
-        // the pair MMAs' commits arrive on this CTA's barriers: wait for the last round
-        // of each so that none lands after the CTA has exited
-        bool w = true;
-        for (int k = 0; k < kStages && w; ++k) {
-          w = mbar_wait(bar(kBarEmptyB + c.s), c.ph ^ 1u, abort_flag, p.status);
-          if (++c.s == kStages) c.s = 0, c.ph ^= 1u;
-        }
-        for (int k = 0; k < kAStages && w; ++k) {
-          w = mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status);
-          if (++c.a == kAStages) c.a = 0, c.pa ^= 1u;
+        // the pair MMAs' commits arrive on this CTA's empty barriers: wait for the last
+        // round of them so that none lands after the CTA has exited
+        for (int k = 0; k < kStages; ++k) {
+          if (!mbar_wait(bar(kBarEmpty + c.s), c.ph ^ 1u, abort_flag, p.status)) break;
+          c.advance();
         }
       } else if (rank == 0) {  // let copies already in flight land before the CTA exits
         int ds = c.s;
@@ -260,49 +231,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
         for (int64_t k = 0; k < kStages && k < issued; ++k) {
           if (ds == 0) ds = kStages - 1, dph ^= 1u;
           else --ds;
-          mbar_drain(bar(kBarFullB + ds), dph);
-        }
-      }
-    }
-  } else if (warp == 14) {
-    // ---------------- TMA producer: code ring ----------------
-    if (lane == 0) {
-      bool ok = true;
-      Ring c;
-      int64_t issued = 0;
-      for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
-        const Unit un = unit_of(p, unit_at(lt));
-        const int f0 = static_cast<int>(tile_f(un.tile) * kTileF);
-        for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
-          const int q = c.q;
-          if (!mbar_wait(bar(kBarEmptyP + q), c.pq ^ 1u, abort_flag, p.status)) { ok = false; break; }
-          if (st < un.nred) {
-            const int k0 = (un.red0 + st) * kStepK;
-            mbar_expect_tx(bar(kBarFullP + q), kPBytes + kScaleBytes);
-            // forward: rows are weight rows f, bytes run along k; dX: rows are weight rows n
-            // (the contraction), bytes run along the features f
-            const int px = p.mode == 0 ? k0 / 2 : f0 / 2, py = p.mode == 0 ? f0 : k0;
-#pragma unroll
-            for (int cb = 0; cb < kPBytes / (128 * kPBox); ++cb)
-              tma_load_2d(stage_p(q) + cb * 128 * kPBox, &tm_packed, bar(kBarFullP + q), px + cb * kPBox, py);
-            // scales [kb][n]: forward blocks (f0.., 2 steps of k), dX blocks (k0.., the tile's 2 of f)
-            if (p.mode == 0)
-              tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), f0, k0 / kBlock);
-            else
-              tma_load_2d(stage_s(q), &tm_scale, bar(kBarFullP + q), k0, f0 / kBlock);
-          } else {
-            mbar_arrive(bar(kBarFullP + q));   // slab steps read no codes; keep the ring in step
-          }
-          ++issued;
-        }
-      }
-      if (!ok) {  // let copies already in flight land before the CTA exits
-        int dq = c.q;
-        uint32_t dpq = c.pq;
-        for (int64_t k = 0; k < kPStages && k < issued; ++k) {
-          if (dq == 0) dq = kPStages - 1, dpq ^= 1u;
-          else --dq;
-          mbar_drain(bar(kBarFullP + dq), dpq);
+          mbar_drain(bar(kBarFull + ds), dph);
         }
       }
     }
@@ -324,8 +253,7 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kTileT;
         for (int st = 0; st < nsteps; ++st, c.advance()) {
-          if (!mbar_wait(bar(kBarFullB + c.s), c.ph, abort_flag, p.status) ||
-              !mbar_wait(bar(kBarAReady + c.a), c.pa, abort_flag, p.status)) {
+          if (!mbar_wait(bar(kBarFull + c.s), c.ph, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -338,8 +266,8 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
                 // K-major: 32 bytes per 16-element k step inside the 128-byte row.
                 // MN-major (dX): two 8-row groups of 1024 bytes per k step; the two
                 // 64-feature halves of the sub-block are 8192 bytes apart.
-                const uint32_t sa = slot_a(c.a) + u * kSubBytes;
-                const uint64_t adesc = p.mode == 1 ? smem_desc(sa + kk * 2048, 8192, 1024)
+                const uint32_t sa = stage_a(c.s) + u * kSubBytes;
+                const uint64_t adesc = p.mode == 1 ? smem_desc(sa + kk * 2048, kHalfSub, 1024)
                                                    : smem_desc(sa + kk * 32, 16, 1024);
                 const uint64_t bdesc = smem_desc(stage_b(c.s) + u * kSubBytes + kk * 32, 16, 1024);
                 umma_bf16_pair(d_tmem, adesc, bdesc, idesc_main, (st > 0 || u > 0 || kk > 0) ? 1u : 0u);
@@ -347,96 +275,11 @@ nf4_tc_gemm(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ 
           } else {
 #pragma unroll
             for (int kk = 0; kk < kSub / 16; ++kk)
-              umma_bf16_pair(d_tmem, smem_desc(slot_a(c.a) + kk * 32, 16, 1024),
+              umma_bf16_pair(d_tmem, smem_desc(stage_a(c.s) + kk * 32, 16, 1024),
                              smem_desc(stage_b(c.s) + kk * 32, 16, 1024), idesc_slab, (st > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit_pair_mc(bar(kBarEmptyB + c.s), 0x3);   // frees token stage s in both CTAs
-          umma_commit_pair_mc(bar(kBarAEmpty + c.a), 0x3);   // and A slot a
+          umma_commit_pair_mc(bar(kBarEmpty + c.s), 0x3);   // frees stage s in both CTAs
           if (st == nsteps - 1) umma_commit_pair_mc(bar(kBarAccFull + b), 0x3);
-        }
-      }
-    }
-  } else if (warp < 10) {
-    // ---------------- NF4 decoders ----------------
-    const int d = (warp - 2) * 32 + lane;
-    const int row = d & 127;                        // row of an A sub-block (one NF4 block)
-    const int u = d >> 7;                           // which sub-block of the step
-    const uint32_t sw = static_cast<uint32_t>(row & 7);
-    // the 32 code bytes of this thread's block are two 16-byte columns of the [4][128][16]
-    // code tile, and its scale one entry of the [2][128] scale tile
-    //   forward: row = weight row f, block u of the step;  dX: weight row n = u*64 + (row & 63),
-    //   feature half row >> 6
-    const int prow = (p.mode == 0) ? row : u * 64 + (row & 63);
-    const int pcol = (p.mode == 0) ? u : row >> 6;
-    const uint32_t poff = static_cast<uint32_t>(2 * pcol * 128 * kPBox + prow * kPBox);
-    const int sidx = pcol * 128 + prow;
-    bool ok = true;
-    Ring c;
-    for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
-      const Unit un = unit_of(p, unit_at(lt));
-      // slab steps: this thread supplies 32 of the 64 ranks of feature row f0 + row from the
-      // bf16 staging (16-rank chunks, zero past slab_ld); the first slab step's are fetched
-      // before the unit's decode steps and only used at the slab step
-      const int64_t fr = tile_f(un.tile) * kTileF + row;
-      const bool fr_ok = fr < p.F;
-      uint4 sl[4];
-      auto load_slab = [&](int j) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c0 = j * kSub + u * 32 + q * 8;   // first rank of this 16-byte chunk
-          sl[q] = (fr_ok && c0 < p.slab_ld)
-                      ? *reinterpret_cast<const uint4*>(p.slab_f + fr * p.slab_ld + c0)
-                      : make_uint4(0, 0, 0, 0);
-        }
-      };
-      if (un.nslab > 0) load_slab(0);
-      for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
-        // every slot's phases are waited, in order, so that none is ever two phases behind
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarFullP + c.q), c.pq, abort_flag, p.status)) ||
-            !__all_sync(0xffffffffu, mbar_wait(bar(kBarAEmpty + c.a), c.pa ^ 1u, abort_flag, p.status))) {
-          ok = false;
-          break;
-        }
-        if (st < un.nred) {
-          const float* sc = reinterpret_cast<const float*>(base_ptr + (stage_s(c.q) - base));
-          uint32_t L[4], H[4];
-          build_lut(sc[sidx], L, H);
-          const uint8_t* src = base_ptr + (stage_p(c.q) - base) + poff;
-          const uint4 w0 = *reinterpret_cast<const uint4*>(src);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(src + 128 * kPBox);
-          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          const uint32_t arow = slot_a(c.a) + u * kSubBytes + row * 128;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t o[4];
-            decode8(words[i], L, H, o);
-            const uint32_t dst = arow + ((static_cast<uint32_t>(i) ^ sw) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                         "r"(o[3])
-                         : "memory");
-          }
-        } else {
-          // adapter slab: the 128 x 64 bf16 tile of the feature-side factor, K-major,
-          // 32 values (four 16-byte chunks) per thread
-          const int j = st - un.nred;
-          if (j > 0) load_slab(j);
-          const uint32_t arow = slot_a(c.a) + row * 128;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t dst = arow + (((static_cast<uint32_t>(u * 4 + q)) ^ sw) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sl[q].x), "r"(sl[q].y),
-                         "r"(sl[q].z), "r"(sl[q].w)
-                         : "memory");
-          }
-        }
-        // the rows are read by this SM's tensor core (a pair MMA takes each CTA's A rows
-        // from that CTA's shared memory): make them visible to the async proxy, then
-        // tell the even CTA, and hand the code slot back to the producer
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(kBarEmptyP + c.q));
-          mbar_arrive_remote(lead_bar(kBarAReady + c.a));
         }
       }
     }
@@ -558,7 +401,7 @@ void split_tail(GemmParams* p, int64_t pairs, int64_t clusters) {
   while (split > 1 && tail * (split - 1) > kMaxPartTiles) --split;
   if (split < 2) return;
   const int chunk = (p->red_steps + split - 1) / split;
-  split = (p->red_steps + chunk - 1) / chunk;   // every part keeps at least one decode step
+  split = (p->red_steps + chunk - 1) / chunk;   // every part keeps at least one contraction step
   if (split < 2) return;
   p->full_units = rounds * clusters;
   p->total_units = p->full_units + tail * split;
@@ -566,8 +409,8 @@ void split_tail(GemmParams* p, int64_t pairs, int64_t clusters) {
   p->chunk = chunk;
 }
 
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUtensorMap& packed,
-                        const CUtensorMap& slab_t, const CUtensorMap& scale, cudaStream_t st) {
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtensorMap& tok,
+                        const CUtensorMap& slab_f, const CUtensorMap& slab_t, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -583,10 +426,10 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUten
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(nf4_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(bf16_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (attr_err != cudaSuccess) return;
     cfg.gridDim = dim3(static_cast<unsigned>(sm_count() / kCluster * kCluster));
-    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, nf4_tc_gemm, &cfg);
+    attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, bf16_tc_gemm, &cfg);
     if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -596,24 +439,12 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& tok, const CUten
   GemmParams q = p;
   split_tail(&q, pairs, clusters);
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, nf4_tc_gemm, tok, packed, slab_t, scale, q);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16_tc_gemm, w, tok, slab_f, slab_t, q);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-int64_t scale_ld(int64_t N) { return (N + 3) / 4 * 4; }
 int64_t pad8(int64_t v) { return (v + 7) / 8 * 8; }
-
-// Block-scale job for the prep launch and the tensor map each GEMM stage reads it by.
-PrepJob scales_job(const LinearArgs& a, float* out) {
-  PrepJob j{};
-  j.kind = kBlockScales;
-  j.width = scale_ld(a.N);
-  j.cols = a.N;
-  j.fdst = out;
-  j.count = (a.K / kBlock) * j.width;
-  return j;
-}
 
 PrepJob zero_flags_job(void* flags) {
   PrepJob j{};
@@ -623,32 +454,31 @@ PrepJob zero_flags_job(void* flags) {
   return j;
 }
 
-// Scales [K/64][N padded to 4]: a box of 128 consecutive n by 2 blocks.
-bool scales_map(const LinearArgs& a, const float* sc, CUtensorMap* map) {
-  const int64_t ldn = scale_ld(a.N);
-  return make_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sc, ldn, a.K / kBlock, 4 * ldn, 128, kSubs,
-                  CU_TENSOR_MAP_SWIZZLE_NONE);
+// The weight decoded to bf16 [N][K] for this call (bit-exact with nf4_dequantize).
+cudaError_t decode_weight(const LinearArgs& a, void* wb, cudaStream_t st) {
+  KernelTimer timer(NF4_TIME_WEIGHT_DECODE, st);
+  return launch_dequantize(a.W, wb, NF4_BF16, st);
 }
 
-// Workspace layouts (every part 1024-byte aligned).
-// `part` holds the skinny passes' partial sums and, while the NF4 GEMM runs (never at the
-// same time), its split tiles' partial sums; `flags` the GEMM's per-part flags.
+// Workspace layouts (every part 1024-byte aligned).  `part` holds the skinny passes'
+// partial sums and, while the GEMM runs (never at the same time), its split tiles'
+// partial sums; `wb` the bf16 weight; `flags` the GEMM's per-part flags.
 struct FwdWs {
-  size_t sTp, Bq, Aq, part, scale, flags, total;
+  size_t sTp, Bp, Aq, part, wb, flags, total;
   FwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r);
     sTp = 0;
-    Bq = sTp + a1024(2 * rp * M);
-    Aq = Bq + a1024(2 * nq * N);
+    Bp = sTp + a1024(2 * rp * M);
+    Aq = Bp + a1024(2 * rp * N);
     part = Aq + a1024(2 * nq * K);
-    scale = part + a1024(std::max(adapter_partial_bytes(M, K, r), kMaxPartTiles * kPartTileBytes));
-    flags = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
+    wb = part + a1024(std::max(adapter_partial_bytes(M, K, r), kMaxPartTiles * kPartTileBytes));
+    flags = wb + a1024(2 * static_cast<size_t>(N) * K);
     total = flags + a1024(kPartFlagBytes);
   }
 };
 
 struct BwdWs {
-  size_t sGp, AqT, Bt, Tt, Gt, part, scale, flags, total;
+  size_t sGp, ApT, Bt, Tt, Gt, part, wb, flags, total;
   BwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r), Mp = pad8(M);
     size_t pb = adapter_partial_bytes(M, N, r);
@@ -656,13 +486,13 @@ struct BwdWs {
     pb = std::max(pb, adapter_partial_bytes(K, M, r));
     pb = std::max(pb, kMaxPartTiles * kPartTileBytes);
     sGp = 0;
-    AqT = sGp + a1024(2 * rp * M);
-    Bt = AqT + a1024(2 * nq * K);
+    ApT = sGp + a1024(2 * rp * M);
+    Bt = ApT + a1024(2 * rp * K);
     Tt = Bt + a1024(2 * nq * N);
     Gt = Tt + a1024(2 * nq * Mp);
     part = Gt + a1024(2 * nq * Mp);
-    scale = part + a1024(pb);
-    flags = scale + a1024(4 * static_cast<size_t>(K / kBlock) * scale_ld(N));
+    wb = part + a1024(pb);
+    flags = wb + a1024(2 * static_cast<size_t>(N) * K);
     total = flags + a1024(kPartFlagBytes);
   }
 };
@@ -681,7 +511,6 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   p.tiles_f = static_cast<int>((p.F + kTileF - 1) / kTileF);
   p.pairs_f = (p.tiles_f + 1) / 2;
   p.f_fast = mode == 1 ? 1 : 0;
-  p.slab_ld = adapter_nq(a.r);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = status;
   return p;
@@ -693,16 +522,17 @@ size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return FwdWs(M,
 
 size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return BwdWs(M, N, K, r).total; }
 
-// Forward: prep (A and B in bf16, block scales) -> T = x A^T (skinny tcgen05) ->
-// T and bf16(s T) -> NF4 GEMM with the (s T) B^T slab.
+// Forward: prep (A and B in bf16) -> W in bf16 -> T = x A^T (skinny tcgen05) ->
+// T and bf16(s T) -> GEMM with the (s T) B^T slab.
 cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y, float* T,
                        void* ws, int* status, cudaStream_t st) {
   const FwdWs L(a.M, a.N, a.K, a.r);
   char* w = static_cast<char*>(ws);
   auto* sTp = reinterpret_cast<__nv_bfloat16*>(w + L.sTp);
+  auto* Bp = reinterpret_cast<__nv_bfloat16*>(w + L.Bp);
   auto* Aq = reinterpret_cast<__nv_bfloat16*>(w + L.Aq);
   auto* part = reinterpret_cast<float*>(w + L.part);
-  auto* sc = reinterpret_cast<float*>(w + L.scale);
+  auto* wb = reinterpret_cast<__nv_bfloat16*>(w + L.wb);
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
   PrepBuilder prep(a.W, a.K);
   {
@@ -715,40 +545,40 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
     j.count = static_cast<int64_t>(nq) * a.K;
     prep.add(j);
     PrepJob b{};
-    b.kind = kStageRows;         // B as the slab's feature side: [N][nq] bf16
+    b.kind = kStageRows;         // B as the slab's feature side: [N][rp]
     b.r = a.r;
-    b.width = nq;
+    b.width = rp;
     b.scale = 1.0f;
     b.src = B;
-    b.dst = reinterpret_cast<__nv_bfloat16*>(w + L.Bq);
-    b.count = a.N * nq;
+    b.dst = Bp;
+    b.count = a.N * rp;
     prep.add(b);
-    prep.add(scales_job(a, sc));
     prep.add(zero_flags_job(w + L.flags));
   }
   cudaError_t e = prep.launch(st);
   if (e != cudaSuccess) return e;
+  if ((e = decode_weight(a, wb, st)) != cudaSuccess) return e;
   int ns = 0;
   if ((e = adapter_pass(x, a.K, a.M, false, Aq, a.K, a.r, a.M, a.K, part, status, &ns, st)) != cudaSuccess) return e;
   if ((e = adapter_finish(part, ns, a.M, a.r, 1.0f, T, 0, sTp, rp, a.s, nullptr, 0, st)) != cudaSuccess) return e;
-  CUtensorMap tok, packed, slab_t, scale;
-  bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kSub, kHalfT,
+  CUtensorMap wm, tok, slab_f, slab_t;
+  bool ok = make_map(&wm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb, a.K, a.N, 2 * a.K, kSub, kTileF,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kPBox, kTileF,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kSub, kHalfT,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_f, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, rp, a.N, 2 * rp, kSub, kTileF,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kSub, kHalfT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && scales_map(a, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 0, y, status);
-  gp.slab_f = reinterpret_cast<const __nv_bfloat16*>(w + L.Bq);
   gp.part_ws = part;
   gp.part_flags = reinterpret_cast<int*>(w + L.flags);
-  return launch_gemm(gp, tok, packed, slab_t, scale, st);
+  return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
 }
 
-// Backward: prep (B^T, T^T, zeroed G^T, A^T in bf16, block scales) -> G = dY B ->
-// G, bf16(s G), bf16(G)^T -> dB = s dY^T T -> NF4 GEMM for dX with the (s G) A slab ->
+// Backward: prep (B^T, T^T, zeroed G^T, A^T in bf16) -> W in bf16 -> G = dY B ->
+// G, bf16(s G), bf16(G)^T -> dB = s dY^T T -> GEMM for dX with the (s G) A slab ->
 // dA = s G^T x.
 cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, const float* T, const float* A,
                         const float* B, void* dx, float* dA, float* dB, float* G, void* ws, int* status,
@@ -756,11 +586,12 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   const BwdWs L(a.M, a.N, a.K, a.r);
   char* w = static_cast<char*>(ws);
   auto* sGp = reinterpret_cast<__nv_bfloat16*>(w + L.sGp);
+  auto* ApT = reinterpret_cast<__nv_bfloat16*>(w + L.ApT);
   auto* Bt = reinterpret_cast<__nv_bfloat16*>(w + L.Bt);
   auto* Tt = reinterpret_cast<__nv_bfloat16*>(w + L.Tt);
   auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + L.Gt);
   auto* part = reinterpret_cast<float*>(w + L.part);
-  auto* sc = reinterpret_cast<float*>(w + L.scale);
+  auto* wb = reinterpret_cast<__nv_bfloat16*>(w + L.wb);
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
   const int64_t Mp = pad8(a.M);
   PrepBuilder prep(a.W, a.K);
@@ -786,19 +617,19 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
     g.dst = Gt;
     prep.add(g);
     PrepJob c{};
-    c.kind = kStageColumns;      // A^T as the slab's feature side: [K][nq] bf16
+    c.kind = kStageColumns;      // A^T as the slab's feature side: [K][rp]
     c.r = a.r;
-    c.width = nq;
+    c.width = rp;
     c.src = A;
-    c.dst = reinterpret_cast<__nv_bfloat16*>(w + L.AqT);
+    c.dst = ApT;
     c.cols = a.K;
-    c.count = a.K * nq;
+    c.count = a.K * rp;
     prep.add(c);
-    prep.add(scales_job(a, sc));
     prep.add(zero_flags_job(w + L.flags));
   }
   cudaError_t e = prep.launch(st);
   if (e != cudaSuccess) return e;
+  if ((e = decode_weight(a, wb, st)) != cudaSuccess) return e;
   int ns = 0;
   // G = dY B: rows M, reduction over N along dY's rows; also bf16(s G) and bf16(G)^T
   if ((e = adapter_pass(dy, a.N, a.M, false, Bt, a.N, a.r, a.M, a.N, part, status, &ns, st)) != cudaSuccess) return e;
@@ -806,20 +637,21 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   // dB = s dY^T T: rows N, reduction over M down dY's columns
   if ((e = adapter_pass(dy, a.N, a.M, true, Tt, Mp, a.r, a.N, a.M, part, status, &ns, st)) != cudaSuccess) return e;
   if ((e = adapter_finish(part, ns, a.N, a.r, a.s, dB, 0, nullptr, 0, 0.0f, nullptr, 0, st)) != cudaSuccess) return e;
-  CUtensorMap tok, packed, slab_t, scale;
-  bool ok = make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT,
+  CUtensorMap wm, tok, slab_f, slab_t;
+  // W [N][K] read as 64 features x 64 rows n (MN-major A: the features are the MMA's M)
+  bool ok = make_map(&wm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb, a.K, a.N, 2 * a.K, kSub, kSub,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kPBox, kStepK,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_f, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ApT, rp, a.K, 2 * rp, kSub, kTileF,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kSub, kHalfT,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && scales_map(a, sc, &scale);
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 1, dx, status);
-  gp.slab_f = reinterpret_cast<const __nv_bfloat16*>(w + L.AqT);
   gp.part_ws = part;
   gp.part_flags = reinterpret_cast<int*>(w + L.flags);
-  if ((e = launch_gemm(gp, tok, packed, slab_t, scale, st)) != cudaSuccess) return e;
+  if ((e = launch_gemm(gp, wm, tok, slab_f, slab_t, st)) != cudaSuccess) return e;
   // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
   if ((e = adapter_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, part, status, &ns, st)) != cudaSuccess) return e;
   return adapter_finish(part, ns, a.K, a.r, a.s, dA, 1, nullptr, 0, 0.0f, nullptr, 0, st);

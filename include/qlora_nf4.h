@@ -192,7 +192,8 @@ typedef enum {
   NF4_TIME_FWD_GEMM = 2,    /* base contraction of the forward (y) */
   NF4_TIME_DX_GEMM = 3,     /* base contraction of the input gradient (dX) */
   NF4_TIME_ADAPTER = 4,     /* adapter-side kernels (T, G, dA, dB, operand staging) */
-  NF4_TIME_KINDS = 5
+  NF4_TIME_WEIGHT_DECODE = 5, /* the bf16 profile's per-call decode of W before its GEMM */
+  NF4_TIME_KINDS = 6
 } nf4_timed_kernel;
 
 void nf4_timing_enable(int32_t on);
