@@ -136,7 +136,9 @@ nf4_status nf4_quantize_noalloc(const void* x, nf4_dtype x_dtype, int64_t numel,
  * even ([ADAPT] "Fused GPU NF4 decodes inside the matrix kernel"). */
 nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream);
 
-/* Workspace (device bytes) needed by qlora_linear_fwd / qlora_linear_bwd. */
+/* Workspace (device bytes) needed by qlora_linear_fwd / qlora_linear_bwd.  With
+ * compute = NF4_BF16 it includes a bf16 copy of the decoded weight (2*N*K bytes): each
+ * call decodes W once into it (the bits nf4_dequantize writes) before the contraction. */
 size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
 size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
 
