@@ -75,7 +75,7 @@ struct GemmParams {
   int tiles_t, tiles_f;
   int pairs_f;         // ceil(tiles_f / 2): feature-tile pairs; an odd count leaves the last pair's
                        // second tile past F (loads read zeros, the epilogue stores nothing)
-  int f_fast;          // pair order: 1 = feature pairs vary fastest (dX), 0 = token tiles (forward)
+  int f_fast;          // pair order: 1 = feature pairs vary fastest, 0 = token tiles
   __nv_bfloat16* out;  // [M, F]
   int* status;
   // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
@@ -510,7 +510,9 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   p.tiles_t = static_cast<int>((a.M + kTileT - 1) / kTileT);
   p.tiles_f = static_cast<int>((p.F + kTileF - 1) / kTileF);
   p.pairs_f = (p.tiles_f + 1) / 2;
-  p.f_fast = mode == 1 ? 1 : 0;
+  // each round of clusters re-reads the whole operand along the fast dimension: run the
+  // feature pairs fastest only when the weight panel set (F rows) is smaller than the tokens
+  p.f_fast = p.F < a.M ? 1 : 0;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = status;
   return p;
