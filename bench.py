@@ -206,6 +206,24 @@ class Layer:
         return [p[k] for p in self.proj for k in ("dA", "dB")]
 
 
+def gemm_traffic(kind):
+    """DRAM bytes per launch of one GEMM kind, from the committed ncu capture of one bench
+    step (profiles/bf16_tc_gemm_llama8b_step_traffic.json), or None once the kernel source
+    differs from the one the counters were taken on."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    try:
+        with open(os.path.join(root, "profiles", "bf16_tc_gemm_llama8b_step_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(root, "bit_nf4_quantized_gb300", "csrc", "linear_tc.cu"), "rb") as f:
+            src = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != src:
+        return None
+    return rec.get("per_launch_bytes", {}).get(kind)
+
+
 def time_steps(fn, steps, stream):
     import torch
     start = torch.cuda.Event(enable_timing=True)
@@ -416,7 +434,7 @@ def main():
             "gpu_launches": launches,
             "phases_ms_per_step": {k: v[0] / args.steps for k, v in kinds.items()},
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": gemm_traffic(dom),
                          "peak_source": f"{pk_src} bf16_tflops_sustained", "launches": dom_n},
             "dequant": {"GB/s": deq_gbs, "frac": deq_gbs / hbm, "peak_gbs": hbm,
                         "bytes_per_step": deq_bytes, "launches": deq_n},
