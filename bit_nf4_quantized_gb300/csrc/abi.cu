@@ -60,25 +60,50 @@ void build_thresholds(const float* codes, int n, float* thr) {
 }
 
 // Bucket table for the quantizer's NF4 search: 64 buckets of width 1/32 over [-1, 1).
+// lo moved down (toward -inf) by 1 to 31 ulps so that `code` fits in its low 4 bits; a lo of
+// 4 (no band) stays at or above 4.
+float band_lo_with_code(float lo, int code) {
+  uint32_t b;
+  std::memcpy(&b, &lo, 4);
+  const uint32_t sign = b & 0x80000000u, mag = b & 0x7FFFFFFFu;
+  uint32_t m;
+  if (lo >= 4.0f) m = (mag & ~0xFu) + static_cast<uint32_t>(code);          // no band: stays >= 4
+  else if (sign == 0) m = (mag & ~0xFu) - 0x10u + static_cast<uint32_t>(code);  // smaller positive
+  else m = (mag & ~0xFu) + 0x10u + static_cast<uint32_t>(code);               // more negative
+  const uint32_t out = sign | m;
+  float f;
+  std::memcpy(&f, &out, 4);
+  return f;
+}
+
 void build_buckets(const float* thr, EncodeTables* e) {
   e->bucket_ok = 1;
-  for (int k = 0; k < 64; ++k) {
-    const double lo = -1.0 + k / 32.0, hi = lo + 1.0 / 32.0;
-    int base = 0, inner = 0;
+  for (int idx = 0; idx < 66; ++idx) {
+    int base = 0;
     float t_in = 4.0f;
-    for (int j = 0; j < 15; ++j) {
-      const double t = thr[j];
-      if (t <= lo) ++base;
-      else if (t < hi) { ++inner; t_in = thr[j]; }
-      if (std::fabs(t - lo) < 1.0 / (1 << 18) || std::fabs(t - hi) < 1.0 / (1 << 18)) e->bucket_ok = 0;
+    if (idx == 0) {
+      base = 0;                       // q below -1: nearest is -1
+    } else if (idx == 65) {
+      base = 15;                      // q >= 1: nearest is 1
+    } else {
+      const int k = idx - 1;
+      const double lo = -1.0 + k / 32.0, hi = lo + 1.0 / 32.0;
+      int inner = 0;
+      for (int j = 0; j < 15; ++j) {
+        const double t = thr[j];
+        if (t <= lo) ++base;
+        else if (t < hi) { ++inner; t_in = thr[j]; }
+        if (std::fabs(t - lo) < 1.0 / (1 << 18) || std::fabs(t - hi) < 1.0 / (1 << 18)) e->bucket_ok = 0;
+      }
+      if (inner > 1) e->bucket_ok = 0;
     }
-    if (inner > 1) e->bucket_ok = 0;
-    e->nf4_bcode[k] = base;
     // band of +-2^-19 (relative) around the threshold: wider than the error of
     // x * RN(1/a) against RN(x / a) (a few ulp)
     const double t = t_in, w = std::fabs(t) / (1 << 19);
-    e->nf4_blo[k] = t_in == 4.0f ? 4.0f : static_cast<float>(t - w);
-    e->nf4_bhi[k] = t_in == 4.0f ? 4.0f : static_cast<float>(t + w);
+    const float lo = t_in == 4.0f ? 4.0f : static_cast<float>(t - w);
+    const float hi = t_in == 4.0f ? 4.0f : static_cast<float>(t + w);
+    e->nf4_band[idx][0] = band_lo_with_code(lo, base);
+    e->nf4_band[idx][1] = hi;
   }
 }
 

@@ -55,14 +55,16 @@ struct DecodeTables {
 struct EncodeTables {
   float nf4_thr[16];   // 15 used
   float dyn8_thr[256]; // 255 used
-  // Bucketed NF4 search over v in [-1, 1): bucket k covers [-1 + k/32, -1 + (k+1)/32);
-  // for a value q within a few ulp of v, code(v) = bcode[k] + (q >= bhi[k]) unless
-  // blo[k] <= q < bhi[k] (the band around the bucket's one threshold; blo = bhi = 4
-  // when none falls inside).  Valid only when bucket_ok (at most one threshold per
-  // bucket, none near an edge).
-  float nf4_blo[64];
-  float nf4_bhi[64];
-  int32_t nf4_bcode[64];
+  // Bucketed NF4 search for a value q within a few ulp of v = x/a in [-1, 1].  The index
+  // idx = (bits(q' ) >> 17) - 8191, q' = fl(x*r + 3) ~ q + 3, is 1 + the bucket k of
+  // [-1 + k/32, -1 + (k+1)/32) (the top 6 mantissa bits of a value in [2, 4)), 0 for q
+  // just below -1 and 65 for q >= 1.  Entry {lo, hi}: code(v) = base + (q >= hi) unless
+  // lo <= q < hi (the band around the bucket's one threshold; lo = hi = 4 when none falls
+  // inside); base sits in the low 4 bits of lo, which is moved away from the threshold to
+  // make room (the band only widens).  Valid only when bucket_ok (at most one threshold per
+  // bucket, none within 2^-18 of an edge, so an index off by one rounding near an edge
+  // gives the same code).
+  float nf4_band[66][2];
   int32_t bucket_ok;
 };
 

@@ -40,109 +40,88 @@ __device__ __forceinline__ int dyn8_encode(float v, const float* thr) {
   return c;
 }
 
-// Loads of the encode kernel: a warp reads 1024 consecutive elements with coalesced
-// 16-byte loads (zero past numel) and parks them in a swizzled shared buffer, from which
-// lane l takes its own 32 elements (half a 64-element block).
-template <typename Tin>
-__device__ __forceinline__ void stage_chunk(const Tin* __restrict__ x, int64_t numel, int64_t c0, int lane,
-                                            uint32_t buf_s) {
-  constexpr int kVec = 16 / sizeof(Tin);                 // elements per 16-byte load
-  constexpr int kRounds = 1024 / (32 * kVec);
-#pragma unroll
-  for (int j = 0; j < kRounds; ++j) {
-    const uint32_t g = 32 * j + lane;                    // 16-byte slot within the chunk
-    const int64_t e = c0 + static_cast<int64_t>(g) * kVec;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (e + kVec <= numel) {
-      v = __ldcs(reinterpret_cast<const uint4*>(x + e));
-    } else if (e < numel) {
-      Tin tmp[kVec];
-#pragma unroll
-      for (int i = 0; i < kVec; ++i) tmp[i] = (e + i < numel) ? x[e + i] : Tin(0.0f);
-      v = *reinterpret_cast<const uint4*>(tmp);
-    }
-    const uint32_t row = g >> 3, col = g & 7;
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf_s + (((row << 3) | (col ^ (row & 7))) << 4)),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-  }
+// Lane's 32 elements (from e0) as fp32, zero past numel, and the largest |x| among them
+// as fp32 bits (bf16 input: an integer max over the 15-bit magnitudes, two at a time, which
+// orders subnormals, Inf and NaN exactly as the fp32 bit patterns do).
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// Lane's 32 elements as fp32 from the staging buffer.
 template <typename Tin>
-__device__ __forceinline__ void lane_values(uint32_t buf_s, int lane, float (&v)[32]) {
+__device__ __forceinline__ uint32_t lane_load(const Tin* __restrict__ x, int64_t numel, int64_t e0, float (&v)[32]) {
   constexpr int kVec = 16 / sizeof(Tin);
+  uint32_t w[32 / kVec * 4];
+  if (e0 + 32 <= numel) {
 #pragma unroll
-  for (int i = 0; i < 32 / kVec; ++i) {
-    const uint32_t g = static_cast<uint32_t>(lane) * (32 / kVec) + i;
-    const uint32_t row = g >> 3, col = g & 7;
-    uint4 u;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                 : "r"(buf_s + (((row << 3) | (col ^ (row & 7))) << 4)));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    if (sizeof(Tin) == 4) {
+    for (int i = 0; i < 32 / kVec; ++i) {
+      const uint4 u = *reinterpret_cast<const uint4*>(x + e0 + i * kVec);
+      w[4 * i] = u.x, w[4 * i + 1] = u.y, w[4 * i + 2] = u.z, w[4 * i + 3] = u.w;
+    }
+  } else {   // ragged tail: zero past numel
+    const uint16_t* x16 = reinterpret_cast<const uint16_t*>(x);
+    const uint32_t* x32 = reinterpret_cast<const uint32_t*>(x);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[4 * i + k] = __uint_as_float(w[k]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
-        v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    for (int i = 0; i < 32 / kVec * 4; ++i) {
+      if (sizeof(Tin) == 4) {
+        w[i] = (e0 + i < numel) ? x32[e0 + i] : 0u;
+      } else {
+        const uint32_t lo = (e0 + 2 * i < numel) ? x16[e0 + 2 * i] : 0u;
+        const uint32_t hi = (e0 + 2 * i + 1 < numel) ? x16[e0 + 2 * i + 1] : 0u;
+        w[i] = lo | (hi << 16);
       }
     }
+  }
+  if (sizeof(Tin) == 4) {
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] = __uint_as_float(w[i]);
+      mb = max(mb, w[i] & 0x7FFFFFFFu);
+    }
+    return mb;
+  } else {
+    uint32_t m2 = 0;   // two 16-bit maxima
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      m2 = max_u16x2(m2, w[k] & 0x7FFF7FFFu);
+    }
+    return max(m2 & 0xFFFFu, m2 >> 16) << 16;
   }
 }
 
 // Block pass: absmax, 4-bit codes and packing for one nested group (256 blocks) per CTA;
 // with double quantization also the float64 pairwise-tree sum of the group's absmax.
-// Codes: q = x * RN(1/a) picks a bucket of the 64-bucket table; when q lies within
-// 1e-6 (relative) of the bucket's threshold, or 1/a overflows, the code is taken from
-// the exact quotient RN(x / a) instead, so the result is always that of the IEEE
-// division.
+// Codes: q = x * RN(1/a), and fl(x * RN(1/a) + 3) picks an entry of the bucket table;
+// when q lies in the entry's band around a threshold, or a or 1/a is not finite, the code
+// is taken from the exact quotient RN(x / a) instead, so the result is always that of
+// the IEEE division.
 template <typename Tin>
 __global__ void __launch_bounds__(kQuantThreads)
 nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict__ packed,
                   float* __restrict__ absmax, double* __restrict__ group_sum, EncodeTables tabs,
                   int* status) {
   __shared__ float thr[16];
-  __shared__ float2 band[64];   // (lo, hi)
-  __shared__ int32_t bcode[64];
+  __shared__ float2 band[66];   // (lo with the base code in its low 4 bits, hi)
   __shared__ double gsum[kNested];
-  // 4 KB of staging per warp: one fp32 chunk at a time, or both bf16 chunks at once
-  __shared__ __align__(16) uint8_t stage[kQuantThreads / 32][4096];
-  constexpr int kChunkBytes = 1024 * static_cast<int>(sizeof(Tin));
-  constexpr bool kBoth = 2 * kChunkBytes <= 4096;
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
-  if (threadIdx.x < 64) {
-    band[threadIdx.x] = make_float2(tabs.nf4_blo[threadIdx.x], tabs.nf4_bhi[threadIdx.x]);
-    bcode[threadIdx.x] = tabs.nf4_bcode[threadIdx.x];
-  }
+  if (threadIdx.x < 66) band[threadIdx.x] = make_float2(tabs.nf4_band[threadIdx.x][0], tabs.nf4_band[threadIdx.x][1]);
   __syncthreads();
   const bool fast_ok = tabs.bucket_ok != 0;   // bucket table usable
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t group_base = static_cast<int64_t>(blockIdx.x) * kGroupElems;
-  const uint32_t buf0 = static_cast<uint32_t>(__cvta_generic_to_shared(stage[warp]));
-  // warp w handles elements [w*2048, (w+1)*2048) of the group: two 1024-element chunks
+  // warp w handles elements [w*2048, (w+1)*2048) of the group: two 1024-element rows
   const int64_t wbase = group_base + warp * 2048;
-  stage_chunk(x, numel, wbase, lane, buf0);
-  if (kBoth) stage_chunk(x, numel, wbase + 1024, lane, buf0 + kChunkBytes);
-  __syncwarp();
   bool nonfinite = false;
 #pragma unroll 1
   for (int u = 0; u < 2; ++u) {
     const int64_t e0 = wbase + u * 1024 + 32 * lane;    // lane's first element
-    if (!kBoth && u == 1) {
-      __syncwarp();
-      stage_chunk(x, numel, wbase + 1024, lane, buf0);
-      __syncwarp();
-    }
     float v[32];
-    lane_values<Tin>(kBoth ? buf0 + u * kChunkBytes : buf0, lane, v);
-    uint32_t mb = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) mb = max(mb, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    uint32_t mb = lane_load<Tin>(x, numel, e0, v);
     mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));  // the lane pair holds one block
     nonfinite |= mb >= 0x7F800000u;
     const float a = __uint_as_float(mb);
@@ -152,7 +131,7 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
 #pragma unroll
       for (int w = 0; w < 4; ++w) words[w] = 0x77777777u;     // every code is that of 0.0
     } else {
-      bool exact = !(fast_ok && isfinite(r));
+      bool exact = !(fast_ok && isfinite(r) && mb < 0x7F800000u);
       if (!exact) {
         bool unsure = false;
 #pragma unroll
@@ -160,11 +139,10 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float q = v[i] * r;
-          const float qc = fminf(fmaxf(q, -1.0f), 0.999f);
-          const uint32_t k = (__float_as_uint(qc + 3.0f) >> 17) & 63u;
+          const uint32_t k = (__float_as_uint(fmaf(v[i], r, 3.0f)) >> 17) - 8191u;   // 0 .. 65
           const float2 b = band[k];
           unsure |= (q >= b.x) & (q < b.y);
-          const uint32_t c = static_cast<uint32_t>(bcode[k]) + (q >= b.y ? 1u : 0u);
+          const uint32_t c = (__float_as_uint(b.x) & 15u) + (q >= b.y ? 1u : 0u);
           words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
         }
         exact = unsure;
@@ -189,7 +167,9 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
       *reinterpret_cast<uint4*>(packed + (e0 >> 1)) = make_uint4(words[0], words[1], words[2], words[3]);
     } else if (e0 < numel) {
       const int64_t nbytes = (numel - e0 + 1) / 2;
-      for (int64_t b = 0; b < nbytes; ++b) packed[(e0 >> 1) + b] = static_cast<uint8_t>(words[b >> 2] >> (8 * (b & 3)));
+#pragma unroll
+      for (int b = 0; b < 16; ++b)
+        if (b < nbytes) packed[(e0 >> 1) + b] = static_cast<uint8_t>(words[b >> 2] >> (8 * (b & 3)));
     }
     const int block_in_group = warp * 32 + u * 16 + (lane >> 1);
     if ((lane & 1) == 0) {
