@@ -61,7 +61,9 @@ constexpr int kTmemCols = 512;
 // the TMEM address
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages, kBarAccEmpty = kBarAccFull + 2,
               kNumBars = kBarAccEmpty + 2;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
+constexpr int kOutRows = 32;                // tokens per epilogue store box
+constexpr int kOutBytes = kOutRows * kTileF * 2;   // 8 KB: [32 tokens][128 features] bf16
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2 * kOutBytes + kNumBars * 8 + 16;
 static_assert(kStageBytes % 1024 == 0, "stage buffers must stay 1024-byte aligned");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
@@ -133,12 +135,13 @@ struct Ring {
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_tok,
              const __grid_constant__ CUtensorMap tm_slab_f, const __grid_constant__ CUtensorMap tm_slab_t,
-             const GemmParams p) {
+             const __grid_constant__ CUtensorMap tm_out, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes);
+  const uint32_t out_stage = base + kStages * kStageBytes;   // two [32][128] bf16 store boxes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + kStages * kStageBytes + 2 * kOutBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars) + 1;
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -285,16 +288,26 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
     }
   } else {
     // ---------------- epilogue ----------------
+    // Output tiles go out through shared memory: each warp converts its 32 feature rows of
+    // 32 tokens to bf16 in a [32 tokens][128 features] box, and one thread stores the box
+    // with TMA (two boxes alternate).  The four warps meet at named barrier 1; whether to
+    // go on is decided by a vote, so that all four always take the same path.
+    __shared__ int votes[2][4];
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
     const int lrow = quarter * 32 + lane;       // this thread's row of the CTA's 128
+    const bool issuer = warp == kWarpEpi && lane == 0;
+    uint32_t nst = 0;                           // boxes stored so far (picks the buffer)
     for (int64_t lt = 0; unit_at(lt) < p.total_units; ++lt) {
       const Unit un = unit_of(p, unit_at(lt));
       const uint32_t b = static_cast<uint32_t>(lt) & 1u;
       const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), aph, abort_flag, p.status))) break;
+      const bool ok_w = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), aph, abort_flag, p.status));
+      if (lane == 0) votes[b][quarter] = ok_w ? 1 : 0;
+      named_sync(1, 128);
+      if (!(votes[b][0] && votes[b][1] && votes[b][2] && votes[b][3])) break;
       tc_fence_after();
       const int64_t t0 = tile_t(un.tile) * kTileT;
-      const int64_t f = tile_f(un.tile) * kTileF + lrow;
+      const int f0 = static_cast<int>(tile_f(un.tile) * kTileF);
       const uint32_t taddr = tmem_base + b * kTileT + (static_cast<uint32_t>(quarter * 32) << 16);
       // partial sums of a split tile: [slot][part][rank][256][128] fp32, coalesced along rows
       auto part_buf = [&](int part) {
@@ -303,62 +316,80 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
       auto part_flag = [&](int part) {
         return p.part_flags + ((un.slot * (p.split - 1) + part) * kCluster + rank) * 4 + quarter;
       };
-      bool have_parts = true;
-      if (un.nparts > 1 && un.part == un.nparts - 1) {
-        // wait (bounded) for the other parts of this tile, rows of this warp only
-        for (int q = 0; q < un.nparts - 1 && have_parts; ++q) {
-          const int* flag = part_flag(q);
-          const uint64_t w0 = global_ns();
-          int v = 0;
-          for (uint32_t i = 0;; ++i) {
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-            if (v != 0) break;
-            if ((i & 31u) == 31u && (*abort_flag || global_ns() - w0 > kWaitLimitNs)) {
-              if (!*abort_flag) {
-                *abort_flag = 1;
-                atomicCAS(p.status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
-              }
-              break;
-            }
-          }
-          have_parts = __all_sync(0xffffffffu, v != 0);
-        }
-      }
+      if (un.part < un.nparts - 1) {
+        // a leading part of a split tile: fp32 partial sums, then this warp's flag
 #pragma unroll 1
-      for (int c0 = 0; c0 < kTileT; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c0, v);
-        tmem_ld_wait();
-        if (un.part < un.nparts - 1) {
+        for (int c0 = 0; c0 < kTileT; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
           float* dst = part_buf(un.part) + static_cast<int64_t>(c0) * 128 + lrow;
 #pragma unroll
           for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(v[j]);
-          continue;
         }
-        if (un.nparts > 1 && have_parts) {
-          for (int q = 0; q < un.nparts - 1; ++q) {   // parts in order: deterministic sums
-            const float* src = part_buf(q) + static_cast<int64_t>(c0) * 128 + lrow;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(src + j * 128));
-          }
-        }
-        if (f < p.F) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int64_t m = t0 + c0 + j;
-            if (m < p.M) p.out[m * p.F + f] = __float2bfloat16_rn(__uint_as_float(v[j]));
-          }
-        }
-      }
-      if (un.part < un.nparts - 1) {   // publish this warp's rows of the partial sums
         __threadfence();
         __syncwarp();
         if (lane == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(part_flag(un.part)), "r"(1) : "memory");
+      } else {
+        bool have_parts = true;
+        if (un.nparts > 1) {
+          // wait (bounded) for the other parts of this tile, rows of this warp only
+          for (int q = 0; q < un.nparts - 1 && have_parts; ++q) {
+            const int* flag = part_flag(q);
+            const uint64_t w0 = global_ns();
+            int v = 0;
+            for (uint32_t i = 0;; ++i) {
+              asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+              if (v != 0) break;
+              if ((i & 31u) == 31u && (*abort_flag || global_ns() - w0 > kWaitLimitNs)) {
+                if (!*abort_flag) {
+                  *abort_flag = 1;
+                  atomicCAS(p.status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
+                }
+                break;
+              }
+            }
+            have_parts = __all_sync(0xffffffffu, v != 0);
+          }
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTileT; c0 += kOutRows, ++nst) {
+          const uint32_t box = out_stage + (nst & 1u) * kOutBytes;
+          if (issuer) bulk_wait_read<1>();      // the store that last used this box has read it
+          named_sync(1, 128);
+#pragma unroll
+          for (int h = 0; h < kOutRows; h += 16) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c0 + h, v);
+            tmem_ld_wait();
+            if (un.nparts > 1 && have_parts) {
+              for (int q = 0; q < un.nparts - 1; ++q) {   // parts in order: deterministic sums
+                const float* src = part_buf(q) + static_cast<int64_t>(c0 + h) * 128 + lrow;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(src + j * 128));
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[j]));
+              asm volatile("st.shared.b16 [%0], %1;" ::"r"(box + static_cast<uint32_t>(((h + j) * kTileF + lrow) * 2)),
+                           "h"(*reinterpret_cast<const uint16_t*>(&o))
+                           : "memory");
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          named_sync(1, 128);
+          if (issuer) {   // rows past M and columns past F are not written
+            tma_store_2d(&tm_out, box, f0, static_cast<int>(t0) + c0);
+            bulk_commit();
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(lead_bar(kBarAccEmpty + b));
     }
+    if (issuer) bulk_wait_all();   // the last boxes are written before the CTA exits
   }
 
   tc_fence_before();
@@ -411,6 +442,10 @@ void split_tail(GemmParams* p, int64_t pairs, int64_t clusters) {
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtensorMap& tok,
                         const CUtensorMap& slab_f, const CUtensorMap& slab_t, cudaStream_t st) {
+  CUtensorMap out;   // [M][F] bf16, stored in [32 tokens][128 features] boxes
+  if (!make_map(&out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, p.F, p.M, 2 * p.F, kTileF, kOutRows,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
@@ -439,7 +474,7 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtenso
   GemmParams q = p;
   split_tail(&q, pairs, clusters);
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16_tc_gemm, w, tok, slab_f, slab_t, q);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16_tc_gemm, w, tok, slab_f, slab_t, out, q);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
