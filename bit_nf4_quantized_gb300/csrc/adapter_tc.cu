@@ -82,6 +82,8 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_allow_next();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -170,6 +172,8 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 __global__ void finish_partials(const float* __restrict__ partial, int nsplit, int64_t rows, int r, float scale,
                                 float* __restrict__ f32, int f32_t, __nv_bfloat16* __restrict__ b_rows, int rp,
                                 float scale_b, __nv_bfloat16* __restrict__ b_t, int64_t ldt) {
+  pdl_allow_next();
+  pdl_wait();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t w = static_cast<int64_t>(rows) * (b_rows ? rp : r);
   if (i >= w) return;
@@ -263,10 +267,11 @@ cudaError_t run_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_ma
     attr = cudaFuncSetAttribute(adapter_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 4 * 49152 + 256);
   });
   if (attr != cudaSuccess) return attr;
-  adapter_tc<<<pl.tiles * pl.nsplit, kAThreads, smem, st>>>(tx, tq, p);
+  const cudaError_t e =
+      launch_pdl(adapter_tc, dim3(pl.tiles * pl.nsplit), dim3(kAThreads), static_cast<size_t>(smem), st, 1, tx, tq, p);
   note_launch();
   *nsplit = pl.nsplit;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -286,10 +291,10 @@ cudaError_t adapter_finish(const float* partial, int nsplit, int64_t rows, int r
                            __nv_bfloat16* b_rows, int rp, float scale_b, __nv_bfloat16* b_t, int64_t ldt,
                            cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  finish_partials<<<blocks(rows * (b_rows ? rp : r)), 256, 0, st>>>(partial, nsplit, rows, r, scale, f32, f32_t,
-                                                                      b_rows, rp, scale_b, b_t, ldt);
+  const cudaError_t e = launch_pdl(finish_partials, dim3(blocks(rows * (b_rows ? rp : r))), dim3(256), 0, st, 1,
+                                    partial, nsplit, rows, r, scale, f32, f32_t, b_rows, rp, scale_b, b_t, ldt);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace qnf4

@@ -6,6 +6,8 @@
 // per-device status word, lives in abi.cu; kernels get its address as `status`.
 #pragma once
 
+#include <utility>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -73,6 +75,43 @@ const EncodeTables& encode_tables();
 
 // Launch accounting (for the launch count reported by the ABI).
 void note_launch(int n = 1);
+
+// Programmatic dependent launch.  Kernels of the bf16 path are launched with
+// programmatic stream serialization: a kernel may start while its predecessor in the
+// stream is finishing.  Each kernel calls pdl_allow_next() once its prologue holds every
+// resource it needs (shared memory set up, TMEM allocated), so the next kernel's CTAs can
+// be placed as this one's retire, and pdl_wait() before it touches global memory, which
+// returns once the predecessor has completed and its writes are visible.  Without a
+// programmatic predecessor both are no-ops.
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch `kernel` on `st` with programmatic stream serialization (and a cluster shape
+// when cluster_x > 1).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Optional event timing of selected kernels (nf4_timing_enable): records a CUDA
 // event pair on the launching stream around the scope when timing is on.

@@ -178,6 +178,8 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
   cluster_sync();   // the peer's barriers are initialised before anything signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_allow_next();
+  pdl_wait();
 
   // every role walks the same units (cluster_id, + n_clusters, ...) and steps
   auto unit_at = [&](int64_t lt) { return cluster_id + lt * n_clusters; };
@@ -450,11 +452,13 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtenso
   static cudaError_t attr_err = cudaSuccess;
   static int max_clusters = 0;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_allow_next
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
@@ -474,6 +478,7 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtenso
   GemmParams q = p;
   split_tail(&q, pairs, clusters);
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16_tc_gemm, w, tok, slab_f, slab_t, out, q);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepJobs p) {
   __shared__ float tile[kScaleTile][kScaleTile + 1];
   dyn8[threadIdx.x] = p.dyn8[threadIdx.x];
   __syncthreads();
+  pdl_allow_next();
+  pdl_wait();
   int j = 0;
   while (j + 1 < p.n && blockIdx.x >= p.job[j + 1].first_block) ++j;
   const PrepJob& jb = p.job[j];
@@ -112,9 +114,9 @@ cudaError_t PrepBuilder::launch(cudaStream_t st) {
   const DecodeTables& t = decode_tables();
   for (int i = 0; i < 256; ++i) jobs_.dyn8[i] = t.dyn8[i];
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  prep_kernel<<<blocks_, kPrepThreads, 0, st>>>(jobs_);
+  const cudaError_t e = launch_pdl(prep_kernel, dim3(blocks_), dim3(kPrepThreads), 0, st, 1, jobs_);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace qnf4

@@ -110,6 +110,8 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
   if (threadIdx.x < 66) band[threadIdx.x] = make_float2(tabs.nf4_band[threadIdx.x][0], tabs.nf4_band[threadIdx.x][1]);
   __syncthreads();
+  pdl_allow_next();
+  pdl_wait();
   const bool fast_ok = tabs.bucket_ok != 0;   // bucket table usable
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -192,6 +194,8 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
 // entries (in place in the workspace), then offset = float(sum / nb).
 __global__ void __launch_bounds__(1024)
 nf4_absmax_mean(double* __restrict__ gs, int64_t ng, int64_t p2, int64_t nb, float* __restrict__ offset) {
+  pdl_allow_next();
+  pdl_wait();
   int64_t valid = ng;
   for (int64_t h = p2 / 2; h >= 1; h /= 2) {
     for (int64_t i = threadIdx.x; i < h; i += blockDim.x) {
@@ -208,6 +212,8 @@ nf4_absmax_mean(double* __restrict__ gs, int64_t ng, int64_t p2, int64_t nb, flo
 __global__ void __launch_bounds__(kNested)
 nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __restrict__ offset_p,
                   uint8_t* __restrict__ codes, float* __restrict__ nested, EncodeTables tabs) {
+  pdl_allow_next();
+  pdl_wait();
   __shared__ float thr[256];
   __shared__ float red[kNested / 32];
   thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
@@ -257,6 +263,8 @@ nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
   dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
   for (int i = threadIdx.x; i < 16 * 32; i += kDeqThreads) lut[i >> 5][i & 31] = tabs.nf4[i >> 5];
   __syncthreads();
+  pdl_allow_next();
+  pdl_wait();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t n = w.numel;
@@ -376,23 +384,22 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
                      : nullptr;
   if (ng > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ng));
+  cudaError_t e;
   if (xd == NF4_F32)
-    nf4_encode_blocks<float><<<grid, kQuantThreads, 0, st>>>(static_cast<const float*>(x), numel,
-                                                             out.packed, absmax_f, gsum, et, status);
+    e = launch_pdl(nf4_encode_blocks<float>, grid, dim3(kQuantThreads), 0, st, 1, static_cast<const float*>(x), numel,
+                   out.packed, absmax_f, gsum, et, status);
   else
-    nf4_encode_blocks<__nv_bfloat16><<<grid, kQuantThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), numel, out.packed, absmax_f, gsum, et, status);
+    e = launch_pdl(nf4_encode_blocks<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, st, 1,
+                   static_cast<const __nv_bfloat16*>(x), numel, out.packed, absmax_f, gsum, et, status);
   note_launch();
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !out.double_quant) return e;
-  nf4_absmax_mean<<<1, 1024, 0, st>>>(gsum, ng, pow2_at_least(ng), nb, out.offset);
+  e = launch_pdl(nf4_absmax_mean, dim3(1), dim3(1024), 0, st, 1, gsum, ng, pow2_at_least(ng), nb, out.offset);
   note_launch();
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  nf4_encode_nested<<<grid, kNested, 0, st>>>(absmax_f, nb, out.offset,
-                                              static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
+  e = launch_pdl(nf4_encode_nested, grid, dim3(kNested), 0, st, 1, static_cast<const float*>(absmax_f), nb,
+                 static_cast<const float*>(out.offset), static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st) {
@@ -400,16 +407,17 @@ cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStrea
   if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ctas));
   const DecodeTables& dt = decode_tables();
+  cudaError_t e;
   if (od == NF4_F32) {
-    if (w.dq) nf4_decode<float, true><<<grid, kDeqThreads, 0, st>>>(w, static_cast<float*>(y), dt);
-    else nf4_decode<float, false><<<grid, kDeqThreads, 0, st>>>(w, static_cast<float*>(y), dt);
+    if (w.dq) e = launch_pdl(nf4_decode<float, true>, grid, dim3(kDeqThreads), 0, st, 1, w, static_cast<float*>(y), dt);
+    else e = launch_pdl(nf4_decode<float, false>, grid, dim3(kDeqThreads), 0, st, 1, w, static_cast<float*>(y), dt);
   } else {
     auto* yb = static_cast<__nv_bfloat16*>(y);
-    if (w.dq) nf4_decode<__nv_bfloat16, true><<<grid, kDeqThreads, 0, st>>>(w, yb, dt);
-    else nf4_decode<__nv_bfloat16, false><<<grid, kDeqThreads, 0, st>>>(w, yb, dt);
+    if (w.dq) e = launch_pdl(nf4_decode<__nv_bfloat16, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt);
+    else e = launch_pdl(nf4_decode<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt);
   }
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace qnf4
