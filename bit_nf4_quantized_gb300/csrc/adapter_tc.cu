@@ -20,7 +20,8 @@ namespace {
 using namespace tc;
 
 constexpr int kRowsT = 128;          // MMA M
-constexpr int kBKa = 64;             // reduction per stage
+constexpr int kBKa = 64;             // reduction per box
+constexpr int kBoxes = 2;            // boxes per stage: 8 MMAs per commit
 constexpr int kAThreads = 192;       // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int kATileBytes = kRowsT * kBKa * 2;
 constexpr int kTargetCtas = 320;     // fixed, so workspace sizes do not depend on the device
@@ -29,7 +30,7 @@ constexpr int kMaxSplit = 64;
 struct SkinnyParams {
   int64_t rows;     // rows of Out
   int tiles;        // ceil(rows / 128)
-  int total_steps;  // ceil(red / 64)
+  int total_steps;  // ceil(red / 128): stages of the whole reduction
   int sps;          // steps per slice
   int a_mn_major;
   int n_mma;        // r rounded up to 16
@@ -87,50 +88,63 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 
   if (warp == 0) {
     if (lane == 0) {
+      // one stage = kBoxes boxes of 64 along the reduction; cursors instead of divisions
       bool ok = true;
-      int last = -1;
-      for (int i = 0; i < nsteps && ok; ++i) {
-        const int s = i % p.stages;
-        const uint32_t ph = (i / p.stages) & 1u;
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < nsteps; ++i) {
         if (!mbar_wait(bar(p.stages + s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
         const uint32_t a_dst = base + s * p.stage_bytes;
-        const uint32_t b_dst = a_dst + kATileBytes;
-        const int k0 = (k_begin + i) * kBKa;
-        mbar_expect_tx(bar(s), kATileBytes + p.b_bytes);
-        if (p.a_mn_major) {
-          // activation [red rows, rows cols]: two 64-column boxes of 64 reduction rows
-          tma_load_2d(a_dst, &tm_x, bar(s), tile * kRowsT, k0);
-          tma_load_2d(a_dst + kATileBytes / 2, &tm_x, bar(s), tile * kRowsT + 64, k0);
-        } else {
-          tma_load_2d(a_dst, &tm_x, bar(s), k0, tile * kRowsT);
+        const uint32_t b_dst = a_dst + kBoxes * kATileBytes;
+        mbar_expect_tx(bar(s), kBoxes * (kATileBytes + p.b_bytes));
+#pragma unroll
+        for (int h = 0; h < kBoxes; ++h) {
+          const int k0 = ((k_begin + i) * kBoxes + h) * kBKa;
+          const uint32_t ad = a_dst + h * kATileBytes;
+          if (p.a_mn_major) {
+            // activation [red rows, rows cols]: two 64-column boxes of 64 reduction rows
+            tma_load_2d(ad, &tm_x, bar(s), tile * kRowsT, k0);
+            tma_load_2d(ad + kATileBytes / 2, &tm_x, bar(s), tile * kRowsT + 64, k0);
+          } else {
+            tma_load_2d(ad, &tm_x, bar(s), k0, tile * kRowsT);
+          }
+          tma_load_2d(b_dst + h * p.b_bytes, &tm_q, bar(s), k0, 0);
         }
-        tma_load_2d(b_dst, &tm_q, bar(s), k0, 0);
-        last = i;
+        ++issued;
+        if (++s == p.stages) s = 0, ph ^= 1u;
       }
-      if (!ok) {
-        for (int i = (last - p.stages + 1 > 0 ? last - p.stages + 1 : 0); i <= last; ++i)
-          mbar_drain(bar(i % p.stages), (i / p.stages) & 1u);
+      if (!ok) {   // let the copies in flight land before the CTA exits
+        for (int q = 0; q < issued && q < p.stages; ++q) {
+          if (s == 0) s = p.stages - 1, ph ^= 1u;
+          else --s;
+          mbar_drain(bar(s), ph);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRowsT, p.n_mma, p.a_mn_major ? 1u : 0u);
       bool ok = true;
+      int s = 0;
+      uint32_t ph = 0;
       for (int i = 0; i < nsteps; ++i) {
-        const int s = i % p.stages;
-        const uint32_t ph = (i / p.stages) & 1u;
         if (!mbar_wait(bar(s), ph, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t a_s = base + s * p.stage_bytes;
-        const uint32_t b_s = a_s + kATileBytes;
+        const uint32_t b_s = a_s + kBoxes * kATileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBKa / 16; ++kk) {
-          const uint64_t adesc = p.a_mn_major ? smem_desc(a_s + kk * 2048, 8192, 1024)
-                                              : smem_desc(a_s + kk * 32, 16, 1024);
-          const uint64_t bdesc = smem_desc(b_s + kk * 32, 16, 1024);
-          umma_bf16(tmem_base, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int h = 0; h < kBoxes; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < kBKa / 16; ++kk) {
+            const uint32_t ah = a_s + h * kATileBytes;
+            const uint64_t adesc = p.a_mn_major ? smem_desc(ah + kk * 2048, 8192, 1024)
+                                                : smem_desc(ah + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc(b_s + h * p.b_bytes + kk * 32, 16, 1024);
+            umma_bf16(tmem_base, adesc, bdesc, idesc, (i > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         umma_commit(bar(p.stages + s));
+        if (++s == p.stages) s = 0, ph ^= 1u;
       }
       if (ok && nsteps > 0) umma_commit(bar(2 * p.stages));
     }
@@ -206,7 +220,7 @@ struct Plan {
 Plan plan(int64_t rows, int64_t red, int target = kTargetCtas) {
   Plan pl;
   pl.tiles = static_cast<int>((rows + kRowsT - 1) / kRowsT);
-  pl.total_steps = static_cast<int>((red + kBKa - 1) / kBKa);
+  pl.total_steps = static_cast<int>((red + kBoxes * kBKa - 1) / (kBoxes * kBKa));
   int ns = target / pl.tiles;
   if (ns > kMaxSplit) ns = kMaxSplit;
   if (ns > pl.total_steps) ns = pl.total_steps;
@@ -256,8 +270,8 @@ cudaError_t run_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_ma
   p.n_mma = nq;
   p.r = r;
   p.b_bytes = static_cast<uint32_t>(nq * 128);
-  p.stage_bytes = static_cast<uint32_t>(al(kATileBytes + p.b_bytes));
-  p.stages = nq <= 32 ? 6 : 4;
+  p.stage_bytes = static_cast<uint32_t>(al(kBoxes * (kATileBytes + p.b_bytes)));
+  p.stages = nq <= 32 ? 3 : 2;
   p.partial = partial;
   p.status = status;
   const int smem = 1024 + p.stages * static_cast<int>(p.stage_bytes) + 256;

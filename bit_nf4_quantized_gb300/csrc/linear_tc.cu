@@ -576,7 +576,7 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   auto* part = reinterpret_cast<float*>(w + L.part);
   auto* wb = reinterpret_cast<__nv_bfloat16*>(w + L.wb);
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
-  PrepBuilder prep(a.W, a.K);
+  PrepBuilder prep;
   {
     PrepJob j{};
     j.kind = kStageRowsDirect;   // A as the skinny pass's Q: [nq][K]
@@ -636,7 +636,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   auto* wb = reinterpret_cast<__nv_bfloat16*>(w + L.wb);
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
   const int64_t Mp = pad8(a.M);
-  PrepBuilder prep(a.W, a.K);
+  PrepBuilder prep;
   {
     PrepJob j{};
     j.kind = kStageTransposed;   // B^T: [nq][N]
