@@ -105,10 +105,11 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
                   float* __restrict__ absmax, double* __restrict__ group_sum, EncodeTables tabs,
                   int* status) {
   __shared__ float thr[16];
-  __shared__ float2 band[66];   // (lo with the base code in its low 4 bits, hi)
+  __shared__ float2 band[66][32];   // (lo with the base code in its low 4 bits, hi), one column per lane
   __shared__ double gsum[kNested];
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
-  if (threadIdx.x < 66) band[threadIdx.x] = make_float2(tabs.nf4_band[threadIdx.x][0], tabs.nf4_band[threadIdx.x][1]);
+  for (int i = threadIdx.x; i < 66 * 32; i += kQuantThreads)
+    band[i >> 5][i & 31] = make_float2(tabs.nf4_band[i >> 5][0], tabs.nf4_band[i >> 5][1]);
   __syncthreads();
   pdl_allow_next();
   pdl_wait();
@@ -142,7 +143,7 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
         for (int i = 0; i < 32; ++i) {
           const float q = v[i] * r;
           const uint32_t k = (__float_as_uint(fmaf(v[i], r, 3.0f)) >> 17) - 8191u;   // 0 .. 65
-          const float2 b = band[k];
+          const float2 b = band[k][lane];
           unsure |= (q >= b.x) & (q < b.y);
           const uint32_t c = (__float_as_uint(b.x) & 15u) + (q >= b.y ? 1u : 0u);
           words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
@@ -182,12 +183,19 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
   if (nonfinite) atomicCAS(status, 0, static_cast<int>(NF4_ERR_NONFINITE));
   if (group_sum == nullptr) return;
   __syncthreads();
-  // float64 pairwise tree: s[i] += s[i + h] for h = 128, 64, ..., 1
-  for (int h = kNested / 2; h >= 1; h >>= 1) {
-    if (threadIdx.x < h) gsum[threadIdx.x] += gsum[threadIdx.x + h];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) group_sum[blockIdx.x] = gsum[0];
+  if (warp != 0) return;
+  // float64 pairwise tree s[i] += s[i + h], h = 128, 64, ..., 1, by one warp: lane l holds
+  // s[l + 32 m]; the levels h >= 32 add within the lane, the rest across lanes
+  double t[kNested / 32];
+#pragma unroll
+  for (int m = 0; m < kNested / 32; ++m) t[m] = gsum[lane + 32 * m];
+#pragma unroll
+  for (int h = kNested / 64; h >= 1; h >>= 1)
+#pragma unroll
+    for (int m = 0; m < h; ++m) t[m] += t[m + h];
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
+  if (lane == 0) group_sum[blockIdx.x] = t[0];
 }
 
 // One CTA: the same pairwise tree over the group sums padded with zeros to p2
