@@ -19,11 +19,12 @@
 #include "common.cuh"
 #include "decode.cuh"
 
+#include <mutex>
+
 namespace qnf4 {
 namespace {
 
 constexpr int kQuantThreads = 256;                 // 8 warps
-constexpr int kQuadRowsPerWarp = 16;               // 8 warps x 16 x 128 = one 16384 group
 
 __device__ __forceinline__ int nf4_encode(float v, const float* thr) {
   int c = (v >= thr[7]) ? 8 : 0;
@@ -199,48 +200,82 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
 }
 
 // One CTA: the same pairwise tree over the group sums padded with zeros to p2
-// entries (in place in the workspace), then offset = float(sum / nb).
+// entries, then offset = float(sum / nb).  The tree runs in shared memory when the p2
+// entries fit (kMeanSmemEntries), in place in the workspace otherwise.
+constexpr int kMeanSmemEntries = 16384;
+
 __global__ void __launch_bounds__(1024)
 nf4_absmax_mean(double* __restrict__ gs, int64_t ng, int64_t p2, int64_t nb, float* __restrict__ offset) {
+  extern __shared__ double tree[];
   pdl_allow_next();
   pdl_wait();
+  const bool in_smem = p2 <= kMeanSmemEntries;
+  double* s = in_smem ? tree : gs;
+  if (in_smem) {
+    for (int64_t i = threadIdx.x; i < ng; i += blockDim.x) s[i] = gs[i];
+    __syncthreads();
+  }
   int64_t valid = ng;
   for (int64_t h = p2 / 2; h >= 1; h /= 2) {
     for (int64_t i = threadIdx.x; i < h; i += blockDim.x) {
-      const double a = (i < valid) ? gs[i] : 0.0;
-      const double b = (i + h < valid) ? gs[i + h] : 0.0;
-      gs[i] = a + b;
+      const double a = (i < valid) ? s[i] : 0.0;
+      const double b = (i + h < valid) ? s[i + h] : 0.0;
+      s[i] = a + b;
     }
     valid = h;
     __syncthreads();
   }
-  if (threadIdx.x == 0) *offset = __double2float_rn(__ddiv_rn(gs[0], static_cast<double>(nb)));
+  if (threadIdx.x == 0) *offset = __double2float_rn(__ddiv_rn(s[0], static_cast<double>(nb)));
 }
 
-__global__ void __launch_bounds__(kNested)
+// Nested quantization of the block maxima: one warp per group of 256 maxima, eight per
+// lane.  c = a - offset; m = max |c| over the group; code = dyn8 code of RN(c / m).
+constexpr int kNestedWarps = 8;
+
+__global__ void __launch_bounds__(kNestedWarps * 32)
 nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __restrict__ offset_p,
                   uint8_t* __restrict__ codes, float* __restrict__ nested, EncodeTables tabs) {
+  __shared__ float thr[256];
+  thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
+  __syncthreads();
   pdl_allow_next();
   pdl_wait();
-  __shared__ float thr[256];
-  __shared__ float red[kNested / 32];
-  thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kNestedWarps + warp;
+  if (g * kNested >= nb) return;
   const float offset = *offset_p;
-  const int64_t b = static_cast<int64_t>(blockIdx.x) * kNested + threadIdx.x;
-  const float c = (b < nb) ? __fsub_rn(absmax[b], offset) : 0.0f;
-  float m = fabsf(c);
+  const int64_t b0 = g * kNested + 8 * lane;
+  float c[8];
+  const bool full = b0 + 8 <= nb && (reinterpret_cast<uintptr_t>(absmax + b0) & 15) == 0;
+  if (full) {
+    const float4 u = *reinterpret_cast<const float4*>(absmax + b0);
+    const float4 v = *reinterpret_cast<const float4*>(absmax + b0 + 4);
+    const float a[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = __fsub_rn(a[i], offset);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = (b0 + i < nb) ? __fsub_rn(absmax[b0 + i], offset) : 0.0f;
+  }
+  float m = fabsf(c[0]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(c[i]));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  m = red[0];
+  uint32_t q[8];
 #pragma unroll
-  for (int w = 1; w < kNested / 32; ++w) m = fmaxf(m, red[w]);
-  if (b < nb) {
-    const int code = (m > 0.0f) ? dyn8_encode(__fdiv_rn(c, m), thr) : kDyn8ZeroCode;
-    codes[b] = static_cast<uint8_t>(code);
+  for (int i = 0; i < 8; ++i)
+    q[i] = static_cast<uint32_t>((m > 0.0f) ? dyn8_encode(__fdiv_rn(c[i], m), thr) : kDyn8ZeroCode);
+  if (b0 + 8 <= nb && (reinterpret_cast<uintptr_t>(codes + b0) & 7) == 0) {
+    *reinterpret_cast<uint2*>(codes + b0) =
+        make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24), q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (b0 + i < nb) codes[b0 + i] = static_cast<uint8_t>(q[i]);
   }
-  if (threadIdx.x == 0) nested[blockIdx.x] = m;
+  if (lane == 0) nested[g] = m;
 }
 
 // ---- dequantize -----------------------------------------------------------------
@@ -401,10 +436,20 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
                    static_cast<const __nv_bfloat16*>(x), numel, out.packed, absmax_f, gsum, et, status);
   note_launch();
   if (e != cudaSuccess || !out.double_quant) return e;
-  e = launch_pdl(nf4_absmax_mean, dim3(1), dim3(1024), 0, st, 1, gsum, ng, pow2_at_least(ng), nb, out.offset);
+  const int64_t p2 = pow2_at_least(ng);
+  const size_t mean_smem = p2 <= kMeanSmemEntries ? sizeof(double) * static_cast<size_t>(p2) : 0;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(nf4_absmax_mean, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(double) * kMeanSmemEntries));
+  });
+  if (attr != cudaSuccess) return attr;
+  e = launch_pdl(nf4_absmax_mean, dim3(1), dim3(1024), mean_smem, st, 1, gsum, ng, p2, nb, out.offset);
   note_launch();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(nf4_encode_nested, grid, dim3(kNested), 0, st, 1, static_cast<const float*>(absmax_f), nb,
+  const dim3 ngrid(static_cast<unsigned>((ng + kNestedWarps - 1) / kNestedWarps));
+  e = launch_pdl(nf4_encode_nested, ngrid, dim3(kNestedWarps * 32), 0, st, 1, static_cast<const float*>(absmax_f), nb,
                  static_cast<const float*>(out.offset), static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
   note_launch();
   return e;
