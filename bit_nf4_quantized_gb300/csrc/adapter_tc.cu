@@ -40,10 +40,20 @@ struct SkinnyParams {
   uint32_t stage_bytes;
   float* partial;   // [nsplit][rows][r]
   int* status;
+  int ctas;         // tiles * nsplit: this pass's CTAs
 };
 
+// One launch runs one or two independent passes: CTAs [0, p0.ctas) take the first,
+// the rest the second (p1.ctas == 0 when there is only one).
 __global__ void __launch_bounds__(kAThreads, 1)
-adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_q, const SkinnyParams p) {
+adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_q0,
+           const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_q1, const SkinnyParams p0,
+           const SkinnyParams p1) {
+  const bool second = static_cast<int>(blockIdx.x) >= p0.ctas;
+  const SkinnyParams p = second ? p1 : p0;
+  const CUtensorMap& tm_x = second ? tm_x1 : tm_x0;
+  const CUtensorMap& tm_q = second ? tm_q1 : tm_q0;
+  const int bid = second ? static_cast<int>(blockIdx.x) - p0.ctas : static_cast<int>(blockIdx.x);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -58,8 +68,8 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   uint32_t tmem_cols = 32;
   while (tmem_cols < static_cast<uint32_t>(p.n_mma)) tmem_cols <<= 1;
 
-  const int tile = blockIdx.x % p.tiles;
-  const int slice = blockIdx.x / p.tiles;
+  const int tile = bid % p.tiles;
+  const int slice = bid / p.tiles;
   const int k_begin = slice * p.sps;
   const int k_end = min(p.total_steps, k_begin + p.sps);
   const int nsteps = k_end - k_begin;
@@ -180,30 +190,50 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   }
 }
 
-// out = scale * sum over slices (fixed order).  Optional outputs:
-//   f32 [rows][r] (or transposed [r][rows] when f32_t), bf16(scale_b * v) [rows][rp]
-//   zero-padded, bf16(v) transposed [nq][ldt] (entries past rows / r must already be zero).
-__global__ void finish_partials(const float* __restrict__ partial, int nsplit, int64_t rows, int r, float scale,
-                                float* __restrict__ f32, int f32_t, __nv_bfloat16* __restrict__ b_rows, int rp,
-                                float scale_b, __nv_bfloat16* __restrict__ b_t, int64_t ldt) {
+// out = scale * sum over slices (fixed order), for up to two passes in one launch.
+// Optional outputs: f32 [rows][r] (or transposed [r][rows] when f32_t), bf16(scale_b * v)
+// [rows][rp] zero-padded, bf16(v) transposed [nq][ldt] (entries past rows / r must
+// already be zero).
+struct FinishJob {
+  const float* partial;
+  int nsplit;
+  int64_t rows;
+  int r;
+  float scale;
+  float* f32;
+  int f32_t;
+  __nv_bfloat16* b_rows;
+  int rp;
+  float scale_b;
+  __nv_bfloat16* b_t;
+  int64_t ldt;
+  unsigned first_block;
+};
+struct FinishJobs {
+  FinishJob job[2];
+  int n;
+};
+
+__global__ void finish_partials(const FinishJobs jobs) {
   pdl_allow_next();
   pdl_wait();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t w = static_cast<int64_t>(rows) * (b_rows ? rp : r);
+  const FinishJob& f = (jobs.n > 1 && blockIdx.x >= jobs.job[1].first_block) ? jobs.job[1] : jobs.job[0];
+  const int64_t i = static_cast<int64_t>(blockIdx.x - f.first_block) * blockDim.x + threadIdx.x;
+  const int width = f.b_rows ? f.rp : f.r;
+  const int64_t w = f.rows * width;
   if (i >= w) return;
-  const int width = b_rows ? rp : r;
   const int64_t row = i / width;
   const int j = static_cast<int>(i % width);
   float v = 0.0f;
-  if (j < r) {
-    for (int sp = 0; sp < nsplit; ++sp) v += partial[(static_cast<int64_t>(sp) * rows + row) * r + j];
-    if (f32) {
-      if (f32_t) f32[static_cast<int64_t>(j) * rows + row] = scale * v;
-      else f32[row * r + j] = scale * v;
+  if (j < f.r) {
+    for (int sp = 0; sp < f.nsplit; ++sp) v += f.partial[(static_cast<int64_t>(sp) * f.rows + row) * f.r + j];
+    if (f.f32) {
+      if (f.f32_t) f.f32[static_cast<int64_t>(j) * f.rows + row] = f.scale * v;
+      else f.f32[row * f.r + j] = f.scale * v;
     }
-    if (b_t) b_t[static_cast<int64_t>(j) * ldt + row] = __float2bfloat16_rn(v);
+    if (f.b_t) f.b_t[static_cast<int64_t>(j) * f.ldt + row] = __float2bfloat16_rn(v);
   }
-  if (b_rows) b_rows[row * rp + j] = __float2bfloat16_rn(j < r ? scale_b * v : 0.0f);
+  if (f.b_rows) f.b_rows[row * f.rp + j] = __float2bfloat16_rn(j < f.r ? f.scale_b * v : 0.0f);
 }
 
 int nq_of(int r) { return (r + 15) / 16 * 16; }
@@ -247,45 +277,48 @@ size_t partial_bytes(int64_t rows, int64_t red, int r) {
   return al(sizeof(float) * static_cast<size_t>(pl.nsplit) * rows * r);
 }
 
-// One skinny pass: partial sums of X . Q into `partial`; returns the slice count.
-cudaError_t run_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
-                     int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
-                     cudaStream_t st) {
-  const Plan pl = plan(rows, red, resident_ctas());
-  const int nq = nq_of(r);
-  CUtensorMap tx, tq;
-  bool ok = mn_major ? make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, x_inner, x_outer, 2 * x_inner, 64, 64,
-                                CU_TENSOR_MAP_SWIZZLE_128B)
-                     : make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, x_inner, x_outer, 2 * x_inner, 64, kRowsT,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Q, q_cols, nq, 2 * q_cols, 64, nq,
+// Parameters and tensor maps of one pass with `target` CTAs.
+bool setup_pass(const AdapterPassArgs& a, int target, int* status, SkinnyParams* p, CUtensorMap* tx, CUtensorMap* tq) {
+  const Plan pl = plan(a.rows, a.red, target);
+  const int nq = nq_of(a.r);
+  bool ok = a.mn_major ? make_map(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.x_inner, a.x_outer, 2 * a.x_inner, 64,
+                                  64, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : make_map(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.x_inner, a.x_outer, 2 * a.x_inner, 64,
+                                  kRowsT, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.Q, a.q_cols, nq, 2 * a.q_cols, 64, nq,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return cudaErrorInvalidValue;
-  SkinnyParams p{};
-  p.rows = rows;
-  p.tiles = pl.tiles;
-  p.total_steps = pl.total_steps;
-  p.sps = pl.sps;
-  p.a_mn_major = mn_major ? 1 : 0;
-  p.n_mma = nq;
-  p.r = r;
-  p.b_bytes = static_cast<uint32_t>(nq * 128);
-  p.stage_bytes = static_cast<uint32_t>(al(kBoxes * (kATileBytes + p.b_bytes)));
-  p.stages = nq <= 32 ? 3 : 2;
-  p.partial = partial;
-  p.status = status;
-  const int smem = 1024 + p.stages * static_cast<int>(p.stage_bytes) + 256;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(adapter_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 4 * 49152 + 256);
-  });
-  if (attr != cudaSuccess) return attr;
-  const cudaError_t e =
-      launch_pdl(adapter_tc, dim3(pl.tiles * pl.nsplit), dim3(kAThreads), static_cast<size_t>(smem), st, 1, tx, tq, p);
-  note_launch();
-  *nsplit = pl.nsplit;
-  return e;
+  *p = SkinnyParams{};
+  p->rows = a.rows;
+  p->tiles = pl.tiles;
+  p->total_steps = pl.total_steps;
+  p->sps = pl.sps;
+  p->a_mn_major = a.mn_major ? 1 : 0;
+  p->n_mma = nq;
+  p->r = a.r;
+  p->b_bytes = static_cast<uint32_t>(nq * 128);
+  p->stage_bytes = static_cast<uint32_t>(al(kBoxes * (kATileBytes + p->b_bytes)));
+  p->stages = nq <= 32 ? 3 : 2;
+  p->partial = a.partial;
+  p->status = status;
+  p->ctas = pl.tiles * pl.nsplit;
+  return ok;
+}
+
+FinishJob finish_job(const AdapterPassArgs& a, const SkinnyParams& p) {
+  FinishJob f{};
+  f.partial = a.partial;
+  f.nsplit = p.ctas / p.tiles;
+  f.rows = a.rows;
+  f.r = a.r;
+  f.scale = a.scale;
+  f.f32 = a.f32;
+  f.f32_t = a.f32_t;
+  f.b_rows = a.b_rows;
+  f.rp = a.rp;
+  f.scale_b = a.scale_b;
+  f.b_t = a.b_t;
+  f.ldt = a.ldt;
+  return f;
 }
 
 }  // namespace
@@ -294,19 +327,47 @@ int adapter_nq(int r) { return nq_of(r); }
 
 size_t adapter_partial_bytes(int64_t rows, int64_t red, int r) { return partial_bytes(rows, red, r); }
 
-cudaError_t adapter_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
-                         int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
-                         cudaStream_t st) {
+cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  return run_pass(X, x_inner, x_outer, mn_major, Q, q_cols, r, rows, red, partial, status, nsplit, st);
-}
-
-cudaError_t adapter_finish(const float* partial, int nsplit, int64_t rows, int r, float scale, float* f32, int f32_t,
-                           __nv_bfloat16* b_rows, int rp, float scale_b, __nv_bfloat16* b_t, int64_t ldt,
-                           cudaStream_t st) {
-  KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const cudaError_t e = launch_pdl(finish_partials, dim3(blocks(rows * (b_rows ? rp : r))), dim3(256), 0, st, 1,
-                                    partial, nsplit, rows, r, scale, f32, f32_t, b_rows, rp, scale_b, b_t, ldt);
+  if (n < 1 || n > 2) return cudaErrorInvalidValue;
+  // the resident CTAs are shared in proportion to the activation bytes each pass reads
+  const int total = resident_ctas();
+  int target[2] = {total, 0};
+  if (n == 2) {
+    const double b0 = static_cast<double>(a[0].rows) * a[0].red, b1 = static_cast<double>(a[1].rows) * a[1].red;
+    target[0] = std::max(1, static_cast<int>(total * b0 / (b0 + b1)));
+    target[1] = std::max(1, total - target[0]);
+  }
+  SkinnyParams p[2];
+  CUtensorMap tx[2], tq[2];
+  for (int i = 0; i < n; ++i)
+    if (!setup_pass(a[i], target[i], status, &p[i], &tx[i], &tq[i])) return cudaErrorInvalidValue;
+  if (n == 1) {
+    p[1] = SkinnyParams{};
+    tx[1] = tx[0];
+    tq[1] = tq[0];
+  }
+  int smem = 0;
+  for (int i = 0; i < n; ++i) smem = std::max(smem, 1024 + p[i].stages * static_cast<int>(p[i].stage_bytes) + 256);
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(adapter_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 4 * 49152 + 256);
+  });
+  if (attr != cudaSuccess) return attr;
+  cudaError_t e = launch_pdl(adapter_tc, dim3(p[0].ctas + p[1].ctas), dim3(kAThreads), static_cast<size_t>(smem), st,
+                             1, tx[0], tq[0], tx[1], tq[1], p[0], p[1]);
+  note_launch();
+  if (e != cudaSuccess) return e;
+  FinishJobs jobs{};
+  jobs.n = n;
+  unsigned nblocks = 0;
+  for (int i = 0; i < n; ++i) {
+    jobs.job[i] = finish_job(a[i], p[i]);
+    jobs.job[i].first_block = nblocks;
+    nblocks += blocks(a[i].rows * (a[i].b_rows ? a[i].rp : a[i].r));
+  }
+  e = launch_pdl(finish_partials, dim3(nblocks), dim3(256), 0, st, 1, jobs);
   note_launch();
   return e;
 }

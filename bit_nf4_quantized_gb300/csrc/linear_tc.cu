@@ -521,8 +521,8 @@ struct BwdWs {
   size_t sGp, ApT, Bt, Tt, Gt, part, wb, flags, total;
   BwdWs(int64_t M, int64_t N, int64_t K, int r) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r), Mp = pad8(M);
-    size_t pb = adapter_partial_bytes(M, N, r);
-    pb = std::max(pb, adapter_partial_bytes(N, M, r));
+    // G's and dB's partial sums side by side (one launch runs both), later dA's
+    size_t pb = adapter_partial_bytes(M, N, r) + adapter_partial_bytes(N, M, r);
     pb = std::max(pb, adapter_partial_bytes(K, M, r));
     pb = std::max(pb, kMaxPartTiles * kPartTileBytes);
     sGp = 0;
@@ -600,9 +600,24 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   cudaError_t e = prep.launch(st);
   if (e != cudaSuccess) return e;
   if ((e = decode_weight(a, wb, st)) != cudaSuccess) return e;
-  int ns = 0;
-  if ((e = adapter_pass(x, a.K, a.M, false, Aq, a.K, a.r, a.M, a.K, part, status, &ns, st)) != cudaSuccess) return e;
-  if ((e = adapter_finish(part, ns, a.M, a.r, 1.0f, T, 0, sTp, rp, a.s, nullptr, 0, st)) != cudaSuccess) return e;
+  {  // T = x A^T: rows M, reduction over K along x's rows; T (fp32) and bf16(s T) for the slab
+    AdapterPassArgs t{};
+    t.X = x;
+    t.x_inner = a.K;
+    t.x_outer = a.M;
+    t.Q = Aq;
+    t.q_cols = a.K;
+    t.r = a.r;
+    t.rows = a.M;
+    t.red = a.K;
+    t.partial = part;
+    t.scale = 1.0f;
+    t.f32 = T;
+    t.b_rows = sTp;
+    t.rp = rp;
+    t.scale_b = a.s;
+    if ((e = adapter_run(&t, 1, status, st)) != cudaSuccess) return e;
+  }
   CUtensorMap wm, tok, slab_f, slab_t;
   bool ok = make_map(&wm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb, a.K, a.N, 2 * a.K, kSub, kTileF,
                      CU_TENSOR_MAP_SWIZZLE_128B);
@@ -672,13 +687,41 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   cudaError_t e = prep.launch(st);
   if (e != cudaSuccess) return e;
   if ((e = decode_weight(a, wb, st)) != cudaSuccess) return e;
-  int ns = 0;
-  // G = dY B: rows M, reduction over N along dY's rows; also bf16(s G) and bf16(G)^T
-  if ((e = adapter_pass(dy, a.N, a.M, false, Bt, a.N, a.r, a.M, a.N, part, status, &ns, st)) != cudaSuccess) return e;
-  if ((e = adapter_finish(part, ns, a.M, a.r, 1.0f, G, 0, sGp, rp, a.s, Gt, Mp, st)) != cudaSuccess) return e;
-  // dB = s dY^T T: rows N, reduction over M down dY's columns
-  if ((e = adapter_pass(dy, a.N, a.M, true, Tt, Mp, a.r, a.N, a.M, part, status, &ns, st)) != cudaSuccess) return e;
-  if ((e = adapter_finish(part, ns, a.N, a.r, a.s, dB, 0, nullptr, 0, 0.0f, nullptr, 0, st)) != cudaSuccess) return e;
+  {  // one launch for G = dY B (rows M, reduction over N along dY's rows; G, bf16(s G), bf16(G)^T)
+     // and dB = s dY^T T (rows N, reduction over M down dY's columns), then one for both finishes
+    AdapterPassArgs pa[2] = {};
+    AdapterPassArgs& g = pa[0];
+    g.X = dy;
+    g.x_inner = a.N;
+    g.x_outer = a.M;
+    g.Q = Bt;
+    g.q_cols = a.N;
+    g.r = a.r;
+    g.rows = a.M;
+    g.red = a.N;
+    g.partial = part;
+    g.scale = 1.0f;
+    g.f32 = G;
+    g.b_rows = sGp;
+    g.rp = rp;
+    g.scale_b = a.s;
+    g.b_t = Gt;
+    g.ldt = Mp;
+    AdapterPassArgs& d = pa[1];
+    d.X = dy;
+    d.x_inner = a.N;
+    d.x_outer = a.M;
+    d.mn_major = true;
+    d.Q = Tt;
+    d.q_cols = Mp;
+    d.r = a.r;
+    d.rows = a.N;
+    d.red = a.M;
+    d.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(part) + adapter_partial_bytes(a.M, a.N, a.r));
+    d.scale = a.s;
+    d.f32 = dB;
+    if ((e = adapter_run(pa, 2, status, st)) != cudaSuccess) return e;
+  }
   CUtensorMap wm, tok, slab_f, slab_t;
   // W [N][K] read as 64 features x 64 rows n (MN-major A: the features are the MMA's M)
   bool ok = make_map(&wm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb, a.K, a.N, 2 * a.K, kSub, kSub,
@@ -695,8 +738,21 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   gp.part_flags = reinterpret_cast<int*>(w + L.flags);
   if ((e = launch_gemm(gp, wm, tok, slab_f, slab_t, st)) != cudaSuccess) return e;
   // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
-  if ((e = adapter_pass(x, a.K, a.M, true, Gt, Mp, a.r, a.K, a.M, part, status, &ns, st)) != cudaSuccess) return e;
-  return adapter_finish(part, ns, a.K, a.r, a.s, dA, 1, nullptr, 0, 0.0f, nullptr, 0, st);
+  AdapterPassArgs da{};
+  da.X = x;
+  da.x_inner = a.K;
+  da.x_outer = a.M;
+  da.mn_major = true;
+  da.Q = Gt;
+  da.q_cols = Mp;
+  da.r = a.r;
+  da.rows = a.K;
+  da.red = a.M;
+  da.partial = part;
+  da.scale = a.s;
+  da.f32 = dA;
+  da.f32_t = 1;
+  return adapter_run(&da, 1, status, st);
 }
 
 }  // namespace qnf4

@@ -18,17 +18,33 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
 // adapter_tc.cu: skinny tcgen05 products Out[rows, r] = X[rows, red] . Q[red, r] for the
 // rank-r contractions.  X is bf16 row-major with `x_inner` columns (the reduction runs
 // along its rows when mn_major == false, down its columns otherwise); Q is bf16
-// [nq][q_cols] (nq = r rounded up to 16).  Reduction slices write partial sums that
-// adapter_finish adds in a fixed order.
+// [nq][q_cols] (nq = r rounded up to 16).  Reduction slices write partial sums to
+// `partial` (adapter_partial_bytes) that a second launch adds in a fixed order, writing:
+//   f32 = scale * sum as [rows][r] (or [r][rows] when f32_t), if f32 is set;
+//   bf16(scale_b * sum) as [rows][rp], zero past r, if b_rows is set;
+//   bf16(sum) as [r][ldt] (rows r.. of a [nq][ldt] buffer untouched), if b_t is set.
+struct AdapterPassArgs {
+  const void* X;
+  int64_t x_inner, x_outer;
+  bool mn_major;
+  const __nv_bfloat16* Q;
+  int64_t q_cols;
+  int r;
+  int64_t rows, red;
+  float* partial;
+  float scale;
+  float* f32;
+  int f32_t;
+  __nv_bfloat16* b_rows;
+  int rp;
+  float scale_b;
+  __nv_bfloat16* b_t;
+  int64_t ldt;
+};
 int adapter_nq(int r);
 size_t adapter_partial_bytes(int64_t rows, int64_t red, int r);
-cudaError_t adapter_pass(const void* X, int64_t x_inner, int64_t x_outer, bool mn_major, const __nv_bfloat16* Q,
-                         int64_t q_cols, int r, int64_t rows, int64_t red, float* partial, int* status, int* nsplit,
-                         cudaStream_t st);
-// Sum of the slices times `scale` into f32 ([rows][r], or [r][rows] when f32_t), and
-// optionally bf16(scale_b * sum) into b_rows [rows][rp] and bf16(sum) into b_t [nq][ldt].
-cudaError_t adapter_finish(const float* partial, int nsplit, int64_t rows, int r, float scale, float* f32, int f32_t,
-                           __nv_bfloat16* b_rows, int rp, float scale_b, __nv_bfloat16* b_t, int64_t ldt,
-                           cudaStream_t st);
+// One or two independent passes (n = 1 or 2, separate `partial` buffers) in one launch,
+// then their finishes in one more.
+cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream_t st);
 
 }  // namespace qnf4
