@@ -143,6 +143,10 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
                             void* ws, int* status, cudaStream_t st);
 size_t quantize_ws_bytes(int64_t numel, int dq);
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st);
+struct PrepJobs;
+// quant.cu: the bf16 decode of w into y and `prep_ctas` CTAs of staging jobs, one launch.
+cudaError_t launch_decode_with_prep(const Nf4View& w, __nv_bfloat16* y, const PrepJobs& jobs, unsigned prep_ctas,
+                                    cudaStream_t st);
 
 // ---- linear_simt.cu (fp32 profile; adapter reductions for both profiles) -------
 struct LinearArgs {

@@ -494,10 +494,12 @@ PrepJob zero_flags_job(void* flags) {
   return j;
 }
 
-// The weight decoded to bf16 [N][K] for this call (bit-exact with nf4_dequantize).
-cudaError_t decode_weight(const LinearArgs& a, void* wb, cudaStream_t st) {
+// The weight decoded to bf16 [N][K] for this call (bit-exact with nf4_dequantize), in the
+// same launch as the call's operand staging (extra CTAs run the prep jobs).
+cudaError_t decode_weight(const LinearArgs& a, void* wb, const PrepBuilder& prep, cudaStream_t st) {
+  if (!prep.ok()) return cudaErrorInvalidValue;
   KernelTimer timer(NF4_TIME_WEIGHT_DECODE, st);
-  return launch_dequantize(a.W, wb, NF4_BF16, st);
+  return launch_decode_with_prep(a.W, static_cast<__nv_bfloat16*>(wb), prep.jobs(), prep.ctas(), st);
 }
 
 // Workspace layouts (every part 1024-byte aligned).  `part` holds the skinny passes'
@@ -564,7 +566,7 @@ size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return FwdWs(M,
 
 size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return BwdWs(M, N, K, r).total; }
 
-// Forward: prep (A and B in bf16) -> W in bf16 -> T = x A^T (skinny tcgen05) ->
+// Forward: W in bf16 with prep (A and B in bf16) -> T = x A^T (skinny tcgen05) ->
 // T and bf16(s T) -> GEMM with the (s T) B^T slab.
 cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y, float* T,
                        void* ws, int* status, cudaStream_t st) {
@@ -597,9 +599,8 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
     prep.add(b);
     prep.add(zero_flags_job(w + L.flags));
   }
-  cudaError_t e = prep.launch(st);
+  cudaError_t e = decode_weight(a, wb, prep, st);
   if (e != cudaSuccess) return e;
-  if ((e = decode_weight(a, wb, st)) != cudaSuccess) return e;
   {  // T = x A^T: rows M, reduction over K along x's rows; T (fp32) and bf16(s T) for the slab
     AdapterPassArgs t{};
     t.X = x;
@@ -634,7 +635,7 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
 }
 
-// Backward: prep (B^T, T^T, zeroed G^T, A^T in bf16) -> W in bf16 -> G = dY B ->
+// Backward: W in bf16 with prep (B^T, T^T, zeroed G^T, A^T in bf16) -> G = dY B ->
 // G, bf16(s G), bf16(G)^T -> dB = s dY^T T -> GEMM for dX with the (s G) A slab ->
 // dA = s G^T x.
 cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, const float* T, const float* A,
@@ -684,9 +685,8 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
     prep.add(c);
     prep.add(zero_flags_job(w + L.flags));
   }
-  cudaError_t e = prep.launch(st);
+  cudaError_t e = decode_weight(a, wb, prep, st);
   if (e != cudaSuccess) return e;
-  if ((e = decode_weight(a, wb, st)) != cudaSuccess) return e;
   {  // one launch for G = dY B (rows M, reduction over N along dY's rows; G, bf16(s G), bf16(G)^T)
      // and dB = s dY^T T (rows N, reduction over M down dY's columns), then one for both finishes
     AdapterPassArgs pa[2] = {};

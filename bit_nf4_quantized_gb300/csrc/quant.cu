@@ -18,6 +18,7 @@
 //   3. nf4_encode_nested: centre, nested absmax per group, dynamic8 codes.
 #include "common.cuh"
 #include "decode.cuh"
+#include "prep.cuh"
 
 #include <mutex>
 
@@ -296,9 +297,10 @@ __device__ __forceinline__ uint32_t stage_slot(uint32_t g) {
   return ((row << 3) | (col ^ (row & 7))) << 4;
 }
 
+// One CTA's share of the decode: block `cta` of the dequantize grid.
 template <typename Tout, bool kDQ>
-__global__ void __launch_bounds__(kDeqThreads)
-nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
+__device__ __forceinline__ void decode_cta(const Nf4View& w, Tout* __restrict__ y, const DecodeTables& tabs,
+                                           int64_t cta) {
   constexpr int kOutBytes = 32 * sizeof(Tout);      // per lane per chunk: 64 (bf16) or 128 (fp32)
   __shared__ float dyn8[256];
   __shared__ float lut[16][32];                     // code values replicated per lane (fp32 path)
@@ -314,7 +316,7 @@ nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
   const float offset = kDQ ? *w.offset : 0.0f;
   uint8_t* buf = stage[warp];
   const uint32_t buf_s = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
-  const int64_t chunk0 = (static_cast<int64_t>(blockIdx.x) * (kDeqThreads / 32) + warp) * kDeqChunks;
+  const int64_t chunk0 = (cta * (kDeqThreads / 32) + warp) * kDeqChunks;
 
   uint4 pk[kDeqChunks];
   float sc[kDeqChunks];
@@ -399,6 +401,21 @@ nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
   }
 }
 
+template <typename Tout, bool kDQ>
+__global__ void __launch_bounds__(kDeqThreads)
+nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
+  decode_cta<Tout, kDQ>(w, y, tabs, blockIdx.x);
+}
+
+// The bf16 decode of the linear's weight and that call's operand staging in one launch:
+// CTAs below `decode_ctas` decode, the rest run the prep jobs.
+template <bool kDQ>
+__global__ void __launch_bounds__(kDeqThreads)
+nf4_decode_prep(Nf4View w, __nv_bfloat16* __restrict__ y, DecodeTables tabs, PrepJobs jobs, unsigned decode_ctas) {
+  if (blockIdx.x < decode_ctas) decode_cta<__nv_bfloat16, kDQ>(w, y, tabs, blockIdx.x);
+  else prep_cta(jobs, blockIdx.x - decode_ctas);
+}
+
 int64_t pow2_at_least(int64_t v) {
   int64_t p = 1;
   while (p < v) p <<= 1;
@@ -469,6 +486,19 @@ cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStrea
     if (w.dq) e = launch_pdl(nf4_decode<__nv_bfloat16, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt);
     else e = launch_pdl(nf4_decode<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt);
   }
+  note_launch();
+  return e;
+}
+
+cudaError_t launch_decode_with_prep(const Nf4View& w, __nv_bfloat16* y, const PrepJobs& jobs, unsigned prep_ctas,
+                                    cudaStream_t st) {
+  const int64_t ctas = (w.numel + kDeqPerCta - 1) / kDeqPerCta;
+  if (ctas + prep_ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(ctas + prep_ctas));
+  const DecodeTables& dt = decode_tables();
+  const unsigned dc = static_cast<unsigned>(ctas);
+  const cudaError_t e = w.dq ? launch_pdl(nf4_decode_prep<true>, grid, dim3(kDeqThreads), 0, st, 1, w, y, dt, jobs, dc)
+                             : launch_pdl(nf4_decode_prep<false>, grid, dim3(kDeqThreads), 0, st, 1, w, y, dt, jobs, dc);
   note_launch();
   return e;
 }
