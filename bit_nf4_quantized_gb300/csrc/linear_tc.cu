@@ -81,14 +81,16 @@ struct GemmParams {
   __nv_bfloat16* out;  // [M, F]
   int* status;
   // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
-  // round of clusters) in `split` parts along the contraction, `chunk` steps each;
-  // the last part runs the slab steps and adds the other parts' partial sums, which
-  // they leave in part_ws ([slot][part < split-1][rank][256 tokens][128 rows] fp32) with
-  // one flag per (slot, part, rank, epilogue warp) in part_flags (zero at launch)
+  // round of clusters) in `split` parts along the contraction, `chunk` steps each (the
+  // last part also runs the slab steps).  Every part leaves its fp32 partial sums in
+  // part_ws ([slot][part][rank][256 tokens][128 rows]) and takes a ticket from
+  // part_tickets[slot][rank] (zero at launch); the CTA that draws the last ticket adds the
+  // parts in part order and stores the tile.  Nothing waits for another cluster, so the
+  // launch completes whether or not all its clusters are resident at once.
   int64_t full_units, total_units;
   int split, chunk;
   float* part_ws;
-  int* part_flags;
+  int* part_tickets;
 };
 
 struct Unit {
@@ -295,6 +297,7 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
     // with TMA (two boxes alternate).  The four warps meet at named barrier 1; whether to
     // go on is decided by a vote, so that all four always take the same path.
     __shared__ int votes[2][4];
+    __shared__ int last_ticket;
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
     const int lrow = quarter * 32 + lane;       // this thread's row of the CTA's 128
     const bool issuer = warp == kWarpEpi && lane == 0;
@@ -313,13 +316,11 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
       const uint32_t taddr = tmem_base + b * kTileT + (static_cast<uint32_t>(quarter * 32) << 16);
       // partial sums of a split tile: [slot][part][rank][256][128] fp32, coalesced along rows
       auto part_buf = [&](int part) {
-        return p.part_ws + ((un.slot * (p.split - 1) + part) * kCluster + rank) * (static_cast<int64_t>(kTileT) * 128);
+        return p.part_ws + ((un.slot * p.split + part) * kCluster + rank) * (static_cast<int64_t>(kTileT) * 128);
       };
-      auto part_flag = [&](int part) {
-        return p.part_flags + ((un.slot * (p.split - 1) + part) * kCluster + rank) * 4 + quarter;
-      };
-      if (un.part < un.nparts - 1) {
-        // a leading part of a split tile: fp32 partial sums, then this warp's flag
+      bool store_tile = true;       // this CTA writes the tile's output
+      if (un.nparts > 1) {
+        // every part: its partial sums, then a ticket; the last ticket finishes the tile
 #pragma unroll 1
         for (int c0 = 0; c0 < kTileT; c0 += 16) {
           uint32_t v[16];
@@ -330,30 +331,16 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
           for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(v[j]);
         }
         __threadfence();
-        __syncwarp();
-        if (lane == 0) asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(part_flag(un.part)), "r"(1) : "memory");
-      } else {
-        bool have_parts = true;
-        if (un.nparts > 1) {
-          // wait (bounded) for the other parts of this tile, rows of this warp only
-          for (int q = 0; q < un.nparts - 1 && have_parts; ++q) {
-            const int* flag = part_flag(q);
-            const uint64_t w0 = global_ns();
-            int v = 0;
-            for (uint32_t i = 0;; ++i) {
-              asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-              if (v != 0) break;
-              if ((i & 31u) == 31u && (*abort_flag || global_ns() - w0 > kWaitLimitNs)) {
-                if (!*abort_flag) {
-                  *abort_flag = 1;
-                  atomicCAS(p.status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
-                }
-                break;
-              }
-            }
-            have_parts = __all_sync(0xffffffffu, v != 0);
-          }
+        named_sync(1, 128);
+        if (issuer) {
+          const int t = atomicAdd(p.part_tickets + un.slot * kCluster + rank, 1);
+          last_ticket = (t == un.nparts - 1) ? 1 : 0;
         }
+        named_sync(1, 128);
+        store_tile = last_ticket != 0;
+        if (store_tile) __threadfence();
+      }
+      if (store_tile) {
 #pragma unroll 1
         for (int c0 = 0; c0 < kTileT; c0 += kOutRows, ++nst) {
           const uint32_t box = out_stage + (nst & 1u) * kOutBytes;
@@ -362,14 +349,20 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
 #pragma unroll
           for (int h = 0; h < kOutRows; h += 16) {
             uint32_t v[16];
-            tmem_ld16(taddr + c0 + h, v);
-            tmem_ld_wait();
-            if (un.nparts > 1 && have_parts) {
-              for (int q = 0; q < un.nparts - 1; ++q) {   // parts in order: deterministic sums
+            if (un.nparts > 1) {   // the parts' sums in part order: deterministic
+              float acc[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+              for (int q = 0; q < un.nparts; ++q) {
                 const float* src = part_buf(q) + static_cast<int64_t>(c0 + h) * 128 + lrow;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(src + j * 128));
+                for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + j * 128);
               }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[j]);
+            } else {
+              tmem_ld16(taddr + c0 + h, v);
+              tmem_ld_wait();
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -415,7 +408,7 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
-constexpr int kMaxPartTiles = 80;   // partial-sum tiles (of a cluster pair) a split may use
+constexpr int kMaxPartTiles = 80;   // partial-sum tiles (of a cluster pair) a split may use (all parts)
 constexpr int kMaxSplit = 4;
 constexpr size_t kPartTileBytes = static_cast<size_t>(kCluster) * kTileT * 128 * sizeof(float);
 constexpr size_t kPartFlagBytes = static_cast<size_t>(kMaxPartTiles) * kCluster * 4 * sizeof(int);
@@ -431,7 +424,7 @@ void split_tail(GemmParams* p, int64_t pairs, int64_t clusters) {
   if (rounds == 0 || tail == 0) return;
   int split = static_cast<int>(std::min<int64_t>(clusters / tail, kMaxSplit));
   split = std::min(split, p->red_steps);
-  while (split > 1 && tail * (split - 1) > kMaxPartTiles) --split;
+  while (split > 1 && tail * split > kMaxPartTiles) --split;
   if (split < 2) return;
   const int chunk = (p->red_steps + split - 1) / split;
   split = (p->red_steps + chunk - 1) / chunk;   // every part keeps at least one contraction step
@@ -631,7 +624,7 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 0, y, status);
   gp.part_ws = part;
-  gp.part_flags = reinterpret_cast<int*>(w + L.flags);
+  gp.part_tickets = reinterpret_cast<int*>(w + L.flags);
   return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
 }
 
@@ -735,7 +728,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   if (!ok) return cudaErrorInvalidValue;
   GemmParams gp = base_params(a, 1, dx, status);
   gp.part_ws = part;
-  gp.part_flags = reinterpret_cast<int*>(w + L.flags);
+  gp.part_tickets = reinterpret_cast<int*>(w + L.flags);
   if ((e = launch_gemm(gp, wm, tok, slab_f, slab_t, st)) != cudaSuccess) return e;
   // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
   AdapterPassArgs da{};

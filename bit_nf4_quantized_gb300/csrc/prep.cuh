@@ -30,7 +30,7 @@ struct PrepJob {
 };
 
 constexpr int kMaxPrepJobs = 8;
-constexpr int kPrepThreads = 256;   // threads of a prep CTA
+constexpr int kPrepThreads = 256;   // threads of a prep CTA (the decode launch's CTA width)
 constexpr int kPrepPer = 8;         // outputs per thread: one 16-byte store
 
 struct PrepJobs {

@@ -107,11 +107,13 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
                   float* __restrict__ absmax, double* __restrict__ group_sum, EncodeTables tabs,
                   int* status) {
   __shared__ float thr[16];
-  __shared__ float2 band[66][32];   // (lo with the base code in its low 4 bits, hi), one column per lane
+  // (lo with the base code in its low 4 bits, hi); 16 copies: the 8-byte lookups of a warp are
+  // served half a warp at a time, so lanes l and l + 16 never meet in one bank access
+  __shared__ float2 band[66][16];
   __shared__ double gsum[kNested];
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
-  for (int i = threadIdx.x; i < 66 * 32; i += kQuantThreads)
-    band[i >> 5][i & 31] = make_float2(tabs.nf4_band[i >> 5][0], tabs.nf4_band[i >> 5][1]);
+  for (int i = threadIdx.x; i < 66 * 16; i += kQuantThreads)
+    band[i >> 4][i & 15] = make_float2(tabs.nf4_band[i >> 4][0], tabs.nf4_band[i >> 4][1]);
   __syncthreads();
   pdl_allow_next();
   pdl_wait();
@@ -145,7 +147,7 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict_
         for (int i = 0; i < 32; ++i) {
           const float q = v[i] * r;
           const uint32_t k = (__float_as_uint(fmaf(v[i], r, 3.0f)) >> 17) - 8191u;   // 0 .. 65
-          const float2 b = band[k][lane];
+          const float2 b = band[k][lane & 15];
           unsure |= (q >= b.x) & (q < b.y);
           const uint32_t c = (__float_as_uint(b.x) & 15u) + (q >= b.y ? 1u : 0u);
           words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
@@ -210,14 +212,20 @@ nf4_absmax_mean(double* __restrict__ gs, int64_t ng, int64_t p2, int64_t nb, flo
   extern __shared__ double tree[];
   pdl_allow_next();
   pdl_wait();
-  const bool in_smem = p2 <= kMeanSmemEntries;
+  const bool in_smem = p2 >= 4 && p2 / 4 <= kMeanSmemEntries;
   double* s = in_smem ? tree : gs;
-  if (in_smem) {
-    for (int64_t i = threadIdx.x; i < ng; i += blockDim.x) s[i] = gs[i];
-    __syncthreads();
-  }
   int64_t valid = ng;
-  for (int64_t h = p2 / 2; h >= 1; h /= 2) {
+  int64_t h = p2 / 2;
+  if (in_smem) {   // the first two levels straight from the workspace into p2 / 4 entries
+    const int64_t q = p2 / 4;
+    auto g = [&](int64_t i) { return i < ng ? gs[i] : 0.0; };
+    for (int64_t i = threadIdx.x; i < q; i += blockDim.x)
+      s[i] = (g(i) + g(i + 2 * q)) + (g(i + q) + g(i + 3 * q));
+    __syncthreads();
+    valid = q;
+    h = q / 2;
+  }
+  for (; h >= 1; h /= 2) {
     for (int64_t i = threadIdx.x; i < h; i += blockDim.x) {
       const double a = (i < valid) ? s[i] : 0.0;
       const double b = (i + h < valid) ? s[i + h] : 0.0;
@@ -290,6 +298,7 @@ nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __r
 constexpr int kDeqThreads = 256;
 constexpr int kDeqChunks = 2;                       // chunks per warp, loads issued together
 constexpr int kDeqPerCta = (kDeqThreads / 32) * kDeqChunks * 1024;
+static_assert(kDeqThreads == kPrepThreads, "prep jobs run in CTAs of the decode launch");
 
 // 16-byte slot g of a warp's staging buffer, rows of 8 slots XOR-swizzled by row.
 __device__ __forceinline__ uint32_t stage_slot(uint32_t g) {
@@ -303,10 +312,15 @@ __device__ __forceinline__ void decode_cta(const Nf4View& w, Tout* __restrict__ 
                                            int64_t cta) {
   constexpr int kOutBytes = 32 * sizeof(Tout);      // per lane per chunk: 64 (bf16) or 128 (fp32)
   __shared__ float dyn8[256];
-  __shared__ float lut[16][32];                     // code values replicated per lane (fp32 path)
   __shared__ __align__(16) uint8_t stage[kDeqThreads / 32][32 * kOutBytes];
-  dyn8[threadIdx.x] = tabs.dyn8[threadIdx.x];
-  for (int i = threadIdx.x; i < 16 * 32; i += kDeqThreads) lut[i >> 5][i & 31] = tabs.nf4[i >> 5];
+  for (int i = threadIdx.x; i < 256; i += kDeqThreads) dyn8[i] = tabs.dyn8[i];
+  // code values replicated per lane (fp32 output only)
+  float (*lut)[32] = nullptr;
+  if constexpr (sizeof(Tout) == 4) {
+    __shared__ float lut_f32[16][32];
+    for (int i = threadIdx.x; i < 16 * 32; i += kDeqThreads) lut_f32[i >> 5][i & 31] = tabs.nf4[i >> 5];
+    lut = lut_f32;
+  }
   __syncthreads();
   pdl_allow_next();
   pdl_wait();
@@ -454,7 +468,7 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
   note_launch();
   if (e != cudaSuccess || !out.double_quant) return e;
   const int64_t p2 = pow2_at_least(ng);
-  const size_t mean_smem = p2 <= kMeanSmemEntries ? sizeof(double) * static_cast<size_t>(p2) : 0;
+  const size_t mean_smem = (p2 >= 4 && p2 / 4 <= kMeanSmemEntries) ? sizeof(double) * static_cast<size_t>(p2 / 4) : 0;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
