@@ -82,11 +82,13 @@ struct GemmParams {
   int* status;
   // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
   // round of clusters) in `split` parts along the contraction, `chunk` steps each (the
-  // last part also runs the slab steps).  Every part leaves its fp32 partial sums in
-  // part_ws ([slot][part][rank][256 tokens][128 rows]) and takes a ticket from
-  // part_tickets[slot][rank] (zero at launch); the CTA that draws the last ticket adds the
-  // parts in part order and stores the tile.  Nothing waits for another cluster, so the
-  // launch completes whether or not all its clusters are resident at once.
+  // last part also runs the slab steps).  The leading parts leave their fp32 partial sums
+  // in part_ws ([slot][part][rank][256 tokens][128 rows]) and take a ticket from
+  // part_tickets[slot][rank] (zero at launch).  The last part, if it finds every ticket
+  // taken, adds their sums to its own (still in TMEM) and stores the tile; otherwise it
+  // leaves its sums too and takes a ticket, and the CTA that draws the last ticket stores
+  // the tile.  The sum is always last part + parts 0, 1, ... in order.  Nothing waits for
+  // another cluster, so a launch completes even when not all its clusters are resident.
   int64_t full_units, total_units;
   int split, chunk;
   float* part_ws;
@@ -319,25 +321,41 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         return p.part_ws + ((un.slot * p.split + part) * kCluster + rank) * (static_cast<int64_t>(kTileT) * 128);
       };
       bool store_tile = true;       // this CTA writes the tile's output
+      bool last_in_tmem = true;     // the last part's sums are in this CTA's TMEM
       if (un.nparts > 1) {
-        // every part: its partial sums, then a ticket; the last ticket finishes the tile
+        int* ticket = p.part_tickets + un.slot * kCluster + rank;
+        bool fast = false;          // the last part, with every other part already done
+        if (un.part == un.nparts - 1) {
+          if (issuer) {
+            int seen;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(ticket) : "memory");
+            last_ticket = (seen == un.nparts - 1) ? 1 : 0;
+          }
+          named_sync(1, 128);
+          fast = last_ticket != 0;
+          named_sync(1, 128);
+        }
+        if (!fast) {
+          // this part's sums to the workspace, then a ticket; the last ticket finishes the tile
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTileT; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
-          float* dst = part_buf(un.part) + static_cast<int64_t>(c0) * 128 + lrow;
+          for (int c0 = 0; c0 < kTileT; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c0, v);
+            tmem_ld_wait();
+            float* dst = part_buf(un.part) + static_cast<int64_t>(c0) * 128 + lrow;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(v[j]);
+            for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(v[j]);
+          }
+          __threadfence();
+          named_sync(1, 128);
+          if (issuer) {
+            const int t = atomicAdd(ticket, 1);
+            last_ticket = (t == un.nparts - 1) ? 1 : 0;
+          }
+          named_sync(1, 128);
+          store_tile = last_ticket != 0;
+          last_in_tmem = false;
         }
-        __threadfence();
-        named_sync(1, 128);
-        if (issuer) {
-          const int t = atomicAdd(p.part_tickets + un.slot * kCluster + rank, 1);
-          last_ticket = (t == un.nparts - 1) ? 1 : 0;
-        }
-        named_sync(1, 128);
-        store_tile = last_ticket != 0;
         if (store_tile) __threadfence();
       }
       if (store_tile) {
@@ -349,20 +367,19 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
 #pragma unroll
           for (int h = 0; h < kOutRows; h += 16) {
             uint32_t v[16];
-            if (un.nparts > 1) {   // the parts' sums in part order: deterministic
-              float acc[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-              for (int q = 0; q < un.nparts; ++q) {
-                const float* src = part_buf(q) + static_cast<int64_t>(c0 + h) * 128 + lrow;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] += __ldcg(src + j * 128);
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[j]);
-            } else {
+            if (last_in_tmem) {
               tmem_ld16(taddr + c0 + h, v);
               tmem_ld_wait();
+            } else {               // the last part's sums from the workspace
+              const float* src = part_buf(un.nparts - 1) + static_cast<int64_t>(c0 + h) * 128 + lrow;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__ldcg(src + j * 128));
+            }
+            // then the other parts in part order: the same sums whichever CTA finishes
+            for (int q = 0; q < un.nparts - 1; ++q) {
+              const float* src = part_buf(q) + static_cast<int64_t>(c0 + h) * 128 + lrow;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(src + j * 128));
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
