@@ -237,7 +237,6 @@ __global__ void finish_partials(const FinishJobs jobs) {
 }
 
 int nq_of(int r) { return (r + 15) / 16 * 16; }
-int rp_of(int r) { return (r + 63) / 64 * 64; }
 size_t al(size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); }
 unsigned blocks(int64_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
