@@ -138,7 +138,8 @@ nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, voi
 
 /* Workspace (device bytes) needed by qlora_linear_fwd / qlora_linear_bwd.  With
  * compute = NF4_BF16 it includes a bf16 copy of the decoded weight (2*N*K bytes): each
- * call decodes W once into it (the bits nf4_dequantize writes) before the contraction. */
+ * call decodes W once into it (the bits nf4_dequantize writes) before the contraction.
+ * Calls on different streams need separate workspaces. */
 size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
 size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
 
@@ -193,8 +194,9 @@ typedef enum {
   NF4_TIME_DEQUANTIZE = 1,  /* the decode kernel */
   NF4_TIME_FWD_GEMM = 2,    /* base contraction of the forward (y) */
   NF4_TIME_DX_GEMM = 3,     /* base contraction of the input gradient (dX) */
-  NF4_TIME_ADAPTER = 4,     /* adapter-side kernels (T, G, dA, dB, operand staging) */
-  NF4_TIME_WEIGHT_DECODE = 5, /* the bf16 profile's per-call decode of W before its GEMM */
+  NF4_TIME_ADAPTER = 4,     /* adapter-side kernels (T, G, dA, dB) */
+  NF4_TIME_WEIGHT_DECODE = 5, /* the bf16 profile's per-call decode of W before its GEMM,
+                               * with the call's operand staging in the same launch */
   NF4_TIME_KINDS = 6
 } nf4_timed_kernel;
 
