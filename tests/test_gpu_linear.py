@@ -154,3 +154,23 @@ def test_linear_is_deterministic(lib):
         outs.append([t.clone() for t in (y, T, dx, dA, dB)])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def test_split_tiles_are_deterministic(lib):
+    """4096 x 1344 x 1344: 96 tile pairs on the GEMM's clusters leave a partial last round
+    whose tiles are split along the contraction.  Whichever CTA finishes a split tile (the
+    last part straight from its accumulator, or the last ticket from the parts' sums), the
+    sum runs in the same order, so repeated calls give identical bits."""
+    q, _ = _quantized_weight(1344, 1344, 11)
+    x = torch.randn(4096, 1344, device=DEV, dtype=torch.bfloat16)
+    dy = torch.randn(4096, 1344, device=DEV, dtype=torch.bfloat16)
+    A = torch.randn(16, 1344, device=DEV) / 16
+    B = torch.randn(1344, 16, device=DEV) / 100
+    outs = []
+    for _ in range(3):
+        y, T = binding.qlora_linear_fwd(x, q, A, B, 16.0)
+        dx, dA, dB = binding.qlora_linear_bwd(dy, x, T, q, A, B, 16.0)
+        outs.append([t.clone() for t in (y, dx, dA, dB)])
+    for later in outs[1:]:
+        for a, b in zip(outs[0], later):
+            assert torch.equal(a, b)
