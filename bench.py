@@ -322,6 +322,61 @@ def reference_arm(args, rank, world):
 
 # ---- main ---------------------------------------------------------------------------
 
+def random_stored_nf4(shape, seed, dev):
+    """An NF4 tensor of random stored bytes on the device (codes, scale codes, nested
+    maxima in U(0.01, 0.05), offset 0.03): any byte pattern is a valid stored tensor."""
+    import torch
+    from bit_nf4_quantized_gb300 import binding as bq
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    q = bq.Nf4Tensor.empty(shape, True, dev)
+    q.packed.copy_(torch.randint(0, 256, q.packed.shape, generator=g, device=dev, dtype=torch.uint8))
+    q.absmax.copy_(torch.randint(0, 256, q.absmax.shape, generator=g, device=dev, dtype=torch.uint8))
+    q.nested_absmax.copy_(torch.rand(q.nested_absmax.shape, generator=g, device=dev) * 0.04 + 0.01)
+    q.offset[0] = 0.03
+    return q
+
+
+def measure_export_rows(dev, row_ms, hbm):
+    """The selected-row embedding decode and the merged-weight export, each one call timed
+    as a replayed graph with L2 flushed between replays; GB/s of algorithmic bytes."""
+    import torch
+    from bit_nf4_quantized_gb300 import binding as bq
+    from bit_nf4_quantized_gb300 import workloads as wl
+    lib = bq.load()
+    e = wl.W6
+    rows, dim, n_ids = e["rows"], e["dim"], e["n_ids"]
+    table = random_stored_nf4((rows, dim), wl.seed_for(6, 10), dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed_for(6, 11))
+    ids = torch.randint(0, rows, (n_ids,), generator=g, device=dev, dtype=torch.int64)
+    rows_out = torch.empty((n_ids, dim), dtype=torch.bfloat16, device=dev)
+    # per id: dim/2 code bytes, dim/64 scale codes, one 4-byte nested maximum (a 4096-wide
+    # row lies in one 16384-element group), the 8-byte id and dim bf16 outputs
+    emb_bytes = n_ids * (dim // 2 + dim // 64 + 4 + 8 + 2 * dim)
+    emb_ms = row_ms(lambda: bq.nf4_embedding_rows(table, ids, out=rows_out), reps=20)
+    del table, rows_out
+
+    m = wl.W7
+    N, K, r = m["N"], m["K"], m["r"]
+    W = random_stored_nf4((N, K), wl.seed_for(7, 20), dev)
+    A = wl.device_normal((r, K), 1.0 / r, wl.seed_for(7, 21), dev, torch.float32)
+    B = wl.device_normal((N, r), 0.01, wl.seed_for(7, 22), dev, torch.float32)
+    merged = torch.empty((N, K), dtype=torch.float32, device=dev)
+    merge_bytes = lib.nf4_packed_bytes(N * K, 1) + 4 * r * K + 4 * N * r + 4 * N * K
+    merge_ms = row_ms(lambda: bq.nf4_merge_lora(W, A, B, m["alpha"], out=merged), reps=20)
+    del W, merged
+    emb_gbs = emb_bytes / (emb_ms / 1e3) / 1e9
+    merge_gbs = merge_bytes / (merge_ms / 1e3) / 1e9
+    return {
+        "embedding": {"GB/s": emb_gbs, "frac": emb_gbs / hbm, "bytes_per_call": emb_bytes, "ms_per_call": emb_ms,
+                      "workload": e["name"], "timing": "one call as a graph, L2 flushed between replays"},
+        "merge": {"GB/s": merge_gbs, "frac": merge_gbs / hbm, "bytes_per_call": merge_bytes,
+                  "ms_per_call": merge_ms, "workload": m["name"],
+                  "timing": "one call as a graph, L2 flushed between replays"},
+    }
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup()
@@ -435,6 +490,7 @@ def main():
                                for p in layer.proj])
     deq_row_gbs = deq_bytes / (d_row_ms / 1e3) / 1e9
     q_row_gbs = q_bytes / (q_row_ms / 1e3) / 1e9
+    export_rows = measure_export_rows(dev, row_ms, hbm)
 
     e2e = None
     if not args.no_e2e:
@@ -515,6 +571,8 @@ def main():
                          "ms_per_step": q_row_ms,
                          "timing": "the 7 quantize calls as one graph, L2 flushed between replays",
                          "GB/s_in_step_events": q_gbs},
+            "embedding": export_rows["embedding"],
+            "merge": export_rows["merge"],
             "clocks": clocks,
             "e2e": e2e,
         }

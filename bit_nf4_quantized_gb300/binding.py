@@ -25,6 +25,7 @@ SCALE_LORA, SCALE_RSLORA = 0, 1
 ENTRY_POINTS = (
     "nf4_abi_version", "nf4_status_str", "nf4_num_blocks", "nf4_num_nested", "nf4_packed_bytes",
     "nf4_code_tables", "nf4_quantize_workspace_bytes", "nf4_quantize", "nf4_dequantize",
+    "nf4_embedding_rows", "nf4_merge_lora",
     "qlora_fwd_workspace_bytes", "qlora_bwd_workspace_bytes", "qlora_linear_fwd",
     "qlora_linear_bwd", "qlora_last_device_status", "nf4_kernel_launch_count",
 )
@@ -72,6 +73,8 @@ def load() -> ctypes.CDLL:
         "nf4_quantize": (i32, [vp, i32, i64, tp, vp, sz, vp]),
         "nf4_dequantize": (i32, [tp, vp, i32, vp]),
         "nf4_quantize_noalloc": (i32, [vp, i32, i64, tp, vp]),
+        "nf4_embedding_rows": (i32, [tp, i64, i64, vp, i64, vp, i32, vp]),
+        "nf4_merge_lora": (i32, [i64, i64, i32, f32, i32, tp, vp, vp, vp, i32, vp]),
         "qlora_fwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "qlora_bwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
         "qlora_linear_fwd": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, tp, vp, vp, vp, vp, vp, sz, vp]),
@@ -212,6 +215,37 @@ def nf4_dequantize(q: Nf4Tensor, dtype=torch.float32, out: torch.Tensor = None, 
     cs = q.c_struct()
     _check(lib.nf4_dequantize(ctypes.byref(cs), _ptr(y), _dtype_code(y.dtype), _stream(stream)),
            "nf4_dequantize")
+    return y
+
+
+def nf4_embedding_rows(E: Nf4Tensor, ids: torch.Tensor, dtype=torch.float32, out: torch.Tensor = None,
+                       stream=None) -> torch.Tensor:
+    """Rows ``ids`` (device int64) of the NF4 table E [rows, dim], decoded: [len(ids), dim].
+
+    An id outside [0, rows) yields a zero row and sets the device status word
+    (read it with ``device_status``).
+    """
+    lib = load()
+    rows, dim = E.shape
+    ids = ids.contiguous()
+    n = ids.numel()
+    y = out if out is not None else torch.empty((n, dim), dtype=dtype, device=E.packed.device)
+    cs = E.c_struct()
+    _check(lib.nf4_embedding_rows(ctypes.byref(cs), rows, dim, _ptr(ids) if n else None, n, _ptr(y),
+                                  _dtype_code(y.dtype), _stream(stream)), "nf4_embedding_rows")
+    return y
+
+
+def nf4_merge_lora(W: Nf4Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float, mode: int = SCALE_LORA,
+                   dtype=torch.float32, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Merged weight deq(W) + s B A ([N, K], fp32 or bf16) of an NF4 base W [N, K] and an adapter."""
+    lib = load()
+    N, K = W.shape
+    r = A.shape[0]
+    y = out if out is not None else torch.empty((N, K), dtype=dtype, device=W.packed.device)
+    cs = W.c_struct()
+    _check(lib.nf4_merge_lora(N, K, r, ctypes.c_float(alpha), mode, ctypes.byref(cs), _ptr(A), _ptr(B),
+                              _ptr(y), _dtype_code(y.dtype), _stream(stream)), "nf4_merge_lora")
     return y
 
 

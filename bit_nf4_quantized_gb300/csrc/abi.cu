@@ -345,6 +345,41 @@ nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, voi
   return from_cuda(launch_dequantize(view_of(w), y, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+nf4_status nf4_embedding_rows(const nf4_tensor* E, int64_t rows, int64_t dim, const int64_t* ids,
+                              int64_t n_ids, void* out, nf4_dtype out_dtype, void* stream) {
+  if (E == nullptr || rows <= 0 || dim <= 0 || n_ids < 0) return NF4_ERR_ARG;
+  if (out_dtype != NF4_F32 && out_dtype != NF4_BF16) return NF4_ERR_DTYPE;
+  if (rows > (int64_t(1) << 40) / dim) return NF4_ERR_SHAPE;
+  nf4_status st = check_tensor(E, rows * dim);
+  if (st != NF4_OK) return st;
+  if (n_ids == 0) return NF4_OK;
+  if (ids == nullptr || out == nullptr) return NF4_ERR_ARG;
+  if (n_ids > (int64_t(1) << 40) / dim) return NF4_ERR_SHAPE;
+  if (!aligned16(ids) || !aligned16(out)) return NF4_ERR_ALIGN;
+  int* status = nullptr;
+  if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+  KernelTimer timer(NF4_TIME_EMBEDDING, static_cast<cudaStream_t>(stream));
+  return from_cuda(launch_embedding_rows(view_of(E), rows, dim, ids, n_ids, out, out_dtype, status,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+nf4_status nf4_merge_lora(int64_t N, int64_t K, int32_t rank, float alpha, qlora_scale_mode mode,
+                          const nf4_tensor* W, const float* A, const float* B, void* out,
+                          nf4_dtype out_dtype, void* stream) {
+  float s = 0.0f;
+  // the scale rules of the linear; the dtype here is the output's
+  if (out_dtype != NF4_F32 && out_dtype != NF4_BF16) return NF4_ERR_DTYPE;
+  nf4_status st = check_linear(0, N, K, rank, alpha, mode, NF4_F32, &s);
+  if (st != NF4_OK) return st;
+  if (K % 8 != 0) return NF4_ERR_SHAPE;
+  if (W == nullptr || A == nullptr || B == nullptr || out == nullptr) return NF4_ERR_ARG;
+  if ((st = check_tensor(W, N * K)) != NF4_OK) return st;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return NF4_ERR_ALIGN;
+  KernelTimer timer(NF4_TIME_MERGE, static_cast<cudaStream_t>(stream));
+  return from_cuda(launch_merge_lora(view_of(W), N, K, rank, s, A, B, out, out_dtype,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 size_t qlora_fwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
   if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256) return 0;
   return fwd_ws(M, N, K, rank, compute);

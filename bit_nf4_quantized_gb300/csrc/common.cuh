@@ -148,6 +148,12 @@ struct PrepJobs;
 cudaError_t launch_decode_with_prep(const Nf4View& w, __nv_bfloat16* y, const PrepJobs& jobs, unsigned prep_ctas,
                                     cudaStream_t st);
 
+// ---- export.cu: selected embedding rows and the merged LoRA weight ------------
+cudaError_t launch_embedding_rows(const Nf4View& w, int64_t rows, int64_t dim, const int64_t* ids, int64_t n_ids,
+                                  void* out, nf4_dtype od, int* status, cudaStream_t st);
+cudaError_t launch_merge_lora(const Nf4View& w, int64_t N, int64_t K, int r, float s, const float* A,
+                              const float* B, void* out, nf4_dtype od, cudaStream_t st);
+
 // ---- linear_simt.cu (fp32 profile; adapter reductions for both profiles) -------
 struct LinearArgs {
   int64_t M, N, K;

@@ -47,4 +47,22 @@ __device__ __forceinline__ void decode8(uint32_t w, const uint32_t (&L)[4], cons
   }
 }
 
+// Output staging in shared memory: 16-byte slot g of a warp's buffer, rows of 8 slots
+// XOR-swizzled by row, so that a warp writing each lane's consecutive slots and a warp
+// reading slots 32j + lane both touch all 32 banks once per 8 lanes.
+__device__ __forceinline__ uint32_t stage_slot(uint32_t g) {
+  const uint32_t row = g >> 3, col = g & 7;
+  return ((row << 3) | (col ^ (row & 7))) << 4;
+}
+
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
 }  // namespace qnf4

@@ -300,12 +300,6 @@ constexpr int kDeqChunks = 2;                       // chunks per warp, loads is
 constexpr int kDeqPerCta = (kDeqThreads / 32) * kDeqChunks * 1024;
 static_assert(kDeqThreads == kPrepThreads, "prep jobs run in CTAs of the decode launch");
 
-// 16-byte slot g of a warp's staging buffer, rows of 8 slots XOR-swizzled by row.
-__device__ __forceinline__ uint32_t stage_slot(uint32_t g) {
-  const uint32_t row = g >> 3, col = g & 7;
-  return ((row << 3) | (col ^ (row & 7))) << 4;
-}
-
 // One CTA's share of the decode: block `cta` of the dequantize grid.
 template <typename Tout, bool kDQ>
 __device__ __forceinline__ void decode_cta(const Nf4View& w, Tout* __restrict__ y, const DecodeTables& tabs,

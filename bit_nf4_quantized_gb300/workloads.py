@@ -42,6 +42,14 @@ W4 = dict(name="Llama-3-8B-shaped matrices, forward, M in {1,2,4,8,16}, r=8, alp
 W5 = dict(name="1-D NF4 double-quant sweep", sizes=tuple(2 ** e for e in (20, 22, 24, 26, 28, 30)) +
           (2 ** 20 + 7 * 16384,), std=0.02, outlier_frac=0.001, outlier_mult=50.0)
 
+# Workload 6: selected rows of a Llama-3-8B-shaped NF4 embedding table.
+W6 = dict(name="NF4 double-quant embedding 128256 x 4096, 4096 token ids, bf16 rows",
+          rows=128256, dim=4096, n_ids=4096)
+
+# Workload 7: merged deployment weight of the gate projection.
+W7 = dict(name="merged fp32 weight of a 14336 x 4096 NF4 double-quant base, r=16, alpha=16",
+          N=14336, K=4096, r=16, alpha=16.0)
+
 
 def seed_for(workload: int, tensor_id: int) -> int:
     return BASE_SEED + 1000 * workload + tensor_id
@@ -96,3 +104,23 @@ def device_student_t(shape, df, scale, seed, device, dtype):
     for _ in range(df):
         chi2 += torch.randn(shape, generator=g, device=device) ** 2
     return (z0 / torch.sqrt(chi2 / df) * scale).to(dtype)
+
+
+def random_nf4_parts(n_packed, n_blocks, n_nested, double_quant, workload, tensor_id) -> dict:
+    """Random stored bytes of an NF4 tensor, sized by the caller: any byte pattern is a
+    valid stored tensor.  packed: uniform bytes; with double quantization absmax holds
+    uniform uint8 codes, nested U(0.01, 0.05) float32 and offset 0.03; without it absmax
+    is |N(0, 0.05)| + 0.001 float32."""
+    g = rng(workload, tensor_id)
+    packed = g.integers(0, 256, size=n_packed, dtype=np.uint8)
+    if double_quant:
+        return dict(packed=packed, absmax=g.integers(0, 256, size=n_blocks, dtype=np.uint8),
+                    nested=g.uniform(0.01, 0.05, size=n_nested).astype(np.float32),
+                    offset=np.float32(0.03))
+    return dict(packed=packed, absmax=(np.abs(g.standard_normal(n_blocks)) * 0.05 + 0.001).astype(np.float32),
+                nested=None, offset=None)
+
+
+def token_ids(n, rows, workload, tensor_id, dtype=np.int64) -> np.ndarray:
+    """n ids drawn uniformly from [0, rows)."""
+    return rng(workload, tensor_id).integers(0, rows, size=n).astype(dtype)

@@ -136,6 +136,32 @@ nf4_status nf4_quantize_noalloc(const void* x, nf4_dtype x_dtype, int64_t numel,
  * even ([ADAPT] "Fused GPU NF4 decodes inside the matrix kernel"). */
 nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream);
 
+/* Selected rows of an NF4-quantized embedding table ([ADAPT] "Packed NF4 and the portable
+ * QLoRA profile": embeddings decode only selected rows; "Fused GPU NF4 decodes inside the
+ * matrix kernel": selected-row embedding kernels decode on the device):
+ *     out[i][d] = deq(E)[ids[i]][d],  i < n_ids, d < dim
+ * E: an nf4_tensor of numel rows*dim holding [rows, dim] row-major.  ids: device int64
+ * [n_ids].  out: device [n_ids, dim] in out_dtype, the same bits nf4_dequantize writes for
+ * those elements.  Shapes and pointers are checked before any launch; an id outside
+ * [0, rows) is found on the device: its output row is written as zeros and the device
+ * status word is set to NF4_ERR_ARG (qlora_last_device_status). */
+nf4_status nf4_embedding_rows(const nf4_tensor* E, int64_t rows, int64_t dim, const int64_t* ids,
+                              int64_t n_ids, void* out, nf4_dtype out_dtype, void* stream);
+
+/* Merged deployment weight of an NF4 base and a LoRA adapter ([ADAPT] "Checkpoints,
+ * exact continuation and deployment": merged F32 deployment weights with the decoded NF4
+ * base, one matrix at a time):
+ *     W'[n][k] = deq(W)[n][k] + s * sum_j B[n][j] * A[j][k]
+ * W: nf4_tensor of numel N*K holding [N, K] row-major; A fp32 [rank, K], B fp32 [N, rank];
+ * s from alpha, rank and mode as for the linear (rank 1..256, rank <= min(N, K)).
+ * out: device [N, K] row-major, NF4_F32 or NF4_BF16.  fp32 arithmetic: the decoded value
+ * (exactly what nf4_dequantize writes for fp32), d = the rank-r dot product accumulated with
+ * fused multiply-adds in order j = 0, 1, ..., then w + s*d with two roundings; bf16 output
+ * rounds that fp32 value once (nearest even).  Needs K % 8 == 0 (NF4_ERR_SHAPE otherwise). */
+nf4_status nf4_merge_lora(int64_t N, int64_t K, int32_t rank, float alpha, qlora_scale_mode mode,
+                          const nf4_tensor* W, const float* A, const float* B, void* out,
+                          nf4_dtype out_dtype, void* stream);
+
 /* Workspace (device bytes) needed by qlora_linear_fwd / qlora_linear_bwd.  With
  * compute = NF4_BF16 it includes a bf16 copy of the decoded weight (2*N*K bytes): each
  * call decodes W once into it (the bits nf4_dequantize writes) before the contraction.
@@ -197,7 +223,9 @@ typedef enum {
   NF4_TIME_ADAPTER = 4,     /* adapter-side kernels (T, G, dA, dB) */
   NF4_TIME_WEIGHT_DECODE = 5, /* the bf16 profile's per-call decode of W before its GEMM,
                                * with the call's operand staging in the same launch */
-  NF4_TIME_KINDS = 6
+  NF4_TIME_EMBEDDING = 6,   /* nf4_embedding_rows */
+  NF4_TIME_MERGE = 7,       /* nf4_merge_lora */
+  NF4_TIME_KINDS = 8
 } nf4_timed_kernel;
 
 void nf4_timing_enable(int32_t on);

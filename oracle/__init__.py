@@ -25,9 +25,10 @@ Sources (the web pages this work follows):
           byte totals.
 
 Modules: ``codebooks`` (the two code tables), ``nf4`` (quantize / dequantize /
-byte formula), ``qlora`` (linear forward and backward in float64).  Every
+byte formula), ``qlora`` (linear forward and backward in float64), ``export``
+(selected embedding rows, merged LoRA weight).  Every
 function is pinned by ``tests/test_oracle_*.py`` against facts the pages or the
 mathematics fix; see each module header.
 """
 
-from . import codebooks, nf4, qlora  # noqa: F401
+from . import codebooks, export, nf4, qlora  # noqa: F401

@@ -111,6 +111,32 @@ def test_validation_refuses_bad_arguments(lib):
         4, 64, 128, 8, ctypes.c_float(16.0), 0, 1, p, p, p, ctypes.byref(w), p, p, p, p, p, ws, wsz, None)
     assert b(0) == binding.NF4_ERR_WORKSPACE
 
+    # selected embedding rows: E [100, 64]
+    e = _fake_tensor(100 * 64)
+    emb = lambda rows, dim, ids, n, out, od=0, et=e: lib.nf4_embedding_rows(  # noqa: E731
+        ctypes.byref(et) if et is not None else None, rows, dim, ids, n, out, od, None)
+    assert emb(100, 64, p, 4, p, et=None) == binding.NF4_ERR_ARG
+    assert emb(0, 64, p, 4, p) == binding.NF4_ERR_ARG
+    assert emb(100, 64, p, -1, p) == binding.NF4_ERR_ARG
+    assert emb(100, 64, p, 4, p, od=4) == binding.NF4_ERR_DTYPE
+    assert emb(100, 32, p, 4, p) == binding.NF4_ERR_CORRUPT          # numel != rows*dim
+    assert emb(100, 64, None, 0, None) == binding.NF4_OK             # no ids: nothing to do
+    assert emb(100, 64, None, 4, p) == binding.NF4_ERR_ARG
+    assert emb(100, 64, p, 4, ctypes.c_void_p(0x50000008)) == binding.NF4_ERR_ALIGN
+
+    # merged weight: W [64, 128]
+    m = lambda N, K, r, od=0, wt=w, a=p, alpha=16.0, mode=0: lib.nf4_merge_lora(  # noqa: E731
+        N, K, r, ctypes.c_float(alpha), mode, ctypes.byref(wt), a, p, p, od, None)
+    assert m(64, 128, 8, od=2) == binding.NF4_ERR_DTYPE
+    assert m(64, 128, 0) == binding.NF4_ERR_ARG
+    assert m(64, 128, 65) == binding.NF4_ERR_ARG
+    assert m(64, 128, 8, alpha=float("inf")) == binding.NF4_ERR_ARG
+    assert m(64, 128, 8, mode=3) == binding.NF4_ERR_ARG
+    assert m(64, 124, 8, wt=_fake_tensor(64 * 124)) == binding.NF4_ERR_SHAPE   # K % 8
+    assert m(64, 64, 8) == binding.NF4_ERR_CORRUPT                             # numel != N*K
+    assert m(64, 128, 8, a=ctypes.c_void_p(0x50000004)) == binding.NF4_ERR_ALIGN
+    assert m(64, 128, 8, a=None) == binding.NF4_ERR_ARG
+
 
 def test_status_strings(lib):
     for s in range(10):
