@@ -337,6 +337,29 @@ def random_stored_nf4(shape, seed, dev):
     return q
 
 
+def measure_no_double_quant(layer, row_ms):
+    """The gate projection's forward + backward with its double-quantized weight and with a
+    copy holding fp32 block maxima instead (same kernels, the plain scale); each timed as a
+    graph with L2 flushed between replays."""
+    from bit_nf4_quantized_gb300 import binding as bq
+    p = next(q for q in layer.proj if q["name"] == "gate_proj")
+    q_plain = bq.nf4_quantize(p["w"], double_quant=False)
+
+    def fwd_bwd(q):
+        bq.qlora_linear_fwd(p["x"], q, p["A"], p["B"], layer.alpha, y=p["y"], T=p["T"], workspace=layer.ws_f)
+        bq.qlora_linear_bwd(p["dy"], p["x"], p["T"], q, p["A"], p["B"], layer.alpha, dx=p["dx"], dA=p["dA"],
+                            dB=p["dB"], workspace=layer.ws_b)
+
+    flops = layer_flops([("gate_proj", p["N"], p["K"])], layer.M, layer.r)
+    ms_dq = row_ms(lambda: fwd_bwd(p["q"]))
+    ms_plain = row_ms(lambda: fwd_bwd(q_plain))
+    return {"shape": [p["N"], p["K"]], "tokens": layer.M,
+            "TFLOP/s_double_quant": flops / (ms_dq / 1e3) / 1e12,
+            "TFLOP/s_fp32_absmax": flops / (ms_plain / 1e3) / 1e12,
+            "ms_double_quant": ms_dq, "ms_fp32_absmax": ms_plain,
+            "timing": "fwd+bwd of one projection as a graph, L2 flushed between replays"}
+
+
 def measure_export_rows(dev, row_ms, hbm):
     """The selected-row embedding decode and the merged-weight export, each one call timed
     as a replayed graph with L2 flushed between replays; GB/s of algorithmic bytes."""
@@ -491,6 +514,7 @@ def main():
     deq_row_gbs = deq_bytes / (d_row_ms / 1e3) / 1e9
     q_row_gbs = q_bytes / (q_row_ms / 1e3) / 1e9
     export_rows = measure_export_rows(dev, row_ms, hbm)
+    no_dq = measure_no_double_quant(layer, row_ms)
 
     e2e = None
     if not args.no_e2e:
@@ -571,6 +595,7 @@ def main():
                          "ms_per_step": q_row_ms,
                          "timing": "the 7 quantize calls as one graph, L2 flushed between replays",
                          "GB/s_in_step_events": q_gbs},
+            "no_double_quant": no_dq,
             "embedding": export_rows["embedding"],
             "merge": export_rows["merge"],
             "clocks": clocks,

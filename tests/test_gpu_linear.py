@@ -21,23 +21,24 @@ DEV = "cuda"
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
-def _quantized_weight(N, K, seed, dist="normal"):
+def _quantized_weight(N, K, seed, dist="normal", dq=True):
     if dist == "t":
         w = wl.student_t((N, K), 5, 0.02, 3, seed)
     else:
         w = wl.normal((N, K), 0.02, 2, seed)
-    ref = onf4.quantize(w, double_quant=True)
-    q = binding.Nf4Tensor.empty((N, K), True, DEV)
+    ref = onf4.quantize(w, double_quant=dq)
+    q = binding.Nf4Tensor.empty((N, K), dq, DEV)
     q.packed.copy_(torch.from_numpy(ref["packed"]))
     q.absmax.copy_(torch.from_numpy(ref["absmax"]))
-    q.nested_absmax.copy_(torch.from_numpy(ref["nested"]))
-    q.offset[0] = float(ref["offset"])
+    if dq:
+        q.nested_absmax.copy_(torch.from_numpy(ref["nested"]))
+        q.offset[0] = float(ref["offset"])
     return q, onf4.dequantize(ref, "f32").reshape(N, K)
 
 
-def _run_case(M, N, K, r, alpha, compute, mode=binding.SCALE_LORA, seed=0, dist="normal", rows=None):
+def _run_case(M, N, K, r, alpha, compute, mode=binding.SCALE_LORA, seed=0, dist="normal", rows=None, dq=True):
     tdt = torch.float32 if compute == "f32" else torch.bfloat16
-    q, w_deq = _quantized_weight(N, K, seed, dist)
+    q, w_deq = _quantized_weight(N, K, seed, dist, dq)
     x = wl.normal((M, K), 1.0, 1, seed + 1)
     dy = wl.normal((M, N), 1.0, 1, seed + 2)
     A, B = wl.adapters(N, K, r, 1, seed + 3)
@@ -83,6 +84,15 @@ def test_bf16_small_m(lib, M):
                                      (511, 1032, 640, 64), (129, 136, 128, 128)])
 def test_bf16_tiles_and_tails(lib, M, N, K, r):
     _run_case(M, N, K, r, 16.0, "bf16", seed=N)
+
+
+@pytest.mark.parametrize("compute", ["bf16", "f32"])
+@pytest.mark.parametrize("M,N,K,r", [(130, 200, 192, 5), (512, 1536, 576, 16)])
+def test_weight_without_double_quant(lib, compute, M, N, K, r):
+    """fp32 block maxima instead of dynamic8 codes: the same kernels with the plain scale."""
+    if compute == "f32" and (N, K) == (1536, 576):
+        M = 64
+    _run_case(M, N, K, r, 16.0, compute, seed=41, dq=False)
 
 
 def test_bf16_rslora_scale(lib):
