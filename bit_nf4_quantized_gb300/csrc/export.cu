@@ -6,6 +6,8 @@
 //     continuation and deployment": merged F32 deployment weights with the decoded base).
 // Both decode with the arithmetic of nf4_dequantize: a' = dyn8[code] * nested + offset
 // (two roundings) or the fp32 absmax, w = nf4[q] * a'.
+#include <atomic>
+
 #include "common.cuh"
 #include "decode.cuh"
 
@@ -14,11 +16,45 @@ namespace {
 
 constexpr int kThreads = 256;
 
+constexpr int kMaxDevices = 64;
+
+// Per-device launch facts, looked up once (a racing first lookup stores the same value).
 int device_sms() {
-  int dev = 0, n = 0;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
   cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  n = n > 0 ? n : 1;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Resident CTAs per SM of `kernel` at kThreads threads (kind 0/1 selects the cache slot).
+template <typename K>
+cudaError_t resident_per_sm(K kernel, int kind, int* out) {
+  static std::atomic<int> cache[kMaxDevices][2];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  if (slot) {
+    const int c = cache[dev][kind].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return cudaSuccess;
+    }
+  }
+  int n = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0);
+  if (e != cudaSuccess) return e;
+  n = n > 0 ? n : 1;
+  if (slot) cache[dev][kind].store(n, std::memory_order_relaxed);
+  *out = n;
+  return cudaSuccess;
 }
 
 struct Decoder {
@@ -384,11 +420,10 @@ cudaError_t launch_embedding_rows(const Nf4View& w, int64_t rows, int64_t dim, c
   if (dim % 32 == 0) {
     // one warp per row; no more CTAs than are resident at once
     int per_sm = 0;
-    e = od == NF4_F32 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nf4_embed_rows32<float>, kThreads, 0)
-                      : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nf4_embed_rows32<__nv_bfloat16>,
-                                                                      kThreads, 0);
+    e = od == NF4_F32 ? resident_per_sm(nf4_embed_rows32<float>, 0, &per_sm)
+                      : resident_per_sm(nf4_embed_rows32<__nv_bfloat16>, 1, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t ctas_max = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * device_sms();
+    const int64_t ctas_max = static_cast<int64_t>(per_sm) * device_sms();
     const int64_t need = (n_ids + kThreads / 32 - 1) / (kThreads / 32);
     const dim3 grid(static_cast<unsigned>(need < ctas_max ? need : ctas_max));
     e = od == NF4_F32 ? launch_pdl(nf4_embed_rows32<float>, grid, dim3(kThreads), 0, st, 1, w, rows, dim, ids, n_ids,

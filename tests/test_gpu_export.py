@@ -163,7 +163,10 @@ def _s32(alpha, r, mode):
     return float(np.float32(float(alpha) / np.sqrt(float(r))))
 
 
-MERGE_CASES = [(64, 256, 16), (200, 520, 17), (7, 8, 1), (130, 264, 64), (300, 512, 256), (72, 1024, 5)]
+# (8, 80000, 4): 313 column tiles, more than the resident CTAs, so a CTA's tiles change
+# column range and A is restaged per tile
+MERGE_CASES = [(64, 256, 16), (200, 520, 17), (7, 8, 1), (130, 264, 64), (300, 512, 256), (72, 1024, 5),
+               (8, 80000, 4)]
 
 
 @pytest.mark.parametrize("N,K,r", MERGE_CASES)
