@@ -78,6 +78,7 @@ __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // ---- selected embedding rows --------------------------------------------------------
+// Rows whose width is not a multiple of 32.
 // CTA (chunk, rows i0 .. i0 + 8): thread t covers dims chunk*2048 + 8t .. +8 of each of the
 // 8 rows.  When dim % 8 == 0 every thread's 8 elements lie in one 64-block and its output
 // is 16-byte aligned: all 8 rows' ids, then all their code words and scales, are loaded
