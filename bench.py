@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--only", default=None,
                    help="restrict the step to one projection (for profiling; not a bench line)")
+    p.add_argument("--sweep", action="store_true",
+                   help="time the other workloads (small-M forward, SmolLM2 stack, 1-D quantize and "
+                        "dequantize sizes) and print one JSON line each; not the bench line")
     return p.parse_args()
 
 
@@ -400,11 +403,144 @@ def measure_export_rows(dev, row_ms, hbm):
     }
 
 
+def graph_ms(fn, dev, stream, flush, reps=10):
+    """Median milliseconds of `fn` captured as one CUDA graph and replayed, with L2 flushed
+    (a 256 MB write) before every replay, outside the timed interval."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def sweep(dev, stream):
+    """The workloads besides the bench line, timed through the C ABI (one JSON line each):
+    the small-M forward of the Llama-3-8B-shaped matrices (GB/s of the bytes a forward must
+    move: stored weight, fp32 adapters, activations), the SmolLM2-shaped 30-layer QLoRA stack
+    (TFLOP/s) and the 1-D quantize / dequantize sizes (GB/s)."""
+    import torch
+    from bit_nf4_quantized_gb300 import binding as bq
+    from bit_nf4_quantized_gb300 import workloads as wl
+    lib = bq.load()
+    pk, pk_src = peaks()
+    hbm, tc = float(pk["hbm_gbs"]), float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+
+    def emit(d):
+        d["peaks"] = pk_src
+        print(json.dumps(d), flush=True)
+
+    # small-M forward, all 7 projections of one layer per timed graph
+    c = wl.W4
+    r, Ms = c["r"], c["Ms"]
+    mmax = max(Ms)
+    ws = torch.empty(max(16, max(lib.qlora_fwd_workspace_bytes(m, N, K, r, 1) for m in Ms for _, N, K in c["shapes"])),
+                     dtype=torch.uint8, device=dev)
+    projs = []
+    for i, (_, N, K) in enumerate(c["shapes"]):
+        seed = wl.seed_for(4, 100 * i)
+        q = bq.nf4_quantize(wl.device_student_t((N, K), 5, 0.02, seed, dev, torch.bfloat16), True)
+        projs.append(dict(N=N, K=K, q=q,
+                          A=wl.device_normal((r, K), 1.0 / r, seed + 3, dev, torch.float32),
+                          B=wl.device_normal((N, r), 0.01, seed + 4, dev, torch.float32),
+                          x=wl.device_normal((mmax, K), 1.0, seed + 1, dev, torch.bfloat16),
+                          y=torch.empty((mmax, N), dtype=torch.bfloat16, device=dev),
+                          T=torch.empty((mmax, r), dtype=torch.float32, device=dev)))
+    for m in Ms:
+        def fwd(m=m):
+            for p in projs:
+                bq.qlora_linear_fwd(p["x"][:m], p["q"], p["A"], p["B"], c["alpha"], y=p["y"][:m], T=p["T"][:m],
+                                    workspace=ws)
+        ms = graph_ms(fwd, dev, stream, flush)
+        nbytes = sum(lib.nf4_packed_bytes(p["N"] * p["K"], 1) + 4 * r * (p["N"] + p["K"]) + 2 * m * (p["N"] + p["K"])
+                     for p in projs)
+        emit({"sweep": "small-M forward, 7 Llama-3-8B-shaped projections", "tokens": m, "rank": r,
+              "ms_per_layer": ms, "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm,
+              "bytes_per_layer": nbytes})
+    del projs, ws
+
+    # SmolLM2-shaped stack: QLoRA forward + backward on q and v of 30 layers
+    c = wl.W2
+    M, r, alpha = c["M"], c["r"], c["alpha"]
+    targets = [(n, N, K) for n, N, K in c["shapes"] if n in c["targets"]]
+    wsf = torch.empty(max(16, max(lib.qlora_fwd_workspace_bytes(M, N, K, r, 1) for _, N, K in targets)),
+                      dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(16, max(lib.qlora_bwd_workspace_bytes(M, N, K, r, 1) for _, N, K in targets)),
+                      dtype=torch.uint8, device=dev)
+    bufs = {}
+    for j, (_, N, K) in enumerate(targets):
+        seed = wl.seed_for(2, 10 * j)
+        bufs[(N, K)] = dict(x=wl.device_normal((M, K), 1.0, seed + 1, dev, torch.bfloat16),
+                            dy=wl.device_normal((M, N), 1.0, seed + 2, dev, torch.bfloat16),
+                            y=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                            T=torch.empty((M, r), dtype=torch.float32, device=dev),
+                            dx=torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                            dA=torch.empty((r, K), dtype=torch.float32, device=dev),
+                            dB=torch.empty((N, r), dtype=torch.float32, device=dev))
+    mats = []
+    for layer in range(c["layers"]):
+        for j, (_, N, K) in enumerate(targets):
+            seed = wl.seed_for(2, 1000 + 10 * (layer * len(targets) + j))
+            mats.append(dict(N=N, K=K, q=bq.nf4_quantize(wl.device_normal((N, K), 0.02, seed, dev, torch.bfloat16), True),
+                             A=wl.device_normal((r, K), 1.0 / r, seed + 3, dev, torch.float32),
+                             B=wl.device_normal((N, r), 0.01, seed + 4, dev, torch.float32)))
+
+    def stack():
+        for p in mats:
+            b = bufs[(p["N"], p["K"])]
+            bq.qlora_linear_fwd(b["x"], p["q"], p["A"], p["B"], alpha, y=b["y"], T=b["T"], workspace=wsf)
+            bq.qlora_linear_bwd(b["dy"], b["x"], b["T"], p["q"], p["A"], p["B"], alpha, dx=b["dx"], dA=b["dA"],
+                                dB=b["dB"], workspace=wsb)
+    ms = graph_ms(stack, dev, stream, flush)
+    flops = sum(linear_flops(M, p["N"], p["K"], r) for p in mats)
+    emit({"sweep": "SmolLM2-shaped stack, QLoRA q and v of 30 layers, fwd+bwd", "tokens": M, "rank": r,
+          "ms_per_step": ms, "TFLOP/s": flops / ms / 1e9, "frac_bf16_burst": flops / ms / 1e9 / tc,
+          "flops_per_step": flops})
+    del mats, bufs, wsf, wsb
+
+    # 1-D quantize (fp32 input) and dequantize (fp32 output)
+    for n in wl.W5["sizes"]:
+        x = wl.device_normal((n,), wl.W5["std"], wl.seed_for(5, 1), dev, torch.float32)
+        q = bq.Nf4Tensor.empty((n,), True, dev)
+        wsq = torch.empty(max(16, lib.nf4_quantize_workspace_bytes(n, 1)), dtype=torch.uint8, device=dev)
+        y = torch.empty(n, dtype=torch.float32, device=dev)
+        q_ms = graph_ms(lambda: bq.nf4_quantize(x, True, out=q, workspace=wsq), dev, stream, flush, reps=5)
+        d_ms = graph_ms(lambda: bq.nf4_dequantize(q, out=y), dev, stream, flush, reps=5)
+        stored = lib.nf4_packed_bytes(n, 1)
+        emit({"sweep": "1-D NF4 double quant, fp32", "numel": n,
+              "quantize_GB/s": (4 * n + stored + 4) / q_ms / 1e6, "dequantize_GB/s": (stored + 4 * n) / d_ms / 1e6,
+              "quantize_frac_hbm": (4 * n + stored + 4) / q_ms / 1e6 / hbm,
+              "dequantize_frac_hbm": (stored + 4 * n) / d_ms / 1e6 / hbm, "quantize_ms": q_ms, "dequantize_ms": d_ms})
+        del x, q, wsq, y
+    if bq.device_status() != bq.NF4_OK:
+        raise RuntimeError("device status word set during the sweep")
+    return 0
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup()
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if args.sweep:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        return sweep(dev, torch.cuda.current_stream(dev)) if rank == 0 else 0
 
     # the oracle sample runs before the first CUDA call in this process
     cpu = None
