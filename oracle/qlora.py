@@ -90,6 +90,37 @@ def adapter_backward(dy, x, A, B, s: float, compute: str = "bf16"):
     return s * (G.T @ x64), s * (dy64.T @ T), G
 
 
+def forward_magnitudes(x, W, A, B, s: float, compute: str = "bf16"):
+    """Sums of the absolute values of the terms of each output of ``forward``, in float64.
+
+    Returns dict(y_base = |x| |W|^T (the terms x[m,k] W[n,k] of y), y_slab = |s| |T| |B|^T
+    (the terms s T[m,j] B[n,j]), T = |x| |A|^T (the terms of T)), on the same rounded
+    operands as ``forward``.  A rounding error of relative size u in every term of a sum
+    moves that sum by at most u times these magnitudes, which is what element-wise error
+    bounds are built from.
+    """
+    x64, W64, A64, B64 = _operands(compute, x, W, A, B)
+    T_abs = np.abs(x64 @ A64.T)
+    ax, aW, aA, aB = (np.abs(t) for t in (x64, W64, A64, B64))
+    return dict(y_base=ax @ aW.T, y_slab=abs(s) * (T_abs @ aB.T), T=ax @ aA.T)
+
+
+def backward_magnitudes(dy, x, W, A, B, s: float, compute: str = "bf16"):
+    """Sums of |terms| of each output of ``backward`` (float64), as ``forward_magnitudes``:
+    dX_base = |dY| |W|, dX_slab = |s| |G| |A|, G = |dY| |B|, dA = |s| |G|^T |x|,
+    dB = |s| |dY|^T |T| with G = dY B and T = x A^T on the rounded operands.  With W = None
+    the two dX entries are left out (the adapter gradients alone, no M x N x K product)."""
+    dy64, x64, A64, B64 = _operands(compute, dy, x, A, B)
+    G_abs = np.abs(dy64 @ B64)
+    T_abs = np.abs(x64 @ A64.T)
+    ady, ax, aA, aB = (np.abs(t) for t in (dy64, x64, A64, B64))
+    out = dict(dX_slab=abs(s) * (G_abs @ aA), G=ady @ aB,
+               dA=abs(s) * (G_abs.T @ ax), dB=abs(s) * (ady.T @ T_abs))
+    if W is not None:
+        out["dX_base"] = ady @ np.abs(_operands(compute, W)[0])
+    return out
+
+
 def rel_frobenius(got, want) -> float:
     """||got - want||_F / ||want||_F (0 when both are zero)."""
     got = np.asarray(got, dtype=np.float64)
@@ -99,6 +130,18 @@ def rel_frobenius(got, want) -> float:
     if den == 0.0:
         return 0.0 if num == 0.0 else math.inf
     return float(num / den)
+
+
+def tile_rel_frobenius(got, want, tile: int = 256) -> float:
+    """Largest ``rel_frobenius`` over the tile x tile blocks of two 2-D arrays (ragged edge
+    blocks included).  A block whose reference is all zero counts only if ``got`` differs."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    worst = 0.0
+    for i in range(0, want.shape[0], tile):
+        for j in range(0, want.shape[1], tile):
+            worst = max(worst, rel_frobenius(got[i:i + tile, j:j + tile], want[i:i + tile, j:j + tile]))
+    return worst
 
 
 def linear_flops(M: int, N: int, K: int, r: int) -> int:

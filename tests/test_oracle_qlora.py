@@ -116,5 +116,97 @@ def test_bf16_profile_rounds_operands():
     y, _ = qlora.forward(x, W, A, B, 1.0, compute="bf16")
     xr, Wr, Ar, Br = (nf4.round_bf16(t).astype(np.float64) for t in (x, W, A, B))
     assert np.allclose(y, xr @ Wr.T + (xr @ Ar.T) @ Br.T, rtol=1e-13, atol=1e-13)
-    assert qlora.rel_frobenius(y, y) == 0.0
-    assert qlora.linear_flops(2, 3, 4, 1) == 4 * 24 + 6 * 2 * 7
+
+
+def test_rel_frobenius_hand_values():
+    # got - want = [3, -1]: sqrt(10) over ||want|| = 5
+    assert qlora.rel_frobenius([3.0, 4.0], [0.0, 5.0]) == math.sqrt(10.0) / 5.0
+    # one wrong entry of a 2 x 2: |0.5| / sqrt(1 + 4 + 9 + 16)
+    assert math.isclose(qlora.rel_frobenius([[1.0, 2.0], [3.0, 4.5]], [[1.0, 2.0], [3.0, 4.0]]),
+                        0.5 / math.sqrt(30.0), rel_tol=1e-15)
+    # not squared: scaling the error by 10 scales the result by 10
+    assert math.isclose(qlora.rel_frobenius([0.0, 50.0], [0.0, 5.0]), 9.0, rel_tol=1e-15)
+    assert qlora.rel_frobenius([0.0, 0.0], [0.0, 0.0]) == 0.0
+    assert qlora.rel_frobenius([1e-30, 0.0], [0.0, 0.0]) == math.inf
+
+
+def test_tile_rel_frobenius_finds_one_bad_tile():
+    want = np.ones((512, 384))
+    got = want.copy()
+    got[256:, 256:] *= 1.1          # the ragged corner block (256 x 128) is 10 % off
+    assert math.isclose(qlora.tile_rel_frobenius(got, want, 256), 0.1, rel_tol=1e-12)
+    # the whole-array norm dilutes it: one block of 6 (1/6 of the entries)
+    assert math.isclose(qlora.rel_frobenius(got, want), 0.1 * math.sqrt(256 * 128 / (512 * 384)), rel_tol=1e-12)
+    assert qlora.tile_rel_frobenius(want, want) == 0.0
+
+
+def _count_loop_flops(M, N, K, r):
+    """Multiply-adds of the six products of one forward + backward, counted one by one in
+    plain loops (T, x W^T, s T B^T, G, dY W, s G A, dA, dB); 2 flops each."""
+    macs = 0
+    for _m in range(M):                     # T = x A^T and y = x W^T + s T B^T
+        for _j in range(r):
+            macs += K
+        for _n in range(N):
+            macs += K + r
+    for _m in range(M):                     # G = dY B and dX = dY W + s G A
+        for _j in range(r):
+            macs += N
+        for _k in range(K):
+            macs += N + r
+    for _j in range(r):                     # dA = s G^T x
+        for _k in range(K):
+            macs += M
+    for _n in range(N):                     # dB = s dY^T T
+        for _j in range(r):
+            macs += M
+    return 2 * macs
+
+
+def test_linear_flops_hand_count():
+    for shape in ((2, 3, 4, 1), (3, 5, 7, 2), (4, 8, 6, 3)):
+        assert qlora.linear_flops(*shape) == _count_loop_flops(*shape)
+    # one Llama-3-8B-shaped projection (q_proj, 4096 x 4096) at 4096 tokens and rank 16, by hand:
+    # 2 x 2 * 4096^3 for y and dX, plus 6 adapter products of 2 * 4096 * 4096 * 16 each
+    assert qlora.linear_flops(4096, 4096, 4096, 16) == 274_877_906_944 + 6 * 536_870_912
+    assert qlora.linear_flops(4096, 4096, 4096, 16) == 278_099_132_416
+
+
+def test_magnitudes_hand_case():
+    # x = [1, -2], W = [3, 4], A = [1, -1], B = [2], s = 0.5:
+    # T = 1 + 2 = 3; y = 3 - 8 + 0.5 * 3 * 2 = -2; |terms| of y: 3 + 8 (base), 3 (slab)
+    x, W, A, B = np.array([[1.0, -2.0]]), np.array([[3.0, 4.0]]), np.array([[1.0, -1.0]]), np.array([[2.0]])
+    y, T = qlora.forward(x, W, A, B, 0.5, compute="f64")
+    mag = qlora.forward_magnitudes(x, W, A, B, 0.5, compute="f64")
+    assert y[0, 0] == -2.0 and T[0, 0] == 3.0
+    assert mag["y_base"][0, 0] == 11.0 and mag["y_slab"][0, 0] == 3.0 and mag["T"][0, 0] == 3.0
+    # backward with dY = [1]: G = 2; dX = [3, 4] + 0.5 * 2 * [1, -1] = [4, 3];
+    # dA = 0.5 * 2 * [1, -2]; dB = 0.5 * 1 * 3
+    dX, dA, dB, G = qlora.backward(np.array([[1.0]]), x, W, A, B, 0.5, compute="f64")
+    bm = qlora.backward_magnitudes(np.array([[1.0]]), x, W, A, B, 0.5, compute="f64")
+    assert dX.tolist() == [[4.0, 3.0]] and dA.tolist() == [[1.0, -2.0]] and dB.tolist() == [[1.5]]
+    assert bm["dX_base"].tolist() == [[3.0, 4.0]] and bm["dX_slab"].tolist() == [[1.0, 1.0]]
+    assert bm["dA"].tolist() == [[1.0, 2.0]] and bm["dB"].tolist() == [[1.5]] and bm["G"].tolist() == [[2.0]]
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_magnitudes_bound_and_equal_on_nonnegative_operands(seed):
+    x, W, A, B, dy = _tiny(seed)
+    s = 1.3
+    # every term non-negative: the sums of |terms| are the outputs themselves
+    ax, aW, aA, aB, ady = (np.abs(t) for t in (x, W, A, B, dy))
+    y, T = qlora.forward(ax, aW, aA, aB, s, compute="f64")
+    m = qlora.forward_magnitudes(ax, aW, aA, aB, s, compute="f64")
+    assert np.allclose(m["y_base"] + m["y_slab"], y, rtol=1e-14) and np.allclose(m["T"], T, rtol=1e-14)
+    dX, dA, dB, G = qlora.backward(ady, ax, aW, aA, aB, s, compute="f64")
+    bm = qlora.backward_magnitudes(ady, ax, aW, aA, aB, s, compute="f64")
+    for got, want in ((bm["dX_base"] + bm["dX_slab"], dX), (bm["dA"], dA), (bm["dB"], dB), (bm["G"], G)):
+        assert np.allclose(got, want, rtol=1e-14)
+    # signed operands: each output is bounded by its magnitude (triangle inequality)
+    y, T = qlora.forward(x, W, A, B, -s, compute="f64")
+    m = qlora.forward_magnitudes(x, W, A, B, -s, compute="f64")
+    assert np.all(np.abs(y) <= m["y_base"] + m["y_slab"] + 1e-12) and np.all(np.abs(T) <= m["T"] + 1e-12)
+    dX, dA, dB, G = qlora.backward(dy, x, W, A, B, -s, compute="f64")
+    bm = qlora.backward_magnitudes(dy, x, W, A, B, -s, compute="f64")
+    assert np.all(np.abs(dX) <= bm["dX_base"] + bm["dX_slab"] + 1e-12)
+    assert np.all(np.abs(dA) <= bm["dA"] + 1e-12) and np.all(np.abs(dB) <= bm["dB"] + 1e-12)
