@@ -442,12 +442,15 @@ def sweep(dev, stream):
         d["peaks"] = pk_src
         print(json.dumps(d), flush=True)
 
-    # small-M forward, all 7 projections of one layer per timed graph
+    # small-M forward of the 7 projections of one layer: the batched call (one T launch and one
+    # weight pass for the whole layer) and the 7 single calls, each as one timed graph
     c = wl.W4
     r, Ms = c["r"], c["Ms"]
     mmax = max(Ms)
-    ws = torch.empty(max(16, max(lib.qlora_fwd_workspace_bytes(m, N, K, r, 1) for m in Ms for _, N, K in c["shapes"])),
-                     dtype=torch.uint8, device=dev)
+    shapes = [(N, K) for _, N, K in c["shapes"]]
+    need = max(max(max(lib.qlora_fwd_workspace_bytes(m, N, K, r, 1) for N, K in shapes),
+                   bq.qlora_fwd_batch_workspace_bytes(m, shapes, r)) for m in Ms)
+    ws = torch.empty(max(16, need), dtype=torch.uint8, device=dev)
     projs = []
     for i, (_, N, K) in enumerate(c["shapes"]):
         seed = wl.seed_for(4, 100 * i)
@@ -458,17 +461,26 @@ def sweep(dev, stream):
                           x=wl.device_normal((mmax, K), 1.0, seed + 1, dev, torch.bfloat16),
                           y=torch.empty((mmax, N), dtype=torch.bfloat16, device=dev),
                           T=torch.empty((mmax, r), dtype=torch.float32, device=dev)))
+    weight_bytes = sum(lib.nf4_packed_bytes(p["N"] * p["K"], 1) for p in projs)
     for m in Ms:
-        def fwd(m=m):
+        items = [dict(x=p["x"][:m], W=p["q"], A=p["A"], B=p["B"], alpha=c["alpha"], y=p["y"][:m], T=p["T"][:m])
+                 for p in projs]
+
+        def batched():
+            bq.qlora_linear_fwd_batch(items, workspace=ws)
+
+        def single(m=m):
             for p in projs:
                 bq.qlora_linear_fwd(p["x"][:m], p["q"], p["A"], p["B"], c["alpha"], y=p["y"][:m], T=p["T"][:m],
                                     workspace=ws)
-        ms = graph_ms(fwd, dev, stream, flush)
-        nbytes = sum(lib.nf4_packed_bytes(p["N"] * p["K"], 1) + 4 * r * (p["N"] + p["K"]) + 2 * m * (p["N"] + p["K"])
-                     for p in projs)
+        ms_b = graph_ms(batched, dev, stream, flush, reps=20)
+        ms_s = graph_ms(single, dev, stream, flush, reps=20)
+        nbytes = weight_bytes + sum(4 * r * (p["N"] + p["K"]) + 2 * m * (p["N"] + p["K"]) for p in projs)
         emit({"sweep": "small-M forward, 7 Llama-3-8B-shaped projections", "tokens": m, "rank": r,
-              "ms_per_layer": ms, "GB/s": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm,
-              "bytes_per_layer": nbytes})
+              "ms_per_layer_batched": ms_b, "ms_per_layer_single_calls": ms_s,
+              "weight_GB/s_batched": weight_bytes / ms_b / 1e6, "frac_hbm_batched": weight_bytes / ms_b / 1e6 / hbm,
+              "GB/s_batched": nbytes / ms_b / 1e6, "GB/s_single_calls": nbytes / ms_s / 1e6,
+              "weight_bytes_per_layer": weight_bytes, "bytes_per_layer": nbytes})
     del projs, ws
 
     # SmolLM2-shaped stack: QLoRA forward + backward on q and v of 30 layers

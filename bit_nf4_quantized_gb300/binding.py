@@ -28,6 +28,7 @@ ENTRY_POINTS = (
     "nf4_embedding_rows", "nf4_merge_lora",
     "qlora_fwd_workspace_bytes", "qlora_bwd_workspace_bytes", "qlora_linear_fwd",
     "qlora_linear_bwd", "qlora_last_device_status", "nf4_kernel_launch_count",
+    "qlora_fwd_batch_workspace_bytes", "qlora_linear_fwd_batch",
 )
 
 
@@ -42,6 +43,13 @@ class _Nf4Tensor(ctypes.Structure):
                 ("reserved", ctypes.c_int32), ("packed", ctypes.c_void_p),
                 ("absmax", ctypes.c_void_p), ("nested_absmax", ctypes.c_void_p),
                 ("offset", ctypes.c_void_p)]
+
+
+class _FwdItem(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("rank", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("mode", ctypes.c_int32), ("W", ctypes.POINTER(_Nf4Tensor)),
+                ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("T_out", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -80,8 +88,11 @@ def load() -> ctypes.CDLL:
         "qlora_linear_fwd": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, tp, vp, vp, vp, vp, vp, sz, vp]),
         "qlora_linear_bwd": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, vp, vp, tp, vp, vp,
                                    vp, vp, vp, vp, sz, vp]),
+        "qlora_fwd_batch_workspace_bytes": (sz, [i64, i32, ctypes.POINTER(_FwdItem), i32]),
+        "qlora_linear_fwd_batch": (i32, [i64, i32, ctypes.POINTER(_FwdItem), i32, vp, sz, vp]),
         "qlora_last_device_status": (i32, [vp, i32]),
         "nf4_kernel_launch_count": (i64, []),
+        "qlora_debug_wait_timeout": (None, [i32]),
         "nf4_timing_enable": (None, [i32]),
         "nf4_timing_read": (i32, [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), i32]),
     }
@@ -271,6 +282,47 @@ def qlora_linear_fwd(x: torch.Tensor, W: Nf4Tensor, A: torch.Tensor, B: torch.Te
     return y, T
 
 
+def qlora_linear_fwd_batch(items, workspace: torch.Tensor = None, stream=None):
+    """Forward of several projections sharing M: ``items`` is a list of dicts with keys x, W,
+    A, B, alpha and optionally mode, y, T (as for qlora_linear_fwd).  Returns [(y, T), ...].
+    With bf16 and M <= 16 every group of up to 8 items runs as one pair of launches."""
+    lib = load()
+    n = len(items)
+    M = items[0]["x"].shape[0]
+    cd = _dtype_code(items[0]["x"].dtype)
+    arr = (_FwdItem * n)()
+    keep = []
+    outs = []
+    for i, it in enumerate(items):
+        x, W, A, B = it["x"], it["W"], it["A"], it["B"]
+        N, K = W.shape
+        r = A.shape[0]
+        y = it.get("y")
+        T = it.get("T")
+        if y is None:
+            y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+        if T is None:
+            T = torch.empty((M, r), dtype=torch.float32, device=x.device)
+        cs = W.c_struct()
+        keep.append(cs)
+        arr[i] = _FwdItem(N, K, r, float(it["alpha"]), int(it.get("mode", SCALE_LORA)), ctypes.pointer(cs),
+                          A.data_ptr(), B.data_ptr(), x.data_ptr(), y.data_ptr(), T.data_ptr())
+        outs.append((y, T))
+    ws = workspace if workspace is not None else _workspace(
+        lib.qlora_fwd_batch_workspace_bytes(M, n, arr, cd), items[0]["x"].device)
+    _check(lib.qlora_linear_fwd_batch(M, n, arr, cd, _ptr(ws), ws.numel(), _stream(stream)), "qlora_linear_fwd_batch")
+    return outs
+
+
+def qlora_fwd_batch_workspace_bytes(M: int, shapes, rank: int, dtype=torch.bfloat16) -> int:
+    """Workspace bytes of qlora_linear_fwd_batch for items of the given (N, K) shapes and rank."""
+    lib = load()
+    arr = (_FwdItem * len(shapes))()
+    for i, (N, K) in enumerate(shapes):
+        arr[i] = _FwdItem(N, K, rank, 1.0, SCALE_LORA, None, None, None, None, None, None)
+    return int(lib.qlora_fwd_batch_workspace_bytes(M, len(shapes), arr, _dtype_code(dtype)))
+
+
 def qlora_linear_bwd(dy: torch.Tensor, x: torch.Tensor, T: torch.Tensor, W: Nf4Tensor, A: torch.Tensor,
                      B: torch.Tensor, alpha: float, mode: int = SCALE_LORA, dx: torch.Tensor = None,
                      dA: torch.Tensor = None, dB: torch.Tensor = None, workspace: torch.Tensor = None,
@@ -294,6 +346,13 @@ def qlora_linear_bwd(dy: torch.Tensor, x: torch.Tensor, T: torch.Tensor, W: Nf4T
                                 ctypes.byref(cs), _ptr(A), _ptr(B), _ptr(dx), _ptr(dA), _ptr(dB),
                                 _ptr(ws), ws.numel(), _stream(stream)), "qlora_linear_bwd")
     return dx, dA, dB
+
+
+def debug_wait_timeout(on: bool = True):
+    """Arm (or disarm) the library's test of its timeout path: the next tensor-core contraction
+    runs with a 20 ms wait limit and its first CTA leaves its first stage unissued, so that
+    launch ends with NF4_ERR_TIMEOUT in the device status word (its outputs unspecified)."""
+    load().qlora_debug_wait_timeout(int(on))
 
 
 def device_status(clear: bool = True, stream=None) -> int:

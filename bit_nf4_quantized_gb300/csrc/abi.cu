@@ -7,6 +7,7 @@
 // s = alpha / rank, rsLoRA a separate scale ("Adapter API", "LoRA FA includes
 // gradient preconditioning"); no CPU fallback and no automatic precision change,
 // unsupported values fail explicitly ("Explicit accelerated training profiles").
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -203,6 +204,15 @@ KernelTimer::~KernelTimer() {
   t.pending[kind_].emplace_back(start_, stop);
 }
 
+namespace {
+std::atomic<int> g_wait_fault{0};
+}  // namespace
+
+WaitSettings take_wait_settings() {
+  if (g_wait_fault.exchange(0) != 0) return WaitSettings{20000000ull, 1};
+  return WaitSettings{4000000000ull, 0};
+}
+
 const DecodeTables& decode_tables() { return tables().dec; }
 const EncodeTables& encode_tables() { return tables().enc; }
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -261,10 +271,46 @@ nf4_status check_linear(int64_t M, int64_t N, int64_t K, int32_t rank, float alp
   return NF4_OK;
 }
 
+bool small_m(int64_t M, nf4_dtype cd) { return cd == NF4_BF16 && M >= 1 && M <= kStreamMaxM; }
+
 // Workspace layouts.  bwd: G fp32 [M, r], then whatever the selected path needs.
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
+  if (small_m(M, cd)) {
+    LinearArgs la{M, N, K, r, 0.0f, Nf4View{}};
+    return stream_fwd_ws_bytes(&la, 1);
+  }
   if (cd == NF4_BF16) return tc_fwd_ws_bytes(M, N, K, r);
   return 0;
+}
+
+// Argument checks of one forward call (everything but the workspace); s receives the scale.
+nf4_status check_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha, qlora_scale_mode mode,
+                     nf4_dtype compute, const void* x, const nf4_tensor* W, const float* A, const float* B,
+                     const void* y, const float* T_out, float* s) {
+  nf4_status st = check_linear(M, N, K, rank, alpha, mode, compute, s);
+  if (st != NF4_OK) return st;
+  if ((st = check_tensor(W, N * K)) != NF4_OK) return st;
+  if (A == nullptr || B == nullptr) return NF4_ERR_ARG;
+  if (M > 0 && (x == nullptr || y == nullptr || T_out == nullptr)) return NF4_ERR_ARG;
+  if (!aligned16(A) || !aligned16(B) || (M > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(T_out))))
+    return NF4_ERR_ALIGN;
+  return NF4_OK;
+}
+
+// Workspace of a batch of forward items: the largest group (small M) or item (otherwise).
+size_t batch_ws(int64_t M, int32_t count, const qlora_fwd_item* it, nf4_dtype cd) {
+  size_t need = 0;
+  if (small_m(M, cd)) {
+    for (int32_t g0 = 0; g0 < count; g0 += kStreamMaxGroup) {
+      LinearArgs la[kStreamMaxGroup];
+      const int n = std::min<int32_t>(kStreamMaxGroup, count - g0);
+      for (int i = 0; i < n; ++i) la[i] = LinearArgs{M, it[g0 + i].N, it[g0 + i].K, it[g0 + i].rank, 0.0f, Nf4View{}};
+      need = std::max(need, stream_fwd_ws_bytes(la, n));
+    }
+    return need;
+  }
+  for (int32_t i = 0; i < count; ++i) need = std::max(need, fwd_ws(M, it[i].N, it[i].K, it[i].rank, cd));
+  return need;
 }
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
   size_t b = a256(sizeof(float) * static_cast<size_t>(M) * r);
@@ -395,19 +441,20 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
                             const void* x, const nf4_tensor* W, const float* A, const float* B,
                             void* y, float* T_out, void* ws, size_t ws_bytes, void* stream) {
   float s = 0.0f;
-  nf4_status st = check_linear(M, N, K, rank, alpha, mode, compute, &s);
+  nf4_status st = check_fwd(M, N, K, rank, alpha, mode, compute, x, W, A, B, y, T_out, &s);
   if (st != NF4_OK) return st;
-  if ((st = check_tensor(W, N * K)) != NF4_OK) return st;
-  if (A == nullptr || B == nullptr) return NF4_ERR_ARG;
-  if (M > 0 && (x == nullptr || y == nullptr || T_out == nullptr)) return NF4_ERR_ARG;
-  if (!aligned16(A) || !aligned16(B) || (M > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(T_out))))
-    return NF4_ERR_ALIGN;
   const size_t need = fwd_ws(M, N, K, rank, compute);
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
   if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
   if (M == 0) return NF4_OK;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   LinearArgs a{M, N, K, rank, s, view_of(W)};
+  if (small_m(M, compute)) {
+    int* status = nullptr;
+    if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+    const StreamItem item{a, x, A, B, y, T_out};
+    return from_cuda(stream_forward(&item, 1, ws, status, cs));
+  }
   if (compute == NF4_BF16) {
     int* status = nullptr;
     if ((st = device_status_ptr(&status)) != NF4_OK) return st;
@@ -416,6 +463,54 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
   cudaError_t e = launch_lora_down(a, compute, x, A, T_out, cs);
   if (e == cudaSuccess) e = launch_fwd_simt(a, compute, x, T_out, B, y, cs);
   return from_cuda(e);
+}
+
+size_t qlora_fwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_fwd_item* items, nf4_dtype compute) {
+  if (M < 0 || count < 1 || items == nullptr) return 0;
+  for (int32_t i = 0; i < count; ++i)
+    if (items[i].N <= 0 || items[i].K <= 0 || items[i].rank < 1 || items[i].rank > 256) return 0;
+  return batch_ws(M, count, items, compute);
+}
+
+nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item* items, nf4_dtype compute,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (count < 1 || items == nullptr) return NF4_ERR_ARG;
+  std::vector<float> s(static_cast<size_t>(count));
+  for (int32_t i = 0; i < count; ++i) {
+    const qlora_fwd_item& it = items[i];
+    const nf4_status st = check_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A, it.B,
+                                    it.y, it.T_out, &s[i]);
+    if (st != NF4_OK) return st;
+  }
+  const size_t need = batch_ws(M, count, items, compute);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
+  if (M == 0) return NF4_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (small_m(M, compute)) {
+    int* status = nullptr;
+    const nf4_status st = device_status_ptr(&status);
+    if (st != NF4_OK) return st;
+    for (int32_t g0 = 0; g0 < count; g0 += kStreamMaxGroup) {
+      StreamItem group[kStreamMaxGroup];
+      const int n = std::min<int32_t>(kStreamMaxGroup, count - g0);
+      for (int i = 0; i < n; ++i) {
+        const qlora_fwd_item& it = items[g0 + i];
+        group[i] = StreamItem{LinearArgs{M, it.N, it.K, it.rank, s[g0 + i], view_of(it.W)}, it.x, it.A, it.B, it.y,
+                              it.T_out};
+      }
+      const cudaError_t e = stream_forward(group, n, ws, status, cs);
+      if (e != cudaSuccess) return NF4_ERR_CUDA;
+    }
+    return NF4_OK;
+  }
+  for (int32_t i = 0; i < count; ++i) {
+    const qlora_fwd_item& it = items[i];
+    const nf4_status st = qlora_linear_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A,
+                                           it.B, it.y, it.T_out, ws, ws_bytes, stream);
+    if (st != NF4_OK) return st;
+  }
+  return NF4_OK;
 }
 
 nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
@@ -472,6 +567,8 @@ nf4_status qlora_last_device_status(void* stream, int32_t clear) {
 }
 
 int64_t nf4_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void qlora_debug_wait_timeout(int32_t on) { g_wait_fault.store(on != 0 ? 1 : 0); }
 
 void nf4_timing_enable(int32_t on) { timing().enabled.store(on != 0); }
 

@@ -83,6 +83,8 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CU
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  pdl_allow_next();
+  pdl_wait();   // TMEM only after the preceding grid has completed (no hold-and-wait on TMEM)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(tmem_cols)
@@ -93,8 +95,6 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_allow_next();
-  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {

@@ -76,6 +76,15 @@ const EncodeTables& encode_tables();
 // Launch accounting (for the launch count reported by the ABI).
 void note_launch(int n = 1);
 
+// Bounded-wait settings of one tensor-core launch: the wait limit, and whether the launch's
+// first CTA leaves its first pipeline stage unissued (so that the waits for that stage run
+// out).  Normally {4 s, 0}; qlora_debug_wait_timeout() arms {20 ms, 1} for the next launch.
+struct WaitSettings {
+  uint64_t wait_ns;
+  int skip_stage0;
+};
+WaitSettings take_wait_settings();
+
 // Programmatic dependent launch.  Kernels of the bf16 path are launched with
 // programmatic stream serialization: a kernel may start while its predecessor in the
 // stream is finishing.  Each kernel calls pdl_allow_next() once its prologue holds every

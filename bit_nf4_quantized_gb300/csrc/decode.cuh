@@ -31,15 +31,18 @@ __device__ __forceinline__ void build_lut(float a, uint32_t (&L)[4], uint32_t (&
 }
 
 // Eight weights of one packed word to four bf16x2 registers in element order.  The
-// word's nibbles, low first, are elements 1 0 3 2 5 4 7 6 (element 2i is the high
-// nibble of byte i); the final byte interleave puts them back in order.
+// word's nibbles, low first, are elements 1 0 3 2 5 4 7 6 (element 2i is the high nibble
+// of byte i); the final byte interleave puts them back in order.  The selectors (the low 3
+// bits of each code, and bit 3 choosing the half table) are formed once for the whole word;
+// prmt reads its selector from the low 16 bits, so the upper four codes take them shifted.
 __device__ __forceinline__ void decode8(uint32_t w, const uint32_t (&L)[4], const uint32_t (&H)[4],
                                         uint32_t* out) {
+  const uint32_t s7w = w & 0x77777777u;                            // index within a half table
+  const uint32_t sbw = ((w >> 1) & 0x44444444u) | 0x32103210u;     // pick the half by bit 3
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint32_t q = h == 0 ? w : (w >> 16);
-    const uint32_t s7 = q & 0x7777u;                      // index within a half table
-    const uint32_t sb = 0x3210u | ((q >> 1) & 0x4444u);   // pick the half by bit 3
+    const uint32_t s7 = h == 0 ? s7w : (s7w >> 16);
+    const uint32_t sb = h == 0 ? sbw : (sbw >> 16);
     const uint32_t lo = prmt(prmt(L[0], L[1], s7), prmt(L[2], L[3], s7), sb);
     const uint32_t hi = prmt(prmt(H[0], H[1], s7), prmt(H[2], H[3], s7), sb);
     out[2 * h] = prmt(lo, hi, 0x4051u);

@@ -57,10 +57,10 @@ constexpr int kStages = 3;
 constexpr int kThreads = 192;               // 6 warps, roles above
 constexpr int kWarpEpi = 2;                 // first of the 4 epilogue warps
 constexpr int kTmemCols = 512;
-// barriers: full[kStages] empty[kStages] accfull[2] accempty[2], then the abort flag and
-// the TMEM address
+// barriers: full[kStages] empty[kStages] accfull[2] accempty[2] done, then the abort flag
+// and the TMEM address
 constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages, kBarAccEmpty = kBarAccFull + 2,
-              kNumBars = kBarAccEmpty + 2;
+              kBarDone = kBarAccEmpty + 2, kNumBars = kBarDone + 1;
 constexpr int kOutRows = 32;                // tokens per epilogue store box
 constexpr int kOutBytes = kOutRows * kTileF * 2;   // 8 KB: [32 tokens][128 features] bf16
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 2 * kOutBytes + kNumBars * 8 + 16;
@@ -93,6 +93,8 @@ struct GemmParams {
   int split, chunk;
   float* part_ws;
   int* part_tickets;
+  uint64_t wait_ns;    // bounded-wait limit of this launch
+  int skip_stage0;     // CTA 0 leaves its first stage unissued (tests of the timeout path)
 };
 
 struct Unit {
@@ -169,9 +171,15 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
       mbar_init(bar(kBarAccFull + b), 1);                  // the pair MMAs' commit
       mbar_init(bar(kBarAccEmpty + b), 4 * kCluster);      // the epilogue warps of both CTAs
     }
+    mbar_init(bar(kBarDone), 1);                           // the issuer's last commit
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  pdl_allow_next();
+  // TMEM is taken only after the preceding grid has completed: a CTA never holds TMEM while
+  // it waits for another grid, so a CTA blocked in tcgen05.alloc always waits for one that
+  // is running to its end
+  pdl_wait();
   if (warp == 1) {   // one warp of each CTA of the pair allocates collectively
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -182,8 +190,6 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
   cluster_sync();   // the peer's barriers are initialised before anything signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_allow_next();
-  pdl_wait();
 
   // every role walks the same units (cluster_id, + n_clusters, ...) and steps
   auto unit_at = [&](int64_t lt) { return cluster_id + lt * n_clusters; };
@@ -200,8 +206,12 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const int f0 = static_cast<int>(tile_f(un.tile) * kTileF);
         for (int st = 0; st < un.nred + un.nslab; ++st, c.advance()) {
           const int s = c.s;
-          if (!mbar_wait(bar(kBarEmpty + s), c.ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(bar(kBarEmpty + s), c.ph ^ 1u, abort_flag, p.status, p.wait_ns)) { ok = false; break; }
           const uint32_t full = lead_bar(kBarFull + s);
+          if (p.skip_stage0 && blockIdx.x == 0 && issued == 0) {   // the stage's waits will run out
+            ++issued;
+            continue;
+          }
           if (st < un.nred) {
             const int k0 = (un.red0 + st) * kStepK;
             if (rank == 0) mbar_expect_tx(bar(kBarFull + s), kCluster * 2 * kSubs * kSubBytes);
@@ -231,7 +241,7 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         // the pair MMAs' commits arrive on this CTA's empty barriers: wait for the last
         // round of them so that none lands after the CTA has exited
         for (int k = 0; k < kStages; ++k) {
-          if (!mbar_wait(bar(kBarEmpty + c.s), c.ph ^ 1u, abort_flag, p.status)) break;
+          if (!mbar_wait(bar(kBarEmpty + c.s), c.ph ^ 1u, abort_flag, p.status, p.wait_ns)) break;
           c.advance();
         }
       } else if (rank == 0) {  // let copies already in flight land before the CTA exits
@@ -255,14 +265,14 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
         const Unit un = unit_of(p, unit_at(lt));
         const int nsteps = un.nred + un.nslab;
         const uint32_t b = static_cast<uint32_t>(lt) & 1u;
-        if (!mbar_wait(bar(kBarAccEmpty + b), (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status)) {
+        if (!mbar_wait(bar(kBarAccEmpty + b), (static_cast<uint32_t>(lt >> 1) & 1u) ^ 1u, abort_flag, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kTileT;
         for (int st = 0; st < nsteps; ++st, c.advance()) {
-          if (!mbar_wait(bar(kBarFull + c.s), c.ph, abort_flag, p.status)) {
+          if (!mbar_wait(bar(kBarFull + c.s), c.ph, abort_flag, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -291,6 +301,10 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
           if (st == nsteps - 1) umma_commit_pair_mc(bar(kBarAccFull + b), 0x3);
         }
       }
+      // every pair MMA issued has completed before either CTA frees its TMEM (the final
+      // cluster barrier holds the odd CTA until this drain is over)
+      umma_commit_pair_mc(bar(kBarDone), 0x1);
+      mbar_drain(bar(kBarDone), 0);
     }
   } else {
     // ---------------- epilogue ----------------
@@ -308,7 +322,7 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
       const Unit un = unit_of(p, unit_at(lt));
       const uint32_t b = static_cast<uint32_t>(lt) & 1u;
       const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-      const bool ok_w = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), aph, abort_flag, p.status));
+      const bool ok_w = __all_sync(0xffffffffu, mbar_wait(bar(kBarAccFull + b), aph, abort_flag, p.status, p.wait_ns));
       if (lane == 0) votes[b][quarter] = ok_w ? 1 : 0;
       named_sync(1, 128);
       if (!(votes[b][0] && votes[b][1] && votes[b][2] && votes[b][3])) break;
@@ -487,6 +501,9 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtenso
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * kCluster));
   GemmParams q = p;
   split_tail(&q, pairs, clusters);
+  const WaitSettings ws = take_wait_settings();
+  q.wait_ns = ws.wait_ns;
+  q.skip_stage0 = ws.skip_stage0;
   KernelTimer timer(p.mode == 0 ? NF4_TIME_FWD_GEMM : NF4_TIME_DX_GEMM, st);
   cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16_tc_gemm, w, tok, slab_f, slab_t, out, q);

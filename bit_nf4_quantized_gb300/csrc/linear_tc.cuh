@@ -15,6 +15,23 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G,
                         void* ws, int* status, cudaStream_t st);
 
+// stream_fwd.cu: the forward for at most kStreamMaxM tokens, for up to kStreamMaxGroup
+// projections (sharing M) in two launches: T by lora_down_small, then one persistent pass that
+// streams every projection's stored weight once, decodes it in registers into TMEM and runs
+// tcgen05.mma with the tokens as the N = 16 operand, the LoRA term in the same accumulator.
+constexpr int kStreamMaxM = 16;
+constexpr int kStreamMaxGroup = 8;
+struct StreamItem {
+  LinearArgs a;
+  const void* x;     // bf16 [M, K]
+  const float* A;    // [r, K]
+  const float* B;    // [N, r]
+  void* y;           // bf16 [M, N]
+  float* T;          // [M, r]
+};
+size_t stream_fwd_ws_bytes(const LinearArgs* a, int n);
+cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status, cudaStream_t st);
+
 // adapter_tc.cu: skinny tcgen05 products Out[rows, r] = X[rows, red] . Q[red, r] for the
 // rank-r contractions.  X is bf16 row-major with `x_inner` columns (the reduction runs
 // along its rows when mn_major == false, down its columns otherwise); Q is bf16

@@ -49,16 +49,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete.  Gives up (returns false) when another
-// thread of the CTA has given up, or after kWaitLimitNs, recording the timeout.
+// thread of the CTA has given up, or after `limit_ns` (kWaitLimitNs unless a launch was
+// given a shorter limit), recording the timeout.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_test(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicCAS(status, 0, static_cast<int>(NF4_ERR_TIMEOUT));
         return false;
@@ -187,7 +188,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 
 // Shared-memory matrix descriptor (tcgen05 format): start, leading and stride byte
 // offsets in 16-byte units, descriptor version 1, 128-byte swizzle.

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define QLORA_NF4_ABI_VERSION 1
+#define QLORA_NF4_ABI_VERSION 2
 
 typedef enum {
   NF4_OK = 0,
@@ -180,12 +180,41 @@ size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, 
  * compute = NF4_BF16: x and y bf16, bf16 tensor-core operands (the decoded weight
  *   rounded once to bf16, A and B rounded to bf16, s*T rounded to bf16) with fp32
  *   accumulation; needs K % 64 == 0 and N % 8 == 0 (NF4_ERR_SHAPE otherwise).
+ *   With M <= 16 the stored weight is streamed once and decoded inside the contraction
+ *   (no decoded copy; workspace of a few MB); larger M decodes W once per call into the
+ *   workspace and runs the tiled tensor-core GEMM.
  * rank 1..256 ([ADAPT] "Adapter API") and rank <= min(N, K); alpha finite.
  * ws: device workspace of qlora_fwd_workspace_bytes() bytes. */
 nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
                             qlora_scale_mode mode, nf4_dtype compute,
                             const void* x, const nf4_tensor* W, const float* A, const float* B,
                             void* y, float* T_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Forward of several projections that share M and the compute dtype, for example the seven
+ * projections of one transformer layer ([GATE] "Shape-matched ceilings": q, k, v, o, gate, up,
+ * down).  Item i computes exactly what qlora_linear_fwd computes for its arguments.
+ * With compute = NF4_BF16 and M <= 16, up to 8 items run as one pair of launches (T for every
+ * item, then one persistent pass over all their stored weights); more items run in groups of
+ * 8.  Otherwise the items run one after another with the single-call path.  Items must not
+ * write to memory another item reads.  ws: qlora_fwd_batch_workspace_bytes() bytes.
+ * Each item is validated as qlora_linear_fwd validates its arguments; the first failing
+ * item's status is returned and nothing is enqueued. */
+typedef struct {
+  int64_t N, K;
+  int32_t rank;
+  float alpha;
+  qlora_scale_mode mode;
+  const nf4_tensor* W;    /* numel N*K, [N, K] row-major */
+  const float* A;         /* [rank, K] fp32 */
+  const float* B;         /* [N, rank] fp32 */
+  const void* x;          /* [M, K] in the compute dtype */
+  void* y;                /* [M, N] in the compute dtype */
+  float* T_out;           /* [M, rank] fp32 */
+} qlora_fwd_item;
+
+size_t qlora_fwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_fwd_item* items, nf4_dtype compute);
+nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item* items, nf4_dtype compute,
+                                  void* ws, size_t ws_bytes, void* stream);
 
 /* Backward ([ADAPT] "Packed NF4 ...": input gradients through the frozen base, no
  * base-weight gradient; [GATE] "The TFLOPS back-check": no dL/dW):
@@ -206,6 +235,15 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
  * device-side condition was recorded); clear != 0 resets it to NF4_OK. */
 nf4_status qlora_last_device_status(void* stream, int32_t clear);
 
+/* Test support for the timeout path of the library's bounded device waits.  After a call
+ * with on != 0, the next tensor-core contraction launched (the bf16 GEMM of qlora_linear_fwd /
+ * qlora_linear_bwd, or the small-M weight pass of the forward) runs with a 20 ms wait limit
+ * instead of 4 s, and its first CTA does not issue the copies of its first pipeline stage, so
+ * the waits for that stage run out.  That launch winds down (copies in flight land, TMEM is
+ * freed), NF4_ERR_TIMEOUT is set in the device status word and its outputs are unspecified;
+ * nothing faults or hangs, and later calls are unaffected.  on = 0 disarms a pending request. */
+void qlora_debug_wait_timeout(int32_t on);
+
 /* Number of kernels this library has launched in this process (all devices). */
 int64_t nf4_kernel_launch_count(void);
 
@@ -225,7 +263,8 @@ typedef enum {
                                * with the call's operand staging in the same launch */
   NF4_TIME_EMBEDDING = 6,   /* nf4_embedding_rows */
   NF4_TIME_MERGE = 7,       /* nf4_merge_lora */
-  NF4_TIME_KINDS = 8
+  NF4_TIME_STREAM_FWD = 8,  /* the forward's small-M pair of launches (T, then the weight pass) */
+  NF4_TIME_KINDS = 9
 } nf4_timed_kernel;
 
 void nf4_timing_enable(int32_t on);

@@ -22,6 +22,9 @@ tolerance.  A whole or partly wrong tile, a missing split-K part or a missing Lo
 its elements by far more than these bounds.
 """
 
+import json
+import os
+
 import numpy as np
 
 from oracle import qlora
@@ -36,12 +39,12 @@ def _units(compute, n_contract):
     return dict(out=2.0 ** -24, op=2.0 ** -24, acc=(n_contract + 4) * 2.0 ** -24)
 
 
-def forward_bounds(x, W, A, B, s, compute, y_ref, T_ref):
-    """Element-wise bounds for y and T of qlora_linear_fwd."""
+def forward_bounds(x, W, A, B, s, compute, y_ref, T_ref, abs_W=None):
+    """Element-wise bounds for y and T of qlora_linear_fwd (``abs_W``: |W| if already held)."""
     K = np.shape(x)[1]
     r = np.shape(A)[0]
     u = _units(compute, K + r)
-    fm = qlora.forward_magnitudes(x, W, A, B, s, compute)
+    fm = qlora.forward_magnitudes(x, W, A, B, s, compute, abs_W=abs_W)
     aB = np.abs(np.asarray(B, dtype=np.float64))
     t_err = u["acc"] * fm["T"]                          # error of the device's T itself
     y = u["out"] * np.abs(y_ref) + (1 + u["out"]) * (
@@ -87,6 +90,10 @@ def check(got: dict, want: dict, bounds: dict, compute: str):
         frob = qlora.rel_frobenius(g, w)
         tile = qlora.tile_rel_frobenius(g.reshape(g.shape[0], -1), w.reshape(w.shape[0], -1), 256)
         report[k] = dict(frob=frob, tile=tile, bound_ratio=ratio)
+    if os.environ.get("PARITY_REPORT"):   # measured figures of every check, one JSON line each
+        with open(os.environ["PARITY_REPORT"], "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                                "compute": compute, "report": report}) + "\n")
     for k, m in report.items():
         assert np.all(np.isfinite(np.asarray(got[k], dtype=np.float64))), (k, "non-finite", report)
         assert m["frob"] <= FROB[compute], (k, "relative Frobenius", report)

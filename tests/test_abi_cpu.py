@@ -41,7 +41,21 @@ def test_every_declared_function_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(binding.ENTRY_POINTS) <= set(names)
-    assert lib.nf4_abi_version() == 1
+    assert lib.nf4_abi_version() == 2
+
+
+def test_noalloc_limit_has_one_source(lib):
+    """The binding's NOALLOC_MAX_NUMEL is the header's NF4_QUANTIZE_NOALLOC_MAX_NUMEL, and the
+    library refuses exactly the sizes above it (a refusal comes before any device work)."""
+    text = open(os.path.join(ROOT, "include", "qlora_nf4.h")).read()
+    m = re.search(r"#define\s+NF4_QUANTIZE_NOALLOC_MAX_NUMEL\s+\((\d+)LL\)", text)
+    assert m and int(m.group(1)) == binding.NOALLOC_MAX_NUMEL
+    t = binding._Nf4Tensor()
+    n = binding.NOALLOC_MAX_NUMEL + 1
+    t.numel, t.double_quant, t.reserved = n, 0, 0
+    t.packed, t.absmax = 0x10000000, 0x11000000
+    assert lib.nf4_quantize_noalloc(ctypes.c_void_p(0x20000000), 0, n, ctypes.byref(t), None) == \
+        binding.NF4_ERR_TOO_LARGE
 
 
 def test_size_queries_match_oracle(lib):

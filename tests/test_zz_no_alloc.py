@@ -51,6 +51,12 @@ def test_noalloc_matches_nf4_quantize_on_two_calls_in_a_row(lib):
         got = binding.nf4_quantize_noalloc(x, binding.Nf4Tensor.empty(tuple(x.shape), True, dev))
         torch.cuda.synchronize()
         _same(got, want)
+    # without double quantization (fp32 block maxima; the scratch array is not used), twice
+    for x in (second.to(dev), first.to(dev)):
+        want = binding.nf4_quantize(x, double_quant=False)
+        got = binding.nf4_quantize_noalloc(x, binding.Nf4Tensor.empty(tuple(x.shape), False, dev))
+        torch.cuda.synchronize()
+        _same(got, want)
     # the largest accepted size, then a small one again
     big = wl.device_normal((binding.NOALLOC_MAX_NUMEL,), 0.02, 91, dev, torch.bfloat16)
     _same(binding.nf4_quantize_noalloc(big, binding.Nf4Tensor.empty(tuple(big.shape), True, dev)),
