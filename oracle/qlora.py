@@ -90,18 +90,20 @@ def adapter_backward(dy, x, A, B, s: float, compute: str = "bf16"):
     return s * (G.T @ x64), s * (dy64.T @ T), G
 
 
-def forward_magnitudes(x, W, A, B, s: float, compute: str = "bf16"):
+def forward_magnitudes(x, W, A, B, s: float, compute: str = "bf16", abs_W=None):
     """Sums of the absolute values of the terms of each output of ``forward``, in float64.
 
     Returns dict(y_base = |x| |W|^T (the terms x[m,k] W[n,k] of y), y_slab = |s| |T| |B|^T
     (the terms s T[m,j] B[n,j]), T = |x| |A|^T (the terms of T)), on the same rounded
     operands as ``forward``.  A rounding error of relative size u in every term of a sum
     moves that sum by at most u times these magnitudes, which is what element-wise error
-    bounds are built from.
+    bounds are built from.  ``abs_W``: |W| of the rounded weight, when the caller already
+    holds it (a large weight is then not converted again).
     """
-    x64, W64, A64, B64 = _operands(compute, x, W, A, B)
+    x64, A64, B64 = _operands(compute, x, A, B)
+    aW = np.abs(_operands(compute, W)[0]) if abs_W is None else abs_W
     T_abs = np.abs(x64 @ A64.T)
-    ax, aW, aA, aB = (np.abs(t) for t in (x64, W64, A64, B64))
+    ax, aA, aB = (np.abs(t) for t in (x64, A64, B64))
     return dict(y_base=ax @ aW.T, y_slab=abs(s) * (T_abs @ aB.T), T=ax @ aA.T)
 
 
