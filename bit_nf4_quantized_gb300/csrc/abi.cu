@@ -460,8 +460,9 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
     if ((st = device_status_ptr(&status)) != NF4_OK) return st;
     return from_cuda(tc_forward(a, x, A, B, y, T_out, ws, status, cs));
   }
-  cudaError_t e = launch_lora_down(a, compute, x, A, T_out, cs);
-  if (e == cudaSuccess) e = launch_fwd_simt(a, compute, x, T_out, B, y, cs);
+  const float* xf = static_cast<const float*>(x);
+  cudaError_t e = launch_lora_down(a, xf, A, T_out, cs);
+  if (e == cudaSuccess) e = launch_fwd_simt(a, xf, T_out, B, static_cast<float*>(y), cs);
   return from_cuda(e);
 }
 
@@ -544,10 +545,11 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
     void* tc_ws = static_cast<char*>(ws) + a256(sizeof(float) * static_cast<size_t>(M) * rank);
     return from_cuda(tc_backward(a, dy, x, T, A, B, dx, dA, dB, G, tc_ws, status, cs));
   }
-  cudaError_t e = launch_lora_g(a, compute, dy, B, G, cs);
-  if (e == cudaSuccess) e = launch_dx_simt(a, compute, dy, G, A, dx, cs);
-  if (e == cudaSuccess) e = launch_lora_dA(a, compute, G, x, dA, cs);
-  if (e == cudaSuccess) e = launch_lora_dB(a, compute, dy, T, dB, cs);
+  const float* dyf = static_cast<const float*>(dy);
+  cudaError_t e = launch_lora_g(a, dyf, B, G, cs);
+  if (e == cudaSuccess) e = launch_dx_simt(a, dyf, G, A, static_cast<float*>(dx), cs);
+  if (e == cudaSuccess) e = launch_lora_dA(a, G, static_cast<const float*>(x), dA, cs);
+  if (e == cudaSuccess) e = launch_lora_dB(a, dyf, T, dB, cs);
   return from_cuda(e);
 }
 

@@ -163,35 +163,23 @@ cudaError_t launch_embedding_rows(const Nf4View& w, int64_t rows, int64_t dim, c
 cudaError_t launch_merge_lora(const Nf4View& w, int64_t N, int64_t K, int r, float s, const float* A,
                               const float* B, void* out, nf4_dtype od, cudaStream_t st);
 
-// ---- linear_simt.cu (fp32 profile; adapter reductions for both profiles) -------
+// ---- linear_simt.cu (the fp32 profile) -----------------------------------------
 struct LinearArgs {
   int64_t M, N, K;
   int r;
   float s;
   Nf4View W;
 };
-cudaError_t launch_lora_down(const LinearArgs& a, nf4_dtype cd, const void* x, const float* A,
-                             float* T, cudaStream_t st);
-cudaError_t launch_fwd_simt(const LinearArgs& a, nf4_dtype cd, const void* x, const float* T,
-                            const float* B, void* y, cudaStream_t st);
-cudaError_t launch_lora_g(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* B,
-                          float* G, cudaStream_t st);
-cudaError_t launch_dx_simt(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* G,
-                           const float* A, void* dx, cudaStream_t st);
-cudaError_t launch_lora_dA(const LinearArgs& a, nf4_dtype cd, const float* G, const void* x,
-                           float* dA, cudaStream_t st);
-cudaError_t launch_lora_dB(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* T,
-                           float* dB, cudaStream_t st);
+cudaError_t launch_lora_down(const LinearArgs& a, const float* x, const float* A, float* T, cudaStream_t st);
+cudaError_t launch_fwd_simt(const LinearArgs& a, const float* x, const float* T, const float* B, float* y,
+                            cudaStream_t st);
+cudaError_t launch_lora_g(const LinearArgs& a, const float* dy, const float* B, float* G, cudaStream_t st);
+cudaError_t launch_dx_simt(const LinearArgs& a, const float* dy, const float* G, const float* A, float* dx,
+                           cudaStream_t st);
+cudaError_t launch_lora_dA(const LinearArgs& a, const float* G, const float* x, float* dA, cudaStream_t st);
+cudaError_t launch_lora_dB(const LinearArgs& a, const float* dy, const float* T, float* dB, cudaStream_t st);
 
 // ---- device helpers -----------------------------------------------------------
-__device__ __forceinline__ float load_as_float(const float* p, int64_t i) { return p[i]; }
-__device__ __forceinline__ float load_as_float(const __nv_bfloat16* p, int64_t i) {
-  return __bfloat162float(p[i]);
-}
-__device__ __forceinline__ void store_from_float(float* p, int64_t i, float v) { p[i] = v; }
-__device__ __forceinline__ void store_from_float(__nv_bfloat16* p, int64_t i, float v) {
-  p[i] = __float2bfloat16_rn(v);
-}
 // Round a float to the nearest bf16 value and return it as a float.
 __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));

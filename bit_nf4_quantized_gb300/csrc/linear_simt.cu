@@ -1,5 +1,5 @@
-// QLoRA linear on CUDA cores: the fp32 profile, and the adapter-side reductions
-// (T, G, dA, dB) that the bf16 profile also uses.
+// QLoRA linear on CUDA cores: the fp32 profile (compute = NF4_F32).  The bf16 profile
+// runs on the tensor cores (linear_tc.cu, adapter_tc.cu, stream_fwd.cu).
 //
 // Math ("Native model adaptation and NF4", sections "One model contract", "Packed
 // NF4 and the portable QLoRA profile", "LoRA FA includes gradient preconditioning"):
@@ -9,41 +9,22 @@
 // the weight decoded inside the shared-memory tile (no global decoded copy), no
 // TF32 and no atomics ("V100 accelerated qualification" record,
 // jit.kernel_identity: shared-f32 tiles, global-decode-scratch-0, no-atomics).
-// In the bf16 profile x, dY, A and B are rounded to bf16 before multiplying, the
-// products accumulate in fp32.
 #include "common.cuh"
 
 namespace qnf4 {
 namespace {
 
-template <typename T>
-__device__ __forceinline__ float ld_operand(const T* p, int64_t i);
-template <>
-__device__ __forceinline__ float ld_operand<float>(const float* p, int64_t i) { return p[i]; }
-template <>
-__device__ __forceinline__ float ld_operand<__nv_bfloat16>(const __nv_bfloat16* p, int64_t i) {
-  return __bfloat162float(p[i]);
-}
-
-// Adapter factor as the profile multiplies it: exact fp32, or rounded to bf16.
-template <bool kBf16>
-__device__ __forceinline__ float adapter_operand(float v) {
-  return kBf16 ? round_bf16(v) : v;
-}
-
 // ---- T = x A^T : one warp per (row m, 32 adapter columns) -----------------------------
-template <typename Tin>
 __global__ void __launch_bounds__(256)
-lora_down_kernel(const Tin* __restrict__ x, const float* __restrict__ A, float* __restrict__ T,
+lora_down_kernel(const float* __restrict__ x, const float* __restrict__ A, float* __restrict__ T,
                  int64_t M, int64_t K, int r) {
-  constexpr bool kBf16 = sizeof(Tin) == 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (m >= M) return;
   for (int j = 0; j < r; ++j) {
     float acc = 0.0f;
     for (int64_t k = lane; k < K; k += 32)
-      acc = fmaf(ld_operand(x, m * K + k), adapter_operand<kBf16>(A[static_cast<int64_t>(j) * K + k]), acc);
+      acc = fmaf(x[m * K + k], A[static_cast<int64_t>(j) * K + k], acc);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) T[m * r + j] = acc;
@@ -51,18 +32,16 @@ lora_down_kernel(const Tin* __restrict__ x, const float* __restrict__ A, float* 
 }
 
 // ---- G = dY B : one warp per row m ------------------------------------------------------
-template <typename Tin>
 __global__ void __launch_bounds__(256)
-lora_g_kernel(const Tin* __restrict__ dy, const float* __restrict__ B, float* __restrict__ G,
+lora_g_kernel(const float* __restrict__ dy, const float* __restrict__ B, float* __restrict__ G,
               int64_t M, int64_t N, int r) {
-  constexpr bool kBf16 = sizeof(Tin) == 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (m >= M) return;
   for (int j = 0; j < r; ++j) {
     float acc = 0.0f;
     for (int64_t n = lane; n < N; n += 32)
-      acc = fmaf(ld_operand(dy, m * N + n), adapter_operand<kBf16>(B[n * r + j]), acc);
+      acc = fmaf(dy[m * N + n], B[n * r + j], acc);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) G[m * r + j] = acc;
@@ -70,30 +49,28 @@ lora_g_kernel(const Tin* __restrict__ dy, const float* __restrict__ B, float* __
 }
 
 // ---- dA[j][k] = s sum_m G[m][j] x[m][k] : one thread per (j, k), fixed order over m ---------
-template <typename Tin>
 __global__ void __launch_bounds__(256)
-lora_dA_kernel(const float* __restrict__ G, const Tin* __restrict__ x, float* __restrict__ dA,
+lora_dA_kernel(const float* __restrict__ G, const float* __restrict__ x, float* __restrict__ dA,
                int64_t M, int64_t K, int r, float s) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(r) * K) return;
   const int j = static_cast<int>(idx / K);
   const int64_t k = idx % K;
   float acc = 0.0f;
-  for (int64_t m = 0; m < M; ++m) acc = fmaf(G[m * r + j], ld_operand(x, m * K + k), acc);
+  for (int64_t m = 0; m < M; ++m) acc = fmaf(G[m * r + j], x[m * K + k], acc);
   dA[idx] = s * acc;
 }
 
 // ---- dB[n][j] = s sum_m dY[m][n] T[m][j] : one thread per (n, j) ------------------------------
-template <typename Tin>
 __global__ void __launch_bounds__(256)
-lora_dB_kernel(const Tin* __restrict__ dy, const float* __restrict__ T, float* __restrict__ dB,
+lora_dB_kernel(const float* __restrict__ dy, const float* __restrict__ T, float* __restrict__ dB,
                int64_t M, int64_t N, int r, float s) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(r) * N) return;
   const int j = static_cast<int>(idx / N);
   const int64_t n = idx % N;
   float acc = 0.0f;
-  for (int64_t m = 0; m < M; ++m) acc = fmaf(ld_operand(dy, m * N + n), T[m * r + j], acc);
+  for (int64_t m = 0; m < M; ++m) acc = fmaf(dy[m * N + n], T[m * r + j], acc);
   dB[n * r + j] = s * acc;
 }
 
@@ -103,21 +80,17 @@ constexpr int kTile = 64;
 constexpr int kKStep = 16;
 
 // Decoded weight element (n, k) of a row-major [N, K] NF4 matrix.
-template <bool kBf16>
 __device__ __forceinline__ float decode_w(const Nf4View& w, int64_t n, int64_t k, int64_t K,
                                           const float* nf4, const float* dyn8, float offset) {
   const int64_t i = n * K + k;
-  const float v = __fmul_rn(nf4[nf4_code_at(w.packed, i)], block_scale(w, i >> 6, dyn8, offset));
-  return kBf16 ? round_bf16(v) : v;
+  return __fmul_rn(nf4[nf4_code_at(w.packed, i)], block_scale(w, i >> 6, dyn8, offset));
 }
 
 // y[m][n] = sum_k x[m][k] W[n][k] + s sum_j T[m][j] B[n][j]
-template <typename Tio>
 __global__ void __launch_bounds__(256)
-fwd_simt_kernel(const Tio* __restrict__ x, Nf4View w, const float* __restrict__ T,
-                const float* __restrict__ B, Tio* __restrict__ y, int64_t M, int64_t N, int64_t K,
+fwd_simt_kernel(const float* __restrict__ x, Nf4View w, const float* __restrict__ T,
+                const float* __restrict__ B, float* __restrict__ y, int64_t M, int64_t N, int64_t K,
                 int r, float s, DecodeTables tabs) {
-  constexpr bool kBf16 = sizeof(Tio) == 2;
   __shared__ float xs[kKStep][kTile + 4];
   __shared__ float ws[kKStep][kTile + 4];
   __shared__ float nf4[16];
@@ -138,8 +111,8 @@ fwd_simt_kernel(const Tio* __restrict__ x, Nf4View w, const float* __restrict__ 
       const int row = e >> 4, kk = e & 15;
       const int64_t k = k0 + kk;
       const int64_t m = m0 + row, n = n0 + row;
-      xs[kk][row] = (m < M && k < K) ? ld_operand(x, m * K + k) : 0.0f;
-      ws[kk][row] = (n < N && k < K) ? decode_w<kBf16>(w, n, k, K, nf4, dyn8, offset) : 0.0f;
+      xs[kk][row] = (m < M && k < K) ? x[m * K + k] : 0.0f;
+      ws[kk][row] = (n < N && k < K) ? decode_w(w, n, k, K, nf4, dyn8, offset) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -165,21 +138,17 @@ fwd_simt_kernel(const Tio* __restrict__ x, Nf4View w, const float* __restrict__ 
       const int64_t n = n0 + tx * 4 + jj;
       if (n >= N) continue;
       float lora = 0.0f;
-      for (int j = 0; j < r; ++j)
-        lora = fmaf(adapter_operand<kBf16>(s * T[m * r + j]), adapter_operand<kBf16>(B[n * r + j]), lora);
-      // bf16 profile: (s T) and B rounded to bf16, as the tensor-core path feeds them
-      store_from_float(y, m * N + n, acc[i][jj] + lora);
+      for (int j = 0; j < r; ++j) lora = fmaf(s * T[m * r + j], B[n * r + j], lora);
+      y[m * N + n] = acc[i][jj] + lora;
     }
   }
 }
 
 // dx[m][k] = sum_n dY[m][n] W[n][k] + s sum_j G[m][j] A[j][k]
-template <typename Tio>
 __global__ void __launch_bounds__(256)
-dx_simt_kernel(const Tio* __restrict__ dy, Nf4View w, const float* __restrict__ G,
-               const float* __restrict__ A, Tio* __restrict__ dx, int64_t M, int64_t N, int64_t K,
+dx_simt_kernel(const float* __restrict__ dy, Nf4View w, const float* __restrict__ G,
+               const float* __restrict__ A, float* __restrict__ dx, int64_t M, int64_t N, int64_t K,
                int r, float s, DecodeTables tabs) {
-  constexpr bool kBf16 = sizeof(Tio) == 2;
   __shared__ float ds[kKStep][kTile + 4];
   __shared__ float ws[kKStep][kTile + 4];
   __shared__ float nf4[16];
@@ -199,10 +168,10 @@ dx_simt_kernel(const Tio* __restrict__ dy, Nf4View w, const float* __restrict__ 
       // dY tile: 64 m x 16 n (n fastest); W tile: 16 n x 64 k (k fastest)
       const int row = e >> 4, nn = e & 15;
       const int64_t m = m0 + row, n = n0 + nn;
-      ds[nn][row] = (m < M && n < N) ? ld_operand(dy, m * N + n) : 0.0f;
+      ds[nn][row] = (m < M && n < N) ? dy[m * N + n] : 0.0f;
       const int wn = e >> 6, wk = e & 63;
       const int64_t n2 = n0 + wn, k = k0 + wk;
-      ws[wn][wk] = (n2 < N && k < K) ? decode_w<kBf16>(w, n2, k, K, nf4, dyn8, offset) : 0.0f;
+      ws[wn][wk] = (n2 < N && k < K) ? decode_w(w, n2, k, K, nf4, dyn8, offset) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -228,10 +197,8 @@ dx_simt_kernel(const Tio* __restrict__ dy, Nf4View w, const float* __restrict__ 
       const int64_t k = k0 + tx * 4 + jj;
       if (k >= K) continue;
       float lora = 0.0f;
-      for (int j = 0; j < r; ++j)
-        lora = fmaf(adapter_operand<kBf16>(s * G[m * r + j]),
-                    adapter_operand<kBf16>(A[static_cast<int64_t>(j) * K + k]), lora);
-      store_from_float(dx, m * K + k, acc[i][jj] + lora);
+      for (int j = 0; j < r; ++j) lora = fmaf(s * G[m * r + j], A[static_cast<int64_t>(j) * K + k], lora);
+      dx[m * K + k] = acc[i][jj] + lora;
     }
   }
 }
@@ -240,88 +207,50 @@ unsigned blocks_for(int64_t n, int per) { return static_cast<unsigned>((n + per 
 
 }  // namespace
 
-cudaError_t launch_lora_down(const LinearArgs& a, nf4_dtype cd, const void* x, const float* A,
-                             float* T, cudaStream_t st) {
+cudaError_t launch_lora_down(const LinearArgs& a, const float* x, const float* A, float* T, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const unsigned g = blocks_for(a.M, 8);
-  if (cd == NF4_F32)
-    lora_down_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(x), A, T, a.M, a.K, a.r);
-  else
-    lora_down_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), A, T,
-                                                        a.M, a.K, a.r);
+  lora_down_kernel<<<blocks_for(a.M, 8), 256, 0, st>>>(x, A, T, a.M, a.K, a.r);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_lora_g(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* B,
-                          float* G, cudaStream_t st) {
+cudaError_t launch_lora_g(const LinearArgs& a, const float* dy, const float* B, float* G, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const unsigned g = blocks_for(a.M, 8);
-  if (cd == NF4_F32)
-    lora_g_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(dy), B, G, a.M, a.N, a.r);
-  else
-    lora_g_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dy), B, G, a.M,
-                                                     a.N, a.r);
+  lora_g_kernel<<<blocks_for(a.M, 8), 256, 0, st>>>(dy, B, G, a.M, a.N, a.r);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_lora_dA(const LinearArgs& a, nf4_dtype cd, const float* G, const void* x,
-                           float* dA, cudaStream_t st) {
+cudaError_t launch_lora_dA(const LinearArgs& a, const float* G, const float* x, float* dA, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const unsigned g = blocks_for(static_cast<int64_t>(a.r) * a.K, 256);
-  if (cd == NF4_F32)
-    lora_dA_kernel<float><<<g, 256, 0, st>>>(G, static_cast<const float*>(x), dA, a.M, a.K, a.r, a.s);
-  else
-    lora_dA_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(G, static_cast<const __nv_bfloat16*>(x), dA, a.M,
-                                                      a.K, a.r, a.s);
+  lora_dA_kernel<<<blocks_for(static_cast<int64_t>(a.r) * a.K, 256), 256, 0, st>>>(G, x, dA, a.M, a.K, a.r, a.s);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_lora_dB(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* T,
-                           float* dB, cudaStream_t st) {
+cudaError_t launch_lora_dB(const LinearArgs& a, const float* dy, const float* T, float* dB, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  const unsigned g = blocks_for(static_cast<int64_t>(a.r) * a.N, 256);
-  if (cd == NF4_F32)
-    lora_dB_kernel<float><<<g, 256, 0, st>>>(static_cast<const float*>(dy), T, dB, a.M, a.N, a.r, a.s);
-  else
-    lora_dB_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dy), T, dB, a.M,
-                                                      a.N, a.r, a.s);
+  lora_dB_kernel<<<blocks_for(static_cast<int64_t>(a.r) * a.N, 256), 256, 0, st>>>(dy, T, dB, a.M, a.N, a.r, a.s);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_simt(const LinearArgs& a, nf4_dtype cd, const void* x, const float* T,
-                            const float* B, void* y, cudaStream_t st) {
+cudaError_t launch_fwd_simt(const LinearArgs& a, const float* x, const float* T, const float* B, float* y,
+                            cudaStream_t st) {
   KernelTimer timer(NF4_TIME_FWD_GEMM, st);
   const dim3 grid(blocks_for(a.N, kTile), blocks_for(a.M, kTile));
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  const DecodeTables& dt = decode_tables();
-  if (cd == NF4_F32)
-    fwd_simt_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), a.W, T, B,
-                                                 static_cast<float*>(y), a.M, a.N, a.K, a.r, a.s, dt);
-  else
-    fwd_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), a.W, T, B,
-                                                         static_cast<__nv_bfloat16*>(y), a.M, a.N, a.K,
-                                                         a.r, a.s, dt);
+  fwd_simt_kernel<<<grid, 256, 0, st>>>(x, a.W, T, B, y, a.M, a.N, a.K, a.r, a.s, decode_tables());
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_dx_simt(const LinearArgs& a, nf4_dtype cd, const void* dy, const float* G,
-                           const float* A, void* dx, cudaStream_t st) {
+cudaError_t launch_dx_simt(const LinearArgs& a, const float* dy, const float* G, const float* A, float* dx,
+                           cudaStream_t st) {
   KernelTimer timer(NF4_TIME_DX_GEMM, st);
   const dim3 grid(blocks_for(a.K, kTile), blocks_for(a.M, kTile));
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  const DecodeTables& dt = decode_tables();
-  if (cd == NF4_F32)
-    dx_simt_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(dy), a.W, G, A,
-                                                static_cast<float*>(dx), a.M, a.N, a.K, a.r, a.s, dt);
-  else
-    dx_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dy), a.W, G, A,
-                                                        static_cast<__nv_bfloat16*>(dx), a.M, a.N, a.K,
-                                                        a.r, a.s, dt);
+  dx_simt_kernel<<<grid, 256, 0, st>>>(dy, a.W, G, A, dx, a.M, a.N, a.K, a.r, a.s, decode_tables());
   note_launch();
   return cudaGetLastError();
 }
