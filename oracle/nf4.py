@@ -177,7 +177,8 @@ def block_scales(qt: dict) -> np.ndarray:
 
 
 def dequantize(qt: dict, out_dtype: str = "f32") -> np.ndarray:
-    """Decode to float32 values; ``out_dtype='bf16'`` returns the bfloat16-rounded values (as float32)."""
+    """Decode to float32 values; ``out_dtype='bf16'`` or ``'f16'`` returns them rounded once to
+    bfloat16 or IEEE half (as float32 values)."""
     n = qt["numel"]
     nf4 = nf4_codebook()
     q = unpack_codes(qt["packed"], n)
@@ -185,6 +186,8 @@ def dequantize(qt: dict, out_dtype: str = "f32") -> np.ndarray:
     w = (nf4[q] * scale).astype(np.float32)
     if out_dtype == "bf16":
         return round_bf16(w)
+    if out_dtype == "f16":
+        return round_f16(w)
     return w
 
 
@@ -197,6 +200,13 @@ def round_bf16(x) -> np.ndarray:
     out = r.view(np.float32).copy()
     out[nan] = np.nan
     return out.reshape(np.shape(x))
+
+
+def round_f16(x) -> np.ndarray:
+    """Round float32 values to IEEE binary16 (nearest, ties to even, gradual underflow, overflow to
+    infinity; numpy's float32 -> float16 conversion); returned as float32 values."""
+    with np.errstate(over="ignore"):   # overflow to infinity is the IEEE result
+        return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
 
 
 def bf16_bits(x) -> np.ndarray:

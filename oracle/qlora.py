@@ -22,8 +22,10 @@ with W = deq(W_nf4) [N, K], A [r, K], B [N, r], no bias, no dropout.  [GATE] sec
 Precision: every product and sum here is float64 (numpy matmul is the library
 step).  The operands are the exact values the device path multiplies: for the
 bfloat16 profile x, dY, A, B and the decoded W are first rounded to bfloat16
-(the decoded W as float32 nf4*a' then rounded once); for the float32 profile they
-stay float32.  Results are compared with a relative Frobenius tolerance because
+(the decoded W as float32 nf4*a' then rounded once); for the half-precision
+profile ([ADAPT] "Mixed precision keeps stable state in FP32": reconstructed
+weights are rounded to FP16 before multiplication) the same operands are rounded
+to IEEE binary16 instead; for the float32 profile they stay float32.  Results are compared with a relative Frobenius tolerance because
 the accumulation order is not unique.
 """
 
@@ -31,7 +33,7 @@ import math
 
 import numpy as np
 
-from .nf4 import round_bf16
+from .nf4 import round_bf16, round_f16
 
 RANK_MIN, RANK_MAX = 1, 256
 
@@ -57,8 +59,10 @@ def _operands(compute: str, *arrays):
         a32 = np.asarray(a, dtype=np.float32)
         if compute == "bf16":
             a32 = round_bf16(a32)
+        elif compute == "f16":
+            a32 = round_f16(a32)
         elif compute != "f32":
-            raise ValueError("compute must be 'bf16', 'f32' or 'f64'")
+            raise ValueError("compute must be 'bf16', 'f16', 'f32' or 'f64'")
         out.append(a32.astype(np.float64))
     return out
 

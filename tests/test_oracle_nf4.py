@@ -273,3 +273,36 @@ def test_bf16_rounding_against_torch():
                                  np.float32)])
     want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
     assert np.array_equal(nf4.round_bf16(x), want)
+
+
+def test_round_f16_hand_values():
+    """IEEE binary16: 11 significant bits, ties to even, subnormals down to 2^-24, overflow to inf."""
+    cases = [
+        (1.0 + 2.0 ** -11, 1.0),                       # halfway between 1 and 1 + 2^-10: even (1)
+        (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9),       # halfway between 1 + 2^-10 and 1 + 2^-9: even
+        (1.0 + 2.0 ** -11 + 2.0 ** -20, 1.0 + 2.0 ** -10),   # just above halfway: up
+        (-1.5 - 2.0 ** -12, -1.5),                     # below half an ulp: down in magnitude
+        (65504.0, 65504.0),                            # largest finite
+        (65519.99, 65504.0),                           # below the overflow threshold
+        (65520.0, np.inf),                             # halfway to 2^16: rounds up, overflows
+        (2.0 ** -24, 2.0 ** -24),                      # smallest subnormal
+        (2.0 ** -25, 0.0),                             # halfway between 0 and 2^-24: even (0)
+        (3 * 2.0 ** -26, 2.0 ** -24),                  # above halfway: up
+        (2.0 ** -14 + 2.0 ** -25, 2.0 ** -14),         # halfway in the subnormal spacing: even
+    ]
+    got = nf4.round_f16(np.array([c[0] for c in cases], dtype=np.float32))
+    want = np.array([c[1] for c in cases], dtype=np.float32)
+    assert np.array_equal(got, want), list(zip(got, want))
+
+
+def test_dequantize_f16_is_one_rounding_of_the_fp32_decode():
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal(64 * 40 + 7) * 0.02).astype(np.float32)
+    q = nf4.quantize(x, double_quant=True)
+    w32 = nf4.dequantize(q, "f32")
+    w16 = nf4.dequantize(q, "f16")
+    # every value is a binary16 number within half an ulp (2^-11 relative) of the fp32 decode
+    assert np.array_equal(w16.astype(np.float16).astype(np.float32), w16)
+    nz = w32 != 0
+    assert np.all(np.abs(w16[nz] - w32[nz]) <= np.abs(w32[nz]) * 2.0 ** -11)
+    assert np.all(w16[~nz] == 0)

@@ -210,3 +210,17 @@ def test_magnitudes_bound_and_equal_on_nonnegative_operands(seed):
     bm = qlora.backward_magnitudes(dy, x, W, A, B, -s, compute="f64")
     assert np.all(np.abs(dX) <= bm["dX_base"] + bm["dX_slab"] + 1e-12)
     assert np.all(np.abs(dA) <= bm["dA"] + 1e-12) and np.all(np.abs(dB) <= bm["dB"] + 1e-12)
+
+
+def test_f16_profile_rounds_operands():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((3, 64)).astype(np.float32)
+    W = (rng.standard_normal((4, 64)) * 0.02).astype(np.float32)
+    A = rng.standard_normal((2, 64)).astype(np.float32)
+    B = rng.standard_normal((4, 2)).astype(np.float32)
+    y, T = qlora.forward(x, W, A, B, 1.5, compute="f16")
+    xr, Wr, Ar, Br = (nf4.round_f16(t).astype(np.float64) for t in (x, W, A, B))
+    assert np.allclose(y, xr @ Wr.T + 1.5 * (xr @ Ar.T) @ Br.T, rtol=1e-13, atol=1e-13)
+    # the operands really were rounded: the result differs from the bf16 and fp32 profiles
+    assert not np.allclose(y, qlora.forward(x, W, A, B, 1.5, compute="bf16")[0], rtol=1e-6, atol=0)
+    assert not np.allclose(y, qlora.forward(x, W, A, B, 1.5, compute="f32")[0], rtol=1e-9, atol=0)
