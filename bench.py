@@ -524,6 +524,29 @@ def measure_no_double_quant(layer, row_ms):
             "timing": "fwd+bwd of one projection as a graph, L2 flushed between replays"}
 
 
+def measure_f16_profile(layer, row_ms):
+    """The gate projection's forward + backward in the FP16 compute profile (IEEE half operands
+    and outputs, fp32 accumulation) beside the bf16 one, same weight, each as a graph with L2
+    flushed between replays."""
+    import torch
+    from bit_nf4_quantized_gb300 import binding as bq
+    p = next(q for q in layer.proj if q["name"] == "gate_proj")
+    x16, dy16 = p["x"].to(torch.float16), p["dy"].to(torch.float16)
+    y16, dx16 = torch.empty_like(p["y"], dtype=torch.float16), torch.empty_like(p["dx"], dtype=torch.float16)
+
+    def fwd_bwd(x, dy, y, dx):
+        bq.qlora_linear_fwd(x, p["q"], p["A"], p["B"], layer.alpha, y=y, T=p["T"], workspace=layer.ws_f)
+        bq.qlora_linear_bwd(dy, x, p["T"], p["q"], p["A"], p["B"], layer.alpha, dx=dx, dA=p["dA"], dB=p["dB"],
+                            workspace=layer.ws_b)
+
+    flops = layer_flops([("gate_proj", p["N"], p["K"])], layer.M, layer.r)
+    ms16 = row_ms(lambda: fwd_bwd(x16, dy16, y16, dx16))
+    msb = row_ms(lambda: fwd_bwd(p["x"], p["dy"], p["y"], p["dx"]))
+    return {"shape": [p["N"], p["K"]], "tokens": layer.M, "TFLOP/s_f16": flops / (ms16 / 1e3) / 1e12,
+            "TFLOP/s_bf16": flops / (msb / 1e3) / 1e12, "ms_f16": ms16, "ms_bf16": msb,
+            "timing": "fwd+bwd of one projection as a graph, L2 flushed between replays"}
+
+
 def measure_export_rows(dev, row_ms, hbm):
     """The selected-row embedding decode and the merged-weight export, each one call timed
     as a replayed graph with L2 flushed between replays; GB/s of algorithmic bytes."""
@@ -992,6 +1015,7 @@ def main():
     export_rows = measure_export_rows(dev, row_ms, hbm)
     no_dq = measure_no_double_quant(layer, row_ms)
     small_m = measure_small_m(layer, row_ms, hbm)
+    f16_profile = measure_f16_profile(layer, row_ms)
     fp32_576 = measure_fp32_576(dev, row_ms)
 
     e2e = None
@@ -1077,6 +1101,7 @@ def main():
                          "GB/s_in_step_events": q_gbs},
             "no_double_quant": no_dq,
             "small_m_forward": small_m,
+            "f16_profile": f16_profile,
             "fp32_576": fp32_576,
             "embedding": export_rows["embedding"],
             "merge": export_rows["merge"],

@@ -19,7 +19,7 @@ NF4_OK, NF4_ERR_ARG, NF4_ERR_SHAPE, NF4_ERR_ALIGN, NF4_ERR_DTYPE = 0, 1, 2, 3, 4
 NF4_ERR_NONFINITE, NF4_ERR_CORRUPT, NF4_ERR_CUDA, NF4_ERR_TIMEOUT, NF4_ERR_WORKSPACE = 5, 6, 7, 8, 9
 NF4_ERR_TOO_LARGE = 10
 NOALLOC_MAX_NUMEL = 1 << 26
-NF4_F32, NF4_BF16 = 0, 1
+NF4_F32, NF4_BF16, NF4_F16 = 0, 1, 2
 SCALE_LORA, SCALE_RSLORA = 0, 1
 
 ENTRY_POINTS = (
@@ -130,6 +130,8 @@ def _dtype_code(dt: torch.dtype) -> int:
         return NF4_F32
     if dt == torch.bfloat16:
         return NF4_BF16
+    if dt == torch.float16:
+        return NF4_F16
     raise TypeError(f"unsupported dtype {dt}")
 
 

@@ -263,15 +263,18 @@ nf4_status check_linear(int64_t M, int64_t N, int64_t K, int32_t rank, float alp
   if (rank < 1 || rank > 256 || rank > N || rank > K) return NF4_ERR_ARG;
   if (!std::isfinite(alpha)) return NF4_ERR_ARG;
   if (mode != QLORA_SCALE_LORA && mode != QLORA_SCALE_RSLORA) return NF4_ERR_ARG;
-  if (compute != NF4_F32 && compute != NF4_BF16) return NF4_ERR_DTYPE;
-  if (compute == NF4_BF16 && (K % 64 != 0 || N % 8 != 0)) return NF4_ERR_SHAPE;
+  if (compute != NF4_F32 && compute != NF4_BF16 && compute != NF4_F16) return NF4_ERR_DTYPE;
+  if (compute != NF4_F32 && (K % 64 != 0 || N % 8 != 0)) return NF4_ERR_SHAPE;
   *s_out = (mode == QLORA_SCALE_LORA)
                ? alpha / static_cast<float>(rank)
                : static_cast<float>(static_cast<double>(alpha) / std::sqrt(static_cast<double>(rank)));
   return NF4_OK;
 }
 
-bool small_m(int64_t M, nf4_dtype cd) { return cd == NF4_BF16 && M >= 1 && M <= kStreamMaxM; }
+// The two 16-bit compute dtypes run on the tensor cores; NF4_F32 on the CUDA cores.
+bool is16(nf4_dtype cd) { return cd == NF4_BF16 || cd == NF4_F16; }
+
+bool small_m(int64_t M, nf4_dtype cd) { return is16(cd) && M >= 1 && M <= kStreamMaxM; }
 
 // Workspace layouts.  bwd: G fp32 [M, r], then whatever the selected path needs.
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
@@ -279,7 +282,7 @@ size_t fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
     LinearArgs la{M, N, K, r, 0.0f, Nf4View{}};
     return stream_fwd_ws_bytes(&la, 1);
   }
-  if (cd == NF4_BF16) return tc_fwd_ws_bytes(M, N, K, r);
+  if (is16(cd)) return tc_fwd_ws_bytes(M, N, K, r);
   return 0;
 }
 
@@ -314,7 +317,7 @@ size_t batch_ws(int64_t M, int32_t count, const qlora_fwd_item* it, nf4_dtype cd
 }
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
   size_t b = a256(sizeof(float) * static_cast<size_t>(M) * r);
-  if (cd == NF4_BF16) b += tc_bwd_ws_bytes(M, N, K, r);
+  if (is16(cd)) b += tc_bwd_ws_bytes(M, N, K, r);
   return b;
 }
 
@@ -383,7 +386,7 @@ nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel, const n
 
 nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream) {
   if (w == nullptr || y == nullptr) return NF4_ERR_ARG;
-  if (out_dtype != NF4_F32 && out_dtype != NF4_BF16) return NF4_ERR_DTYPE;
+  if (out_dtype != NF4_F32 && out_dtype != NF4_BF16 && out_dtype != NF4_F16) return NF4_ERR_DTYPE;
   nf4_status st = check_tensor(w, w->numel);
   if (st != NF4_OK) return st;
   if (!aligned16(y)) return NF4_ERR_ALIGN;
@@ -453,12 +456,12 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
     int* status = nullptr;
     if ((st = device_status_ptr(&status)) != NF4_OK) return st;
     const StreamItem item{a, x, A, B, y, T_out};
-    return from_cuda(stream_forward(&item, 1, ws, status, cs));
+    return from_cuda(stream_forward(&item, 1, compute == NF4_F16, ws, status, cs));
   }
-  if (compute == NF4_BF16) {
+  if (is16(compute)) {
     int* status = nullptr;
     if ((st = device_status_ptr(&status)) != NF4_OK) return st;
-    return from_cuda(tc_forward(a, x, A, B, y, T_out, ws, status, cs));
+    return from_cuda(tc_forward(a, compute == NF4_F16, x, A, B, y, T_out, ws, status, cs));
   }
   const float* xf = static_cast<const float*>(x);
   cudaError_t e = launch_lora_down(a, xf, A, T_out, cs);
@@ -500,7 +503,7 @@ nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item
         group[i] = StreamItem{LinearArgs{M, it.N, it.K, it.rank, s[g0 + i], view_of(it.W)}, it.x, it.A, it.B, it.y,
                               it.T_out};
       }
-      const cudaError_t e = stream_forward(group, n, ws, status, cs);
+      const cudaError_t e = stream_forward(group, n, compute == NF4_F16, ws, status, cs);
       if (e != cudaSuccess) return NF4_ERR_CUDA;
     }
     return NF4_OK;
@@ -539,11 +542,11 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
   }
   LinearArgs a{M, N, K, rank, s, view_of(W)};
   float* G = static_cast<float*>(ws);
-  if (compute == NF4_BF16) {
+  if (is16(compute)) {
     int* status = nullptr;
     if ((st = device_status_ptr(&status)) != NF4_OK) return st;
     void* tc_ws = static_cast<char*>(ws) + a256(sizeof(float) * static_cast<size_t>(M) * rank);
-    return from_cuda(tc_backward(a, dy, x, T, A, B, dx, dA, dB, G, tc_ws, status, cs));
+    return from_cuda(tc_backward(a, compute == NF4_F16, dy, x, T, A, B, dx, dA, dB, G, tc_ws, status, cs));
   }
   const float* dyf = static_cast<const float*>(dy);
   cudaError_t e = launch_lora_g(a, dyf, B, G, cs);

@@ -11,6 +11,8 @@
 // (K-major, N = r rounded up to 16); the fp32 accumulator lives in TMEM.  Slices
 // write partial sums that a second kernel adds in a fixed order (deterministic,
 // no atomics) and scales.
+#include <cuda_fp16.h>
+
 #include "linear_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -41,6 +43,7 @@ struct SkinnyParams {
   float* partial;   // [nsplit][rows][r]
   int* status;
   int ctas;         // tiles * nsplit: this pass's CTAs
+  int f16;          // operands are IEEE half (else bf16)
 };
 
 // One launch runs one or two independent passes: CTAs [0, p0.ctas) take the first,
@@ -133,7 +136,7 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CU
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kRowsT, p.n_mma, p.a_mn_major ? 1u : 0u);
+      const uint32_t idesc = idesc_16(kRowsT, p.n_mma, p.a_mn_major ? 1u : 0u, p.f16 ? 1u : 0u);
       bool ok = true;
       int s = 0;
       uint32_t ph = 0;
@@ -191,9 +194,9 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CU
 }
 
 // out = scale * sum over slices (fixed order), for up to two passes in one launch.
-// Optional outputs: f32 [rows][r] (or transposed [r][rows] when f32_t), bf16(scale_b * v)
-// [rows][rp] zero-padded, bf16(v) transposed [nq][ldt] (entries past rows / r must
-// already be zero).
+// Optional outputs: f32 [rows][r] (or transposed [r][rows] when f32_t), T16(scale_b * v)
+// [rows][rp] zero-padded, T16(v) transposed [nq][ldt] (entries past rows / r must
+// already be zero); T16 is IEEE half when f16, else bf16.
 struct FinishJob {
   const float* partial;
   int nsplit;
@@ -202,13 +205,19 @@ struct FinishJob {
   float scale;
   float* f32;
   int f32_t;
-  __nv_bfloat16* b_rows;
+  void* b_rows;
   int rp;
   float scale_b;
-  __nv_bfloat16* b_t;
+  void* b_t;
   int64_t ldt;
   unsigned first_block;
+  int f16;
 };
+
+__device__ __forceinline__ void put16(void* base, int64_t i, float v, int f16) {
+  if (f16) static_cast<__half*>(base)[i] = __float2half_rn(v);
+  else static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+}
 struct FinishJobs {
   FinishJob job[2];
   int n;
@@ -231,9 +240,9 @@ __global__ void finish_partials(const FinishJobs jobs) {
       if (f.f32_t) f.f32[static_cast<int64_t>(j) * f.rows + row] = f.scale * v;
       else f.f32[row * f.r + j] = f.scale * v;
     }
-    if (f.b_t) f.b_t[static_cast<int64_t>(j) * f.ldt + row] = __float2bfloat16_rn(v);
+    if (f.b_t) put16(f.b_t, static_cast<int64_t>(j) * f.ldt + row, v, f.f16);
   }
-  if (f.b_rows) f.b_rows[row * f.rp + j] = __float2bfloat16_rn(j < f.r ? f.scale_b * v : 0.0f);
+  if (f.b_rows) put16(f.b_rows, row * f.rp + j, j < f.r ? f.scale_b * v : 0.0f, f.f16);
 }
 
 int nq_of(int r) { return (r + 15) / 16 * 16; }
@@ -280,12 +289,10 @@ size_t partial_bytes(int64_t rows, int64_t red, int r) {
 bool setup_pass(const AdapterPassArgs& a, int target, int* status, SkinnyParams* p, CUtensorMap* tx, CUtensorMap* tq) {
   const Plan pl = plan(a.rows, a.red, target);
   const int nq = nq_of(a.r);
-  bool ok = a.mn_major ? make_map(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.x_inner, a.x_outer, 2 * a.x_inner, 64,
-                                  64, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : make_map(tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.X, a.x_inner, a.x_outer, 2 * a.x_inner, 64,
-                                  kRowsT, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.Q, a.q_cols, nq, 2 * a.q_cols, 64, nq,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+  const CUtensorMapDataType dt = a.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = a.mn_major ? make_map(tx, dt, a.X, a.x_inner, a.x_outer, 2 * a.x_inner, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : make_map(tx, dt, a.X, a.x_inner, a.x_outer, 2 * a.x_inner, 64, kRowsT, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(tq, dt, a.Q, a.q_cols, nq, 2 * a.q_cols, 64, nq, CU_TENSOR_MAP_SWIZZLE_128B);
   *p = SkinnyParams{};
   p->rows = a.rows;
   p->tiles = pl.tiles;
@@ -300,6 +307,7 @@ bool setup_pass(const AdapterPassArgs& a, int target, int* status, SkinnyParams*
   p->partial = a.partial;
   p->status = status;
   p->ctas = pl.tiles * pl.nsplit;
+  p->f16 = a.f16;
   return ok;
 }
 
@@ -317,6 +325,7 @@ FinishJob finish_job(const AdapterPassArgs& a, const SkinnyParams& p) {
   f.scale_b = a.scale_b;
   f.b_t = a.b_t;
   f.ldt = a.ldt;
+  f.f16 = a.f16;
   return f;
 }
 

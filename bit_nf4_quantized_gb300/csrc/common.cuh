@@ -153,8 +153,9 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
 size_t quantize_ws_bytes(int64_t numel, int dq);
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st);
 struct PrepJobs;
-// quant.cu: the bf16 decode of w into y and `prep_ctas` CTAs of staging jobs, one launch.
-cudaError_t launch_decode_with_prep(const Nf4View& w, __nv_bfloat16* y, const PrepJobs& jobs, unsigned prep_ctas,
+// quant.cu: the 16-bit decode of w into y (IEEE half when f16, else bf16) and `prep_ctas`
+// CTAs of staging jobs, one launch.
+cudaError_t launch_decode_with_prep(const Nf4View& w, void* y, bool f16, const PrepJobs& jobs, unsigned prep_ctas,
                                     cudaStream_t st);
 
 // ---- export.cu: selected embedding rows and the merged LoRA weight ------------

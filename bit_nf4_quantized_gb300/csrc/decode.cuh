@@ -1,12 +1,42 @@
-// Register-table decode of packed NF4 codes to bf16, shared by the dequantize kernel
-// and the tensor-core GEMM.  For a block with scale a', entry q of the table is
-// bf16(nf4[q] * a') -- the fp32 product rounded once -- so the decoded values are
-// exactly what nf4_dequantize writes for bf16 output.
+// Register-table decode of packed NF4 codes to 16-bit values (bf16, or IEEE half for the
+// FP16 profile), shared by the dequantize, selected-row and small-M forward kernels.  For a
+// block with scale a', entry q of the table is T16(nf4[q] * a') -- the fp32 product rounded
+// once -- so the decoded values are exactly what nf4_dequantize writes for that output type.
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
 namespace qnf4 {
+
+// Two floats rounded to nearest even and packed, the first in the low half.
+template <typename T16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// One float rounded to nearest even, stored as T16.
+__device__ __forceinline__ void store16(__nv_bfloat16* p, int64_t i, float v) { p[i] = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store16(__half* p, int64_t i, float v) { p[i] = __float2half_rn(v); }
+
+// A 16-bit value (bf16 or half bits in the low half of `bits`) as a float.
+template <typename T16>
+__device__ __forceinline__ float from16(uint32_t bits);
+template <>
+__device__ __forceinline__ float from16<__nv_bfloat16>(uint32_t bits) { return __uint_as_float(bits << 16); }
+template <>
+__device__ __forceinline__ float from16<__half>(uint32_t bits) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xFFFFu)));
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -14,23 +44,20 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Scaled lookup table of one block: entry i = bf16(nf4[i] * a'), split into low bytes
+// Scaled lookup table of one block: entry i = T16(nf4[i] * a'), split into low bytes
 // (L, 4 registers of 4 entries) and high bytes (H), so prmt can index it by nibble.
+template <typename T16 = __nv_bfloat16>
 __device__ __forceinline__ void build_lut(float a, uint32_t (&L)[4], uint32_t (&H)[4]) {
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const __nv_bfloat162 p0 = __floats2bfloat162_rn(__fmul_rn(nf4_value(4 * t + 0), a),
-                                                    __fmul_rn(nf4_value(4 * t + 1), a));
-    const __nv_bfloat162 p1 = __floats2bfloat162_rn(__fmul_rn(nf4_value(4 * t + 2), a),
-                                                    __fmul_rn(nf4_value(4 * t + 3), a));
-    const uint32_t u0 = *reinterpret_cast<const uint32_t*>(&p0);
-    const uint32_t u1 = *reinterpret_cast<const uint32_t*>(&p1);
+    const uint32_t u0 = pack2<T16>(__fmul_rn(nf4_value(4 * t + 0), a), __fmul_rn(nf4_value(4 * t + 1), a));
+    const uint32_t u1 = pack2<T16>(__fmul_rn(nf4_value(4 * t + 2), a), __fmul_rn(nf4_value(4 * t + 3), a));
     L[t] = prmt(u0, u1, 0x6420u);
     H[t] = prmt(u0, u1, 0x7531u);
   }
 }
 
-// Eight weights of one packed word to four bf16x2 registers in element order.  The
+// Eight weights of one packed word to four registers of two 16-bit values, in element order.  The
 // word's nibbles, low first, are elements 1 0 3 2 5 4 7 6 (element 2i is the high nibble
 // of byte i); the final byte interleave puts them back in order.  The selectors (the low 3
 // bits of each code, and bit 3 choosing the half table) are formed once for the whole word;

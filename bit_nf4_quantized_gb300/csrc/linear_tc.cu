@@ -34,6 +34,8 @@
 // NF4_ERR_TIMEOUT in the status word and the CTA winds down, freeing its TMEM.
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
 #include "linear_tc.cuh"
 #include "prep.cuh"
 #include "tc_ptx.cuh"
@@ -78,7 +80,8 @@ struct GemmParams {
   int pairs_f;         // ceil(tiles_f / 2): feature-tile pairs; an odd count leaves the last pair's
                        // second tile past F (loads read zeros, the epilogue stores nothing)
   int f_fast;          // pair order: 1 = feature pairs vary fastest, 0 = token tiles
-  __nv_bfloat16* out;  // [M, F]
+  int f16;             // operands and output are IEEE half (else bf16)
+  void* out;           // [M, F] 16-bit
   int* status;
   // work units: tiles [0, full_units) whole, then the remaining tiles (fewer than one
   // round of clusters) in `split` parts along the contraction, `chunk` steps each (the
@@ -257,8 +260,8 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (even CTA) ----------------
-      const uint32_t idesc_main = idesc_bf16(kCluster * kTileF, kTileT, p.mode == 1 ? 1u : 0u);
-      const uint32_t idesc_slab = idesc_bf16(kCluster * kTileF, kTileT, 0u);
+      const uint32_t idesc_main = idesc_16(kCluster * kTileF, kTileT, p.mode == 1 ? 1u : 0u, p.f16 ? 1u : 0u);
+      const uint32_t idesc_slab = idesc_16(kCluster * kTileF, kTileT, 0u, p.f16 ? 1u : 0u);
       bool ok = true;
       Ring c;
       for (int64_t lt = 0; ok && unit_at(lt) < p.total_units; ++lt) {
@@ -397,9 +400,10 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(__uint_as_float(v[j]));
+              const float f = __uint_as_float(v[j]);
+              const uint16_t o = p.f16 ? __half_as_ushort(__float2half_rn(f)) : __bfloat16_as_ushort(__float2bfloat16_rn(f));
               asm volatile("st.shared.b16 [%0], %1;" ::"r"(box + static_cast<uint32_t>(((h + j) * kTileF + lrow) * 2)),
-                           "h"(*reinterpret_cast<const uint16_t*>(&o))
+                           "h"(o)
                            : "memory");
             }
           }
@@ -468,9 +472,9 @@ void split_tail(GemmParams* p, int64_t pairs, int64_t clusters) {
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& w, const CUtensorMap& tok,
                         const CUtensorMap& slab_f, const CUtensorMap& slab_t, cudaStream_t st) {
-  CUtensorMap out;   // [M][F] bf16, stored in [32 tokens][128 features] boxes
-  if (!make_map(&out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, p.F, p.M, 2 * p.F, kTileF, kOutRows,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+  CUtensorMap out;   // [M][F] 16-bit, stored in [32 tokens][128 features] boxes
+  if (!make_map(&out, p.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, p.F, p.M,
+                2 * p.F, kTileF, kOutRows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -521,12 +525,12 @@ PrepJob zero_flags_job(void* flags) {
   return j;
 }
 
-// The weight decoded to bf16 [N][K] for this call (bit-exact with nf4_dequantize), in the
+// The weight decoded to 16 bits [N][K] for this call (bit-exact with nf4_dequantize), in the
 // same launch as the call's operand staging (extra CTAs run the prep jobs).
-cudaError_t decode_weight(const LinearArgs& a, void* wb, const PrepBuilder& prep, cudaStream_t st) {
+cudaError_t decode_weight(const LinearArgs& a, bool f16, void* wb, const PrepBuilder& prep, cudaStream_t st) {
   if (!prep.ok()) return cudaErrorInvalidValue;
   KernelTimer timer(NF4_TIME_WEIGHT_DECODE, st);
-  return launch_decode_with_prep(a.W, static_cast<__nv_bfloat16*>(wb), prep.jobs(), prep.ctas(), st);
+  return launch_decode_with_prep(a.W, wb, f16, prep.jobs(), prep.ctas(), st);
 }
 
 // Workspace layouts (every part 1024-byte aligned).  `part` holds the skinny passes'
@@ -566,8 +570,9 @@ struct BwdWs {
   }
 };
 
-GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
+GemmParams base_params(const LinearArgs& a, bool f16, int mode, void* out, int* status) {
   GemmParams p{};
+  p.f16 = f16 ? 1 : 0;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
@@ -582,7 +587,7 @@ GemmParams base_params(const LinearArgs& a, int mode, void* out, int* status) {
   // each round of clusters re-reads the whole operand along the fast dimension: run the
   // feature pairs fastest only when the weight panel set (F rows) is smaller than the tokens
   p.f_fast = p.F < a.M ? 1 : 0;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
   p.status = status;
   return p;
 }
@@ -595,17 +600,18 @@ size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return BwdWs(M,
 
 // Forward: W in bf16 with prep (A and B in bf16) -> T = x A^T (skinny tcgen05) ->
 // T and bf16(s T) -> GEMM with the (s T) B^T slab.
-cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y, float* T,
-                       void* ws, int* status, cudaStream_t st) {
+cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float* A, const float* B, void* y,
+                       float* T, void* ws, int* status, cudaStream_t st) {
   const FwdWs L(a.M, a.N, a.K, a.r);
   char* w = static_cast<char*>(ws);
-  auto* sTp = reinterpret_cast<__nv_bfloat16*>(w + L.sTp);
-  auto* Bp = reinterpret_cast<__nv_bfloat16*>(w + L.Bp);
-  auto* Aq = reinterpret_cast<__nv_bfloat16*>(w + L.Aq);
+  void* sTp = w + L.sTp;
+  void* Bp = w + L.Bp;
+  void* Aq = w + L.Aq;
   auto* part = reinterpret_cast<float*>(w + L.part);
-  auto* wb = reinterpret_cast<__nv_bfloat16*>(w + L.wb);
+  void* wb = w + L.wb;
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
-  PrepBuilder prep;
+  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  PrepBuilder prep(f16);
   {
     PrepJob j{};
     j.kind = kStageRowsDirect;   // A as the skinny pass's Q: [nq][K]
@@ -626,9 +632,9 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
     prep.add(b);
     prep.add(zero_flags_job(w + L.flags));
   }
-  cudaError_t e = decode_weight(a, wb, prep, st);
+  cudaError_t e = decode_weight(a, f16, wb, prep, st);
   if (e != cudaSuccess) return e;
-  {  // T = x A^T: rows M, reduction over K along x's rows; T (fp32) and bf16(s T) for the slab
+  {  // T = x A^T: rows M, reduction over K along x's rows; T (fp32) and 16-bit s T for the slab
     AdapterPassArgs t{};
     t.X = x;
     t.x_inner = a.K;
@@ -644,19 +650,16 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
     t.b_rows = sTp;
     t.rp = rp;
     t.scale_b = a.s;
+    t.f16 = f16 ? 1 : 0;
     if ((e = adapter_run(&t, 1, status, st)) != cudaSuccess) return e;
   }
   CUtensorMap wm, tok, slab_f, slab_t;
-  bool ok = make_map(&wm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb, a.K, a.N, 2 * a.K, kSub, kTileF,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.K, a.M, 2 * a.K, kSub, kHalfT,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_f, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, rp, a.N, 2 * rp, kSub, kTileF,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sTp, rp, a.M, 2 * rp, kSub, kHalfT,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = make_map(&wm, dt16, wb, a.K, a.N, 2 * a.K, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tok, dt16, x, a.K, a.M, 2 * a.K, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_f, dt16, Bp, rp, a.N, 2 * rp, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_t, dt16, sTp, rp, a.M, 2 * rp, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  GemmParams gp = base_params(a, 0, y, status);
+  GemmParams gp = base_params(a, f16, 0, y, status);
   gp.part_ws = part;
   gp.part_tickets = reinterpret_cast<int*>(w + L.flags);
   return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
@@ -665,21 +668,22 @@ cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const
 // Backward: W in bf16 with prep (B^T, T^T, zeroed G^T, A^T in bf16) -> G = dY B ->
 // G, bf16(s G), bf16(G)^T -> dB = s dY^T T -> GEMM for dX with the (s G) A slab ->
 // dA = s G^T x.
-cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, const float* T, const float* A,
-                        const float* B, void* dx, float* dA, float* dB, float* G, void* ws, int* status,
-                        cudaStream_t st) {
+cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const void* x, const float* T,
+                        const float* A, const float* B, void* dx, float* dA, float* dB, float* G, void* ws,
+                        int* status, cudaStream_t st) {
   const BwdWs L(a.M, a.N, a.K, a.r);
   char* w = static_cast<char*>(ws);
-  auto* sGp = reinterpret_cast<__nv_bfloat16*>(w + L.sGp);
-  auto* ApT = reinterpret_cast<__nv_bfloat16*>(w + L.ApT);
-  auto* Bt = reinterpret_cast<__nv_bfloat16*>(w + L.Bt);
-  auto* Tt = reinterpret_cast<__nv_bfloat16*>(w + L.Tt);
-  auto* Gt = reinterpret_cast<__nv_bfloat16*>(w + L.Gt);
+  void* sGp = w + L.sGp;
+  void* ApT = w + L.ApT;
+  void* Bt = w + L.Bt;
+  void* Tt = w + L.Tt;
+  void* Gt = w + L.Gt;
   auto* part = reinterpret_cast<float*>(w + L.part);
-  auto* wb = reinterpret_cast<__nv_bfloat16*>(w + L.wb);
+  void* wb = w + L.wb;
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
   const int64_t Mp = pad8(a.M);
-  PrepBuilder prep;
+  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  PrepBuilder prep(f16);
   {
     PrepJob j{};
     j.kind = kStageTransposed;   // B^T: [nq][N]
@@ -712,7 +716,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
     prep.add(c);
     prep.add(zero_flags_job(w + L.flags));
   }
-  cudaError_t e = decode_weight(a, wb, prep, st);
+  cudaError_t e = decode_weight(a, f16, wb, prep, st);
   if (e != cudaSuccess) return e;
   {  // one launch for G = dY B (rows M, reduction over N along dY's rows; G, bf16(s G), bf16(G)^T)
      // and dB = s dY^T T (rows N, reduction over M down dY's columns), then one for both finishes
@@ -747,20 +751,17 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
     d.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(part) + adapter_partial_bytes(a.M, a.N, a.r));
     d.scale = a.s;
     d.f32 = dB;
+    g.f16 = d.f16 = f16 ? 1 : 0;
     if ((e = adapter_run(pa, 2, status, st)) != cudaSuccess) return e;
   }
   CUtensorMap wm, tok, slab_f, slab_t;
   // W [N][K] read as 64 features x 64 rows n (MN-major A: the features are the MMA's M)
-  bool ok = make_map(&wm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wb, a.K, a.N, 2 * a.K, kSub, kSub,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tok, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_f, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ApT, rp, a.K, 2 * rp, kSub, kTileF,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sGp, rp, a.M, 2 * rp, kSub, kHalfT,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = make_map(&wm, dt16, wb, a.K, a.N, 2 * a.K, kSub, kSub, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tok, dt16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_f, dt16, ApT, rp, a.K, 2 * rp, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_t, dt16, sGp, rp, a.M, 2 * rp, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
-  GemmParams gp = base_params(a, 1, dx, status);
+  GemmParams gp = base_params(a, f16, 1, dx, status);
   gp.part_ws = part;
   gp.part_tickets = reinterpret_cast<int*>(w + L.flags);
   if ((e = launch_gemm(gp, wm, tok, slab_f, slab_t, st)) != cudaSuccess) return e;
@@ -779,6 +780,7 @@ cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, cons
   da.scale = a.s;
   da.f32 = dA;
   da.f32_t = 1;
+  da.f16 = f16 ? 1 : 0;
   return adapter_run(&da, 1, status, st);
 }
 

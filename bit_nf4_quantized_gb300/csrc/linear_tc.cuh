@@ -9,9 +9,10 @@ namespace qnf4 {
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
 
-cudaError_t tc_forward(const LinearArgs& a, const void* x, const float* A, const float* B, void* y,
+// f16: the operands and outputs are IEEE half (the FP16 profile) instead of bf16.
+cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float* A, const float* B, void* y,
                        float* T, void* ws, int* status, cudaStream_t st);
-cudaError_t tc_backward(const LinearArgs& a, const void* dy, const void* x, const float* T,
+cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const void* x, const float* T,
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G,
                         void* ws, int* status, cudaStream_t st);
 
@@ -23,28 +24,30 @@ constexpr int kStreamMaxM = 16;
 constexpr int kStreamMaxGroup = 8;
 struct StreamItem {
   LinearArgs a;
-  const void* x;     // bf16 [M, K]
+  const void* x;     // 16-bit [M, K]
   const float* A;    // [r, K]
   const float* B;    // [N, r]
-  void* y;           // bf16 [M, N]
+  void* y;           // 16-bit [M, N]
   float* T;          // [M, r]
 };
 size_t stream_fwd_ws_bytes(const LinearArgs* a, int n);
-cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status, cudaStream_t st);
+// f16: x, y and every tensor-core operand are IEEE half (the FP16 profile) instead of bf16.
+cudaError_t stream_forward(const StreamItem* items, int n, bool f16, void* ws, int* status, cudaStream_t st);
 
 // adapter_tc.cu: skinny tcgen05 products Out[rows, r] = X[rows, red] . Q[red, r] for the
-// rank-r contractions.  X is bf16 row-major with `x_inner` columns (the reduction runs
-// along its rows when mn_major == false, down its columns otherwise); Q is bf16
-// [nq][q_cols] (nq = r rounded up to 16).  Reduction slices write partial sums to
-// `partial` (adapter_partial_bytes) that a second launch adds in a fixed order, writing:
+// rank-r contractions.  X is 16-bit (T16: bf16, or IEEE half when f16) row-major with
+// `x_inner` columns (the reduction runs along its rows when mn_major == false, down its
+// columns otherwise); Q is T16 [nq][q_cols] (nq = r rounded up to 16).  Reduction slices
+// write partial sums to `partial` (adapter_partial_bytes) that a second launch adds in a
+// fixed order, writing:
 //   f32 = scale * sum as [rows][r] (or [r][rows] when f32_t), if f32 is set;
-//   bf16(scale_b * sum) as [rows][rp], zero past r, if b_rows is set;
-//   bf16(sum) as [r][ldt] (rows r.. of a [nq][ldt] buffer untouched), if b_t is set.
+//   T16(scale_b * sum) as [rows][rp], zero past r, if b_rows is set;
+//   T16(sum) as [r][ldt] (rows r.. of a [nq][ldt] buffer untouched), if b_t is set.
 struct AdapterPassArgs {
   const void* X;
   int64_t x_inner, x_outer;
   bool mn_major;
-  const __nv_bfloat16* Q;
+  const void* Q;
   int64_t q_cols;
   int r;
   int64_t rows, red;
@@ -52,11 +55,12 @@ struct AdapterPassArgs {
   float scale;
   float* f32;
   int f32_t;
-  __nv_bfloat16* b_rows;
+  void* b_rows;
   int rp;
   float scale_b;
-  __nv_bfloat16* b_t;
+  void* b_t;
   int64_t ldt;
+  int f16;
 };
 int adapter_nq(int r);
 size_t adapter_partial_bytes(int64_t rows, int64_t red, int r);

@@ -1,18 +1,22 @@
-// Staging of the per-call operands of the bf16 QLoRA linear: jobs built on the host
-// (PrepBuilder, prep.cu), run by extra CTAs of the weight-decode launch (prep_cta).
+// Staging of the per-call operands of the 16-bit QLoRA linear (bf16, or IEEE half for the
+// FP16 profile): jobs built on the host (PrepBuilder, prep.cu), run by extra CTAs of the
+// weight-decode launch (prep_cta).
 #pragma once
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
 namespace qnf4 {
 
-// Every bf16 job writes rows whose length (`width`, or `cols` for kStageRowsDirect) is a
+// Every 16-bit job writes rows whose length (`width`, or `cols` for kStageRowsDirect) is a
 // multiple of 8, eight outputs per thread; kZeroWords clears a multiple of 4 words.
+// T16 below is the call's 16-bit type (PrepJobs::f16 selects IEEE half over bf16).
 enum PrepKind {
-  kStageRows = 0,         // dst[row][c] = bf16(scale * src[row][c]), c < r; zero up to `width`
-  kStageRowsDirect = 1,   // dst[j][c] = bf16(src[j][c]) for j < r; zero rows up to `width` rows
-  kStageTransposed = 2,   // dst[j][c] = bf16(src[c][j]), j < r, c < cols; rows of `width`
-  kStageColumns = 3,      // dst[c][j] = bf16(src[j][c]) (src rows of `cols`), j < r; rows of `width`
+  kStageRows = 0,         // dst[row][c] = T16(scale * src[row][c]), c < r; zero up to `width`
+  kStageRowsDirect = 1,   // dst[j][c] = T16(src[j][c]) for j < r; zero rows up to `width` rows
+  kStageTransposed = 2,   // dst[j][c] = T16(src[c][j]), j < r, c < cols; rows of `width`
+  kStageColumns = 3,      // dst[c][j] = T16(src[j][c]) (src rows of `cols`), j < r; rows of `width`
   kZeroWords = 4          // fdst[i] = 0 (as 32-bit words)
 };
 
@@ -22,7 +26,7 @@ struct PrepJob {
   int64_t width;
   float scale;
   const float* src;
-  __nv_bfloat16* dst;
+  void* dst;              // 16-bit elements
   float* fdst;
   int64_t cols;
   int64_t count;          // elements (words for kZeroWords) written
@@ -36,6 +40,7 @@ constexpr int kPrepPer = 8;         // outputs per thread: one 16-byte store
 struct PrepJobs {
   PrepJob job[kMaxPrepJobs];
   int n;
+  int f16;                // 16-bit outputs are IEEE half (else bf16)
 };
 
 namespace prep_detail {
@@ -51,13 +56,17 @@ __device__ __forceinline__ void split_index(uint64_t idx, uint64_t width, uint64
   }
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&v)[kPrepPer]) {
+__device__ __forceinline__ uint4 pack8(const float (&v)[kPrepPer], int f16) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i]));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1]));
-    w[i] = lo | (hi << 16);
+    if (f16) {
+      const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -84,26 +93,26 @@ __device__ __forceinline__ void prep_cta(const PrepJobs& p, unsigned cta) {
   float v[kPrepPer];
   uint64_t a, b;
   switch (jb.kind) {
-    case kStageRows: {         // dst[row][c] = bf16(scale * src[row][c]) for c < r, 0 up to width
+    case kStageRows: {         // dst[row][c] = T16(scale * src[row][c]) for c < r, 0 up to width
       split_index(idx, jb.width, &a, &b);
 #pragma unroll
       for (int i = 0; i < kPrepPer; ++i) v[i] = (b + i < r) ? jb.scale * jb.src[a * r + b + i] : 0.0f;
       break;
     }
-    case kStageRowsDirect: {   // dst[j][c] = bf16(src[j][c]) for j < r, 0 for j in [r, width rows)
+    case kStageRowsDirect: {   // dst[j][c] = T16(src[j][c]) for j < r, 0 for j in [r, width rows)
       split_index(idx, jb.cols, &a, &b);
 #pragma unroll
       for (int i = 0; i < kPrepPer; ++i) v[i] = (a < r) ? jb.src[idx + i] : 0.0f;
       break;
     }
-    case kStageTransposed: {   // dst[j][c] = bf16(src[c][j]) for j < r, c < cols; row length width
+    case kStageTransposed: {   // dst[j][c] = T16(src[c][j]) for j < r, c < cols; row length width
       split_index(idx, jb.width, &a, &b);
       const uint64_t cols = static_cast<uint64_t>(jb.cols);
 #pragma unroll
       for (int i = 0; i < kPrepPer; ++i) v[i] = (a < r && b + i < cols) ? jb.src[(b + i) * r + a] : 0.0f;
       break;
     }
-    case kStageColumns: {      // dst[c][j] = bf16(src[j][c]) for j < r; rows of width entries
+    case kStageColumns: {      // dst[c][j] = T16(src[j][c]) for j < r; rows of width entries
       split_index(idx, jb.width, &a, &b);
       const uint64_t cols = static_cast<uint64_t>(jb.cols);
 #pragma unroll
@@ -113,12 +122,15 @@ __device__ __forceinline__ void prep_cta(const PrepJobs& p, unsigned cta) {
     default:
       return;
   }
-  *reinterpret_cast<uint4*>(jb.dst + idx) = pack8(v);
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(jb.dst) + idx) = pack8(v, p.f16);
 }
 
 class PrepBuilder {
  public:
-  PrepBuilder() { jobs_.n = 0; }
+  explicit PrepBuilder(bool f16 = false) {
+    jobs_.n = 0;
+    jobs_.f16 = f16 ? 1 : 0;
+  }
   void add(const PrepJob& job);   // at most kMaxPrepJobs; further jobs, or a job whose row
                                   // length breaks the rule above, make ok() false
   bool ok() const { return !bad_; }

@@ -351,9 +351,9 @@ __device__ __forceinline__ void decode_cta(const Nf4View& w, Tout* __restrict__ 
     const float a = sc[u];
     if (c0 + 1024 <= n) {
       const uint32_t words[4] = {pk[u].x, pk[u].y, pk[u].z, pk[u].w};
-      if (sizeof(Tout) == 2) {
+      if constexpr (sizeof(Tout) == 2) {
         uint32_t L[4], H[4];
-        build_lut(a, L, H);
+        build_lut<Tout>(a, L, H);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint32_t o[4];
@@ -402,8 +402,8 @@ __device__ __forceinline__ void decode_cta(const Nf4View& w, Tout* __restrict__ 
         const uint8_t byte = w.packed[e >> 1];
         const int q = (e & 1) ? (byte & 15) : (byte >> 4);
         const float v = __fmul_rn(tabs.nf4[q], a);
-        if (sizeof(Tout) == 2) reinterpret_cast<__nv_bfloat16*>(y)[e] = __float2bfloat16_rn(v);
-        else reinterpret_cast<float*>(y)[e] = v;
+        if constexpr (sizeof(Tout) == 2) store16(y, e, v);
+        else y[e] = v;
       }
     }
   }
@@ -415,12 +415,12 @@ nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
   decode_cta<Tout, kDQ>(w, y, tabs, blockIdx.x);
 }
 
-// The bf16 decode of the linear's weight and that call's operand staging in one launch:
+// The 16-bit decode of the linear's weight and that call's operand staging in one launch:
 // CTAs below `decode_ctas` decode, the rest run the prep jobs.
-template <bool kDQ>
+template <typename T16, bool kDQ>
 __global__ void __launch_bounds__(kDeqThreads)
-nf4_decode_prep(Nf4View w, __nv_bfloat16* __restrict__ y, DecodeTables tabs, PrepJobs jobs, unsigned decode_ctas) {
-  if (blockIdx.x < decode_ctas) decode_cta<__nv_bfloat16, kDQ>(w, y, tabs, blockIdx.x);
+nf4_decode_prep(Nf4View w, T16* __restrict__ y, DecodeTables tabs, PrepJobs jobs, unsigned decode_ctas) {
+  if (blockIdx.x < decode_ctas) decode_cta<T16, kDQ>(w, y, tabs, blockIdx.x);
   else prep_cta(jobs, blockIdx.x - decode_ctas);
 }
 
@@ -489,24 +489,36 @@ cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStrea
   if (od == NF4_F32) {
     if (w.dq) e = launch_pdl(nf4_decode<float, true>, grid, dim3(kDeqThreads), 0, st, 1, w, static_cast<float*>(y), dt);
     else e = launch_pdl(nf4_decode<float, false>, grid, dim3(kDeqThreads), 0, st, 1, w, static_cast<float*>(y), dt);
-  } else {
+  } else if (od == NF4_BF16) {
     auto* yb = static_cast<__nv_bfloat16*>(y);
     if (w.dq) e = launch_pdl(nf4_decode<__nv_bfloat16, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt);
     else e = launch_pdl(nf4_decode<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt);
+  } else {
+    auto* yh = static_cast<__half*>(y);
+    if (w.dq) e = launch_pdl(nf4_decode<__half, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yh, dt);
+    else e = launch_pdl(nf4_decode<__half, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yh, dt);
   }
   note_launch();
   return e;
 }
 
-cudaError_t launch_decode_with_prep(const Nf4View& w, __nv_bfloat16* y, const PrepJobs& jobs, unsigned prep_ctas,
+cudaError_t launch_decode_with_prep(const Nf4View& w, void* y, bool f16, const PrepJobs& jobs, unsigned prep_ctas,
                                     cudaStream_t st) {
   const int64_t ctas = (w.numel + kDeqPerCta - 1) / kDeqPerCta;
   if (ctas + prep_ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(ctas + prep_ctas));
   const DecodeTables& dt = decode_tables();
   const unsigned dc = static_cast<unsigned>(ctas);
-  const cudaError_t e = w.dq ? launch_pdl(nf4_decode_prep<true>, grid, dim3(kDeqThreads), 0, st, 1, w, y, dt, jobs, dc)
-                             : launch_pdl(nf4_decode_prep<false>, grid, dim3(kDeqThreads), 0, st, 1, w, y, dt, jobs, dc);
+  cudaError_t e;
+  if (f16) {
+    auto* yh = static_cast<__half*>(y);
+    e = w.dq ? launch_pdl(nf4_decode_prep<__half, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yh, dt, jobs, dc)
+             : launch_pdl(nf4_decode_prep<__half, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yh, dt, jobs, dc);
+  } else {
+    auto* yb = static_cast<__nv_bfloat16*>(y);
+    e = w.dq ? launch_pdl(nf4_decode_prep<__nv_bfloat16, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt, jobs, dc)
+             : launch_pdl(nf4_decode_prep<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt, jobs, dc);
+  }
   note_launch();
   return e;
 }

@@ -43,6 +43,9 @@
 // timeout sets NF4_ERR_TIMEOUT in the status word and the CTA winds down.
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
+
+#include <cuda_fp16.h>
 
 #include "decode.cuh"
 #include "linear_tc.cuh"
@@ -79,8 +82,8 @@ struct StreamProj {
   const float* nested;
   const float* offset;
   const float* B;          // [N][r] fp32
-  const __nv_bfloat16* sT; // [16][rp64] bf16(s T), written by lora_down_small
-  __nv_bfloat16* y;        // [M][N]
+  const void* sT;          // [16][rp64] 16-bit s T, written by lora_down_small
+  void* y;                 // [M][N] 16-bit
   int64_t N, K;
   int64_t unit0;           // first unit of this projection
   int r, rp64;
@@ -105,7 +108,7 @@ struct StreamParams {
 
 struct StreamMaps {
   CUtensorMap codes[kMaxGroup];   // uint8 [N][K/2], box [128 rows][128 bytes]
-  CUtensorMap x[kMaxGroup];       // bf16 [M][K], box [16][64]
+  CUtensorMap x[kMaxGroup];       // 16-bit [M][K], box [16][64]
 };
 
 struct Pos {
@@ -167,24 +170,27 @@ __device__ __forceinline__ float scale_of(const ScaleIn& in, int dq, const float
   return __fadd_rn(__fmul_rn(dyn8[in.code], in.nested_or_max), in.offset);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 __device__ __forceinline__ uint32_t ld_shared32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
-// D += A (16 x 16, bf16, row) * B (16 x 8, bf16, col), fp32 accumulate, fragments per thread.
+// D += A (16 x 16, row) * B (16 x 8, col), bf16 or (F16) IEEE half operands, fp32 accumulate,
+// fragments per thread.
+template <bool F16>
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-               "{%0, %1, %2, %3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  if constexpr (F16)
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Decoder thread layout.  Warp w (0..15) owns tile rows 16w .. 16w+15; in the mma.sync fragments
@@ -196,9 +202,10 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // of each shared-memory phase on distinct banks.  One table of bf16(nf4[q] * a') serves each
 // thread's 64 weights of one row and block.
 
-template <int NT>   // 8-token MMA tiles: 1 (M <= 8) or 2 (M <= 16)
+template <int NT, typename T16>   // 8-token MMA tiles: 1 (M <= 8) or 2 (M <= 16); bf16 or IEEE half
 __global__ void __launch_bounds__(kThreads, 1)
 nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ StreamParams p) {
+  constexpr bool F16 = sizeof(T16) == 2 && !std::is_same<T16, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -313,7 +320,7 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
       // this unit's tables from the scale inputs loaded one unit ago; the next unit's inputs
       uint32_t Lt[2][4], Ht[2][4];
 #pragma unroll
-      for (int r8 = 0; r8 < 2; ++r8) build_lut(scale_of(nxt[r8], P.dq, dyn8), Lt[r8], Ht[r8]);
+      for (int r8 = 0; r8 < 2; ++r8) build_lut<T16>(scale_of(nxt[r8], P.dq, dyn8), Lt[r8], Ht[r8]);
       if (u + 1 < ub) {
         const Pos nx = advance(p, cur);
         const StreamProj& Q = p.proj[nx.proj];
@@ -334,8 +341,8 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
         decode8(ld_shared32(cb1 + coff[j]), Lt[1], Ht[1], o[1]);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          mma16816(acc[t], o[0][0], o[1][0], o[0][1], o[1][1], xb[t].x, xb[t].y);
-          mma16816(acc[t], o[0][2], o[1][2], o[0][3], o[1][3], xb[t].z, xb[t].w);
+          mma16816<F16>(acc[t], o[0][0], o[1][0], o[0][1], o[1][1], xb[t].x, xb[t].y);
+          mma16816<F16>(acc[t], o[0][2], o[1][2], o[0][3], o[1][3], xb[t].z, xb[t].w);
         }
       }
       __syncwarp();
@@ -344,7 +351,7 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
       if (last) {
         const int64_t row0 = static_cast<int64_t>(cur.tile) * kTileRows;
         if (seg_s0 == 0) {
-          // the LoRA term, s T B^T: bf16(B[row][j]) against bf16(s T)[token][j] of
+          // the LoRA term, s T B^T: T16(B[row][j]) against T16(s T)[token][j] of
           // lora_down_small, 16 ranks per step
           if (!waited) {
             pdl_wait();
@@ -360,14 +367,15 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
 #pragma unroll
               for (int hp = 0; hp < 2; ++hp) {
                 const int jj = j0 + 2 * c + 8 * hp;
-                a[r8][hp] = pack_bf16x2(live && jj < P.r ? __ldg(brow + jj) : 0.0f,
-                                        live && jj + 1 < P.r ? __ldg(brow + jj + 1) : 0.0f);
+                a[r8][hp] = pack2<T16>(live && jj < P.r ? __ldg(brow + jj) : 0.0f,
+                                       live && jj + 1 < P.r ? __ldg(brow + jj + 1) : 0.0f);
               }
             }
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-              const uint32_t* st_row = reinterpret_cast<const uint32_t*>(P.sT + (8 * t + g) * P.rp64 + j0 + 2 * c);
-              mma16816(acc[t], a[0][0], a[1][0], a[0][1], a[1][1], __ldcg(st_row), __ldcg(st_row + 4));
+              const uint32_t* st_row =
+                  reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(P.sT) + (8 * t + g) * P.rp64 + j0 + 2 * c);
+              mma16816<F16>(acc[t], a[0][0], a[1][0], a[0][1], a[1][1], __ldcg(st_row), __ldcg(st_row + 4));
             }
           }
         }
@@ -382,7 +390,7 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   const int m = 8 * t + 2 * c + e;
-                  if (m < p.M) P.y[static_cast<int64_t>(m) * P.N + row] = __float2bfloat16_rn(acc[t][2 * r8 + e]);
+                  if (m < p.M) store16(static_cast<T16*>(P.y), static_cast<int64_t>(m) * P.N + row, acc[t][2 * r8 + e]);
                 }
             }
           }
@@ -441,7 +449,7 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                   const int m = 8 * t + 2 * c + e;
-                  if (m < p.M) P.y[static_cast<int64_t>(m) * P.N + row] = __float2bfloat16_rn(v[4 * t + 2 * r8 + e]);
+                  if (m < p.M) store16(static_cast<T16*>(P.y), static_cast<int64_t>(m) * P.N + row, v[4 * t + 2 * r8 + e]);
                 }
             }
           }
@@ -456,10 +464,10 @@ nf4_stream_fwd(const __grid_constant__ StreamMaps maps, const __grid_constant__ 
 // ---- T = x A^T for the small-M forward ----------------------------------------------------
 
 struct DownItem {
-  const __nv_bfloat16* x;   // [M][K]
+  const void* x;            // 16-bit [M][K]
   const float* A;           // [r][K]
   float* T;                 // [M][r]
-  __nv_bfloat16* sT;        // [16][rp64]
+  void* sT;                 // 16-bit [16][rp64]
   int64_t K;
   int r, rp64;
   float s;
@@ -476,6 +484,13 @@ struct DownParams {
 
 constexpr int kDownThreads = 1024;   // at most two rounds of loads per thread for K <= 16384
 
+template <typename T16>
+__device__ __forceinline__ float round16(float v) {
+  if constexpr (std::is_same<T16, __nv_bfloat16>::value) return round_bf16(v);
+  else return __half2float(__float2half_rn(v));
+}
+
+template <typename T16>
 __global__ void __launch_bounds__(kDownThreads)
 lora_down_small(const __grid_constant__ DownParams p) {
   pdl_wait();         // x is written by the stream's earlier work
@@ -495,17 +510,18 @@ lora_down_small(const __grid_constant__ DownParams p) {
   for (int64_t c = threadIdx.x; c < chunks; c += kDownThreads) {
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(arow) + 2 * c);
     const float4 a1 = __ldg(reinterpret_cast<const float4*>(arow) + 2 * c + 1);
-    const float av[8] = {round_bf16(a0.x), round_bf16(a0.y), round_bf16(a0.z), round_bf16(a0.w),
-                         round_bf16(a1.x), round_bf16(a1.y), round_bf16(a1.z), round_bf16(a1.w)};
+    const float av[8] = {round16<T16>(a0.x), round16<T16>(a0.y), round16<T16>(a0.z), round16<T16>(a0.w),
+                         round16<T16>(a1.x), round16<T16>(a1.y), round16<T16>(a1.z), round16<T16>(a1.w)};
 #pragma unroll
     for (int m = 0; m < kStreamMaxM; ++m) {
       if (m < p.M) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(it.x + static_cast<int64_t>(m) * it.K) + c);
+        const uint4 xv =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(it.x) + static_cast<int64_t>(m) * it.K) + c);
         const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          acc[m] = fmaf(__uint_as_float(w[e] << 16), av[2 * e], acc[m]);
-          acc[m] = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), av[2 * e + 1], acc[m]);
+          acc[m] = fmaf(from16<T16>(w[e]), av[2 * e], acc[m]);
+          acc[m] = fmaf(from16<T16>(w[e] >> 16), av[2 * e + 1], acc[m]);
         }
       }
     }
@@ -529,11 +545,11 @@ lora_down_small(const __grid_constant__ DownParams p) {
     float t = 0.0f;
     for (int w = 0; w < kDownThreads / 32; ++w) t += wsum[w][m];
     if (m < p.M) it.T[static_cast<int64_t>(m) * it.r + j] = t;
-    it.sT[m * it.rp64 + j] = __float2bfloat16_rn(m < p.M ? it.s * t : 0.0f);
+    store16(static_cast<T16*>(it.sT), m * it.rp64 + j, m < p.M ? it.s * t : 0.0f);
   }
   if (j == 0)   // the slab's padding columns r .. rp64-1
     for (int t = threadIdx.x; t < kStreamMaxM * (it.rp64 - it.r); t += kDownThreads)
-      it.sT[(t / (it.rp64 - it.r)) * it.rp64 + it.r + t % (it.rp64 - it.r)] = __float2bfloat16_rn(0.0f);
+      store16(static_cast<T16*>(it.sT), (t / (it.rp64 - it.r)) * it.rp64 + it.r + t % (it.rp64 - it.r), 0.0f);
 }
 
 size_t al1024(size_t b) { return (b + 1023) & ~static_cast<size_t>(1023); }
@@ -576,7 +592,27 @@ int sm_count_cached() {
 
 size_t stream_fwd_ws_bytes(const LinearArgs* a, int n) { return StreamWs(a, n).total; }
 
-cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status, cudaStream_t st) {
+template <typename T16>
+cudaError_t launch_stream(int64_t M, int ctas_down, const DownParams& dp, const StreamMaps& maps,
+                          const StreamParams& sp, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(nf4_stream_fwd<1, T16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(nf4_stream_fwd<2, T16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr != cudaSuccess) return attr;
+  cudaError_t e = launch_pdl(lora_down_small<T16>, dim3(ctas_down), dim3(kDownThreads), 0, st, 1, dp);
+  note_launch();
+  if (e != cudaSuccess) return e;
+  e = M <= 8 ? launch_pdl(nf4_stream_fwd<1, T16>, dim3(sp.ctas), dim3(kThreads), kSmemBytes, st, 1, maps, sp)
+             : launch_pdl(nf4_stream_fwd<2, T16>, dim3(sp.ctas), dim3(kThreads), kSmemBytes, st, 1, maps, sp);
+  note_launch();
+  return e;
+}
+
+cudaError_t stream_forward(const StreamItem* items, int n, bool f16, void* ws, int* status, cudaStream_t st) {
   if (n < 1 || n > kMaxGroup) return cudaErrorInvalidValue;
   const int64_t M = items[0].a.M;
   if (M < 1 || M > kStreamMaxM) return cudaErrorInvalidValue;
@@ -598,9 +634,9 @@ cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status
     const StreamItem& it = items[i];
     const LinearArgs& a = it.a;
     const int rp64 = rp64_of(a.r);
-    auto* sT = reinterpret_cast<__nv_bfloat16*>(w + L.slab[i]);
+    void* sT = w + L.slab[i];
     DownItem& d = dp.item[i];
-    d.x = static_cast<const __nv_bfloat16*>(it.x);
+    d.x = it.x;
     d.A = it.A;
     d.T = it.T;
     d.sT = sT;
@@ -617,7 +653,7 @@ cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status
     q.dq = a.W.dq;
     q.B = it.B;
     q.sT = sT;
-    q.y = static_cast<__nv_bfloat16*>(it.y);
+    q.y = it.y;
     q.N = a.N;
     q.K = a.K;
     q.r = a.r;
@@ -631,8 +667,8 @@ cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status
     tiles += q.tiles;
     bool ok = make_map(&maps.codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, a.W.packed, a.K / 2, a.N, a.K / 2, kSpanBytes,
                        kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.x, a.K, M, 2 * a.K, 64, kTok,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&maps.x[i], f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.x,
+                        a.K, M, 2 * a.K, 64, kTok, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
   }
   for (int i = n; i < kMaxGroup; ++i) maps.codes[i] = maps.x[i] = maps.codes[0];
@@ -647,22 +683,9 @@ cudaError_t stream_forward(const StreamItem* items, int n, void* ws, int* status
   sp.wait_ns = wsettings.wait_ns;
   sp.skip_stage0 = wsettings.skip_stage0;
 
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(nf4_stream_fwd<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(nf4_stream_fwd<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  if (attr != cudaSuccess) return attr;
   KernelTimer timer(NF4_TIME_STREAM_FWD, st);
-  cudaError_t e = launch_pdl(lora_down_small, dim3(ctas_down), dim3(kDownThreads), 0, st, 1, dp);
-  note_launch();
-  if (e != cudaSuccess) return e;
-  e = M <= 8 ? launch_pdl(nf4_stream_fwd<1>, dim3(sp.ctas), dim3(kThreads), kSmemBytes, st, 1, maps, sp)
-             : launch_pdl(nf4_stream_fwd<2>, dim3(sp.ctas), dim3(kThreads), kSmemBytes, st, 1, maps, sp);
-  note_launch();
-  return e;
+  return f16 ? launch_stream<__half>(M, ctas_down, dp, maps, sp, st)
+             : launch_stream<__nv_bfloat16>(M, ctas_down, dp, maps, sp, st);
 }
 
 }  // namespace qnf4

@@ -200,11 +200,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B and an fp32
-// accumulator: D format bits [4,6), A/B formats [7,10)/[10,13), A major bit 15,
-// N >> 3 at [17,23), M >> 4 at [24,29).
+// Instruction descriptor of tcgen05.mma kind::f16 with bf16 (or, with f16 != 0, IEEE half)
+// A and B and an fp32 accumulator: D format bits [4,6), A/B formats [7,10)/[10,13) (0 half,
+// 1 bf16), A major bit 15, N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_16(uint32_t M, uint32_t N, uint32_t a_mn_major, uint32_t f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | (a_mn_major << 15) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, uint32_t a_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) | ((N >> 3) << 17) | ((M >> 4) << 24);
+  return idesc_16(M, N, a_mn_major, 0u);
 }
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

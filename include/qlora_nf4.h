@@ -59,7 +59,10 @@ typedef enum {
   NF4_ERR_TOO_LARGE = 10  /* numel above NF4_QUANTIZE_NOALLOC_MAX_NUMEL (nf4_quantize_noalloc) */
 } nf4_status;
 
-typedef enum { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
+/* Element types.  NF4_F16 (IEEE binary16) is the pages' reduced-precision profile ([ADAPT]
+ * "Mixed precision keeps stable state in FP32": reconstructed weights rounded to FP16 before
+ * multiplication); it is a compute dtype of the linear and an output type of nf4_dequantize. */
+typedef enum { NF4_F32 = 0, NF4_BF16 = 1, NF4_F16 = 2 } nf4_dtype;
 
 typedef enum {
   QLORA_SCALE_LORA = 0,   /* s = alpha / rank        ([ADAPT] "LoRA FA includes ...") */
@@ -131,8 +134,8 @@ nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel,
 nf4_status nf4_quantize_noalloc(const void* x, nf4_dtype x_dtype, int64_t numel,
                                 const nf4_tensor* out, void* stream);
 
-/* Decode *w into y (device, out_dtype NF4_F32 or NF4_BF16, w->numel elements).
- * fp32 output is exact nf4[q]*a'; bf16 output is that value rounded to nearest
+/* Decode *w into y (device, out_dtype NF4_F32, NF4_BF16 or NF4_F16, w->numel elements).
+ * fp32 output is exact nf4[q]*a'; bf16 and half outputs are that value rounded to nearest
  * even ([ADAPT] "Fused GPU NF4 decodes inside the matrix kernel"). */
 nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream);
 
@@ -180,6 +183,9 @@ size_t qlora_bwd_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, 
  * compute = NF4_BF16: x and y bf16, bf16 tensor-core operands (the decoded weight
  *   rounded once to bf16, A and B rounded to bf16, s*T rounded to bf16) with fp32
  *   accumulation; needs K % 64 == 0 and N % 8 == 0 (NF4_ERR_SHAPE otherwise).
+ * compute = NF4_F16: the same with IEEE half in place of bf16 everywhere (the pages' FP16
+ *   profile, [ADAPT] "Mixed precision keeps stable state in FP32": reconstructed weights
+ *   rounded to FP16 before multiplication; adapters, T and accumulation in fp32).
  *   With M <= 16 the stored weight is streamed once and decoded inside the contraction
  *   (no decoded copy; workspace of a few MB); larger M decodes W once per call into the
  *   workspace and runs the tiled tensor-core GEMM.
@@ -217,7 +223,8 @@ nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item
                                   void* ws, size_t ws_bytes, void* stream);
 
 /* Backward ([ADAPT] "Packed NF4 ...": input gradients through the frozen base, no
- * base-weight gradient; [GATE] "The TFLOPS back-check": no dL/dW):
+ * base-weight gradient; [GATE] "The TFLOPS back-check": no dL/dW), in the same three
+ * compute dtypes as the forward:
  *     G  = dY B                    (internal, fp32 [M, rank])
  *     dX = dY W + s G A            [M, K], dtype of compute
  *     dA = s G^T x                 fp32 [rank, K]  (overwritten, not accumulated)

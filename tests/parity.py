@@ -6,7 +6,7 @@ rounding, bounded element by element from the magnitudes of the terms of each su
 (``oracle.qlora.forward_magnitudes`` / ``backward_magnitudes``):
 
   u_out   the rounding of the output itself: 2^-8 relative for a bfloat16 output (half an ulp
-          of an 8-bit significand), 2^-24 for float32;
+          of an 8-bit significand), 2^-11 for IEEE half, 2^-24 for float32;
   u_op    the rounding of an intermediate that the profile feeds to a tensor-core slab or
           adapter pass: bfloat16(s T), bfloat16(s G), bfloat16(G), bfloat16(T) for the bf16
           profile (2^-8 of that intermediate's terms), float32 products for the fp32 profile;
@@ -29,13 +29,15 @@ import numpy as np
 
 from oracle import qlora
 
-FROB = {"f32": 1e-5, "bf16": 2e-2}
-TILE_FROB = {"f32": 1e-5, "bf16": 5e-3}
+FROB = {"f32": 1e-5, "bf16": 2e-2, "f16": 2e-2}
+TILE_FROB = {"f32": 1e-5, "bf16": 5e-3, "f16": 5e-3}
 
 
 def _units(compute, n_contract):
     if compute == "bf16":
         return dict(out=2.0 ** -8, op=2.0 ** -8, acc=2.0 ** -14)
+    if compute == "f16":   # IEEE half: 11 significant bits, half an ulp is 2^-11 relative
+        return dict(out=2.0 ** -11, op=2.0 ** -11, acc=2.0 ** -14)
     return dict(out=2.0 ** -24, op=2.0 ** -24, acc=(n_contract + 4) * 2.0 ** -24)
 
 

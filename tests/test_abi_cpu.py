@@ -103,6 +103,9 @@ def test_validation_refuses_bad_arguments(lib):
 
     assert lib.nf4_dequantize(None, x, 0, None) == binding.NF4_ERR_ARG
     assert lib.nf4_dequantize(ctypes.byref(t), x, 3, None) == binding.NF4_ERR_DTYPE
+    # half precision: an output of the dequantize and a compute dtype of the linear, not an
+    # input of the quantizer nor an output of the selected-row and merge calls
+    assert q(x, binding.NF4_F16, 1000, ctypes.byref(t), ws, 1 << 20, None) == binding.NF4_ERR_DTYPE
 
     w = _fake_tensor(64 * 128)
     p = ctypes.c_void_p(0x50000000)
@@ -116,6 +119,7 @@ def test_validation_refuses_bad_arguments(lib):
     assert f(4, 64, 128, 8, cd=9) == binding.NF4_ERR_DTYPE
     w2 = _fake_tensor(100 * 96)
     assert f(4, 100, 96, 8, wt=w2) == binding.NF4_ERR_SHAPE  # bf16 needs K % 64 == 0
+    assert f(4, 100, 96, 8, cd=binding.NF4_F16, wt=w2) == binding.NF4_ERR_SHAPE   # and so does half
     w3 = _fake_tensor(100 * 128)
     assert f(4, 100, 128, 8, wt=w3) == binding.NF4_ERR_SHAPE  # bf16 needs N % 8 == 0
     assert f(4, 64, 64, 8) == binding.NF4_ERR_CORRUPT        # numel != N*K
@@ -133,6 +137,7 @@ def test_validation_refuses_bad_arguments(lib):
     assert emb(0, 64, p, 4, p) == binding.NF4_ERR_ARG
     assert emb(100, 64, p, -1, p) == binding.NF4_ERR_ARG
     assert emb(100, 64, p, 4, p, od=4) == binding.NF4_ERR_DTYPE
+    assert emb(100, 64, p, 4, p, od=binding.NF4_F16) == binding.NF4_ERR_DTYPE
     assert emb(100, 32, p, 4, p) == binding.NF4_ERR_CORRUPT          # numel != rows*dim
     assert emb(100, 64, None, 0, None) == binding.NF4_OK             # no ids: nothing to do
     assert emb(100, 64, None, 4, p) == binding.NF4_ERR_ARG
@@ -141,7 +146,8 @@ def test_validation_refuses_bad_arguments(lib):
     # merged weight: W [64, 128]
     m = lambda N, K, r, od=0, wt=w, a=p, alpha=16.0, mode=0: lib.nf4_merge_lora(  # noqa: E731
         N, K, r, ctypes.c_float(alpha), mode, ctypes.byref(wt), a, p, p, od, None)
-    assert m(64, 128, 8, od=2) == binding.NF4_ERR_DTYPE
+    assert m(64, 128, 8, od=binding.NF4_F16) == binding.NF4_ERR_DTYPE
+    assert m(64, 128, 8, od=3) == binding.NF4_ERR_DTYPE
     assert m(64, 128, 0) == binding.NF4_ERR_ARG
     assert m(64, 128, 65) == binding.NF4_ERR_ARG
     assert m(64, 128, 8, alpha=float("inf")) == binding.NF4_ERR_ARG

@@ -40,7 +40,7 @@ def _quantized_weight(N, K, seed, dist="normal", dq=True):
 
 
 def _run_case(M, N, K, r, alpha, compute, mode=binding.SCALE_LORA, seed=0, dist="normal", rows=None, dq=True):
-    tdt = torch.float32 if compute == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[compute]
     q, w_deq = _quantized_weight(N, K, seed, dist, dq)
     x = wl.normal((M, K), 1.0, 1, seed + 1)
     dy = wl.normal((M, N), 1.0, 1, seed + 2)
@@ -188,3 +188,31 @@ def test_split_tiles_are_deterministic(lib):
     for later in outs[1:]:
         for a, b in zip(outs[0], later):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("M,N,K,r", [(64, 8, 64, 1), (130, 200, 192, 5), (300, 264, 576, 16),
+                                     (511, 1032, 640, 64), (129, 136, 128, 128), (1, 520, 1024, 8),
+                                     (5, 264, 576, 16), (16, 1032, 320, 64)])
+def test_f16_profile_tiles_tails_and_small_m(lib, M, N, K, r):
+    """The FP16 profile: IEEE half operands and outputs, fp32 accumulation, on the tiled path
+    and (M <= 16) the small-M pass."""
+    _run_case(M, N, K, r, 16.0, "f16", seed=N + 3)
+
+
+def test_f16_profile_smollm2_qv_shapes(lib):
+    c = wl.W2
+    for name, N, K in c["shapes"]:
+        if name in c["targets"]:
+            _run_case(c["M"], N, K, c["r"], c["alpha"], "f16", seed=N + 5)
+
+
+@pytest.mark.parametrize("name", ["gate_proj", "down_proj"])
+def test_f16_profile_llama8b_sampled_rows(lib, name):
+    c = wl.W3
+    N, K = {n: (a, b) for n, a, b in c["shapes"]}[name]
+    rows = np.sort(np.random.default_rng(6).choice(c["M"], 64, replace=False))
+    _run_case(c["M"], N, K, c["r"], c["alpha"], "f16", seed=K + 1, dist="t", rows=rows)
+
+
+def test_f16_profile_rslora_without_double_quant(lib):
+    _run_case(96, 520, 512, 8, 16.0, "f16", mode=binding.SCALE_RSLORA, seed=3, dq=False)

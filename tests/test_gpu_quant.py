@@ -142,7 +142,7 @@ def test_dequantize_bit_exact(lib, n, dq):
     x = wl.student_t(n, 5, 0.02, 5, 7)
     ref = onf4.quantize(x, double_quant=dq)
     q = _upload(ref, (n,))
-    for dtype, odt in ((torch.float32, "f32"), (torch.bfloat16, "bf16")):
+    for dtype, odt in ((torch.float32, "f32"), (torch.bfloat16, "bf16"), (torch.float16, "f16")):
         y = binding.nf4_dequantize(q, dtype)
         want = onf4.dequantize(ref, odt)
         got = y.float().cpu().numpy()
