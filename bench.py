@@ -187,6 +187,9 @@ class Layer:
         max_w = max(N * K for _, N, K in self.shapes)
         self.deq = torch.empty(max_w, dtype=torch.bfloat16, device=dev)
         ws_q = max(lib.nf4_quantize_workspace_bytes(N * K, 1) for _, N, K in self.shapes)
+        # the step decodes each weight once (the dequantize row) and both contractions read that
+        # bf16 copy; decode_once = False runs the NF4-input calls, which decode once per call
+        self.decode_once = True
         ws_f = max(lib.qlora_fwd_workspace_bytes(self.M, N, K, self.r, 1) for _, N, K in self.shapes)
         ws_b = max(lib.qlora_bwd_workspace_bytes(self.M, N, K, self.r, 1) for _, N, K in self.shapes)
         self.ws_q = torch.empty(max(ws_q, 16), dtype=torch.uint8, device=dev)
@@ -211,7 +214,14 @@ class Layer:
     def step_one(self, p):
         from bit_nf4_quantized_gb300 import binding as b
         b.nf4_quantize(p["w"], True, out=p["q"], workspace=self.ws_q)
-        b.nf4_dequantize(p["q"], out=self.deq[:p["N"] * p["K"]].view(p["N"], p["K"]))
+        w16 = self.deq[:p["N"] * p["K"]].view(p["N"], p["K"])
+        b.nf4_dequantize(p["q"], out=w16)
+        if self.decode_once:
+            b.qlora_linear_fwd_w16(p["x"], w16, p["A"], p["B"], self.alpha, y=p["y"], T=p["T"],
+                                   workspace=self.ws_f)
+            b.qlora_linear_bwd_w16(p["dy"], p["x"], p["T"], w16, p["A"], p["B"], self.alpha, dx=p["dx"],
+                                   dA=p["dA"], dB=p["dB"], workspace=self.ws_b)
+            return
         b.qlora_linear_fwd(p["x"], p["q"], p["A"], p["B"], self.alpha, y=p["y"], T=p["T"],
                            workspace=self.ws_f)
         b.qlora_linear_bwd(p["dy"], p["x"], p["T"], p["q"], p["A"], p["B"], self.alpha, dx=p["dx"],
@@ -1017,6 +1027,15 @@ def main():
     small_m = measure_small_m(layer, row_ms, hbm)
     f16_profile = measure_f16_profile(layer, row_ms)
     fp32_576 = measure_fp32_576(dev, row_ms)
+    # the same step as one graph with L2 flushed before it, decoding once per projection (the
+    # headline's step) and with the NF4-input calls, which decode the weight once per call
+    once_ms = row_ms(layer.step, reps=5)
+    layer.decode_once = False
+    per_call_ms = row_ms(layer.step, reps=5)
+    layer.decode_once = True
+    step_variants = {"decode_once": {"ms_per_step": once_ms, "TFLOP/s": flops / (once_ms / 1e3) / 1e12},
+                     "decode_per_call": {"ms_per_step": per_call_ms, "TFLOP/s": flops / (per_call_ms / 1e3) / 1e12},
+                     "timing": "one step as a graph, L2 flushed before each replay, launch included"}
 
     e2e = None
     if not args.no_e2e:
@@ -1081,8 +1100,9 @@ def main():
             "config": {"workload": WORKLOAD_NAME, "tokens": M, "rank": r, "alpha": layer.alpha,
                        "targets": [n for n, _, _ in layer.shapes], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: each step touches ~1.5 GB of distinct buffers",
-                       "step": "per projection: nf4_quantize, nf4_dequantize (bf16), qlora_linear_fwd, "
-                               "qlora_linear_bwd",
+                       "step": "per projection: nf4_quantize, nf4_dequantize (bf16), qlora_linear_fwd_w16 and "
+                               "qlora_linear_bwd_w16 reading that decoded bf16 weight (one decode per projection "
+                               "per step; key step_variants times the NF4-input calls, one decode per call)",
                        "launch": "one step captured as a CUDA graph, replayed per timed step"},
             "gpu_launches": launches,
             "phases_ms_per_step": {k: v[0] / args.steps for k, v in kinds.items()},
@@ -1099,6 +1119,7 @@ def main():
                          "ms_per_step": q_row_ms,
                          "timing": "the 7 quantize calls as one graph, L2 flushed between replays",
                          "GB/s_in_step_events": q_gbs},
+            "step_variants": step_variants,
             "no_double_quant": no_dq,
             "small_m_forward": small_m,
             "f16_profile": f16_profile,

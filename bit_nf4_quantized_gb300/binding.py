@@ -29,6 +29,8 @@ ENTRY_POINTS = (
     "qlora_fwd_workspace_bytes", "qlora_bwd_workspace_bytes", "qlora_linear_fwd",
     "qlora_linear_bwd", "qlora_last_device_status", "nf4_kernel_launch_count",
     "qlora_fwd_batch_workspace_bytes", "qlora_linear_fwd_batch",
+    "qlora_fwd_w16_workspace_bytes", "qlora_bwd_w16_workspace_bytes", "qlora_linear_fwd_w16",
+    "qlora_linear_bwd_w16",
 )
 
 
@@ -90,6 +92,11 @@ def load() -> ctypes.CDLL:
                                    vp, vp, vp, vp, sz, vp]),
         "qlora_fwd_batch_workspace_bytes": (sz, [i64, i32, ctypes.POINTER(_FwdItem), i32]),
         "qlora_linear_fwd_batch": (i32, [i64, i32, ctypes.POINTER(_FwdItem), i32, vp, sz, vp]),
+        "qlora_fwd_w16_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
+        "qlora_bwd_w16_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
+        "qlora_linear_fwd_w16": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "qlora_linear_bwd_w16": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                       vp, vp, vp, vp, sz, vp]),
         "qlora_last_device_status": (i32, [vp, i32]),
         "nf4_kernel_launch_count": (i64, []),
         "qlora_debug_wait_timeout": (None, [i32]),
@@ -347,6 +354,53 @@ def qlora_linear_bwd(dy: torch.Tensor, x: torch.Tensor, T: torch.Tensor, W: Nf4T
     _check(lib.qlora_linear_bwd(M, N, K, r, ctypes.c_float(alpha), mode, cd, _ptr(dy), _ptr(x), _ptr(T),
                                 ctypes.byref(cs), _ptr(A), _ptr(B), _ptr(dx), _ptr(dA), _ptr(dB),
                                 _ptr(ws), ws.numel(), _stream(stream)), "qlora_linear_bwd")
+    return dx, dA, dB
+
+
+def qlora_linear_fwd_w16(x: torch.Tensor, w16: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                         mode: int = SCALE_LORA, y: torch.Tensor = None, T: torch.Tensor = None,
+                         workspace: torch.Tensor = None, stream=None):
+    """qlora_linear_fwd with the weight given decoded: ``w16`` [N, K] in x's dtype (bf16 or
+    half) as nf4_dequantize writes it.  Returns (y, T)."""
+    lib = load()
+    M, K = x.shape
+    N = w16.shape[0]
+    r = A.shape[0]
+    cd = _dtype_code(x.dtype)
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else _workspace(
+        lib.qlora_fwd_w16_workspace_bytes(M, N, K, r, cd), x.device)
+    _check(lib.qlora_linear_fwd_w16(M, N, K, r, ctypes.c_float(alpha), mode, cd, _ptr(x), _ptr(w16), _ptr(A),
+                                    _ptr(B), _ptr(y), _ptr(T), _ptr(ws), ws.numel(), _stream(stream)),
+           "qlora_linear_fwd_w16")
+    return y, T
+
+
+def qlora_linear_bwd_w16(dy: torch.Tensor, x: torch.Tensor, T: torch.Tensor, w16: torch.Tensor, A: torch.Tensor,
+                         B: torch.Tensor, alpha: float, mode: int = SCALE_LORA, dx: torch.Tensor = None,
+                         dA: torch.Tensor = None, dB: torch.Tensor = None, workspace: torch.Tensor = None,
+                         stream=None):
+    """qlora_linear_bwd with the weight given decoded (as qlora_linear_fwd_w16).  Returns
+    (dX, dA, dB)."""
+    lib = load()
+    M, K = x.shape
+    N = w16.shape[0]
+    r = A.shape[0]
+    cd = _dtype_code(x.dtype)
+    if dx is None:
+        dx = torch.empty((M, K), dtype=x.dtype, device=x.device)
+    if dA is None:
+        dA = torch.empty((r, K), dtype=torch.float32, device=x.device)
+    if dB is None:
+        dB = torch.empty((N, r), dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else _workspace(
+        lib.qlora_bwd_w16_workspace_bytes(M, N, K, r, cd), x.device)
+    _check(lib.qlora_linear_bwd_w16(M, N, K, r, ctypes.c_float(alpha), mode, cd, _ptr(dy), _ptr(x), _ptr(T),
+                                    _ptr(w16), _ptr(A), _ptr(B), _ptr(dx), _ptr(dA), _ptr(dB), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "qlora_linear_bwd_w16")
     return dx, dA, dB
 
 

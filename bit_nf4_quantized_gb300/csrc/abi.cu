@@ -108,6 +108,73 @@ void build_buckets(const float* thr, EncodeTables* e) {
   }
 }
 
+// The bf16 cut table (EncodeTables::nf4_sep): every pair x = s * mx * 2^-d, a = ma with mx, ma
+// the 128 bf16 significands in [1, 2), d = 0..15 (below that |x/a| < 2^-15 and q' lands in
+// the two buckets around 3, which hold code 7 alone), |x| <= a, and x = 0; scaling both by
+// a power of two changes neither x/a nor fl(x*r) while 1/a stays normal.  The code of each
+// pair is taken from RN(x/a) against the thresholds (the definition); its q' bits must then
+// split each bucket into at most two codes with every lower-code q' below every
+// higher-code q'.
+void build_bf16_cuts(const float* thr, EncodeTables* e) {
+  uint32_t lo_max[66], hi_min[66];
+  int lo_code[66], hi_code[66];
+  for (int i = 0; i < 66; ++i) lo_code[i] = 99, hi_code[i] = -1, lo_max[i] = 0, hi_min[i] = ~0u;
+  bool ok = true;
+  struct Pair { float x, a; };
+  std::vector<Pair> pairs;
+  pairs.reserve(128 * 128 * 32 + 128);
+  for (int ia = 0; ia < 128; ++ia) {
+    const float a = 1.0f + static_cast<float>(ia) / 128.0f;
+    pairs.push_back({0.0f, a});
+    for (int d = 0; d < 16; ++d)
+      for (int ix = 0; ix < 128; ++ix) {
+        const float m = std::ldexp(1.0f + static_cast<float>(ix) / 128.0f, -d);
+        if (m > a) continue;
+        pairs.push_back({m, a});
+        pairs.push_back({-m, a});
+      }
+  }
+  // two passes: the codes present in each bucket, then the cut between them
+  for (int pass = 0; pass < 2 && ok; ++pass) {
+    for (const Pair& p : pairs) {
+      const float v = p.x / p.a;
+      int code = 0;
+      for (int j = 0; j < 15; ++j) code += (v >= thr[j]) ? 1 : 0;
+      const float r = 1.0f / p.a;
+      const float qp = std::fmaf(p.x, r, 3.0f);
+      uint32_t qb;
+      std::memcpy(&qb, &qp, 4);
+      const int64_t idx = static_cast<int64_t>(qb >> 17) - 8191;
+      if (idx < 0 || idx > 65) { ok = false; break; }
+      if (pass == 0) {
+        lo_code[idx] = std::min(lo_code[idx], code);
+        hi_code[idx] = std::max(hi_code[idx], code);
+      } else if (code == lo_code[idx]) {
+        lo_max[idx] = std::max(lo_max[idx], qb);
+      } else {
+        hi_min[idx] = std::min(hi_min[idx], qb);
+      }
+    }
+    if (pass == 0)
+      for (int i = 0; i < 66; ++i)
+        if (hi_code[i] - lo_code[i] > 1) ok = false;
+  }
+  for (int i = 0; i < 66 && ok; ++i) {
+    if (hi_code[i] < 0) {                      // no bf16 pair lands here
+      e->nf4_sep_base[i] = 0;
+      e->nf4_sep[i] = ~0u;
+    } else if (hi_code[i] == lo_code[i]) {
+      e->nf4_sep_base[i] = static_cast<uint32_t>(lo_code[i]);
+      e->nf4_sep[i] = ~0u;
+    } else {
+      if (!(lo_max[i] < hi_min[i])) ok = false;
+      e->nf4_sep_base[i] = static_cast<uint32_t>(lo_code[i]);
+      e->nf4_sep[i] = hi_min[i];
+    }
+  }
+  e->sep_ok = ok ? 1 : 0;
+}
+
 struct Tables {
   DecodeTables dec;
   EncodeTables enc;
@@ -117,6 +184,7 @@ struct Tables {
     build_thresholds(dec.nf4, 16, enc.nf4_thr);
     build_thresholds(dec.dyn8, 256, enc.dyn8_thr);
     build_buckets(enc.nf4_thr, &enc);
+    build_bf16_cuts(enc.nf4_thr, &enc);
   }
 };
 
@@ -215,6 +283,22 @@ WaitSettings take_wait_settings() {
 
 const DecodeTables& decode_tables() { return tables().dec; }
 const EncodeTables& encode_tables() { return tables().enc; }
+
+int device_sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDev) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  n = n > 0 ? n : 1;
+  if (dev >= 0 && dev < kMaxDev) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 }  // namespace qnf4
@@ -554,6 +638,70 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
   if (e == cudaSuccess) e = launch_lora_dA(a, G, static_cast<const float*>(x), dA, cs);
   if (e == cudaSuccess) e = launch_lora_dB(a, dyf, T, dB, cs);
   return from_cuda(e);
+}
+
+size_t qlora_fwd_w16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
+  if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256 || !is16(compute)) return 0;
+  return tc_fwd_ws_bytes(M, N, K, rank, true);
+}
+
+size_t qlora_bwd_w16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
+  if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256 || !is16(compute)) return 0;
+  return a256(sizeof(float) * static_cast<size_t>(M) * rank) + tc_bwd_ws_bytes(M, N, K, rank, true);
+}
+
+nf4_status qlora_linear_fwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                                qlora_scale_mode mode, nf4_dtype compute,
+                                const void* x, const void* w16, const float* A, const float* B,
+                                void* y, float* T_out, void* ws, size_t ws_bytes, void* stream) {
+  float s = 0.0f;
+  nf4_status st = check_linear(M, N, K, rank, alpha, mode, compute, &s);
+  if (st != NF4_OK) return st;
+  if (!is16(compute)) return NF4_ERR_DTYPE;
+  if (w16 == nullptr || A == nullptr || B == nullptr) return NF4_ERR_ARG;
+  if (M > 0 && (x == nullptr || y == nullptr || T_out == nullptr)) return NF4_ERR_ARG;
+  if (!aligned16(w16) || !aligned16(A) || !aligned16(B) ||
+      (M > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(T_out))))
+    return NF4_ERR_ALIGN;
+  const size_t need = tc_fwd_ws_bytes(M, N, K, rank, true);
+  if (ws == nullptr || ws_bytes < need) return NF4_ERR_WORKSPACE;
+  if (!aligned16(ws)) return NF4_ERR_ALIGN;
+  if (M == 0) return NF4_OK;
+  int* status = nullptr;
+  if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+  const LinearArgs a{M, N, K, rank, s, Nf4View{}};
+  return from_cuda(tc_forward(a, compute == NF4_F16, x, A, B, y, T_out, ws, status,
+                              static_cast<cudaStream_t>(stream), w16));
+}
+
+nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                                qlora_scale_mode mode, nf4_dtype compute,
+                                const void* dy, const void* x, const float* T, const void* w16,
+                                const float* A, const float* B, void* dx, float* dA, float* dB,
+                                void* ws, size_t ws_bytes, void* stream) {
+  float s = 0.0f;
+  nf4_status st = check_linear(M, N, K, rank, alpha, mode, compute, &s);
+  if (st != NF4_OK) return st;
+  if (!is16(compute)) return NF4_ERR_DTYPE;
+  if (w16 == nullptr || A == nullptr || B == nullptr || dA == nullptr || dB == nullptr) return NF4_ERR_ARG;
+  if (M > 0 && (dy == nullptr || x == nullptr || T == nullptr || dx == nullptr)) return NF4_ERR_ARG;
+  if (!aligned16(w16) || !aligned16(A) || !aligned16(B) || !aligned16(dA) || !aligned16(dB)) return NF4_ERR_ALIGN;
+  if (M > 0 && (!aligned16(dy) || !aligned16(x) || !aligned16(T) || !aligned16(dx))) return NF4_ERR_ALIGN;
+  const size_t need = qlora_bwd_w16_workspace_bytes(M, N, K, rank, compute);
+  if (ws == nullptr || ws_bytes < need) return NF4_ERR_WORKSPACE;
+  if (!aligned16(ws)) return NF4_ERR_ALIGN;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (M == 0) {   // no tokens: the adapter gradients are zero
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * static_cast<size_t>(rank) * K, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, sizeof(float) * static_cast<size_t>(N) * rank, cs);
+    return from_cuda(e);
+  }
+  int* status = nullptr;
+  if ((st = device_status_ptr(&status)) != NF4_OK) return st;
+  const LinearArgs a{M, N, K, rank, s, Nf4View{}};
+  float* G = static_cast<float*>(ws);
+  void* tc_ws = static_cast<char*>(ws) + a256(sizeof(float) * static_cast<size_t>(M) * rank);
+  return from_cuda(tc_backward(a, compute == NF4_F16, dy, x, T, A, B, dx, dA, dB, G, tc_ws, status, cs, w16));
 }
 
 nf4_status qlora_last_device_status(void* stream, int32_t clear) {

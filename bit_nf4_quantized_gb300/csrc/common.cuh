@@ -68,6 +68,15 @@ struct EncodeTables {
   // gives the same code).
   float nf4_band[66][2];
   int32_t bucket_ok;
+  // bf16 input needs no band: with x and a bf16 values (a = max |x| of the block, so the
+  // ratio is a quotient of two 8-bit significands times a power of two) and a in
+  // [2^-126, 2^126) (1/a normal), the bits of q' = fl(x*r + 3) alone decide the code:
+  // code(v) = sep_base[idx] + (bits(q') >= sep[idx]).  The host builds sep by running every
+  // such pair through both formulas and sets sep_ok only if one cut per bucket separates
+  // the codes (sep = ~0u where a bucket holds one code).
+  uint32_t nf4_sep[66];
+  uint32_t nf4_sep_base[66];
+  int32_t sep_ok;
 };
 
 const DecodeTables& decode_tables();
@@ -75,6 +84,9 @@ const EncodeTables& encode_tables();
 
 // Launch accounting (for the launch count reported by the ABI).
 void note_launch(int n = 1);
+
+// SM count of the current device (looked up once per device).
+int device_sm_count();
 
 // Bounded-wait settings of one tensor-core launch: the wait limit, and whether the launch's
 // first CTA leaves its first pipeline stage unissued (so that the waits for that stage run
@@ -157,6 +169,8 @@ struct PrepJobs;
 // CTAs of staging jobs, one launch.
 cudaError_t launch_decode_with_prep(const Nf4View& w, void* y, bool f16, const PrepJobs& jobs, unsigned prep_ctas,
                                     cudaStream_t st);
+// The prep jobs alone (a call whose weight comes already decoded).
+cudaError_t launch_prep_only(bool f16, const PrepJobs& jobs, unsigned prep_ctas, cudaStream_t st);
 
 // ---- export.cu: selected embedding rows and the merged LoRA weight ------------
 cudaError_t launch_embedding_rows(const Nf4View& w, int64_t rows, int64_t dim, const int64_t* ids, int64_t n_ids,

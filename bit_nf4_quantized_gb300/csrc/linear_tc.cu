@@ -526,9 +526,12 @@ PrepJob zero_flags_job(void* flags) {
 }
 
 // The weight decoded to 16 bits [N][K] for this call (bit-exact with nf4_dequantize), in the
-// same launch as the call's operand staging (extra CTAs run the prep jobs).
-cudaError_t decode_weight(const LinearArgs& a, bool f16, void* wb, const PrepBuilder& prep, cudaStream_t st) {
+// same launch as the call's operand staging (extra CTAs run the prep jobs); with the weight
+// given decoded (w16), the staging alone.
+cudaError_t decode_weight(const LinearArgs& a, bool f16, void* wb, const PrepBuilder& prep, cudaStream_t st,
+                          const void* w16) {
   if (!prep.ok()) return cudaErrorInvalidValue;
+  if (w16 != nullptr) return launch_prep_only(f16, prep.jobs(), prep.ctas(), st);
   KernelTimer timer(NF4_TIME_WEIGHT_DECODE, st);
   return launch_decode_with_prep(a.W, wb, f16, prep.jobs(), prep.ctas(), st);
 }
@@ -538,21 +541,21 @@ cudaError_t decode_weight(const LinearArgs& a, bool f16, void* wb, const PrepBui
 // partial sums; `wb` the bf16 weight; `flags` the GEMM's per-part flags.
 struct FwdWs {
   size_t sTp, Bp, Aq, part, wb, flags, total;
-  FwdWs(int64_t M, int64_t N, int64_t K, int r) {
+  FwdWs(int64_t M, int64_t N, int64_t K, int r, bool w16 = false) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r);
     sTp = 0;
     Bp = sTp + a1024(2 * rp * M);
     Aq = Bp + a1024(2 * rp * N);
     part = Aq + a1024(2 * nq * K);
     wb = part + a1024(std::max(adapter_partial_bytes(M, K, r), kMaxPartTiles * kPartTileBytes));
-    flags = wb + a1024(2 * static_cast<size_t>(N) * K);
+    flags = wb + (w16 ? 0 : a1024(2 * static_cast<size_t>(N) * K));
     total = flags + a1024(kPartFlagBytes);
   }
 };
 
 struct BwdWs {
   size_t sGp, ApT, Bt, Tt, Gt, part, wb, flags, total;
-  BwdWs(int64_t M, int64_t N, int64_t K, int r) {
+  BwdWs(int64_t M, int64_t N, int64_t K, int r, bool w16 = false) {
     const size_t rp = padded_rank(r), nq = adapter_nq(r), Mp = pad8(M);
     // G's and dB's partial sums side by side (one launch runs both), later dA's
     size_t pb = adapter_partial_bytes(M, N, r) + adapter_partial_bytes(N, M, r);
@@ -565,7 +568,7 @@ struct BwdWs {
     Gt = Tt + a1024(2 * nq * Mp);
     part = Gt + a1024(2 * nq * Mp);
     wb = part + a1024(pb);
-    flags = wb + a1024(2 * static_cast<size_t>(N) * K);
+    flags = wb + (w16 ? 0 : a1024(2 * static_cast<size_t>(N) * K));
     total = flags + a1024(kPartFlagBytes);
   }
 };
@@ -594,21 +597,21 @@ GemmParams base_params(const LinearArgs& a, bool f16, int mode, void* out, int* 
 
 }  // namespace
 
-size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return FwdWs(M, N, K, r).total; }
+size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool w16) { return FwdWs(M, N, K, r, w16).total; }
 
-size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r) { return BwdWs(M, N, K, r).total; }
+size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool w16) { return BwdWs(M, N, K, r, w16).total; }
 
 // Forward: W in bf16 with prep (A and B in bf16) -> T = x A^T (skinny tcgen05) ->
 // T and bf16(s T) -> GEMM with the (s T) B^T slab.
 cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float* A, const float* B, void* y,
-                       float* T, void* ws, int* status, cudaStream_t st) {
-  const FwdWs L(a.M, a.N, a.K, a.r);
+                       float* T, void* ws, int* status, cudaStream_t st, const void* w16) {
+  const FwdWs L(a.M, a.N, a.K, a.r, w16 != nullptr);
   char* w = static_cast<char*>(ws);
   void* sTp = w + L.sTp;
   void* Bp = w + L.Bp;
   void* Aq = w + L.Aq;
   auto* part = reinterpret_cast<float*>(w + L.part);
-  void* wb = w + L.wb;
+  const void* wb = w16 != nullptr ? w16 : w + L.wb;
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
   const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   PrepBuilder prep(f16);
@@ -632,7 +635,7 @@ cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float
     prep.add(b);
     prep.add(zero_flags_job(w + L.flags));
   }
-  cudaError_t e = decode_weight(a, f16, wb, prep, st);
+  cudaError_t e = decode_weight(a, f16, w + L.wb, prep, st, w16);
   if (e != cudaSuccess) return e;
   {  // T = x A^T: rows M, reduction over K along x's rows; T (fp32) and 16-bit s T for the slab
     AdapterPassArgs t{};
@@ -670,8 +673,8 @@ cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float
 // dA = s G^T x.
 cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const void* x, const float* T,
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G, void* ws,
-                        int* status, cudaStream_t st) {
-  const BwdWs L(a.M, a.N, a.K, a.r);
+                        int* status, cudaStream_t st, const void* w16) {
+  const BwdWs L(a.M, a.N, a.K, a.r, w16 != nullptr);
   char* w = static_cast<char*>(ws);
   void* sGp = w + L.sGp;
   void* ApT = w + L.ApT;
@@ -679,7 +682,7 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
   void* Tt = w + L.Tt;
   void* Gt = w + L.Gt;
   auto* part = reinterpret_cast<float*>(w + L.part);
-  void* wb = w + L.wb;
+  const void* wb = w16 != nullptr ? w16 : w + L.wb;
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
   const int64_t Mp = pad8(a.M);
   const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -716,7 +719,7 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
     prep.add(c);
     prep.add(zero_flags_job(w + L.flags));
   }
-  cudaError_t e = decode_weight(a, f16, wb, prep, st);
+  cudaError_t e = decode_weight(a, f16, w + L.wb, prep, st, w16);
   if (e != cudaSuccess) return e;
   {  // one launch for G = dY B (rows M, reduction over N along dY's rows; G, bf16(s G), bf16(G)^T)
      // and dB = s dY^T T (rows N, reduction over M down dY's columns), then one for both finishes

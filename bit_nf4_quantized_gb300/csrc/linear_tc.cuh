@@ -6,20 +6,24 @@
 
 namespace qnf4 {
 
-size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
-size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r);
+// w16: the weight comes decoded (no room for a per-call decoded copy in the workspace).
+size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool w16 = false);
+size_t tc_bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool w16 = false);
 
-// f16: the operands and outputs are IEEE half (the FP16 profile) instead of bf16.
+// f16: the operands and outputs are IEEE half (the FP16 profile) instead of bf16.  w16, when
+// given, is W already decoded to the 16-bit type ([N][K], as nf4_dequantize writes it): the
+// call then runs its operand staging alone instead of decoding a.W first.
 cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float* A, const float* B, void* y,
-                       float* T, void* ws, int* status, cudaStream_t st);
+                       float* T, void* ws, int* status, cudaStream_t st, const void* w16 = nullptr);
 cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const void* x, const float* T,
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G,
-                        void* ws, int* status, cudaStream_t st);
+                        void* ws, int* status, cudaStream_t st, const void* w16 = nullptr);
 
 // stream_fwd.cu: the forward for at most kStreamMaxM tokens, for up to kStreamMaxGroup
 // projections (sharing M) in two launches: T by lora_down_small, then one persistent pass that
-// streams every projection's stored weight once, decodes it in registers into TMEM and runs
-// tcgen05.mma with the tokens as the N = 16 operand, the LoRA term in the same accumulator.
+// streams every projection's stored weight once, decodes it in registers straight into
+// mma.sync fragments with the tokens as the 16-row operand, the LoRA term in the same
+// accumulators.
 constexpr int kStreamMaxM = 16;
 constexpr int kStreamMaxGroup = 8;
 struct StreamItem {

@@ -7,19 +7,20 @@
 // kernel".  Deterministic, byte-identical requantization: "NF4 Layer Streaming --
 // Gate results", section "P3 is solved".
 //
-// Lane mapping (all kernels here): a warp walks "quad rows" of 128 elements; lane l
-// owns elements 4l..4l+3 of the row, so a half warp covers one 64-element block and
-// every global access of a warp instruction is contiguous.
+// Lane mapping of the block and decode kernels: a warp walks rows of 1024 elements and lane
+// l owns elements 32l .. 32l + 31 of a row, so a lane pair holds one 64-element block.
 //
-// quantize = three launches:
+// quantize = two launches:
 //   1. nf4_encode_blocks: absmax, 4-bit codes, packing; per 256-block group the
-//      float64 pairwise-tree sum of the absmax values (double quant only).
-//   2. nf4_absmax_mean: one CTA finishes the tree over the group sums -> offset.
-//   3. nf4_encode_nested: centre, nested absmax per group, dynamic8 codes.
+//      float64 pairwise-tree sum of the absmax values, and in the CTA that finishes
+//      last the tree over the group sums -> offset (double quant only).
+//   2. nf4_encode_nested: centre, nested absmax per group, dynamic8 codes.
 #include "common.cuh"
 #include "decode.cuh"
 #include "prep.cuh"
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace qnf4 {
@@ -42,30 +43,40 @@ __device__ __forceinline__ int dyn8_encode(float v, const float* thr) {
   return c;
 }
 
-// Lane's 32 elements (from e0) as fp32, zero past numel, and the largest |x| among them
-// as fp32 bits (bf16 input: an integer max over the 15-bit magnitudes, two at a time, which
-// orders subnormals, Inf and NaN exactly as the fp32 bit patterns do).
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-template <typename Tin>
-__device__ __forceinline__ uint32_t lane_load(const Tin* __restrict__ x, int64_t numel, int64_t e0, float (&v)[32]) {
-  constexpr int kVec = 16 / sizeof(Tin);
-  uint32_t w[32 / kVec * 4];
+// The raw bits of the lane's 32 elements from e0 (16 words of two bf16, or 32 fp32
+// words), zero past numel.  The input is read once: read-only loads that allocate no L1
+// line, 32 bytes per instruction when the input is 32-byte aligned (kV8), else 16.
+template <typename Tin, bool kV8>
+__device__ __forceinline__ void lane_words(const Tin* __restrict__ x, int64_t numel, int64_t e0,
+                                           uint32_t (&w)[8 * sizeof(Tin)]) {
+  constexpr int kW = 8 * sizeof(Tin);
   if (e0 + 32 <= numel) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(x + e0);
+    if constexpr (kV8) {
 #pragma unroll
-    for (int i = 0; i < 32 / kVec; ++i) {
-      const uint4 u = *reinterpret_cast<const uint4*>(x + e0 + i * kVec);
-      w[4 * i] = u.x, w[4 * i + 1] = u.y, w[4 * i + 2] = u.z, w[4 * i + 3] = u.w;
+      for (int i = 0; i < kW / 8; ++i)
+        asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(w[8 * i]), "=r"(w[8 * i + 1]), "=r"(w[8 * i + 2]), "=r"(w[8 * i + 3]),
+                       "=r"(w[8 * i + 4]), "=r"(w[8 * i + 5]), "=r"(w[8 * i + 6]), "=r"(w[8 * i + 7])
+                     : "l"(p + 8 * i));
+    } else {
+#pragma unroll
+      for (int i = 0; i < kW / 4; ++i)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+                     : "l"(p + 4 * i));
     }
-  } else {   // ragged tail: zero past numel
+  } else {   // ragged tail
     const uint16_t* x16 = reinterpret_cast<const uint16_t*>(x);
     const uint32_t* x32 = reinterpret_cast<const uint32_t*>(x);
 #pragma unroll
-    for (int i = 0; i < 32 / kVec * 4; ++i) {
+    for (int i = 0; i < kW; ++i) {
       if (sizeof(Tin) == 4) {
         w[i] = (e0 + i < numel) ? x32[e0 + i] : 0u;
       } else {
@@ -75,185 +86,287 @@ __device__ __forceinline__ uint32_t lane_load(const Tin* __restrict__ x, int64_t
       }
     }
   }
+}
+
+// Element i of the lane as fp32.
+template <typename Tin>
+__device__ __forceinline__ float lane_elem(const uint32_t (&w)[8 * sizeof(Tin)], int i) {
+  if (sizeof(Tin) == 4) return __uint_as_float(w[i]);
+  return __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
+}
+
+// Largest |x| of the lane's elements as fp32 bits (bf16: an integer max over the 15-bit
+// magnitudes, two at a time, which orders subnormals, Inf and NaN as the fp32 bit
+// patterns do).
+template <typename Tin>
+__device__ __forceinline__ uint32_t lane_absmax_bits(const uint32_t (&w)[8 * sizeof(Tin)]) {
   if (sizeof(Tin) == 4) {
     uint32_t mb = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      v[i] = __uint_as_float(w[i]);
-      mb = max(mb, w[i] & 0x7FFFFFFFu);
-    }
+    for (int i = 0; i < 32; ++i) mb = max(mb, w[i] & 0x7FFFFFFFu);
     return mb;
-  } else {
-    uint32_t m2 = 0;   // two 16-bit maxima
+  }
+  uint32_t m2 = 0;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      v[2 * k] = __uint_as_float(w[k] << 16);
-      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-      m2 = max_u16x2(m2, w[k] & 0x7FFF7FFFu);
+  for (int k = 0; k < 16; ++k) m2 = max_u16x2(m2, w[k] & 0x7FFF7FFFu);
+  return max(m2 & 0xFFFFu, m2 >> 16) << 16;
+}
+
+// Codes of one lane (32 elements, one half block) with the block maximum a = bits mb.
+// Words: element i sits in word i / 8, byte (i % 8) / 2, high nibble for even i; a word is
+// built by shifting in elements 6, 7, 4, 5, 2, 3, 0, 1 of its eight.
+//   bf16 input, a in [2^-126, 2^126), cut table valid: code = base + (bits(q') >= cut),
+//     q' = fl(x*r + 3), r = RN(1/a), from the bucket row of q' (no band: see EncodeTables).
+//   fp32 input: q = x*r and q' pick the bucket; code = base + (q >= hi); a q inside the
+//     band [lo, hi) marks the lane unsure, and an unsure lane (or a, r not finite, or the
+//     bucket table unusable) is redone with the IEEE quotient RN(x / a).
+// Bucket row (bits(q') >> 17) of the lane's table copy; tab_base is the shared-memory address
+// of row 0 of the copy minus 8191 rows.
+__device__ __forceinline__ uint2 bucket_row(uint32_t tab_base, uint32_t qb) {
+  uint2 e;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(e.x), "=r"(e.y) : "r"(tab_base + ((qb >> 17) << 7)));
+  return e;
+}
+
+template <typename Tin>
+__device__ __forceinline__ void lane_codes(const uint32_t (&w)[8 * sizeof(Tin)], uint32_t mb, uint32_t tab_base,
+                                           bool fast_ok, const float* thr, uint32_t (&words)[4]) {
+  const float a = __uint_as_float(mb);
+  if (a == 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) words[j] = 0x77777777u;     // every code is that of 0.0
+    return;
+  }
+  const float r = __frcp_rn(a);
+  bool exact;
+  if (sizeof(Tin) == 2) {
+    exact = !(fast_ok && mb >= 0x00800000u && mb < 0x7E800000u);
+    if (!exact) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int i = 8 * j + (6 - 2 * (t >> 1)) + (t & 1);
+          const uint32_t qb = __float_as_uint(fmaf(lane_elem<Tin>(w, i), r, 3.0f));
+          const uint2 e = bucket_row(tab_base, qb);
+          acc = (acc << 4) + e.y + (qb >= e.x ? 1u : 0u);
+        }
+        words[j] = acc;
+      }
     }
-    return max(m2 & 0xFFFFu, m2 >> 16) << 16;
+  } else {
+    exact = !(fast_ok && isfinite(r) && mb < 0x7F800000u);
+    if (!exact) {
+      bool unsure = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const int i = 8 * j + (6 - 2 * (t >> 1)) + (t & 1);
+          const float v = lane_elem<Tin>(w, i);
+          const float q = v * r;
+          const uint32_t qb = __float_as_uint(fmaf(v, r, 3.0f));
+          const uint2 e = bucket_row(tab_base, qb);
+          const float lo = __uint_as_float(e.x), hi = __uint_as_float(e.y);
+          unsure |= (q >= lo) & (q < hi);
+          acc = (acc << 4) + (e.x & 15u) + (q >= hi ? 1u : 0u);
+        }
+        words[j] = acc;
+      }
+      exact = unsure;
+    }
+  }
+  if (exact) {  // rare: the lane again with the IEEE quotient
+#pragma unroll
+    for (int j = 0; j < 4; ++j) words[j] = 0u;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t c = static_cast<uint32_t>(nf4_encode(__fdiv_rn(lane_elem<Tin>(w, i), a), thr));
+      words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
+    }
   }
 }
 
-// Block pass: absmax, 4-bit codes and packing for one nested group (256 blocks) per CTA;
-// with double quantization also the float64 pairwise-tree sum of the group's absmax.
-// Codes: q = x * RN(1/a), and fl(x * RN(1/a) + 3) picks an entry of the bucket table;
-// when q lies in the entry's band around a threshold, or a or 1/a is not finite, the code
-// is taken from the exact quotient RN(x / a) instead, so the result is always that of
-// the IEEE division.
+// One row of 1024 elements from the lane's words: block maxima, codes, the packed bytes and
+// the fp32 maxima; the group's double copy of each maximum goes to gs_slot.  Returns true if
+// the lane's block holds a non-finite value.
 template <typename Tin>
-__global__ void __launch_bounds__(kQuantThreads)
-nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, uint8_t* __restrict__ packed,
-                  float* __restrict__ absmax, double* __restrict__ group_sum, EncodeTables tabs,
-                  int* status) {
+__device__ __forceinline__ bool encode_row(const uint32_t (&w)[8 * sizeof(Tin)], int64_t e0, int64_t numel,
+                                           uint8_t* __restrict__ packed, float* __restrict__ absmax,
+                                           double* gs_slot, uint32_t tab_base, bool fast_ok,
+                                           const float* thr, int lane) {
+  uint32_t mb = lane_absmax_bits<Tin>(w);
+  mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));  // the lane pair holds one block
+  uint32_t words[4];
+  lane_codes<Tin>(w, mb, tab_base, fast_ok, thr, words);
+  if (e0 + 31 >= numel) {  // ragged tail: codes past numel are 0 (the pad nibble of an odd tail)
+    const int64_t vc = numel - e0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i >= vc) words[i >> 3] &= ~(0xFu << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4)));
+  }
+  if (e0 + 31 < numel) {
+    *reinterpret_cast<uint4*>(packed + (e0 >> 1)) = make_uint4(words[0], words[1], words[2], words[3]);
+  } else if (e0 < numel) {
+    const int64_t nbytes = (numel - e0 + 1) / 2;
+#pragma unroll
+    for (int b = 0; b < 16; ++b)
+      if (b < nbytes) packed[(e0 >> 1) + b] = static_cast<uint8_t>(words[b >> 2] >> (8 * (b & 3)));
+  }
+  if ((lane & 1) == 0) {
+    const float a = __uint_as_float(mb);
+    if (e0 < numel) absmax[e0 >> 6] = a;
+    *gs_slot = (e0 < numel) ? static_cast<double>(a) : 0.0;
+  }
+  return mb >= 0x7F800000u;
+}
+
+// The offset: the float64 pairwise tree s[i] += s[i + h], h = p2/2, ..., 1, over the group
+// sums gs padded with zeros to p2 entries, divided by nb and rounded once to fp32, by one CTA
+// (the last of the block pass to finish).  Levels above 8192 entries run in place in gs (the
+// workspace holds p2 entries); then each of the (at most) 1024 entries left after the next
+// levels is summed from its column of up to 8 loads in registers, in the tree's own order; the
+// levels down to 32 run in shared memory `sm` and the last five across the lanes of warp 0.
+// Returns the offset in thread 0.
+__device__ __forceinline__ float offset_tree(double* gs, int64_t ng, int64_t p2, int64_t nb, double* sm) {
+  int64_t n = p2, valid = ng;   // live entries, of which the first `valid` hold data
+  for (; n > 8192; n /= 2) {
+    const int64_t h = n / 2;
+    for (int64_t i = threadIdx.x; i < h; i += kQuantThreads) {
+      const double a = i < valid ? gs[i] : 0.0;
+      const double b = i + h < valid ? gs[i + h] : 0.0;
+      gs[i] = a + b;
+    }
+    valid = valid < h ? valid : h;
+    __syncthreads();
+  }
+  // entry i of the first w = min(n, 1024) entries is the tree over column j = 0 .. m-1 of
+  // gs[i + w j] (m = n / w), whose pairs are (j, j + m/2), then (j, j + m/4), ...
+  const int64_t w = n < 1024 ? n : 1024, m = n / w;
+#pragma unroll 1
+  for (int64_t i = threadIdx.x; i < w; i += kQuantThreads) {
+    double c[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j] = (j < m && i + w * j < valid) ? gs[i + w * j] : 0.0;
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1)
+      if (h < m)
+#pragma unroll
+        for (int j = 0; j < h; ++j) c[j] = c[j] + c[j + h];
+    sm[i] = c[0];
+  }
+  __syncthreads();
+  for (n = w; n > 32; n /= 2) {
+    const int64_t h = n / 2;
+    for (int64_t i = threadIdx.x; i < h; i += kQuantThreads) sm[i] = sm[i] + sm[i + h];
+    __syncthreads();
+  }
+  float offset = 0.0f;
+  if (threadIdx.x < 32) {
+    double t = threadIdx.x < n ? sm[threadIdx.x] : 0.0;
+    for (int64_t h = n / 2; h >= 1; h /= 2) t += __shfl_down_sync(0xffffffffu, t, static_cast<int>(h));
+    if (threadIdx.x == 0) offset = __double2float_rn(__ddiv_rn(t, static_cast<double>(nb)));
+  }
+  return offset;
+}
+
+// Block pass: absmax, 4-bit codes and packing, one nested group (256 blocks, 16384
+// elements) at a time; with double quantization also the float64 pairwise-tree sum of each
+// group's absmax.  Persistent: CTA c takes groups c, c + G, c + 2G, ... (G = gridDim.x,
+// sized to the CTAs resident at once).  Warp w codes rows 2w and 2w + 1 of a group (1024
+// elements each; lane l elements 32l .. 32l + 31, so a lane pair holds one block); after
+// coding a row it loads the same row of its next group into the row's registers, so one
+// row per warp is always in flight while the other is coded.  The group's 256 maxima meet
+// in shared memory (two buffers, by group parity) and one warp, rotating, sums them.
+template <typename Tin, bool kV8>
+__global__ void __launch_bounds__(kQuantThreads, sizeof(Tin) == 2 ? 3 : 2)
+nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, int64_t ng, uint8_t* __restrict__ packed,
+                  float* __restrict__ absmax, double* __restrict__ group_sum, int64_t p2,
+                  unsigned* __restrict__ ticket, float* __restrict__ offset, EncodeTables tabs, int* status) {
   __shared__ float thr[16];
-  // (lo with the base code in its low 4 bits, hi); 16 copies: the 8-byte lookups of a warp are
-  // served half a warp at a time, so lanes l and l + 16 never meet in one bank access
-  __shared__ float2 band[66][16];
-  __shared__ double gsum[kNested];
+  // bucket rows, 16 copies: the 8-byte lookups of a warp are served half a warp at a time,
+  // and lanes l, l + 16 never meet in one bank access.  bf16: {cut, base}; fp32: {bits of
+  // lo with the base code in its low 4 bits, bits of hi}
+  // the tables and the group-sum buffers, then (last CTA) the offset tree's 1024 entries
+  __shared__ __align__(16) unsigned char smem_raw[66 * 16 * 8 + 2 * kNested * 8];
+  __shared__ unsigned s_last;
+  auto tab = reinterpret_cast<uint2 (*)[16]>(smem_raw);
+  auto gsum = reinterpret_cast<double (*)[kNested]>(smem_raw + 66 * 16 * 8);
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
-  for (int i = threadIdx.x; i < 66 * 16; i += kQuantThreads)
-    band[i >> 4][i & 15] = make_float2(tabs.nf4_band[i >> 4][0], tabs.nf4_band[i >> 4][1]);
+  for (int i = threadIdx.x; i < 66 * 16; i += kQuantThreads) {
+    const int k = i >> 4;
+    tab[k][i & 15] = (sizeof(Tin) == 2)
+                         ? make_uint2(tabs.nf4_sep[k], tabs.nf4_sep_base[k])
+                         : make_uint2(__float_as_uint(tabs.nf4_band[k][0]), __float_as_uint(tabs.nf4_band[k][1]));
+  }
   __syncthreads();
   pdl_allow_next();
   pdl_wait();
-  const bool fast_ok = tabs.bucket_ok != 0;   // bucket table usable
+  const bool fast_ok = (sizeof(Tin) == 2) ? tabs.sep_ok != 0 : tabs.bucket_ok != 0;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t group_base = static_cast<int64_t>(blockIdx.x) * kGroupElems;
-  // warp w handles elements [w*2048, (w+1)*2048) of the group: two 1024-element rows
-  const int64_t wbase = group_base + warp * 2048;
+  // row (bits(q') >> 17) of this lane's copy: q' in [2, 4] gives rows 8191 .. 8256 of the
+  // shifted origin, i.e. table rows 0 .. 65 (rows are 128 bytes: 16 copies of 8)
+  const uint32_t tab_base = static_cast<uint32_t>(__cvta_generic_to_shared(&tab[0][lane & 15])) - 8191u * 128u;
+  constexpr int kW = 8 * sizeof(Tin);
+  const int64_t lane_off = warp * 2048 + 32 * lane;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroupElems;
+  int64_t g = blockIdx.x;
+  uint32_t wa[kW], wb[kW];
+  lane_words<Tin, kV8>(x, numel, g * kGroupElems + lane_off, wa);
+  lane_words<Tin, kV8>(x, numel, g * kGroupElems + lane_off + 1024, wb);
   bool nonfinite = false;
+  const int slot = warp * 32 + (lane >> 1);    // block of the group held by the lane pair (row 2w)
 #pragma unroll 1
-  for (int u = 0; u < 2; ++u) {
-    const int64_t e0 = wbase + u * 1024 + 32 * lane;    // lane's first element
-    float v[32];
-    uint32_t mb = lane_load<Tin>(x, numel, e0, v);
-    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));  // the lane pair holds one block
-    nonfinite |= mb >= 0x7F800000u;
-    const float a = __uint_as_float(mb);
-    const float r = __frcp_rn(a);
-    uint32_t words[4];
-    if (a == 0.0f) {
+  for (int it = 0; g < ng; g += gridDim.x, ++it) {
+    const int64_t e0 = g * kGroupElems + lane_off;
+    const bool more = g + gridDim.x < ng;
+    double* gs = gsum[it & 1];
+    nonfinite |= encode_row<Tin>(wa, e0, numel, packed, absmax, gs + slot, tab_base, fast_ok, thr, lane);
+    if (more) lane_words<Tin, kV8>(x, numel, e0 + stride, wa);
+    nonfinite |= encode_row<Tin>(wb, e0 + 1024, numel, packed, absmax, gs + slot + 16, tab_base, fast_ok, thr, lane);
+    if (more) lane_words<Tin, kV8>(x, numel, e0 + 1024 + stride, wb);
+    if (group_sum == nullptr) continue;
+    __syncthreads();
+    if (warp != (it & 7)) continue;
+    // float64 pairwise tree s[i] += s[i + h], h = 128, 64, ..., 1, by one warp: lane l holds
+    // s[l + 32 m]; the levels h >= 32 add within the lane, the rest across lanes
+    double t[kNested / 32];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) words[w] = 0x77777777u;     // every code is that of 0.0
-    } else {
-      bool exact = !(fast_ok && isfinite(r) && mb < 0x7F800000u);
-      if (!exact) {
-        bool unsure = false;
+    for (int m = 0; m < kNested / 32; ++m) t[m] = gs[lane + 32 * m];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) words[w] = 0u;
+    for (int h = kNested / 64; h >= 1; h >>= 1)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float q = v[i] * r;
-          const uint32_t k = (__float_as_uint(fmaf(v[i], r, 3.0f)) >> 17) - 8191u;   // 0 .. 65
-          const float2 b = band[k][lane & 15];
-          unsure |= (q >= b.x) & (q < b.y);
-          const uint32_t c = (__float_as_uint(b.x) & 15u) + (q >= b.y ? 1u : 0u);
-          words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
-        }
-        exact = unsure;
-      }
-      if (exact) {  // rare: redo the lane with the IEEE quotient
+      for (int m = 0; m < h; ++m) t[m] += t[m + h];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) words[w] = 0u;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t c = static_cast<uint32_t>(nf4_encode(__fdiv_rn(v[i], a), thr));
-          words[i >> 3] |= c << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4));
-        }
-      }
-    }
-    if (e0 + 31 >= numel) {  // ragged tail: codes past numel are 0 (the pad nibble of an odd tail)
-      const int64_t vc = numel - e0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i >= vc) words[i >> 3] &= ~(0xFu << (((i >> 1) & 3) * 8 + ((i & 1) ? 0 : 4)));
-    }
-    if (e0 + 31 < numel) {
-      *reinterpret_cast<uint4*>(packed + (e0 >> 1)) = make_uint4(words[0], words[1], words[2], words[3]);
-    } else if (e0 < numel) {
-      const int64_t nbytes = (numel - e0 + 1) / 2;
-#pragma unroll
-      for (int b = 0; b < 16; ++b)
-        if (b < nbytes) packed[(e0 >> 1) + b] = static_cast<uint8_t>(words[b >> 2] >> (8 * (b & 3)));
-    }
-    const int block_in_group = warp * 32 + u * 16 + (lane >> 1);
-    if ((lane & 1) == 0) {
-      if (e0 < numel) absmax[e0 >> 6] = a;
-      gsum[block_in_group] = (e0 < numel) ? static_cast<double>(a) : 0.0;
-    }
+    for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
+    if (lane == 0) group_sum[g] = t[0];
   }
   if (nonfinite) atomicCAS(status, 0, static_cast<int>(NF4_ERR_NONFINITE));
   if (group_sum == nullptr) return;
+  // the last CTA to finish sums the group sums into the offset (every thread fences its
+  // writes before the CTA takes its ticket, so all group sums are visible to that CTA), then
+  // puts the ticket counter back to zero for the next call that draws this slot
+  __threadfence();
   __syncthreads();
-  if (warp != 0) return;
-  // float64 pairwise tree s[i] += s[i + h], h = 128, 64, ..., 1, by one warp: lane l holds
-  // s[l + 32 m]; the levels h >= 32 add within the lane, the rest across lanes
-  double t[kNested / 32];
-#pragma unroll
-  for (int m = 0; m < kNested / 32; ++m) t[m] = gsum[lane + 32 * m];
-#pragma unroll
-  for (int h = kNested / 64; h >= 1; h >>= 1)
-#pragma unroll
-    for (int m = 0; m < h; ++m) t[m] += t[m + h];
-#pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
-  if (lane == 0) group_sum[blockIdx.x] = t[0];
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (s_last == 0) return;
+  __threadfence();
+  const float off = offset_tree(group_sum, ng, p2, (numel + kBlock - 1) / kBlock,
+                                reinterpret_cast<double*>(smem_raw));
+  if (threadIdx.x == 0) {
+    *offset = off;
+    *ticket = 0u;
+  }
 }
 
-// One CTA: the same pairwise tree over the group sums padded with zeros to p2
-// entries, then offset = float(sum / nb).  The tree runs in shared memory when the p2
-// entries fit (kMeanSmemEntries), in place in the workspace otherwise.
-constexpr int kMeanSmemEntries = 16384;
-
-__global__ void __launch_bounds__(1024)
-nf4_absmax_mean(double* __restrict__ gs, int64_t ng, int64_t p2, int64_t nb, float* __restrict__ offset) {
-  extern __shared__ double tree[];
-  pdl_allow_next();
-  pdl_wait();
-  const bool in_smem = p2 >= 4 && p2 / 4 <= kMeanSmemEntries;
-  double* s = in_smem ? tree : gs;
-  int64_t valid = ng;
-  int64_t h = p2 / 2;
-  if (in_smem) {   // the first two levels straight from the workspace into p2 / 4 entries
-    const int64_t q = p2 / 4;
-    auto g = [&](int64_t i) { return i < ng ? gs[i] : 0.0; };
-    for (int64_t i = threadIdx.x; i < q; i += blockDim.x)
-      s[i] = (g(i) + g(i + 2 * q)) + (g(i + q) + g(i + 3 * q));
-    __syncthreads();
-    valid = q;
-    h = q / 2;
-  }
-  for (; h >= 1; h /= 2) {
-    for (int64_t i = threadIdx.x; i < h; i += blockDim.x) {
-      const double a = (i < valid) ? s[i] : 0.0;
-      const double b = (i + h < valid) ? s[i + h] : 0.0;
-      s[i] = a + b;
-    }
-    valid = h;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) *offset = __double2float_rn(__ddiv_rn(s[0], static_cast<double>(nb)));
-}
-
-// Nested quantization of the block maxima: one warp per group of 256 maxima, eight per
-// lane.  c = a - offset; m = max |c| over the group; code = dyn8 code of RN(c / m).
-constexpr int kNestedWarps = 8;
-
-__global__ void __launch_bounds__(kNestedWarps * 32)
-nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __restrict__ offset_p,
-                  uint8_t* __restrict__ codes, float* __restrict__ nested, EncodeTables tabs) {
-  __shared__ float thr[256];
-  thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
-  __syncthreads();
-  pdl_allow_next();
-  pdl_wait();
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * kNestedWarps + warp;
-  if (g * kNested >= nb) return;
-  const float offset = *offset_p;
+// Nested codes of group g: one warp, eight maxima per lane.
+__device__ __forceinline__ void nested_group(const float* __restrict__ absmax, int64_t nb, int64_t g, float offset,
+                                             const float* thr, uint8_t* __restrict__ codes,
+                                             float* __restrict__ nested, int lane) {
   const int64_t b0 = g * kNested + 8 * lane;
   float c[8];
   const bool full = b0 + 8 <= nb && (reinterpret_cast<uintptr_t>(absmax + b0) & 15) == 0;
@@ -285,6 +398,24 @@ nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, const float* __r
       if (b0 + i < nb) codes[b0 + i] = static_cast<uint8_t>(q[i]);
   }
   if (lane == 0) nested[g] = m;
+}
+
+// Nested quantization of the block maxima: one warp per group of 256 maxima, eight per
+// lane.  c = a - offset (the offset written by the block pass's last CTA); m = max |c| over
+// the group; code = dyn8 code of RN(c / m).
+constexpr int kNestedWarps = 8;
+
+__global__ void __launch_bounds__(kNestedWarps * 32)
+nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, int64_t ng, const float* __restrict__ offset_p,
+                  uint8_t* __restrict__ codes, float* __restrict__ nested, EncodeTables tabs) {
+  __shared__ float thr[256];
+  thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
+  __syncthreads();
+  pdl_allow_next();
+  pdl_wait();
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kNestedWarps + (threadIdx.x >> 5);
+  if (g >= ng) return;
+  nested_group(absmax, nb, g, *offset_p, thr, codes, nested, threadIdx.x & 31);
 }
 
 // ---- dequantize -----------------------------------------------------------------
@@ -432,6 +563,56 @@ int64_t pow2_at_least(int64_t v) {
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
+// Ticket counters of the block pass (which CTA finishes last), in the library's own device
+// memory: zero at module load, and every double-quant call puts its counter back to zero.
+// Calls draw slots round-robin, so calls in flight at the same time (other streams, other
+// host threads) use different counters unless more than kTicketSlots of them overlap.
+constexpr unsigned kTicketSlots = 4096;
+__device__ unsigned g_quant_tickets[kTicketSlots];
+
+cudaError_t ticket_slot(unsigned** out) {
+  constexpr int kMaxDev = 64;
+  static unsigned* base[kMaxDev] = {};
+  static std::mutex mu;
+  static std::atomic<unsigned> next{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (base[dev] == nullptr) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_quant_tickets)) != cudaSuccess) return e;
+      base[dev] = static_cast<unsigned*>(p);
+    }
+    *out = base[dev] + next.fetch_add(1, std::memory_order_relaxed) % kTicketSlots;
+  }
+  return cudaSuccess;
+}
+
+// Resident CTAs per SM of an encode kernel (kind: input type and load width), per device,
+// looked up once (a racing first lookup stores the same value).
+template <typename K>
+cudaError_t encode_ctas_per_sm(K kernel, int kind, int* out) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cache[kMaxDev][4];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool slot = dev >= 0 && dev < kMaxDev;
+  if (slot) {
+    const int c = cache[dev][kind].load(std::memory_order_relaxed);
+    if (c > 0) return (*out = c), cudaSuccess;
+  }
+  int n = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kQuantThreads, 0);
+  if (e != cudaSuccess) return e;
+  n = n > 0 ? n : 1;
+  if (slot) cache[dev][kind].store(n, std::memory_order_relaxed);
+  *out = n;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 size_t quantize_ws_bytes(int64_t numel, int dq) {
@@ -450,32 +631,39 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
   double* gsum = out.double_quant
                      ? reinterpret_cast<double*>(static_cast<char*>(ws) + align256(sizeof(float) * nb))
                      : nullptr;
-  if (ng > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(ng));
-  cudaError_t e;
+  const int64_t p2 = pow2_at_least(ng);
+  unsigned* ticket = nullptr;
+  cudaError_t e = out.double_quant ? ticket_slot(&ticket) : cudaSuccess;
+  if (e != cudaSuccess) return e;
+  int resident = 0;
+  const bool v8 = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
   if (xd == NF4_F32)
-    e = launch_pdl(nf4_encode_blocks<float>, grid, dim3(kQuantThreads), 0, st, 1, static_cast<const float*>(x), numel,
-                   out.packed, absmax_f, gsum, et, status);
+    e = v8 ? encode_ctas_per_sm(nf4_encode_blocks<float, true>, 0, &resident)
+           : encode_ctas_per_sm(nf4_encode_blocks<float, false>, 1, &resident);
   else
-    e = launch_pdl(nf4_encode_blocks<__nv_bfloat16>, grid, dim3(kQuantThreads), 0, st, 1,
-                   static_cast<const __nv_bfloat16*>(x), numel, out.packed, absmax_f, gsum, et, status);
+    e = v8 ? encode_ctas_per_sm(nf4_encode_blocks<__nv_bfloat16, true>, 2, &resident)
+           : encode_ctas_per_sm(nf4_encode_blocks<__nv_bfloat16, false>, 3, &resident);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(ng, static_cast<int64_t>(resident) * device_sm_count())));
+  const dim3 block(kQuantThreads);
+  if (xd == NF4_F32) {
+    const auto* xf = static_cast<const float*>(x);
+    e = v8 ? launch_pdl(nf4_encode_blocks<float, true>, grid, block, 0, st, 1, xf, numel, ng, out.packed, absmax_f,
+                        gsum, p2, ticket, out.offset, et, status)
+           : launch_pdl(nf4_encode_blocks<float, false>, grid, block, 0, st, 1, xf, numel, ng, out.packed, absmax_f,
+                        gsum, p2, ticket, out.offset, et, status);
+  } else {
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    e = v8 ? launch_pdl(nf4_encode_blocks<__nv_bfloat16, true>, grid, block, 0, st, 1, xb, numel, ng, out.packed,
+                        absmax_f, gsum, p2, ticket, out.offset, et, status)
+           : launch_pdl(nf4_encode_blocks<__nv_bfloat16, false>, grid, block, 0, st, 1, xb, numel, ng, out.packed,
+                        absmax_f, gsum, p2, ticket, out.offset, et, status);
+  }
   note_launch();
   if (e != cudaSuccess || !out.double_quant) return e;
-  const int64_t p2 = pow2_at_least(ng);
-  const size_t mean_smem = (p2 >= 4 && p2 / 4 <= kMeanSmemEntries) ? sizeof(double) * static_cast<size_t>(p2 / 4) : 0;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(nf4_absmax_mean, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(sizeof(double) * kMeanSmemEntries));
-  });
-  if (attr != cudaSuccess) return attr;
-  e = launch_pdl(nf4_absmax_mean, dim3(1), dim3(1024), mean_smem, st, 1, gsum, ng, p2, nb, out.offset);
-  note_launch();
-  if (e != cudaSuccess) return e;
   const dim3 ngrid(static_cast<unsigned>((ng + kNestedWarps - 1) / kNestedWarps));
   e = launch_pdl(nf4_encode_nested, ngrid, dim3(kNestedWarps * 32), 0, st, 1, static_cast<const float*>(absmax_f), nb,
-                 static_cast<const float*>(out.offset), static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
+                 ng, static_cast<const float*>(out.offset), static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
   note_launch();
   return e;
 }
@@ -519,6 +707,19 @@ cudaError_t launch_decode_with_prep(const Nf4View& w, void* y, bool f16, const P
     e = w.dq ? launch_pdl(nf4_decode_prep<__nv_bfloat16, true>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt, jobs, dc)
              : launch_pdl(nf4_decode_prep<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, w, yb, dt, jobs, dc);
   }
+  note_launch();
+  return e;
+}
+
+cudaError_t launch_prep_only(bool f16, const PrepJobs& jobs, unsigned prep_ctas, cudaStream_t st) {
+  if (prep_ctas == 0) return cudaSuccess;
+  const dim3 grid(prep_ctas);
+  const DecodeTables& dt = decode_tables();
+  const Nf4View none{};
+  cudaError_t e = f16 ? launch_pdl(nf4_decode_prep<__half, false>, grid, dim3(kDeqThreads), 0, st, 1, none,
+                                   static_cast<__half*>(nullptr), dt, jobs, 0u)
+                      : launch_pdl(nf4_decode_prep<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, none,
+                                   static_cast<__nv_bfloat16*>(nullptr), dt, jobs, 0u);
   note_launch();
   return e;
 }

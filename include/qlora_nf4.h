@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define QLORA_NF4_ABI_VERSION 2
+#define QLORA_NF4_ABI_VERSION 3
 
 typedef enum {
   NF4_OK = 0,
@@ -238,6 +238,29 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
                             void* dx, float* dA, float* dB,
                             void* ws, size_t ws_bytes, void* stream);
 
+/* The 16-bit profiles with the weight already decoded, so that one decode serves several
+ * calls, e.g. the forward and the backward of one step ([ADAPT] "Fused GPU NF4 decodes inside
+ * the matrix kernel": the reconstructed weight is what the contraction multiplies).
+ * w16: device [N, K] row-major in the compute dtype (NF4_BF16 or NF4_F16; NF4_ERR_DTYPE
+ * otherwise), holding the weight as nf4_dequantize writes it for that dtype; the library
+ * cannot check that, and with any other contents the result is that of those contents.
+ * Every other argument, the arithmetic and the results are those of qlora_linear_fwd /
+ * qlora_linear_bwd for the weight w16 decodes, bit for bit on the tiled path (every M; the
+ * small-M pass of qlora_linear_fwd, which decodes in registers, is not used here).  The
+ * workspaces hold no decoded copy (2*N*K bytes smaller than the tiled path's).  w16 is read,
+ * never written, and must stay unchanged until the call's work on the stream is done. */
+size_t qlora_fwd_w16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
+size_t qlora_bwd_w16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute);
+nf4_status qlora_linear_fwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                                qlora_scale_mode mode, nf4_dtype compute,
+                                const void* x, const void* w16, const float* A, const float* B,
+                                void* y, float* T_out, void* ws, size_t ws_bytes, void* stream);
+nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
+                                qlora_scale_mode mode, nf4_dtype compute,
+                                const void* dy, const void* x, const float* T, const void* w16,
+                                const float* A, const float* B, void* dx, float* dA, float* dB,
+                                void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronize `stream`, then return the current device's status word (NF4_OK if no
  * device-side condition was recorded); clear != 0 resets it to NF4_OK. */
 nf4_status qlora_last_device_status(void* stream, int32_t clear);
@@ -261,7 +284,7 @@ int64_t nf4_kernel_launch_count(void);
  * the number of launches, and with reset != 0 clears that kind.  No device memory
  * is allocated; events are created once and reused. */
 typedef enum {
-  NF4_TIME_QUANTIZE = 0,    /* the three quantize kernels of one nf4_quantize call */
+  NF4_TIME_QUANTIZE = 0,    /* the kernels of one nf4_quantize call (two; three above 2^26 elements) */
   NF4_TIME_DEQUANTIZE = 1,  /* the decode kernel */
   NF4_TIME_FWD_GEMM = 2,    /* base contraction of the forward (y) */
   NF4_TIME_DX_GEMM = 3,     /* base contraction of the input gradient (dX) */

@@ -41,7 +41,7 @@ def test_every_declared_function_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(binding.ENTRY_POINTS) <= set(names)
-    assert lib.nf4_abi_version() == 2
+    assert lib.nf4_abi_version() == 3
 
 
 def test_noalloc_limit_has_one_source(lib):
@@ -128,6 +128,23 @@ def test_validation_refuses_bad_arguments(lib):
     b = lambda wsz: lib.qlora_linear_bwd(  # noqa: E731
         4, 64, 128, 8, ctypes.c_float(16.0), 0, 1, p, p, p, ctypes.byref(w), p, p, p, p, p, ws, wsz, None)
     assert b(0) == binding.NF4_ERR_WORKSPACE
+
+    # the decoded-weight entry points: 16-bit compute only, a 16-byte aligned weight
+    fw = lambda M, N, K, r, cd=1, w16=p, wsz=1 << 30: lib.qlora_linear_fwd_w16(  # noqa: E731
+        M, N, K, r, ctypes.c_float(16.0), 0, cd, p, w16, p, p, p, p, ws, wsz, None)
+    assert fw(4, 64, 128, 8, cd=binding.NF4_F32) == binding.NF4_ERR_DTYPE
+    assert fw(4, 64, 128, 8, w16=None) == binding.NF4_ERR_ARG
+    assert fw(4, 64, 128, 8, w16=ctypes.c_void_p(0x50000002)) == binding.NF4_ERR_ALIGN
+    assert fw(4, 100, 96, 8) == binding.NF4_ERR_SHAPE
+    assert fw(4, 64, 128, 8, wsz=1) == binding.NF4_ERR_WORKSPACE
+    assert lib.qlora_fwd_w16_workspace_bytes(4, 64, 128, 8, binding.NF4_F32) == 0
+    assert 0 < lib.qlora_fwd_w16_workspace_bytes(4096, 14336, 4096, 16, 1) < lib.qlora_fwd_workspace_bytes(
+        4096, 14336, 4096, 16, 1)
+    bw = lambda cd=1, w16=p, wsz=1 << 30: lib.qlora_linear_bwd_w16(  # noqa: E731
+        4, 64, 128, 8, ctypes.c_float(16.0), 0, cd, p, p, p, w16, p, p, p, p, p, ws, wsz, None)
+    assert bw(cd=binding.NF4_F32) == binding.NF4_ERR_DTYPE
+    assert bw(w16=None) == binding.NF4_ERR_ARG
+    assert bw(wsz=1) == binding.NF4_ERR_WORKSPACE
 
     # selected embedding rows: E [100, 64]
     e = _fake_tensor(100 * 64)

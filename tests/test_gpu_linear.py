@@ -216,3 +216,37 @@ def test_f16_profile_llama8b_sampled_rows(lib, name):
 
 def test_f16_profile_rslora_without_double_quant(lib):
     _run_case(96, 520, 512, 8, 16.0, "f16", mode=binding.SCALE_RSLORA, seed=3, dq=False)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("M,N,K,r", [(5, 40, 128, 3), (300, 264, 576, 16), (700, 1344, 1344, 16)])
+def test_decoded_weight_entry_points_equal_the_nf4_calls(lib, dtype, M, N, K, r):
+    """qlora_linear_fwd_w16 / _bwd_w16 with the weight as nf4_dequantize writes it: every output
+    bit-identical to the tiled NF4-input calls (M > 16; at M <= 16 the NF4 forward takes the
+    small-M pass, so the comparison there is the oracle's tolerance)."""
+    q, w_deq = _quantized_weight(N, K, 31 + M)
+    x = torch.from_numpy(wl.normal((M, K), 1.0, 1, 32 + M)).to(DEV).to(dtype)
+    dy = torch.from_numpy(wl.normal((M, N), 1.0, 1, 33 + M)).to(DEV).to(dtype)
+    A, B = (torch.from_numpy(t).to(DEV) for t in wl.adapters(N, K, r, 1, 34 + M))
+    w16 = binding.nf4_dequantize(q, dtype)
+    y, T = binding.qlora_linear_fwd(x, q, A, B, 16.0)
+    y2, T2 = binding.qlora_linear_fwd_w16(x, w16, A, B, 16.0)
+    dx, dA, dB = binding.qlora_linear_bwd(dy, x, T, q, A, B, 16.0)
+    dx2, dA2, dB2 = binding.qlora_linear_bwd_w16(dy, x, T, w16, A, B, 16.0)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    same = [(dx, dx2), (dA, dA2), (dB, dB2)]
+    if M > 16:
+        same += [(y, y2), (T, T2)]
+    for a, b in same:
+        assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype != torch.float32 else b.view(torch.int32))
+    if M <= 16:
+        compute = "bf16" if dtype == torch.bfloat16 else "f16"
+        xh = x.float().cpu().numpy()
+        Ah, Bh = A.cpu().numpy(), B.cpu().numpy()
+        s = qlora.lora_scale(16.0, r, "lora")
+        y_ref, T_ref = qlora.forward(xh, w_deq, Ah, Bh, s, compute)
+        fb = parity.forward_bounds(xh, w_deq, Ah, Bh, s, compute, y_ref, T_ref)
+        parity.check({"y": y2.float().cpu().numpy(), "T": T2.cpu().numpy()}, {"y": y_ref, "T": T_ref},
+                     {"y": fb["y"], "T": fb["T"]}, compute)

@@ -86,6 +86,62 @@ def test_quantize_near_every_threshold(lib):
     assert binding.device_status() == binding.NF4_OK
 
 
+def test_quantize_bf16_every_ratio(lib):
+    """bf16 input: every quotient of two bf16 values that the encoder's bf16 path decides
+    from one fused multiply-add.  Each block holds its maximum a and 63 values x; a runs
+    over all 128 bf16 significands at binary exponents inside the range where 1/a is normal
+    (-126 .. 125) and outside it (126, 127, and subnormal a); x runs over all significands
+    at a*2^-d, d = 0..17, both signs.  The codes must be the oracle's, which divides."""
+    sig = 1.0 + np.arange(128) / 128.0
+    rng = np.random.default_rng(5)
+    blocks = []
+    for ea in (-126, -70, -3, 0, 7, 88, 125, 126, 127, -127, -131):
+        for ma in sig:
+            a = np.float32(ma * 2.0 ** ea)
+            xs = np.concatenate([sgn * sig * 2.0 ** (ea - d) for d in range(18) for sgn in (1.0, -1.0)])
+            xs = xs[np.abs(xs) <= np.float64(a)].astype(np.float32)
+            xs = rng.permutation(xs)
+            for c0 in range(0, xs.size, 63):
+                chunk = xs[c0:c0 + 63]
+                blocks.append(np.concatenate([[a], chunk, np.zeros(63 - chunk.size, np.float32)]))
+    x = np.concatenate(blocks).astype(np.float32)
+    xd = _to_device(x, torch.bfloat16)
+    xh = _host_values(xd)
+    # the block maxima survive the rounding to bf16 as maxima
+    assert np.array_equal(onf4.block_absmax(xh), np.abs(xh[0::64]))
+    for dq in (False, True):
+        q = binding.nf4_quantize(xd, double_quant=dq)
+        _assert_same_quant(q, onf4.quantize(xh, double_quant=dq))
+    assert binding.device_status() == binding.NF4_OK
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_16_byte_aligned_view(lib, dtype):
+    """An input 16 but not 32 bytes aligned takes the 16-byte loads; same bytes as the oracle."""
+    n = 3 * 16384 + 1000
+    per16 = 16 // torch.tensor([], dtype=dtype).element_size()
+    big = wl.device_normal((n + per16,), 0.02, wl.seed_for(5, 77), DEV, dtype)
+    x = big[per16:]
+    assert x.data_ptr() % 32 == 16
+    for dq in (True, False):
+        q = binding.nf4_quantize(x, double_quant=dq)
+        _assert_same_quant(q, onf4.quantize(_host_values(x), double_quant=dq))
+    assert binding.device_status() == binding.NF4_OK
+
+
+@pytest.mark.parametrize("n", [2 ** 26, 2 ** 26 + 16384])
+def test_quantize_offset_inside_and_outside_the_nested_pass(lib, n):
+    """At 4096 groups of 256 blocks the offset is computed inside the nested pass; one group
+    more takes the separate one-CTA tree first.  Both give the oracle's offset, nested
+    maxima and codes (sampled groups), bf16 input."""
+    x = wl.device_normal((n,), 0.02, wl.seed_for(5, n % 1000), DEV, torch.bfloat16)
+    q = binding.nf4_quantize(x)
+    x_host = _host_values(x)
+    ng = -(-n // 16384)
+    _sampled_groups_check(x_host, q, [0, 1, ng // 2, ng - 2, ng - 1])
+    assert binding.device_status() == binding.NF4_OK
+
+
 def test_quantize_special_blocks(lib):
     nf4 = cb.nf4_codebook()
     x = np.zeros(64 * 300 + 5, np.float32)
