@@ -30,7 +30,7 @@ ENTRY_POINTS = (
     "qlora_linear_bwd", "qlora_last_device_status", "nf4_kernel_launch_count",
     "qlora_fwd_batch_workspace_bytes", "qlora_linear_fwd_batch",
     "qlora_fwd_w16_workspace_bytes", "qlora_bwd_w16_workspace_bytes", "qlora_linear_fwd_w16",
-    "qlora_linear_bwd_w16",
+    "qlora_linear_bwd_w16", "nf4_quantize_batch_workspace_bytes", "nf4_quantize_batch",
 )
 
 
@@ -52,6 +52,11 @@ class _FwdItem(ctypes.Structure):
                 ("alpha", ctypes.c_float), ("mode", ctypes.c_int32), ("W", ctypes.POINTER(_Nf4Tensor)),
                 ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("T_out", ctypes.c_void_p)]
+
+
+class _QuantItem(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("x_dtype", ctypes.c_int32), ("numel", ctypes.c_int64),
+                ("out", ctypes.POINTER(_Nf4Tensor))]
 
 
 _LIB = None
@@ -82,6 +87,8 @@ def load() -> ctypes.CDLL:
         "nf4_quantize_workspace_bytes": (sz, [i64, i32]),
         "nf4_quantize": (i32, [vp, i32, i64, tp, vp, sz, vp]),
         "nf4_dequantize": (i32, [tp, vp, i32, vp]),
+        "nf4_quantize_batch_workspace_bytes": (sz, [i32, ctypes.POINTER(_QuantItem)]),
+        "nf4_quantize_batch": (i32, [i32, ctypes.POINTER(_QuantItem), vp, sz, vp]),
         "nf4_quantize_noalloc": (i32, [vp, i32, i64, tp, vp]),
         "nf4_embedding_rows": (i32, [tp, i64, i64, vp, i64, vp, i32, vp]),
         "nf4_merge_lora": (i32, [i64, i64, i32, f32, i32, tp, vp, vp, vp, i32, vp]),
@@ -212,6 +219,33 @@ def nf4_quantize(x: torch.Tensor, double_quant: bool = True, out: Nf4Tensor = No
     _check(lib.nf4_quantize(_ptr(x), _dtype_code(x.dtype), x.numel(), ctypes.byref(cs), _ptr(ws),
                             ws.numel(), _stream(stream)), "nf4_quantize")
     return out
+
+
+def _quant_items(pairs):
+    arr = (_QuantItem * len(pairs))()
+    keep = []
+    for i, (x, q) in enumerate(pairs):
+        cs = q.c_struct()
+        keep.append(cs)
+        arr[i] = _QuantItem(x.data_ptr(), _dtype_code(x.dtype), x.numel(), ctypes.pointer(cs))
+    return arr, keep
+
+
+def nf4_quantize_batch_workspace_bytes(pairs) -> int:
+    """Workspace bytes of nf4_quantize_batch for [(x, out), ...]."""
+    arr, _keep = _quant_items(pairs)
+    return int(load().nf4_quantize_batch_workspace_bytes(len(pairs), arr))
+
+
+def nf4_quantize_batch(pairs, workspace: torch.Tensor = None, stream=None):
+    """Quantize several tensors in one call: ``pairs`` is [(x, out Nf4Tensor), ...] (x contiguous,
+    out preallocated); each out gets what nf4_quantize(x, out=out) gives.  Returns the outs."""
+    lib = load()
+    arr, _keep = _quant_items(pairs)
+    need = lib.nf4_quantize_batch_workspace_bytes(len(pairs), arr)
+    ws = workspace if workspace is not None else _workspace(need, pairs[0][0].device)
+    _check(lib.nf4_quantize_batch(len(pairs), arr, _ptr(ws), ws.numel(), _stream(stream)), "nf4_quantize_batch")
+    return [q for _, q in pairs]
 
 
 def nf4_quantize_noalloc(x: torch.Tensor, out: Nf4Tensor, stream=None) -> Nf4Tensor:

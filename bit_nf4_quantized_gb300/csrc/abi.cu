@@ -468,6 +468,52 @@ nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel, const n
                                    static_cast<cudaStream_t>(stream)));
 }
 
+size_t nf4_quantize_batch_workspace_bytes(int32_t count, const nf4_quantize_item* items) {
+  if (count < 1 || items == nullptr) return 0;
+  size_t total = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    if (items[i].numel <= 0 || items[i].out == nullptr) return 0;
+    total += a256(quantize_ws_bytes(items[i].numel, items[i].out->double_quant ? 1 : 0));
+  }
+  return total;
+}
+
+nf4_status nf4_quantize_batch(int32_t count, const nf4_quantize_item* items, void* ws, size_t ws_bytes,
+                              void* stream) {
+  if (count < 1 || items == nullptr) return NF4_ERR_ARG;
+  size_t need = 0;
+  for (int32_t i = 0; i < count; ++i) {   // every item is checked before anything is enqueued
+    const nf4_quantize_item& it = items[i];
+    if (it.x == nullptr || it.numel <= 0 || it.out == nullptr) return NF4_ERR_ARG;
+    if (it.x_dtype != NF4_F32 && it.x_dtype != NF4_BF16) return NF4_ERR_DTYPE;
+    const nf4_status st = check_tensor(it.out, it.numel);
+    if (st != NF4_OK) return st;
+    if (!aligned16(it.x)) return NF4_ERR_ALIGN;
+    need += a256(quantize_ws_bytes(it.numel, it.out->double_quant ? 1 : 0));
+  }
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
+  int* status = nullptr;
+  nf4_status st = device_status_ptr(&status);
+  if (st != NF4_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  KernelTimer timer(NF4_TIME_QUANTIZE, cs);
+  // runs of up to kQuantBatchMax items of one input type, in the items' order
+  std::vector<QuantJob> jobs;
+  char* w = static_cast<char*>(ws);
+  for (int32_t i = 0; i < count;) {
+    jobs.clear();
+    const nf4_dtype xd = items[i].x_dtype;
+    for (; i < count && items[i].x_dtype == xd && static_cast<int>(jobs.size()) < kQuantBatchMax; ++i) {
+      jobs.push_back(QuantJob{items[i].x, items[i].numel, items[i].out, w});
+      w += a256(quantize_ws_bytes(items[i].numel, items[i].out->double_quant ? 1 : 0));
+    }
+    const cudaError_t e = launch_quantize_batch(jobs.data(), static_cast<int>(jobs.size()), xd, status, cs);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return NF4_OK;
+}
+
 nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream) {
   if (w == nullptr || y == nullptr) return NF4_ERR_ARG;
   if (out_dtype != NF4_F32 && out_dtype != NF4_BF16 && out_dtype != NF4_F16) return NF4_ERR_DTYPE;

@@ -162,6 +162,16 @@ struct Nf4View {
 // ---- quant.cu -----------------------------------------------------------------
 cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf4_tensor& out,
                             void* ws, int* status, cudaStream_t st);
+// Up to kQuantBatchMax tensors of one input type in one block pass and one nested pass;
+// each job's workspace slice holds quantize_ws_bytes(numel, dq) bytes.
+constexpr int kQuantBatchMax = 8;
+struct QuantJob {
+  const void* x;
+  int64_t numel;
+  const nf4_tensor* out;
+  void* ws;
+};
+cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int* status, cudaStream_t st);
 size_t quantize_ws_bytes(int64_t numel, int dq);
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st);
 struct PrepJobs;

@@ -112,14 +112,6 @@ __device__ __forceinline__ uint32_t lane_absmax_bits(const uint32_t (&w)[8 * siz
   return max(m2 & 0xFFFFu, m2 >> 16) << 16;
 }
 
-// Codes of one lane (32 elements, one half block) with the block maximum a = bits mb.
-// Words: element i sits in word i / 8, byte (i % 8) / 2, high nibble for even i; a word is
-// built by shifting in elements 6, 7, 4, 5, 2, 3, 0, 1 of its eight.
-//   bf16 input, a in [2^-126, 2^126), cut table valid: code = base + (bits(q') >= cut),
-//     q' = fl(x*r + 3), r = RN(1/a), from the bucket row of q' (no band: see EncodeTables).
-//   fp32 input: q = x*r and q' pick the bucket; code = base + (q >= hi); a q inside the
-//     band [lo, hi) marks the lane unsure, and an unsure lane (or a, r not finite, or the
-//     bucket table unusable) is redone with the IEEE quotient RN(x / a).
 // Bucket row (bits(q') >> 17) of the lane's table copy; tab_base is the shared-memory address
 // of row 0 of the copy minus 8191 rows.
 __device__ __forceinline__ uint2 bucket_row(uint32_t tab_base, uint32_t qb) {
@@ -128,6 +120,14 @@ __device__ __forceinline__ uint2 bucket_row(uint32_t tab_base, uint32_t qb) {
   return e;
 }
 
+// Codes of one lane (32 elements, one half block) with the block maximum a = bits mb.
+// Words: element i sits in word i / 8, byte (i % 8) / 2, high nibble for even i; a word is
+// built by shifting in elements 6, 7, 4, 5, 2, 3, 0, 1 of its eight.
+//   bf16 input, a in [2^-126, 2^126), cut table valid: code = base + (bits(q') >= cut),
+//     q' = fl(x*r + 3), r = RN(1/a), from the bucket row of q' (no band: see EncodeTables).
+//   fp32 input: q = x*r and q' pick the bucket; code = base + (q >= hi); a q inside the
+//     band [lo, hi) marks the lane unsure, and an unsure lane (or a, r not finite, or the
+//     bucket table unusable) is redone with the IEEE quotient RN(x / a).
 template <typename Tin>
 __device__ __forceinline__ void lane_codes(const uint32_t (&w)[8 * sizeof(Tin)], uint32_t mb, uint32_t tab_base,
                                            bool fast_ok, const float* thr, uint32_t (&words)[4]) {
@@ -272,28 +272,59 @@ __device__ __forceinline__ float offset_tree(double* gs, int64_t ng, int64_t p2,
   return offset;
 }
 
+// One tensor of a block pass.  Its groups are numbers g0 .. g0 + ng - 1 of the launch's
+// concatenated group list; `ctas` CTAs (min(ng, grid)) take at least one of them.
+struct EncodeItem {
+  const void* x;
+  int64_t numel, ng, g0, p2;
+  uint8_t* packed;
+  float* absmax;          // fp32 maxima: the output, or (double quant) the workspace's copy
+  double* group_sum;      // double quant: the workspace's group sums, p2 entries; else null
+  unsigned* ticket;       // double quant: a zero counter of the library's ticket pool
+  float* offset;          // double quant: the tensor's offset
+  unsigned ctas;
+};
+constexpr int kEncodeBatch = kQuantBatchMax;
+struct EncodeBatch {
+  EncodeItem it[kEncodeBatch];
+  int n;
+  int64_t total;          // groups of all items
+};
+
+__device__ __forceinline__ int item_of(const EncodeItem* items, int n, int64_t g) {
+  int i = 0;
+#pragma unroll 1
+  while (i + 1 < n && g >= items[i + 1].g0) ++i;
+  return i;
+}
+
 // Block pass: absmax, 4-bit codes and packing, one nested group (256 blocks, 16384
-// elements) at a time; with double quantization also the float64 pairwise-tree sum of each
-// group's absmax.  Persistent: CTA c takes groups c, c + G, c + 2G, ... (G = gridDim.x,
-// sized to the CTAs resident at once).  Warp w codes rows 2w and 2w + 1 of a group (1024
-// elements each; lane l elements 32l .. 32l + 31, so a lane pair holds one block); after
-// coding a row it loads the same row of its next group into the row's registers, so one
-// row per warp is always in flight while the other is coded.  The group's 256 maxima meet
-// in shared memory (two buffers, by group parity) and one warp, rotating, sums them.
+// elements) at a time, over the groups of up to 8 tensors of one input type; with double
+// quantization also the float64 pairwise-tree sum of each group's absmax.  Persistent: CTA c
+// takes groups c, c + G, c + 2G, ... of the concatenated list (G = gridDim.x, sized to the
+// CTAs resident at once).  Warp w codes rows 2w and 2w + 1 of a group (1024 elements each;
+// lane l elements 32l .. 32l + 31, so a lane pair holds one block); after coding a row it
+// loads the same row of its next group into the row's registers, so one row per warp is
+// always in flight while the other is coded.  The group's 256 maxima meet in shared memory
+// (two buffers, by group parity) and one warp, rotating, sums them.  When a CTA leaves a
+// tensor it takes that tensor's ticket; the CTA that draws the last one sums the tensor's
+// group sums into its offset and puts the counter back to zero (the pattern of a grid
+// barrier's arrival: the CTA's threads meet, thread 0 fences and counts).
 template <typename Tin, bool kV8>
 __global__ void __launch_bounds__(kQuantThreads, sizeof(Tin) == 2 ? 3 : 2)
-nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, int64_t ng, uint8_t* __restrict__ packed,
-                  float* __restrict__ absmax, double* __restrict__ group_sum, int64_t p2,
-                  unsigned* __restrict__ ticket, float* __restrict__ offset, EncodeTables tabs, int* status) {
+nf4_encode_blocks(EncodeBatch b, EncodeTables tabs, int* status) {
   __shared__ float thr[16];
   // bucket rows, 16 copies: the 8-byte lookups of a warp are served half a warp at a time,
   // and lanes l, l + 16 never meet in one bank access.  bf16: {cut, base}; fp32: {bits of
   // lo with the base code in its low 4 bits, bits of hi}
-  // the tables and the group-sum buffers, then (last CTA) the offset tree's 1024 entries
-  __shared__ __align__(16) unsigned char smem_raw[66 * 16 * 8 + 2 * kNested * 8];
+  __shared__ uint2 tab[66][16];
+  __shared__ double gsum[2][kNested];
+  __shared__ double tree[1024];      // the offset tree of a tensor this CTA finishes last
+  __shared__ EncodeItem items[kEncodeBatch];   // indexed at run time: kept out of the parameters
   __shared__ unsigned s_last;
-  auto tab = reinterpret_cast<uint2 (*)[16]>(smem_raw);
-  auto gsum = reinterpret_cast<double (*)[kNested]>(smem_raw + 66 * 16 * 8);
+#pragma unroll
+  for (int k = 0; k < kEncodeBatch; ++k)
+    if (threadIdx.x == k) items[k] = b.it[k];   // static indices into the parameters
   if (threadIdx.x < 16) thr[threadIdx.x] = tabs.nf4_thr[threadIdx.x];
   for (int i = threadIdx.x; i < 66 * 16; i += kQuantThreads) {
     const int k = i >> 4;
@@ -312,55 +343,72 @@ nf4_encode_blocks(const Tin* __restrict__ x, int64_t numel, int64_t ng, uint8_t*
   const uint32_t tab_base = static_cast<uint32_t>(__cvta_generic_to_shared(&tab[0][lane & 15])) - 8191u * 128u;
   constexpr int kW = 8 * sizeof(Tin);
   const int64_t lane_off = warp * 2048 + 32 * lane;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kGroupElems;
-  int64_t g = blockIdx.x;
-  uint32_t wa[kW], wb[kW];
-  lane_words<Tin, kV8>(x, numel, g * kGroupElems + lane_off, wa);
-  lane_words<Tin, kV8>(x, numel, g * kGroupElems + lane_off + 1024, wb);
-  bool nonfinite = false;
   const int slot = warp * 32 + (lane >> 1);    // block of the group held by the lane pair (row 2w)
+  int64_t g = blockIdx.x;
+  int ci = item_of(items, b.n, g);
+  uint32_t wa[kW], wb[kW];
+  {
+    const EncodeItem& e = items[ci];
+    const Tin* x = static_cast<const Tin*>(e.x);
+    lane_words<Tin, kV8>(x, e.numel, (g - e.g0) * kGroupElems + lane_off, wa);
+    lane_words<Tin, kV8>(x, e.numel, (g - e.g0) * kGroupElems + lane_off + 1024, wb);
+  }
+  bool nonfinite = false;
 #pragma unroll 1
-  for (int it = 0; g < ng; g += gridDim.x, ++it) {
-    const int64_t e0 = g * kGroupElems + lane_off;
-    const bool more = g + gridDim.x < ng;
+  for (int it = 0; g < b.total; ++it) {
+    const EncodeItem& e = items[ci];
+    const int64_t gl = g - e.g0;                 // group within the tensor
+    const int64_t e0 = gl * kGroupElems + lane_off;
+    const int64_t gn = g + gridDim.x;            // this CTA's next group
+    const int ni = gn < b.total ? item_of(items, b.n, gn) : ci;
     double* gs = gsum[it & 1];
-    nonfinite |= encode_row<Tin>(wa, e0, numel, packed, absmax, gs + slot, tab_base, fast_ok, thr, lane);
-    if (more) lane_words<Tin, kV8>(x, numel, e0 + stride, wa);
-    nonfinite |= encode_row<Tin>(wb, e0 + 1024, numel, packed, absmax, gs + slot + 16, tab_base, fast_ok, thr, lane);
-    if (more) lane_words<Tin, kV8>(x, numel, e0 + 1024 + stride, wb);
-    if (group_sum == nullptr) continue;
-    __syncthreads();
-    if (warp != (it & 7)) continue;
-    // float64 pairwise tree s[i] += s[i + h], h = 128, 64, ..., 1, by one warp: lane l holds
-    // s[l + 32 m]; the levels h >= 32 add within the lane, the rest across lanes
-    double t[kNested / 32];
+    nonfinite |= encode_row<Tin>(wa, e0, e.numel, e.packed, e.absmax, gs + slot, tab_base, fast_ok, thr, lane);
+    if (gn < b.total)
+      lane_words<Tin, kV8>(static_cast<const Tin*>(items[ni].x), items[ni].numel,
+                           (gn - items[ni].g0) * kGroupElems + lane_off, wa);
+    nonfinite |= encode_row<Tin>(wb, e0 + 1024, e.numel, e.packed, e.absmax, gs + slot + 16, tab_base, fast_ok, thr,
+                                 lane);
+    if (gn < b.total)
+      lane_words<Tin, kV8>(static_cast<const Tin*>(items[ni].x), items[ni].numel,
+                           (gn - items[ni].g0) * kGroupElems + lane_off + 1024, wb);
+    if (e.group_sum != nullptr) {
+      __syncthreads();
+      if (warp == (it & 7)) {
+        // float64 pairwise tree s[i] += s[i + h], h = 128, 64, ..., 1, by one warp: lane l
+        // holds s[l + 32 m]; the levels h >= 32 add within the lane, the rest across lanes
+        double t[kNested / 32];
 #pragma unroll
-    for (int m = 0; m < kNested / 32; ++m) t[m] = gs[lane + 32 * m];
+        for (int m = 0; m < kNested / 32; ++m) t[m] = gs[lane + 32 * m];
 #pragma unroll
-    for (int h = kNested / 64; h >= 1; h >>= 1)
+        for (int h = kNested / 64; h >= 1; h >>= 1)
 #pragma unroll
-      for (int m = 0; m < h; ++m) t[m] += t[m + h];
+          for (int m = 0; m < h; ++m) t[m] += t[m + h];
 #pragma unroll
-    for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
-    if (lane == 0) group_sum[g] = t[0];
+        for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
+        if (lane == 0) e.group_sum[gl] = t[0];
+      }
+      if (gn >= e.g0 + e.ng) {   // this CTA's last group of the tensor: its ticket
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          __threadfence();
+          s_last = (atomicAdd(e.ticket, 1u) == e.ctas - 1) ? 1u : 0u;
+        }
+        __syncthreads();
+        if (s_last != 0) {
+          __threadfence();
+          const float off = offset_tree(e.group_sum, e.ng, e.p2, (e.numel + kBlock - 1) / kBlock, tree);
+          if (threadIdx.x == 0) {
+            *e.offset = off;
+            *e.ticket = 0u;
+          }
+          __syncthreads();   // `tree` is free again before this CTA could need it for another tensor
+        }
+      }
+    }
+    g = gn;
+    ci = ni;
   }
   if (nonfinite) atomicCAS(status, 0, static_cast<int>(NF4_ERR_NONFINITE));
-  if (group_sum == nullptr) return;
-  // the last CTA to finish sums the group sums into the offset (every thread fences its
-  // writes before the CTA takes its ticket, so all group sums are visible to that CTA), then
-  // puts the ticket counter back to zero for the next call that draws this slot
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
-  __syncthreads();
-  if (s_last == 0) return;
-  __threadfence();
-  const float off = offset_tree(group_sum, ng, p2, (numel + kBlock - 1) / kBlock,
-                                reinterpret_cast<double*>(smem_raw));
-  if (threadIdx.x == 0) {
-    *offset = off;
-    *ticket = 0u;
-  }
 }
 
 // Nested codes of group g: one warp, eight maxima per lane.
@@ -401,21 +449,41 @@ __device__ __forceinline__ void nested_group(const float* __restrict__ absmax, i
 }
 
 // Nested quantization of the block maxima: one warp per group of 256 maxima, eight per
-// lane.  c = a - offset (the offset written by the block pass's last CTA); m = max |c| over
-// the group; code = dyn8 code of RN(c / m).
+// lane, over the groups of up to 8 tensors (numbered as in the block pass).  c = a - offset
+// (the offset written by the block pass's last CTA of the tensor); m = max |c| over the
+// group; code = dyn8 code of RN(c / m).
 constexpr int kNestedWarps = 8;
 
+struct NestedItem {
+  const float* absmax;   // the fp32 maxima
+  int64_t nb, ng, g0;
+  const float* offset;
+  uint8_t* codes;
+  float* nested;
+};
+struct NestedBatch {
+  NestedItem it[kEncodeBatch];
+  int n;
+  int64_t total;
+};
+
 __global__ void __launch_bounds__(kNestedWarps * 32)
-nf4_encode_nested(const float* __restrict__ absmax, int64_t nb, int64_t ng, const float* __restrict__ offset_p,
-                  uint8_t* __restrict__ codes, float* __restrict__ nested, EncodeTables tabs) {
+nf4_encode_nested(NestedBatch b, EncodeTables tabs) {
   __shared__ float thr[256];
+  __shared__ NestedItem items[kEncodeBatch];
   thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
+#pragma unroll
+  for (int k = 0; k < kEncodeBatch; ++k)
+    if (threadIdx.x == k) items[k] = b.it[k];
   __syncthreads();
   pdl_allow_next();
   pdl_wait();
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kNestedWarps + (threadIdx.x >> 5);
-  if (g >= ng) return;
-  nested_group(absmax, nb, g, *offset_p, thr, codes, nested, threadIdx.x & 31);
+  if (g >= b.total) return;
+  int i = 0;
+  while (i + 1 < b.n && g >= items[i + 1].g0) ++i;
+  const NestedItem& e = items[i];
+  nested_group(e.absmax, e.nb, g - e.g0, *e.offset, thr, e.codes, e.nested, threadIdx.x & 31);
 }
 
 // ---- dequantize -----------------------------------------------------------------
@@ -622,21 +690,13 @@ size_t quantize_ws_bytes(int64_t numel, int dq) {
   return align256(sizeof(float) * nb) + align256(sizeof(double) * pow2_at_least(ng));
 }
 
-cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf4_tensor& out,
-                            void* ws, int* status, cudaStream_t st) {
-  const int64_t nb = (numel + kBlock - 1) / kBlock;
-  const int64_t ng = (nb + kNested - 1) / kNested;
+cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int* status, cudaStream_t st) {
+  if (n < 1 || n > kEncodeBatch) return cudaErrorInvalidValue;
   const EncodeTables& et = encode_tables();
-  float* absmax_f = out.double_quant ? static_cast<float*>(ws) : static_cast<float*>(out.absmax);
-  double* gsum = out.double_quant
-                     ? reinterpret_cast<double*>(static_cast<char*>(ws) + align256(sizeof(float) * nb))
-                     : nullptr;
-  const int64_t p2 = pow2_at_least(ng);
-  unsigned* ticket = nullptr;
-  cudaError_t e = out.double_quant ? ticket_slot(&ticket) : cudaSuccess;
-  if (e != cudaSuccess) return e;
+  bool v8 = true;
+  for (int i = 0; i < n; ++i) v8 = v8 && (reinterpret_cast<uintptr_t>(jobs[i].x) & 31) == 0;
   int resident = 0;
-  const bool v8 = (reinterpret_cast<uintptr_t>(x) & 31) == 0;
+  cudaError_t e;
   if (xd == NF4_F32)
     e = v8 ? encode_ctas_per_sm(nf4_encode_blocks<float, true>, 0, &resident)
            : encode_ctas_per_sm(nf4_encode_blocks<float, false>, 1, &resident);
@@ -644,28 +704,67 @@ cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf
     e = v8 ? encode_ctas_per_sm(nf4_encode_blocks<__nv_bfloat16, true>, 2, &resident)
            : encode_ctas_per_sm(nf4_encode_blocks<__nv_bfloat16, false>, 3, &resident);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(ng, static_cast<int64_t>(resident) * device_sm_count())));
-  const dim3 block(kQuantThreads);
-  if (xd == NF4_F32) {
-    const auto* xf = static_cast<const float*>(x);
-    e = v8 ? launch_pdl(nf4_encode_blocks<float, true>, grid, block, 0, st, 1, xf, numel, ng, out.packed, absmax_f,
-                        gsum, p2, ticket, out.offset, et, status)
-           : launch_pdl(nf4_encode_blocks<float, false>, grid, block, 0, st, 1, xf, numel, ng, out.packed, absmax_f,
-                        gsum, p2, ticket, out.offset, et, status);
-  } else {
-    const auto* xb = static_cast<const __nv_bfloat16*>(x);
-    e = v8 ? launch_pdl(nf4_encode_blocks<__nv_bfloat16, true>, grid, block, 0, st, 1, xb, numel, ng, out.packed,
-                        absmax_f, gsum, p2, ticket, out.offset, et, status)
-           : launch_pdl(nf4_encode_blocks<__nv_bfloat16, false>, grid, block, 0, st, 1, xb, numel, ng, out.packed,
-                        absmax_f, gsum, p2, ticket, out.offset, et, status);
+  EncodeBatch eb{};
+  NestedBatch nbt{};
+  eb.n = n;
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t nb = (jobs[i].numel + kBlock - 1) / kBlock;
+    const int64_t ng = (nb + kNested - 1) / kNested;
+    eb.it[i].x = jobs[i].x;
+    eb.it[i].numel = jobs[i].numel;
+    eb.it[i].ng = ng;
+    eb.it[i].g0 = total;
+    eb.it[i].p2 = pow2_at_least(ng);
+    eb.it[i].packed = jobs[i].out->packed;
+    total += ng;
   }
+  eb.total = total;
+  const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(resident) * device_sm_count());
+  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  for (int i = 0; i < n; ++i) {
+    const nf4_tensor& out = *jobs[i].out;
+    EncodeItem& it = eb.it[i];
+    it.ctas = static_cast<unsigned>(std::min<int64_t>(it.ng, grid));
+    if (!out.double_quant) {
+      it.absmax = static_cast<float*>(out.absmax);
+      continue;
+    }
+    const int64_t nb = (jobs[i].numel + kBlock - 1) / kBlock;
+    it.absmax = static_cast<float*>(jobs[i].ws);
+    it.group_sum = reinterpret_cast<double*>(static_cast<char*>(jobs[i].ws) + align256(sizeof(float) * nb));
+    it.offset = out.offset;
+    if ((e = ticket_slot(&it.ticket)) != cudaSuccess) return e;
+    NestedItem& ni = nbt.it[nbt.n++];
+    ni.absmax = it.absmax;
+    ni.nb = nb;
+    ni.ng = it.ng;
+    ni.g0 = nbt.total;
+    ni.offset = out.offset;
+    ni.codes = static_cast<uint8_t*>(out.absmax);
+    ni.nested = out.nested_absmax;
+    nbt.total += it.ng;
+  }
+  const dim3 egrid(static_cast<unsigned>(grid)), block(kQuantThreads);
+  if (xd == NF4_F32)
+    e = v8 ? launch_pdl(nf4_encode_blocks<float, true>, egrid, block, 0, st, 1, eb, et, status)
+           : launch_pdl(nf4_encode_blocks<float, false>, egrid, block, 0, st, 1, eb, et, status);
+  else
+    e = v8 ? launch_pdl(nf4_encode_blocks<__nv_bfloat16, true>, egrid, block, 0, st, 1, eb, et, status)
+           : launch_pdl(nf4_encode_blocks<__nv_bfloat16, false>, egrid, block, 0, st, 1, eb, et, status);
   note_launch();
-  if (e != cudaSuccess || !out.double_quant) return e;
-  const dim3 ngrid(static_cast<unsigned>((ng + kNestedWarps - 1) / kNestedWarps));
-  e = launch_pdl(nf4_encode_nested, ngrid, dim3(kNestedWarps * 32), 0, st, 1, static_cast<const float*>(absmax_f), nb,
-                 ng, static_cast<const float*>(out.offset), static_cast<uint8_t*>(out.absmax), out.nested_absmax, et);
+  if (e != cudaSuccess || nbt.n == 0) return e;
+  const int64_t ngrid = (nbt.total + kNestedWarps - 1) / kNestedWarps;
+  if (ngrid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  e = launch_pdl(nf4_encode_nested, dim3(static_cast<unsigned>(ngrid)), dim3(kNestedWarps * 32), 0, st, 1, nbt, et);
   note_launch();
   return e;
+}
+
+cudaError_t launch_quantize(const void* x, nf4_dtype xd, int64_t numel, const nf4_tensor& out,
+                            void* ws, int* status, cudaStream_t st) {
+  const QuantJob job{x, numel, &out, ws};
+  return launch_quantize_batch(&job, 1, xd, status, st);
 }
 
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st) {

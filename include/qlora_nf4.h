@@ -116,6 +116,25 @@ size_t nf4_quantize_workspace_bytes(int64_t numel, int32_t double_quant);
 nf4_status nf4_quantize(const void* x, nf4_dtype x_dtype, int64_t numel,
                         const nf4_tensor* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Several tensors in one call, e.g. the seven weights of one transformer layer: item i gets
+ * exactly what nf4_quantize(items[i].x, items[i].x_dtype, items[i].numel, items[i].out, ...)
+ * gives.  Consecutive items of one input dtype run together, up to 8 at a time, as one block
+ * pass over all their 64-element blocks and one nested pass over all their maxima, so small
+ * tensors share the GPU instead of running one after another.  ws: device workspace of
+ * nf4_quantize_batch_workspace_bytes() bytes, 16-byte aligned (each item takes its own slice,
+ * laid out in the items' order).  Every item is validated as nf4_quantize validates it; the
+ * first failing item's status is returned and nothing is enqueued.  Items must not overlap
+ * one another's outputs. */
+typedef struct {
+  const void* x;            /* device input, 16-byte aligned */
+  nf4_dtype x_dtype;        /* NF4_F32 or NF4_BF16 */
+  int64_t numel;
+  const nf4_tensor* out;    /* preallocated for numel and its double_quant setting */
+} nf4_quantize_item;
+size_t nf4_quantize_batch_workspace_bytes(int32_t count, const nf4_quantize_item* items);
+nf4_status nf4_quantize_batch(int32_t count, const nf4_quantize_item* items, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* nf4_quantize without a workspace, for callers that cannot allocate device
  * memory: code running inside a host engine or framework that owns all device
  * memory and hands it only input and output buffers, or a latency-critical loop

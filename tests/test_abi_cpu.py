@@ -101,6 +101,21 @@ def test_validation_refuses_bad_arguments(lib):
     nodq.offset = 0x40000000
     assert q(x, 0, 1000, ctypes.byref(nodq), ws, 1 << 20, None) == binding.NF4_ERR_CORRUPT
 
+    # the batch: every item checked before anything is enqueued
+    items = (binding._QuantItem * 2)()
+    items[0] = binding._QuantItem(x.value, 0, 1000, ctypes.pointer(t))
+    items[1] = binding._QuantItem(x.value, 1, 1000, ctypes.pointer(t))
+    qb = lambda n, wsz=1 << 20, w=ws: lib.nf4_quantize_batch(n, items, w, wsz, None)  # noqa: E731
+    assert qb(0) == binding.NF4_ERR_ARG
+    assert qb(2, wsz=8) == binding.NF4_ERR_WORKSPACE
+    assert lib.nf4_quantize_batch_workspace_bytes(2, items) == 2 * lib.nf4_quantize_workspace_bytes(1000, 1)
+    items[1] = binding._QuantItem(x.value, binding.NF4_F16, 1000, ctypes.pointer(t))
+    assert qb(2) == binding.NF4_ERR_DTYPE
+    items[1] = binding._QuantItem(0x20000004, 1, 1000, ctypes.pointer(t))
+    assert qb(2) == binding.NF4_ERR_ALIGN
+    items[1] = binding._QuantItem(x.value, 1, 999, ctypes.pointer(t))
+    assert qb(2) == binding.NF4_ERR_CORRUPT
+
     assert lib.nf4_dequantize(None, x, 0, None) == binding.NF4_ERR_ARG
     assert lib.nf4_dequantize(ctypes.byref(t), x, 3, None) == binding.NF4_ERR_DTYPE
     # half precision: an output of the dequantize and a compute dtype of the linear, not an

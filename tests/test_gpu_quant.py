@@ -142,6 +142,51 @@ def test_quantize_offset_inside_and_outside_the_nested_pass(lib, n):
     assert binding.device_status() == binding.NF4_OK
 
 
+def test_quantize_batch_equals_single_calls(lib):
+    """nf4_quantize_batch over 11 tensors (bf16 and fp32, with and without double quantization,
+    ragged sizes; more than 8, so the items run in several launches) gives every tensor the
+    bytes a single nf4_quantize call gives, and those are the oracle's."""
+    specs = [(torch.bfloat16, True, 16384 * 5 + 3), (torch.bfloat16, False, 1000), (torch.bfloat16, True, 64),
+             (torch.float32, True, 16384 * 3), (torch.float32, False, 77777), (torch.float32, True, 1),
+             (torch.bfloat16, True, 4096 * 1024), (torch.bfloat16, True, 129), (torch.bfloat16, False, 65),
+             (torch.bfloat16, True, 300000), (torch.bfloat16, True, 16385)]
+    pairs, singles = [], []
+    for i, (dt, dq, n) in enumerate(specs):
+        x = wl.device_normal((n,), 0.02, wl.seed_for(5, 500 + i), DEV, dt)
+        pairs.append((x, binding.Nf4Tensor.empty((n,), dq, DEV)))
+        singles.append(binding.nf4_quantize(x, dq))
+    binding.nf4_quantize_batch(pairs)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    for (x, q), one, (dt, dq, n) in zip(pairs, singles, specs):
+        assert torch.equal(q.packed, one.packed)
+        assert torch.equal(q.absmax.view(torch.uint8), one.absmax.view(torch.uint8))
+        if dq:
+            assert torch.equal(q.nested_absmax.view(torch.int32), one.nested_absmax.view(torch.int32))
+            assert torch.equal(q.offset.view(torch.int32), one.offset.view(torch.int32))
+        if n <= 100000:
+            _assert_same_quant(q, onf4.quantize(_host_values(x), double_quant=dq))
+
+
+def test_quantize_ticket_counters_wrap(lib):
+    """The block pass's ticket counters come from a pool of 4096 that every double-quant call
+    puts back to zero: 4200 calls in a row (every counter used again) all give the oracle's
+    offset."""
+    x = wl.device_normal((16384 * 2 + 5,), 0.02, wl.seed_for(5, 600), DEV, torch.bfloat16)
+    ref = onf4.quantize(_host_values(x), double_quant=True)
+    q = binding.Nf4Tensor.empty(tuple(x.shape), True, DEV)
+    ws = torch.empty(binding.load().nf4_quantize_workspace_bytes(x.numel(), 1), dtype=torch.uint8, device=DEV)
+    offsets = torch.empty(4200, dtype=torch.float32, device=DEV)
+    for i in range(4200):
+        binding.nf4_quantize(x, True, out=q, workspace=ws)
+        offsets[i:i + 1].copy_(q.offset[:1])
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    want = np.float32(ref["offset"]).view(np.uint32)
+    assert np.all(offsets.cpu().numpy().view(np.uint32) == want)
+    _assert_same_quant(q, ref)
+
+
 def test_quantize_special_blocks(lib):
     nf4 = cb.nf4_codebook()
     x = np.zeros(64 * 300 + 5, np.float32)
