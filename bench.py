@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--only", default=None,
                    help="restrict the step to one projection (for profiling; not a bench line)")
     p.add_argument("--cpu-sample-worker", type=float, default=None, help=argparse.SUPPRESS)
-    p.add_argument("--profile-case", choices=("gate_linear", "small_m", "export"), default=None,
+    p.add_argument("--profile-case", choices=("gate_linear", "small_m", "export", "smollm2"), default=None,
                    help="run one fixed workload for a profiler (no timing, no bench line): gate_linear = "
                         "quantize x2, dequantize x2, fwd x3, bwd x3 at the gate shape (M=4096, 14336x4096); "
                         "small_m = the 7-projection batched forward x4 at --tokens; export = embedding rows "
@@ -696,6 +696,76 @@ def graph_ms(fn, dev, stream, flush, reps=10):
     return ts[len(ts) // 2]
 
 
+def measure_smollm2(dev, time_ms, tc):
+    """The SmolLM2-135M-shaped stack (workload 2): forward + backward of q and v in each of 30
+    layers at M = 512, r = 16, bf16.  Within a layer q and v read the same x.  Timed two ways,
+    each as one graph: per layer one qlora_linear_fwd_batch and one qlora_linear_bwd_batch over
+    (q, v) (the grouped launches), and one qlora_linear_fwd + qlora_linear_bwd call per
+    projection."""
+    import torch
+    from bit_nf4_quantized_gb300 import binding as bq
+    from bit_nf4_quantized_gb300 import workloads as wl
+    lib = bq.load()
+    c = wl.W2
+    M, r, alpha = c["M"], c["r"], c["alpha"]
+    targets = [(n, N, K) for n, N, K in c["shapes"] if n in c["targets"]]
+    shapes = [(N, K) for _, N, K in targets]
+    ws = torch.empty(max(16, max(lib.qlora_fwd_workspace_bytes(M, N, K, r, 1) for N, K in shapes),
+                         max(lib.qlora_bwd_workspace_bytes(M, N, K, r, 1) for N, K in shapes),
+                         bq.qlora_bwd_batch_workspace_bytes(M, shapes, r),
+                         bq.qlora_fwd_batch_workspace_bytes(M, shapes, r)), dtype=torch.uint8, device=dev)
+    K0 = targets[0][2]
+    x = wl.device_normal((M, K0), 1.0, wl.seed_for(2, 1), dev, torch.bfloat16)   # the layer input, shared
+    bufs = []
+    for j, (_, N, K) in enumerate(targets):
+        seed = wl.seed_for(2, 10 * j)
+        bufs.append(dict(dy=wl.device_normal((M, N), 1.0, seed + 2, dev, torch.bfloat16),
+                         y=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                         T=torch.empty((M, r), dtype=torch.float32, device=dev),
+                         dx=torch.empty((M, K), dtype=torch.bfloat16, device=dev),
+                         dA=torch.empty((r, K), dtype=torch.float32, device=dev),
+                         dB=torch.empty((N, r), dtype=torch.float32, device=dev)))
+    layers = []
+    for layer in range(c["layers"]):
+        mats = []
+        for j, (_, N, K) in enumerate(targets):
+            seed = wl.seed_for(2, 1000 + 10 * (layer * len(targets) + j))
+            mats.append(dict(q=bq.nf4_quantize(wl.device_normal((N, K), 0.02, seed, dev, torch.bfloat16), True),
+                             A=wl.device_normal((r, K), 1.0 / r, seed + 3, dev, torch.float32),
+                             B=wl.device_normal((N, r), 0.01, seed + 4, dev, torch.float32)))
+        layers.append(mats)
+
+    def grouped():
+        for mats in layers:
+            bq.qlora_linear_fwd_batch([dict(x=x, W=m["q"], A=m["A"], B=m["B"], alpha=alpha, y=b["y"], T=b["T"])
+                                       for m, b in zip(mats, bufs)], workspace=ws)
+            bq.qlora_linear_bwd_batch([dict(dy=b["dy"], x=x, T=b["T"], W=m["q"], A=m["A"], B=m["B"], alpha=alpha,
+                                            dx=b["dx"], dA=b["dA"], dB=b["dB"]) for m, b in zip(mats, bufs)],
+                                      workspace=ws)
+
+    def single():
+        for mats in layers:
+            for m, b in zip(mats, bufs):
+                bq.qlora_linear_fwd(x, m["q"], m["A"], m["B"], alpha, y=b["y"], T=b["T"], workspace=ws)
+                bq.qlora_linear_bwd(b["dy"], x, b["T"], m["q"], m["A"], m["B"], alpha, dx=b["dx"], dA=b["dA"],
+                                    dB=b["dB"], workspace=ws)
+
+    launches0 = bq.launch_count()
+    grouped()
+    torch.cuda.synchronize(dev)
+    launches = bq.launch_count() - launches0
+    ms_g = time_ms(grouped)
+    ms_s = time_ms(single)
+    flops = sum(linear_flops(M, N, K, r) for mats in layers for (N, K) in shapes)
+    if bq.device_status() != bq.NF4_OK:
+        raise RuntimeError("device status word set in the SmolLM2-shaped stack")
+    return {"tokens": M, "rank": r, "layers": c["layers"], "ms_per_step": ms_g, "TFLOP/s": flops / ms_g / 1e9,
+            "frac_bf16_burst": flops / ms_g / 1e9 / tc, "launches_per_step": launches,
+            "single_calls": {"ms_per_step": ms_s, "TFLOP/s": flops / ms_s / 1e9},
+            "flops_per_step": flops,
+            "timing": "one step as a CUDA graph, L2 flushed before each replay, launch included"}
+
+
 def sweep(dev, stream):
     """The workloads besides the bench line, timed through the C ABI (one JSON line each):
     the small-M forward of the Llama-3-8B-shaped matrices (GB/s of the bytes a forward must
@@ -755,43 +825,8 @@ def sweep(dev, stream):
     del projs, ws
 
     # SmolLM2-shaped stack: QLoRA forward + backward on q and v of 30 layers
-    c = wl.W2
-    M, r, alpha = c["M"], c["r"], c["alpha"]
-    targets = [(n, N, K) for n, N, K in c["shapes"] if n in c["targets"]]
-    wsf = torch.empty(max(16, max(lib.qlora_fwd_workspace_bytes(M, N, K, r, 1) for _, N, K in targets)),
-                      dtype=torch.uint8, device=dev)
-    wsb = torch.empty(max(16, max(lib.qlora_bwd_workspace_bytes(M, N, K, r, 1) for _, N, K in targets)),
-                      dtype=torch.uint8, device=dev)
-    bufs = {}
-    for j, (_, N, K) in enumerate(targets):
-        seed = wl.seed_for(2, 10 * j)
-        bufs[(N, K)] = dict(x=wl.device_normal((M, K), 1.0, seed + 1, dev, torch.bfloat16),
-                            dy=wl.device_normal((M, N), 1.0, seed + 2, dev, torch.bfloat16),
-                            y=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
-                            T=torch.empty((M, r), dtype=torch.float32, device=dev),
-                            dx=torch.empty((M, K), dtype=torch.bfloat16, device=dev),
-                            dA=torch.empty((r, K), dtype=torch.float32, device=dev),
-                            dB=torch.empty((N, r), dtype=torch.float32, device=dev))
-    mats = []
-    for layer in range(c["layers"]):
-        for j, (_, N, K) in enumerate(targets):
-            seed = wl.seed_for(2, 1000 + 10 * (layer * len(targets) + j))
-            mats.append(dict(N=N, K=K, q=bq.nf4_quantize(wl.device_normal((N, K), 0.02, seed, dev, torch.bfloat16), True),
-                             A=wl.device_normal((r, K), 1.0 / r, seed + 3, dev, torch.float32),
-                             B=wl.device_normal((N, r), 0.01, seed + 4, dev, torch.float32)))
-
-    def stack():
-        for p in mats:
-            b = bufs[(p["N"], p["K"])]
-            bq.qlora_linear_fwd(b["x"], p["q"], p["A"], p["B"], alpha, y=b["y"], T=b["T"], workspace=wsf)
-            bq.qlora_linear_bwd(b["dy"], b["x"], b["T"], p["q"], p["A"], p["B"], alpha, dx=b["dx"], dA=b["dA"],
-                                dB=b["dB"], workspace=wsb)
-    ms = graph_ms(stack, dev, stream, flush)
-    flops = sum(linear_flops(M, p["N"], p["K"], r) for p in mats)
-    emit({"sweep": "SmolLM2-shaped stack, QLoRA q and v of 30 layers, fwd+bwd", "tokens": M, "rank": r,
-          "ms_per_step": ms, "TFLOP/s": flops / ms / 1e9, "frac_bf16_burst": flops / ms / 1e9 / tc,
-          "flops_per_step": flops})
-    del mats, bufs, wsf, wsb
+    st2 = measure_smollm2(dev, lambda fn: graph_ms(fn, dev, stream, flush), tc)
+    emit(dict({"sweep": "SmolLM2-shaped stack, QLoRA q and v of 30 layers, fwd+bwd"}, **st2))
 
     # 1-D quantize (fp32 input) and dequantize (fp32 output)
     for n in wl.W5["sizes"]:
@@ -837,6 +872,28 @@ def profile_case(args):
             y, T = bq.qlora_linear_fwd(x, q, A, B, c["alpha"])
         for _ in range(3):
             bq.qlora_linear_bwd(dy, x, T, q, A, B, c["alpha"])
+    elif args.profile_case == "smollm2":
+        # two SmolLM2-shaped layers (q and v share x, M = 512, r = 16): per layer one grouped forward
+        # and one grouped backward, three times
+        c = wl.W2
+        M, r = c["M"], c["r"]
+        targets = [(N, K) for n, N, K in c["shapes"] if n in c["targets"]]
+        x = wl.device_normal((M, targets[0][1]), 1.0, wl.seed_for(2, 1), dev, torch.bfloat16)
+        mats = []
+        for layer in range(2):
+            for j, (N, K) in enumerate(targets):
+                seed = wl.seed_for(2, 1000 + 10 * (layer * 2 + j))
+                q = bq.nf4_quantize(wl.device_normal((N, K), 0.02, seed, dev, torch.bfloat16), True)
+                mats.append(dict(W=q, A=wl.device_normal((r, K), 1.0 / r, seed + 3, dev, torch.float32),
+                                 B=wl.device_normal((N, r), 0.01, seed + 4, dev, torch.float32),
+                                 dy=wl.device_normal((M, N), 1.0, seed + 2, dev, torch.bfloat16)))
+        for _ in range(3):
+            for layer in range(2):
+                group = mats[2 * layer:2 * layer + 2]
+                outs = bq.qlora_linear_fwd_batch([dict(x=x, W=m["W"], A=m["A"], B=m["B"], alpha=c["alpha"])
+                                                  for m in group])
+                bq.qlora_linear_bwd_batch([dict(dy=m["dy"], x=x, T=o[1], W=m["W"], A=m["A"], B=m["B"],
+                                                alpha=c["alpha"]) for m, o in zip(group, outs)])
     elif args.profile_case == "small_m":
         c = wl.W4
         M = args.tokens
@@ -1042,6 +1099,7 @@ def main():
     small_m = measure_small_m(layer, row_ms, hbm)
     f16_profile = measure_f16_profile(layer, row_ms)
     fp32_576 = measure_fp32_576(dev, row_ms)
+    smollm2 = measure_smollm2(dev, row_ms, peak)
     # the same step as one graph with L2 flushed before it, decoding once per projection (the
     # headline's step) and with the NF4-input calls, which decode the weight once per call
     once_ms = row_ms(layer.step, reps=5)
@@ -1144,6 +1202,7 @@ def main():
             "small_m_forward": small_m,
             "f16_profile": f16_profile,
             "fp32_576": fp32_576,
+            "smollm2_stack": smollm2,
             "embedding": export_rows["embedding"],
             "merge": export_rows["merge"],
             "clocks": clocks,

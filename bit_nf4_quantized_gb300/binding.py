@@ -31,6 +31,7 @@ ENTRY_POINTS = (
     "qlora_fwd_batch_workspace_bytes", "qlora_linear_fwd_batch",
     "qlora_fwd_w16_workspace_bytes", "qlora_bwd_w16_workspace_bytes", "qlora_linear_fwd_w16",
     "qlora_linear_bwd_w16", "nf4_quantize_batch_workspace_bytes", "nf4_quantize_batch",
+    "qlora_bwd_batch_workspace_bytes", "qlora_linear_bwd_batch",
 )
 
 
@@ -52,6 +53,14 @@ class _FwdItem(ctypes.Structure):
                 ("alpha", ctypes.c_float), ("mode", ctypes.c_int32), ("W", ctypes.POINTER(_Nf4Tensor)),
                 ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("T_out", ctypes.c_void_p)]
+
+
+class _BwdItem(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("rank", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("mode", ctypes.c_int32), ("W", ctypes.POINTER(_Nf4Tensor)),
+                ("w16", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("dy", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("T", ctypes.c_void_p), ("dx", ctypes.c_void_p), ("dA", ctypes.c_void_p),
+                ("dB", ctypes.c_void_p)]
 
 
 class _QuantItem(ctypes.Structure):
@@ -104,6 +113,8 @@ def load() -> ctypes.CDLL:
         "qlora_linear_fwd_w16": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "qlora_linear_bwd_w16": (i32, [i64, i64, i64, i32, f32, i32, i32, vp, vp, vp, vp, vp, vp,
                                        vp, vp, vp, vp, sz, vp]),
+        "qlora_bwd_batch_workspace_bytes": (sz, [i64, i32, ctypes.POINTER(_BwdItem), i32]),
+        "qlora_linear_bwd_batch": (i32, [i64, i32, ctypes.POINTER(_BwdItem), i32, vp, sz, vp]),
         "qlora_last_device_status": (i32, [vp, i32]),
         "nf4_kernel_launch_count": (i64, []),
         "qlora_debug_wait_timeout": (None, [i32]),
@@ -436,6 +447,55 @@ def qlora_linear_bwd_w16(dy: torch.Tensor, x: torch.Tensor, T: torch.Tensor, w16
                                     _ptr(w16), _ptr(A), _ptr(B), _ptr(dx), _ptr(dA), _ptr(dB), _ptr(ws),
                                     ws.numel(), _stream(stream)), "qlora_linear_bwd_w16")
     return dx, dA, dB
+
+
+def qlora_linear_bwd_batch(items, workspace: torch.Tensor = None, stream=None):
+    """Backward of several projections sharing M: ``items`` is a list of dicts with keys dy, x,
+    T, A, B, alpha, W (an Nf4Tensor) or w16 (the decoded weight), and optionally mode, dx, dA,
+    dB.  Returns [(dX, dA, dB), ...]; each item equals its single qlora_linear_bwd (or _w16)."""
+    lib = load()
+    n = len(items)
+    M = items[0]["x"].shape[0]
+    cd = _dtype_code(items[0]["x"].dtype)
+    arr = (_BwdItem * n)()
+    keep, outs = [], []
+    for i, it in enumerate(items):
+        x, A, B = it["x"], it["A"], it["B"]
+        K = x.shape[1]
+        N = it["dy"].shape[1]
+        r = A.shape[0]
+        dx = it.get("dx")
+        dA = it.get("dA")
+        dB = it.get("dB")
+        if dx is None:
+            dx = torch.empty((M, K), dtype=x.dtype, device=x.device)
+        if dA is None:
+            dA = torch.empty((r, K), dtype=torch.float32, device=x.device)
+        if dB is None:
+            dB = torch.empty((N, r), dtype=torch.float32, device=x.device)
+        W = it.get("W")
+        cs = W.c_struct() if W is not None else None
+        keep.append(cs)
+        w16 = it.get("w16")
+        arr[i] = _BwdItem(N, K, r, float(it["alpha"]), int(it.get("mode", SCALE_LORA)),
+                          ctypes.pointer(cs) if cs is not None else None,
+                          w16.data_ptr() if w16 is not None else None, A.data_ptr(), B.data_ptr(),
+                          it["dy"].data_ptr(), x.data_ptr(), it["T"].data_ptr(), dx.data_ptr(), dA.data_ptr(),
+                          dB.data_ptr())
+        outs.append((dx, dA, dB))
+    ws = workspace if workspace is not None else _workspace(
+        lib.qlora_bwd_batch_workspace_bytes(M, n, arr, cd), items[0]["x"].device)
+    _check(lib.qlora_linear_bwd_batch(M, n, arr, cd, _ptr(ws), ws.numel(), _stream(stream)), "qlora_linear_bwd_batch")
+    return outs
+
+
+def qlora_bwd_batch_workspace_bytes(M: int, shapes, rank: int, dtype=torch.bfloat16) -> int:
+    """Workspace bytes of qlora_linear_bwd_batch for items of the given (N, K) shapes and rank."""
+    lib = load()
+    arr = (_BwdItem * len(shapes))()
+    for i, (N, K) in enumerate(shapes):
+        arr[i] = _BwdItem(N, K, rank, 1.0, SCALE_LORA, None, None, None, None, None, None, None, None, None, None)
+    return int(lib.qlora_bwd_batch_workspace_bytes(M, len(shapes), arr, _dtype_code(dtype)))
 
 
 def debug_wait_timeout(on: bool = True):

@@ -360,12 +360,24 @@ bool is16(nf4_dtype cd) { return cd == NF4_BF16 || cd == NF4_F16; }
 
 bool small_m(int64_t M, nf4_dtype cd) { return is16(cd) && M >= 1 && M <= kStreamMaxM; }
 
+// Small weights at M > 16 run the fused small-shape kernels (one launch forward, one backward).
+bool small_w(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
+  return is16(cd) && M > kStreamMaxM && small_fused_fits(N, K, r);
+}
+
+size_t small_bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r) {
+  SmallItem it{};
+  it.a = LinearArgs{M, N, K, r, 0.0f, Nf4View{}};
+  return small_fused_bwd_ws_bytes(&it, 1, M);
+}
+
 // Workspace layouts.  bwd: G fp32 [M, r], then whatever the selected path needs.
 size_t fwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
   if (small_m(M, cd)) {
     LinearArgs la{M, N, K, r, 0.0f, Nf4View{}};
     return stream_fwd_ws_bytes(&la, 1);
   }
+  if (small_w(M, N, K, r, cd)) return 0;
   if (is16(cd)) return tc_fwd_ws_bytes(M, N, K, r);
   return 0;
 }
@@ -400,6 +412,7 @@ size_t batch_ws(int64_t M, int32_t count, const qlora_fwd_item* it, nf4_dtype cd
   return need;
 }
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
+  if (small_w(M, N, K, r, cd)) return small_bwd_ws(M, N, K, r);
   size_t b = a256(sizeof(float) * static_cast<size_t>(M) * r);
   if (is16(cd)) b += tc_bwd_ws_bytes(M, N, K, r);
   return b;
@@ -588,6 +601,12 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
     const StreamItem item{a, x, A, B, y, T_out};
     return from_cuda(stream_forward(&item, 1, compute == NF4_F16, ws, status, cs));
   }
+  if (small_w(M, N, K, rank, compute)) {
+    SmallItem it{};
+    it.a = a;
+    it.x = x, it.A = A, it.B = B, it.y = y, it.T = T_out;
+    return from_cuda(small_fused_forward(&it, 1, M, compute == NF4_F16, cs));
+  }
   if (is16(compute)) {
     int* status = nullptr;
     if ((st = device_status_ptr(&status)) != NF4_OK) return st;
@@ -638,13 +657,32 @@ nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item
     }
     return NF4_OK;
   }
+  // small weights: up to 8 per launch of the fused forward; the others one call each
+  std::vector<SmallItem> small;
+  auto flush = [&]() -> nf4_status {
+    if (small.empty()) return NF4_OK;
+    const cudaError_t e = small_fused_forward(small.data(), static_cast<int>(small.size()), M, compute == NF4_F16, cs);
+    small.clear();
+    return from_cuda(e);
+  };
   for (int32_t i = 0; i < count; ++i) {
     const qlora_fwd_item& it = items[i];
+    if (small_w(M, it.N, it.K, it.rank, compute)) {
+      SmallItem si{};
+      si.a = LinearArgs{M, it.N, it.K, it.rank, s[i], view_of(it.W)};
+      si.x = it.x, si.A = it.A, si.B = it.B, si.y = it.y, si.T = it.T_out;
+      small.push_back(si);
+      if (static_cast<int>(small.size()) == kSmallMaxGroup) {
+        const nf4_status st = flush();
+        if (st != NF4_OK) return st;
+      }
+      continue;
+    }
     const nf4_status st = qlora_linear_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A,
                                            it.B, it.y, it.T_out, ws, ws_bytes, stream);
     if (st != NF4_OK) return st;
   }
-  return NF4_OK;
+  return flush();
 }
 
 nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
@@ -671,6 +709,12 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
     return from_cuda(e);
   }
   LinearArgs a{M, N, K, rank, s, view_of(W)};
+  if (small_w(M, N, K, rank, compute)) {
+    SmallItem it{};
+    it.a = a;
+    it.x = x, it.A = A, it.B = B, it.T = const_cast<float*>(T), it.dy = dy, it.dx = dx, it.dA = dA, it.dB = dB;
+    return from_cuda(small_fused_backward(&it, 1, M, compute == NF4_F16, ws, cs));
+  }
   float* G = static_cast<float*>(ws);
   if (is16(compute)) {
     int* status = nullptr;
@@ -688,11 +732,13 @@ nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
 
 size_t qlora_fwd_w16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
   if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256 || !is16(compute)) return 0;
+  if (small_w(M, N, K, rank, compute)) return 0;
   return tc_fwd_ws_bytes(M, N, K, rank, true);
 }
 
 size_t qlora_bwd_w16_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t rank, nf4_dtype compute) {
   if (M < 0 || N <= 0 || K <= 0 || rank < 1 || rank > 256 || !is16(compute)) return 0;
+  if (small_w(M, N, K, rank, compute)) return small_bwd_ws(M, N, K, rank);
   return a256(sizeof(float) * static_cast<size_t>(M) * rank) + tc_bwd_ws_bytes(M, N, K, rank, true);
 }
 
@@ -709,13 +755,19 @@ nf4_status qlora_linear_fwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
   if (!aligned16(w16) || !aligned16(A) || !aligned16(B) ||
       (M > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(T_out))))
     return NF4_ERR_ALIGN;
-  const size_t need = tc_fwd_ws_bytes(M, N, K, rank, true);
-  if (ws == nullptr || ws_bytes < need) return NF4_ERR_WORKSPACE;
-  if (!aligned16(ws)) return NF4_ERR_ALIGN;
+  const size_t need = qlora_fwd_w16_workspace_bytes(M, N, K, rank, compute);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
   if (M == 0) return NF4_OK;
+  const LinearArgs a{M, N, K, rank, s, Nf4View{}};
+  if (small_w(M, N, K, rank, compute)) {
+    SmallItem it{};
+    it.a = a;
+    it.x = x, it.A = A, it.B = B, it.y = y, it.T = T_out, it.w16 = w16;
+    return from_cuda(small_fused_forward(&it, 1, M, compute == NF4_F16, static_cast<cudaStream_t>(stream)));
+  }
   int* status = nullptr;
   if ((st = device_status_ptr(&status)) != NF4_OK) return st;
-  const LinearArgs a{M, N, K, rank, s, Nf4View{}};
   return from_cuda(tc_forward(a, compute == NF4_F16, x, A, B, y, T_out, ws, status,
                               static_cast<cudaStream_t>(stream), w16));
 }
@@ -742,12 +794,93 @@ nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
     if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, sizeof(float) * static_cast<size_t>(N) * rank, cs);
     return from_cuda(e);
   }
+  const LinearArgs a{M, N, K, rank, s, Nf4View{}};
+  if (small_w(M, N, K, rank, compute)) {
+    SmallItem it{};
+    it.a = a;
+    it.x = x, it.A = A, it.B = B, it.T = const_cast<float*>(T), it.dy = dy, it.dx = dx, it.dA = dA, it.dB = dB;
+    it.w16 = w16;
+    return from_cuda(small_fused_backward(&it, 1, M, compute == NF4_F16, ws, cs));
+  }
   int* status = nullptr;
   if ((st = device_status_ptr(&status)) != NF4_OK) return st;
-  const LinearArgs a{M, N, K, rank, s, Nf4View{}};
   float* G = static_cast<float*>(ws);
   void* tc_ws = static_cast<char*>(ws) + a256(sizeof(float) * static_cast<size_t>(M) * rank);
   return from_cuda(tc_backward(a, compute == NF4_F16, dy, x, T, A, B, dx, dA, dB, G, tc_ws, status, cs, w16));
+}
+
+size_t qlora_bwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_bwd_item* items, nf4_dtype compute) {
+  if (M < 0 || count < 1 || items == nullptr) return 0;
+  size_t single = 0, group = 0, fused = 0;
+  int in_group = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    const qlora_bwd_item& it = items[i];
+    if (it.N <= 0 || it.K <= 0 || it.rank < 1 || it.rank > 256) return 0;
+    if (small_w(M, it.N, it.K, it.rank, compute)) {
+      group += small_bwd_ws(M, it.N, it.K, it.rank);
+      if (++in_group == kSmallMaxGroup) fused = std::max(fused, group), group = 0, in_group = 0;
+      continue;
+    }
+    single = std::max(single, it.w16 != nullptr ? qlora_bwd_w16_workspace_bytes(M, it.N, it.K, it.rank, compute)
+                                                : bwd_ws(M, it.N, it.K, it.rank, compute));
+  }
+  return std::max(single, std::max(fused, group));
+}
+
+nf4_status qlora_linear_bwd_batch(int64_t M, int32_t count, const qlora_bwd_item* items, nf4_dtype compute,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (count < 1 || items == nullptr) return NF4_ERR_ARG;
+  std::vector<float> s(static_cast<size_t>(count));
+  for (int32_t i = 0; i < count; ++i) {   // the single calls' checks, before anything is enqueued
+    const qlora_bwd_item& it = items[i];
+    nf4_status st = check_linear(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, &s[i]);
+    if (st != NF4_OK) return st;
+    if (it.w16 != nullptr) {
+      if (!is16(compute)) return NF4_ERR_DTYPE;
+      if (!aligned16(it.w16)) return NF4_ERR_ALIGN;
+    } else if ((st = check_tensor(it.W, it.N * it.K)) != NF4_OK) {
+      return st;
+    }
+    if (it.A == nullptr || it.B == nullptr || it.dA == nullptr || it.dB == nullptr) return NF4_ERR_ARG;
+    if (M > 0 && (it.dy == nullptr || it.x == nullptr || it.T == nullptr || it.dx == nullptr)) return NF4_ERR_ARG;
+    if (!aligned16(it.A) || !aligned16(it.B) || !aligned16(it.dA) || !aligned16(it.dB)) return NF4_ERR_ALIGN;
+    if (M > 0 && (!aligned16(it.dy) || !aligned16(it.x) || !aligned16(it.T) || !aligned16(it.dx))) return NF4_ERR_ALIGN;
+  }
+  const size_t need = qlora_bwd_batch_workspace_bytes(M, count, items, compute);
+  if (ws == nullptr || ws_bytes < need) return NF4_ERR_WORKSPACE;
+  if (!aligned16(ws)) return NF4_ERR_ALIGN;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  std::vector<SmallItem> small;
+  auto flush = [&]() -> nf4_status {
+    if (small.empty()) return NF4_OK;
+    const cudaError_t e = small_fused_backward(small.data(), static_cast<int>(small.size()), M, compute == NF4_F16,
+                                               ws, cs);
+    small.clear();
+    return from_cuda(e);
+  };
+  for (int32_t i = 0; i < count; ++i) {
+    const qlora_bwd_item& it = items[i];
+    if (M > 0 && small_w(M, it.N, it.K, it.rank, compute)) {
+      SmallItem si{};
+      si.a = LinearArgs{M, it.N, it.K, it.rank, s[i], it.w16 != nullptr ? Nf4View{} : view_of(it.W)};
+      si.x = it.x, si.A = it.A, si.B = it.B, si.T = const_cast<float*>(it.T), si.dy = it.dy, si.dx = it.dx;
+      si.dA = it.dA, si.dB = it.dB, si.w16 = it.w16;
+      small.push_back(si);
+      if (static_cast<int>(small.size()) == kSmallMaxGroup) {
+        const nf4_status st = flush();
+        if (st != NF4_OK) return st;
+      }
+      continue;
+    }
+    const nf4_status st =
+        it.w16 != nullptr
+            ? qlora_linear_bwd_w16(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.dy, it.x, it.T, it.w16,
+                                   it.A, it.B, it.dx, it.dA, it.dB, ws, ws_bytes, stream)
+            : qlora_linear_bwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.dy, it.x, it.T, it.W, it.A,
+                               it.B, it.dx, it.dA, it.dB, ws, ws_bytes, stream);
+    if (st != NF4_OK) return st;
+  }
+  return flush();
 }
 
 nf4_status qlora_last_device_status(void* stream, int32_t clear) {

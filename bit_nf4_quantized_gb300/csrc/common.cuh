@@ -88,6 +88,10 @@ void note_launch(int n = 1);
 // SM count of the current device (looked up once per device).
 int device_sm_count();
 
+// n zero ticket counters of the library's pool for one launch (which CTA of a group finishes
+// last); the launch must put every counter it uses back to zero.
+cudaError_t ticket_range(unsigned n, unsigned** out);
+
 // Bounded-wait settings of one tensor-core launch: the wait limit, and whether the launch's
 // first CTA leaves its first pipeline stage unissued (so that the waits for that stage run
 // out).  Normally {4 s, 0}; qlora_debug_wait_timeout() arms {20 ms, 1} for the next launch.

@@ -38,6 +38,29 @@ size_t stream_fwd_ws_bytes(const LinearArgs* a, int n);
 // f16: x, y and every tensor-core operand are IEEE half (the FP16 profile) instead of bf16.
 cudaError_t stream_forward(const StreamItem* items, int n, bool f16, void* ws, int* status, cudaStream_t st);
 
+// small_fused.cu: the 16-bit profiles for small weights (K, N <= 1024, N*K <= 2^21, rank <= 32)
+// and M > 16: the forward of up to kSmallMaxGroup projections sharing M in one launch, and
+// their backward in one (the dX tiles with the adapter gradients' per-tile parts, whose ordered
+// sums the last CTA of each column tile takes).
+constexpr int kSmallMaxGroup = 8;
+struct SmallItem {
+  LinearArgs a;
+  const void* x;     // 16-bit [M, K]
+  const float* A;    // [r, K]
+  const float* B;    // [N, r]
+  void* y;           // forward: 16-bit [M, N]
+  float* T;          // forward: written; backward: read [M, r]
+  const void* dy;    // backward: 16-bit [M, N]
+  const void* w16;   // W decoded to 16 bits [N, K], or null (decoded in the kernels)
+  void* dx;          // backward: 16-bit [M, K]
+  float* dA;         // backward: [r, K]
+  float* dB;         // backward: [N, r]
+};
+bool small_fused_fits(int64_t N, int64_t K, int r);
+cudaError_t small_fused_forward(const SmallItem* items, int n, int64_t M, bool f16, cudaStream_t st);
+size_t small_fused_bwd_ws_bytes(const SmallItem* items, int n, int64_t M);
+cudaError_t small_fused_backward(const SmallItem* items, int n, int64_t M, bool f16, void* ws, cudaStream_t st);
+
 // adapter_tc.cu: skinny tcgen05 products Out[rows, r] = X[rows, red] . Q[red, r] for the
 // rank-r contractions.  X is 16-bit (T16: bf16, or IEEE half when f16) row-major with
 // `x_inner` columns (the reduction runs along its rows when mn_major == false, down its

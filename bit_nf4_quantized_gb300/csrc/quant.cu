@@ -631,33 +631,39 @@ int64_t pow2_at_least(int64_t v) {
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-// Ticket counters of the block pass (which CTA finishes last), in the library's own device
-// memory: zero at module load, and every double-quant call puts its counter back to zero.
-// Calls draw slots round-robin, so calls in flight at the same time (other streams, other
-// host threads) use different counters unless more than kTicketSlots of them overlap.
-constexpr unsigned kTicketSlots = 4096;
-__device__ unsigned g_quant_tickets[kTicketSlots];
+// Ticket counters (which CTA of a group finishes last), in the library's own device memory:
+// zero at module load, and every kernel that counts on one puts it back to zero.  Calls draw
+// ranges round-robin, so calls in flight at the same time (other streams, other host threads)
+// use different counters unless more than kTicketSlots counters' worth of them overlap.
+constexpr unsigned kTicketSlots = 16384;
+__device__ unsigned g_tickets[kTicketSlots];
 
-cudaError_t ticket_slot(unsigned** out) {
+}  // namespace
+
+cudaError_t ticket_range(unsigned n, unsigned** out) {
   constexpr int kMaxDev = 64;
   static unsigned* base[kMaxDev] = {};
   static std::mutex mu;
-  static std::atomic<unsigned> next{0};
+  static unsigned next = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (base[dev] == nullptr) {
-      void* p = nullptr;
-      if ((e = cudaGetSymbolAddress(&p, g_quant_tickets)) != cudaSuccess) return e;
-      base[dev] = static_cast<unsigned*>(p);
-    }
-    *out = base[dev] + next.fetch_add(1, std::memory_order_relaxed) % kTicketSlots;
+  if (dev < 0 || dev >= kMaxDev || n == 0 || n > kTicketSlots / 4) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(mu);
+  if (base[dev] == nullptr) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_tickets)) != cudaSuccess) return e;
+    base[dev] = static_cast<unsigned*>(p);
   }
+  if (next + n > kTicketSlots) next = 0;   // a range never wraps
+  *out = base[dev] + next;
+  next += n;
   return cudaSuccess;
 }
+
+namespace {
+
+cudaError_t ticket_slot(unsigned** out) { return ticket_range(1, out); }
 
 // Resident CTAs per SM of an encode kernel (kind: input type and load width), per device,
 // looked up once (a racing first lookup stores the same value).

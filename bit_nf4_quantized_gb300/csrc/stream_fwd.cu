@@ -48,6 +48,7 @@
 #include <cuda_fp16.h>
 
 #include "decode.cuh"
+#include "mma_sync.cuh"
 #include "linear_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -168,29 +169,6 @@ __device__ __forceinline__ float scale_of(const ScaleIn& in, int dq, const float
   if (!in.live) return 0.0f;
   if (!dq) return in.nested_or_max;
   return __fadd_rn(__fmul_rn(dyn8[in.code], in.nested_or_max), in.offset);
-}
-
-__device__ __forceinline__ uint32_t ld_shared32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-// D += A (16 x 16, row) * B (16 x 8, col), bf16 or (F16) IEEE half operands, fp32 accumulate,
-// fragments per thread.
-template <bool F16>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-  if constexpr (F16)
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-                 "{%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  else
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-                 "{%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Decoder thread layout.  Warp w (0..15) owns tile rows 16w .. 16w+15; in the mma.sync fragments

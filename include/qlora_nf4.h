@@ -280,6 +280,36 @@ nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
                                 const float* A, const float* B, void* dx, float* dA, float* dB,
                                 void* ws, size_t ws_bytes, void* stream);
 
+/* Backward of several projections that share M and the compute dtype, e.g. the projections of
+ * one layer that read the same x (q and v): item i computes exactly what qlora_linear_bwd (w16
+ * == NULL) or qlora_linear_bwd_w16 (w16 != NULL: W decoded as nf4_dequantize writes it)
+ * computes for its arguments; W may be NULL when w16 is given.  Items with small weights
+ * (16-bit compute, M > 16, K and N at most 1024, N*K at most 2^21, rank at most 32) run up to
+ * 8 at a time in one pair of launches; the others run one call each.  Items must not write to
+ * memory another item reads.  ws: qlora_bwd_batch_workspace_bytes() bytes.  Each item is
+ * validated as the single call validates it; the first failing item's status is returned and
+ * nothing is enqueued. */
+typedef struct {
+  int64_t N, K;
+  int32_t rank;
+  float alpha;
+  qlora_scale_mode mode;
+  const nf4_tensor* W;    /* numel N*K, [N, K] row-major; or NULL with w16 */
+  const void* w16;        /* [N, K] decoded in the compute dtype, or NULL */
+  const float* A;         /* [rank, K] fp32 */
+  const float* B;         /* [N, rank] fp32 */
+  const void* dy;         /* [M, N] in the compute dtype */
+  const void* x;          /* [M, K] in the compute dtype */
+  const float* T;         /* [M, rank] fp32, the forward's T_out */
+  void* dx;               /* [M, K] in the compute dtype */
+  float* dA;              /* [rank, K] fp32 */
+  float* dB;              /* [N, rank] fp32 */
+} qlora_bwd_item;
+
+size_t qlora_bwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_bwd_item* items, nf4_dtype compute);
+nf4_status qlora_linear_bwd_batch(int64_t M, int32_t count, const qlora_bwd_item* items, nf4_dtype compute,
+                                  void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronize `stream`, then return the current device's status word (NF4_OK if no
  * device-side condition was recorded); clear != 0 resets it to NF4_OK. */
 nf4_status qlora_last_device_status(void* stream, int32_t clear);

@@ -250,3 +250,69 @@ def test_decoded_weight_entry_points_equal_the_nf4_calls(lib, dtype, M, N, K, r)
         fb = parity.forward_bounds(xh, w_deq, Ah, Bh, s, compute, y_ref, T_ref)
         parity.check({"y": y2.float().cpu().numpy(), "T": T2.cpu().numpy()}, {"y": y_ref, "T": T_ref},
                      {"y": fb["y"], "T": fb["T"]}, compute)
+
+
+@pytest.mark.parametrize("compute", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,r", [(17, 8, 64, 2), (65, 72, 128, 1), (511, 576, 576, 16), (1000, 192, 576, 17),
+                                     (97, 1024, 1024, 32), (300, 520, 960, 24)])
+def test_fused_small_shape_path(lib, compute, M, N, K, r):
+    """Weights of at most 2^21 elements with K, N <= 1024 and rank <= 32 at M > 16 run the fused
+    small-shape kernels (one forward launch, two backward): ragged token and feature tiles,
+    ranks that fill 1 to 32 of the padded rank, the full-size limits."""
+    _run_case(M, N, K, r, 16.0, compute, seed=M + N + r)
+
+
+@pytest.mark.parametrize("M,N,K,r", [(130, 200, 192, 40), (300, 264, 576, 48)])
+def test_tiled_path_small_ragged_shapes(lib, M, N, K, r):
+    """A rank above 32 keeps small weights on the tiled tensor-core path: its ragged tiles at
+    the shapes the fused path otherwise takes."""
+    _run_case(M, N, K, r, 16.0, "bf16", seed=M + r)
+
+
+def test_fused_small_shape_batch_forward_equals_single_calls(lib):
+    """qlora_linear_fwd_batch runs its small-weight items in one fused launch (8 at most per
+    launch) and the rest one call each; every item equals its single call bit for bit."""
+    M = 384
+    shapes = [(576, 576, 16), (192, 576, 16)] * 5 + [(1536, 576, 16)]
+    items, singles = [], []
+    for i, (N, K, r) in enumerate(shapes):
+        q, _ = _quantized_weight(N, K, 70 + i)
+        x = torch.from_numpy(wl.normal((M, K), 1.0, 1, 80 + i)).to(DEV).bfloat16()
+        A, B = (torch.from_numpy(t).to(DEV) for t in wl.adapters(N, K, r, 1, 90 + i))
+        items.append(dict(x=x, W=q, A=A, B=B, alpha=32.0))
+        singles.append(binding.qlora_linear_fwd(x, q, A, B, 32.0))
+    outs = binding.qlora_linear_fwd_batch(items)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    for (y, T), (y1, T1) in zip(outs, singles):
+        assert torch.equal(y.view(torch.int16), y1.view(torch.int16))
+        assert torch.equal(T.view(torch.int32), T1.view(torch.int32))
+
+
+def test_batch_backward_equals_single_calls(lib):
+    """qlora_linear_bwd_batch: the small-weight items (some with the stored weight, some with
+    the decoded one) in fused groups of at most 8, the others one call each; every item equals
+    its single qlora_linear_bwd bit for bit."""
+    M = 300
+    shapes = [(576, 576, 16), (192, 576, 16)] * 5 + [(1536, 576, 16), (264, 576, 5)]
+    x = torch.from_numpy(wl.normal((M, 576), 1.0, 1, 111)).to(DEV).bfloat16()
+    items, singles = [], []
+    for i, (N, K, r) in enumerate(shapes):
+        q, _ = _quantized_weight(N, K, 120 + i)
+        A, B = (torch.from_numpy(t).to(DEV) for t in wl.adapters(N, K, r, 1, 130 + i))
+        dy = torch.from_numpy(wl.normal((M, N), 1.0, 1, 140 + i)).to(DEV).bfloat16()
+        _, T = binding.qlora_linear_fwd(x, q, A, B, 32.0)
+        it = dict(dy=dy, x=x, T=T, A=A, B=B, alpha=32.0)
+        if i % 3 == 1:
+            it["w16"] = binding.nf4_dequantize(q, torch.bfloat16)
+        else:
+            it["W"] = q
+        items.append(it)
+        singles.append(binding.qlora_linear_bwd(dy, x, T, q, A, B, 32.0))
+    outs = binding.qlora_linear_bwd_batch(items)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    for got, want in zip(outs, singles):
+        assert torch.equal(got[0].view(torch.int16), want[0].view(torch.int16))
+        assert torch.equal(got[1].view(torch.int32), want[1].view(torch.int32))
+        assert torch.equal(got[2].view(torch.int32), want[2].view(torch.int32))

@@ -169,15 +169,15 @@ def test_quantize_batch_equals_single_calls(lib):
 
 
 def test_quantize_ticket_counters_wrap(lib):
-    """The block pass's ticket counters come from a pool of 4096 that every double-quant call
-    puts back to zero: 4200 calls in a row (every counter used again) all give the oracle's
-    offset."""
+    """The block pass's ticket counters come from the library's pool of 16384 that every call
+    puts back to zero: 16500 double-quant calls in a row (every counter used again) all give the
+    oracle's offset."""
     x = wl.device_normal((16384 * 2 + 5,), 0.02, wl.seed_for(5, 600), DEV, torch.bfloat16)
     ref = onf4.quantize(_host_values(x), double_quant=True)
     q = binding.Nf4Tensor.empty(tuple(x.shape), True, DEV)
     ws = torch.empty(binding.load().nf4_quantize_workspace_bytes(x.numel(), 1), dtype=torch.uint8, device=DEV)
-    offsets = torch.empty(4200, dtype=torch.float32, device=DEV)
-    for i in range(4200):
+    offsets = torch.empty(16500, dtype=torch.float32, device=DEV)
+    for i in range(16500):
         binding.nf4_quantize(x, True, out=q, workspace=ws)
         offsets[i:i + 1].copy_(q.offset[:1])
     torch.cuda.synchronize()
