@@ -105,6 +105,30 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def gpu_local_cpus(dev):
+    """The host CPUs that the kernel lists as local to this GPU's PCI function, or None.
+
+    Pinned host pages land on the memory node of the thread that allocates them; on a
+    machine with several host memory nodes, a node far from the GPU roughly halves the
+    host-to-device copy rate, so the e2e buffers are allocated from a thread held here."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    path = f"/sys/bus/pci/devices/{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0/local_cpulist"
+    try:
+        text = open(path).read().strip()
+    except OSError:
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        elif part:
+            cpus.add(int(part))
+    cpus &= os.sched_getaffinity(0)
+    return cpus or None
+
+
 # ---- clock sampling ---------------------------------------------------------------
 
 class ClockSampler:
@@ -1115,6 +1139,10 @@ def main():
         # each projection's inputs (bf16 master weight, x, dY) come from pinned host memory and
         # its dA, dB go back; the copies run on two copy streams (each tensor in halves, one per
         # copy engine) ahead of the compute, and each projection waits only for its own inputs
+        local_cpus = gpu_local_cpus(dev)
+        saved_affinity = os.sched_getaffinity(0)
+        if local_cpus:
+            os.sched_setaffinity(0, local_cpus)
         host_in = [[t.cpu().pin_memory() for t in layer.inputs_of(p)] for p in layer.proj]
         host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in layer.results_of(p)]
                     for p in layer.proj]
@@ -1162,8 +1190,12 @@ def main():
         e_steps = max(3, args.steps // 3)
         e_ms = max_over_ranks(time_e2e(e_steps), world)
         barrier(world)
+        os.sched_setaffinity(0, saved_affinity)
         e2e = {"value": world * flops * e_steps / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "host_threads": (f"held on the GPU's {len(local_cpus)} local CPUs while the pinned "
+                                "buffers are allocated and the steps are issued") if local_cpus
+                               else "not held (no local CPU list for this GPU)"}
 
     if rank == 0:
         line = {

@@ -28,7 +28,10 @@
 //   warp 1      TMEM allocation (pair-wide); in the even CTA, lane 0 issues the MMAs;
 //   warps 2..5  epilogue: tcgen05.ld of this CTA's accumulator rows, bf16 stores.
 // Two accumulators of 256 columns let the epilogue of one tile overlap the main loop of
-// the next.  Tiles left for a last, partial round of clusters are split along the
+// the next.  A cluster's units alternate the direction of the contraction (even units
+// forwards, odd ones backwards), so that a round of clusters starts where the previous one
+// ended and finds those slices of the token operand still in L2.  Tiles left for a last,
+// partial round of clusters are split along the
 // contraction; the parts' fp32 partial sums are added in a fixed order.  Every mbarrier
 // wait and the partial-sum flag wait is bounded in time; a wait that gives up sets
 // NF4_ERR_TIMEOUT in the status word and the CTA winds down, freeing its TMEM.
@@ -216,7 +219,11 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
             continue;
           }
           if (st < un.nred) {
-            const int k0 = (un.red0 + st) * kStepK;
+            // odd units walk the contraction backwards: the clusters of one round move through
+            // it together, so the next round starts on the slices this one read last, which
+            // are still in L2 when an operand is too large for L2 to hold whole
+            const int kst = (lt & 1) ? un.nred - 1 - st : st;
+            const int k0 = (un.red0 + kst) * kStepK;
             if (rank == 0) mbar_expect_tx(bar(kBarFull + s), kCluster * 2 * kSubs * kSubBytes);
 #pragma unroll
             for (int u = 0; u < kSubs; ++u) {
