@@ -83,6 +83,8 @@ struct GemmParams {
   int pairs_f;         // ceil(tiles_f / 2): feature-tile pairs; an odd count leaves the last pair's
                        // second tile past F (loads read zeros, the epilogue stores nothing)
   int f_fast;          // pair order: 1 = feature pairs vary fastest, 0 = token tiles
+  int band;            // > 0: token tiles in bands of `band`, the band's tiles fastest within a
+                       // feature pair, the feature pairs next, the bands slowest (overrides f_fast)
   int f16;             // operands and output are IEEE half (else bf16)
   void* out;           // [M, F] 16-bit
   int* status;
@@ -135,6 +137,19 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int64_t u) {
   return x;
 }
 
+// Token tile (x) and feature pair (y) of tile pair `pair`, in the launch's order.
+__device__ __forceinline__ longlong2 tile_pair_of(const GemmParams& p, int64_t pair) {
+  if (p.band > 0) {
+    const int64_t per = static_cast<int64_t>(p.band) * p.pairs_f;
+    const int64_t bi = pair / per, t0 = bi * p.band;
+    const int64_t bt = min(static_cast<int64_t>(p.band), static_cast<int64_t>(p.tiles_t) - t0);
+    const int64_t idx = pair - bi * per;
+    return make_longlong2(t0 + idx % bt, idx / bt);
+  }
+  if (p.f_fast) return make_longlong2(pair / p.pairs_f, pair % p.pairs_f);
+  return make_longlong2(pair % p.tiles_t, pair / p.tiles_t);
+}
+
 // Slot and phase of the stage ring, advanced once per step by every role.
 struct Ring {
   int s = 0;
@@ -163,8 +178,8 @@ bf16_tc_gemm(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ C
   auto lead_bar = [&](int i) { return mapa_shared(bar(i), 0); };
   const int64_t cluster_id = blockIdx.x / kCluster;
   const int64_t n_clusters = gridDim.x / kCluster;
-  auto tile_t = [&](int64_t pair) { return p.f_fast ? pair / p.pairs_f : pair % p.tiles_t; };
-  auto tile_f = [&](int64_t pair) { return 2 * (p.f_fast ? pair % p.pairs_f : pair / p.tiles_t) + rank; };
+  auto tile_t = [&](int64_t pair) { return tile_pair_of(p, pair).x; };
+  auto tile_f = [&](int64_t pair) { return 2 * tile_pair_of(p, pair).y + rank; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -597,6 +612,12 @@ GemmParams base_params(const LinearArgs& a, bool f16, int mode, void* out, int* 
   // each round of clusters re-reads the whole operand along the fast dimension: run the
   // feature pairs fastest only when the weight panel set (F rows) is smaller than the tokens
   p.f_fast = p.F < a.M ? 1 : 0;
+  // when neither operand fits in half of L2 (down's forward, gate's and up's dX at 4096
+  // tokens), a round of clusters covers a block of 8 token tiles by about 76 / 8 feature pairs
+  // (8 is near the square root of the 76 clusters): it reads 8 token panels and 9 or 10 weight
+  // panels where the plain order reads every token panel, and the next round shares half of them
+  const int64_t half_l2 = 64ll << 20;
+  p.band = (2 * a.M * red > half_l2 && 2 * p.F * red > half_l2 && p.tiles_t > 8 && p.pairs_f > 8) ? 8 : 0;
   p.out = out;
   p.status = status;
   return p;

@@ -10,11 +10,11 @@
 // Lane mapping of the block and decode kernels: a warp walks rows of 1024 elements and lane
 // l owns elements 32l .. 32l + 31 of a row, so a lane pair holds one 64-element block.
 //
-// quantize = two launches:
-//   1. nf4_encode_blocks: absmax, 4-bit codes, packing; per 256-block group the
-//      float64 pairwise-tree sum of the absmax values, and in the CTA that finishes
-//      last the tree over the group sums -> offset (double quant only).
-//   2. nf4_encode_nested: centre, nested absmax per group, dynamic8 codes.
+// quantize = two launches (a call, or a batch of up to 8 tensors):
+//   1. nf4_encode_blocks: absmax, 4-bit codes, packing; with double quantization per 256-block
+//      group the float64 pairwise-tree sum of the absmax values, and, by the CTA that counts a
+//      tensor's last group, the tree over the group sums -> offset.
+//   2. nf4_encode_nested (double quantization): centre, nested absmax per group, dynamic8 codes.
 #include "common.cuh"
 #include "decode.cuh"
 #include "prep.cuh"
@@ -190,12 +190,12 @@ __device__ __forceinline__ void lane_codes(const uint32_t (&w)[8 * sizeof(Tin)],
 }
 
 // One row of 1024 elements from the lane's words: block maxima, codes, the packed bytes and
-// the fp32 maxima; the group's double copy of each maximum goes to gs_slot.  Returns true if
+// the fp32 maxima; the group's copy of each maximum goes to gs_slot.  Returns true if
 // the lane's block holds a non-finite value.
 template <typename Tin>
 __device__ __forceinline__ bool encode_row(const uint32_t (&w)[8 * sizeof(Tin)], int64_t e0, int64_t numel,
                                            uint8_t* __restrict__ packed, float* __restrict__ absmax,
-                                           double* gs_slot, uint32_t tab_base, bool fast_ok,
+                                           float* gs_slot, uint32_t tab_base, bool fast_ok,
                                            const float* thr, int lane) {
   uint32_t mb = lane_absmax_bits<Tin>(w);
   mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));  // the lane pair holds one block
@@ -218,9 +218,55 @@ __device__ __forceinline__ bool encode_row(const uint32_t (&w)[8 * sizeof(Tin)],
   if ((lane & 1) == 0) {
     const float a = __uint_as_float(mb);
     if (e0 < numel) absmax[e0 >> 6] = a;
-    *gs_slot = (e0 < numel) ? static_cast<double>(a) : 0.0;
+    *gs_slot = (e0 < numel) ? a : 0.0f;
   }
   return mb >= 0x7F800000u;
+}
+
+// Sum of a group's 256 block maxima (non-negative fp32, gs[0..255]) as the float64 pairwise
+// tree s[i] += s[i + h], h = 128, 64, ..., 1 computes it, by one warp; the result is in lane 0.
+// Write each maximum as M * 2^(E - 150) with an integer M < 2^24 and E = max(biased exponent, 1).
+// When the group's E span at most 21 (and all are finite), every partial sum of the tree is a
+// multiple of 2^(Emin - 150) below 2^53 of those units, so each float64 addition is exact and
+// the tree's result is the exact sum: it is formed in integers (two 32-bit warp sums of the
+// 24-bit halves) and scaled once by a power of two.  Otherwise the tree runs in float64, lane l
+// holding s[l + 32 m]: the levels h >= 32 add within the lane, the rest across lanes.
+__device__ __forceinline__ double group_sum(const float* gs, int lane) {
+  uint32_t v[kNested / 32];
+  uint32_t emin = 255u, emax = 0u;
+#pragma unroll
+  for (int m = 0; m < kNested / 32; ++m) {
+    v[m] = __float_as_uint(gs[lane + 32 * m]);
+    const uint32_t e = max(v[m] >> 23, 1u);
+    if (v[m] != 0u) emin = min(emin, e), emax = max(emax, e);
+  }
+  emin = __reduce_min_sync(0xffffffffu, emin);
+  emax = __reduce_max_sync(0xffffffffu, emax);
+  if (emax == 0u) return 0.0;   // every maximum is +0
+  if (emax < 255u && emax - emin <= 21u) {
+    uint64_t acc = 0;
+#pragma unroll
+    for (int m = 0; m < kNested / 32; ++m) {
+      const uint32_t be = v[m] >> 23;
+      const uint64_t mant = (v[m] & 0x7FFFFFu) | (be != 0u ? 0x800000u : 0u);
+      if (v[m] != 0u) acc += mant << (max(be, 1u) - emin);
+    }
+    const uint32_t lo = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(acc & 0xFFFFFFu));
+    const uint32_t hi = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(acc >> 24));
+    const uint64_t total = (static_cast<uint64_t>(hi) << 24) + lo;   // < 2^53: converts exactly
+    const double unit = __longlong_as_double(static_cast<long long>(static_cast<int>(emin) - 150 + 1023) << 52);
+    return __dmul_rn(__ull2double_rn(total), unit);
+  }
+  double t[kNested / 32];
+#pragma unroll
+  for (int m = 0; m < kNested / 32; ++m) t[m] = static_cast<double>(__uint_as_float(v[m]));
+#pragma unroll
+  for (int h = kNested / 64; h >= 1; h >>= 1)
+#pragma unroll
+    for (int m = 0; m < h; ++m) t[m] += t[m + h];
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
+  return t[0];
 }
 
 // The offset: the float64 pairwise tree s[i] += s[i + h], h = p2/2, ..., 1, over the group
@@ -272,8 +318,29 @@ __device__ __forceinline__ float offset_tree(double* gs, int64_t ng, int64_t p2,
   return offset;
 }
 
+// Nested quantization (per nested group of 256 maxima): c = a - offset, m = max |c| over the
+// group, code = dyn8 code of RN(c / m), i.e. the number of thresholds at or below it.
+// Rows of the dyn8 search: |q| in [2^-7, 1] split by sign and by the float's top six
+// fraction bits (64 rows a binade, 449 rows a sign, the last holding 1.0).  Each CTA derives
+// every row from the thresholds: with lo and hi the row's most negative and most positive
+// floats, base = code(lo), and if code(hi) <= base + 1 then code(q) = base + (q >= thr[base])
+// for every q of the row (code is a step function that crosses at most one threshold there);
+// a row that crosses more (none does for the dyn8 values) is marked and searched in full.
+constexpr uint32_t kDynRow0 = 7680u;          // bits(2^-7) >> 17
+constexpr int kDynRows = 449;
+constexpr uint32_t kDynAmbiguous = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t dyn8_code(float q, const uint2* rows, const float* thr) {
+  const uint32_t qb = __float_as_uint(q), ab = qb & 0x7FFFFFFFu;
+  if (ab >= (kDynRow0 << 17) && ab < ((kDynRow0 + kDynRows) << 17)) {
+    const uint2 e = rows[(ab >> 17) - kDynRow0 + (qb >> 31) * kDynRows];
+    if (e.y != kDynAmbiguous) return e.y + (q >= __uint_as_float(e.x) ? 1u : 0u);
+  }
+  return static_cast<uint32_t>(dyn8_encode(q, thr));   // small |q|, NaN, or a marked row
+}
+
 // One tensor of a block pass.  Its groups are numbers g0 .. g0 + ng - 1 of the launch's
-// concatenated group list; `ctas` CTAs (min(ng, grid)) take at least one of them.
+// concatenated group list.
 struct EncodeItem {
   const void* x;
   int64_t numel, ng, g0, p2;
@@ -282,13 +349,13 @@ struct EncodeItem {
   double* group_sum;      // double quant: the workspace's group sums, p2 entries; else null
   unsigned* ticket;       // double quant: a zero counter of the library's ticket pool
   float* offset;          // double quant: the tensor's offset
-  unsigned ctas;
 };
 constexpr int kEncodeBatch = kQuantBatchMax;
 struct EncodeBatch {
   EncodeItem it[kEncodeBatch];
   int n;
   int64_t total;          // groups of all items
+  unsigned* work;         // with any double-quant item: a zero counter handing out groups
 };
 
 __device__ __forceinline__ int item_of(const EncodeItem* items, int n, int64_t g) {
@@ -300,16 +367,20 @@ __device__ __forceinline__ int item_of(const EncodeItem* items, int n, int64_t g
 
 // Block pass: absmax, 4-bit codes and packing, one nested group (256 blocks, 16384
 // elements) at a time, over the groups of up to 8 tensors of one input type; with double
-// quantization also the float64 pairwise-tree sum of each group's absmax.  Persistent: CTA c
-// takes groups c, c + G, c + 2G, ... of the concatenated list (G = gridDim.x, sized to the
-// CTAs resident at once).  Warp w codes rows 2w and 2w + 1 of a group (1024 elements each;
-// lane l elements 32l .. 32l + 31, so a lane pair holds one block); after coding a row it
-// loads the same row of its next group into the row's registers, so one row per warp is
-// always in flight while the other is coded.  The group's 256 maxima meet in shared memory
-// (two buffers, by group parity) and one warp, rotating, sums them.  When a CTA leaves a
-// tensor it takes that tensor's ticket; the CTA that draws the last one sums the tensor's
-// group sums into its offset and puts the counter back to zero (the pattern of a grid
-// barrier's arrival: the CTA's threads meet, thread 0 fences and counts).
+// quantization also the float64 pairwise-tree sum of each group's absmax.  Persistent (the grid
+// is the CTAs resident at once): CTA c takes group c first, then, without double quantization,
+// c + G, c + 2G, ... (G = gridDim.x); with any double-quant item the further groups are handed
+// out by a counter in the order CTAs ask, so that CTAs the warp schedulers serve less often take
+// fewer groups and all finish together.  Warp w codes rows 2w and 2w + 1 of a group (1024
+// elements each; lane l elements 32l .. 32l + 31, so a lane pair holds one block); after coding
+// a row it loads the same row of its next group into the row's registers, so one row per warp
+// is always in flight while the other is coded.  With the counter, thread 0 asks for the group
+// after next while the CTA codes a group, and the CTA's threads meet once per group, which
+// publishes the answer.  With double quantization the group's 256 maxima meet in shared memory
+// (two buffers, by group parity) and one warp, rotating, sums them; it then fences and counts
+// the group on its tensor's ticket, and the warp that counts a tensor's last group has its CTA
+// sum the tensor's group sums into the offset after the CTA's next meeting, then put the
+// counter back to zero (the arrival pattern of a grid barrier, without any waiting).
 template <typename Tin, bool kV8>
 __global__ void __launch_bounds__(kQuantThreads, sizeof(Tin) == 2 ? 3 : 2)
 nf4_encode_blocks(EncodeBatch b, EncodeTables tabs, int* status) {
@@ -318,10 +389,11 @@ nf4_encode_blocks(EncodeBatch b, EncodeTables tabs, int* status) {
   // and lanes l, l + 16 never meet in one bank access.  bf16: {cut, base}; fp32: {bits of
   // lo with the base code in its low 4 bits, bits of hi}
   __shared__ uint2 tab[66][16];
-  __shared__ double gsum[2][kNested];
-  __shared__ double tree[1024];      // the offset tree of a tensor this CTA finishes last
+  __shared__ float gsum[2][kNested];
+  __shared__ double tree[1024];      // the offset tree of a tensor this CTA finishes
   __shared__ EncodeItem items[kEncodeBatch];   // indexed at run time: kept out of the parameters
-  __shared__ unsigned s_last;
+  __shared__ int s_next[2];          // the group after next, by group parity (counter mode)
+  __shared__ int s_fin;              // item whose offset this CTA computes next, or -1
 #pragma unroll
   for (int k = 0; k < kEncodeBatch; ++k)
     if (threadIdx.x == k) items[k] = b.it[k];   // static indices into the parameters
@@ -344,7 +416,25 @@ nf4_encode_blocks(EncodeBatch b, EncodeTables tabs, int* status) {
   constexpr int kW = 8 * sizeof(Tin);
   const int64_t lane_off = warp * 2048 + 32 * lane;
   const int slot = warp * 32 + (lane >> 1);    // block of the group held by the lane pair (row 2w)
-  int64_t g = blockIdx.x;
+  const bool dyn = b.work != nullptr;
+  // the counter hands out groups G, G + 1, ...; every CTA asks until it is refused once, so
+  // the counter ends at `total` and the CTA given total - 1 puts it back to zero
+  // (group numbers fit in 31 bits: the host checks the total)
+  const int total = static_cast<int>(b.total);
+  auto ask = [&]() -> int {
+    const unsigned v = atomicAdd(b.work, 1u);
+    if (static_cast<int>(v) == total - 1) *b.work = 0u;
+    return static_cast<int>(gridDim.x + v);
+  };
+  int g = blockIdx.x, gn = g + gridDim.x;
+  if (dyn) {
+    if (threadIdx.x == 0) {
+      s_next[0] = ask();
+      s_fin = -1;
+    }
+    __syncthreads();
+    gn = s_next[0];
+  }
   int ci = item_of(items, b.n, g);
   uint32_t wa[kW], wb[kW];
   {
@@ -353,105 +443,66 @@ nf4_encode_blocks(EncodeBatch b, EncodeTables tabs, int* status) {
     lane_words<Tin, kV8>(x, e.numel, (g - e.g0) * kGroupElems + lane_off, wa);
     lane_words<Tin, kV8>(x, e.numel, (g - e.g0) * kGroupElems + lane_off + 1024, wb);
   }
+  // the offset of item f, by the whole CTA (its last group sum is written and counted)
+  auto finish = [&](int f) {
+    __syncthreads();   // every thread has read s_fin
+    if (threadIdx.x == 0) s_fin = -1;
+    __threadfence();
+    const EncodeItem& e = items[f];
+    const float off = offset_tree(e.group_sum, e.ng, e.p2, (e.numel + kBlock - 1) / kBlock, tree);
+    if (threadIdx.x == 0) {
+      *e.offset = off;
+      *e.ticket = 0u;
+    }
+    __syncthreads();   // `tree` is free again
+  };
   bool nonfinite = false;
 #pragma unroll 1
-  for (int it = 0; g < b.total; ++it) {
+  for (int it = 0; g < total; ++it) {
     const EncodeItem& e = items[ci];
     const int64_t gl = g - e.g0;                 // group within the tensor
     const int64_t e0 = gl * kGroupElems + lane_off;
-    const int64_t gn = g + gridDim.x;            // this CTA's next group
-    const int ni = gn < b.total ? item_of(items, b.n, gn) : ci;
-    double* gs = gsum[it & 1];
+    const int ni = gn < total ? item_of(items, b.n, gn) : ci;
+    if (dyn && threadIdx.x == 0) s_next[(it + 1) & 1] = gn < total ? ask() : total;
+    float* gs = gsum[it & 1];
     nonfinite |= encode_row<Tin>(wa, e0, e.numel, e.packed, e.absmax, gs + slot, tab_base, fast_ok, thr, lane);
-    if (gn < b.total)
+    if (gn < total)
       lane_words<Tin, kV8>(static_cast<const Tin*>(items[ni].x), items[ni].numel,
                            (gn - items[ni].g0) * kGroupElems + lane_off, wa);
     nonfinite |= encode_row<Tin>(wb, e0 + 1024, e.numel, e.packed, e.absmax, gs + slot + 16, tab_base, fast_ok, thr,
                                  lane);
-    if (gn < b.total)
+    if (gn < total)
       lane_words<Tin, kV8>(static_cast<const Tin*>(items[ni].x), items[ni].numel,
                            (gn - items[ni].g0) * kGroupElems + lane_off + 1024, wb);
-    if (e.group_sum != nullptr) {
+    int gnn = gn + gridDim.x;
+    if (dyn) {
       __syncthreads();
-      if (warp == (it & 7)) {
-        // float64 pairwise tree s[i] += s[i + h], h = 128, 64, ..., 1, by one warp: lane l
-        // holds s[l + 32 m]; the levels h >= 32 add within the lane, the rest across lanes
-        double t[kNested / 32];
-#pragma unroll
-        for (int m = 0; m < kNested / 32; ++m) t[m] = gs[lane + 32 * m];
-#pragma unroll
-        for (int h = kNested / 64; h >= 1; h >>= 1)
-#pragma unroll
-          for (int m = 0; m < h; ++m) t[m] += t[m + h];
-#pragma unroll
-        for (int h = 16; h >= 1; h >>= 1) t[0] += __shfl_down_sync(0xffffffffu, t[0], h);
-        if (lane == 0) e.group_sum[gl] = t[0];
-      }
-      if (gn >= e.g0 + e.ng) {   // this CTA's last group of the tensor: its ticket
-        __syncthreads();
-        if (threadIdx.x == 0) {
+      gnn = s_next[(it + 1) & 1];
+      const int f = s_fin;
+      if (f >= 0) finish(f);
+      if (e.group_sum != nullptr && warp == (it & 7)) {
+        const double sum = group_sum(gs, lane);
+        if (lane == 0) {
+          e.group_sum[gl] = sum;
           __threadfence();
-          s_last = (atomicAdd(e.ticket, 1u) == e.ctas - 1) ? 1u : 0u;
-        }
-        __syncthreads();
-        if (s_last != 0) {
-          __threadfence();
-          const float off = offset_tree(e.group_sum, e.ng, e.p2, (e.numel + kBlock - 1) / kBlock, tree);
-          if (threadIdx.x == 0) {
-            *e.offset = off;
-            *e.ticket = 0u;
-          }
-          __syncthreads();   // `tree` is free again before this CTA could need it for another tensor
+          if (atomicAdd(e.ticket, 1u) == static_cast<unsigned>(e.ng - 1)) s_fin = ci;
         }
       }
     }
     g = gn;
+    gn = gnn;
     ci = ni;
+  }
+  if (dyn) {
+    __syncthreads();
+    const int f = s_fin;
+    if (f >= 0) finish(f);
   }
   if (nonfinite) atomicCAS(status, 0, static_cast<int>(NF4_ERR_NONFINITE));
 }
 
-// Nested codes of group g: one warp, eight maxima per lane.
-__device__ __forceinline__ void nested_group(const float* __restrict__ absmax, int64_t nb, int64_t g, float offset,
-                                             const float* thr, uint8_t* __restrict__ codes,
-                                             float* __restrict__ nested, int lane) {
-  const int64_t b0 = g * kNested + 8 * lane;
-  float c[8];
-  const bool full = b0 + 8 <= nb && (reinterpret_cast<uintptr_t>(absmax + b0) & 15) == 0;
-  if (full) {
-    const float4 u = *reinterpret_cast<const float4*>(absmax + b0);
-    const float4 v = *reinterpret_cast<const float4*>(absmax + b0 + 4);
-    const float a[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = __fsub_rn(a[i], offset);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = (b0 + i < nb) ? __fsub_rn(absmax[b0 + i], offset) : 0.0f;
-  }
-  float m = fabsf(c[0]);
-#pragma unroll
-  for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(c[i]));
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  uint32_t q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    q[i] = static_cast<uint32_t>((m > 0.0f) ? dyn8_encode(__fdiv_rn(c[i], m), thr) : kDyn8ZeroCode);
-  if (b0 + 8 <= nb && (reinterpret_cast<uintptr_t>(codes + b0) & 7) == 0) {
-    *reinterpret_cast<uint2*>(codes + b0) =
-        make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24), q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (b0 + i < nb) codes[b0 + i] = static_cast<uint8_t>(q[i]);
-  }
-  if (lane == 0) nested[g] = m;
-}
-
-// Nested quantization of the block maxima: one warp per group of 256 maxima, eight per
-// lane, over the groups of up to 8 tensors (numbered as in the block pass).  c = a - offset
-// (the offset written by the block pass's last CTA of the tensor); m = max |c| over the
-// group; code = dyn8 code of RN(c / m).
+// Nested quantization of the block maxima: one warp per group of 256 maxima, eight per lane,
+// over the groups of up to 8 tensors (numbered as in the block pass).
 constexpr int kNestedWarps = 8;
 
 struct NestedItem {
@@ -467,23 +518,88 @@ struct NestedBatch {
   int64_t total;
 };
 
+// The lane's eight maxima of group gl of a tensor (zero past nb).
+__device__ __forceinline__ void nested_load(const NestedItem& e, int64_t gl, int lane, float (&a)[8]) {
+  const int64_t b0 = gl * kNested + 8 * lane;
+  if (b0 + 8 <= e.nb && (reinterpret_cast<uintptr_t>(e.absmax + b0) & 15) == 0) {
+    const float4 u = *reinterpret_cast<const float4*>(e.absmax + b0);
+    const float4 v = *reinterpret_cast<const float4*>(e.absmax + b0 + 4);
+    a[0] = u.x, a[1] = u.y, a[2] = u.z, a[3] = u.w, a[4] = v.x, a[5] = v.y, a[6] = v.z, a[7] = v.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (b0 + i < e.nb) ? e.absmax[b0 + i] : 0.0f;
+  }
+}
+
+// Persistent: warp w of CTA b takes groups b * 8 + w, then + 8 * gridDim.x, ...; while it codes
+// one group the maxima of its next group are in flight.
 __global__ void __launch_bounds__(kNestedWarps * 32)
 nf4_encode_nested(NestedBatch b, EncodeTables tabs) {
   __shared__ float thr[256];
+  __shared__ uint2 rows[2 * kDynRows];
   __shared__ NestedItem items[kEncodeBatch];
   thr[threadIdx.x] = tabs.dyn8_thr[threadIdx.x];
 #pragma unroll
   for (int k = 0; k < kEncodeBatch; ++k)
     if (threadIdx.x == k) items[k] = b.it[k];
   __syncthreads();
+  for (int i = threadIdx.x; i < 2 * kDynRows; i += kNestedWarps * 32) {
+    const bool neg = i >= kDynRows;
+    const uint32_t r0 = (kDynRow0 + static_cast<uint32_t>(neg ? i - kDynRows : i)) << 17;
+    const float lo = neg ? -__uint_as_float(r0 | 0x1FFFFu) : __uint_as_float(r0);
+    const float hi = neg ? -__uint_as_float(r0) : __uint_as_float(r0 | 0x1FFFFu);
+    const int clo = dyn8_encode(lo, thr), chi = dyn8_encode(hi, thr);
+    rows[i] = make_uint2(__float_as_uint(thr[clo]), chi - clo <= 1 ? static_cast<uint32_t>(clo) : kDynAmbiguous);
+  }
+  __syncthreads();
   pdl_allow_next();
   pdl_wait();
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * kNestedWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kNestedWarps;
+  int64_t g = static_cast<int64_t>(blockIdx.x) * kNestedWarps + (threadIdx.x >> 5);
   if (g >= b.total) return;
-  int i = 0;
-  while (i + 1 < b.n && g >= items[i + 1].g0) ++i;
-  const NestedItem& e = items[i];
-  nested_group(e.absmax, e.nb, g - e.g0, *e.offset, thr, e.codes, e.nested, threadIdx.x & 31);
+  int ci = 0;
+  while (ci + 1 < b.n && g >= items[ci + 1].g0) ++ci;
+  float a[8];
+  nested_load(items[ci], g - items[ci].g0, lane, a);
+  int oi = -1;
+  float offset = 0.0f;
+  while (g < b.total) {
+    const NestedItem& e = items[ci];
+    if (oi != ci) offset = *e.offset, oi = ci;
+    const int64_t gl = g - e.g0;
+    float c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = __fsub_rn(a[i], offset);
+    const int64_t gn = g + stride;
+    int ni = ci;
+    if (gn < b.total) {   // the next group's maxima, loaded while this one is coded
+      while (ni + 1 < b.n && gn >= items[ni + 1].g0) ++ni;
+      nested_load(items[ni], gn - items[ni].g0, lane, a);
+    }
+    const int64_t b0 = gl * kNested + 8 * lane;
+    // maxima past nb do not count
+    float m = b0 < e.nb ? fabsf(c[0]) : 0.0f;
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+      if (b0 + i < e.nb) m = fmaxf(m, fabsf(c[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = (m > 0.0f) ? dyn8_code(__fdiv_rn(c[i], m), rows, thr) : kDyn8ZeroCode;
+    if (b0 + 8 <= e.nb && (reinterpret_cast<uintptr_t>(e.codes + b0) & 7) == 0) {
+      *reinterpret_cast<uint2*>(e.codes + b0) = make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24),
+                                                           q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (b0 + i < e.nb) e.codes[b0 + i] = static_cast<uint8_t>(q[i]);
+    }
+    if (lane == 0) e.nested[gl] = m;
+    g = gn;
+    ci = ni;
+  }
 }
 
 // ---- dequantize -----------------------------------------------------------------
@@ -665,12 +781,12 @@ namespace {
 
 cudaError_t ticket_slot(unsigned** out) { return ticket_range(1, out); }
 
-// Resident CTAs per SM of an encode kernel (kind: input type and load width), per device,
-// looked up once (a racing first lookup stores the same value).
+// Resident CTAs per SM of an encode kernel (kind: input type and load width; 4 the nested
+// pass), per device, looked up once (a racing first lookup stores the same value).
 template <typename K>
 cudaError_t encode_ctas_per_sm(K kernel, int kind, int* out) {
   constexpr int kMaxDev = 64;
-  static std::atomic<int> cache[kMaxDev][4];
+  static std::atomic<int> cache[kMaxDev][5];
   int dev = 0;
   cudaGetDevice(&dev);
   const bool slot = dev >= 0 && dev < kMaxDev;
@@ -726,12 +842,11 @@ cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int
     total += ng;
   }
   eb.total = total;
+  if (total + device_sm_count() * static_cast<int64_t>(resident) > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(resident) * device_sm_count());
-  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   for (int i = 0; i < n; ++i) {
     const nf4_tensor& out = *jobs[i].out;
     EncodeItem& it = eb.it[i];
-    it.ctas = static_cast<unsigned>(std::min<int64_t>(it.ng, grid));
     if (!out.double_quant) {
       it.absmax = static_cast<float*>(out.absmax);
       continue;
@@ -751,6 +866,7 @@ cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int
     ni.nested = out.nested_absmax;
     nbt.total += it.ng;
   }
+  if (nbt.n > 0 && (e = ticket_slot(&eb.work)) != cudaSuccess) return e;
   const dim3 egrid(static_cast<unsigned>(grid)), block(kQuantThreads);
   if (xd == NF4_F32)
     e = v8 ? launch_pdl(nf4_encode_blocks<float, true>, egrid, block, 0, st, 1, eb, et, status)
@@ -760,8 +876,10 @@ cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int
            : launch_pdl(nf4_encode_blocks<__nv_bfloat16, false>, egrid, block, 0, st, 1, eb, et, status);
   note_launch();
   if (e != cudaSuccess || nbt.n == 0) return e;
-  const int64_t ngrid = (nbt.total + kNestedWarps - 1) / kNestedWarps;
-  if (ngrid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  int nres = 1;
+  if ((e = encode_ctas_per_sm(nf4_encode_nested, 4, &nres)) != cudaSuccess) return e;
+  const int64_t ngrid = std::min<int64_t>((nbt.total + kNestedWarps - 1) / kNestedWarps,
+                                          static_cast<int64_t>(nres) * device_sm_count());
   e = launch_pdl(nf4_encode_nested, dim3(static_cast<unsigned>(ngrid)), dim3(kNestedWarps * 32), 0, st, 1, nbt, et);
   note_launch();
   return e;

@@ -13,11 +13,13 @@
 // Why a separate path.  At these sizes (the SmolLM2-135M-shaped layers: K = 576, N = 576 or
 // 192, M = 512) the tiled path's chain of about ten launches per call (decode and staging,
 // skinny adapter passes and their finishes, the GEMM) costs more than the arithmetic, and its
-// 256 x 256 tiles leave most SMs idle.  Here one CTA holds a 64-token x 64-feature output tile
+// 256 x 256 tiles leave most SMs idle.  Here one CTA holds a 32-token x 64-feature output tile
 // with the whole contraction in shared memory and does every step of the tile itself: the
 // weight is decoded from the stored codes in registers straight into mma.sync fragments, the
-// rank-r down-projection of its 64 tokens is recomputed by every feature tile (r = 16 columns
+// rank-r down-projection of its 32 tokens is recomputed by every feature tile (r = 16 columns
 // against 64), and the adapter term is added from shared memory before the tile is stored.
+// Tiles are sized so that two CTAs fit an SM (about 82 KB of shared memory each at K = 576)
+// and a SmolLM2-shaped layer's q and v tiles (192 forward, 288 backward) run in one wave.
 //
 // Fragment order along the contraction.  Within each 32-deep slice, lane 4g + c of a warp
 // takes contraction indices 8c .. 8c + 7 for both operands: one 16-byte shared load of x (or
@@ -36,7 +38,7 @@
 namespace qnf4 {
 namespace {
 
-constexpr int kTT = 64;          // tokens per tile
+constexpr int kTT = 32;          // tokens per forward tile
 constexpr int kTF = 64;          // output features (forward) or input features (dX) per tile
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
@@ -60,6 +62,15 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// One float rounded to T16 into shared memory.
+template <typename T16>
+__device__ __forceinline__ void st_shared16(uint32_t addr, float v) {
+  const uint32_t p = pack2<T16>(v, 0.0f);
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(p & 0xFFFFu)) : "memory");
+}
 
 // Four 8 x 8 16-bit matrices; lane i gives the address of row i & 7 of matrix i >> 3.
 __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -69,31 +80,6 @@ __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t& r0, uint32_t& r1,
 __device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-
-// The block scales a' = dyn8[code] * nested + offset (two roundings), or the fp32 maxima without
-// double quantization, of blocks g[u] (< 0: none, giving 0), for up to U blocks per thread:
-// every load is issued before any is used.
-template <int U>
-__device__ __forceinline__ void block_scales(const Nf4View& W, const int64_t (&g)[U], const float* dyn8,
-                                             float (&out)[U]) {
-  uint32_t code[U];
-  float nest[U];
-  const float off = W.dq ? __ldg(W.offset) : 0.0f;
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    code[u] = 0, nest[u] = 0.0f;
-    if (g[u] < 0) continue;
-    if (W.dq) {
-      code[u] = __ldg(static_cast<const uint8_t*>(W.absmax) + g[u]);
-      nest[u] = __ldg(W.nested + (g[u] >> 8));
-    } else {
-      nest[u] = __ldg(static_cast<const float*>(W.absmax) + g[u]);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < U; ++u)
-    out[u] = g[u] < 0 ? 0.0f : (W.dq ? __fadd_rn(__fmul_rn(dyn8[code[u]], nest[u]), off) : nest[u]);
 }
 
 // Rows [r0, r0 + rows) of a 16-bit row-major matrix with `cols` columns (a multiple of 8) into
@@ -174,15 +160,14 @@ struct FwdParams {
 __host__ __device__ inline int64_t wrow(int64_t K, bool w16) { return w16 ? row16(K) : rowp(K); }
 
 // Shared memory of the forward: x rows, weight rows, T16(A) rows, T16(s T); with the stored
-// codes also the block scales and A's fp32 staging (with the decoded weight, A is staged in the
-// weight rows' space before they are copied).
+// codes also the block scales.
 __host__ __device__ inline int64_t fwd_smem_bytes(int64_t K, int rp, bool w16) {
   const int64_t base = kTT * row16(K) + kTF * wrow(K, w16) + rp * row16(K) + kTT * rowr(rp);
-  return w16 ? base : base + kTF * (K / 64) * 4 + rp * K * 4;
+  return w16 ? base : base + kTF * (K / 64) * 4;
 }
 
 template <typename T16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 small_fused_fwd(FwdParams p, DecodeTables tabs) {
   constexpr bool F16 = std::is_same<T16, __half>::value;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -204,6 +189,9 @@ small_fused_fwd(FwdParams p, DecodeTables tabs) {
   const int64_t local = blockIdx.x - item.unit0;
   const int64_t t0 = (local / item.tiles_f) * kTT, f0 = (local % item.tiles_f) * kTF;
   const int64_t nbr = K / 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int fw = 8 * warp;
 
   const uint32_t s_x = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   const bool dec = item.w16 == nullptr;   // decode from the stored codes
@@ -213,57 +201,111 @@ small_fused_fwd(FwdParams p, DecodeTables tabs) {
   const uint32_t s_t = s_a + rp * row16(K);
   const uint32_t s_end = s_t + kTT * rowr(rp);
   float* s_sc = reinterpret_cast<float*>(smem + (s_end - s_x));              // stored codes: scales
-  const uint32_t s_rawa = dec ? s_end + static_cast<uint32_t>(kTF * nbr * 4) : s_w;   // A, fp32
 
-  // every copy in flight at once: x rows, the packed weight rows, A (fp32), the block scales
+  // every copy in flight at once: x rows, the weight rows (packed codes or decoded values), the
+  // block scales; A straight from global memory into registers, in batches of 8 float4
   stage_rows16(s_x, row16(K), static_cast<const T16*>(item.x), t0, kTT, M, K);
-  stage_f32_raw(s_rawa, item.A, 0, rp, a.r, K, K, true);
   if (dec) {
     const int chunks = static_cast<int>(K / 32);   // 16-byte chunks of a packed row
     for (int i = threadIdx.x; i < kTF * chunks; i += kThreads) {
-      const int r = i / chunks, c = i - r * chunks;
-      const uint32_t d = s_w + static_cast<uint32_t>(r * rowp(K) + c * 16);
-      if (f0 + r < N) cp_async16(d, a.W.packed + (f0 + r) * (K / 2) + c * 16);
+      const int r = i / chunks, cc = i - r * chunks;
+      const uint32_t d = s_w + static_cast<uint32_t>(r * rowp(K) + cc * 16);
+      if (f0 + r < N) cp_async16(d, a.W.packed + (f0 + r) * (K / 2) + cc * 16);
       else asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
     }
-    constexpr int U = 1024 / kThreads;   // 64 rows x at most 16 blocks
-    int64_t gi[U];
-    float sc[U];
-    const int nb32 = static_cast<int>(nbr);
+  } else {
+    stage_rows16(s_w, row16(K), static_cast<const T16*>(item.w16), f0, kTF, N, K);
+  }
+  // B's fragments for the adapter term (8 values a lane), used after the main loop
+  float bv[2][4];
+  {
+    const int64_t f = f0 + fw + g;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = threadIdx.x + u * kThreads, r = i / nb32, kb = i - r * nb32;
-      gi[u] = (i < kTF * nb32 && f0 + r < N) ? (f0 + r) * nbr + kb : -1;
+    for (int kk = 0; kk < 2; ++kk) {
+      const int j0 = 16 * kk + 2 * c;
+      const int js[4] = {j0, j0 + 1, j0 + 8, j0 + 9};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) bv[kk][e] = (f < N && js[e] < a.r) ? __ldg(item.B + f * a.r + js[e]) : 0.0f;
     }
-    block_scales<U>(a.W, gi, dyn8, sc);
+  }
+  // the block scales' inputs and A's first 12 float4 a thread: every load issued before any is
+  // used, so that the staging costs one round trip to memory
+  constexpr int U = 1024 / kThreads;   // 64 rows x at most 16 blocks
+  uint32_t scode[U];
+  float snest[U];
+  const float soff = (dec && a.W.dq) ? __ldg(a.W.offset) : 0.0f;
+  const int nb32 = static_cast<int>(nbr);
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (threadIdx.x + u * kThreads < kTF * nbr) s_sc[threadIdx.x + u * kThreads] = sc[u];
+  for (int u = 0; u < U; ++u) {
+    const int i = threadIdx.x + u * kThreads, r = i / nb32, kb = i - r * nb32;
+    scode[u] = 0, snest[u] = 0.0f;
+    if (dec && i < kTF * nb32 && f0 + r < N) {
+      const int64_t gi = (f0 + r) * nbr + kb;
+      if (a.W.dq) {
+        scode[u] = __ldg(static_cast<const uint8_t*>(a.W.absmax) + gi);
+        snest[u] = __ldg(a.W.nested + (gi >> 8));
+      } else {
+        snest[u] = __ldg(static_cast<const float*>(a.W.absmax) + gi);
+      }
+    }
+  }
+  // T16(A) rows [rp][K]: rows past r are zero
+  const int q4 = static_cast<int>(K / 4), atotal = rp * q4;
+  const bool avec = (reinterpret_cast<uintptr_t>(item.A) & 15) == 0;
+  constexpr int kAB = 12;   // float4 a thread per batch
+  auto a_load = [&](int i0, float4 (&v)[kAB]) {
+#pragma unroll
+    for (int u = 0; u < kAB; ++u) {
+      const int i = i0 + u * kThreads, j = i / q4, c4 = i - j * q4;
+      v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (i < atotal && j < a.r) {
+        const float* src = item.A + static_cast<int64_t>(j) * K + 4 * c4;
+        v[u] = avec ? __ldg(reinterpret_cast<const float4*>(src))
+                    : make_float4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+      }
+    }
+  };
+  auto a_store = [&](int i0, const float4 (&v)[kAB]) {
+#pragma unroll
+    for (int u = 0; u < kAB; ++u) {
+      const int i = i0 + u * kThreads, j = i / q4, c4 = i - j * q4;
+      if (i < atotal)
+        asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(s_a + static_cast<uint32_t>(j * row16(K) + 8 * c4)),
+                     "r"(pack2<T16>(v[u].x, v[u].y)), "r"(pack2<T16>(v[u].z, v[u].w))
+                     : "memory");
+    }
+  };
+  {
+    float4 v[kAB];
+    a_load(threadIdx.x, v);
+    if (dec) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = threadIdx.x + u * kThreads;
+        if (i < kTF * nb32)
+          s_sc[i] = a.W.dq ? __fadd_rn(__fmul_rn(dyn8[scode[u]], snest[u]), soff) : snest[u];
+      }
+    }
+    a_store(threadIdx.x, v);
+    for (int i0 = threadIdx.x + kAB * kThreads; i0 < atotal; i0 += kAB * kThreads) {
+      a_load(i0, v);
+      a_store(i0, v);
+    }
   }
   cp_async_wait_all();
   __syncthreads();
-  convert_raw<T16>(s_a, row16(K), reinterpret_cast<const float*>(smem + (s_rawa - s_x)), rp, K);
-  if (!dec) {   // A's staging space is free: the decoded weight rows
-    __syncthreads();
-    stage_rows16(s_w, row16(K), static_cast<const T16*>(item.w16), f0, kTF, N, K);
-    cp_async_wait_all();
-  }
-  __syncthreads();
 
-  // warp w: output features 8w .. 8w + 7 of the tile for all 4 token blocks, and T of token
-  // block w & 3 for rank blocks (w >> 2) + 2 qq
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int fw = 8 * warp;
-  const int tb = warp & 3, q0 = warp >> 2;
+  // warp w: output features 8w .. 8w + 7 of the tile for both token blocks, and T of token
+  // block tb = w & 1 for rank block q = w >> 1 (when 8 q < rp)
+  const int tb = warp & 1, q = warp >> 1;
+  const bool has_t = 8 * q < rp;
   const uint32_t R16 = static_cast<uint32_t>(row16(K));
   const uint32_t xrow = s_x + (g * R16 + 16 * c);           // + 16 mb R16 (+ 8 R16), + 64 ks
   const uint32_t wrow_ = dec ? s_w + static_cast<uint32_t>((fw + g) * rowp(K) + 4 * c)
                              : s_w + (fw + g) * R16 + 16 * c;
-  const uint32_t arow = s_a + g * R16 + 16 * c;             // + 8 q R16, + 64 ks
-  float acc[4][4] = {};                  // [token block][fragment]
-  float tac[2][4] = {};                  // T of token block tb: rank blocks q0, q0 + 2
-  const int nb32 = static_cast<int>(nbr);
+  const uint32_t arow = s_a + (8 * q + g) * R16 + 16 * c;   // + 64 ks
+  float acc[2][4] = {};                  // [token block][fragment]
+  float tac[4] = {};                     // T of token block tb, rank block q
   for (int kb = 0; kb < nb32; ++kb) {
     uint32_t L[4], H[4];
     if (dec) build_lut<T16>(s_sc[(fw + g) * nb32 + kb], L, H);
@@ -279,7 +321,7 @@ small_fused_fwd(FwdParams p, DecodeTables tabs) {
       }
       uint4 xt0{}, xt1{};
 #pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
+      for (int mb = 0; mb < 2; ++mb) {
         const uint32_t xa_addr = xrow + static_cast<uint32_t>(16 * mb) * R16 + ks * 64;
         const uint4 xa = lds128(xa_addr);
         const uint4 xb = lds128(xa_addr + 8 * R16);
@@ -287,44 +329,26 @@ small_fused_fwd(FwdParams p, DecodeTables tabs) {
         mma16816<F16>(acc[mb], xa.z, xb.z, xa.w, xb.w, bw[2], bw[3]);
         if (mb == tb) xt0 = xa, xt1 = xb;
       }
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        const int q = q0 + 2 * qq;
-        if (8 * q >= rp) break;
-        const uint4 ta = lds128(arow + static_cast<uint32_t>(8 * q) * R16 + ks * 64);
-        mma16816<F16>(tac[qq], xt0.x, xt1.x, xt0.y, xt1.y, ta.x, ta.y);
-        mma16816<F16>(tac[qq], xt0.z, xt1.z, xt0.w, xt1.w, ta.z, ta.w);
+      if (has_t) {
+        const uint4 ta = lds128(arow + ks * 64);
+        mma16816<F16>(tac, xt0.x, xt1.x, xt0.y, xt1.y, ta.x, ta.y);
+        mma16816<F16>(tac, xt0.z, xt1.z, xt0.w, xt1.w, ta.z, ta.w);
       }
     }
   }
   // T (fp32, written by the first feature tile) and 16-bit s T for the adapter term
-  const int64_t tr0 = t0 + 16 * tb + g;
-#pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {
-    const int q = q0 + 2 * qq;
-    if (8 * q >= rp) break;
+  if (has_t) {
+    const int64_t tr0 = t0 + 16 * tb + g;
     const int j0 = 8 * q + 2 * c;
     if (f0 == 0) {
-      if (tr0 < M && j0 < a.r) item.T[tr0 * a.r + j0] = tac[qq][0];
-      if (tr0 < M && j0 + 1 < a.r) item.T[tr0 * a.r + j0 + 1] = tac[qq][1];
-      if (tr0 + 8 < M && j0 < a.r) item.T[(tr0 + 8) * a.r + j0] = tac[qq][2];
-      if (tr0 + 8 < M && j0 + 1 < a.r) item.T[(tr0 + 8) * a.r + j0 + 1] = tac[qq][3];
+      if (tr0 < M && j0 < a.r) item.T[tr0 * a.r + j0] = tac[0];
+      if (tr0 < M && j0 + 1 < a.r) item.T[tr0 * a.r + j0 + 1] = tac[1];
+      if (tr0 + 8 < M && j0 < a.r) item.T[(tr0 + 8) * a.r + j0] = tac[2];
+      if (tr0 + 8 < M && j0 + 1 < a.r) item.T[(tr0 + 8) * a.r + j0 + 1] = tac[3];
     }
     const uint32_t row = s_t + static_cast<uint32_t>((16 * tb + g) * rowr(rp) + j0 * 2);
-    st_shared32(row, pack2<T16>(__fmul_rn(a.s, tac[qq][0]), __fmul_rn(a.s, tac[qq][1])));
-    st_shared32(row + 8 * rowr(rp), pack2<T16>(__fmul_rn(a.s, tac[qq][2]), __fmul_rn(a.s, tac[qq][3])));
-  }
-  // B's fragments for the adapter term straight from global memory (8 values a lane)
-  float bv[2][4];
-  {
-    const int64_t f = f0 + fw + g;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int j0 = 16 * kk + 2 * c;
-      const int js[4] = {j0, j0 + 1, j0 + 8, j0 + 9};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) bv[kk][e] = (f < N && js[e] < a.r) ? __ldg(item.B + f * a.r + js[e]) : 0.0f;
-    }
+    st_shared32(row, pack2<T16>(__fmul_rn(a.s, tac[0]), __fmul_rn(a.s, tac[1])));
+    st_shared32(row + 8 * rowr(rp), pack2<T16>(__fmul_rn(a.s, tac[2]), __fmul_rn(a.s, tac[3])));
   }
   __syncthreads();
   // + (s T) B^T over the rank
@@ -334,17 +358,17 @@ small_fused_fwd(FwdParams p, DecodeTables tabs) {
     if (16 * kk >= rp) break;
     const uint32_t b0 = pack2<T16>(bv[kk][0], bv[kk][1]), b1 = pack2<T16>(bv[kk][2], bv[kk][3]);
 #pragma unroll
-    for (int mb = 0; mb < 4; ++mb) {
+    for (int mb = 0; mb < 2; ++mb) {
       const uint32_t arow2 = s_t + (16 * mb + g) * RR + (16 * kk + 2 * c) * 2;
       const uint32_t a0 = ld_shared32(arow2), a1 = ld_shared32(arow2 + 8 * RR);
       const uint32_t a2 = ld_shared32(arow2 + 16), a3 = ld_shared32(arow2 + 8 * RR + 16);
       mma16816<F16>(acc[mb], a0, a1, a2, a3, b0, b1);
     }
   }
-  // y through shared memory (the x rows are no longer read): [64 tokens][64 features] 16-bit
+  // y through shared memory (the x rows are no longer read): [32 tokens][64 features] 16-bit
   constexpr int kYRow = 2 * kTF + 16;
 #pragma unroll
-  for (int mb = 0; mb < 4; ++mb) {
+  for (int mb = 0; mb < 2; ++mb) {
     const uint32_t yrow = s_x + static_cast<uint32_t>((16 * mb + g) * kYRow + (fw + 2 * c) * 2);
     st_shared32(yrow, pack2<T16>(acc[mb][0], acc[mb][1]));
     st_shared32(yrow + 8 * kYRow, pack2<T16>(acc[mb][2], acc[mb][3]));
@@ -362,14 +386,16 @@ small_fused_fwd(FwdParams p, DecodeTables tabs) {
 //
 // Kernel small_fused_dx: one CTA per (projection, 32-token tile, 64-input-feature tile).
 //   dX tile = dY[32, N] W[N, 64] + s G A[:, 64] with G = dY B over the whole N (recomputed by
-//   every input-feature tile of the token tile); W's 64 columns are decoded into shared memory
-//   once per CTA (or copied, when the caller gives the decoded weight).
+//   every input-feature tile of the token tile).  N is taken in chunks of 128 rows: a chunk
+//   of W's 64 columns is decoded into shared memory (or copied, when the caller gives the
+//   decoded weight) together with its rows of T16(B), while the next chunk's packed codes and
+//   B rows are in flight, and both products run over the chunk.
 //   The token tile's shares of the adapter gradients go to fp32 workspace slices, unscaled:
 //   dA part [r][K] (its 64 columns) = T16(G)^T x over the 32 tokens, and dB part [N][r] (an
 //   equal share of W's rows per input-feature tile) = dY^T T16(T).
 // The last CTA of each input-feature tile (a ticket counter per tile) then sums that tile's
 //   share of dA and dB over the token tiles' parts, in tile order, times s.
-// Warps: warp w takes token block w & 1 (16 tokens) and input features 32 (w >> 1) .. + 31.
+// Warps: warp w takes token block w & 1 (16 tokens) and input features 16 (w >> 1) .. + 15.
 
 constexpr int kBT = 32;           // tokens per backward tile
 constexpr int kRow64 = 2 * kTF + 16;   // a row of 64 16-bit values, padded
@@ -398,16 +424,18 @@ struct BwdParams {
 };
 
 // The contraction over N runs in steps of 16: the weight and B tiles hold N16 = N rounded up to
-// 16 rows, and dY's columns N .. N16 - 1, all zero past N.
+// 16 rows, and dY's columns N .. N16 - 1, all zero past N.  W's 64 columns and B are taken in
+// chunks of kNC rows of N, so that two CTAs fit an SM at the SmolLM2 shapes.
 __host__ __device__ inline int64_t n16(int64_t N) { return (N + 15) / 16 * 16; }
+constexpr int kNC = 128;
 
-// Shared memory of the backward: dY rows, W's 64 columns (B's fp32 staging first), T16(B),
-// T16(A) columns, x columns, G (fp32), T16(T), the fp32 staging of A's columns and T, and with
-// the stored codes the packed columns.
+// Shared memory of the backward: dY rows, a chunk of W's 64 columns (16-bit), a chunk of T16(B),
+// T16(A) columns, x columns, G (fp32), T16(T), two chunks of B in flight (fp32), and with the
+// stored codes all of N's packed columns and block scales.
 __host__ __device__ inline int64_t bwd_smem_bytes(int64_t N, int rp, bool w16) {
   const int64_t N16 = n16(N);
-  return kBT * row16(N16) + N16 * kRow64 + N16 * rowr(rp) + rp * kRow64 + kBT * kRow64 + kBT * (4 * rp + 16) +
-         kBT * rowr(rp) + rp * kTF * 4 + kBT * rp * 4 + (w16 ? 0 : N16 * 32);
+  return kBT * row16(N16) + kNC * kRow64 + kNC * rowr(rp) + rp * kRow64 + kBT * kRow64 + kBT * (4 * rp + 16) +
+         kBT * rowr(rp) + 2 * kNC * rp * 4 + (w16 ? 0 : N16 * 36);
 }
 
 // ldmatrix lane addresses.  A operand (m16 x k16) from [m][k] rows: row (i & 7) + 8 ((i >> 3) & 1),
@@ -415,7 +443,7 @@ __host__ __device__ inline int64_t bwd_smem_bytes(int64_t N, int rp, bool w16) {
 // 8 ((i >> 3) & 1).  B operand (k16 x two n8 blocks) from [k][n] rows (.trans): row (i & 7) +
 // 8 ((i >> 3) & 1), column 8 (i >> 4).
 template <typename T16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 small_fused_dx(BwdParams p, DecodeTables tabs) {
   constexpr bool F16 = std::is_same<T16, __half>::value;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -440,23 +468,44 @@ small_fused_dx(BwdParams p, DecodeTables tabs) {
   const int gstride = 4 * rp + 16;         // fp32 G rows
   const int64_t N16 = n16(N);
   const int64_t dys = row16(N16);          // dY row stride
+  const int nch = static_cast<int>((N16 + kNC - 1) / kNC);
 
   const uint32_t s_dy = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  const uint32_t s_w = s_dy + kBT * dys;                  // W[:, k0 .. k0 + 63], [N16][64]
-  const uint32_t s_b = s_w + N16 * kRow64;                // B, [N16][rp]
-  const uint32_t s_a = s_b + N16 * rowr(rp);              // A[:, k0 .. +63], [rp][64]
+  const uint32_t s_w = s_dy + kBT * dys;                  // W[chunk rows, k0 .. k0 + 63], [kNC][64]
+  const uint32_t s_b = s_w + kNC * kRow64;                // B chunk, [kNC][rp]
+  const uint32_t s_a = s_b + kNC * rowr(rp);              // A[:, k0 .. +63], [rp][64]
   const uint32_t s_x = s_a + rp * kRow64;                 // x tile, [32][64]
   const uint32_t s_g = s_x + kBT * kRow64;                // G (fp32), [32][rp]
   const uint32_t s_t = s_g + kBT * gstride;               // T (16-bit), [32][rp]
-  const uint32_t s_rawa = s_t + kBT * rowr(rp);           // A's columns, fp32 [rp][64]
-  const uint32_t s_rawt = s_rawa + rp * kTF * 4;          // T, fp32 [32][rp]
-  const uint32_t s_code = s_rawt + kBT * rp * 4;          // packed columns [N16][32 bytes]
+  const uint32_t s_rawb = s_t + kBT * rowr(rp);           // two B chunks in flight, fp32 [2][kNC][rp]
+  const uint32_t s_code = s_rawb + 2 * kNC * rp * 4;      // stored codes: packed columns [N16][32 bytes]
+  float* s_sc = reinterpret_cast<float*>(smem + (s_code + N16 * 32 - s_dy));   // and block scales [N16]
   const bool dec = item.w16 == nullptr;
   const float* g_f = reinterpret_cast<const float*>(smem + (s_g - s_dy));
   auto raw = [&](uint32_t a) { return reinterpret_cast<const float*>(smem + (a - s_dy)); };
+  const int64_t nbr = K / 64;
+  auto rows_of = [&](int c) { return static_cast<int>(std::min<int64_t>(kNC, N16 - static_cast<int64_t>(c) * kNC)); };
+  // B's rows of chunk c (fp32) into staging buffer c & 1, as one group of copies
+  auto issue_b = [&](int c) {
+    stage_f32_raw(s_rawb + static_cast<uint32_t>((c & 1) * kNC * rp * 4), item.B, static_cast<int64_t>(c) * kNC,
+                  rows_of(c), N, r, rp, r == rp);
+    cp_async_commit();
+  };
+  // with the decoded weight: chunk c's 16-bit columns straight into the chunk buffer
+  auto issue_w16 = [&](int c) {
+    const T16* w = static_cast<const T16*>(item.w16);
+    const int64_t nb0 = static_cast<int64_t>(c) * kNC;
+    for (int i = threadIdx.x; i < rows_of(c) * 8; i += kThreads) {
+      const int rr = i >> 3, ch = i & 7;
+      const uint32_t d = s_w + static_cast<uint32_t>(rr * kRow64 + ch * 16);
+      if (nb0 + rr < N) cp_async16(d, w + (nb0 + rr) * K + k0 + 8 * ch);
+      else asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
+    }
+    cp_async_commit();
+  };
 
-  // first round of copies: dY rows, x columns, B (fp32, in W's space), A's columns, T, and the
-  // packed columns with the block scales of the weight
+  // the copies: dY rows, x columns, all packed columns (or chunk 0 of the decoded weight), then
+  // B's chunks 0 and 1; the block scales' inputs, A's columns and T straight into registers
   stage_rows16(s_dy, dys, static_cast<const T16*>(item.dy), t0, kBT, M, N);
   if (N16 > N)   // dY columns N .. N16 - 1 (8 of them) are zero
     for (int i = threadIdx.x; i < kBT; i += kThreads)
@@ -472,11 +521,6 @@ small_fused_dx(BwdParams p, DecodeTables tabs) {
       else asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
     }
   }
-  stage_f32_raw(s_w, item.B, 0, static_cast<int>(N16), N, r, rp, r == rp);
-  stage_f32_raw(s_rawa, item.A + k0, 0, rp, r, K, kTF, true);
-  stage_f32_raw(s_rawt, item.T, t0, kBT, M, r, rp, r == rp);
-  constexpr int U = 1024 / kThreads;       // rows per thread (N16 <= 1024)
-  float sc[U];
   if (dec) {
     for (int i = threadIdx.x; i < static_cast<int>(N16) * 2; i += kThreads) {
       const int rr = i >> 1, h = i & 1;
@@ -484,50 +528,60 @@ small_fused_dx(BwdParams p, DecodeTables tabs) {
       if (rr < N) cp_async16(d, a.W.packed + rr * (K / 2) + k0 / 2 + h * 16);
       else asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
     }
-    int64_t gi[U];
-    const int64_t nbr = K / 64;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t rr = threadIdx.x + u * kThreads;
-      gi[u] = rr < N ? rr * nbr + kt : -1;
-    }
-    block_scales<U>(a.W, gi, dyn8, sc);
+    cp_async_commit();
+  } else {
+    issue_w16(0);
   }
-  cp_async_wait_all();
-  __syncthreads();
-  convert_raw<T16>(s_b, rowr(rp), raw(s_w), static_cast<int>(N16), rp);
-  convert_raw<T16>(s_a, kRow64, raw(s_rawa), rp, kTF);
-  convert_raw<T16>(s_t, rowr(rp), raw(s_rawt), kBT, rp);
-  __syncthreads();
-  // second round: W's columns k0 .. k0 + 63 into the space B's staging left
-  if (dec) {   // row n's 64 columns are exactly one block
+  issue_b(0);
+  if (nch > 1) issue_b(1);
+  constexpr int U = 1024 / kThreads;       // rows per thread (N16 <= 1024)
+  uint32_t scode[U];
+  float snest[U];
+  const float soff = (dec && a.W.dq) ? __ldg(a.W.offset) : 0.0f;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t rr = threadIdx.x + u * kThreads;
-      if (rr >= N16) break;
-      uint32_t L[4], H[4];
-      build_lut<T16>(sc[u], L, H);
-      const uint4 c0 = lds128(s_code + static_cast<uint32_t>(rr * 32)), c1 = lds128(s_code + static_cast<uint32_t>(rr * 32 + 16));
-      const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t o[4];
-        decode8(cw[q], L, H, o);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_w + static_cast<uint32_t>(rr * kRow64 + q * 16)),
-                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
-                     : "memory");
+  for (int u = 0; u < U; ++u) {
+    const int64_t rr = threadIdx.x + u * kThreads;
+    scode[u] = 0, snest[u] = 0.0f;
+    if (dec && rr < N) {
+      if (a.W.dq) {
+        scode[u] = __ldg(static_cast<const uint8_t*>(a.W.absmax) + rr * nbr + kt);
+        snest[u] = __ldg(a.W.nested + ((rr * nbr + kt) >> 8));
+      } else {
+        snest[u] = __ldg(static_cast<const float*>(a.W.absmax) + rr * nbr + kt);
       }
     }
-  } else {
-    const T16* w = static_cast<const T16*>(item.w16);
-    for (int i = threadIdx.x; i < static_cast<int>(N16) * 8; i += kThreads) {
-      const int rr = i >> 3, ch = i & 7;
-      const uint32_t d = s_w + static_cast<uint32_t>(rr * kRow64 + ch * 16);
-      if (rr < N) cp_async16(d, w + rr * K + k0 + 8 * ch);
-      else asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
-    }
-    cp_async_wait_all();
   }
+  // A's columns [rp][64] (8 a thread at most) and T [32][rp] (4 a thread at most), zero past r / M
+  float av[8], tv[4];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int ia = threadIdx.x + u * kThreads, ja = ia / kTF, ca = ia - ja * kTF;
+    av[u] = (ia < rp * kTF && ja < r) ? __ldg(item.A + ja * K + k0 + ca) : 0.0f;
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int it = threadIdx.x + u * kThreads, jt = it / rp, ct = it - jt * rp;
+    tv[u] = (it < kBT * rp && t0 + jt < M && ct < r) ? __ldg(item.T + (t0 + jt) * r + ct) : 0.0f;
+  }
+  if (dec)
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int rr = threadIdx.x + u * kThreads;
+      if (rr < N16) s_sc[rr] = rr >= N ? 0.0f : a.W.dq ? __fadd_rn(__fmul_rn(dyn8[scode[u]], snest[u]), soff) : snest[u];
+    }
+  // T16(A) and T16(T), one 16-bit value a store
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int ia = threadIdx.x + u * kThreads, ja = ia / kTF, ca = ia - ja * kTF;
+    if (ia < rp * kTF) st_shared16<T16>(s_a + static_cast<uint32_t>(ja * kRow64 + 2 * ca), av[u]);
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int it = threadIdx.x + u * kThreads, jt = it / rp, ct = it - jt * rp;
+    if (it < kBT * rp) st_shared16<T16>(s_t + static_cast<uint32_t>(jt * rowr(rp) + 2 * ct), tv[u]);
+  }
+  if (nch > 1) cp_async_wait_group1();   // all but B's chunk 1
+  else cp_async_wait_all();
   __syncthreads();
 
   // warp w: token block mb = w & 1 and input features 16 nq .. 16 nq + 15 (nq = w >> 1) of the
@@ -539,23 +593,63 @@ small_fused_dx(BwdParams p, DecodeTables tabs) {
   const int ar = (lane & 7) + 8 * ((lane >> 3) & 1), ac = 8 * (lane >> 4);   // [m][k] A, and [k][n] B
   const int tr = 8 * (lane >> 4) + (lane & 7), tc = 8 * ((lane >> 3) & 1);   // [k][m] A (.trans)
   const uint32_t DYS = static_cast<uint32_t>(dys), RR = static_cast<uint32_t>(rowr(rp));
-  const uint32_t dy_a = s_dy + (16 * mb + ar) * DYS + ac * 2;                 // + 2 n0
-  const uint32_t w_b = s_w + ar * kRow64 + (16 * nq + ac) * 2;                // + n0 kRow64
+  const uint32_t dy_a = s_dy + (16 * mb + ar) * DYS + ac * 2;                 // + 2 n
+  const uint32_t w_b = s_w + ar * kRow64 + (16 * nq + ac) * 2;                // + n0 kRow64 (chunk row)
   const bool has_g = 8 * nq < rp;
-  const uint32_t b_b = s_b + ar * RR + (8 * nq + (ac & 8)) * 2;             // + n0 RR
+  const uint32_t b_b = s_b + ar * RR + (8 * nq + (ac & 8)) * 2;             // + n0 RR (chunk row)
   float acc[2][4] = {};                    // dX: [feature block of 8][fragment]
   float gac[4] = {};                       // G: rank block nq of the token block
-  const int n16s = static_cast<int>(N16 / 16);
-  for (int st = 0; st < n16s; ++st) {
-    const uint32_t n0 = static_cast<uint32_t>(16 * st);
-    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-    ldsm4(dy_a + 2 * n0, a0, a1, a2, a3);
-    ldsm4t(w_b + n0 * kRow64, b0, b1, b2, b3);
-    mma16816<F16>(acc[0], a0, a1, a2, a3, b0, b1);
-    mma16816<F16>(acc[1], a0, a1, a2, a3, b2, b3);
-    if (has_g) {                           // the x4's second column pair is not used
-      ldsm4t(b_b + n0 * RR, b0, b1, b2, b3);
-      mma16816<F16>(gac, a0, a1, a2, a3, b0, b1);
+  for (int ch = 0; ch < nch; ++ch) {
+    const int64_t nb0 = static_cast<int64_t>(ch) * kNC;
+    const int rows = rows_of(ch);
+    // chunk ch into the chunk buffers: T16(B) from its staging buffer, and W's columns decoded
+    // from the packed columns (two threads a row, the row's 64 columns being exactly one block)
+    convert_raw<T16>(s_b, rowr(rp), raw(s_rawb + static_cast<uint32_t>((ch & 1) * kNC * rp * 4)), rows, rp);
+    if (dec) {
+      const int rr = threadIdx.x >> 1, h = threadIdx.x & 1;
+      if (rr < rows) {
+        const int64_t n = nb0 + rr;
+        const uint32_t d = s_w + static_cast<uint32_t>(rr * kRow64 + h * 64);
+        uint32_t L[4], H[4];
+        build_lut<T16>(s_sc[n], L, H);   // scale 0 past N: those rows decode to zeros
+        const uint4 cw = lds128(s_code + static_cast<uint32_t>(n * 32 + h * 16));
+        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[4];
+          decode8(cws[q], L, H, o);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d + q * 16), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                       "r"(o[3])
+                       : "memory");
+        }
+      }
+    }
+    __syncthreads();   // the chunk is in place; its B staging buffer is free
+    if (ch + 2 < nch) issue_b(ch + 2);   // lands while this chunk and the next are contracted
+    const int n16s = rows / 16;
+    for (int st = 0; st < n16s; ++st) {
+      const uint32_t n0 = static_cast<uint32_t>(16 * st);
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      ldsm4(dy_a + 2 * (static_cast<uint32_t>(nb0) + n0), a0, a1, a2, a3);
+      ldsm4t(w_b + n0 * kRow64, b0, b1, b2, b3);
+      mma16816<F16>(acc[0], a0, a1, a2, a3, b0, b1);
+      mma16816<F16>(acc[1], a0, a1, a2, a3, b2, b3);
+      if (has_g) {                           // the x4's second column pair is not used
+        ldsm4t(b_b + n0 * RR, b0, b1, b2, b3);
+        mma16816<F16>(gac, a0, a1, a2, a3, b0, b1);
+      }
+    }
+    if (ch + 1 < nch) {
+      __syncthreads();   // every warp is done with the chunk buffers
+      if (!dec) {
+        issue_w16(ch + 1);
+        cp_async_wait_all();
+      } else if (ch + 2 < nch) {
+        cp_async_wait_group1();   // B's chunk ch + 1 has landed; chunk ch + 2 may be in flight
+      } else {
+        cp_async_wait_all();
+      }
+      __syncthreads();
     }
   }
   // G, fp32, to shared memory: every warp of a token block needs all of its ranks

@@ -333,7 +333,7 @@ int64_t nf4_kernel_launch_count(void);
  * the number of launches, and with reset != 0 clears that kind.  No device memory
  * is allocated; events are created once and reused. */
 typedef enum {
-  NF4_TIME_QUANTIZE = 0,    /* the kernels of one nf4_quantize call (two; three above 2^26 elements) */
+  NF4_TIME_QUANTIZE = 0,    /* the kernels of one nf4_quantize call (two with double quantization) */
   NF4_TIME_DEQUANTIZE = 1,  /* the decode kernel */
   NF4_TIME_FWD_GEMM = 2,    /* base contraction of the forward (y) */
   NF4_TIME_DX_GEMM = 3,     /* base contraction of the input gradient (dX) */

@@ -114,12 +114,18 @@ def test_smollm2_qv_shapes(lib):
             _run_case(c["M"], N, K, c["r"], c["alpha"], "bf16", seed=N)
 
 
-@pytest.mark.parametrize("name", ["k_proj", "gate_proj", "down_proj"])
-def test_llama8b_layer_sampled_rows(lib, name):
+@pytest.mark.parametrize("name,M", [("k_proj", 4096), ("gate_proj", 4096), ("down_proj", 4096),
+                                    ("gate_proj", 4881), ("down_proj", 4881)])
+def test_llama8b_layer_sampled_rows(lib, name, M):
+    """The Llama-3-8B-shaped projections at 4096 tokens, and gate and down at 4881 tokens.
+    Down's forward and gate's dX have both operands larger than half of L2, so their GEMM
+    takes the tile pairs in bands of 8 token tiles; 4881 tokens make 20 token tiles, the last
+    band 4 tiles and ragged.  Sampled token rows, always with those at band and tile edges."""
     c = wl.W3
     N, K = {n: (a, b) for n, a, b in c["shapes"]}[name]
-    rows = np.sort(np.random.default_rng(5).choice(c["M"], 64, replace=False))
-    _run_case(c["M"], N, K, c["r"], c["alpha"], "bf16", seed=K, dist="t", rows=rows)
+    edges = [r for r in (0, 255, 256, 2047, 2048, 4095, 4096, M - 1) if r < M]
+    rows = np.unique(np.concatenate([np.random.default_rng(5).choice(M, 64, replace=False), edges]))
+    _run_case(M, N, K, c["r"], c["alpha"], "bf16", seed=K, dist="t", rows=rows)
 
 
 @pytest.mark.parametrize("N,K", [(1344, 1344), (1344, 320)])

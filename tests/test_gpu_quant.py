@@ -130,10 +130,11 @@ def test_quantize_16_byte_aligned_view(lib, dtype):
 
 
 @pytest.mark.parametrize("n", [2 ** 26, 2 ** 26 + 16384])
-def test_quantize_offset_inside_and_outside_the_nested_pass(lib, n):
-    """At 4096 groups of 256 blocks the offset is computed inside the nested pass; one group
-    more takes the separate one-CTA tree first.  Both give the oracle's offset, nested
-    maxima and codes (sampled groups), bf16 input."""
+def test_quantize_offset_at_a_power_of_two_group_count(lib, n):
+    """4096 groups of 256 blocks (the offset tree is exactly the 4096 group sums) and one
+    group more (the tree pads to 8192 with zeros): the offset, which the block pass's last
+    CTA computes, and the nested maxima and codes (sampled groups) are the oracle's; bf16
+    input."""
     x = wl.device_normal((n,), 0.02, wl.seed_for(5, n % 1000), DEV, torch.bfloat16)
     q = binding.nf4_quantize(x)
     x_host = _host_values(x)
@@ -204,6 +205,60 @@ def test_quantize_special_blocks(lib):
         xd = torch.from_numpy(x).to(DEV)
         q = binding.nf4_quantize(xd, double_quant=dq)
         _assert_same_quant(q, onf4.quantize(x, double_quant=dq))
+
+
+def _group_of_maxima(maxima: np.ndarray, seed: int) -> np.ndarray:
+    """One nested group (256 blocks of 64) whose block b has the largest magnitude maxima[b]:
+    that value at a seeded position of the block, with a seeded sign, the other entries of
+    the block smaller in magnitude."""
+    rng = np.random.default_rng(seed)
+    x = (rng.uniform(-1.0, 1.0, (256, 64)) * maxima[:, None].astype(np.float64) * 0.999).astype(np.float32)
+    pos = rng.integers(0, 64, 256)
+    sign = np.where(rng.integers(0, 2, 256) == 1, np.float32(-1.0), np.float32(1.0))
+    x[np.arange(256), pos] = maxima * sign
+    return x.reshape(-1)
+
+
+def _maxima_with_exponents(lo: int, hi: int, seed: int) -> np.ndarray:
+    """256 fp32 values with biased exponents spread over [lo, hi] (both ends present) and
+    seeded 23-bit fractions."""
+    rng = np.random.default_rng(seed)
+    e = rng.integers(lo, hi + 1, 256).astype(np.uint32)
+    e[0], e[1] = lo, hi
+    frac = rng.integers(0, 1 << 23, 256).astype(np.uint32)
+    return ((e << 23) | frac).view(np.float32)
+
+
+def test_quantize_group_sum_regimes(lib):
+    """The block pass forms a group's sum of maxima exactly in integers when the maxima's
+    exponents span at most 21 binades, else by the float64 tree; both must give the oracle's
+    float64 tree result.  One-group tensors (offset = that sum / 256, rounded to fp32) and a
+    tensor of all of them: exponent spans 0, 21 (the last exact case) and 22, 30 (tree), all
+    subnormal maxima, subnormal next to the smallest normals, zero and non-zero blocks mixed,
+    and the near-equal maxima of real weights."""
+    groups = {
+        "span0": _maxima_with_exponents(120, 120, 1),
+        "span21": _maxima_with_exponents(100, 121, 2),
+        "span22": _maxima_with_exponents(100, 122, 3),
+        "span30": _maxima_with_exponents(97, 127, 4),
+        "subnormal": (np.random.default_rng(5).integers(1, 1 << 23, 256).astype(np.uint32)).view(np.float32),
+        "subnormal_and_min_normal": _maxima_with_exponents(0, 1, 6),
+        "zeros_mixed": np.where(np.arange(256) % 3 == 0, np.float32(0.0), _maxima_with_exponents(110, 125, 7)),
+        "weights": np.abs(wl.normal(256, 0.05, 5, 77)) + np.float32(0.05),
+    }
+    parts = []
+    for i, (name, m) in enumerate(groups.items()):
+        x = _group_of_maxima(m.astype(np.float32), 100 + i)
+        parts.append(x)
+        for dtype in (torch.float32,):
+            xd = _to_device(x, dtype)
+            q = binding.nf4_quantize(xd, double_quant=True)
+            _assert_same_quant(q, onf4.quantize(_host_values(xd), double_quant=True))
+    x = np.concatenate(parts)
+    xd = _to_device(x, torch.float32)
+    q = binding.nf4_quantize(xd, double_quant=True)
+    _assert_same_quant(q, onf4.quantize(x, double_quant=True))
+    assert binding.device_status() == binding.NF4_OK
 
 
 def test_quantize_is_deterministic(lib):
