@@ -290,18 +290,41 @@ __device__ __forceinline__ float offset_tree(double* gs, int64_t ng, int64_t p2,
   }
   // entry i of the first w = min(n, 1024) entries is the tree over column j = 0 .. m-1 of
   // gs[i + w j] (m = n / w), whose pairs are (j, j + m/2), then (j, j + m/4), ...
+  // (read from L2, where the other CTAs' writes are; with m <= 4 two entries a thread at a
+  // time, so that 8 loads are in flight)
   const int64_t w = n < 1024 ? n : 1024, m = n / w;
+  if (m <= 4) {
 #pragma unroll 1
-  for (int64_t i = threadIdx.x; i < w; i += kQuantThreads) {
-    double c[8];
+    for (int64_t i0 = threadIdx.x; i0 < w; i0 += 2 * kQuantThreads) {
+      double c[2][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = (j < m && i + w * j < valid) ? gs[i + w * j] : 0.0;
+      for (int e = 0; e < 2; ++e) {
+        const int64_t i = i0 + e * kQuantThreads;
 #pragma unroll
-    for (int h = 4; h >= 1; h >>= 1)
-      if (h < m)
+        for (int j = 0; j < 4; ++j) c[e][j] = (i < w && j < m && i + w * j < valid) ? __ldcg(gs + i + w * j) : 0.0;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+#pragma unroll
+        for (int h = 2; h >= 1; h >>= 1)
+          if (h < m)
+#pragma unroll
+            for (int j = 0; j < h; ++j) c[e][j] = c[e][j] + c[e][j + h];
+        if (i0 + e * kQuantThreads < w) sm[i0 + e * kQuantThreads] = c[e][0];
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int64_t i = threadIdx.x; i < w; i += kQuantThreads) {
+      double c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = (i + w * j < valid) ? __ldcg(gs + i + w * j) : 0.0;
+#pragma unroll
+      for (int h = 4; h >= 1; h >>= 1)
 #pragma unroll
         for (int j = 0; j < h; ++j) c[j] = c[j] + c[j + h];
-    sm[i] = c[0];
+      sm[i] = c[0];
+    }
   }
   __syncthreads();
   for (n = w; n > 32; n /= 2) {
@@ -826,6 +849,12 @@ cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int
     e = v8 ? encode_ctas_per_sm(nf4_encode_blocks<__nv_bfloat16, true>, 2, &resident)
            : encode_ctas_per_sm(nf4_encode_blocks<__nv_bfloat16, false>, 3, &resident);
   if (e != cudaSuccess) return e;
+  // the tensors' groups go largest tensor first: the last groups handed out belong to the
+  // smallest tensor, whose offset tree (the tail after the last group) is the shortest
+  QuantJob sorted[kEncodeBatch];
+  for (int i = 0; i < n; ++i) sorted[i] = jobs[i];
+  std::stable_sort(sorted, sorted + n, [](const QuantJob& a, const QuantJob& b) { return a.numel > b.numel; });
+  jobs = sorted;
   EncodeBatch eb{};
   NestedBatch nbt{};
   eb.n = n;
