@@ -235,7 +235,17 @@ __global__ void finish_partials(const FinishJobs jobs) {
   const int j = static_cast<int>(i % width);
   float v = 0.0f;
   if (j < f.r) {
-    for (int sp = 0; sp < f.nsplit; ++sp) v += f.partial[(static_cast<int64_t>(sp) * f.rows + row) * f.r + j];
+    // the slices in order, 8 loads in flight before their adds
+    const float* src = f.partial + row * f.r + j;
+    const int64_t stride = f.rows * f.r;
+    for (int sp0 = 0; sp0 < f.nsplit; sp0 += 8) {
+      float t[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) t[u] = sp0 + u < f.nsplit ? src[(sp0 + u) * stride] : 0.0f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (sp0 + u < f.nsplit) v += t[u];
+    }
     if (f.f32) {
       if (f.f32_t) f.f32[static_cast<int64_t>(j) * f.rows + row] = f.scale * v;
       else f.f32[row * f.r + j] = f.scale * v;
