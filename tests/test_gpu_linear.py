@@ -176,16 +176,19 @@ def test_linear_is_deterministic(lib):
         assert torch.equal(a, b)
 
 
-def test_split_tiles_are_deterministic(lib):
-    """4096 x 1344 x 1344: 96 tile pairs on the GEMM's clusters leave a partial last round
-    whose tiles are split along the contraction.  Whichever CTA finishes a split tile (the
-    last part straight from its accumulator, or the last ticket from the parts' sums), the
-    sum runs in the same order, so repeated calls give identical bits."""
-    q, _ = _quantized_weight(1344, 1344, 11)
-    x = torch.randn(4096, 1344, device=DEV, dtype=torch.bfloat16)
-    dy = torch.randn(4096, 1344, device=DEV, dtype=torch.bfloat16)
-    A = torch.randn(16, 1344, device=DEV) / 16
-    B = torch.randn(1344, 16, device=DEV) / 100
+@pytest.mark.parametrize("N,K", [(1344, 1344), (1024, 4096), (4096, 4096)])
+def test_split_tiles_are_deterministic(lib, N, K):
+    """4096 tokens: the GEMM's tile pairs leave a partial last round (1344 x 1344: 96 pairs,
+    its 20 tail tiles cut into 3 equal parts each; 4096 x 4096: 256 pairs, 28 tail tiles in
+    halves; 1024 x 4096: the forward's 64 pairs, fewer than the clusters, whole, and the
+    dX's 256 in halves).  Whichever CTA finishes a split tile (the last part straight from
+    its accumulator, or the last ticket from the parts' sums), the sum runs in the same
+    order, so repeated calls give identical bits."""
+    q, _ = _quantized_weight(N, K, 11)
+    x = torch.randn(4096, K, device=DEV, dtype=torch.bfloat16)
+    dy = torch.randn(4096, N, device=DEV, dtype=torch.bfloat16)
+    A = torch.randn(16, K, device=DEV) / 16
+    B = torch.randn(N, 16, device=DEV) / 100
     outs = []
     for _ in range(3):
         y, T = binding.qlora_linear_fwd(x, q, A, B, 16.0)
