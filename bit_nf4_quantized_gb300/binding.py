@@ -31,7 +31,7 @@ ENTRY_POINTS = (
     "qlora_fwd_batch_workspace_bytes", "qlora_linear_fwd_batch",
     "qlora_fwd_w16_workspace_bytes", "qlora_bwd_w16_workspace_bytes", "qlora_linear_fwd_w16",
     "qlora_linear_bwd_w16", "nf4_quantize_batch_workspace_bytes", "nf4_quantize_batch",
-    "qlora_bwd_batch_workspace_bytes", "qlora_linear_bwd_batch",
+    "qlora_bwd_batch_workspace_bytes", "qlora_linear_bwd_batch", "nf4_dequantize_batch",
 )
 
 
@@ -68,6 +68,10 @@ class _QuantItem(ctypes.Structure):
                 ("out", ctypes.POINTER(_Nf4Tensor))]
 
 
+class _DequantItem(ctypes.Structure):
+    _fields_ = [("w", ctypes.POINTER(_Nf4Tensor)), ("y", ctypes.c_void_p)]
+
+
 _LIB = None
 
 
@@ -99,6 +103,7 @@ def load() -> ctypes.CDLL:
         "nf4_quantize_batch_workspace_bytes": (sz, [i32, ctypes.POINTER(_QuantItem)]),
         "nf4_quantize_batch": (i32, [i32, ctypes.POINTER(_QuantItem), vp, sz, vp]),
         "nf4_quantize_noalloc": (i32, [vp, i32, i64, tp, vp]),
+        "nf4_dequantize_batch": (i32, [i32, ctypes.POINTER(_DequantItem), i32, vp]),
         "nf4_embedding_rows": (i32, [tp, i64, i64, vp, i64, vp, i32, vp]),
         "nf4_merge_lora": (i32, [i64, i64, i32, f32, i32, tp, vp, vp, vp, i32, vp]),
         "qlora_fwd_workspace_bytes": (sz, [i64, i64, i64, i32, i32]),
@@ -281,6 +286,24 @@ def nf4_dequantize(q: Nf4Tensor, dtype=torch.float32, out: torch.Tensor = None, 
     _check(lib.nf4_dequantize(ctypes.byref(cs), _ptr(y), _dtype_code(y.dtype), _stream(stream)),
            "nf4_dequantize")
     return y
+
+
+def nf4_dequantize_batch(pairs, stream=None):
+    """Decode several tensors in one call: ``pairs`` is a list of (Nf4Tensor, output tensor),
+    all outputs of one dtype; each output gets exactly what ``nf4_dequantize`` writes."""
+    lib = load()
+    if not pairs:
+        return
+    dtypes = {y.dtype for _, y in pairs}
+    if len(dtypes) != 1:
+        raise ValueError("nf4_dequantize_batch: outputs of one dtype")
+    structs = [q.c_struct() for q, _ in pairs]
+    items = (_DequantItem * len(pairs))()
+    for i, ((q, y), cs) in enumerate(zip(pairs, structs)):
+        items[i].w = ctypes.pointer(cs)
+        items[i].y = _ptr(y)
+    _check(lib.nf4_dequantize_batch(len(pairs), items, _dtype_code(pairs[0][1].dtype), _stream(stream)),
+           "nf4_dequantize_batch")
 
 
 def nf4_embedding_rows(E: Nf4Tensor, ids: torch.Tensor, dtype=torch.float32, out: torch.Tensor = None,

@@ -537,6 +537,33 @@ nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, voi
   return from_cuda(launch_dequantize(view_of(w), y, out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+nf4_status nf4_dequantize_batch(int32_t count, const nf4_dequantize_item* items, nf4_dtype out_dtype, void* stream) {
+  if (count < 1 || items == nullptr) return NF4_ERR_ARG;
+  if (out_dtype != NF4_F32 && out_dtype != NF4_BF16 && out_dtype != NF4_F16) return NF4_ERR_DTYPE;
+  for (int32_t i = 0; i < count; ++i) {   // every item is checked before anything is enqueued
+    const nf4_dequantize_item& it = items[i];
+    if (it.w == nullptr || it.y == nullptr) return NF4_ERR_ARG;
+    const nf4_status st = check_tensor(it.w, it.w->numel);
+    if (st != NF4_OK) return st;
+    if (!aligned16(it.y)) return NF4_ERR_ALIGN;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  KernelTimer timer(NF4_TIME_DEQUANTIZE, cs);
+  // runs of up to kQuantBatchMax items, in the items' order
+  for (int32_t i = 0; i < count;) {
+    Nf4View views[kQuantBatchMax];
+    void* ys[kQuantBatchMax];
+    int n = 0;
+    for (; i < count && n < kQuantBatchMax; ++i, ++n) {
+      views[n] = view_of(items[i].w);
+      ys[n] = items[i].y;
+    }
+    const cudaError_t e = launch_dequantize_batch(views, ys, n, out_dtype, cs);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return NF4_OK;
+}
+
 nf4_status nf4_embedding_rows(const nf4_tensor* E, int64_t rows, int64_t dim, const int64_t* ids,
                               int64_t n_ids, void* out, nf4_dtype out_dtype, void* stream) {
   if (E == nullptr || rows <= 0 || dim <= 0 || n_ids < 0) return NF4_ERR_ARG;

@@ -178,6 +178,8 @@ struct QuantJob {
 cudaError_t launch_quantize_batch(const QuantJob* jobs, int n, nf4_dtype xd, int* status, cudaStream_t st);
 size_t quantize_ws_bytes(int64_t numel, int dq);
 cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStream_t st);
+// up to kQuantBatchMax tensors: one launch for those with double quantization, one for the rest
+cudaError_t launch_dequantize_batch(const Nf4View* w, void* const* y, int n, nf4_dtype od, cudaStream_t st);
 struct PrepJobs;
 // quant.cu: the 16-bit decode of w into y (IEEE half when f16, else bf16) and `prep_ctas`
 // CTAs of staging jobs, one launch.

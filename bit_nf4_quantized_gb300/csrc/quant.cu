@@ -753,6 +753,34 @@ nf4_decode(Nf4View w, Tout* __restrict__ y, DecodeTables tabs) {
   decode_cta<Tout, kDQ>(w, y, tabs, blockIdx.x);
 }
 
+// Up to 8 tensors of one double-quant setting in one launch: CTA b decodes chunk b - cta0 of
+// the item whose CTA range holds it.
+struct DecodeItem {
+  Nf4View w;
+  void* y;
+  int64_t cta0;
+};
+struct DecodeBatch {
+  DecodeItem it[kEncodeBatch];
+  int n;
+};
+
+template <typename Tout, bool kDQ>
+__global__ void __launch_bounds__(kDeqThreads)
+nf4_decode_batch(DecodeBatch b, DecodeTables tabs) {
+  int i = 0;
+#pragma unroll 1
+  while (i + 1 < b.n && static_cast<int64_t>(blockIdx.x) >= b.it[i + 1].cta0) ++i;
+  // static indices into the parameters (a run-time index would copy them to local memory)
+  Nf4View w{};
+  void* y = nullptr;
+  int64_t cta0 = 0;
+#pragma unroll
+  for (int k = 0; k < kEncodeBatch; ++k)
+    if (k == i) w = b.it[k].w, y = b.it[k].y, cta0 = b.it[k].cta0;
+  decode_cta<Tout, kDQ>(w, static_cast<Tout*>(y), tabs, static_cast<int64_t>(blockIdx.x) - cta0);
+}
+
 // The 16-bit decode of the linear's weight and that call's operand staging in one launch:
 // CTAs below `decode_ctas` decode, the rest run the prep jobs.
 template <typename T16, bool kDQ>
@@ -940,6 +968,40 @@ cudaError_t launch_dequantize(const Nf4View& w, void* y, nf4_dtype od, cudaStrea
   }
   note_launch();
   return e;
+}
+
+// The items with double quantization in one launch, those without in another.
+cudaError_t launch_dequantize_batch(const Nf4View* ws, void* const* ys, int n, nf4_dtype od, cudaStream_t st) {
+  if (n < 1 || n > kEncodeBatch) return cudaErrorInvalidValue;
+  const DecodeTables& dt = decode_tables();
+  for (int dq = 1; dq >= 0; --dq) {
+    DecodeBatch b{};
+    int64_t ctas = 0;
+    for (int i = 0; i < n; ++i) {
+      if ((ws[i].dq != 0) != (dq != 0)) continue;
+      DecodeItem& it = b.it[b.n++];
+      it.w = ws[i];
+      it.y = ys[i];
+      it.cta0 = ctas;
+      ctas += (ws[i].numel + kDeqPerCta - 1) / kDeqPerCta;
+    }
+    if (ctas == 0) continue;
+    if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(ctas));
+    cudaError_t e;
+    if (od == NF4_F32)
+      e = dq ? launch_pdl(nf4_decode_batch<float, true>, grid, dim3(kDeqThreads), 0, st, 1, b, dt)
+             : launch_pdl(nf4_decode_batch<float, false>, grid, dim3(kDeqThreads), 0, st, 1, b, dt);
+    else if (od == NF4_BF16)
+      e = dq ? launch_pdl(nf4_decode_batch<__nv_bfloat16, true>, grid, dim3(kDeqThreads), 0, st, 1, b, dt)
+             : launch_pdl(nf4_decode_batch<__nv_bfloat16, false>, grid, dim3(kDeqThreads), 0, st, 1, b, dt);
+    else
+      e = dq ? launch_pdl(nf4_decode_batch<__half, true>, grid, dim3(kDeqThreads), 0, st, 1, b, dt)
+             : launch_pdl(nf4_decode_batch<__half, false>, grid, dim3(kDeqThreads), 0, st, 1, b, dt);
+    note_launch();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode_with_prep(const Nf4View& w, void* y, bool f16, const PrepJobs& jobs, unsigned prep_ctas,

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define QLORA_NF4_ABI_VERSION 3
+#define QLORA_NF4_ABI_VERSION 4
 
 typedef enum {
   NF4_OK = 0,
@@ -157,6 +157,19 @@ nf4_status nf4_quantize_noalloc(const void* x, nf4_dtype x_dtype, int64_t numel,
  * fp32 output is exact nf4[q]*a'; bf16 and half outputs are that value rounded to nearest
  * even ([ADAPT] "Fused GPU NF4 decodes inside the matrix kernel"). */
 nf4_status nf4_dequantize(const nf4_tensor* w, void* y, nf4_dtype out_dtype, void* stream);
+
+/* Several tensors in one call, e.g. the seven weights of one transformer layer: item i gets
+ * exactly what nf4_dequantize(items[i].w, items[i].y, out_dtype, stream) writes.  Up to 8
+ * items at a time decode in one launch per double-quant setting, so small tensors share the
+ * GPU instead of running one after another.  Every item is validated as nf4_dequantize
+ * validates it; the first failing item's status is returned and nothing is enqueued.
+ * Outputs must not overlap. */
+typedef struct {
+  const nf4_tensor* w;      /* the quantized tensor */
+  void* y;                  /* device output, w->numel elements of out_dtype, 16-byte aligned */
+} nf4_dequantize_item;
+nf4_status nf4_dequantize_batch(int32_t count, const nf4_dequantize_item* items, nf4_dtype out_dtype,
+                                void* stream);
 
 /* Selected rows of an NF4-quantized embedding table ([ADAPT] "Packed NF4 and the portable
  * QLoRA profile": embeddings decode only selected rows; "Fused GPU NF4 decodes inside the

@@ -41,7 +41,7 @@ def test_every_declared_function_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(binding.ENTRY_POINTS) <= set(names)
-    assert lib.nf4_abi_version() == 3
+    assert lib.nf4_abi_version() == 4
 
 
 def test_noalloc_limit_has_one_source(lib):
@@ -188,6 +188,28 @@ def test_validation_refuses_bad_arguments(lib):
     assert m(64, 64, 8) == binding.NF4_ERR_CORRUPT                             # numel != N*K
     assert m(64, 128, 8, a=ctypes.c_void_p(0x50000004)) == binding.NF4_ERR_ALIGN
     assert m(64, 128, 8, a=None) == binding.NF4_ERR_ARG
+
+
+def test_dequantize_batch_validation(lib):
+    """nf4_dequantize_batch checks every item before enqueueing anything (no device work)."""
+    t = _fake_tensor(1000)
+    items = (binding._DequantItem * 2)()
+    items[0].w = ctypes.pointer(t)
+    items[0].y = 0x50000000
+    items[1].w = ctypes.pointer(t)
+    items[1].y = None
+    bf16 = binding.NF4_BF16
+    assert lib.nf4_dequantize_batch(0, items, bf16, None) == binding.NF4_ERR_ARG
+    assert lib.nf4_dequantize_batch(1, None, bf16, None) == binding.NF4_ERR_ARG
+    assert lib.nf4_dequantize_batch(1, items, 9, None) == binding.NF4_ERR_DTYPE
+    assert lib.nf4_dequantize_batch(2, items, bf16, None) == binding.NF4_ERR_ARG     # item 1: no output
+    items[1].y = 0x50000008
+    assert lib.nf4_dequantize_batch(2, items, bf16, None) == binding.NF4_ERR_ALIGN   # item 1: misaligned
+    bad = _fake_tensor(1000)
+    bad.nested_absmax = None
+    items[1].w = ctypes.pointer(bad)
+    items[1].y = 0x50001000
+    assert lib.nf4_dequantize_batch(2, items, bf16, None) != binding.NF4_OK          # item 1: no nested maxima
 
 
 def test_status_strings(lib):

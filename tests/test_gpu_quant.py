@@ -169,6 +169,32 @@ def test_quantize_batch_equals_single_calls(lib):
             _assert_same_quant(q, onf4.quantize(_host_values(x), double_quant=dq))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.float16])
+def test_dequantize_batch_equals_single_calls(lib, dtype):
+    """nf4_dequantize_batch over 10 tensors (with and without double quantization, ragged
+    sizes; more than 8, so two runs of launches) writes every output exactly as a single
+    nf4_dequantize call does, and those are the oracle's values."""
+    odt = {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16"}[dtype]
+    sizes = [(16384 * 5 + 3, True), (1000, False), (64, True), (16384 * 3, True), (77777, False),
+             (1, True), (4096 * 1024, True), (129, True), (65, False), (300000, True)]
+    xs, pairs, singles = [], [], []
+    for i, (n, dq) in enumerate(sizes):
+        x = wl.device_normal((n,), 0.02, wl.seed_for(5, 700 + i), DEV, torch.bfloat16)
+        q = binding.nf4_quantize(x, dq)
+        xs.append(x)
+        pairs.append((q, torch.full((n,), float("nan"), dtype=dtype, device=DEV)))
+        singles.append(binding.nf4_dequantize(q, dtype))
+    binding.nf4_dequantize_batch(pairs)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    for (q, y), one, x, (n, dq) in zip(pairs, singles, xs, sizes):
+        assert torch.equal(y.view(torch.int16 if dtype != torch.float32 else torch.int32),
+                           one.view(torch.int16 if dtype != torch.float32 else torch.int32))
+        if n <= 100000:
+            want = onf4.dequantize(onf4.quantize(_host_values(x), double_quant=dq), odt)
+            assert np.array_equal(y.float().cpu().numpy().view(np.uint32), want.astype(np.float32).view(np.uint32))
+
+
 def test_quantize_ticket_counters_wrap(lib):
     """The block pass's ticket counters come from the library's pool of 16384 that every call
     puts back to zero: 16500 double-quant calls in a row (every counter used again) all give the
