@@ -214,6 +214,11 @@ class Layer:
         # the step decodes each weight once (the dequantize row) and both contractions read that
         # bf16 copy; decode_once = False runs the NF4-input calls, which decode once per call
         self.decode_once = True
+        # decode_batch = True (the headline step) decodes all 7 weights in one
+        # nf4_dequantize_batch call after the quantize (7 bf16 copies); False decodes each right
+        # before its projection's calls
+        self.decode_batch = True
+        self.deq_all = None
         ws_f = max(lib.qlora_fwd_workspace_bytes(self.M, N, K, self.r, 1) for _, N, K in self.shapes)
         ws_b = max(lib.qlora_bwd_workspace_bytes(self.M, N, K, self.r, 1) for _, N, K in self.shapes)
         self.ws_q = torch.empty(max(ws_q, 16), dtype=torch.uint8, device=dev)
@@ -264,10 +269,23 @@ class Layer:
 
     def step(self):
         """One step: the layer's 7 weights quantized in one batch call, then per projection the
-        dequantize, forward and backward."""
+        dequantize, forward and backward (or, with decode_batch, all 7 dequantized in one call
+        first)."""
+        import torch
+        from bit_nf4_quantized_gb300 import binding as b
         self.quantize_all()
-        for p in self.proj:
-            self.step_one(p, quantize=False)
+        if not self.decode_batch:
+            for p in self.proj:
+                self.step_one(p, quantize=False)
+            return
+        if self.deq_all is None:
+            self.deq_all = [torch.empty((p["N"], p["K"]), dtype=torch.bfloat16, device=self.dev) for p in self.proj]
+        b.nf4_dequantize_batch([(p["q"], w16) for p, w16 in zip(self.proj, self.deq_all)])
+        for p, w16 in zip(self.proj, self.deq_all):
+            b.qlora_linear_fwd_w16(p["x"], w16, p["A"], p["B"], self.alpha, y=p["y"], T=p["T"],
+                                   workspace=self.ws_f)
+            b.qlora_linear_bwd_w16(p["dy"], p["x"], p["T"], w16, p["A"], p["B"], self.alpha, dx=p["dx"],
+                                   dA=p["dA"], dB=p["dB"], workspace=self.ws_b)
 
     @staticmethod
     def inputs_of(p):
@@ -1129,13 +1147,18 @@ def main():
     f16_profile = measure_f16_profile(layer, row_ms)
     fp32_576 = measure_fp32_576(dev, row_ms)
     smollm2 = measure_smollm2(dev, row_ms, peak)
-    # the same step as one graph with L2 flushed before it, decoding once per projection (the
-    # headline's step) and with the NF4-input calls, which decode the weight once per call
+    # the same step as one graph with L2 flushed before it: all 7 weights decoded first (the
+    # headline's step), each decoded right before its projection, and the NF4-input calls, which
+    # decode the weight once per call
+    first_ms = row_ms(layer.step, reps=5)
+    layer.decode_batch = False
     once_ms = row_ms(layer.step, reps=5)
     layer.decode_once = False
     per_call_ms = row_ms(layer.step, reps=5)
     layer.decode_once = True
-    step_variants = {"decode_once": {"ms_per_step": once_ms, "TFLOP/s": flops / (once_ms / 1e3) / 1e12},
+    layer.decode_batch = True
+    step_variants = {"decode_all_first": {"ms_per_step": first_ms, "TFLOP/s": flops / (first_ms / 1e3) / 1e12},
+                     "decode_before_each": {"ms_per_step": once_ms, "TFLOP/s": flops / (once_ms / 1e3) / 1e12},
                      "decode_per_call": {"ms_per_step": per_call_ms, "TFLOP/s": flops / (per_call_ms / 1e3) / 1e12},
                      "timing": "one step as a graph, L2 flushed before each replay, launch included"}
 
@@ -1210,10 +1233,11 @@ def main():
             "config": {"workload": WORKLOAD_NAME, "tokens": M, "rank": r, "alpha": layer.alpha,
                        "targets": [n for n, _, _ in layer.shapes], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: each step touches ~1.5 GB of distinct buffers",
-                       "step": "nf4_quantize_batch of the 7 bf16 masters, then per projection nf4_dequantize "
-                               "(bf16), qlora_linear_fwd_w16 and qlora_linear_bwd_w16 reading that decoded bf16 "
-                               "weight (one decode per projection per step; key step_variants times the NF4-input "
-                               "calls, one decode per call)",
+                       "step": "nf4_quantize_batch of the 7 bf16 masters, nf4_dequantize_batch of the 7 "
+                               "quantized weights (bf16), then per projection qlora_linear_fwd_w16 and "
+                               "qlora_linear_bwd_w16 reading its decoded bf16 weight (one decode per weight per step; "
+                               "key step_variants also times a decode right before each projection and the "
+                               "NF4-input calls, one decode per call)",
                        "launch": "one step captured as a CUDA graph, replayed per timed step"},
             "gpu_launches": launches,
             "phases_ms_per_step": {k: v[0] / args.steps for k, v in kinds.items()},
