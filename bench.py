@@ -224,11 +224,15 @@ class Layer:
         self.ws_q = torch.empty(max(ws_q, 16), dtype=torch.uint8, device=dev)
         self.ws_f = torch.empty(max(ws_f, 16), dtype=torch.uint8, device=dev)
         self.ws_b = torch.empty(max(ws_b, 16), dtype=torch.uint8, device=dev)
+        # projections that read the same activation (q, k, v; gate, up) share one x tensor
+        shared_x = {}
         for i, (name, N, K) in enumerate(self.shapes):
             seed = wl.seed_for(3, 100 * i) + seed_base
-            p = dict(name=name, N=N, K=K)
+            p = dict(name=name, N=N, K=K, x_of=wl.LAYER_INPUTS.get(name, name))
             p["w"] = wl.device_student_t((N, K), c["t_df"], c["w_scale"], seed, dev, torch.bfloat16)
-            p["x"] = wl.device_normal((self.M, K), 1.0, seed + 1, dev, torch.bfloat16)
+            if p["x_of"] not in shared_x:
+                shared_x[p["x_of"]] = wl.device_normal((self.M, K), 1.0, seed + 1, dev, torch.bfloat16)
+            p["x"] = shared_x[p["x_of"]]
             p["dy"] = wl.device_normal((self.M, N), 1.0, seed + 2, dev, torch.bfloat16)
             p["A"] = wl.device_normal((self.r, K), 1.0 / self.r, seed + 3, dev, torch.float32)
             p["B"] = wl.device_normal((N, self.r), 0.01, seed + 4, dev, torch.float32)
@@ -241,6 +245,21 @@ class Layer:
             self.proj.append(p)
         self.ws_qb = torch.empty(max(16, binding.nf4_quantize_batch_workspace_bytes(self.quant_pairs())),
                                  dtype=torch.uint8, device=dev)
+        # the grouped calls (the headline step): one forward and one backward batch over the 7
+        # projections with their weights decoded; consecutive projections with one x share a pass
+        shapes = [(p["N"], p["K"]) for p in self.proj]
+        xs = [p["x_of"] for p in self.proj]
+        self.grouped = True
+        self.ws_fb = torch.empty(max(16, binding.qlora_fwd_batch_workspace_bytes(self.M, shapes, self.r, xs=xs,
+                                                                                 w16=True)),
+                                 dtype=torch.uint8, device=dev)
+        self.ws_bb = torch.empty(max(16, binding.qlora_bwd_batch_workspace_bytes(self.M, shapes, self.r, xs=xs,
+                                                                                 w16=True)),
+                                 dtype=torch.uint8, device=dev)
+        # the activations once each (the e2e copies)
+        self.x_first = {}
+        for i, p in enumerate(self.proj):
+            self.x_first.setdefault(p["x_of"], i)
 
     def quant_pairs(self):
         return [(p["w"], p["q"]) for p in self.proj]
@@ -267,12 +286,35 @@ class Layer:
         b.qlora_linear_bwd(p["dy"], p["x"], p["T"], p["q"], p["A"], p["B"], self.alpha, dx=p["dx"],
                            dA=p["dA"], dB=p["dB"], workspace=self.ws_b)
 
-    def step(self):
-        """One step: the layer's 7 weights quantized in one batch call, then per projection the
-        dequantize, forward and backward (or, with decode_batch, all 7 dequantized in one call
-        first)."""
+    def run_group(self, idx, quantize=True):
+        """Projections idx (the whole layer, or one set that reads one x): quantize (one batch
+        call), dequantize (one batch call), then one grouped forward and one grouped backward
+        call reading the decoded weights."""
         import torch
         from bit_nf4_quantized_gb300 import binding as b
+        if self.deq_all is None:
+            self.deq_all = [torch.empty((p["N"], p["K"]), dtype=torch.bfloat16, device=self.dev) for p in self.proj]
+        ps = [self.proj[i] for i in idx]
+        if quantize:
+            b.nf4_quantize_batch([(p["w"], p["q"]) for p in ps], workspace=self.ws_qb)
+        b.nf4_dequantize_batch([(self.proj[i]["q"], self.deq_all[i]) for i in idx])
+        b.qlora_linear_fwd_batch([dict(x=p["x"], w16=self.deq_all[i], A=p["A"], B=p["B"], alpha=self.alpha,
+                                       y=p["y"], T=p["T"]) for i, p in zip(idx, ps)], workspace=self.ws_fb)
+        b.qlora_linear_bwd_batch([dict(dy=p["dy"], x=p["x"], T=p["T"], w16=self.deq_all[i], A=p["A"], B=p["B"],
+                                       alpha=self.alpha, dx=p["dx"], dA=p["dA"], dB=p["dB"])
+                                  for i, p in zip(idx, ps)], workspace=self.ws_bb)
+
+    def step(self):
+        """One step: the layer's 7 weights quantized in one batch call and dequantized in one batch
+        call, then one grouped forward and one grouped backward call (q, k, v and gate, up each
+        share one pass over their x).  Variants: grouped = False runs per projection single
+        forward and backward calls on the decoded weights; decode_batch = False decodes each
+        weight right before its projection's single calls."""
+        import torch
+        from bit_nf4_quantized_gb300 import binding as b
+        if self.grouped and self.decode_batch:
+            self.run_group(list(range(len(self.proj))))
+            return
         self.quantize_all()
         if not self.decode_batch:
             for p in self.proj:
@@ -287,6 +329,16 @@ class Layer:
             b.qlora_linear_bwd_w16(p["dy"], p["x"], p["T"], w16, p["A"], p["B"], self.alpha, dx=p["dx"],
                                    dA=p["dA"], dB=p["dB"], workspace=self.ws_b)
 
+    def x_groups(self):
+        """Projection indices in runs that read one x (in order)."""
+        out = []
+        for i, p in enumerate(self.proj):
+            if out and self.proj[out[-1][0]]["x_of"] == p["x_of"]:
+                out[-1].append(i)
+            else:
+                out.append([i])
+        return out
+
     @staticmethod
     def inputs_of(p):
         return [p[k] for k in ("w", "x", "dy")]
@@ -296,7 +348,11 @@ class Layer:
         return [p[k] for k in ("dA", "dB")]
 
     def input_tensors(self):
-        return [t for p in self.proj for t in self.inputs_of(p)]
+        # a shared x once
+        out = []
+        for i, p in enumerate(self.proj):
+            out += [p["w"], p["dy"]] + ([p["x"]] if self.x_first[p["x_of"]] == i else [])
+        return out
 
     def result_tensors(self):
         return [t for p in self.proj for t in self.results_of(p)]
@@ -631,6 +687,9 @@ def measure_export_rows(dev, row_ms, hbm):
     # row lies in one 16384-element group), the 8-byte id and dim bf16 outputs
     emb_bytes = n_ids * (dim // 2 + dim // 64 + 4 + 8 + 2 * dim)
     emb_ms = row_ms(lambda: bq.nf4_embedding_rows(table, ids, out=rows_out), reps=20)
+    # the store floor: filling the same output buffer (a library fill kernel), timed the same
+    # way; after the flush L2 holds dirty lines, so every output line written evicts one
+    emb_floor_ms = row_ms(lambda: rows_out.zero_(), reps=20)
     del table, rows_out
 
     m = wl.W7
@@ -641,15 +700,19 @@ def measure_export_rows(dev, row_ms, hbm):
     merged = torch.empty((N, K), dtype=torch.float32, device=dev)
     merge_bytes = lib.nf4_packed_bytes(N * K, 1) + 4 * r * K + 4 * N * r + 4 * N * K
     merge_ms = row_ms(lambda: bq.nf4_merge_lora(W, A, B, m["alpha"], out=merged), reps=20)
+    merge_floor_ms = row_ms(lambda: merged.zero_(), reps=20)
     del W, merged
     emb_gbs = emb_bytes / (emb_ms / 1e3) / 1e9
     merge_gbs = merge_bytes / (merge_ms / 1e3) / 1e9
     return {
         "embedding": {"GB/s": emb_gbs, "frac": emb_gbs / hbm, "bytes_per_call": emb_bytes, "ms_per_call": emb_ms,
+                      "store_floor_ms": emb_floor_ms, "frac_of_store_floor": emb_floor_ms / emb_ms,
                       "workload": e["name"], "timing": "one call as a graph, L2 flushed between replays"},
         "merge": {"GB/s": merge_gbs, "frac": merge_gbs / hbm, "bytes_per_call": merge_bytes,
-                  "ms_per_call": merge_ms, "workload": m["name"],
-                  "timing": "one call as a graph, L2 flushed between replays"},
+                  "ms_per_call": merge_ms, "store_floor_ms": merge_floor_ms,
+                  "frac_of_store_floor": merge_floor_ms / merge_ms, "workload": m["name"],
+                  "timing": "one call as a graph, L2 flushed between replays; store_floor_ms = zero-filling "
+                            "the same output the same way"},
     }
 
 
@@ -1151,52 +1214,65 @@ def main():
     # headline's step), each decoded right before its projection, and the NF4-input calls, which
     # decode the weight once per call
     first_ms = row_ms(layer.step, reps=5)
+    layer.grouped = False
+    single_ms = row_ms(layer.step, reps=5)
     layer.decode_batch = False
     once_ms = row_ms(layer.step, reps=5)
     layer.decode_once = False
     per_call_ms = row_ms(layer.step, reps=5)
     layer.decode_once = True
     layer.decode_batch = True
-    step_variants = {"decode_all_first": {"ms_per_step": first_ms, "TFLOP/s": flops / (first_ms / 1e3) / 1e12},
+    layer.grouped = True
+    step_variants = {"grouped": {"ms_per_step": first_ms, "TFLOP/s": flops / (first_ms / 1e3) / 1e12},
+                     "single_calls": {"ms_per_step": single_ms, "TFLOP/s": flops / (single_ms / 1e3) / 1e12},
                      "decode_before_each": {"ms_per_step": once_ms, "TFLOP/s": flops / (once_ms / 1e3) / 1e12},
                      "decode_per_call": {"ms_per_step": per_call_ms, "TFLOP/s": flops / (per_call_ms / 1e3) / 1e12},
-                     "timing": "one step as a graph, L2 flushed before each replay, launch included"}
+                     "timing": "one step as a graph, L2 flushed before each replay, launch included",
+                     "what": "grouped = the headline step; single_calls = the same decode, then per projection "
+                             "qlora_linear_fwd_w16 / qlora_linear_bwd_w16; decode_before_each = each weight "
+                             "decoded right before its single calls; decode_per_call = the NF4-input calls"}
 
     e2e = None
     if not args.no_e2e:
-        # each projection's inputs (bf16 master weight, x, dY) come from pinned host memory and
-        # its dA, dB go back; the copies run on two copy streams (each tensor in halves, one per
-        # copy engine) ahead of the compute, and each projection waits only for its own inputs
+        # each projection's inputs (bf16 master weight, dY; a shared x once) come from pinned host
+        # memory and its dA, dB go back; the copies run on two copy streams (each tensor in halves,
+        # one per copy engine) ahead of the compute; each set of projections that reads one x runs
+        # the headline's calls (quantize batch, dequantize batch, grouped forward and backward)
+        # once its own inputs are in
         local_cpus = gpu_local_cpus(dev)
         saved_affinity = os.sched_getaffinity(0)
         if local_cpus:
             os.sched_setaffinity(0, local_cpus)
-        host_in = [[t.cpu().pin_memory() for t in layer.inputs_of(p)] for p in layer.proj]
-        host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in layer.results_of(p)]
-                    for p in layer.proj]
+        groups = layer.x_groups()
+        dev_in = [[t for i in idx for t in ([layer.proj[i]["w"], layer.proj[i]["dy"]] +
+                                            ([layer.proj[i]["x"]] if layer.x_first[layer.proj[i]["x_of"]] == i
+                                             else []))] for idx in groups]
+        dev_out = [[t for i in idx for t in layer.results_of(layer.proj[i])] for idx in groups]
+        host_in = [[t.cpu().pin_memory() for t in ts] for ts in dev_in]
+        host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ts] for ts in dev_out]
         h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
         d2h = sum(t.numel() * t.element_size() for hs in host_out for t in hs)
         copy_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-        ready = [[torch.cuda.Event() for _ in copy_streams] for _ in layer.proj]
-        done = [torch.cuda.Event() for _ in layer.proj]   # projection's compute and read-back issued
+        ready = [[torch.cuda.Event() for _ in copy_streams] for _ in groups]
+        done = [torch.cuda.Event() for _ in groups]   # the set's compute and read-back issued
 
         def e2e_step():
-            for i, p in enumerate(layer.proj):
+            for g in range(len(groups)):
                 for c, cs in enumerate(copy_streams):
                     with torch.cuda.stream(cs):
-                        cs.wait_event(done[i])   # the previous step has finished with these buffers
-                        for h, d in zip(host_in[i], layer.inputs_of(p)):
+                        cs.wait_event(done[g])   # the previous step has finished with these buffers
+                        for h, d in zip(host_in[g], dev_in[g]):
                             half = (h.shape[0] + 1) // 2
                             lo, hi = (0, half) if c == 0 else (half, h.shape[0])
                             d[lo:hi].copy_(h[lo:hi], non_blocking=True)
-                        ready[i][c].record(cs)
-            for i, p in enumerate(layer.proj):
-                for ev in ready[i]:
+                        ready[g][c].record(cs)
+            for g, idx in enumerate(groups):
+                for ev in ready[g]:
                     stream.wait_event(ev)
-                layer.step_one(p)
-                for h, d in zip(host_out[i], layer.results_of(p)):
+                layer.run_group(idx)
+                for h, d in zip(host_out[g], dev_out[g]):
                     h.copy_(d, non_blocking=True)
-                done[i].record(stream)
+                done[g].record(stream)
 
         def time_e2e(steps):
             # the copy streams start after the start event; each step's copies then wait only
@@ -1234,10 +1310,11 @@ def main():
                        "targets": [n for n, _, _ in layer.shapes], "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: each step touches ~1.5 GB of distinct buffers",
                        "step": "nf4_quantize_batch of the 7 bf16 masters, nf4_dequantize_batch of the 7 "
-                               "quantized weights (bf16), then per projection qlora_linear_fwd_w16 and "
-                               "qlora_linear_bwd_w16 reading its decoded bf16 weight (one decode per weight per step; "
-                               "key step_variants also times a decode right before each projection and the "
-                               "NF4-input calls, one decode per call)",
+                               "quantized weights (bf16), then one qlora_linear_fwd_batch and one "
+                               "qlora_linear_bwd_batch over the 7 projections reading their decoded weights; q, k, v "
+                               "read one x and gate, up another (as in a transformer layer), and each such set "
+                               "shares one T pass and one dA pass (key step_variants also times per-projection "
+                               "single calls)",
                        "launch": "one step captured as a CUDA graph, replayed per timed step"},
             "gpu_launches": launches,
             "phases_ms_per_step": {k: v[0] / args.steps for k, v in kinds.items()},

@@ -52,7 +52,7 @@ class _FwdItem(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("rank", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("mode", ctypes.c_int32), ("W", ctypes.POINTER(_Nf4Tensor)),
                 ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
-                ("T_out", ctypes.c_void_p)]
+                ("T_out", ctypes.c_void_p), ("w16", ctypes.c_void_p)]
 
 
 class _BwdItem(ctypes.Structure):
@@ -360,9 +360,10 @@ def qlora_linear_fwd(x: torch.Tensor, W: Nf4Tensor, A: torch.Tensor, B: torch.Te
 
 
 def qlora_linear_fwd_batch(items, workspace: torch.Tensor = None, stream=None):
-    """Forward of several projections sharing M: ``items`` is a list of dicts with keys x, W,
-    A, B, alpha and optionally mode, y, T (as for qlora_linear_fwd).  Returns [(y, T), ...].
-    With bf16 and M <= 16 every group of up to 8 items runs as one pair of launches."""
+    """Forward of several projections sharing M: ``items`` is a list of dicts with keys x, A, B,
+    alpha, W (an Nf4Tensor) or w16 (the decoded weight), and optionally mode, y, T (as for
+    qlora_linear_fwd / qlora_linear_fwd_w16).  Returns [(y, T), ...]; each item equals its
+    single call.  Consecutive items that pass the same x tensor share one T pass."""
     lib = load()
     n = len(items)
     M = items[0]["x"].shape[0]
@@ -371,8 +372,10 @@ def qlora_linear_fwd_batch(items, workspace: torch.Tensor = None, stream=None):
     keep = []
     outs = []
     for i, it in enumerate(items):
-        x, W, A, B = it["x"], it["W"], it["A"], it["B"]
-        N, K = W.shape
+        x, A, B = it["x"], it["A"], it["B"]
+        W = it.get("W")
+        w16 = it.get("w16")
+        N, K = (w16 if w16 is not None else W).shape
         r = A.shape[0]
         y = it.get("y")
         T = it.get("T")
@@ -380,10 +383,11 @@ def qlora_linear_fwd_batch(items, workspace: torch.Tensor = None, stream=None):
             y = torch.empty((M, N), dtype=x.dtype, device=x.device)
         if T is None:
             T = torch.empty((M, r), dtype=torch.float32, device=x.device)
-        cs = W.c_struct()
+        cs = W.c_struct() if W is not None else None
         keep.append(cs)
-        arr[i] = _FwdItem(N, K, r, float(it["alpha"]), int(it.get("mode", SCALE_LORA)), ctypes.pointer(cs),
-                          A.data_ptr(), B.data_ptr(), x.data_ptr(), y.data_ptr(), T.data_ptr())
+        arr[i] = _FwdItem(N, K, r, float(it["alpha"]), int(it.get("mode", SCALE_LORA)),
+                          ctypes.pointer(cs) if cs is not None else None, A.data_ptr(), B.data_ptr(),
+                          x.data_ptr(), y.data_ptr(), T.data_ptr(), w16.data_ptr() if w16 is not None else None)
         outs.append((y, T))
     ws = workspace if workspace is not None else _workspace(
         lib.qlora_fwd_batch_workspace_bytes(M, n, arr, cd), items[0]["x"].device)
@@ -391,12 +395,23 @@ def qlora_linear_fwd_batch(items, workspace: torch.Tensor = None, stream=None):
     return outs
 
 
-def qlora_fwd_batch_workspace_bytes(M: int, shapes, rank: int, dtype=torch.bfloat16) -> int:
-    """Workspace bytes of qlora_linear_fwd_batch for items of the given (N, K) shapes and rank."""
+def _x_ids(n, xs):
+    # stand-in x addresses for workspace queries (never dereferenced): equal ids share an x
+    ids = list(range(n)) if xs is None else list(xs)
+    first = {}
+    return [16 * (1 + first.setdefault(v, len(first))) for v in ids]
+
+
+def qlora_fwd_batch_workspace_bytes(M: int, shapes, rank: int, dtype=torch.bfloat16, xs=None,
+                                    w16: bool = False) -> int:
+    """Workspace bytes of qlora_linear_fwd_batch for items of the given (N, K) shapes and rank.
+    ``xs``: one hashable per item, equal where items pass the same x (default: all distinct);
+    ``w16``: the items give their weights decoded."""
     lib = load()
     arr = (_FwdItem * len(shapes))()
+    xid = _x_ids(len(shapes), xs)
     for i, (N, K) in enumerate(shapes):
-        arr[i] = _FwdItem(N, K, rank, 1.0, SCALE_LORA, None, None, None, None, None, None)
+        arr[i] = _FwdItem(N, K, rank, 1.0, SCALE_LORA, None, None, None, xid[i], None, None, 16 if w16 else None)
     return int(lib.qlora_fwd_batch_workspace_bytes(M, len(shapes), arr, _dtype_code(dtype)))
 
 
@@ -512,12 +527,16 @@ def qlora_linear_bwd_batch(items, workspace: torch.Tensor = None, stream=None):
     return outs
 
 
-def qlora_bwd_batch_workspace_bytes(M: int, shapes, rank: int, dtype=torch.bfloat16) -> int:
-    """Workspace bytes of qlora_linear_bwd_batch for items of the given (N, K) shapes and rank."""
+def qlora_bwd_batch_workspace_bytes(M: int, shapes, rank: int, dtype=torch.bfloat16, xs=None,
+                                    w16: bool = False) -> int:
+    """Workspace bytes of qlora_linear_bwd_batch for items of the given (N, K) shapes and rank
+    (``xs`` and ``w16`` as for qlora_fwd_batch_workspace_bytes)."""
     lib = load()
     arr = (_BwdItem * len(shapes))()
+    xid = _x_ids(len(shapes), xs)
     for i, (N, K) in enumerate(shapes):
-        arr[i] = _BwdItem(N, K, rank, 1.0, SCALE_LORA, None, None, None, None, None, None, None, None, None, None)
+        arr[i] = _BwdItem(N, K, rank, 1.0, SCALE_LORA, None, 16 if w16 else None, None, None, None, xid[i], None,
+                          None, None, None)
     return int(lib.qlora_bwd_batch_workspace_bytes(M, len(shapes), arr, _dtype_code(dtype)))
 
 

@@ -396,26 +396,102 @@ nf4_status check_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
   return NF4_OK;
 }
 
-// Workspace of a batch of forward items: the largest group (small M) or item (otherwise).
-size_t batch_ws(int64_t M, int32_t count, const qlora_fwd_item* it, nf4_dtype cd) {
-  size_t need = 0;
-  if (small_m(M, cd)) {
-    for (int32_t g0 = 0; g0 < count; g0 += kStreamMaxGroup) {
-      LinearArgs la[kStreamMaxGroup];
-      const int n = std::min<int32_t>(kStreamMaxGroup, count - g0);
-      for (int i = 0; i < n; ++i) la[i] = LinearArgs{M, it[g0 + i].N, it[g0 + i].K, it[g0 + i].rank, 0.0f, Nf4View{}};
-      need = std::max(need, stream_fwd_ws_bytes(la, n));
-    }
-    return need;
-  }
-  for (int32_t i = 0; i < count; ++i) need = std::max(need, fwd_ws(M, it[i].N, it[i].K, it[i].rank, cd));
-  return need;
-}
 size_t bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
   if (small_w(M, N, K, r, cd)) return small_bwd_ws(M, N, K, r);
   size_t b = a256(sizeof(float) * static_cast<size_t>(M) * r);
   if (is16(cd)) b += tc_bwd_ws_bytes(M, N, K, r);
   return b;
+}
+
+// How a batch runs, as a list of runs in order; every run uses the whole workspace, one
+// after another on the stream:
+//   kRunStream: items given as NF4 at M <= 16 (16-bit), up to kStreamMaxGroup, one stream pass;
+//   kRunSmall:  small weights, up to kSmallMaxGroup in one fused launch (a pair backward);
+//   kRunGroup:  tiled items in a row that read the same x (pointer and K), up to kTcGroupMax
+//               whose padded ranks fit kTcGroupMaxRank: one shared skinny pass (a run of one
+//               item is the single call);
+//   kRunSingle: one single call (fp32 compute, or no tokens).
+enum { kRunStream, kRunSmall, kRunGroup, kRunSingle };
+struct BatchRun {
+  int kind;
+  std::vector<int> idx;
+};
+
+template <typename KindOf, typename XOf, typename KOf, typename ROf>
+std::vector<BatchRun> plan_batch(int32_t count, KindOf kind_of, XOf x_of, KOf k_of, ROf r_of) {
+  std::vector<BatchRun> runs;
+  BatchRun stream{kRunStream, {}}, small{kRunSmall, {}}, group{kRunGroup, {}};
+  int group_nq = 0;
+  auto flush = [&](BatchRun& b) {
+    if (!b.idx.empty()) runs.push_back(b);
+    b.idx.clear();
+  };
+  for (int i = 0; i < count; ++i) {
+    const int k = kind_of(i);
+    if (k == kRunStream) {
+      stream.idx.push_back(i);
+      if (static_cast<int>(stream.idx.size()) == kStreamMaxGroup) flush(stream);
+    } else if (k == kRunSmall) {
+      small.idx.push_back(i);
+      if (static_cast<int>(small.idx.size()) == kSmallMaxGroup) flush(small);
+    } else if (k == kRunGroup) {
+      const int nq = adapter_nq(r_of(i));
+      if (!group.idx.empty()) {
+        const int g0 = group.idx[0];
+        if (x_of(i) != x_of(g0) || k_of(i) != k_of(g0) || static_cast<int>(group.idx.size()) == kTcGroupMax ||
+            group_nq + nq > kTcGroupMaxRank) {
+          flush(group);
+          group_nq = 0;
+        }
+      }
+      group.idx.push_back(i);
+      group_nq += nq;
+    } else {
+      runs.push_back(BatchRun{kRunSingle, {i}});
+    }
+  }
+  flush(group);
+  flush(stream);
+  flush(small);
+  return runs;
+}
+
+std::vector<BatchRun> plan_fwd(int64_t M, int32_t count, const qlora_fwd_item* it, nf4_dtype cd) {
+  return plan_batch(
+      count,
+      [&](int i) {
+        if (!is16(cd) || M == 0) return static_cast<int>(kRunSingle);
+        if (it[i].w16 == nullptr && small_m(M, cd)) return static_cast<int>(kRunStream);
+        if (small_w(M, it[i].N, it[i].K, it[i].rank, cd)) return static_cast<int>(kRunSmall);
+        return static_cast<int>(kRunGroup);
+      },
+      [&](int i) { return it[i].x; }, [&](int i) { return it[i].K; }, [&](int i) { return it[i].rank; });
+}
+
+std::vector<BatchRun> plan_bwd(int64_t M, int32_t count, const qlora_bwd_item* it, nf4_dtype cd) {
+  return plan_batch(
+      count,
+      [&](int i) {
+        if (!is16(cd) || M == 0) return static_cast<int>(kRunSingle);
+        if (small_w(M, it[i].N, it[i].K, it[i].rank, cd)) return static_cast<int>(kRunSmall);
+        return static_cast<int>(kRunGroup);
+      },
+      [&](int i) { return it[i].x; }, [&](int i) { return it[i].K; }, [&](int i) { return it[i].rank; });
+}
+
+// (the weight view only when `view`: workspace sizes are asked before any validation)
+TcFwdItem tc_fwd_item(int64_t M, const qlora_fwd_item& it, float s, bool view = true) {
+  TcFwdItem t{};
+  t.a = LinearArgs{M, it.N, it.K, it.rank, s, (it.w16 != nullptr || !view) ? Nf4View{} : view_of(it.W)};
+  t.A = it.A, t.B = it.B, t.y = it.y, t.T = it.T_out, t.w16 = it.w16;
+  return t;
+}
+
+TcBwdItem tc_bwd_item(int64_t M, const qlora_bwd_item& it, float s, bool view = true) {
+  TcBwdItem t{};
+  t.a = LinearArgs{M, it.N, it.K, it.rank, s, (it.w16 != nullptr || !view) ? Nf4View{} : view_of(it.W)};
+  t.dy = it.dy, t.T = it.T, t.A = it.A, t.B = it.B, t.dx = it.dx, t.dA = it.dA, t.dB = it.dB, t.w16 = it.w16;
+  return t;
 }
 
 }  // namespace
@@ -649,67 +725,99 @@ size_t qlora_fwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_fwd
   if (M < 0 || count < 1 || items == nullptr) return 0;
   for (int32_t i = 0; i < count; ++i)
     if (items[i].N <= 0 || items[i].K <= 0 || items[i].rank < 1 || items[i].rank > 256) return 0;
-  return batch_ws(M, count, items, compute);
+  size_t need = 0;
+  for (const BatchRun& r : plan_fwd(M, count, items, compute)) {
+    const int n = static_cast<int>(r.idx.size());
+    if (r.kind == kRunStream) {
+      LinearArgs la[kStreamMaxGroup];
+      for (int k = 0; k < n; ++k) {
+        const qlora_fwd_item& it = items[r.idx[k]];
+        la[k] = LinearArgs{M, it.N, it.K, it.rank, 0.0f, Nf4View{}};
+      }
+      need = std::max(need, stream_fwd_ws_bytes(la, n));
+    } else if (r.kind == kRunGroup && n > 1) {
+      TcFwdItem t[kTcGroupMax];
+      for (int k = 0; k < n; ++k) t[k] = tc_fwd_item(M, items[r.idx[k]], 0.0f, false);
+      need = std::max(need, tc_fwd_group_ws_bytes(t, n));
+    } else if (r.kind != kRunSmall) {
+      const qlora_fwd_item& it = items[r.idx[0]];
+      need = std::max(need, it.w16 != nullptr ? qlora_fwd_w16_workspace_bytes(M, it.N, it.K, it.rank, compute)
+                                              : fwd_ws(M, it.N, it.K, it.rank, compute));
+    }
+  }
+  return need;
 }
 
 nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item* items, nf4_dtype compute,
                                   void* ws, size_t ws_bytes, void* stream) {
   if (count < 1 || items == nullptr) return NF4_ERR_ARG;
   std::vector<float> s(static_cast<size_t>(count));
-  for (int32_t i = 0; i < count; ++i) {
+  for (int32_t i = 0; i < count; ++i) {   // the single calls' checks, before anything is enqueued
     const qlora_fwd_item& it = items[i];
-    const nf4_status st = check_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A, it.B,
-                                    it.y, it.T_out, &s[i]);
-    if (st != NF4_OK) return st;
+    nf4_status st;
+    if (it.w16 != nullptr) {
+      if ((st = check_linear(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, &s[i])) != NF4_OK) return st;
+      if (!is16(compute)) return NF4_ERR_DTYPE;
+      if (it.A == nullptr || it.B == nullptr) return NF4_ERR_ARG;
+      if (M > 0 && (it.x == nullptr || it.y == nullptr || it.T_out == nullptr)) return NF4_ERR_ARG;
+      if (!aligned16(it.w16) || !aligned16(it.A) || !aligned16(it.B) ||
+          (M > 0 && (!aligned16(it.x) || !aligned16(it.y) || !aligned16(it.T_out))))
+        return NF4_ERR_ALIGN;
+    } else if ((st = check_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A, it.B, it.y,
+                               it.T_out, &s[i])) != NF4_OK) {
+      return st;
+    }
   }
-  const size_t need = batch_ws(M, count, items, compute);
+  const size_t need = qlora_fwd_batch_workspace_bytes(M, count, items, compute);
   if (need > 0 && (ws == nullptr || ws_bytes < need)) return NF4_ERR_WORKSPACE;
   if (need > 0 && !aligned16(ws)) return NF4_ERR_ALIGN;
   if (M == 0) return NF4_OK;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (small_m(M, compute)) {
-    int* status = nullptr;
-    const nf4_status st = device_status_ptr(&status);
-    if (st != NF4_OK) return st;
-    for (int32_t g0 = 0; g0 < count; g0 += kStreamMaxGroup) {
+  const bool f16 = compute == NF4_F16;
+  int* status = nullptr;
+  for (const BatchRun& r : plan_fwd(M, count, items, compute)) {
+    const int n = static_cast<int>(r.idx.size());
+    const int i0 = r.idx[0];
+    if ((r.kind == kRunStream || (r.kind == kRunGroup && n > 1)) && status == nullptr) {
+      const nf4_status st = device_status_ptr(&status);
+      if (st != NF4_OK) return st;
+    }
+    cudaError_t e = cudaSuccess;
+    if (r.kind == kRunStream) {
       StreamItem group[kStreamMaxGroup];
-      const int n = std::min<int32_t>(kStreamMaxGroup, count - g0);
-      for (int i = 0; i < n; ++i) {
-        const qlora_fwd_item& it = items[g0 + i];
-        group[i] = StreamItem{LinearArgs{M, it.N, it.K, it.rank, s[g0 + i], view_of(it.W)}, it.x, it.A, it.B, it.y,
+      for (int k = 0; k < n; ++k) {
+        const qlora_fwd_item& it = items[r.idx[k]];
+        group[k] = StreamItem{LinearArgs{M, it.N, it.K, it.rank, s[r.idx[k]], view_of(it.W)}, it.x, it.A, it.B, it.y,
                               it.T_out};
       }
-      const cudaError_t e = stream_forward(group, n, compute == NF4_F16, ws, status, cs);
-      if (e != cudaSuccess) return NF4_ERR_CUDA;
-    }
-    return NF4_OK;
-  }
-  // small weights: up to 8 per launch of the fused forward; the others one call each
-  std::vector<SmallItem> small;
-  auto flush = [&]() -> nf4_status {
-    if (small.empty()) return NF4_OK;
-    const cudaError_t e = small_fused_forward(small.data(), static_cast<int>(small.size()), M, compute == NF4_F16, cs);
-    small.clear();
-    return from_cuda(e);
-  };
-  for (int32_t i = 0; i < count; ++i) {
-    const qlora_fwd_item& it = items[i];
-    if (small_w(M, it.N, it.K, it.rank, compute)) {
-      SmallItem si{};
-      si.a = LinearArgs{M, it.N, it.K, it.rank, s[i], view_of(it.W)};
-      si.x = it.x, si.A = it.A, si.B = it.B, si.y = it.y, si.T = it.T_out;
-      small.push_back(si);
-      if (static_cast<int>(small.size()) == kSmallMaxGroup) {
-        const nf4_status st = flush();
-        if (st != NF4_OK) return st;
+      e = stream_forward(group, n, f16, ws, status, cs);
+    } else if (r.kind == kRunSmall) {
+      SmallItem small[kSmallMaxGroup];
+      for (int k = 0; k < n; ++k) {
+        const qlora_fwd_item& it = items[r.idx[k]];
+        SmallItem& si = small[k];
+        si = SmallItem{};
+        si.a = LinearArgs{M, it.N, it.K, it.rank, s[r.idx[k]], it.w16 != nullptr ? Nf4View{} : view_of(it.W)};
+        si.x = it.x, si.A = it.A, si.B = it.B, si.y = it.y, si.T = it.T_out, si.w16 = it.w16;
       }
-      continue;
+      e = small_fused_forward(small, n, M, f16, cs);
+    } else if (r.kind == kRunGroup && n > 1) {
+      TcFwdItem t[kTcGroupMax];
+      for (int k = 0; k < n; ++k) t[k] = tc_fwd_item(M, items[r.idx[k]], s[r.idx[k]]);
+      e = tc_forward_group(t, n, f16, items[i0].x, ws, status, cs);
+    } else {
+      const qlora_fwd_item& it = items[i0];
+      const nf4_status st =
+          it.w16 != nullptr
+              ? qlora_linear_fwd_w16(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.w16, it.A, it.B,
+                                     it.y, it.T_out, ws, ws_bytes, stream)
+              : qlora_linear_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A, it.B, it.y,
+                                 it.T_out, ws, ws_bytes, stream);
+      if (st != NF4_OK) return st;
     }
-    const nf4_status st = qlora_linear_fwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.x, it.W, it.A,
-                                           it.B, it.y, it.T_out, ws, ws_bytes, stream);
-    if (st != NF4_OK) return st;
+    if (e != cudaSuccess) return NF4_ERR_CUDA;
   }
-  return flush();
+  return NF4_OK;
 }
 
 nf4_status qlora_linear_bwd(int64_t M, int64_t N, int64_t K, int32_t rank, float alpha,
@@ -838,20 +946,30 @@ nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
 
 size_t qlora_bwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_bwd_item* items, nf4_dtype compute) {
   if (M < 0 || count < 1 || items == nullptr) return 0;
-  size_t single = 0, group = 0, fused = 0;
-  int in_group = 0;
-  for (int32_t i = 0; i < count; ++i) {
-    const qlora_bwd_item& it = items[i];
-    if (it.N <= 0 || it.K <= 0 || it.rank < 1 || it.rank > 256) return 0;
-    if (small_w(M, it.N, it.K, it.rank, compute)) {
-      group += small_bwd_ws(M, it.N, it.K, it.rank);
-      if (++in_group == kSmallMaxGroup) fused = std::max(fused, group), group = 0, in_group = 0;
-      continue;
+  for (int32_t i = 0; i < count; ++i)
+    if (items[i].N <= 0 || items[i].K <= 0 || items[i].rank < 1 || items[i].rank > 256) return 0;
+  size_t need = 0;
+  for (const BatchRun& r : plan_bwd(M, count, items, compute)) {
+    const int n = static_cast<int>(r.idx.size());
+    if (r.kind == kRunSmall) {
+      SmallItem small[kSmallMaxGroup];
+      for (int k = 0; k < n; ++k) {
+        const qlora_bwd_item& it = items[r.idx[k]];
+        small[k] = SmallItem{};
+        small[k].a = LinearArgs{M, it.N, it.K, it.rank, 0.0f, Nf4View{}};
+      }
+      need = std::max(need, small_fused_bwd_ws_bytes(small, n, M));
+    } else if (r.kind == kRunGroup && n > 1) {
+      TcBwdItem t[kTcGroupMax];
+      for (int k = 0; k < n; ++k) t[k] = tc_bwd_item(M, items[r.idx[k]], 0.0f, false);
+      need = std::max(need, tc_bwd_group_ws_bytes(t, n));
+    } else {
+      const qlora_bwd_item& it = items[r.idx[0]];
+      need = std::max(need, it.w16 != nullptr ? qlora_bwd_w16_workspace_bytes(M, it.N, it.K, it.rank, compute)
+                                              : bwd_ws(M, it.N, it.K, it.rank, compute));
     }
-    single = std::max(single, it.w16 != nullptr ? qlora_bwd_w16_workspace_bytes(M, it.N, it.K, it.rank, compute)
-                                                : bwd_ws(M, it.N, it.K, it.rank, compute));
   }
-  return std::max(single, std::max(fused, group));
+  return need;
 }
 
 nf4_status qlora_linear_bwd_batch(int64_t M, int32_t count, const qlora_bwd_item* items, nf4_dtype compute,
@@ -877,37 +995,44 @@ nf4_status qlora_linear_bwd_batch(int64_t M, int32_t count, const qlora_bwd_item
   if (ws == nullptr || ws_bytes < need) return NF4_ERR_WORKSPACE;
   if (!aligned16(ws)) return NF4_ERR_ALIGN;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  std::vector<SmallItem> small;
-  auto flush = [&]() -> nf4_status {
-    if (small.empty()) return NF4_OK;
-    const cudaError_t e = small_fused_backward(small.data(), static_cast<int>(small.size()), M, compute == NF4_F16,
-                                               ws, cs);
-    small.clear();
-    return from_cuda(e);
-  };
-  for (int32_t i = 0; i < count; ++i) {
-    const qlora_bwd_item& it = items[i];
-    if (M > 0 && small_w(M, it.N, it.K, it.rank, compute)) {
-      SmallItem si{};
-      si.a = LinearArgs{M, it.N, it.K, it.rank, s[i], it.w16 != nullptr ? Nf4View{} : view_of(it.W)};
-      si.x = it.x, si.A = it.A, si.B = it.B, si.T = const_cast<float*>(it.T), si.dy = it.dy, si.dx = it.dx;
-      si.dA = it.dA, si.dB = it.dB, si.w16 = it.w16;
-      small.push_back(si);
-      if (static_cast<int>(small.size()) == kSmallMaxGroup) {
-        const nf4_status st = flush();
+  const bool f16 = compute == NF4_F16;
+  int* status = nullptr;
+  for (const BatchRun& r : plan_bwd(M, count, items, compute)) {
+    const int n = static_cast<int>(r.idx.size());
+    const int i0 = r.idx[0];
+    cudaError_t e = cudaSuccess;
+    if (r.kind == kRunSmall) {
+      SmallItem small[kSmallMaxGroup];
+      for (int k = 0; k < n; ++k) {
+        const qlora_bwd_item& it = items[r.idx[k]];
+        SmallItem& si = small[k];
+        si = SmallItem{};
+        si.a = LinearArgs{M, it.N, it.K, it.rank, s[r.idx[k]], it.w16 != nullptr ? Nf4View{} : view_of(it.W)};
+        si.x = it.x, si.A = it.A, si.B = it.B, si.T = const_cast<float*>(it.T), si.dy = it.dy, si.dx = it.dx;
+        si.dA = it.dA, si.dB = it.dB, si.w16 = it.w16;
+      }
+      e = small_fused_backward(small, n, M, f16, ws, cs);
+    } else if (r.kind == kRunGroup && n > 1) {
+      if (status == nullptr) {
+        const nf4_status st = device_status_ptr(&status);
         if (st != NF4_OK) return st;
       }
-      continue;
+      TcBwdItem t[kTcGroupMax];
+      for (int k = 0; k < n; ++k) t[k] = tc_bwd_item(M, items[r.idx[k]], s[r.idx[k]]);
+      e = tc_backward_group(t, n, f16, items[i0].x, ws, status, cs);
+    } else {
+      const qlora_bwd_item& it = items[i0];
+      const nf4_status st =
+          it.w16 != nullptr
+              ? qlora_linear_bwd_w16(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.dy, it.x, it.T, it.w16,
+                                     it.A, it.B, it.dx, it.dA, it.dB, ws, ws_bytes, stream)
+              : qlora_linear_bwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.dy, it.x, it.T, it.W, it.A,
+                                 it.B, it.dx, it.dA, it.dB, ws, ws_bytes, stream);
+      if (st != NF4_OK) return st;
     }
-    const nf4_status st =
-        it.w16 != nullptr
-            ? qlora_linear_bwd_w16(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.dy, it.x, it.T, it.w16,
-                                   it.A, it.B, it.dx, it.dA, it.dB, ws, ws_bytes, stream)
-            : qlora_linear_bwd(M, it.N, it.K, it.rank, it.alpha, it.mode, compute, it.dy, it.x, it.T, it.W, it.A,
-                               it.B, it.dx, it.dA, it.dB, ws, ws_bytes, stream);
-    if (st != NF4_OK) return st;
+    if (e != cudaSuccess) return NF4_ERR_CUDA;
   }
-  return flush();
+  return NF4_OK;
 }
 
 nf4_status qlora_last_device_status(void* stream, int32_t clear) {

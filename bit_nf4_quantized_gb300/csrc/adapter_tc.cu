@@ -193,14 +193,17 @@ adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CU
   }
 }
 
-// out = scale * sum over slices (fixed order), for up to two passes in one launch.
-// Optional outputs: f32 [rows][r] (or transposed [r][rows] when f32_t), T16(scale_b * v)
-// [rows][rp] zero-padded, T16(v) transposed [nq][ldt] (entries past rows / r must
-// already be zero); T16 is IEEE half when f16, else bf16.
+// out = scale * sum over slices (fixed order), for up to kAdapterMaxOuts consumers of one or
+// two passes in one launch; a consumer takes columns [col0, col0 + r) of its pass's sums
+// (partial rows of pstride floats).  Optional outputs: f32 [rows][r] (or transposed
+// [r][rows] when f32_t), T16(scale_b * v) [rows][rp] zero-padded, T16(v) transposed
+// [nq][ldt] (entries past rows / r must already be zero); T16 is IEEE half when f16, else
+// bf16.
 struct FinishJob {
   const float* partial;
   int nsplit;
   int64_t rows;
+  int col0, pstride;
   int r;
   float scale;
   float* f32;
@@ -219,14 +222,16 @@ __device__ __forceinline__ void put16(void* base, int64_t i, float v, int f16) {
   else static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
 }
 struct FinishJobs {
-  FinishJob job[2];
+  FinishJob job[kAdapterMaxOuts];
   int n;
 };
 
 __global__ void finish_partials(const FinishJobs jobs) {
   pdl_allow_next();
   pdl_wait();
-  const FinishJob& f = (jobs.n > 1 && blockIdx.x >= jobs.job[1].first_block) ? jobs.job[1] : jobs.job[0];
+  int k = 0;
+  while (k + 1 < jobs.n && blockIdx.x >= jobs.job[k + 1].first_block) ++k;
+  const FinishJob& f = jobs.job[k];
   const int64_t i = static_cast<int64_t>(blockIdx.x - f.first_block) * blockDim.x + threadIdx.x;
   const int width = f.b_rows ? f.rp : f.r;
   const int64_t w = f.rows * width;
@@ -236,8 +241,8 @@ __global__ void finish_partials(const FinishJobs jobs) {
   float v = 0.0f;
   if (j < f.r) {
     // the slices in order, 8 loads in flight before their adds
-    const float* src = f.partial + row * f.r + j;
-    const int64_t stride = f.rows * f.r;
+    const float* src = f.partial + row * f.pstride + f.col0 + j;
+    const int64_t stride = f.rows * f.pstride;
     for (int sp0 = 0; sp0 < f.nsplit; sp0 += 8) {
       float t[8];
 #pragma unroll
@@ -321,21 +326,38 @@ bool setup_pass(const AdapterPassArgs& a, int target, int* status, SkinnyParams*
   return ok;
 }
 
-FinishJob finish_job(const AdapterPassArgs& a, const SkinnyParams& p) {
+// The finish of consumer `o` of a pass (o < 0: the pass's own output fields, all columns).
+FinishJob finish_job(const AdapterPassArgs& a, const SkinnyParams& p, int o) {
   FinishJob f{};
   f.partial = a.partial;
   f.nsplit = p.ctas / p.tiles;
   f.rows = a.rows;
-  f.r = a.r;
-  f.scale = a.scale;
-  f.f32 = a.f32;
-  f.f32_t = a.f32_t;
-  f.b_rows = a.b_rows;
-  f.rp = a.rp;
-  f.scale_b = a.scale_b;
-  f.b_t = a.b_t;
-  f.ldt = a.ldt;
+  f.pstride = a.r;
   f.f16 = a.f16;
+  if (o < 0) {
+    f.col0 = 0;
+    f.r = a.r;
+    f.scale = a.scale;
+    f.f32 = a.f32;
+    f.f32_t = a.f32_t;
+    f.b_rows = a.b_rows;
+    f.rp = a.rp;
+    f.scale_b = a.scale_b;
+    f.b_t = a.b_t;
+    f.ldt = a.ldt;
+  } else {
+    const AdapterOut& c = a.outs[o];
+    f.col0 = c.col0;
+    f.r = c.r;
+    f.scale = c.scale;
+    f.f32 = c.f32;
+    f.f32_t = c.f32_t;
+    f.b_rows = c.b_rows;
+    f.rp = c.rp;
+    f.scale_b = c.scale_b;
+    f.b_t = c.b_t;
+    f.ldt = c.ldt;
+  }
   return f;
 }
 
@@ -348,6 +370,15 @@ size_t adapter_partial_bytes(int64_t rows, int64_t red, int r) { return partial_
 cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
   if (n < 1 || n > 2) return cudaErrorInvalidValue;
+  int outs = 0;
+  for (int i = 0; i < n; ++i) {
+    if (a[i].nouts < 0 || (a[i].nouts > 0 && a[i].outs == nullptr)) return cudaErrorInvalidValue;
+    outs += a[i].nouts > 0 ? a[i].nouts : 1;
+    for (int o = 0; o < a[i].nouts; ++o)
+      if (a[i].outs[o].col0 < 0 || a[i].outs[o].r < 1 || a[i].outs[o].col0 + a[i].outs[o].r > a[i].r)
+        return cudaErrorInvalidValue;
+  }
+  if (outs > kAdapterMaxOuts) return cudaErrorInvalidValue;
   // the resident CTAs are shared in proportion to the activation bytes each pass reads
   const int total = resident_ctas();
   int target[2] = {total, 0};
@@ -378,12 +409,14 @@ cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream
   note_launch();
   if (e != cudaSuccess) return e;
   FinishJobs jobs{};
-  jobs.n = n;
   unsigned nblocks = 0;
   for (int i = 0; i < n; ++i) {
-    jobs.job[i] = finish_job(a[i], p[i]);
-    jobs.job[i].first_block = nblocks;
-    nblocks += blocks(a[i].rows * (a[i].b_rows ? a[i].rp : a[i].r));
+    for (int o = a[i].nouts > 0 ? 0 : -1; o < a[i].nouts; ++o) {
+      FinishJob& f = jobs.job[jobs.n++];
+      f = finish_job(a[i], p[i], o);
+      f.first_block = nblocks;
+      nblocks += blocks(f.rows * (f.b_rows ? f.rp : f.r));
+    }
   }
   e = launch_pdl(finish_partials, dim3(nblocks), dim3(256), 0, st, 1, jobs);
   note_launch();

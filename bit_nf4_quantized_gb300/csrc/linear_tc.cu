@@ -36,6 +36,7 @@
 // wait and the partial-sum flag wait is bounded in time; a wait that gives up sets
 // NF4_ERR_TIMEOUT in the status word and the CTA winds down, freeing its TMEM.
 #include <algorithm>
+#include <vector>
 
 #include <cuda_fp16.h>
 
@@ -623,6 +624,189 @@ GemmParams base_params(const LinearArgs& a, bool f16, int mode, void* out, int* 
   return p;
 }
 
+// The forward GEMM y = x W^T + (s T) B^T of one projection: W 16-bit [N][K] (wb), B's
+// staged copy Bp [N][rp], 16-bit s T sTp [M][rp]; part / flags for split tiles.
+cudaError_t fwd_gemm(const LinearArgs& a, bool f16, const void* x, const void* wb, const void* Bp, const void* sTp,
+                     void* part, void* flags, void* y, int* status, cudaStream_t st) {
+  const int rp = padded_rank(a.r);
+  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap wm, tok, slab_f, slab_t;
+  bool ok = make_map(&wm, dt16, wb, a.K, a.N, 2 * a.K, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tok, dt16, x, a.K, a.M, 2 * a.K, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_f, dt16, Bp, rp, a.N, 2 * rp, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_t, dt16, sTp, rp, a.M, 2 * rp, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  GemmParams gp = base_params(a, f16, 0, y, status);
+  gp.part_ws = static_cast<float*>(part);
+  gp.part_tickets = static_cast<int*>(flags);
+  return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
+}
+
+// The dX GEMM dX = dY W + (s G) A of one projection: A's staged copy ApT [K][rp], 16-bit
+// s G sGp [M][rp].
+cudaError_t dx_gemm(const LinearArgs& a, bool f16, const void* dy, const void* wb, const void* ApT, const void* sGp,
+                    void* part, void* flags, void* dx, int* status, cudaStream_t st) {
+  const int rp = padded_rank(a.r);
+  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap wm, tok, slab_f, slab_t;
+  // W [N][K] read as 64 features x 64 rows n (MN-major A: the features are the MMA's M)
+  bool ok = make_map(&wm, dt16, wb, a.K, a.N, 2 * a.K, kSub, kSub, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&tok, dt16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_f, dt16, ApT, rp, a.K, 2 * rp, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map(&slab_t, dt16, sGp, rp, a.M, 2 * rp, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  GemmParams gp = base_params(a, f16, 1, dx, status);
+  gp.part_ws = static_cast<float*>(part);
+  gp.part_tickets = static_cast<int*>(flags);
+  return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
+}
+
+// The backward's staging jobs of one projection (B^T, T^T, A^T and the GEMM's flags) and,
+// when Gt_zero, the zeroed G^T [nq][Mp].
+void bwd_prep_jobs(const LinearArgs& a, const float* T, const float* A, const float* B, const BwdWs& L, char* w,
+                   bool Gt_zero, std::vector<PrepJob>* jobs) {
+  const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
+  const int64_t Mp = pad8(a.M);
+  PrepJob j{};
+  j.kind = kStageTransposed;   // B^T: [nq][N]
+  j.r = a.r;
+  j.width = a.N;
+  j.src = B;
+  j.dst = w + L.Bt;
+  j.cols = a.N;
+  j.count = static_cast<int64_t>(nq) * a.N;
+  jobs->push_back(j);
+  PrepJob t = j;               // T^T: [nq][Mp]
+  t.width = Mp;
+  t.src = T;
+  t.dst = w + L.Tt;
+  t.cols = a.M;
+  t.count = static_cast<int64_t>(nq) * Mp;
+  jobs->push_back(t);
+  if (Gt_zero) {
+    PrepJob g = t;             // G^T starts zero; the G finish fills rows < r, columns < M
+    g.r = 0;
+    g.dst = w + L.Gt;
+    jobs->push_back(g);
+  }
+  PrepJob c{};
+  c.kind = kStageColumns;      // A^T as the slab's feature side: [K][rp]
+  c.r = a.r;
+  c.width = rp;
+  c.src = A;
+  c.dst = w + L.ApT;
+  c.cols = a.K;
+  c.count = a.K * rp;
+  jobs->push_back(c);
+  jobs->push_back(zero_flags_job(w + L.flags));
+}
+
+// One launch for G = dY B (rows M, reduction over N along dY's rows; G, 16-bit s G, 16-bit
+// G^T into Gt with row stride ldt) and dB = s dY^T T (rows N, reduction over M down dY's
+// columns), then one for both finishes.
+cudaError_t gdb_pass(const LinearArgs& a, bool f16, const void* dy, float* G, float* dB, const BwdWs& L, char* w,
+                     void* Gt, int64_t ldt, int* status, cudaStream_t st) {
+  const int rp = padded_rank(a.r);
+  const int64_t Mp = pad8(a.M);
+  auto* part = reinterpret_cast<float*>(w + L.part);
+  AdapterPassArgs pa[2] = {};
+  AdapterPassArgs& g = pa[0];
+  g.X = dy;
+  g.x_inner = a.N;
+  g.x_outer = a.M;
+  g.Q = w + L.Bt;
+  g.q_cols = a.N;
+  g.r = a.r;
+  g.rows = a.M;
+  g.red = a.N;
+  g.partial = part;
+  g.scale = 1.0f;
+  g.f32 = G;
+  g.b_rows = w + L.sGp;
+  g.rp = rp;
+  g.scale_b = a.s;
+  g.b_t = Gt;
+  g.ldt = ldt;
+  AdapterPassArgs& d = pa[1];
+  d.X = dy;
+  d.x_inner = a.N;
+  d.x_outer = a.M;
+  d.mn_major = true;
+  d.Q = w + L.Tt;
+  d.q_cols = Mp;
+  d.r = a.r;
+  d.rows = a.N;
+  d.red = a.M;
+  d.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(part) + adapter_partial_bytes(a.M, a.N, a.r));
+  d.scale = a.s;
+  d.f32 = dB;
+  g.f16 = d.f16 = f16 ? 1 : 0;
+  return adapter_run(pa, 2, status, st);
+}
+
+// Staging jobs in launches of at most kMaxPrepJobs each.
+cudaError_t run_prep(const std::vector<PrepJob>& jobs, bool f16, cudaStream_t st) {
+  for (size_t j0 = 0; j0 < jobs.size(); j0 += kMaxPrepJobs) {
+    PrepBuilder b(f16);
+    for (size_t j = j0; j < jobs.size() && j < j0 + kMaxPrepJobs; ++j) b.add(jobs[j]);
+    if (!b.ok()) return cudaErrorInvalidValue;
+    const cudaError_t e = launch_prep_only(f16, b.jobs(), b.ctas(), st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Group workspaces: each item's single-call layout, then the group's stacked rank side and
+// the shared pass's partial sums (and, backward, each item's fp32 G first).
+struct FwdGroupWs {
+  size_t item[kTcGroupMax] = {};
+  size_t Aq = 0, part = 0, total = 0;
+  int nqt = 0;
+  FwdGroupWs(const TcFwdItem* it, int n) {
+    size_t off = 0;
+    for (int i = 0; i < n; ++i) {
+      const LinearArgs& a = it[i].a;
+      item[i] = off;
+      off += a1024(FwdWs(a.M, a.N, a.K, a.r, it[i].w16 != nullptr).total);
+      nqt += adapter_nq(a.r);
+    }
+    Aq = off;
+    part = Aq + a1024(2 * static_cast<size_t>(nqt) * it[0].a.K);
+    total = part + a1024(adapter_partial_bytes(it[0].a.M, it[0].a.K, nqt));
+  }
+};
+
+struct BwdGroupWs {
+  size_t G[kTcGroupMax] = {}, item[kTcGroupMax] = {};
+  size_t Gt = 0, part = 0, total = 0;
+  int nqt = 0;
+  BwdGroupWs(const TcBwdItem* it, int n) {
+    size_t off = 0;
+    for (int i = 0; i < n; ++i) {
+      const LinearArgs& a = it[i].a;
+      G[i] = off;
+      off += a1024(sizeof(float) * static_cast<size_t>(a.M) * a.r);
+      item[i] = off;
+      off += a1024(BwdWs(a.M, a.N, a.K, a.r, it[i].w16 != nullptr).total);
+      nqt += adapter_nq(a.r);
+    }
+    Gt = off;
+    part = Gt + a1024(2 * static_cast<size_t>(nqt) * pad8(it[0].a.M));
+    total = part + a1024(adapter_partial_bytes(it[0].a.K, it[0].a.M, nqt));
+  }
+};
+
+// Every item reads x [M][K] with the same M and K; the padded ranks fit one skinny pass.
+bool group_ok(const LinearArgs* const* a, int n) {
+  if (n < 1 || n > kTcGroupMax) return false;
+  int nqt = 0;
+  for (int i = 0; i < n; ++i) {
+    if (a[i]->M != a[0]->M || a[i]->K != a[0]->K) return false;
+    nqt += adapter_nq(a[i]->r);
+  }
+  return nqt <= kTcGroupMaxRank;
+}
+
 }  // namespace
 
 size_t tc_fwd_ws_bytes(int64_t M, int64_t N, int64_t K, int r, bool w16) { return FwdWs(M, N, K, r, w16).total; }
@@ -641,7 +825,6 @@ cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float
   auto* part = reinterpret_cast<float*>(w + L.part);
   const void* wb = w16 != nullptr ? w16 : w + L.wb;
   const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
-  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   PrepBuilder prep(f16);
   {
     PrepJob j{};
@@ -684,16 +867,7 @@ cudaError_t tc_forward(const LinearArgs& a, bool f16, const void* x, const float
     t.f16 = f16 ? 1 : 0;
     if ((e = adapter_run(&t, 1, status, st)) != cudaSuccess) return e;
   }
-  CUtensorMap wm, tok, slab_f, slab_t;
-  bool ok = make_map(&wm, dt16, wb, a.K, a.N, 2 * a.K, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tok, dt16, x, a.K, a.M, 2 * a.K, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_f, dt16, Bp, rp, a.N, 2 * rp, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_t, dt16, sTp, rp, a.M, 2 * rp, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return cudaErrorInvalidValue;
-  GemmParams gp = base_params(a, f16, 0, y, status);
-  gp.part_ws = part;
-  gp.part_tickets = reinterpret_cast<int*>(w + L.flags);
-  return launch_gemm(gp, wm, tok, slab_f, slab_t, st);
+  return fwd_gemm(a, f16, x, wb, Bp, sTp, part, w + L.flags, y, status, st);
 }
 
 // Backward: W in bf16 with prep (B^T, T^T, zeroed G^T, A^T in bf16) -> G = dY B ->
@@ -704,106 +878,26 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
                         int* status, cudaStream_t st, const void* w16) {
   const BwdWs L(a.M, a.N, a.K, a.r, w16 != nullptr);
   char* w = static_cast<char*>(ws);
-  void* sGp = w + L.sGp;
-  void* ApT = w + L.ApT;
-  void* Bt = w + L.Bt;
-  void* Tt = w + L.Tt;
-  void* Gt = w + L.Gt;
   auto* part = reinterpret_cast<float*>(w + L.part);
   const void* wb = w16 != nullptr ? w16 : w + L.wb;
-  const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
-  const int64_t Mp = pad8(a.M);
-  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   PrepBuilder prep(f16);
   {
-    PrepJob j{};
-    j.kind = kStageTransposed;   // B^T: [nq][N]
-    j.r = a.r;
-    j.width = a.N;
-    j.src = B;
-    j.dst = Bt;
-    j.cols = a.N;
-    j.count = static_cast<int64_t>(nq) * a.N;
-    prep.add(j);
-    PrepJob t = j;               // T^T: [nq][Mp]
-    t.width = Mp;
-    t.src = T;
-    t.dst = Tt;
-    t.cols = a.M;
-    t.count = static_cast<int64_t>(nq) * Mp;
-    prep.add(t);
-    PrepJob g = t;               // G^T starts zero; the G finish fills rows < r, columns < M
-    g.r = 0;
-    g.dst = Gt;
-    prep.add(g);
-    PrepJob c{};
-    c.kind = kStageColumns;      // A^T as the slab's feature side: [K][rp]
-    c.r = a.r;
-    c.width = rp;
-    c.src = A;
-    c.dst = ApT;
-    c.cols = a.K;
-    c.count = a.K * rp;
-    prep.add(c);
-    prep.add(zero_flags_job(w + L.flags));
+    std::vector<PrepJob> jobs;
+    bwd_prep_jobs(a, T, A, B, L, w, true, &jobs);
+    for (const PrepJob& j : jobs) prep.add(j);
   }
   cudaError_t e = decode_weight(a, f16, w + L.wb, prep, st, w16);
   if (e != cudaSuccess) return e;
-  {  // one launch for G = dY B (rows M, reduction over N along dY's rows; G, bf16(s G), bf16(G)^T)
-     // and dB = s dY^T T (rows N, reduction over M down dY's columns), then one for both finishes
-    AdapterPassArgs pa[2] = {};
-    AdapterPassArgs& g = pa[0];
-    g.X = dy;
-    g.x_inner = a.N;
-    g.x_outer = a.M;
-    g.Q = Bt;
-    g.q_cols = a.N;
-    g.r = a.r;
-    g.rows = a.M;
-    g.red = a.N;
-    g.partial = part;
-    g.scale = 1.0f;
-    g.f32 = G;
-    g.b_rows = sGp;
-    g.rp = rp;
-    g.scale_b = a.s;
-    g.b_t = Gt;
-    g.ldt = Mp;
-    AdapterPassArgs& d = pa[1];
-    d.X = dy;
-    d.x_inner = a.N;
-    d.x_outer = a.M;
-    d.mn_major = true;
-    d.Q = Tt;
-    d.q_cols = Mp;
-    d.r = a.r;
-    d.rows = a.N;
-    d.red = a.M;
-    d.partial = reinterpret_cast<float*>(reinterpret_cast<char*>(part) + adapter_partial_bytes(a.M, a.N, a.r));
-    d.scale = a.s;
-    d.f32 = dB;
-    g.f16 = d.f16 = f16 ? 1 : 0;
-    if ((e = adapter_run(pa, 2, status, st)) != cudaSuccess) return e;
-  }
-  CUtensorMap wm, tok, slab_f, slab_t;
-  // W [N][K] read as 64 features x 64 rows n (MN-major A: the features are the MMA's M)
-  bool ok = make_map(&wm, dt16, wb, a.K, a.N, 2 * a.K, kSub, kSub, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&tok, dt16, dy, a.N, a.M, 2 * a.N, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_f, dt16, ApT, rp, a.K, 2 * rp, kSub, kTileF, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map(&slab_t, dt16, sGp, rp, a.M, 2 * rp, kSub, kHalfT, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return cudaErrorInvalidValue;
-  GemmParams gp = base_params(a, f16, 1, dx, status);
-  gp.part_ws = part;
-  gp.part_tickets = reinterpret_cast<int*>(w + L.flags);
-  if ((e = launch_gemm(gp, wm, tok, slab_f, slab_t, st)) != cudaSuccess) return e;
+  if ((e = gdb_pass(a, f16, dy, G, dB, L, w, w + L.Gt, pad8(a.M), status, st)) != cudaSuccess) return e;
+  if ((e = dx_gemm(a, f16, dy, wb, w + L.ApT, w + L.sGp, part, w + L.flags, dx, status, st)) != cudaSuccess) return e;
   // dA = s G^T x: rows K, reduction over M down x's columns; written as [r][K]
   AdapterPassArgs da{};
   da.X = x;
   da.x_inner = a.K;
   da.x_outer = a.M;
   da.mn_major = true;
-  da.Q = Gt;
-  da.q_cols = Mp;
+  da.Q = w + L.Gt;
+  da.q_cols = pad8(a.M);
   da.r = a.r;
   da.rows = a.K;
   da.red = a.M;
@@ -812,6 +906,186 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
   da.f32 = dA;
   da.f32_t = 1;
   da.f16 = f16 ? 1 : 0;
+  return adapter_run(&da, 1, status, st);
+}
+
+size_t tc_fwd_group_ws_bytes(const TcFwdItem* it, int n) {
+  if (n < 1 || n > kTcGroupMax) return 0;
+  return FwdGroupWs(it, n).total;
+}
+
+size_t tc_bwd_group_ws_bytes(const TcBwdItem* it, int n) {
+  if (n < 1 || n > kTcGroupMax) return 0;
+  return BwdGroupWs(it, n).total;
+}
+
+bool tc_groupable(const LinearArgs* const* a, int n) { return group_ok(a, n); }
+
+// Forward of a group reading one x: the NF4 weights decoded by one batched launch, the
+// staging of every item, one T pass over x for all of them (Q = the items' A, each padded
+// to 16 rows, stacked), then each item's GEMM.
+cudaError_t tc_forward_group(const TcFwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
+                             cudaStream_t st) {
+  const LinearArgs* args[kTcGroupMax];
+  for (int i = 0; i < n && i < kTcGroupMax; ++i) args[i] = &it[i].a;
+  if (!group_ok(args, n)) return cudaErrorInvalidValue;
+  const FwdGroupWs Gw(it, n);
+  char* w = static_cast<char*>(ws);
+  const int64_t M = it[0].a.M, K = it[0].a.K;
+  std::vector<PrepJob> jobs;
+  Nf4View views[kTcGroupMax];
+  void* outs[kTcGroupMax];
+  AdapterOut tout[kTcGroupMax];
+  int m = 0, col = 0;
+  for (int i = 0; i < n; ++i) {
+    const LinearArgs& a = it[i].a;
+    const FwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
+    char* wi = w + Gw.item[i];
+    const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
+    PrepJob j{};
+    j.kind = kStageRowsDirect;   // A as rows col .. col + nq of the stacked Q: [nqt][K]
+    j.r = a.r;
+    j.src = it[i].A;
+    j.dst = w + Gw.Aq + 2 * static_cast<size_t>(col) * K;
+    j.cols = K;
+    j.count = static_cast<int64_t>(nq) * K;
+    jobs.push_back(j);
+    PrepJob b{};
+    b.kind = kStageRows;         // B as the slab's feature side: [N][rp]
+    b.r = a.r;
+    b.width = rp;
+    b.scale = 1.0f;
+    b.src = it[i].B;
+    b.dst = wi + L.Bp;
+    b.count = a.N * rp;
+    jobs.push_back(b);
+    jobs.push_back(zero_flags_job(wi + L.flags));
+    if (it[i].w16 == nullptr) {
+      views[m] = a.W;
+      outs[m] = wi + L.wb;
+      ++m;
+    }
+    AdapterOut& o = tout[i];
+    o = AdapterOut{};
+    o.col0 = col;
+    o.r = a.r;
+    o.scale = 1.0f;
+    o.f32 = it[i].T;
+    o.b_rows = wi + L.sTp;
+    o.rp = rp;
+    o.scale_b = a.s;
+    col += nq;
+  }
+  cudaError_t e = cudaSuccess;
+  if (m > 0) {
+    KernelTimer timer(NF4_TIME_WEIGHT_DECODE, st);
+    e = launch_dequantize_batch(views, outs, m, f16 ? NF4_F16 : NF4_BF16, st);
+  }
+  if (e == cudaSuccess) e = run_prep(jobs, f16, st);
+  if (e != cudaSuccess) return e;
+  AdapterPassArgs t{};
+  t.X = x;
+  t.x_inner = K;
+  t.x_outer = M;
+  t.Q = w + Gw.Aq;
+  t.q_cols = K;
+  t.r = Gw.nqt;
+  t.rows = M;
+  t.red = K;
+  t.partial = reinterpret_cast<float*>(w + Gw.part);
+  t.f16 = f16 ? 1 : 0;
+  t.outs = tout;
+  t.nouts = n;
+  if ((e = adapter_run(&t, 1, status, st)) != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i) {
+    const LinearArgs& a = it[i].a;
+    const FwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
+    char* wi = w + Gw.item[i];
+    const void* wb = it[i].w16 != nullptr ? it[i].w16 : wi + L.wb;
+    e = fwd_gemm(a, f16, x, wb, wi + L.Bp, wi + L.sTp, wi + L.part, wi + L.flags, it[i].y, status, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Backward of a group reading one x: decode and staging as above (one zeroed G^T for the
+// group, [nqt][Mp]), each item's G and dB pass (its 16-bit G^T into its rows of the group's
+// G^T) and dX GEMM, then one dA pass over x for all of them.
+cudaError_t tc_backward_group(const TcBwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
+                              cudaStream_t st) {
+  const LinearArgs* args[kTcGroupMax];
+  for (int i = 0; i < n && i < kTcGroupMax; ++i) args[i] = &it[i].a;
+  if (!group_ok(args, n)) return cudaErrorInvalidValue;
+  const BwdGroupWs Gw(it, n);
+  char* w = static_cast<char*>(ws);
+  const int64_t M = it[0].a.M, K = it[0].a.K, Mp = pad8(M);
+  std::vector<PrepJob> jobs;
+  {
+    PrepJob g{};                 // the group's G^T starts zero
+    g.kind = kStageTransposed;
+    g.r = 0;
+    g.width = Mp;
+    g.dst = w + Gw.Gt;
+    g.cols = M;
+    g.count = static_cast<int64_t>(Gw.nqt) * Mp;
+    jobs.push_back(g);
+  }
+  Nf4View views[kTcGroupMax];
+  void* outs[kTcGroupMax];
+  AdapterOut aout[kTcGroupMax];
+  int m = 0, col = 0;
+  for (int i = 0; i < n; ++i) {
+    const LinearArgs& a = it[i].a;
+    const BwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
+    char* wi = w + Gw.item[i];
+    bwd_prep_jobs(a, it[i].T, it[i].A, it[i].B, L, wi, false, &jobs);
+    if (it[i].w16 == nullptr) {
+      views[m] = a.W;
+      outs[m] = wi + L.wb;
+      ++m;
+    }
+    AdapterOut& o = aout[i];
+    o = AdapterOut{};
+    o.col0 = col;
+    o.r = a.r;
+    o.scale = a.s;
+    o.f32 = it[i].dA;
+    o.f32_t = 1;
+    col += adapter_nq(a.r);
+  }
+  cudaError_t e = cudaSuccess;
+  if (m > 0) {
+    KernelTimer timer(NF4_TIME_WEIGHT_DECODE, st);
+    e = launch_dequantize_batch(views, outs, m, f16 ? NF4_F16 : NF4_BF16, st);
+  }
+  if (e == cudaSuccess) e = run_prep(jobs, f16, st);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i) {
+    const LinearArgs& a = it[i].a;
+    const BwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
+    char* wi = w + Gw.item[i];
+    const void* wb = it[i].w16 != nullptr ? it[i].w16 : wi + L.wb;
+    void* Gt_i = w + Gw.Gt + 2 * static_cast<size_t>(aout[i].col0) * Mp;
+    auto* G = reinterpret_cast<float*>(w + Gw.G[i]);
+    if ((e = gdb_pass(a, f16, it[i].dy, G, it[i].dB, L, wi, Gt_i, Mp, status, st)) != cudaSuccess) return e;
+    e = dx_gemm(a, f16, it[i].dy, wb, wi + L.ApT, wi + L.sGp, wi + L.part, wi + L.flags, it[i].dx, status, st);
+    if (e != cudaSuccess) return e;
+  }
+  // dA of every item: rows K, reduction over M down x's columns, Q = the group's G^T
+  AdapterPassArgs da{};
+  da.X = x;
+  da.x_inner = K;
+  da.x_outer = M;
+  da.mn_major = true;
+  da.Q = w + Gw.Gt;
+  da.q_cols = Mp;
+  da.r = Gw.nqt;
+  da.rows = K;
+  da.red = M;
+  da.partial = reinterpret_cast<float*>(w + Gw.part);
+  da.f16 = f16 ? 1 : 0;
+  da.outs = aout;
+  da.nouts = n;
   return adapter_run(&da, 1, status, st);
 }
 

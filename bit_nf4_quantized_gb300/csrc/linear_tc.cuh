@@ -19,6 +19,43 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G,
                         void* ws, int* status, cudaStream_t st, const void* w16 = nullptr);
 
+// Groups of projections that read the same input x [M][K] (the same M and K; e.g. a
+// layer's q, k and v, or gate and up): one skinny pass over x computes T for every item of
+// a forward group, and one computes dA for every item of a backward group, with Q stacking
+// the items' rank sides (each padded to 16 rows; at most kTcGroupMaxRank rows in all).
+// Everything else is what the single calls do, and every output is bit for bit the single
+// call's.  w16: the item's weight decoded to 16 bits, or nullptr (a.W is decoded, all such
+// items of the group in one batched launch).  The group's workspace holds each item's
+// single-call workspace (w16-aware) and the shared pass's buffers.
+constexpr int kTcGroupMax = 8;
+constexpr int kTcGroupMaxRank = 256;
+struct TcFwdItem {
+  LinearArgs a;
+  const float* A;
+  const float* B;
+  void* y;
+  float* T;
+  const void* w16;
+};
+struct TcBwdItem {
+  LinearArgs a;
+  const void* dy;
+  const float* T;
+  const float* A;
+  const float* B;
+  void* dx;
+  float* dA;
+  float* dB;
+  const void* w16;
+};
+bool tc_groupable(const LinearArgs* const* a, int n);
+size_t tc_fwd_group_ws_bytes(const TcFwdItem* it, int n);
+size_t tc_bwd_group_ws_bytes(const TcBwdItem* it, int n);
+cudaError_t tc_forward_group(const TcFwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
+                             cudaStream_t st);
+cudaError_t tc_backward_group(const TcBwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
+                              cudaStream_t st);
+
 // stream_fwd.cu: the forward for at most kStreamMaxM tokens, for up to kStreamMaxGroup
 // projections (sharing M) in two launches: T by lora_down_small, then one persistent pass that
 // streams every projection's stored weight once, decodes it in registers straight into
@@ -70,6 +107,21 @@ cudaError_t small_fused_backward(const SmallItem* items, int n, int64_t M, bool 
 //   f32 = scale * sum as [rows][r] (or [r][rows] when f32_t), if f32 is set;
 //   T16(scale_b * sum) as [rows][rp], zero past r, if b_rows is set;
 //   T16(sum) as [r][ldt] (rows r.. of a [nq][ldt] buffer untouched), if b_t is set.
+// A pass may instead serve several consumers that share X (the projections of a layer that
+// read the same input): Q stacks their rank sides, and `outs` lists, for each consumer, its
+// columns [col0, col0 + r) of the sums with its own outputs as above.
+struct AdapterOut {
+  int col0, r;
+  float scale;
+  float* f32;
+  int f32_t;
+  void* b_rows;
+  int rp;
+  float scale_b;
+  void* b_t;
+  int64_t ldt;
+};
+constexpr int kAdapterMaxOuts = 8;
 struct AdapterPassArgs {
   const void* X;
   int64_t x_inner, x_outer;
@@ -88,11 +140,13 @@ struct AdapterPassArgs {
   void* b_t;
   int64_t ldt;
   int f16;
+  const AdapterOut* outs;   // nouts consumers (at most kAdapterMaxOuts); 0: the fields above
+  int nouts;
 };
 int adapter_nq(int r);
 size_t adapter_partial_bytes(int64_t rows, int64_t red, int r);
 // One or two independent passes (n = 1 or 2, separate `partial` buffers) in one launch,
-// then their finishes in one more.
+// then their finishes (at most kAdapterMaxOuts outputs in all) in one more.
 cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream_t st);
 
 }  // namespace qnf4

@@ -31,6 +31,11 @@ W2 = dict(name="SmolLM2-135M-shaped 30-layer stack, QLoRA q,v, M=512, r=16, alph
 LLAMA8B_LAYER = [("q_proj", 4096, 4096), ("k_proj", 1024, 4096), ("v_proj", 1024, 4096),
                  ("o_proj", 4096, 4096), ("gate_proj", 14336, 4096), ("up_proj", 14336, 4096),
                  ("down_proj", 4096, 14336)]
+# The activation each projection of a transformer layer reads: q, k and v read the attention
+# block's normalised input, gate and up the MLP block's, o the attention output, down the MLP's
+# gated activation.  Projections that read the same activation get one shared x.
+LAYER_INPUTS = {"q_proj": "attn_in", "k_proj": "attn_in", "v_proj": "attn_in", "o_proj": "attn_out",
+                "gate_proj": "mlp_in", "up_proj": "mlp_in", "down_proj": "mlp_act"}
 W3 = dict(name="Llama-3-8B-shaped layer, 7 QLoRA targets, M=4096 (2x2048), r=16, alpha=16, bf16",
           shapes=LLAMA8B_LAYER, M=4096, r=16, alpha=16.0, w_scale=0.02, t_df=5, compute="bf16")
 

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define QLORA_NF4_ABI_VERSION 4
+#define QLORA_NF4_ABI_VERSION 5
 
 typedef enum {
   NF4_OK = 0,
@@ -230,24 +230,34 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
 
 /* Forward of several projections that share M and the compute dtype, for example the seven
  * projections of one transformer layer ([GATE] "Shape-matched ceilings": q, k, v, o, gate, up,
- * down).  Item i computes exactly what qlora_linear_fwd computes for its arguments.
- * With compute = NF4_BF16 and M <= 16, up to 8 items run as one pair of launches (T for every
- * item, then one persistent pass over all their stored weights); more items run in groups of
- * 8.  Otherwise the items run one after another with the single-call path.  Items must not
- * write to memory another item reads.  ws: qlora_fwd_batch_workspace_bytes() bytes.
- * Each item is validated as qlora_linear_fwd validates its arguments; the first failing
- * item's status is returned and nothing is enqueued. */
+ * down).  Item i computes exactly what qlora_linear_fwd (w16 == NULL) or qlora_linear_fwd_w16
+ * (w16 != NULL: W decoded as nf4_dequantize writes it; W may then be NULL) computes for its
+ * arguments, bit for bit.
+ *   - compute = NF4_BF16 or NF4_F16, M <= 16, items given as NF4: up to 8 run as one pair of
+ *     launches (T for every item, then one persistent pass over all their stored weights).
+ *   - 16-bit compute, small weights (M > 16, K and N at most 1024, N*K at most 2^21, rank at
+ *     most 32): up to 8 at a time in one launch.
+ *   - 16-bit compute, the other items (the tiled tensor-core path): consecutive such items
+ *     that read the same x (the same pointer and K) form groups of up to 8 whose ranks,
+ *     each rounded up to 16, add up to at most 256 (a layer's q, k and v; gate and up).  A
+ *     group decodes its NF4 weights in one launch and computes T for all its items in one
+ *     pass over x, then runs each item's GEMM.  A group of one is the single call.
+ *   - anything else runs the single call.
+ * Items must not write to memory another item reads.  ws: qlora_fwd_batch_workspace_bytes()
+ * bytes.  Each item is validated as the single call validates it; the first failing item's
+ * status is returned and nothing is enqueued. */
 typedef struct {
   int64_t N, K;
   int32_t rank;
   float alpha;
   qlora_scale_mode mode;
-  const nf4_tensor* W;    /* numel N*K, [N, K] row-major */
+  const nf4_tensor* W;    /* numel N*K, [N, K] row-major; or NULL with w16 */
   const float* A;         /* [rank, K] fp32 */
   const float* B;         /* [N, rank] fp32 */
   const void* x;          /* [M, K] in the compute dtype */
   void* y;                /* [M, N] in the compute dtype */
   float* T_out;           /* [M, rank] fp32 */
+  const void* w16;        /* [N, K] decoded in the compute dtype (16-bit compute only), or NULL */
 } qlora_fwd_item;
 
 size_t qlora_fwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_fwd_item* items, nf4_dtype compute);
@@ -294,14 +304,17 @@ nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
                                 void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of several projections that share M and the compute dtype, e.g. the projections of
- * one layer that read the same x (q and v): item i computes exactly what qlora_linear_bwd (w16
- * == NULL) or qlora_linear_bwd_w16 (w16 != NULL: W decoded as nf4_dequantize writes it)
- * computes for its arguments; W may be NULL when w16 is given.  Items with small weights
- * (16-bit compute, M > 16, K and N at most 1024, N*K at most 2^21, rank at most 32) run up to
- * 8 at a time in one pair of launches; the others run one call each.  Items must not write to
- * memory another item reads.  ws: qlora_bwd_batch_workspace_bytes() bytes.  Each item is
- * validated as the single call validates it; the first failing item's status is returned and
- * nothing is enqueued. */
+ * one layer that read the same x (q, k and v): item i computes exactly what qlora_linear_bwd
+ * (w16 == NULL) or qlora_linear_bwd_w16 (w16 != NULL: W decoded as nf4_dequantize writes it)
+ * computes for its arguments, bit for bit; W may be NULL when w16 is given.  Items with small
+ * weights (16-bit compute, M > 16, K and N at most 1024, N*K at most 2^21, rank at most 32)
+ * run up to 8 at a time in one pair of launches.  Other 16-bit items form groups as in
+ * qlora_linear_fwd_batch (consecutive, the same x and K, up to 8, padded ranks at most 256
+ * in all): each item's G, dB and dX as in the single call, then dA for all the group's items
+ * in one pass over x.  The others run one call each.  Items must not write to memory another
+ * item reads.  ws: qlora_bwd_batch_workspace_bytes() bytes.  Each item is validated as the
+ * single call validates it; the first failing item's status is returned and nothing is
+ * enqueued. */
 typedef struct {
   int64_t N, K;
   int32_t rank;

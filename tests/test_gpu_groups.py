@@ -1,0 +1,113 @@
+"""Grouped calls on the tiled tensor-core path: consecutive items of qlora_linear_fwd_batch /
+qlora_linear_bwd_batch that read the same x share one skinny pass over x (T in the forward,
+dA in the backward).  Every output must equal the single call's bit for bit; the single
+calls are themselves checked against the oracle in tests/test_gpu_linear.py, so equality
+carries that parity over to the groups.  The launch counts show that the grouping happened.
+"""
+
+import pytest
+import torch
+
+from bit_nf4_quantized_gb300 import binding
+from bit_nf4_quantized_gb300 import workloads as wl
+from oracle import nf4 as onf4
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _weight(N, K, seed):
+    ref = onf4.quantize(wl.normal((N, K), 0.02, 2, seed), double_quant=True)
+    q = binding.Nf4Tensor.empty((N, K), True, DEV)
+    q.packed.copy_(torch.from_numpy(ref["packed"]))
+    q.absmax.copy_(torch.from_numpy(ref["absmax"]))
+    q.nested_absmax.copy_(torch.from_numpy(ref["nested"]))
+    q.offset[0] = float(ref["offset"])
+    return q
+
+
+def _same(a, b):
+    if a.dtype in (torch.bfloat16, torch.float16):
+        return torch.equal(a.view(torch.int16), b.view(torch.int16))
+    return torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def _check_group(M, specs, seed, dtype=torch.bfloat16, device_weights=False):
+    """specs: per item (N, K, r, alpha, mode, x_id, decoded).  Runs one forward batch and one
+    backward batch over all items, and each item's single NF4-input calls; compares all.
+    device_weights: the stored weights come from nf4_quantize on the device (large shapes;
+    both sides read the same stored weight either way)."""
+    xs = {}
+    items_f, items_b, want_f, want_b = [], [], [], []
+    for i, (N, K, r, alpha, mode, xid, decoded) in enumerate(specs):
+        if xid not in xs:
+            xs[xid] = torch.from_numpy(wl.normal((M, K), 1.0, 1, seed + 500 + xid)).to(DEV).to(dtype)
+        x = xs[xid]
+        if device_weights:
+            w = wl.device_student_t((N, K), 5, 0.02, seed + 10 * i, DEV, torch.bfloat16)
+            q = binding.nf4_quantize(w, True)
+        else:
+            q = _weight(N, K, seed + 10 * i)
+        A, B = (torch.from_numpy(t).to(DEV) for t in wl.adapters(N, K, r, 1, seed + 10 * i + 1))
+        dy = torch.from_numpy(wl.normal((M, N), 1.0, 1, seed + 10 * i + 3)).to(DEV).to(dtype)
+        y1, T1 = binding.qlora_linear_fwd(x, q, A, B, alpha, mode)
+        want_f.append((y1, T1))
+        want_b.append(binding.qlora_linear_bwd(dy, x, T1, q, A, B, alpha, mode))
+        wsrc = dict(w16=binding.nf4_dequantize(q, dtype)) if decoded else dict(W=q)
+        items_f.append(dict(x=x, A=A, B=B, alpha=alpha, mode=mode, **wsrc))
+        items_b.append(dict(dy=dy, x=x, T=T1, A=A, B=B, alpha=alpha, mode=mode, **wsrc))
+    torch.cuda.synchronize()
+    n0 = binding.launch_count()
+    got_f = binding.qlora_linear_fwd_batch(items_f)
+    n1 = binding.launch_count()
+    got_b = binding.qlora_linear_bwd_batch(items_b)
+    n2 = binding.launch_count()
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    for i, ((y, T), (y1, T1)) in enumerate(zip(got_f, want_f)):
+        assert _same(y, y1), f"item {i}: y"
+        assert _same(T, T1), f"item {i}: T"
+    for i, (got, want) in enumerate(zip(got_b, want_b)):
+        for name, g, w in zip(("dX", "dA", "dB"), got, want):
+            assert _same(g, w), f"item {i}: {name}"
+    return n1 - n0, n2 - n1
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_group_of_three_equals_single_calls(lib, dtype):
+    """q, k, v-like items on one x with different ranks, scales and scale rules, weights given
+    stored and decoded: one T pass and one dA pass for the three."""
+    M, K = 300, 1280
+    specs = [(1152, K, 16, 16.0, binding.SCALE_LORA, 0, True),
+             (384, K, 8, 16.0, binding.SCALE_RSLORA, 0, False),
+             (640, K, 24, 32.0, binding.SCALE_LORA, 0, True)]
+    nf, nb = _check_group(M, specs, 7000, dtype)
+    # forward: one batched decode (the stored weight), one staging, the T pass and its
+    # finish, three GEMMs; backward: decode, staging, per item the G/dB pass, its finish and
+    # the dX GEMM, then the dA pass and its finish
+    assert nf == 1 + 1 + 2 + 3
+    assert nb == 1 + 1 + 3 * 3 + 2
+
+
+def test_groups_break_at_x_changes_rank_and_count_limits(lib):
+    """Items on x0, x0, x1, x0 (three groups), ranks 128 + 128 + 16 (the third item opens a
+    new group: at most 256 stacked rows) and nine items on one x (8 + 1)."""
+    M, K = 130, 1152
+    specs = [(1104, K, 16, 16.0, binding.SCALE_LORA, 0, True), (1200, K, 16, 16.0, binding.SCALE_LORA, 0, True),
+             (1048, K, 16, 16.0, binding.SCALE_LORA, 1, True), (1104, K, 16, 16.0, binding.SCALE_LORA, 0, True)]
+    _check_group(M, specs, 7100)
+    specs = [(1040, K, 128, 16.0, binding.SCALE_LORA, 0, True), (1088, K, 128, 16.0, binding.SCALE_LORA, 0, True),
+             (1104, K, 16, 16.0, binding.SCALE_LORA, 0, False)]
+    _check_group(M, specs, 7200)
+    specs = [(1040 + 8 * i, K, 8, 16.0, binding.SCALE_LORA, 0, i % 2 == 0) for i in range(9)]
+    _check_group(M, specs, 7300)
+
+
+def test_llama8b_qkv_group_equals_single_calls(lib):
+    """The Llama-3-8B-shaped q, k and v at 4096 tokens (r = 16) on one x, decoded weights,
+    as in the bench step."""
+    M, K = 4096, 4096
+    specs = [(4096, K, 16, 16.0, binding.SCALE_LORA, 0, True), (1024, K, 16, 16.0, binding.SCALE_LORA, 0, True),
+             (1024, K, 16, 16.0, binding.SCALE_LORA, 0, True)]
+    _check_group(M, specs, 7400, device_weights=True)
