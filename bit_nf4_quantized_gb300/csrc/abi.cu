@@ -407,9 +407,9 @@ size_t bwd_ws(int64_t M, int64_t N, int64_t K, int32_t r, nf4_dtype cd) {
 // after another on the stream:
 //   kRunStream: items given as NF4 at M <= 16 (16-bit), up to kStreamMaxGroup, one stream pass;
 //   kRunSmall:  small weights, up to kSmallMaxGroup in one fused launch (a pair backward);
-//   kRunGroup:  tiled items in a row that read the same x (pointer and K), up to kTcGroupMax
-//               whose padded ranks fit kTcGroupMaxRank: one shared skinny pass (a run of one
-//               item is the single call);
+//   kRunGroup:  up to kTcGroupMax tiled items in a row: their adapter passes share launches,
+//               and items that read the same x share a pass (a run of one item is the single
+//               call);
 //   kRunSingle: one single call (fp32 compute, or no tokens).
 enum { kRunStream, kRunSmall, kRunGroup, kRunSingle };
 struct BatchRun {
@@ -417,11 +417,10 @@ struct BatchRun {
   std::vector<int> idx;
 };
 
-template <typename KindOf, typename XOf, typename KOf, typename ROf>
-std::vector<BatchRun> plan_batch(int32_t count, KindOf kind_of, XOf x_of, KOf k_of, ROf r_of) {
+template <typename KindOf>
+std::vector<BatchRun> plan_batch(int32_t count, KindOf kind_of) {
   std::vector<BatchRun> runs;
   BatchRun stream{kRunStream, {}}, small{kRunSmall, {}}, group{kRunGroup, {}};
-  int group_nq = 0;
   auto flush = [&](BatchRun& b) {
     if (!b.idx.empty()) runs.push_back(b);
     b.idx.clear();
@@ -435,17 +434,8 @@ std::vector<BatchRun> plan_batch(int32_t count, KindOf kind_of, XOf x_of, KOf k_
       small.idx.push_back(i);
       if (static_cast<int>(small.idx.size()) == kSmallMaxGroup) flush(small);
     } else if (k == kRunGroup) {
-      const int nq = adapter_nq(r_of(i));
-      if (!group.idx.empty()) {
-        const int g0 = group.idx[0];
-        if (x_of(i) != x_of(g0) || k_of(i) != k_of(g0) || static_cast<int>(group.idx.size()) == kTcGroupMax ||
-            group_nq + nq > kTcGroupMaxRank) {
-          flush(group);
-          group_nq = 0;
-        }
-      }
       group.idx.push_back(i);
-      group_nq += nq;
+      if (static_cast<int>(group.idx.size()) == kTcGroupMax) flush(group);
     } else {
       runs.push_back(BatchRun{kRunSingle, {i}});
     }
@@ -464,8 +454,7 @@ std::vector<BatchRun> plan_fwd(int64_t M, int32_t count, const qlora_fwd_item* i
         if (it[i].w16 == nullptr && small_m(M, cd)) return static_cast<int>(kRunStream);
         if (small_w(M, it[i].N, it[i].K, it[i].rank, cd)) return static_cast<int>(kRunSmall);
         return static_cast<int>(kRunGroup);
-      },
-      [&](int i) { return it[i].x; }, [&](int i) { return it[i].K; }, [&](int i) { return it[i].rank; });
+      });
 }
 
 std::vector<BatchRun> plan_bwd(int64_t M, int32_t count, const qlora_bwd_item* it, nf4_dtype cd) {
@@ -475,22 +464,22 @@ std::vector<BatchRun> plan_bwd(int64_t M, int32_t count, const qlora_bwd_item* i
         if (!is16(cd) || M == 0) return static_cast<int>(kRunSingle);
         if (small_w(M, it[i].N, it[i].K, it[i].rank, cd)) return static_cast<int>(kRunSmall);
         return static_cast<int>(kRunGroup);
-      },
-      [&](int i) { return it[i].x; }, [&](int i) { return it[i].K; }, [&](int i) { return it[i].rank; });
+      });
 }
 
 // (the weight view only when `view`: workspace sizes are asked before any validation)
 TcFwdItem tc_fwd_item(int64_t M, const qlora_fwd_item& it, float s, bool view = true) {
   TcFwdItem t{};
   t.a = LinearArgs{M, it.N, it.K, it.rank, s, (it.w16 != nullptr || !view) ? Nf4View{} : view_of(it.W)};
-  t.A = it.A, t.B = it.B, t.y = it.y, t.T = it.T_out, t.w16 = it.w16;
+  t.x = it.x, t.A = it.A, t.B = it.B, t.y = it.y, t.T = it.T_out, t.w16 = it.w16;
   return t;
 }
 
 TcBwdItem tc_bwd_item(int64_t M, const qlora_bwd_item& it, float s, bool view = true) {
   TcBwdItem t{};
   t.a = LinearArgs{M, it.N, it.K, it.rank, s, (it.w16 != nullptr || !view) ? Nf4View{} : view_of(it.W)};
-  t.dy = it.dy, t.T = it.T, t.A = it.A, t.B = it.B, t.dx = it.dx, t.dA = it.dA, t.dB = it.dB, t.w16 = it.w16;
+  t.x = it.x, t.dy = it.dy, t.T = it.T, t.A = it.A, t.B = it.B, t.dx = it.dx, t.dA = it.dA, t.dB = it.dB;
+  t.w16 = it.w16;
   return t;
 }
 
@@ -738,7 +727,7 @@ size_t qlora_fwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_fwd
     } else if (r.kind == kRunGroup && n > 1) {
       TcFwdItem t[kTcGroupMax];
       for (int k = 0; k < n; ++k) t[k] = tc_fwd_item(M, items[r.idx[k]], 0.0f, false);
-      need = std::max(need, tc_fwd_group_ws_bytes(t, n));
+      need = std::max(need, tc_fwd_run_ws_bytes(t, n));
     } else if (r.kind != kRunSmall) {
       const qlora_fwd_item& it = items[r.idx[0]];
       need = std::max(need, it.w16 != nullptr ? qlora_fwd_w16_workspace_bytes(M, it.N, it.K, it.rank, compute)
@@ -804,7 +793,7 @@ nf4_status qlora_linear_fwd_batch(int64_t M, int32_t count, const qlora_fwd_item
     } else if (r.kind == kRunGroup && n > 1) {
       TcFwdItem t[kTcGroupMax];
       for (int k = 0; k < n; ++k) t[k] = tc_fwd_item(M, items[r.idx[k]], s[r.idx[k]]);
-      e = tc_forward_group(t, n, f16, items[i0].x, ws, status, cs);
+      e = tc_forward_run(t, n, f16, ws, status, cs);
     } else {
       const qlora_fwd_item& it = items[i0];
       const nf4_status st =
@@ -962,7 +951,7 @@ size_t qlora_bwd_batch_workspace_bytes(int64_t M, int32_t count, const qlora_bwd
     } else if (r.kind == kRunGroup && n > 1) {
       TcBwdItem t[kTcGroupMax];
       for (int k = 0; k < n; ++k) t[k] = tc_bwd_item(M, items[r.idx[k]], 0.0f, false);
-      need = std::max(need, tc_bwd_group_ws_bytes(t, n));
+      need = std::max(need, tc_bwd_run_ws_bytes(t, n));
     } else {
       const qlora_bwd_item& it = items[r.idx[0]];
       need = std::max(need, it.w16 != nullptr ? qlora_bwd_w16_workspace_bytes(M, it.N, it.K, it.rank, compute)
@@ -1019,7 +1008,7 @@ nf4_status qlora_linear_bwd_batch(int64_t M, int32_t count, const qlora_bwd_item
       }
       TcBwdItem t[kTcGroupMax];
       for (int k = 0; k < n; ++k) t[k] = tc_bwd_item(M, items[r.idx[k]], s[r.idx[k]]);
-      e = tc_backward_group(t, n, f16, items[i0].x, ws, status, cs);
+      e = tc_backward_run(t, n, f16, ws, status, cs);
     } else {
       const qlora_bwd_item& it = items[i0];
       const nf4_status st =

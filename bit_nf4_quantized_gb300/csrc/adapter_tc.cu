@@ -11,6 +11,9 @@
 // (K-major, N = r rounded up to 16); the fp32 accumulator lives in TMEM.  Slices
 // write partial sums that a second kernel adds in a fixed order (deterministic,
 // no atomics) and scales.
+#include <algorithm>
+#include <mutex>
+
 #include <cuda_fp16.h>
 
 #include "linear_tc.cuh"
@@ -46,17 +49,24 @@ struct SkinnyParams {
   int f16;          // operands are IEEE half (else bf16)
 };
 
-// One launch runs one or two independent passes: CTAs [0, p0.ctas) take the first,
-// the rest the second (p1.ctas == 0 when there is only one).
+// One launch runs up to kAdapterMaxPasses independent passes: CTAs [cta0[k], cta0[k + 1])
+// take pass k.
+struct AdapterLaunch {
+  CUtensorMap tx[kAdapterMaxPasses];
+  CUtensorMap tq[kAdapterMaxPasses];
+  SkinnyParams p[kAdapterMaxPasses];
+  int cta0[kAdapterMaxPasses + 1];
+  int n;
+};
+
 __global__ void __launch_bounds__(kAThreads, 1)
-adapter_tc(const __grid_constant__ CUtensorMap tm_x0, const __grid_constant__ CUtensorMap tm_q0,
-           const __grid_constant__ CUtensorMap tm_x1, const __grid_constant__ CUtensorMap tm_q1, const SkinnyParams p0,
-           const SkinnyParams p1) {
-  const bool second = static_cast<int>(blockIdx.x) >= p0.ctas;
-  const SkinnyParams p = second ? p1 : p0;
-  const CUtensorMap& tm_x = second ? tm_x1 : tm_x0;
-  const CUtensorMap& tm_q = second ? tm_q1 : tm_q0;
-  const int bid = second ? static_cast<int>(blockIdx.x) - p0.ctas : static_cast<int>(blockIdx.x);
+adapter_tc(const __grid_constant__ AdapterLaunch L) {
+  int k = 0;
+  while (k + 1 < L.n && static_cast<int>(blockIdx.x) >= L.cta0[k + 1]) ++k;
+  const SkinnyParams p = L.p[k];
+  const CUtensorMap& tm_x = L.tx[k];
+  const CUtensorMap& tm_q = L.tq[k];
+  const int bid = static_cast<int>(blockIdx.x) - L.cta0[k];
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -365,11 +375,20 @@ FinishJob finish_job(const AdapterPassArgs& a, const SkinnyParams& p, int o) {
 
 int adapter_nq(int r) { return nq_of(r); }
 
+int adapter_total_ctas() { return resident_ctas(); }
+
+void adapter_pair_targets(int64_t rows0, int64_t red0, int64_t rows1, int64_t red1, int* t0, int* t1) {
+  const int total = resident_ctas();
+  const double b0 = static_cast<double>(rows0) * red0, b1 = static_cast<double>(rows1) * red1;
+  *t0 = std::max(1, static_cast<int>(total * b0 / (b0 + b1)));
+  *t1 = std::max(1, total - *t0);
+}
+
 size_t adapter_partial_bytes(int64_t rows, int64_t red, int r) { return partial_bytes(rows, red, r); }
 
 cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream_t st) {
   KernelTimer timer(NF4_TIME_ADAPTER, st);
-  if (n < 1 || n > 2) return cudaErrorInvalidValue;
+  if (n < 1 || n > kAdapterMaxPasses) return cudaErrorInvalidValue;
   int outs = 0;
   for (int i = 0; i < n; ++i) {
     if (a[i].nouts < 0 || (a[i].nouts > 0 && a[i].outs == nullptr)) return cudaErrorInvalidValue;
@@ -379,33 +398,30 @@ cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream
         return cudaErrorInvalidValue;
   }
   if (outs > kAdapterMaxOuts) return cudaErrorInvalidValue;
-  // the resident CTAs are shared in proportion to the activation bytes each pass reads
+  // each pass's reduction split: its own target if given; otherwise one pass takes every
+  // resident CTA and two share them in proportion to the activation bytes each reads
   const int total = resident_ctas();
-  int target[2] = {total, 0};
-  if (n == 2) {
-    const double b0 = static_cast<double>(a[0].rows) * a[0].red, b1 = static_cast<double>(a[1].rows) * a[1].red;
-    target[0] = std::max(1, static_cast<int>(total * b0 / (b0 + b1)));
-    target[1] = std::max(1, total - target[0]);
+  int target[kAdapterMaxPasses];
+  for (int i = 0; i < n; ++i) target[i] = a[i].target > 0 ? std::min(a[i].target, total) : total;
+  if (n == 2 && a[0].target <= 0 && a[1].target <= 0)
+    adapter_pair_targets(a[0].rows, a[0].red, a[1].rows, a[1].red, &target[0], &target[1]);
+  AdapterLaunch L{};
+  L.n = n;
+  int ctas = 0, smem = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!setup_pass(a[i], target[i], status, &L.p[i], &L.tx[i], &L.tq[i])) return cudaErrorInvalidValue;
+    L.cta0[i] = ctas;
+    ctas += L.p[i].ctas;
+    smem = std::max(smem, 1024 + L.p[i].stages * static_cast<int>(L.p[i].stage_bytes) + 256);
   }
-  SkinnyParams p[2];
-  CUtensorMap tx[2], tq[2];
-  for (int i = 0; i < n; ++i)
-    if (!setup_pass(a[i], target[i], status, &p[i], &tx[i], &tq[i])) return cudaErrorInvalidValue;
-  if (n == 1) {
-    p[1] = SkinnyParams{};
-    tx[1] = tx[0];
-    tq[1] = tq[0];
-  }
-  int smem = 0;
-  for (int i = 0; i < n; ++i) smem = std::max(smem, 1024 + p[i].stages * static_cast<int>(p[i].stage_bytes) + 256);
+  L.cta0[n] = ctas;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
     attr = cudaFuncSetAttribute(adapter_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 1024 + 4 * 49152 + 256);
   });
   if (attr != cudaSuccess) return attr;
-  cudaError_t e = launch_pdl(adapter_tc, dim3(p[0].ctas + p[1].ctas), dim3(kAThreads), static_cast<size_t>(smem), st,
-                             1, tx[0], tq[0], tx[1], tq[1], p[0], p[1]);
+  cudaError_t e = launch_pdl(adapter_tc, dim3(ctas), dim3(kAThreads), static_cast<size_t>(smem), st, 1, L);
   note_launch();
   if (e != cudaSuccess) return e;
   FinishJobs jobs{};
@@ -413,7 +429,7 @@ cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream
   for (int i = 0; i < n; ++i) {
     for (int o = a[i].nouts > 0 ? 0 : -1; o < a[i].nouts; ++o) {
       FinishJob& f = jobs.job[jobs.n++];
-      f = finish_job(a[i], p[i], o);
+      f = finish_job(a[i], L.p[i], o);
       f.first_block = nblocks;
       nblocks += blocks(f.rows * (f.b_rows ? f.rp : f.r));
     }

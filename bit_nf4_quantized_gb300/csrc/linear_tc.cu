@@ -701,15 +701,16 @@ void bwd_prep_jobs(const LinearArgs& a, const float* T, const float* A, const fl
   jobs->push_back(zero_flags_job(w + L.flags));
 }
 
-// One launch for G = dY B (rows M, reduction over N along dY's rows; G, 16-bit s G, 16-bit
+// The pair of passes G = dY B (rows M, reduction over N along dY's rows; G, 16-bit s G, 16-bit
 // G^T into Gt with row stride ldt) and dB = s dY^T T (rows N, reduction over M down dY's
-// columns), then one for both finishes.
-cudaError_t gdb_pass(const LinearArgs& a, bool f16, const void* dy, float* G, float* dB, const BwdWs& L, char* w,
-                     void* Gt, int64_t ldt, int* status, cudaStream_t st) {
+// columns), both reading only dY.
+void gdb_args(const LinearArgs& a, bool f16, const void* dy, float* G, float* dB, const BwdWs& L, char* w, void* Gt,
+              int64_t ldt, AdapterPassArgs* pa) {
   const int rp = padded_rank(a.r);
   const int64_t Mp = pad8(a.M);
   auto* part = reinterpret_cast<float*>(w + L.part);
-  AdapterPassArgs pa[2] = {};
+  pa[0] = AdapterPassArgs{};
+  pa[1] = AdapterPassArgs{};
   AdapterPassArgs& g = pa[0];
   g.X = dy;
   g.x_inner = a.N;
@@ -741,6 +742,13 @@ cudaError_t gdb_pass(const LinearArgs& a, bool f16, const void* dy, float* G, fl
   d.scale = a.s;
   d.f32 = dB;
   g.f16 = d.f16 = f16 ? 1 : 0;
+}
+
+// One launch for the pair, then one for both finishes.
+cudaError_t gdb_pass(const LinearArgs& a, bool f16, const void* dy, float* G, float* dB, const BwdWs& L, char* w,
+                     void* Gt, int64_t ldt, int* status, cudaStream_t st) {
+  AdapterPassArgs pa[2];
+  gdb_args(a, f16, dy, G, dB, L, w, Gt, ldt, pa);
   return adapter_run(pa, 2, status, st);
 }
 
@@ -756,31 +764,59 @@ cudaError_t run_prep(const std::vector<PrepJob>& jobs, bool f16, cudaStream_t st
   return cudaSuccess;
 }
 
-// Group workspaces: each item's single-call layout, then the group's stacked rank side and
-// the shared pass's partial sums (and, backward, each item's fp32 G first).
-struct FwdGroupWs {
-  size_t item[kTcGroupMax] = {};
-  size_t Aq = 0, part = 0, total = 0;
-  int nqt = 0;
-  FwdGroupWs(const TcFwdItem* it, int n) {
+// The input sets of a run: maximal stretches of consecutive items that read the same x (the
+// same pointer and K) whose ranks, each rounded up to 16, add up to at most kTcGroupMaxRank.
+// Set g holds items [first[g], first[g + 1]); item i's rank side sits at rows col[i] of its
+// set's stacked Q (nqt[g] rows).
+struct XSets {
+  int n = 0;
+  int first[kTcGroupMax + 1] = {};
+  int nqt[kTcGroupMax] = {};
+  int col[kTcGroupMax] = {};
+  template <typename Item>
+  XSets(const Item* it, int m) {
+    for (int i = 0; i < m; ++i) {
+      const int nq = adapter_nq(it[i].a.r);
+      const bool join = n > 0 && it[i].x == it[first[n - 1]].x && it[i].a.K == it[first[n - 1]].a.K &&
+                        nqt[n - 1] + nq <= kTcGroupMaxRank;
+      if (!join) {
+        first[n] = i;
+        nqt[n] = 0;
+        ++n;
+      }
+      col[i] = nqt[n - 1];
+      nqt[n - 1] += nq;
+    }
+    first[n] = m;
+  }
+};
+
+// Run workspaces: each item's single-call layout (after its fp32 G, backward), then per input
+// set its stacked rank side (A forward, G^T backward) and its shared pass's partial sums.
+struct FwdRunWs {
+  size_t item[kTcGroupMax] = {}, Aq[kTcGroupMax] = {}, part[kTcGroupMax] = {};
+  size_t total = 0;
+  FwdRunWs(const TcFwdItem* it, int n, const XSets& xs) {
     size_t off = 0;
     for (int i = 0; i < n; ++i) {
       const LinearArgs& a = it[i].a;
       item[i] = off;
       off += a1024(FwdWs(a.M, a.N, a.K, a.r, it[i].w16 != nullptr).total);
-      nqt += adapter_nq(a.r);
     }
-    Aq = off;
-    part = Aq + a1024(2 * static_cast<size_t>(nqt) * it[0].a.K);
-    total = part + a1024(adapter_partial_bytes(it[0].a.M, it[0].a.K, nqt));
+    for (int g = 0; g < xs.n; ++g) {
+      const LinearArgs& a = it[xs.first[g]].a;
+      Aq[g] = off;
+      part[g] = Aq[g] + a1024(2 * static_cast<size_t>(xs.nqt[g]) * a.K);
+      off = part[g] + a1024(adapter_partial_bytes(a.M, a.K, xs.nqt[g]));
+    }
+    total = off;
   }
 };
 
-struct BwdGroupWs {
-  size_t G[kTcGroupMax] = {}, item[kTcGroupMax] = {};
-  size_t Gt = 0, part = 0, total = 0;
-  int nqt = 0;
-  BwdGroupWs(const TcBwdItem* it, int n) {
+struct BwdRunWs {
+  size_t G[kTcGroupMax] = {}, item[kTcGroupMax] = {}, Gt[kTcGroupMax] = {}, part[kTcGroupMax] = {};
+  size_t total = 0;
+  BwdRunWs(const TcBwdItem* it, int n, const XSets& xs) {
     size_t off = 0;
     for (int i = 0; i < n; ++i) {
       const LinearArgs& a = it[i].a;
@@ -788,23 +824,23 @@ struct BwdGroupWs {
       off += a1024(sizeof(float) * static_cast<size_t>(a.M) * a.r);
       item[i] = off;
       off += a1024(BwdWs(a.M, a.N, a.K, a.r, it[i].w16 != nullptr).total);
-      nqt += adapter_nq(a.r);
     }
-    Gt = off;
-    part = Gt + a1024(2 * static_cast<size_t>(nqt) * pad8(it[0].a.M));
-    total = part + a1024(adapter_partial_bytes(it[0].a.K, it[0].a.M, nqt));
+    for (int g = 0; g < xs.n; ++g) {
+      const LinearArgs& a = it[xs.first[g]].a;
+      Gt[g] = off;
+      part[g] = Gt[g] + a1024(2 * static_cast<size_t>(xs.nqt[g]) * pad8(a.M));
+      off = part[g] + a1024(adapter_partial_bytes(a.K, a.M, xs.nqt[g]));
+    }
+    total = off;
   }
 };
 
-// Every item reads x [M][K] with the same M and K; the padded ranks fit one skinny pass.
-bool group_ok(const LinearArgs* const* a, int n) {
+template <typename Item>
+bool run_ok(const Item* it, int n) {
   if (n < 1 || n > kTcGroupMax) return false;
-  int nqt = 0;
-  for (int i = 0; i < n; ++i) {
-    if (a[i]->M != a[0]->M || a[i]->K != a[0]->K) return false;
-    nqt += adapter_nq(a[i]->r);
-  }
-  return nqt <= kTcGroupMaxRank;
+  for (int i = 0; i < n; ++i)
+    if (it[i].a.M != it[0].a.M || adapter_nq(it[i].a.r) > kTcGroupMaxRank) return false;
+  return true;
 }
 
 }  // namespace
@@ -909,72 +945,68 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
   return adapter_run(&da, 1, status, st);
 }
 
-size_t tc_fwd_group_ws_bytes(const TcFwdItem* it, int n) {
-  if (n < 1 || n > kTcGroupMax) return 0;
-  return FwdGroupWs(it, n).total;
+size_t tc_fwd_run_ws_bytes(const TcFwdItem* it, int n) {
+  if (!run_ok(it, n)) return 0;
+  return FwdRunWs(it, n, XSets(it, n)).total;
 }
 
-size_t tc_bwd_group_ws_bytes(const TcBwdItem* it, int n) {
-  if (n < 1 || n > kTcGroupMax) return 0;
-  return BwdGroupWs(it, n).total;
+size_t tc_bwd_run_ws_bytes(const TcBwdItem* it, int n) {
+  if (!run_ok(it, n)) return 0;
+  return BwdRunWs(it, n, XSets(it, n)).total;
 }
 
-bool tc_groupable(const LinearArgs* const* a, int n) { return group_ok(a, n); }
-
-// Forward of a group reading one x: the NF4 weights decoded by one batched launch, the
-// staging of every item, one T pass over x for all of them (Q = the items' A, each padded
-// to 16 rows, stacked), then each item's GEMM.
-cudaError_t tc_forward_group(const TcFwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
-                             cudaStream_t st) {
-  const LinearArgs* args[kTcGroupMax];
-  for (int i = 0; i < n && i < kTcGroupMax; ++i) args[i] = &it[i].a;
-  if (!group_ok(args, n)) return cudaErrorInvalidValue;
-  const FwdGroupWs Gw(it, n);
+// Forward of a run: the stored weights decoded by one batched launch, the staging of every
+// item, one launch with a T pass per input set (Q = the set's A rows, each item's padded to
+// 16, stacked) and one finish, then each item's GEMM.
+cudaError_t tc_forward_run(const TcFwdItem* it, int n, bool f16, void* ws, int* status, cudaStream_t st) {
+  if (!run_ok(it, n)) return cudaErrorInvalidValue;
+  const XSets xs(it, n);
+  const FwdRunWs Rw(it, n, xs);
   char* w = static_cast<char*>(ws);
-  const int64_t M = it[0].a.M, K = it[0].a.K;
   std::vector<PrepJob> jobs;
   Nf4View views[kTcGroupMax];
   void* outs[kTcGroupMax];
   AdapterOut tout[kTcGroupMax];
-  int m = 0, col = 0;
-  for (int i = 0; i < n; ++i) {
-    const LinearArgs& a = it[i].a;
-    const FwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
-    char* wi = w + Gw.item[i];
-    const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
-    PrepJob j{};
-    j.kind = kStageRowsDirect;   // A as rows col .. col + nq of the stacked Q: [nqt][K]
-    j.r = a.r;
-    j.src = it[i].A;
-    j.dst = w + Gw.Aq + 2 * static_cast<size_t>(col) * K;
-    j.cols = K;
-    j.count = static_cast<int64_t>(nq) * K;
-    jobs.push_back(j);
-    PrepJob b{};
-    b.kind = kStageRows;         // B as the slab's feature side: [N][rp]
-    b.r = a.r;
-    b.width = rp;
-    b.scale = 1.0f;
-    b.src = it[i].B;
-    b.dst = wi + L.Bp;
-    b.count = a.N * rp;
-    jobs.push_back(b);
-    jobs.push_back(zero_flags_job(wi + L.flags));
-    if (it[i].w16 == nullptr) {
-      views[m] = a.W;
-      outs[m] = wi + L.wb;
-      ++m;
+  int m = 0;
+  for (int g = 0; g < xs.n; ++g) {
+    for (int i = xs.first[g]; i < xs.first[g + 1]; ++i) {
+      const LinearArgs& a = it[i].a;
+      const FwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
+      char* wi = w + Rw.item[i];
+      const int rp = padded_rank(a.r), nq = adapter_nq(a.r);
+      PrepJob j{};
+      j.kind = kStageRowsDirect;   // A as rows col .. col + nq of the set's stacked Q
+      j.r = a.r;
+      j.src = it[i].A;
+      j.dst = w + Rw.Aq[g] + 2 * static_cast<size_t>(xs.col[i]) * a.K;
+      j.cols = a.K;
+      j.count = static_cast<int64_t>(nq) * a.K;
+      jobs.push_back(j);
+      PrepJob b{};
+      b.kind = kStageRows;         // B as the slab's feature side: [N][rp]
+      b.r = a.r;
+      b.width = rp;
+      b.scale = 1.0f;
+      b.src = it[i].B;
+      b.dst = wi + L.Bp;
+      b.count = a.N * rp;
+      jobs.push_back(b);
+      jobs.push_back(zero_flags_job(wi + L.flags));
+      if (it[i].w16 == nullptr) {
+        views[m] = a.W;
+        outs[m] = wi + L.wb;
+        ++m;
+      }
+      AdapterOut& o = tout[i];
+      o = AdapterOut{};
+      o.col0 = xs.col[i];
+      o.r = a.r;
+      o.scale = 1.0f;
+      o.f32 = it[i].T;
+      o.b_rows = wi + L.sTp;
+      o.rp = rp;
+      o.scale_b = a.s;
     }
-    AdapterOut& o = tout[i];
-    o = AdapterOut{};
-    o.col0 = col;
-    o.r = a.r;
-    o.scale = 1.0f;
-    o.f32 = it[i].T;
-    o.b_rows = wi + L.sTp;
-    o.rp = rp;
-    o.scale_b = a.s;
-    col += nq;
   }
   cudaError_t e = cudaSuccess;
   if (m > 0) {
@@ -983,75 +1015,85 @@ cudaError_t tc_forward_group(const TcFwdItem* it, int n, bool f16, const void* x
   }
   if (e == cudaSuccess) e = run_prep(jobs, f16, st);
   if (e != cudaSuccess) return e;
-  AdapterPassArgs t{};
-  t.X = x;
-  t.x_inner = K;
-  t.x_outer = M;
-  t.Q = w + Gw.Aq;
-  t.q_cols = K;
-  t.r = Gw.nqt;
-  t.rows = M;
-  t.red = K;
-  t.partial = reinterpret_cast<float*>(w + Gw.part);
-  t.f16 = f16 ? 1 : 0;
-  t.outs = tout;
-  t.nouts = n;
-  if ((e = adapter_run(&t, 1, status, st)) != cudaSuccess) return e;
+  AdapterPassArgs t[kTcGroupMax] = {};
+  for (int g = 0; g < xs.n; ++g) {
+    const TcFwdItem& f = it[xs.first[g]];
+    t[g].X = f.x;
+    t[g].x_inner = f.a.K;
+    t[g].x_outer = f.a.M;
+    t[g].Q = w + Rw.Aq[g];
+    t[g].q_cols = f.a.K;
+    t[g].r = xs.nqt[g];
+    t[g].rows = f.a.M;
+    t[g].red = f.a.K;
+    t[g].partial = reinterpret_cast<float*>(w + Rw.part[g]);
+    t[g].f16 = f16 ? 1 : 0;
+    t[g].outs = tout + xs.first[g];
+    t[g].nouts = xs.first[g + 1] - xs.first[g];
+    t[g].target = adapter_total_ctas();   // as the single call's lone pass
+  }
+  if ((e = adapter_run(t, xs.n, status, st)) != cudaSuccess) return e;
   for (int i = 0; i < n; ++i) {
     const LinearArgs& a = it[i].a;
     const FwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
-    char* wi = w + Gw.item[i];
+    char* wi = w + Rw.item[i];
     const void* wb = it[i].w16 != nullptr ? it[i].w16 : wi + L.wb;
-    e = fwd_gemm(a, f16, x, wb, wi + L.Bp, wi + L.sTp, wi + L.part, wi + L.flags, it[i].y, status, st);
+    e = fwd_gemm(a, f16, it[i].x, wb, wi + L.Bp, wi + L.sTp, wi + L.part, wi + L.flags, it[i].y, status, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-// Backward of a group reading one x: decode and staging as above (one zeroed G^T for the
-// group, [nqt][Mp]), each item's G and dB pass (its 16-bit G^T into its rows of the group's
-// G^T) and dX GEMM, then one dA pass over x for all of them.
-cudaError_t tc_backward_group(const TcBwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
-                              cudaStream_t st) {
-  const LinearArgs* args[kTcGroupMax];
-  for (int i = 0; i < n && i < kTcGroupMax; ++i) args[i] = &it[i].a;
-  if (!group_ok(args, n)) return cudaErrorInvalidValue;
-  const BwdGroupWs Gw(it, n);
+// Backward of a run: decode and staging as above (a zeroed G^T [nqt][Mp] per input set), one
+// launch with every item's G and dB passes (each pair split as in the single call) and one
+// finish (each item's 16-bit G^T into its rows of its set's G^T), each item's dX GEMM, then
+// one launch with a dA pass per input set and one finish.
+cudaError_t tc_backward_run(const TcBwdItem* it, int n, bool f16, void* ws, int* status, cudaStream_t st) {
+  if (!run_ok(it, n)) return cudaErrorInvalidValue;
+  const XSets xs(it, n);
+  const BwdRunWs Rw(it, n, xs);
   char* w = static_cast<char*>(ws);
-  const int64_t M = it[0].a.M, K = it[0].a.K, Mp = pad8(M);
   std::vector<PrepJob> jobs;
-  {
-    PrepJob g{};                 // the group's G^T starts zero
-    g.kind = kStageTransposed;
-    g.r = 0;
-    g.width = Mp;
-    g.dst = w + Gw.Gt;
-    g.cols = M;
-    g.count = static_cast<int64_t>(Gw.nqt) * Mp;
-    jobs.push_back(g);
+  for (int g = 0; g < xs.n; ++g) {
+    const int64_t M = it[xs.first[g]].a.M, Mp = pad8(M);
+    PrepJob z{};                 // the set's G^T starts zero
+    z.kind = kStageTransposed;
+    z.r = 0;
+    z.width = Mp;
+    z.dst = w + Rw.Gt[g];
+    z.cols = M;
+    z.count = static_cast<int64_t>(xs.nqt[g]) * Mp;
+    jobs.push_back(z);
   }
   Nf4View views[kTcGroupMax];
   void* outs[kTcGroupMax];
   AdapterOut aout[kTcGroupMax];
-  int m = 0, col = 0;
-  for (int i = 0; i < n; ++i) {
-    const LinearArgs& a = it[i].a;
-    const BwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
-    char* wi = w + Gw.item[i];
-    bwd_prep_jobs(a, it[i].T, it[i].A, it[i].B, L, wi, false, &jobs);
-    if (it[i].w16 == nullptr) {
-      views[m] = a.W;
-      outs[m] = wi + L.wb;
-      ++m;
+  AdapterPassArgs gd[2 * kTcGroupMax] = {};
+  int m = 0;
+  for (int g = 0; g < xs.n; ++g) {
+    for (int i = xs.first[g]; i < xs.first[g + 1]; ++i) {
+      const LinearArgs& a = it[i].a;
+      const BwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
+      char* wi = w + Rw.item[i];
+      const int64_t Mp = pad8(a.M);
+      bwd_prep_jobs(a, it[i].T, it[i].A, it[i].B, L, wi, false, &jobs);
+      if (it[i].w16 == nullptr) {
+        views[m] = a.W;
+        outs[m] = wi + L.wb;
+        ++m;
+      }
+      gdb_args(a, f16, it[i].dy, reinterpret_cast<float*>(w + Rw.G[i]), it[i].dB, L, wi,
+               w + Rw.Gt[g] + 2 * static_cast<size_t>(xs.col[i]) * Mp, Mp, &gd[2 * i]);
+      adapter_pair_targets(gd[2 * i].rows, gd[2 * i].red, gd[2 * i + 1].rows, gd[2 * i + 1].red, &gd[2 * i].target,
+                           &gd[2 * i + 1].target);
+      AdapterOut& o = aout[i];
+      o = AdapterOut{};
+      o.col0 = xs.col[i];
+      o.r = a.r;
+      o.scale = a.s;
+      o.f32 = it[i].dA;
+      o.f32_t = 1;
     }
-    AdapterOut& o = aout[i];
-    o = AdapterOut{};
-    o.col0 = col;
-    o.r = a.r;
-    o.scale = a.s;
-    o.f32 = it[i].dA;
-    o.f32_t = 1;
-    col += adapter_nq(a.r);
   }
   cudaError_t e = cudaSuccess;
   if (m > 0) {
@@ -1059,34 +1101,37 @@ cudaError_t tc_backward_group(const TcBwdItem* it, int n, bool f16, const void* 
     e = launch_dequantize_batch(views, outs, m, f16 ? NF4_F16 : NF4_BF16, st);
   }
   if (e == cudaSuccess) e = run_prep(jobs, f16, st);
+  if (e == cudaSuccess) e = adapter_run(gd, 2 * n, status, st);
   if (e != cudaSuccess) return e;
   for (int i = 0; i < n; ++i) {
     const LinearArgs& a = it[i].a;
     const BwdWs L(a.M, a.N, a.K, a.r, it[i].w16 != nullptr);
-    char* wi = w + Gw.item[i];
+    char* wi = w + Rw.item[i];
     const void* wb = it[i].w16 != nullptr ? it[i].w16 : wi + L.wb;
-    void* Gt_i = w + Gw.Gt + 2 * static_cast<size_t>(aout[i].col0) * Mp;
-    auto* G = reinterpret_cast<float*>(w + Gw.G[i]);
-    if ((e = gdb_pass(a, f16, it[i].dy, G, it[i].dB, L, wi, Gt_i, Mp, status, st)) != cudaSuccess) return e;
     e = dx_gemm(a, f16, it[i].dy, wb, wi + L.ApT, wi + L.sGp, wi + L.part, wi + L.flags, it[i].dx, status, st);
     if (e != cudaSuccess) return e;
   }
-  // dA of every item: rows K, reduction over M down x's columns, Q = the group's G^T
-  AdapterPassArgs da{};
-  da.X = x;
-  da.x_inner = K;
-  da.x_outer = M;
-  da.mn_major = true;
-  da.Q = w + Gw.Gt;
-  da.q_cols = Mp;
-  da.r = Gw.nqt;
-  da.rows = K;
-  da.red = M;
-  da.partial = reinterpret_cast<float*>(w + Gw.part);
-  da.f16 = f16 ? 1 : 0;
-  da.outs = aout;
-  da.nouts = n;
-  return adapter_run(&da, 1, status, st);
+  // dA of every item: rows K, reduction over M down x's columns, Q = its set's G^T
+  AdapterPassArgs da[kTcGroupMax] = {};
+  for (int g = 0; g < xs.n; ++g) {
+    const TcBwdItem& f = it[xs.first[g]];
+    const int64_t Mp = pad8(f.a.M);
+    da[g].X = f.x;
+    da[g].x_inner = f.a.K;
+    da[g].x_outer = f.a.M;
+    da[g].mn_major = true;
+    da[g].Q = w + Rw.Gt[g];
+    da[g].q_cols = Mp;
+    da[g].r = xs.nqt[g];
+    da[g].rows = f.a.K;
+    da[g].red = f.a.M;
+    da[g].partial = reinterpret_cast<float*>(w + Rw.part[g]);
+    da[g].f16 = f16 ? 1 : 0;
+    da[g].outs = aout + xs.first[g];
+    da[g].nouts = xs.first[g + 1] - xs.first[g];
+    da[g].target = adapter_total_ctas();
+  }
+  return adapter_run(da, xs.n, status, st);
 }
 
 }  // namespace qnf4

@@ -19,18 +19,21 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
                         const float* A, const float* B, void* dx, float* dA, float* dB, float* G,
                         void* ws, int* status, cudaStream_t st, const void* w16 = nullptr);
 
-// Groups of projections that read the same input x [M][K] (the same M and K; e.g. a
-// layer's q, k and v, or gate and up): one skinny pass over x computes T for every item of
-// a forward group, and one computes dA for every item of a backward group, with Q stacking
-// the items' rank sides (each padded to 16 rows; at most kTcGroupMaxRank rows in all).
-// Everything else is what the single calls do, and every output is bit for bit the single
-// call's.  w16: the item's weight decoded to 16 bits, or nullptr (a.W is decoded, all such
-// items of the group in one batched launch).  The group's workspace holds each item's
-// single-call workspace (w16-aware) and the shared pass's buffers.
+// Runs of up to kTcGroupMax projections that share M (the tiled path of the batch calls).
+// Consecutive items that read the same input x [M][K] (the same pointer and K; e.g. a
+// layer's q, k and v, or gate and up) form an input set whose ranks, each rounded up to 16,
+// add up to at most kTcGroupMaxRank: one skinny pass over x computes T for every item of a
+// set (forward) and one computes dA (backward), with Q stacking the items' rank sides.  All
+// sets' passes go in one launch, and so do all items' G and dB passes; each pass is split as
+// the single call splits it, so every output is bit for bit the single call's.  w16: the
+// item's weight decoded to 16 bits, or nullptr (a.W is decoded, all such items of the run in
+// one batched launch).  The run's workspace holds each item's single-call workspace
+// (w16-aware) and each set's shared buffers.
 constexpr int kTcGroupMax = 8;
 constexpr int kTcGroupMaxRank = 256;
 struct TcFwdItem {
   LinearArgs a;
+  const void* x;
   const float* A;
   const float* B;
   void* y;
@@ -39,6 +42,7 @@ struct TcFwdItem {
 };
 struct TcBwdItem {
   LinearArgs a;
+  const void* x;
   const void* dy;
   const float* T;
   const float* A;
@@ -48,13 +52,10 @@ struct TcBwdItem {
   float* dB;
   const void* w16;
 };
-bool tc_groupable(const LinearArgs* const* a, int n);
-size_t tc_fwd_group_ws_bytes(const TcFwdItem* it, int n);
-size_t tc_bwd_group_ws_bytes(const TcBwdItem* it, int n);
-cudaError_t tc_forward_group(const TcFwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
-                             cudaStream_t st);
-cudaError_t tc_backward_group(const TcBwdItem* it, int n, bool f16, const void* x, void* ws, int* status,
-                              cudaStream_t st);
+size_t tc_fwd_run_ws_bytes(const TcFwdItem* it, int n);
+size_t tc_bwd_run_ws_bytes(const TcBwdItem* it, int n);
+cudaError_t tc_forward_run(const TcFwdItem* it, int n, bool f16, void* ws, int* status, cudaStream_t st);
+cudaError_t tc_backward_run(const TcBwdItem* it, int n, bool f16, void* ws, int* status, cudaStream_t st);
 
 // stream_fwd.cu: the forward for at most kStreamMaxM tokens, for up to kStreamMaxGroup
 // projections (sharing M) in two launches: T by lora_down_small, then one persistent pass that
@@ -121,7 +122,8 @@ struct AdapterOut {
   void* b_t;
   int64_t ldt;
 };
-constexpr int kAdapterMaxOuts = 8;
+constexpr int kAdapterMaxOuts = 16;
+constexpr int kAdapterMaxPasses = 16;
 struct AdapterPassArgs {
   const void* X;
   int64_t x_inner, x_outer;
@@ -140,13 +142,21 @@ struct AdapterPassArgs {
   void* b_t;
   int64_t ldt;
   int f16;
-  const AdapterOut* outs;   // nouts consumers (at most kAdapterMaxOuts); 0: the fields above
+  const AdapterOut* outs;   // nouts consumers (at most kAdapterMaxOuts in a launch); 0: the fields above
   int nouts;
+  int target;               // CTAs the reduction split is planned for; 0: see adapter_run
 };
 int adapter_nq(int r);
+// The CTAs a lone pass plans its split for, and the split of them between two passes in one
+// launch (the single calls' G and dB passes).
+int adapter_total_ctas();
+void adapter_pair_targets(int64_t rows0, int64_t red0, int64_t rows1, int64_t red1, int* t0, int* t1);
 size_t adapter_partial_bytes(int64_t rows, int64_t red, int r);
-// One or two independent passes (n = 1 or 2, separate `partial` buffers) in one launch,
-// then their finishes (at most kAdapterMaxOuts outputs in all) in one more.
+// Up to kAdapterMaxPasses independent passes (separate `partial` buffers) in one launch,
+// then their finishes (at most kAdapterMaxOuts outputs in all) in one more.  A pass's
+// reduction split (and so its sums' rounding order) depends only on its rows, reduction
+// length and target: without targets one pass plans for every resident CTA and two passes
+// share them in proportion to the bytes each reads.
 cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream_t st);
 
 }  // namespace qnf4

@@ -237,11 +237,12 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
  *     launches (T for every item, then one persistent pass over all their stored weights).
  *   - 16-bit compute, small weights (M > 16, K and N at most 1024, N*K at most 2^21, rank at
  *     most 32): up to 8 at a time in one launch.
- *   - 16-bit compute, the other items (the tiled tensor-core path): consecutive such items
- *     that read the same x (the same pointer and K) form groups of up to 8 whose ranks,
- *     each rounded up to 16, add up to at most 256 (a layer's q, k and v; gate and up).  A
- *     group decodes its NF4 weights in one launch and computes T for all its items in one
- *     pass over x, then runs each item's GEMM.  A group of one is the single call.
+ *   - 16-bit compute, the other items (the tiled tensor-core path): up to 8 consecutive
+ *     such items run together.  Their NF4 weights are decoded in one launch, and one launch
+ *     computes T for all of them: items in a row that read the same x (the same pointer and
+ *     K; a layer's q, k and v, or gate and up) share one pass over x as long as their ranks,
+ *     each rounded up to 16, add up to at most 256.  Then each item's GEMM runs.  A run of
+ *     one item is the single call.
  *   - anything else runs the single call.
  * Items must not write to memory another item reads.  ws: qlora_fwd_batch_workspace_bytes()
  * bytes.  Each item is validated as the single call validates it; the first failing item's
@@ -308,10 +309,10 @@ nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
  * (w16 == NULL) or qlora_linear_bwd_w16 (w16 != NULL: W decoded as nf4_dequantize writes it)
  * computes for its arguments, bit for bit; W may be NULL when w16 is given.  Items with small
  * weights (16-bit compute, M > 16, K and N at most 1024, N*K at most 2^21, rank at most 32)
- * run up to 8 at a time in one pair of launches.  Other 16-bit items form groups as in
- * qlora_linear_fwd_batch (consecutive, the same x and K, up to 8, padded ranks at most 256
- * in all): each item's G, dB and dX as in the single call, then dA for all the group's items
- * in one pass over x.  The others run one call each.  Items must not write to memory another
+ * run up to 8 at a time in one pair of launches.  Other 16-bit items run up to 8 at a time
+ * as in qlora_linear_fwd_batch: one launch for every item's G and dB passes, each item's dX
+ * GEMM, then one launch for every item's dA, where items in a row that read the same x share
+ * one pass over x.  The others run one call each.  Items must not write to memory another
  * item reads.  ws: qlora_bwd_batch_workspace_bytes() bytes.  Each item is validated as the
  * single call validates it; the first failing item's status is returned and nothing is
  * enqueued. */

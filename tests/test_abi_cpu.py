@@ -226,20 +226,20 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
 
 
 def test_group_workspace_covers_each_single_layout(lib):
-    """The batch workspace of a shared-x group of tiled items holds every item's single-call
-    workspace; items on distinct inputs need only the largest single workspace."""
+    """The batch workspace of a run of tiled items holds every item's single-call workspace,
+    whether the items share x or not, plus the shared passes' buffers."""
     M, r = 1000, 16
     shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
     single = [lib.qlora_fwd_w16_workspace_bytes(M, N, K, r, 1) for N, K in shapes]
     grouped = binding.qlora_fwd_batch_workspace_bytes(M, shapes, r, xs=[0, 0, 0], w16=True)
     apart = binding.qlora_fwd_batch_workspace_bytes(M, shapes, r, xs=[0, 1, 2], w16=True)
     assert grouped >= sum(single)
-    assert apart == max(single)
+    assert apart >= sum(single)
     single_b = [lib.qlora_bwd_w16_workspace_bytes(M, N, K, r, 1) for N, K in shapes]
     grouped_b = binding.qlora_bwd_batch_workspace_bytes(M, shapes, r, xs=[0, 0, 0], w16=True)
     apart_b = binding.qlora_bwd_batch_workspace_bytes(M, shapes, r, xs=[0, 1, 2], w16=True)
     assert grouped_b >= sum(single_b)
-    assert apart_b == max(single_b)
+    assert apart_b >= sum(single_b)
     # a group of one is the single call; nine items on one x run as 8 + 1
     assert binding.qlora_fwd_batch_workspace_bytes(M, shapes[:1], r, w16=True) == single[0]
     nine = binding.qlora_fwd_batch_workspace_bytes(M, [(1024, 4096)] * 9, r, xs=[0] * 9, w16=True)

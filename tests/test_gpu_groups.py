@@ -84,15 +84,16 @@ def test_group_of_three_equals_single_calls(lib, dtype):
              (640, K, 24, 32.0, binding.SCALE_LORA, 0, True)]
     nf, nb = _check_group(M, specs, 7000, dtype)
     # forward: one batched decode (the stored weight), one staging, the T pass and its
-    # finish, three GEMMs; backward: decode, staging, per item the G/dB pass, its finish and
-    # the dX GEMM, then the dA pass and its finish
+    # finish, three GEMMs; backward: decode, staging, every G and dB pass in one launch and
+    # their finishes in one more, three dX GEMMs, then the dA pass and its finish
     assert nf == 1 + 1 + 2 + 3
-    assert nb == 1 + 1 + 3 * 3 + 2
+    assert nb == 1 + 1 + 2 + 3 + 2
 
 
-def test_groups_break_at_x_changes_rank_and_count_limits(lib):
-    """Items on x0, x0, x1, x0 (three groups), ranks 128 + 128 + 16 (the third item opens a
-    new group: at most 256 stacked rows) and nine items on one x (8 + 1)."""
+def test_input_sets_break_at_x_changes_rank_and_count_limits(lib):
+    """One run of items on x0, x0, x1, x0 (three input sets), ranks 128 + 128 + 16 (the third
+    item opens a new set: at most 256 stacked rows) and nine items on one x (a run of 8, then
+    the single call)."""
     M, K = 130, 1152
     specs = [(1104, K, 16, 16.0, binding.SCALE_LORA, 0, True), (1200, K, 16, 16.0, binding.SCALE_LORA, 0, True),
              (1048, K, 16, 16.0, binding.SCALE_LORA, 1, True), (1104, K, 16, 16.0, binding.SCALE_LORA, 0, True)]
@@ -104,10 +105,18 @@ def test_groups_break_at_x_changes_rank_and_count_limits(lib):
     _check_group(M, specs, 7300)
 
 
-def test_llama8b_qkv_group_equals_single_calls(lib):
-    """The Llama-3-8B-shaped q, k and v at 4096 tokens (r = 16) on one x, decoded weights,
-    as in the bench step."""
-    M, K = 4096, 4096
-    specs = [(4096, K, 16, 16.0, binding.SCALE_LORA, 0, True), (1024, K, 16, 16.0, binding.SCALE_LORA, 0, True),
-             (1024, K, 16, 16.0, binding.SCALE_LORA, 0, True)]
-    _check_group(M, specs, 7400, device_weights=True)
+def test_llama8b_layer_run_equals_single_calls(lib):
+    """The Llama-3-8B-shaped layer at 4096 tokens (r = 16, decoded weights) as the bench step
+    runs it: q, k, v on one x, o on its own, gate and up on one x, down on its own."""
+    M = 4096
+    L = binding.SCALE_LORA
+    specs = [(4096, 4096, 16, 16.0, L, 0, True), (1024, 4096, 16, 16.0, L, 0, True),
+             (1024, 4096, 16, 16.0, L, 0, True), (4096, 4096, 16, 16.0, L, 1, True),
+             (14336, 4096, 16, 16.0, L, 2, True), (14336, 4096, 16, 16.0, L, 2, True),
+             (4096, 14336, 16, 16.0, L, 3, True)]
+    nf, nb = _check_group(M, specs, 7400, device_weights=True)
+    # forward: one staging launch for 21 jobs is two, one T launch for the four input sets and
+    # its finish, seven GEMMs; backward: two staging launches (32 jobs), one G/dB launch and its
+    # finish, seven dX GEMMs, one dA launch and its finish
+    assert nf == 2 + 2 + 7
+    assert nb == 2 + 2 + 7 + 2
