@@ -1053,9 +1053,9 @@ def traffic_json(csv_path):
     names = [n for n, _, _ in wl.W3["shapes"]]
     rec = {"kernel": "bf16_tc_gemm", "workload": "one step of the Llama-3-8B-shaped layer (7 projections, M = 4096, r = 16)",
            "launches": {"fwd_gemm": [], "dx_gemm": []}}
-    for i, d in enumerate(launches):   # per projection: the forward GEMM, then the dX GEMM
-        kind = "fwd_gemm" if i % 2 == 0 else "dx_gemm"
-        rec["launches"][kind].append({"projection": names[i // 2].split("_")[0],
+    for i, d in enumerate(launches):   # the step's 7 forward GEMMs, then its 7 dX GEMMs
+        kind = "fwd_gemm" if i < len(names) else "dx_gemm"
+        rec["launches"][kind].append({"projection": names[i % len(names)].split("_")[0],
                                       "dram_bytes": int(d.get("dram__bytes_read.sum", 0) + d.get("dram__bytes_write.sum", 0)),
                                       "duration_ns": int(d.get("gpu__time_duration.sum", 0))})
     rec["per_launch_bytes"] = {k: int(sum(x["dram_bytes"] for x in v) / max(1, len(v))) for k, v in rec["launches"].items()}

@@ -33,7 +33,7 @@ struct PrepJob {
   int first_block;        // set by PrepBuilder
 };
 
-constexpr int kMaxPrepJobs = 16;
+constexpr int kMaxPrepJobs = 32;
 constexpr int kPrepThreads = 256;   // threads of a prep CTA (the decode launch's CTA width)
 constexpr int kPrepPer = 8;         // outputs per thread: one 16-byte store
 

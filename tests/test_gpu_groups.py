@@ -115,8 +115,8 @@ def test_llama8b_layer_run_equals_single_calls(lib):
              (14336, 4096, 16, 16.0, L, 2, True), (14336, 4096, 16, 16.0, L, 2, True),
              (4096, 14336, 16, 16.0, L, 3, True)]
     nf, nb = _check_group(M, specs, 7400, device_weights=True)
-    # forward: one staging launch for 21 jobs is two, one T launch for the four input sets and
-    # its finish, seven GEMMs; backward: two staging launches (32 jobs), one G/dB launch and its
+    # forward: one staging launch (21 jobs), one T launch for the four input sets and its
+    # finish, seven GEMMs; backward: one staging launch (32 jobs), one G/dB launch and its
     # finish, seven dX GEMMs, one dA launch and its finish
-    assert nf == 2 + 2 + 7
-    assert nb == 2 + 2 + 7 + 2
+    assert nf == 1 + 2 + 7
+    assert nb == 1 + 2 + 7 + 2
