@@ -236,6 +236,8 @@ struct FinishJobs {
   int n;
 };
 
+// One thread per 4 consecutive columns of a row: the sums of its columns below r (the slices
+// in order), and for b_rows the 4 16-bit values (zeros past r) as one 8-byte store.
 __global__ void finish_partials(const FinishJobs jobs) {
   pdl_allow_next();
   pdl_wait();
@@ -243,31 +245,52 @@ __global__ void finish_partials(const FinishJobs jobs) {
   while (k + 1 < jobs.n && blockIdx.x >= jobs.job[k + 1].first_block) ++k;
   const FinishJob& f = jobs.job[k];
   const int64_t i = static_cast<int64_t>(blockIdx.x - f.first_block) * blockDim.x + threadIdx.x;
-  const int width = f.b_rows ? f.rp : f.r;
-  const int64_t w = f.rows * width;
-  if (i >= w) return;
-  const int64_t row = i / width;
-  const int j = static_cast<int>(i % width);
-  float v = 0.0f;
-  if (j < f.r) {
-    // the slices in order, 8 loads in flight before their adds
-    const float* src = f.partial + row * f.pstride + f.col0 + j;
+  const int chunks = ((f.b_rows ? f.rp : f.r) + 3) / 4;
+  if (i >= f.rows * chunks) return;
+  const int64_t row = i / chunks;
+  const int j0 = static_cast<int>(i - row * chunks) * 4;
+  const int nj = min(4, f.r - j0);   // columns of this chunk below r (none in the padding)
+  float v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) v[u] = 0.0f;
+  if (nj > 0) {
+    const float* src = f.partial + row * f.pstride + f.col0 + j0;
     const int64_t stride = f.rows * f.pstride;
-    for (int sp0 = 0; sp0 < f.nsplit; sp0 += 8) {
-      float t[8];
+#pragma unroll 4
+    for (int sp = 0; sp < f.nsplit; ++sp) {
+      float t[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) t[u] = sp0 + u < f.nsplit ? src[(sp0 + u) * stride] : 0.0f;
+      for (int u = 0; u < 4; ++u) t[u] = u < nj ? src[sp * stride + u] : 0.0f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (sp0 + u < f.nsplit) v += t[u];
+      for (int u = 0; u < 4; ++u) v[u] += t[u];
     }
-    if (f.f32) {
-      if (f.f32_t) f.f32[static_cast<int64_t>(j) * f.rows + row] = f.scale * v;
-      else f.f32[row * f.r + j] = f.scale * v;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (u >= nj) break;
+      const int j = j0 + u;
+      if (f.f32) {
+        if (f.f32_t) f.f32[static_cast<int64_t>(j) * f.rows + row] = f.scale * v[u];
+        else f.f32[row * f.r + j] = f.scale * v[u];
+      }
+      if (f.b_t) put16(f.b_t, static_cast<int64_t>(j) * f.ldt + row, v[u], f.f16);
     }
-    if (f.b_t) put16(f.b_t, static_cast<int64_t>(j) * f.ldt + row, v, f.f16);
   }
-  if (f.b_rows) put16(f.b_rows, row * f.rp + j, j < f.r ? f.scale_b * v : 0.0f, f.f16);
+  if (f.b_rows) {   // rp is a multiple of 64: the 4 values are one aligned 8-byte store
+    uint32_t w[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float lo = 2 * q < nj ? f.scale_b * v[2 * q] : 0.0f;
+      const float hi = 2 * q + 1 < nj ? f.scale_b * v[2 * q + 1] : 0.0f;
+      if (f.f16) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        w[q] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        w[q] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+    }
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(f.b_rows) + row * f.rp + j0) = make_uint2(w[0], w[1]);
+  }
 }
 
 int nq_of(int r) { return (r + 15) / 16 * 16; }
@@ -431,7 +454,7 @@ cudaError_t adapter_run(const AdapterPassArgs* a, int n, int* status, cudaStream
       FinishJob& f = jobs.job[jobs.n++];
       f = finish_job(a[i], L.p[i], o);
       f.first_block = nblocks;
-      nblocks += blocks(f.rows * (f.b_rows ? f.rp : f.r));
+      nblocks += blocks(f.rows * (((f.b_rows ? f.rp : f.r) + 3) / 4));
     }
   }
   e = launch_pdl(finish_partials, dim3(nblocks), dim3(256), 0, st, 1, jobs);
