@@ -120,3 +120,37 @@ def test_llama8b_layer_run_equals_single_calls(lib):
     # finish, seven dX GEMMs, one dA launch and its finish
     assert nf == 1 + 2 + 7
     assert nb == 1 + 2 + 7 + 2
+
+
+def test_small_m_batch_mixes_streamed_and_decoded_items(lib):
+    """At M <= 16 the items given as NF4 go through the streaming pass (grouped) and the items
+    given decoded through the tiled run (as qlora_linear_fwd_w16 does).  Decoded items equal
+    their single calls bit for bit; streamed items differ from theirs only in the order of the
+    fp32 partial sums (the group's split), so they agree within one bf16 rounding, plus the
+    fp32 sums' own order error near zero."""
+    M, K = 5, 1024
+    x = torch.from_numpy(wl.normal((M, K), 1.0, 1, 7600)).to(DEV).bfloat16()
+    specs = [(1152, 16, True), (384, 8, False), (640, 24, True), (1024, 16, False)]
+    items, want, decoded = [], [], []
+    for i, (N, r, dec) in enumerate(specs):
+        q = _weight(N, K, 7610 + 10 * i)
+        A, B = (torch.from_numpy(t).to(DEV) for t in wl.adapters(N, K, r, 1, 7611 + 10 * i))
+        if dec:
+            w16 = binding.nf4_dequantize(q, torch.bfloat16)
+            want.append(binding.qlora_linear_fwd_w16(x, w16, A, B, 16.0))
+            items.append(dict(x=x, w16=w16, A=A, B=B, alpha=16.0))
+        else:
+            want.append(binding.qlora_linear_fwd(x, q, A, B, 16.0))
+            items.append(dict(x=x, W=q, A=A, B=B, alpha=16.0))
+        decoded.append(dec)
+    got = binding.qlora_linear_fwd_batch(items)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.NF4_OK
+    for i, ((y, T), (y1, T1), dec) in enumerate(zip(got, want, decoded)):
+        if dec:
+            assert _same(y, y1), f"item {i}: y"
+            assert _same(T, T1), f"item {i}: T"
+        else:
+            yf, y1f = y.float(), y1.float()
+            assert torch.all((yf - y1f).abs() <= 2.0 ** -7 * y1f.abs() + 4e-6), f"item {i}: y"
+            assert torch.allclose(T, T1, rtol=1e-5, atol=1e-6), f"item {i}: T"
