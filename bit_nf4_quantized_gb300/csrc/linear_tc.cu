@@ -835,6 +835,16 @@ struct BwdRunWs {
   }
 };
 
+// The resident CTAs shared between a launch's passes in proportion to the activation bytes
+// each reads (the passes then hold about one wave of CTAs together).
+void share_targets(AdapterPassArgs* a, int n) {
+  const int total = adapter_total_ctas();
+  double bytes = 0.0;
+  for (int i = 0; i < n; ++i) bytes += static_cast<double>(a[i].rows) * a[i].red;
+  for (int i = 0; i < n; ++i)
+    a[i].target = std::max(1, static_cast<int>(total * (static_cast<double>(a[i].rows) * a[i].red) / bytes));
+}
+
 template <typename Item>
 bool run_ok(const Item* it, int n) {
   if (n < 1 || n > kTcGroupMax) return false;
@@ -1030,8 +1040,8 @@ cudaError_t tc_forward_run(const TcFwdItem* it, int n, bool f16, void* ws, int* 
     t[g].f16 = f16 ? 1 : 0;
     t[g].outs = tout + xs.first[g];
     t[g].nouts = xs.first[g + 1] - xs.first[g];
-    t[g].target = adapter_total_ctas();   // as the single call's lone pass
   }
+  share_targets(t, xs.n);
   if ((e = adapter_run(t, xs.n, status, st)) != cudaSuccess) return e;
   for (int i = 0; i < n; ++i) {
     const LinearArgs& a = it[i].a;
@@ -1129,8 +1139,8 @@ cudaError_t tc_backward_run(const TcBwdItem* it, int n, bool f16, void* ws, int*
     da[g].f16 = f16 ? 1 : 0;
     da[g].outs = aout + xs.first[g];
     da[g].nouts = xs.first[g + 1] - xs.first[g];
-    da[g].target = adapter_total_ctas();
   }
+  share_targets(da, xs.n);
   return adapter_run(da, xs.n, status, st);
 }
 

@@ -24,8 +24,11 @@ cudaError_t tc_backward(const LinearArgs& a, bool f16, const void* dy, const voi
 // layer's q, k and v, or gate and up) form an input set whose ranks, each rounded up to 16,
 // add up to at most kTcGroupMaxRank: one skinny pass over x computes T for every item of a
 // set (forward) and one computes dA (backward), with Q stacking the items' rank sides.  All
-// sets' passes go in one launch, and so do all items' G and dB passes; each pass is split as
-// the single call splits it, so every output is bit for bit the single call's.  w16: the
+// sets' passes go in one launch, and so do all items' G and dB passes.  Each G/dB pair is
+// split as the single call splits it (dX and dB are the single call's bits); the T or dA
+// passes of a launch share the resident CTAs in proportion to the bytes each reads, so with
+// one input set they are the single call's bits and with several their fp32 partial sums
+// are added in another order (deterministic for a given run).  w16: the
 // item's weight decoded to 16 bits, or nullptr (a.W is decoded, all such items of the run in
 // one batched launch).  The run's workspace holds each item's single-call workspace
 // (w16-aware) and each set's shared buffers.

@@ -230,9 +230,12 @@ nf4_status qlora_linear_fwd(int64_t M, int64_t N, int64_t K, int32_t rank, float
 
 /* Forward of several projections that share M and the compute dtype, for example the seven
  * projections of one transformer layer ([GATE] "Shape-matched ceilings": q, k, v, o, gate, up,
- * down).  Item i computes exactly what qlora_linear_fwd (w16 == NULL) or qlora_linear_fwd_w16
+ * down).  Item i computes what qlora_linear_fwd (w16 == NULL) or qlora_linear_fwd_w16
  * (w16 != NULL: W decoded as nf4_dequantize writes it; W may then be NULL) computes for its
- * arguments, bit for bit.
+ * arguments: the same operands and products, with some fp32 partial sums added in another
+ * order where the item shares a pass's work split with other items (the M <= 16 pass; the T
+ * passes of a run that reads more than one x), so y and T_out may differ from the single
+ * call's in their last bits.  The results are deterministic for a given batch.
  *   - compute = NF4_BF16 or NF4_F16, M <= 16, items given as NF4: up to 8 run as one pair of
  *     launches (T for every item, then one persistent pass over all their stored weights).
  *   - 16-bit compute, small weights (M > 16, K and N at most 1024, N*K at most 2^21, rank at
@@ -305,9 +308,11 @@ nf4_status qlora_linear_bwd_w16(int64_t M, int64_t N, int64_t K, int32_t rank, f
                                 void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of several projections that share M and the compute dtype, e.g. the projections of
- * one layer that read the same x (q, k and v): item i computes exactly what qlora_linear_bwd
+ * one layer that read the same x (q, k and v): item i computes what qlora_linear_bwd
  * (w16 == NULL) or qlora_linear_bwd_w16 (w16 != NULL: W decoded as nf4_dequantize writes it)
- * computes for its arguments, bit for bit; W may be NULL when w16 is given.  Items with small
+ * computes for its arguments; W may be NULL when w16 is given.  dX and dB are the single
+ * call's bits; dA's fp32 partial sums are added in another order when the run reads more
+ * than one x (deterministic for a given batch).  Items with small
  * weights (16-bit compute, M > 16, K and N at most 1024, N*K at most 2^21, rank at most 32)
  * run up to 8 at a time in one pair of launches.  Other 16-bit items run up to 8 at a time
  * as in qlora_linear_fwd_batch: one launch for every item's G and dB passes, each item's dX

@@ -1,8 +1,11 @@
 """Grouped calls on the tiled tensor-core path: consecutive items of qlora_linear_fwd_batch /
 qlora_linear_bwd_batch that read the same x share one skinny pass over x (T in the forward,
-dA in the backward).  Every output must equal the single call's bit for bit; the single
-calls are themselves checked against the oracle in tests/test_gpu_linear.py, so equality
-carries that parity over to the groups.  The launch counts show that the grouping happened.
+dA in the backward), and a run's passes share launches.  With one input set every output
+equals the single call's bit for bit; with several, dX and dB still do and y, T and dA agree
+within the reordering of fp32 partial sums (each set's pass gets its share of the CTAs).  The
+single calls are themselves checked against the oracle in tests/test_gpu_linear.py, so the
+comparison carries that parity over to the runs.  The launch counts show that the grouping
+happened.
 """
 
 import pytest
@@ -33,13 +36,37 @@ def _same(a, b):
     return torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+def _close(a, b, rtol):
+    """fp32 tensors equal up to the order of their sums: within rtol of each element, or a
+    tenth of that of the largest magnitude (a sum of K terms reordered moves by about K
+    roundings of its partial sums, which near a zero result is large relative to it)."""
+    return torch.allclose(a, b, rtol=rtol, atol=rtol * float(b.abs().max()) * 0.1)
+
+
+def _single_set_runs(specs):
+    """Per item: whether its run (up to 8 items in a row) holds one input set (items in a row
+    on the same x whose ranks, each rounded up to 16, add up to at most 256)."""
+    out = []
+    for r0 in range(0, len(specs), 8):
+        run = specs[r0:r0 + 8]
+        sets, used, prev = 0, 0, None
+        for N, K, r, alpha, mode, xid, decoded in run:
+            nq = (r + 15) // 16 * 16
+            if prev is None or xid != prev or used + nq > 256:
+                sets, used = sets + 1, 0
+            used += nq
+            prev = xid
+        out += [sets == 1] * len(run)
+    return out
+
+
 def _check_group(M, specs, seed, dtype=torch.bfloat16, device_weights=False):
     """specs: per item (N, K, r, alpha, mode, x_id, decoded).  Runs one forward batch and one
     backward batch over all items, and each item's single NF4-input calls; compares all.
     device_weights: the stored weights come from nf4_quantize on the device (large shapes;
     both sides read the same stored weight either way)."""
     xs = {}
-    items_f, items_b, want_f, want_b = [], [], [], []
+    items_f, items_b, want_f, want_b, scales = [], [], [], [], []
     for i, (N, K, r, alpha, mode, xid, decoded) in enumerate(specs):
         if xid not in xs:
             xs[xid] = torch.from_numpy(wl.normal((M, K), 1.0, 1, seed + 500 + xid)).to(DEV).to(dtype)
@@ -50,6 +77,7 @@ def _check_group(M, specs, seed, dtype=torch.bfloat16, device_weights=False):
         else:
             q = _weight(N, K, seed + 10 * i)
         A, B = (torch.from_numpy(t).to(DEV) for t in wl.adapters(N, K, r, 1, seed + 10 * i + 1))
+        scales.append((B, alpha / r if mode == binding.SCALE_LORA else alpha / r ** 0.5))
         dy = torch.from_numpy(wl.normal((M, N), 1.0, 1, seed + 10 * i + 3)).to(DEV).to(dtype)
         y1, T1 = binding.qlora_linear_fwd(x, q, A, B, alpha, mode)
         want_f.append((y1, T1))
@@ -65,12 +93,25 @@ def _check_group(M, specs, seed, dtype=torch.bfloat16, device_weights=False):
     n2 = binding.launch_count()
     torch.cuda.synchronize()
     assert binding.device_status() == binding.NF4_OK
+    one_set = _single_set_runs(specs)
     for i, ((y, T), (y1, T1)) in enumerate(zip(got_f, want_f)):
-        assert _same(y, y1), f"item {i}: y"
-        assert _same(T, T1), f"item {i}: T"
+        if one_set[i]:
+            assert _same(y, y1), f"item {i}: y"
+            assert _same(T, T1), f"item {i}: T"
+        else:   # T's slices added in another order; y through a 16-bit s T
+            assert _close(T, T1, 1e-4), f"item {i}: T"
+            # each entry of the 16-bit s T may round one unit (2^-7 relative) the other way,
+            # and y itself one unit
+            B, sc = scales[i]
+            bound = 2.0 ** -7 * (sc * (T1.abs() @ B.abs().T) + y1.float().abs()) + 1e-6
+            assert torch.all((y.float() - y1.float()).abs() <= bound), f"item {i}: y"
     for i, (got, want) in enumerate(zip(got_b, want_b)):
-        for name, g, w in zip(("dX", "dA", "dB"), got, want):
-            assert _same(g, w), f"item {i}: {name}"
+        assert _same(got[0], want[0]), f"item {i}: dX"
+        assert _same(got[2], want[2]), f"item {i}: dB"
+        if one_set[i]:
+            assert _same(got[1], want[1]), f"item {i}: dA"
+        else:
+            assert _close(got[1], want[1], 1e-4), f"item {i}: dA"
     return n1 - n0, n2 - n1
 
 
